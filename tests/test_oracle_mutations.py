@@ -1,0 +1,60 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a temporary copy of the oracle's C++ source
+(on the CPU), builds it, and runs the pin suite against that copy: the suite
+has to fail.  The committed oracle is never modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "nvfp4_oracle.cpp")
+
+MUTATIONS = {
+    "e2m1 ties round up": ("else pick = (k % 2 == 0) ? k : k + 1;", "else pick = k + 1;"),
+    "e2m1 negative zero loses its sign": (
+        "const uint8_t sign = std::signbit(v) ? 0x8 : 0x0;\n    const double a = std::fabs(static_cast<double>(v));\n    if (a >= 6.0) return static_cast<uint8_t>(sign | 7);\n    for (int k = 0; k < 7; ++k) {\n        if (a >= kGrid[k] && a < kGrid[k + 1]) {\n            const double twice",
+        "const uint8_t sign = (v < 0.0f) ? 0x8 : 0x0;\n    const double a = std::fabs(static_cast<double>(v));\n    if (a >= 6.0) return static_cast<uint8_t>(sign | 7);\n    for (int k = 0; k < 7; ++k) {\n        if (a >= kGrid[k] && a < kGrid[k + 1]) {\n            const double twice"),
+    "e4m3 ties round up": ("else pick = (c % 2 == 0) ? c : c + 1;", "else pick = c + 1;"),
+    "scale uses a reciprocal multiply": ("return (b / 6.0f) * S_enc;", "return b * (1.0f / 6.0f) * S_enc;"),
+    "map-to-4 expansion not 1.5": ("min_nd(s6f * 1.5f, 448.0f)", "min_nd(s6f * 1.25f, 448.0f)"),
+    "ties pick map-to-4": ("(E[1] < E[0]) ? 1 : 0", "(E[1] <= E[0]) ? 1 : 0"),
+    "error sum in reverse order": ("for (int t = 0; t < 16; ++t) E = E + e[t];",
+                                   "for (int t = 15; t >= 0; --t) E = E + e[t];"),
+    "16x16 rows summed sequentially": (
+        "return (((R[0] + R[8]) + (R[4] + R[12])) + ((R[2] + R[10]) + (R[6] + R[14]))) +",
+        "float S = 0.0f; for (int r = 0; r < 16; ++r) S = S + R[r]; return S; return (((R[0] + R[8]) + (R[4] + R[12])) + ((R[2] + R[10]) + (R[6] + R[14]))) +"),
+    "block amax propagates NaN": ("float max_nd(float a, float b) { return std::fmax(a, b); }",
+                                  "float max_nd(float a, float b) { return (a > b || a != a) ? a : b; }"),
+    "SR rounds up on u == p": ("(u < p ? k + 1 : k)", "(u <= p ? k + 1 : k)"),
+    "Philox multipliers swapped": ("const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;",
+                                   "const uint32_t M0 = 0xCD9E8D57u, M1 = 0xD2511F53u;"),
+    "SR counter uses idx, not idx/4": ("const uint64_t blk = idx >> 2;", "const uint64_t blk = idx;"),
+    "residual ignores the previous residual": ("residual[i] = y[i] - dq[i];",
+                                               "residual[i] = widen(x, dtype, i) - dq[i];"),
+    "nibbles swapped": ("if (c % 2 == 0) byte = static_cast<uint8_t>((byte & 0xF0) | code);",
+                        "if (c % 2 == 1) byte = static_cast<uint8_t>((byte & 0xF0) | code); else if (0) byte = 0;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor not found: {name}"
+    mutated = src.replace(old, new, 1)
+    cpp = tmp_path / "nvfp4_oracle.cpp"
+    cpp.write_text(mutated)
+    hdr = os.path.join(ROOT, "oracle", "nvfp4_oracle.h")
+    (tmp_path / "nvfp4_oracle.h").write_text(open(hdr).read())
+    so = tmp_path / "liboracle_mut.so"
+    subprocess.run(["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-w",
+                    "-shared", "-fPIC", str(cpp), "-o", str(so)], check=True)
+    env = dict(os.environ, NVFP4_ORACLE_LIB=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins did not catch: {name}\n{r.stdout[-2000:]}"
