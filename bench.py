@@ -1,0 +1,424 @@
+"""Throughput of the NVFP4 quantization hot path on GB300.
+
+One step = one pass of the whole path over the LLM-shaped bf16 sweep
+(W1 [4096,14336], W2 [14336,4096] ~ 0.02*N(0,1); A [16384,4096] ~ Student-t(4)
+with 0.1% outlier channels x100; seed 4):
+  1. W1  SR + error feedback, 1x16            (fp32 residual read + written)
+  2. W2  SR + error feedback, 16x16
+  3. A   four-over-six MAE, bound 256, 1x16 rowwise, per-tensor amax computed
+  4. W1  four-over-six MAE, bound 256, 16x16 rowwise + columnwise, amax computed
+  5. W2  four-over-six MAE, bound 256, 16x16 rowwise + columnwise, amax computed
+  6. A   round-to-nearest, 1x16
+  7. W2  stochastic rounding, 1x16
+  8. A   dequantize (codes of 3) to bf16
+Metric: algorithmic GB/s (bytes read + written once each, amax passes counted
+with their real extra read) and Gelem/s, as a fraction of measured HBM peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+N > 1 runs under torchrun: every rank processes its own copy of the sweep
+(independent problems, no collective on the data path; weak scaling).
+--impl reference times the CPU oracle on a bounded sample of the same step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+GB = 1e9
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+WORKLOAD = ("c5 LLM-shaped sweep, bf16: W1[4096,14336], W2[14336,4096] ~ 0.02*N(0,1), "
+            "A[16384,4096] ~ Student-t(4) with 4 outlier channels x100 (seed 4); SR+EF 1x16 "
+            "and 16x16 (seed 0, step t), four-over-six MAE bound 256 (1x16 rowwise on A, 16x16 "
+            "row+col on W1/W2, per-tensor amax computed), RTN, SR, dequantize")
+
+
+def step_plan(M1, K1, M2, K2, Ma, Ka):
+    """(name, elements, algorithmic bytes) per call of one step."""
+    e1, e2, ea = M1 * K1, M2 * K2, Ma * Ka
+    q = 0.5 + 1 / 16                       # codes + scales per element
+    return [
+        ("W1 SR+EF 1x16", e1, e1 * (2 + 4 + 4 + q)),
+        ("W2 SR+EF 16x16", e2, e2 * (2 + 4 + 4 + q)),
+        ("A 4o6 1x16 (amax computed)", ea, ea * (2 + 2 + q)),
+        ("W1 4o6 16x16 row+col (amax computed)", e1, e1 * (2 + 2 + 2 * q)),
+        ("W2 4o6 16x16 row+col (amax computed)", e2, e2 * (2 + 2 + 2 * q)),
+        ("A RTN 1x16", ea, ea * (2 + q)),
+        ("W2 SR 1x16", e2, e2 * (2 + q)),
+        ("A dequantize", ea, ea * (q + 2)),
+    ]
+
+
+# ---------------------------------------------------------------------------------------
+def clocks_sampler_start(path):
+    try:
+        f = open(path, "w")
+        return subprocess.Popen(
+            ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "200"],
+            stdout=f, stderr=subprocess.DEVNULL), f
+    except (OSError, FileNotFoundError):
+        return None, None
+
+
+def clocks_sampler_stop(proc, f, path, gpu_index):
+    if proc is None:
+        return None
+    proc.terminate()
+    try:
+        proc.wait(timeout=5)
+    except subprocess.TimeoutExpired:
+        proc.kill()
+    f.close()
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    rows = [[s.strip() for s in line.split(",")] for line in open(path)]
+    rows = [r for r in rows if len(r) >= 9]
+    if any(r[0] == str(gpu_index) for r in rows) and len({r[0] for r in rows}) > 1:
+        rows = [r for r in rows if r[0] == str(gpu_index)]
+    for parts in rows:
+        try:
+            sm.append(float(parts[1]))
+            smax.append(float(parts[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return None
+
+
+def ncu_traffic(kernel_name):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, when it was taken on the current kernel source."""
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+    except (OSError, ValueError):
+        return None
+    from nvfp4_block_quantization_quantize_gb300.build import source_digest
+    ent = rec.get(kernel_name)
+    if not ent or ent.get("source_digest") != source_digest():
+        return None
+    return ent.get("dram_bytes_per_launch_full_size")
+
+
+# ---------------------------------------------------------------------------------------
+_C5 = None
+
+
+def c5_inputs():
+    global _C5
+    if _C5 is None:
+        import nvfp4_workloads as W
+        _C5 = W.C5()
+    return _C5
+
+
+def cpu_baseline(sample_rows=1024, repeats=1):
+    """The oracle as it stands, single-threaded, on a bounded sample of the step:
+    the first `sample_rows` rows of each tensor (16-row aligned), every call."""
+    import oracle
+    c5 = c5_inputs()
+    W1, W2, A = (np.ascontiguousarray(c5.W1[:sample_rows]), np.ascontiguousarray(c5.W2[:sample_rows]),
+                 np.ascontiguousarray(c5.A[:sample_rows]))
+    plan = step_plan(*W1.shape, *W2.shape, *A.shape)
+    r1 = np.zeros(W1.shape, np.float32)
+    r2 = np.zeros(W2.shape, np.float32)
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        oracle.quantize(W1, rounding=oracle.SR, residual=r1, seed=0, step=7)
+        oracle.quantize(W2, block=oracle.BLOCK_16X16, rounding=oracle.SR, residual=r2, seed=0, step=7)
+        qa = oracle.quantize(A, gamax_mode=oracle.GAMAX_TENSOR, err_mode=oracle.ERR_MAE, scale_bound=256.0)
+        oracle.quantize(W1, block=oracle.BLOCK_16X16, gamax_mode=oracle.GAMAX_TENSOR,
+                        err_mode=oracle.ERR_MAE, scale_bound=256.0, colwise=True)
+        oracle.quantize(W2, block=oracle.BLOCK_16X16, gamax_mode=oracle.GAMAX_TENSOR,
+                        err_mode=oracle.ERR_MAE, scale_bound=256.0, colwise=True)
+        oracle.quantize(A)
+        oracle.quantize(W2, rounding=oracle.SR, seed=0, step=7)
+        oracle.dequantize(qa["codes"], qa["scales"], *A.shape, gamax_mode=oracle.GAMAX_TENSOR_GIVEN,
+                          gamax=qa["gamax"], scale_bound=256.0)
+    dt = (time.perf_counter() - t0) / repeats
+    total_bytes = sum(b for _, _, b in plan)
+    total_elems = sum(e for _, e, _ in plan)
+    return {"value": total_bytes / dt / GB, "unit": "GB/s", "gelem_per_s": total_elems / dt / GB,
+            "cores": 1, "kind": "oracle", "seconds_per_sample_step": dt,
+            "sample": f"first {sample_rows} rows of W1, W2 and A (every call of the step), "
+                      f"single-threaded C++ oracle"}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle as it stands, on a bounded sample."""
+    if rank != 0:
+        return
+    if args.warmup > 0:
+        cpu_baseline(sample_rows=16)
+    times = []
+    res = None
+    for _ in range(args.steps):
+        res = cpu_baseline(sample_rows=64)
+        times.append(res["seconds_per_sample_step"])
+    val = res["value"]
+    line = {"impl": "reference", "metric": "NVFP4 quantize GB/s (Gelem/s alongside); % of HBM roofline",
+            "value": round(val, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.median(times), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "gelem_per_s": round(res["gelem_per_s"], 6),
+            "config": {"workload": WORKLOAD, "sample": res["sample"]},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": res["sample"]},
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import nvfp4_block_quantization_quantize_gb300 as nv
+    import nvfp4_workloads as W
+
+    torch.cuda.set_device(local_rank)
+    nv.build()
+    nv.load_library()
+    dev = torch.device("cuda", local_rank)
+
+    c5 = c5_inputs()
+
+    def up(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    W1, W2, A = up(c5.W1), up(c5.W2), up(c5.A)
+    (M1, K1), (M2, K2), (Ma, Ka) = W1.shape, W2.shape, A.shape
+    plan = step_plan(M1, K1, M2, K2, Ma, Ka)
+    bytes_step = sum(b for _, _, b in plan)
+    elems_step = sum(e for _, e, _ in plan)
+
+    u8 = lambda *s: torch.empty(s, dtype=torch.uint8, device=dev)   # noqa: E731
+    f32 = lambda *s: torch.empty(s, dtype=torch.float32, device=dev)  # noqa: E731
+    R1 = torch.zeros((M1, K1), dtype=torch.float32, device=dev)
+    R2 = torch.zeros((M2, K2), dtype=torch.float32, device=dev)
+    out = {
+        "c1": u8(M1, K1 // 2), "s1": u8(M1, K1 // 16),
+        "c2": u8(M2, K2 // 2), "s2": u8(M2, K2 // 16),
+        "ca": u8(Ma, Ka // 2), "sa": u8(Ma, Ka // 16), "ga": f32(1),
+        "c1r": u8(M1, K1 // 2), "s1r": u8(M1, K1 // 16), "c1c": u8(K1, M1 // 2),
+        "s1c": u8(K1, M1 // 16), "g1": f32(1),
+        "c2r": u8(M2, K2 // 2), "s2r": u8(M2, K2 // 16), "c2c": u8(K2, M2 // 2),
+        "s2c": u8(K2, M2 // 16), "g2": f32(1),
+        "car": u8(Ma, Ka // 2), "sar": u8(Ma, Ka // 16),
+        "c2s": u8(M2, K2 // 2), "s2s": u8(M2, K2 // 16),
+        "da": torch.empty((Ma, Ka), dtype=torch.bfloat16, device=dev),
+    }
+    stream = torch.cuda.current_stream(dev)
+    o = out
+
+    def step(t, ev=None):
+        calls = [
+            lambda: nv.nvfp4_quantize(W1, rounding="sr", residual=R1, seed=0, step=t,
+                                      codes=o["c1"], scales=o["s1"]),
+            lambda: nv.nvfp4_quantize(W2, block="16x16", rounding="sr", residual=R2, seed=0, step=t,
+                                      codes=o["c2"], scales=o["s2"]),
+            lambda: nv.nvfp4_quantize(A, gamax_mode="tensor", gamax=o["ga"], err_mode="mae",
+                                      scale_bound=256.0, codes=o["ca"], scales=o["sa"]),
+            lambda: nv.nvfp4_quantize(W1, block="16x16", gamax_mode="tensor", gamax=o["g1"],
+                                      err_mode="mae", scale_bound=256.0, colwise=True,
+                                      codes=o["c1r"], scales=o["s1r"], codes_col=o["c1c"],
+                                      scales_col=o["s1c"]),
+            lambda: nv.nvfp4_quantize(W2, block="16x16", gamax_mode="tensor", gamax=o["g2"],
+                                      err_mode="mae", scale_bound=256.0, colwise=True,
+                                      codes=o["c2r"], scales=o["s2r"], codes_col=o["c2c"],
+                                      scales_col=o["s2c"]),
+            lambda: nv.nvfp4_quantize(A, codes=o["car"], scales=o["sar"]),
+            lambda: nv.nvfp4_quantize(W2, rounding="sr", seed=0, step=t, codes=o["c2s"],
+                                      scales=o["s2s"]),
+            lambda: nv.nvfp4_dequantize(o["ca"], o["sa"], Ma, Ka, gamax_mode="tensor_given",
+                                        gamax=o["ga"], scale_bound=256.0, out=o["da"]),
+        ]
+        for i, c in enumerate(calls):
+            if ev is not None:
+                ev[i][0].record(stream)
+            c()
+            if ev is not None:
+                ev[i][1].record(stream)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for t in range(args.warmup):
+        step(t)
+    torch.cuda.synchronize()
+
+    nsteps = args.steps
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in plan] for _ in range(nsteps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_rank{rank}.csv")
+    os.makedirs(os.path.dirname(clk_path), exist_ok=True)
+    proc, fh = clocks_sampler_start(clk_path)
+    time.sleep(0.5 if proc else 0)
+    barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(nsteps):
+        step(args.warmup + k, evs[k])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = clocks_sampler_stop(proc, fh, clk_path, local_rank)
+    total_ms = start.elapsed_time(stop)
+    per_call_ms = [statistics.mean(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(nsteps))
+                   for i in range(len(plan))]
+    if dist is not None:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / nsteps
+    value = world * bytes_step / (ms_per_step * 1e-3) / GB
+    gelem = world * elems_step / (ms_per_step * 1e-3) / GB
+
+    # ---- end to end: host (pinned) buffers through the public API ----
+    e2e = None
+    if args.e2e_steps > 0:
+        pin = lambda t: t.cpu().pin_memory()   # noqa: E731
+        hW1, hW2, hA = pin(W1), pin(W2), pin(A)
+        hR1, hR2 = pin(R1), pin(R2)
+        h2d = sum(t.numel() * t.element_size() for t in (hW1, hW2, hA, hR1, hR2))
+        d2h = [0]
+
+        def e2e_step(t):
+            outs = []
+            outs.append(nv.nvfp4_quantize(hW1, rounding="sr", residual=hR1, seed=0, step=t))
+            outs.append(nv.nvfp4_quantize(hW2, block="16x16", rounding="sr", residual=hR2, seed=0,
+                                          step=t))
+            qa = nv.nvfp4_quantize(hA, gamax_mode="tensor", err_mode="mae", scale_bound=256.0)
+            outs.append(qa)
+            outs.append(nv.nvfp4_quantize(hW1, block="16x16", gamax_mode="tensor", err_mode="mae",
+                                          scale_bound=256.0, colwise=True))
+            outs.append(nv.nvfp4_quantize(hW2, block="16x16", gamax_mode="tensor", err_mode="mae",
+                                          scale_bound=256.0, colwise=True))
+            outs.append(nv.nvfp4_quantize(hA))
+            outs.append(nv.nvfp4_quantize(hW2, rounding="sr", seed=0, step=t))
+            dq = nv.nvfp4_dequantize(qa["codes"], qa["scales"], Ma, Ka, gamax_mode="tensor_given",
+                                     gamax=qa["gamax"], scale_bound=256.0)
+            n = sum(v.numel() * v.element_size() for d in outs for v in d.values())
+            n += dq.numel() * dq.element_size() + hR1.numel() * 4 + hR2.numel() * 4
+            d2h[0] = n
+
+        e2e_step(0)
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        for k in range(args.e2e_steps):
+            e2e_step(1 + k)
+        torch.cuda.synchronize()
+        barrier()
+        dt = (time.perf_counter() - t0) / args.e2e_steps
+        if dist is not None:
+            tt = torch.tensor([dt], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            dt = float(tt.item())
+        e2e = {"value": round(world * bytes_step / dt / GB, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h[0]),
+               "ms_per_step": round(dt * 1e3, 3)}
+
+    if rank != 0:
+        return
+    # ---- roofline of the dominant kernel ----
+    dom = int(np.argmax(per_call_ms))
+    name, elems, nbytes = plan[dom]
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    achieved = nbytes / (per_call_ms[dom] * 1e-3) / GB
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(name),
+                "kernel": name, "peak_source": "measured" if peaks else "fallback",
+                "algorithmic_bytes_per_launch": int(nbytes), "ms_per_launch": round(per_call_ms[dom], 4)}
+    calls = [{"call": n, "ms": round(ms, 4), "GB/s": round(b / (ms * 1e-3) / GB, 1),
+              "frac_of_peak": round(b / (ms * 1e-3) / GB / peak, 3)}
+             for (n, _, b), ms in zip(plan, per_call_ms)]
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline()
+        cpu = {"value": round(cb["value"], 4), "unit": "GB/s", "cores": cb["cores"],
+               "kind": "oracle", "sample": cb["sample"]}
+    line = {
+        "metric": "NVFP4 quantize GB/s (Gelem/s alongside); % of HBM roofline",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": nsteps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded numpy generators; no dataset)",
+        "gelem_per_s": round(gelem, 3),
+        "config": {"workload": WORKLOAD, "bytes_per_step": int(bytes_step),
+                   "elements_per_step": int(elems_step),
+                   "l2": "inputs larger than L2: each step streams ~2.7 GB and no tensor is "
+                         "re-read within 129 MB of other traffic, except the second (quantize) "
+                         "pass after an amax pass over the same tensor",
+                   "parallelism": f"{world} independent replica(s), no data-path collective"},
+        "gpu_launches": 11 * nsteps,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "calls": calls,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if world > 1 and rank != 0:
+            return
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_gpu(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

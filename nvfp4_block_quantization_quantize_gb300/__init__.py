@@ -1,0 +1,278 @@
+"""NVFP4 block quantization on GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over ``libnvfp4_gb300.so`` (the C ABI in
+``include/nvfp4.h``).  It only marshals arguments: torch supplies device
+memory and the current stream, and every step of quantization runs in the
+library's CUDA kernels.  There is no CPU or eager fallback: if the library is
+not built, or no CUDA device is present, calls raise.
+
+Functions (same names as the C ABI):
+  nvfp4_quantize(x, ...)   -> dict(codes, scales[, codes_col, scales_col][, gamax])
+  nvfp4_dequantize(codes, scales, M, K, ...) -> tensor
+  nvfp4_qdq(x, ...)        -> dict(out[, codes, scales][, gamax])
+  nvfp4_amax(x, ...)       -> tensor
+Inputs on the CPU are staged to the current CUDA device and the results are
+copied back (the host-buffer path); CUDA inputs stay on their device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH, build  # noqa: F401  (build is re-exported)
+
+F32, BF16 = 0, 1
+BLOCK_1X16, BLOCK_16X16 = 0, 1
+RTN, SR = 0, 1
+GAMAX_NONE, GAMAX_TENSOR, GAMAX_ROW, GAMAX_TENSOR_GIVEN, GAMAX_ROW_GIVEN = 0, 1, 2, 3, 4
+ERR_NONE, ERR_MAE, ERR_MSE = 0, 1, 2
+OK, EINVAL, ECUDA = 0, 1, 2
+
+_NAMES = {
+    "block": {"1x16": BLOCK_1X16, "16x16": BLOCK_16X16},
+    "rounding": {"rtn": RTN, "sr": SR},
+    "gamax_mode": {"none": GAMAX_NONE, "tensor": GAMAX_TENSOR, "row": GAMAX_ROW,
+                   "tensor_given": GAMAX_TENSOR_GIVEN, "row_given": GAMAX_ROW_GIVEN},
+    "err_mode": {"none": ERR_NONE, "mae": ERR_MAE, "mse": ERR_MSE},
+    "dtype": {"f32": F32, "bf16": BF16},
+}
+
+EXPORTED = ("nvfp4_quantize", "nvfp4_dequantize", "nvfp4_qdq", "nvfp4_amax",
+            "nvfp4_last_error", "nvfp4_abi_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class NVFP4Error(RuntimeError):
+    """A non-OK status from the library (message from nvfp4_last_error)."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"nvfp4 status {status}: {message}")
+        self.status = status
+
+
+def load_library(path: str | None = None):
+    """Load the C library (no CUDA call is made).  Raises if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it first with "
+                               "nvfp4_block_quantization_quantize_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        P, i64, u64, i32, f32 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int,
+                                 ctypes.c_float)
+        lib.nvfp4_quantize.restype = i32
+        lib.nvfp4_quantize.argtypes = [P, i64, i64, i32, i32, i32, P, u64, u64, i64, i32, P, i32,
+                                       f32, P, P, P, P, P]
+        lib.nvfp4_qdq.restype = i32
+        lib.nvfp4_qdq.argtypes = [P, i64, i64, i32, i32, i32, P, u64, u64, i64, i32, P, i32, f32,
+                                  P, P, P, P]
+        lib.nvfp4_dequantize.restype = i32
+        lib.nvfp4_dequantize.argtypes = [P, P, i64, i64, i32, P, f32, P, i32, P]
+        lib.nvfp4_amax.restype = i32
+        lib.nvfp4_amax.argtypes = [P, i64, i64, i32, P, i32, P, P]
+        lib.nvfp4_last_error.restype = ctypes.c_char_p
+        lib.nvfp4_last_error.argtypes = []
+        lib.nvfp4_abi_version.restype = i32
+        lib.nvfp4_abi_version.argtypes = []
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _enum(kind: str, v) -> int:
+    if isinstance(v, str):
+        try:
+            return _NAMES[kind][v.lower()]
+        except KeyError:
+            raise ValueError(f"unknown {kind} {v!r}; expected one of {list(_NAMES[kind])}")
+    return int(v)
+
+
+def _check(lib, rc: int):
+    if rc != OK:
+        raise NVFP4Error(rc, lib.nvfp4_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _x_dtype(x: torch.Tensor) -> int:
+    if x.dtype == torch.float32:
+        return F32
+    if x.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"x must be float32 or bfloat16, got {x.dtype}")
+
+
+def _device_of(*ts):
+    for t in ts:
+        if t is not None and t.is_cuda:
+            return t.device
+    if not torch.cuda.is_available():
+        raise RuntimeError("nvfp4: no CUDA device (this library has no CPU path)")
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def _stage(t, dev):
+    if t is None or t.device == dev:
+        return t
+    return t.to(dev, non_blocking=True)
+
+
+def _empty(shape, dtype, dev):
+    return torch.empty(shape, dtype=dtype, device=dev)
+
+
+def _default_bound(err_mode: int, scale_bound):
+    if scale_bound is not None:
+        return float(scale_bound)
+    return 448.0 if err_mode == ERR_NONE else 256.0
+
+
+def _gamax_buffer(mode: int, gamax, M: int, dev):
+    if mode in (GAMAX_TENSOR, GAMAX_ROW):
+        if gamax is not None:
+            return gamax
+        return _empty((1,) if mode == GAMAX_TENSOR else (max(M, 1),), torch.float32, dev)
+    if mode in (GAMAX_TENSOR_GIVEN, GAMAX_ROW_GIVEN):
+        if gamax is None:
+            raise ValueError("a *_given gamax_mode needs gamax")
+        if not torch.is_tensor(gamax):
+            gamax = torch.tensor([float(gamax)], dtype=torch.float32)
+        return gamax.to(dev, torch.float32).contiguous()
+    return None
+
+
+def nvfp4_quantize(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=None, seed: int = 0,
+                   step: int = 0, row_offset: int = 0, gamax_mode="none", gamax=None,
+                   err_mode="none", scale_bound=None, colwise: bool = False, codes=None,
+                   scales=None, codes_col=None, scales_col=None, stream=None) -> dict:
+    """NVFP4 quantize of a row-major [M,K] float32/bfloat16 tensor (see nvfp4.h).
+
+    ``residual`` (float32 [M,K]) is updated in place.  Output tensors may be
+    passed in; otherwise they are allocated with torch on x's device."""
+    lib = load_library()
+    host = not x.is_cuda
+    dev = _device_of(x, residual)
+    M, K = x.shape
+    blk, rnd = _enum("block", block), _enum("rounding", rounding)
+    gm, em = _enum("gamax_mode", gamax_mode), _enum("err_mode", err_mode)
+    bound = _default_bound(em, scale_bound)
+    xd = _stage(x.contiguous(), dev)
+    rd = _stage(residual, dev)
+    g = _gamax_buffer(gm, gamax, M, dev)
+    codes = codes if codes is not None else _empty((M, K // 2), torch.uint8, dev)
+    scales = scales if scales is not None else _empty((M, K // 16), torch.uint8, dev)
+    if colwise:
+        codes_col = codes_col if codes_col is not None else _empty((K, M // 2), torch.uint8, dev)
+        scales_col = scales_col if scales_col is not None else _empty((K, M // 16), torch.uint8, dev)
+    rc = lib.nvfp4_quantize(_ptr(xd), M, K, _x_dtype(x), blk, rnd, _ptr(rd), seed, step,
+                            row_offset, gm, _ptr(g), em, bound, _ptr(codes), _ptr(scales),
+                            _ptr(codes_col), _ptr(scales_col), _stream(stream))
+    _check(lib, rc)
+    out = {"codes": codes, "scales": scales}
+    if colwise:
+        out["codes_col"], out["scales_col"] = codes_col, scales_col
+    if g is not None:
+        out["gamax"] = g
+    if host:
+        out = {k: v.cpu() for k, v in out.items()}
+        if residual is not None and rd is not residual:
+            residual.copy_(rd.cpu())
+    return out
+
+
+def nvfp4_qdq(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=None, seed: int = 0,
+              step: int = 0, row_offset: int = 0, gamax_mode="none", gamax=None, err_mode="none",
+              scale_bound=None, want_codes: bool = False, out=None, stream=None) -> dict:
+    """quantize then dequantize to bf16 in one pass; ``out`` is bf16 [M,K]."""
+    lib = load_library()
+    host = not x.is_cuda
+    dev = _device_of(x, residual)
+    M, K = x.shape
+    blk, rnd = _enum("block", block), _enum("rounding", rounding)
+    gm, em = _enum("gamax_mode", gamax_mode), _enum("err_mode", err_mode)
+    bound = _default_bound(em, scale_bound)
+    xd = _stage(x.contiguous(), dev)
+    rd = _stage(residual, dev)
+    g = _gamax_buffer(gm, gamax, M, dev)
+    o = out if out is not None and out.is_cuda else _empty((M, K), torch.bfloat16, dev)
+    codes = _empty((M, K // 2), torch.uint8, dev) if want_codes else None
+    scales = _empty((M, K // 16), torch.uint8, dev) if want_codes else None
+    rc = lib.nvfp4_qdq(_ptr(xd), M, K, _x_dtype(x), blk, rnd, _ptr(rd), seed, step, row_offset,
+                       gm, _ptr(g), em, bound, _ptr(codes), _ptr(scales), _ptr(o),
+                       _stream(stream))
+    _check(lib, rc)
+    res = {"out": o}
+    if want_codes:
+        res["codes"], res["scales"] = codes, scales
+    if g is not None:
+        res["gamax"] = g
+    if host:
+        res = {k: v.cpu() for k, v in res.items()}
+        if residual is not None and rd is not residual:
+            residual.copy_(rd.cpu())
+        if out is not None:
+            out.copy_(res["out"])
+            res["out"] = out
+    return res
+
+
+def nvfp4_dequantize(codes: torch.Tensor, scales: torch.Tensor, M: int, K: int, *,
+                     gamax_mode="none", gamax=None, scale_bound=None, out_dtype="bf16", out=None,
+                     stream=None) -> torch.Tensor:
+    lib = load_library()
+    host = not codes.is_cuda
+    dev = _device_of(codes, scales)
+    gm = _enum("gamax_mode", gamax_mode)
+    od = _enum("dtype", out_dtype)
+    bound = 448.0 if scale_bound is None else float(scale_bound)
+    c = _stage(codes.contiguous(), dev)
+    s = _stage(scales.contiguous(), dev)
+    g = None
+    if gm != GAMAX_NONE:
+        if gamax is None:
+            raise ValueError("gamax_mode needs gamax")
+        g = (gamax if torch.is_tensor(gamax) else torch.tensor([float(gamax)])).to(dev, torch.float32)
+    o = out if out is not None and out.is_cuda else _empty(
+        (M, K), torch.bfloat16 if od == BF16 else torch.float32, dev)
+    rc = lib.nvfp4_dequantize(_ptr(c), _ptr(s), M, K, gm, _ptr(g), bound, _ptr(o), od,
+                              _stream(stream))
+    _check(lib, rc)
+    return o.cpu() if host else o
+
+
+def nvfp4_amax(x: torch.Tensor, *, residual=None, per_row: bool = False, out=None,
+               stream=None) -> torch.Tensor:
+    lib = load_library()
+    host = not x.is_cuda
+    dev = _device_of(x, residual)
+    M, K = x.shape
+    xd = _stage(x.contiguous(), dev)
+    rd = _stage(residual, dev)
+    o = out if out is not None else _empty((max(M, 1),) if per_row else (1,), torch.float32, dev)
+    rc = lib.nvfp4_amax(_ptr(xd), M, K, _x_dtype(x), _ptr(rd), GAMAX_ROW if per_row else GAMAX_TENSOR,
+                        _ptr(o), _stream(stream))
+    _check(lib, rc)
+    return o.cpu() if host else o
+
+
+def nvfp4_last_error() -> str:
+    return load_library().nvfp4_last_error().decode()

@@ -1,0 +1,162 @@
+// nvfp4_aux.cu -- global amax and dequantize kernels for sm_103a.
+//
+// amax: max |x (+ residual)| with NaN dropped, per tensor or per row, the
+// global scale's input ("Add NVFP4 four-over-six (row-wise) quantization to
+// the training prototype", What: scalar vs (rows,) global_amax; CuTe DSL
+// kernel (SM100), Design: NaN-dropping max).
+// dequantize: (q * dec(scale)) * S_dec ("fp4-train", API: dequantize).
+#include "nvfp4_device.cuh"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+template <int DT, bool EF>
+__device__ __forceinline__ float block_absmax(const void* x, const float* res, int64_t e0) {
+    float y[16];
+    load16<DT>(x, e0, y);
+    if (EF) {
+        float r[16];
+        load16_f32(res, e0, r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = max_nd(m, fabsf(y[i]));
+    return m;
+}
+
+__device__ __forceinline__ float warp_max(float m) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max_nd(m, __shfl_xor_sync(kFull, m, o));
+    return m;
+}
+
+// Per-tensor amax; *out must hold +0 on entry.  The maximum of non-negative
+// floats orders like their bit patterns, so an unsigned atomic max is exact.
+template <int DT, bool EF>
+__global__ void __launch_bounds__(kThreads) k_amax_tensor(const void* x, const float* res,
+                                                          int64_t nblk, float* out) {
+    __shared__ float part[kThreads / 32];
+    float m = 0.0f;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblk; b += stride)
+        m = max_nd(m, block_absmax<DT, EF>(x, res, b * 16));
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        m = threadIdx.x < kThreads / 32 ? part[threadIdx.x] : 0.0f;
+        m = warp_max(m);
+        if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(out), __float_as_uint(m));
+    }
+}
+
+// Per-row amax: one warp per row.
+template <int DT, bool EF>
+__global__ void __launch_bounds__(kThreads) k_amax_rows(const void* x, const float* res, int64_t M,
+                                                        int64_t K, float* out) {
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+    if (row >= M) return;
+    const int lane = threadIdx.x & 31;
+    float m = 0.0f;
+    for (int64_t b = lane; b < K / 16; b += 32) m = max_nd(m, block_absmax<DT, EF>(x, res, row * K + b * 16));
+    m = warp_max(m);
+    if (lane == 0) out[row] = m;
+}
+
+template <int ODT>
+__global__ void __launch_bounds__(kThreads) k_dequant(const DequantArgs a) {
+    const int64_t bpr = a.K / 16;
+    const int64_t nblk = a.M * bpr;
+    float Senc = 1.0f, Sdec = 1.0f;
+    const bool per_tensor = a.gamax_mode == NVFP4_GAMAX_TENSOR || a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN;
+    const bool per_row = a.gamax_mode == NVFP4_GAMAX_ROW || a.gamax_mode == NVFP4_GAMAX_ROW_GIVEN;
+    if (per_tensor) global_scales(a.gamax[0], a.bound, Senc, Sdec);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; blk < nblk;
+         blk += stride) {
+        const uint2 w = reinterpret_cast<const uint2*>(a.codes)[blk];
+        const float d = e4m3_decode(a.scales[blk]);
+        float Sd = Sdec;
+        if (per_row) {
+            float se;
+            global_scales(a.gamax[blk / bpr], a.bound, se, Sd);
+        }
+        float q[16];
+        e2m1_decode8(w.x, q);
+        e2m1_decode8(w.y, q + 8);
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = mul_rn(mul_rn(q[i], d), Sd);
+        if (ODT == NVFP4_BF16) store16_bf16(static_cast<uint16_t*>(a.out), blk * 16, v);
+        else store16_f32(static_cast<float*>(a.out), blk * 16, v);
+    }
+}
+
+int grid_for(int64_t nblk) {
+    const int64_t want = (nblk + kThreads - 1) / kThreads;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+    return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+}  // namespace
+
+int sm_count() {
+    static thread_local int dev = -1, count = 0;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    if (cur != dev) {
+        cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, cur);
+        if (count <= 0) count = 1;
+        dev = cur;
+    }
+    return count;
+}
+
+int launch_amax(const void* x, int64_t M, int64_t K, int dtype, const float* residual, int mode,
+                float* out, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool ef = residual != nullptr;
+    if (mode == NVFP4_GAMAX_TENSOR) {
+        cudaMemsetAsync(out, 0, sizeof(float), s);
+        const int64_t nblk = M * (K / 16);
+        if (nblk > 0) {
+            const int g = grid_for(nblk);
+            if (dtype == NVFP4_BF16) {
+                if (ef) k_amax_tensor<NVFP4_BF16, true><<<g, kThreads, 0, s>>>(x, residual, nblk, out);
+                else k_amax_tensor<NVFP4_BF16, false><<<g, kThreads, 0, s>>>(x, residual, nblk, out);
+            } else {
+                if (ef) k_amax_tensor<NVFP4_F32, true><<<g, kThreads, 0, s>>>(x, residual, nblk, out);
+                else k_amax_tensor<NVFP4_F32, false><<<g, kThreads, 0, s>>>(x, residual, nblk, out);
+            }
+        }
+    } else {
+        if (M > 0) {
+            const int g = static_cast<int>((M + kThreads / 32 - 1) / (kThreads / 32));
+            if (dtype == NVFP4_BF16) {
+                if (ef) k_amax_rows<NVFP4_BF16, true><<<g, kThreads, 0, s>>>(x, residual, M, K, out);
+                else k_amax_rows<NVFP4_BF16, false><<<g, kThreads, 0, s>>>(x, residual, M, K, out);
+            } else {
+                if (ef) k_amax_rows<NVFP4_F32, true><<<g, kThreads, 0, s>>>(x, residual, M, K, out);
+                else k_amax_rows<NVFP4_F32, false><<<g, kThreads, 0, s>>>(x, residual, M, K, out);
+            }
+        }
+    }
+    return static_cast<int>(cudaGetLastError());
+}
+
+int launch_dequantize(const DequantArgs& a, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t nblk = a.M * (a.K / 16);
+    if (nblk == 0) return 0;
+    const int g = grid_for(nblk);
+    if (a.out_dtype == NVFP4_BF16) k_dequant<NVFP4_BF16><<<g, kThreads, 0, s>>>(a);
+    else k_dequant<NVFP4_F32><<<g, kThreads, 0, s>>>(a);
+    return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,47 @@
+// nvfp4_params.h -- argument bundle passed from the C ABI to the kernels.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/nvfp4.h"
+
+namespace nvfp4 {
+
+struct QuantArgs {
+    const void* x;
+    int64_t M, K;
+    int dtype, block, rounding;
+    float* residual;          // null = no error feedback
+    uint64_t seed, step;
+    int64_t row_offset;
+    int gamax_mode;           // after the amax step: NONE, TENSOR_GIVEN or ROW_GIVEN
+    const float* gamax;
+    int err_mode;
+    float bound;
+    uint8_t* codes;           // may be null for qdq
+    uint8_t* scales;          // may be null for qdq
+    uint8_t* codes_col;       // null = no columnwise output
+    uint8_t* scales_col;
+    uint16_t* dq_bf16;        // qdq output, null otherwise
+};
+
+struct DequantArgs {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    int64_t M, K;
+    int gamax_mode;
+    const float* gamax;
+    float bound;
+    void* out;
+    int out_dtype;
+};
+
+// launchers (each returns cudaGetLastError() after its launches)
+int launch_quantize_rows(const QuantArgs& a, void* stream);    // 1x16, rowwise only
+int launch_quantize_tiles(const QuantArgs& a, void* stream);   // 16x16, or any columnwise
+int launch_dequantize(const DequantArgs& a, void* stream);
+int launch_amax(const void* x, int64_t M, int64_t K, int dtype, const float* residual, int mode,
+                float* out, void* stream);
+int sm_count();
+
+}  // namespace nvfp4

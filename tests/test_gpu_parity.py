@@ -1,0 +1,232 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle,
+element by element, tolerance zero, on seeded inputs from nvfp4_workloads.
+
+Sizes here let the oracle finish in seconds while spanning many CTAs, several
+256-column chunks and ragged tails (K not a multiple of 256, M not a multiple
+of 128).  The full-size configurations are in test_gpu_configs.py.
+"""
+import itertools
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_workloads as W
+import oracle
+from parity_helpers import assert_same, compare_quant, quantize_both, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+nv = pytest.importorskip("nvfp4_block_quantization_quantize_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    nv.build()
+    nv.load_library()
+
+
+def mat(shape, seed, dtype="f32", dist="normal", outliers=0.0):
+    return W.matrix(shape, seed=seed, dtype=dtype, dist=dist, outlier_frac=outliers,
+                    outlier_factor=50.0)
+
+
+# ---- the fp4-train recipe (no global scale) ----------------------------------------------
+@pytest.mark.parametrize("rounding", ["rtn", "sr"])
+def test_c1_quantize_dequantize_qdq(rounding):
+    x = W.c1()
+    gpu, o = quantize_both(x, rounding=rounding, seed=0, step=0)
+    compare_quant(gpu, o)
+    M, K = x.shape
+    for od, ood in (("bf16", oracle.BF16), ("f32", oracle.F32)):
+        d = nv.nvfp4_dequantize(to_dev(gpu["codes"]), to_dev(gpu["scales"]), M, K, out_dtype=od)
+        assert_same(to_np(d), oracle.dequantize(o["codes"], o["scales"], M, K, out_dtype=ood),
+                    f"dequantize {od}")
+    q = nv.nvfp4_qdq(to_dev(x), rounding=rounding, want_codes=True)
+    oq = oracle.qdq(x, rounding=oracle.SR if rounding == "sr" else oracle.RTN)
+    assert_same(to_np(q["out"]), oq["out"], "qdq out")
+    assert_same(to_np(q["codes"]), oq["codes"], "qdq codes")
+
+
+@pytest.mark.parametrize("rounding", ["rtn", "sr"])
+def test_c1_scalar_2_3(rounding):
+    for x in (W.c1_23(), W.c1_23b()):
+        gpu, o = quantize_both(x, rounding=rounding, seed=0, step=0)
+        compare_quant(gpu, o)
+    dq = to_np(nv.nvfp4_dequantize(to_dev(gpu["codes"]), to_dev(gpu["scales"]), *x.shape,
+                                   out_dtype="f32"))
+    mean = dq[:, 1:].astype(np.float64).mean()
+    if rounding == "sr":
+        assert abs(mean - 2.3) <= 0.005      # "fp4-train", Correctness
+    else:
+        assert mean == 2.0
+
+
+PLAIN = list(itertools.product(["f32", "bf16"], ["1x16", "16x16"], ["rtn", "sr"], [False, True],
+                               ["none", "tensor", "row", "tensor_given"]))
+
+
+@pytest.mark.parametrize("dtype,block,rounding,ef,gm", PLAIN)
+def test_plain_matrix(dtype, block, rounding, ef, gm):
+    if block == "16x16" and gm == "row":
+        pytest.skip("per-row global scale is 1x16 only")
+    x = mat((304, 304), seed=zlib.crc32(f"{dtype}{block}{rounding}{ef}{gm}".encode()) % 1000, dtype=dtype,
+            dist="t")
+    res = (np.random.default_rng(1).standard_normal(x.shape) * 0.05).astype(np.float32) if ef else None
+    kw = dict(block=block, rounding=rounding, seed=11, step=5, row_offset=3, gamax_mode=gm,
+              scale_bound=448.0)
+    if gm == "tensor_given":
+        kw["gamax"] = np.array([7.5], np.float32)
+    gpu, o = quantize_both(x, residual=res, **kw)
+    compare_quant(gpu, o)
+
+
+FOUR_SIX = list(itertools.product(["f32", "bf16"], ["mae", "mse"], [256.0, 448.0],
+                                  ["1x16", "16x16"], ["tensor", "row"], [False, True]))
+
+
+@pytest.mark.parametrize("dtype,err,bound,block,gm,colwise", FOUR_SIX)
+def test_four_over_six_matrix(dtype, err, bound, block, gm, colwise):
+    if gm == "row" and (block == "16x16" or colwise):
+        pytest.skip("a row-scaled tensor has no 16x16 or columnwise form")
+    for shape in ((128, 128), (256, 512), (304, 304), (128, 320)):
+        x = mat(shape, seed=sum(shape), dtype=dtype, outliers=0.02)
+        gpu, o = quantize_both(x, block=block, gamax_mode=gm, err_mode=err, scale_bound=bound,
+                               colwise=colwise)
+        compare_quant(gpu, o)
+
+
+@pytest.mark.parametrize("shape", [(16, 16), (1, 16), (3, 48), (32, 272), (48, 4112), (2048, 1024),
+                                   (64, 1024)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ragged_and_page_shapes(shape, dtype):
+    x = mat(shape, seed=shape[0] * 7 + shape[1], dtype=dtype)
+    gpu, o = quantize_both(x, rounding="sr", seed=3, step=1)
+    compare_quant(gpu, o)
+    if shape[0] % 16 == 0:
+        gpu, o = quantize_both(x, block="16x16", gamax_mode="tensor", err_mode="mse",
+                               colwise=True)
+        compare_quant(gpu, o)
+        gpu, o = quantize_both(x, gamax_mode="tensor", err_mode="mae", colwise=True)
+        compare_quant(gpu, o)
+
+
+def test_empty_inputs():
+    for M, K in ((0, 64), (16, 0), (0, 0)):
+        x = torch.empty((M, K), dtype=torch.float32, device="cuda")
+        r = nv.nvfp4_quantize(x, gamax_mode="tensor")
+        torch.cuda.synchronize()
+        assert r["codes"].numel() == M * K // 2
+        assert float(r["gamax"][0]) == 0.0
+    r = nv.nvfp4_quantize(torch.empty((8, 0), device="cuda"), gamax_mode="row")
+    torch.cuda.synchronize()
+    assert np.all(to_np(r["gamax"]) == 0)
+
+
+def test_special_values():
+    x = W.c4_specials(W.c4(256, 512), with_inf_nan=False)
+    xi = W.c4_specials(W.c4(256, 512), with_inf_nan=True)
+    for xx in (x, xi):
+        for kw in (dict(), dict(rounding="sr", seed=5), dict(block="16x16"),
+                   dict(gamax_mode="tensor", err_mode="mse", block="16x16", colwise=True),
+                   dict(gamax_mode="tensor", err_mode="mse", block="16x16", colwise=True,
+                        scale_bound=448.0),
+                   dict(gamax_mode="row", err_mode="mae"),
+                   dict(gamax_mode="tensor", err_mode="mae", colwise=True)):
+            gpu, o = quantize_both(xx, **kw)
+            compare_quant(gpu, o)
+        res = np.zeros(xx.shape, np.float32)
+        gpu, o = quantize_both(xx, residual=res, rounding="sr", seed=2, step=9)
+        compare_quant(gpu, o)
+
+
+def test_subnormal_and_large_plain_scales():
+    rng = np.random.default_rng(44)
+    x = rng.standard_normal((64, 256)).astype(np.float32)
+    x *= np.exp2(rng.integers(-140, 12, (64, 16))).repeat(16, axis=1).astype(np.float32)
+    for kw in (dict(), dict(rounding="sr", seed=9), dict(gamax_mode="tensor"),
+               dict(gamax_mode="row"), dict(block="16x16")):
+        gpu, o = quantize_both(x, **kw)
+        compare_quant(gpu, o)
+
+
+def test_dequantize_global_modes():
+    x = mat((128, 256), seed=5, outliers=0.05)
+    for gm, given in (("tensor", "tensor_given"), ("row", "row_given")):
+        gpu, o = quantize_both(x, gamax_mode=gm, err_mode="mse", scale_bound=256.0)
+        compare_quant(gpu, o)
+        for od, ood in (("bf16", oracle.BF16), ("f32", oracle.F32)):
+            d = nv.nvfp4_dequantize(to_dev(gpu["codes"]), to_dev(gpu["scales"]), *x.shape,
+                                    gamax_mode=given, gamax=to_dev(gpu["gamax"]),
+                                    scale_bound=256.0, out_dtype=od)
+            e = oracle.dequantize(o["codes"], o["scales"], *x.shape,
+                                  gamax_mode=oracle.GAMAX_TENSOR_GIVEN if gm == "tensor"
+                                  else oracle.GAMAX_ROW_GIVEN, gamax=o["gamax"],
+                                  scale_bound=256.0, out_dtype=ood)
+            assert_same(to_np(d), e, f"dequantize {gm} {od}")
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(rounding="sr", seed=4, step=2),
+                                dict(gamax_mode="tensor", err_mode="mae"),
+                                dict(gamax_mode="row", err_mode="mse"),
+                                dict(block="16x16", rounding="sr")])
+def test_qdq_matches(kw):
+    x = mat((256, 512), seed=8, dtype="bf16", dist="t")
+    res = (np.random.default_rng(3).standard_normal(x.shape) * 0.01).astype(np.float32)
+    use_res = kw.get("err_mode", "none") == "none"
+    rd = to_dev(res) if use_res else None
+    q = nv.nvfp4_qdq(to_dev(x), residual=rd, want_codes=True, **kw)
+    ro = res.copy() if use_res else None
+    from parity_helpers import oracle_kwargs
+    oq = oracle.qdq(x, residual=ro, **oracle_kwargs(kw))
+    assert_same(to_np(q["out"]), oq["out"], "qdq out")
+    assert_same(to_np(q["codes"]), oq["codes"], "qdq codes")
+    assert_same(to_np(q["scales"]), oq["scales"], "qdq scales")
+    if use_res:
+        assert_same(to_np(rd), ro, "qdq residual")
+
+
+def test_amax_entry_point():
+    x = mat((96, 160), seed=9, dtype="bf16", outliers=0.1)
+    res = (np.random.default_rng(4).standard_normal(x.shape)).astype(np.float32)
+    for per_row in (False, True):
+        for r in (None, res):
+            g = nv.nvfp4_amax(to_dev(x), residual=None if r is None else to_dev(r), per_row=per_row)
+            e = oracle.amax(x, residual=r, per_row=per_row)
+            assert_same(to_np(g), e, "amax")
+
+
+def test_row_shards_match_the_whole_tensor():
+    """Row shards quantized with row_offset and the whole tensor's amax
+    reproduce the unsharded result, stochastic rounding included."""
+    x = mat((512, 256), seed=10, dtype="bf16")
+    whole = nv.nvfp4_quantize(to_dev(x), rounding="sr", seed=77, step=3, gamax_mode="tensor")
+    A = whole["gamax"]
+    parts = [nv.nvfp4_quantize(to_dev(x[r0:r0 + 128]), rounding="sr", seed=77, step=3,
+                               row_offset=r0, gamax_mode="tensor_given", gamax=A)
+             for r0 in range(0, 512, 128)]
+    torch.cuda.synchronize()
+    assert_same(np.concatenate([to_np(p["codes"]) for p in parts]), to_np(whole["codes"]), "codes")
+    assert_same(np.concatenate([to_np(p["scales"]) for p in parts]), to_np(whole["scales"]), "scales")
+
+
+def test_host_buffer_path():
+    x = mat((64, 128), seed=12)
+    r = nv.nvfp4_quantize(torch.from_numpy(x), rounding="sr", seed=1)
+    assert r["codes"].device.type == "cpu"
+    o = oracle.quantize(x, rounding=oracle.SR, seed=1)
+    assert_same(r["codes"].numpy(), o["codes"], "codes")
+
+
+def test_stream_argument_is_honoured():
+    x = to_dev(mat((256, 256), seed=13))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        r = nv.nvfp4_quantize(x, stream=s)
+    s.synchronize()
+    ref = nv.nvfp4_quantize(x)
+    torch.cuda.synchronize()
+    assert torch.equal(r["codes"], ref["codes"])

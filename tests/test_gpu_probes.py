@@ -1,0 +1,89 @@
+"""Device probes of the conversion instructions and the generator, run through
+the library's own entry points (in-bounds inputs only).
+
+- e2m1: blocks [6.0, y1..y15] have scale exactly 1.0 (6/6), so the stored code
+  of each y is the hardware's e2m1 rounding of y itself.  Every fp32 value with
+  0.125 <= |y| <= 6 (all decision boundaries of the grid) is checked against
+  the oracle's encoder, plus signed zeros, tiny values and subnormals.
+- e4m3: blocks [b, 0 x 15] give scale E4M3(b / 6); b sweeps +-4096 ulps around
+  6x every e4m3 midpoint, plus random values over the whole scale range.
+- Philox: stochastic rounding at global indices whose counter uses all four
+  words (row_offset beyond 2^32 blocks, steps beyond 2^32, a 64-bit seed).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_helpers import assert_same, quantize_both, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+nv = pytest.importorskip("nvfp4_block_quantization_quantize_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    nv.build()
+    nv.load_library()
+
+
+def blocks_of(values, lead):
+    n = (values.size + 14) // 15
+    v = np.zeros(n * 15, np.float32)
+    v[:values.size] = values
+    x = np.empty((n, 16), np.float32)
+    x[:, 0] = lead
+    x[:, 1:] = v.reshape(n, 15)
+    return x, values.size
+
+
+def unpack_codes(codes):
+    lo = codes & 0x0F
+    hi = codes >> 4
+    return np.stack([lo, hi], axis=-1).reshape(codes.shape[0], -1)
+
+
+def test_e2m1_conversion_exhaustive_window():
+    lo = np.array([0.125], np.float32).view(np.uint32)[0]
+    hi = np.array([6.0], np.float32).view(np.uint32)[0]
+    pos = np.arange(lo, hi + 1, dtype=np.uint32).view(np.float32)
+    extra = np.array([0.0, -0.0, 1e-30, -1e-30, 2.0 ** -149, -(2.0 ** -149), 2.0 ** -126,
+                      0.0625, -0.0625], np.float32)
+    for vals in (pos, -pos, extra):
+        x, n = blocks_of(vals, 6.0)
+        r = nv.nvfp4_quantize(to_dev(x))
+        torch.cuda.synchronize()
+        assert np.all(to_np(r["scales"]) == 0x38)
+        got = unpack_codes(to_np(r["codes"]))[:, 1:].reshape(-1)[:n]
+        assert_same(got, oracle.e2m1_encode_rn(vals), "e2m1 codes")
+
+
+def test_e4m3_conversion_near_midpoints():
+    tab = oracle.e4m3_decode(np.arange(0x7F)).astype(np.float64)
+    mids = ((tab[:-1] + tab[1:]) / 2 * 6).astype(np.float32)
+    b = np.concatenate([
+        (mids.view(np.uint32)[:, None].astype(np.int64) + np.arange(-4096, 4097)[None, :])
+        .astype(np.uint32).reshape(-1).view(np.float32),
+        np.exp2(np.random.default_rng(1).uniform(-12, 12, 2_000_000)).astype(np.float32),
+        np.array([6 * 448.0, 6 * 464.0, 1e30, 2.0 ** -130], np.float32)])
+    b = b[b > 0]
+    x = np.zeros((b.size, 16), np.float32)
+    x[:, 0] = b
+    r = nv.nvfp4_quantize(to_dev(x))
+    torch.cuda.synchronize()
+    expect = oracle.e4m3_encode(np.minimum(b / np.float32(6.0), np.float32(448.0)))
+    assert_same(to_np(r["scales"])[:, 0], expect, "e4m3 scales")
+
+
+@pytest.mark.parametrize("block", ["1x16", "16x16"])
+def test_philox_all_counter_words(block):
+    x = np.full((32, 64), 2.3, np.float32)
+    x[:, ::16] = 6.0
+    for seed, step, row_offset in ((0xFEDCBA9876543210, 0, 0), (3, (1 << 32) + 5, 0),
+                                   (3, 7, (1 << 34) // 64 * 16), (2**64 - 1, 2**64 - 1, 1 << 40)):
+        gpu, o = quantize_both(x, block=block, rounding="sr", seed=seed, step=step,
+                               row_offset=row_offset)
+        assert_same(gpu["codes"], o["codes"], f"sr codes seed={seed} step={step}")
