@@ -197,13 +197,22 @@ def amax(x: np.ndarray, residual: np.ndarray | None = None, per_row: bool = Fals
 
 
 # ---- the three calls ------------------------------------------------------------------
+def _default_bound(err_mode: int, scale_bound):
+    if scale_bound is not None:
+        return float(scale_bound)
+    return 448.0 if err_mode == ERR_NONE else 256.0
+
+
 def quantize(x: np.ndarray, *, block: int = BLOCK_1X16, rounding: int = RTN,
              residual: np.ndarray | None = None, seed: int = 0, step: int = 0,
              row_offset: int = 0, gamax_mode: int = GAMAX_NONE, gamax=None,
-             err_mode: int = ERR_NONE, scale_bound: float = 448.0, colwise: bool = False):
+             err_mode: int = ERR_NONE, scale_bound: float | None = None, colwise: bool = False):
     """Returns dict(codes, scales[, codes_col, scales_col], gamax).  ``residual``
-    (float32, contiguous) is updated in place, as the library does."""
+    (float32, contiguous) is updated in place, as the library does.  The bound
+    defaults to 448 for the plain quantizer and 256 for four-over-six (the
+    four-over-six page's default)."""
     lib = _load()
+    scale_bound = _default_bound(err_mode, scale_bound)
     x = np.ascontiguousarray(x)
     M, K = x.shape
     codes = np.zeros((M, K // 2), np.uint8)
@@ -248,9 +257,10 @@ def dequantize(codes: np.ndarray, scales: np.ndarray, M: int, K: int, *,
 def qdq(x: np.ndarray, *, block: int = BLOCK_1X16, rounding: int = RTN,
         residual: np.ndarray | None = None, seed: int = 0, step: int = 0, row_offset: int = 0,
         gamax_mode: int = GAMAX_NONE, gamax=None, err_mode: int = ERR_NONE,
-        scale_bound: float = 448.0):
+        scale_bound: float | None = None):
     """Returns dict(out (bf16 bits, uint16), codes, scales, gamax)."""
     lib = _load()
+    scale_bound = _default_bound(err_mode, scale_bound)
     x = np.ascontiguousarray(x)
     M, K = x.shape
     codes = np.zeros((M, K // 2), np.uint8)
