@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--only", default=None,
+                   help="run only the step's calls whose name contains this text (profiling)")
     return p.parse_args()
 
 
@@ -269,6 +271,8 @@ def run_gpu(args, rank, world, local_rank):
                                         gamax=o["ga"], scale_bound=256.0, out=o["da"]),
         ]
         for i, c in enumerate(calls):
+            if args.only and args.only not in plan[i][0]:
+                continue
             if ev is not None:
                 ev[i][0].record(stream)
             c()
@@ -393,7 +397,8 @@ def run_gpu(args, rank, world, local_rank):
                          "re-read within 129 MB of other traffic, except the second (quantize) "
                          "pass after an amax pass over the same tensor",
                    "parallelism": f"{world} independent replica(s), no data-path collective"},
-        "gpu_launches": 11 * nsteps,
+        "gpu_launches": nsteps * sum(n for (name, _, _), n in zip(plan, (1, 1, 2, 2, 2, 1, 1, 1))
+                                     if not args.only or args.only in name),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "calls": calls,
     }
     print(json.dumps(line), flush=True)

@@ -157,6 +157,16 @@ int nvfp4_qdq(const void* x, int64_t M, int64_t K, int dtype, int block, int rou
 int nvfp4_amax(const void* x, int64_t M, int64_t K, int dtype, const float* residual,
                int mode, float* out, void* stream);
 
+/*
+ * nvfp4_probe_divide -- diagnostic.  out[i] = a[i] / b[i] computed by the
+ * device routine the plain quantizer uses for "every element is divided by the
+ * decoded scale" [fp4-train, Method] (its stochastic-rounding form, which must
+ * equal IEEE round-to-nearest division for every input).  Device pointers,
+ * n >= 0 elements, 4-byte aligned; EINVAL on bad arguments.  It exists so the
+ * routine can be checked exhaustively against IEEE division.
+ */
+int nvfp4_probe_divide(const float* a, const float* b, float* out, int64_t n, void* stream);
+
 /* message for the calling thread's last non-OK status ("" if none) */
 const char* nvfp4_last_error(void);
 

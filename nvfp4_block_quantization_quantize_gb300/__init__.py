@@ -41,7 +41,7 @@ _NAMES = {
 }
 
 EXPORTED = ("nvfp4_quantize", "nvfp4_dequantize", "nvfp4_qdq", "nvfp4_amax",
-            "nvfp4_last_error", "nvfp4_abi_version")
+            "nvfp4_probe_divide", "nvfp4_last_error", "nvfp4_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +78,8 @@ def load_library(path: str | None = None):
         lib.nvfp4_dequantize.argtypes = [P, P, i64, i64, i32, P, f32, P, i32, P]
         lib.nvfp4_amax.restype = i32
         lib.nvfp4_amax.argtypes = [P, i64, i64, i32, P, i32, P, P]
+        lib.nvfp4_probe_divide.restype = i32
+        lib.nvfp4_probe_divide.argtypes = [P, P, P, i64, P]
         lib.nvfp4_last_error.restype = ctypes.c_char_p
         lib.nvfp4_last_error.argtypes = []
         lib.nvfp4_abi_version.restype = i32
@@ -272,6 +274,16 @@ def nvfp4_amax(x: torch.Tensor, *, residual=None, per_row: bool = False, out=Non
                         _ptr(o), _stream(stream))
     _check(lib, rc)
     return o.cpu() if host else o
+
+
+def nvfp4_probe_divide(a: torch.Tensor, b: torch.Tensor, stream=None) -> torch.Tensor:
+    """Diagnostic: the plain path's device division a / b, elementwise (fp32)."""
+    lib = load_library()
+    a = a.contiguous()
+    b = b.contiguous()
+    out = torch.empty_like(a)
+    _check(lib, lib.nvfp4_probe_divide(_ptr(a), _ptr(b), _ptr(out), a.numel(), _stream(stream)))
+    return out
 
 
 def nvfp4_last_error() -> str:

@@ -177,6 +177,18 @@ int nvfp4_amax(const void* x, int64_t M, int64_t K, int dtype, const float* resi
     return NVFP4_OK;
 }
 
+int nvfp4_probe_divide(const float* a, const float* b, float* out, int64_t n, void* stream) {
+    g_msg[0] = '\0';
+    if (n < 0) return fail(NVFP4_EINVAL, "n must be >= 0");
+    int rc;
+    if ((rc = check_ptr(a, "a", n > 0, 4))) return rc;
+    if ((rc = check_ptr(b, "b", n > 0, 4))) return rc;
+    if ((rc = check_ptr(out, "out", n > 0, 4))) return rc;
+    const int err = nvfp4::launch_probe_divide(a, b, out, n, stream);
+    if (err) return cuda_fail(err, "probe launch");
+    return NVFP4_OK;
+}
+
 const char* nvfp4_last_error(void) { return g_msg; }
 
 int nvfp4_abi_version(void) { return 100; }

@@ -5,7 +5,7 @@
 // the training prototype", What: scalar vs (rows,) global_amax; CuTe DSL
 // kernel (SM100), Design: NaN-dropping max).
 // dequantize: (q * dec(scale)) * S_dec ("fp4-train", API: dequantize).
-#include "nvfp4_device.cuh"
+#include "nvfp4_block.cuh"
 
 namespace nvfp4 {
 namespace {
@@ -97,6 +97,19 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DequantArgs a) {
     }
 }
 
+// out[i] = the plain path's division a[i] / b[i] (its exact, stochastic-
+// rounding form), with the block amax taken as |a[i]|.
+__global__ void __launch_bounds__(kThreads) k_probe_divide(const float* a, const float* b,
+                                                           float* out, int64_t n) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const float y = a[i], D = b[i];
+        const bool fast = plain_fast(D, fabsf(y));
+        const float r = fast ? div_rn(1.0f, D) : 0.0f;
+        out[i] = plain_quotient<true>(y, D, r, fast);
+    }
+}
+
 int grid_for(int64_t nblk) {
     const int64_t want = (nblk + kThreads - 1) / kThreads;
     const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
@@ -146,6 +159,13 @@ int launch_amax(const void* x, int64_t M, int64_t K, int dtype, const float* res
             }
         }
     }
+    return static_cast<int>(cudaGetLastError());
+}
+
+int launch_probe_divide(const float* a, const float* b, float* out, int64_t n, void* stream) {
+    if (n <= 0) return 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    k_probe_divide<<<grid_for((n + 15) / 16), kThreads, 0, s>>>(a, b, out, n);
     return static_cast<int>(cudaGetLastError());
 }
 

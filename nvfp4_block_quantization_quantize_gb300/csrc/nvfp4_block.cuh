@@ -1,0 +1,207 @@
+// nvfp4_block.cuh -- quantization of one 16-value group, shared by the kernels.
+//
+// Method: "fp4-train" (Method: block_absmax/6 scale in e4m3, division by the
+// decoded scale, e2m1 grid, stochastic rounding, error feedback) and "Add NVFP4
+// four-over-six (row-wise) quantization to the training prototype" (What;
+// CuTe DSL kernel (SM100), Design: the (b/6)*S_enc association, the 1.5x
+// map-to-4 scale, encode reciprocals, the 6*bound error denominator,
+// element-order error sums, the width-16 tree, strict err4 < err6).
+#pragma once
+
+#include "nvfp4_device.cuh"
+
+namespace nvfp4 {
+
+constexpr unsigned kFullMask = 0xFFFFFFFFu;
+
+// Global scale of one tensor or row.
+struct GScale {
+    float A, Senc, Sdec;
+};
+
+// Block scale s6f = (b / 6) * S_enc.  Without a global scale S_enc = 1 and the
+// product is the identity.
+template <bool GS>
+__device__ __forceinline__ float block_s6f(float b, float Senc) {
+    const float s = div6(b);
+    return GS ? mul_rn(s, Senc) : s;
+}
+
+// Width-16 tree over a half warp's 16 lanes, broadcast to all of them:
+// (((e0+e8)+(e4+e12))+((e2+e10)+(e6+e14))) + (((e1+e9)+(e5+e13))+((e3+e11)+(e7+e15))).
+// The xor butterfly forms exactly these pairs (commuted on some lanes).
+__device__ __forceinline__ float tree16_lanes(float E) {
+    E = add_rn(E, __shfl_xor_sync(kFullMask, E, 8));
+    E = add_rn(E, __shfl_xor_sync(kFullMask, E, 4));
+    E = add_rn(E, __shfl_xor_sync(kFullMask, E, 2));
+    E = add_rn(E, __shfl_xor_sync(kFullMask, E, 1));
+    return E;
+}
+
+// The same tree over 16 values held by one thread.
+__device__ __forceinline__ float tree16_regs(const float* e) {
+    return add_rn(add_rn(add_rn(add_rn(e[0], e[8]), add_rn(e[4], e[12])),
+                         add_rn(add_rn(e[2], e[10]), add_rn(e[6], e[14]))),
+                  add_rn(add_rn(add_rn(e[1], e[9]), add_rn(e[5], e[13])),
+                         add_rn(add_rn(e[3], e[11]), add_rn(e[7], e[15]))));
+}
+
+__device__ __forceinline__ float max16_lanes(float m) {
+    m = max_nd(m, __shfl_xor_sync(kFullMask, m, 8));
+    m = max_nd(m, __shfl_xor_sync(kFullMask, m, 4));
+    m = max_nd(m, __shfl_xor_sync(kFullMask, m, 2));
+    m = max_nd(m, __shfl_xor_sync(kFullMask, m, 1));
+    return m;
+}
+
+__device__ __forceinline__ float absmax16(const float* y) {
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = max_nd(m, fabsf(y[i]));
+    return m;
+}
+
+// ---- plain path ---------------------------------------------------------------------------
+// codes of y / D (D = decoded scale * S_dec), nearest or stochastic; a zero
+// divisor zeroes the block.  b is the block amax (bounds |y|).
+// The plain path's division y / D.  2^-20 <= D <= 2^20 and |y| <= b <= 2^60
+// keep quotients and remainders normal for |y| >= 2^-80, so the reciprocal
+// sequence is exact there; below that the quotient is under 2^-60 and its
+// nearest code is the signed zero either way, while stochastic rounding (EXACT)
+// takes the IEEE division.  Outside the range: IEEE division throughout.
+__device__ __forceinline__ bool plain_fast(float D, float b) {
+    return D >= 9.5367431640625e-07f && D <= 1048576.0f && b <= 1.152921504606847e+18f;
+}
+
+template <bool EXACT>
+__device__ __forceinline__ float plain_quotient(float y, float D, float r, bool fast) {
+    if (!fast) return div_rn(y, D);
+    float q = div_by_recip(y, D, r);
+    if (EXACT && fabsf(y) < 8.271806125530277e-25f) q = div_rn(y, D);
+    return (q == 0.0f) ? copysign_bits(q, y) : q;      // a zero keeps y's sign
+}
+
+// codes of y / D (D = decoded scale * S_dec), nearest or stochastic; a zero
+// divisor zeroes the block.  b is the block amax (bounds |y|).
+template <int RND>
+__device__ __forceinline__ void encode_plain16(const float* y, float D, float b, uint64_t idx0,
+                                               uint64_t seed, uint64_t step, uint32_t& w0,
+                                               uint32_t& w1) {
+    float v[16];
+    const bool fast = plain_fast(D, b);
+    const float r = fast ? div_rn(1.0f, D) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = plain_quotient<RND == NVFP4_SR>(y[i], D, r, fast);
+    if (RND == NVFP4_RTN) {
+        w0 = e2m1_encode8(v);
+        w1 = e2m1_encode8(v + 8);
+    } else {
+        uint32_t wd[16];
+        sr_words16(idx0, seed, step, wd);
+        w0 = 0;
+        w1 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            w0 |= e2m1_encode_sr(v[i], wd[i]) << (4 * i);
+            w1 |= e2m1_encode_sr(v[8 + i], wd[8 + i]) << (4 * i);
+        }
+    }
+    if (D == 0.0f) {
+        w0 = 0;
+        w1 = 0;
+    }
+}
+
+// ---- four-over-six --------------------------------------------------------------------------
+// codes of y * enc for one candidate
+__device__ __forceinline__ void encode_scaled16(const float* y, float enc, uint32_t& w0, uint32_t& w1) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = mul_rn(y[i], enc);
+    w0 = e2m1_encode8(v);
+    w1 = e2m1_encode8(v + 8);
+}
+
+// per-element errors |dq - y| (MAE) or (dq - y)^2 (MSE) of one candidate
+template <int ERR>
+__device__ __forceinline__ void candidate_errors16(const float* y, uint32_t w0, uint32_t w1,
+                                                   const Cand& c, float d, float A, float C,
+                                                   float* e) {
+    float dq[16];
+    if (c.fast) {
+        error_values8(w0, c.X1, c.X15, dq);
+        error_values8(w1, c.X1, c.X15, dq + 8);
+    } else {
+        float q[16];
+        e2m1_decode8(w0, q);
+        e2m1_decode8(w1, q + 8);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dq[i] = div_rn(mul_rn(mul_rn(q[i], d), A), C);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float diff = sub_rn(dq[i], y[i]);
+        e[i] = (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff);
+    }
+}
+
+// sequential sum e[0] + ... + e[15] from 0
+__device__ __forceinline__ float seq_sum16(const float* e) {
+    float E = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) E = add_rn(E, e[i]);
+    return E;
+}
+
+// Per-tensor candidate table: entry sf holds the candidate data of scale byte
+// sf (every block scale is a non-negative E4M3 byte <= 0x7E).
+__device__ __forceinline__ void fill_cand_table(Cand* tab, float Sdec, float A, float C) {
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) tab[i] = make_cand(static_cast<uint32_t>(i), Sdec, A, C);
+    __syncthreads();
+}
+
+// Four-over-six for one 16-value group (1x16 block, or one row of a 16x16 tile
+// when TREE: the row error sums are combined over the half warp).
+template <int ERR, bool TREE>
+__device__ __forceinline__ void four_over_six16(const float* y, float b, const GScale& g, float C,
+                                                const Cand* tab, uint32_t& w0, uint32_t& w1,
+                                                uint32_t& sf, float& d) {
+    const float s6f = block_s6f<true>(b, g.Senc);
+    const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
+    const uint32_t sf4 = e4m3_encode(min_nd(mul_rn(s6f, 1.5f), 448.0f));
+    const Cand c6 = tab ? tab[sf6] : make_cand(sf6, g.Sdec, g.A, C);
+    const Cand c4 = tab ? tab[sf4] : make_cand(sf4, g.Sdec, g.A, C);
+    const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
+    uint32_t a0, a1, b0, b1;
+    encode_scaled16(y, c6.enc, a0, a1);
+    encode_scaled16(y, c4.enc, b0, b1);
+    float e[16];
+    candidate_errors16<ERR>(y, a0, a1, c6, d6, g.A, C, e);
+    float E6 = seq_sum16(e);
+    candidate_errors16<ERR>(y, b0, b1, c4, d4, g.A, C, e);
+    float E4 = seq_sum16(e);
+    if (TREE) {
+        E6 = tree16_lanes(E6);
+        E4 = tree16_lanes(E4);
+    }
+    const bool pick4 = E4 < E6;                 // ties and NaN keep map-to-6
+    w0 = pick4 ? b0 : a0;
+    w1 = pick4 ? b1 : a1;
+    sf = pick4 ? sf4 : sf6;
+    d = pick4 ? d4 : d6;
+}
+
+// dequantized values (q * d) * S_dec of 16 codes
+template <bool GS>
+__device__ __forceinline__ void dequant16(uint32_t w0, uint32_t w1, float d, float Sdec, float* dq) {
+    float q[16];
+    e2m1_decode8(w0, q);
+    e2m1_decode8(w1, q + 8);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float v = mul_rn(q[i], d);
+        dq[i] = GS ? mul_rn(v, Sdec) : v;
+    }
+}
+
+}  // namespace nvfp4

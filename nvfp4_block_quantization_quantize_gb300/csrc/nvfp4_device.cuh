@@ -62,22 +62,25 @@ __device__ __forceinline__ uint32_t e2m1_encode8(const float* v) {
     return r;
 }
 
+// One code byte (two 4-bit codes) -> an f16 pair of grid values, low nibble in
+// the low half.  The byte is taken with an explicit cvt.u8.u32 of the shifted
+// word: decoding straight from a four-byte vector unpack of the word was
+// observed to read zeros for some byte positions.
+__device__ __forceinline__ uint32_t e2m1_decode_byte(uint32_t w, int byte) {
+    uint32_t h;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(h)
+        : "r"(w >> (8 * byte)));
+    return h;
+}
+
 // Eight 4-bit codes -> their exact signed grid values.
 __device__ __forceinline__ void e2m1_decode8(uint32_t w, float* q) {
-    uint32_t h0, h1, h2, h3;
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
-        : "r"(w));
-    const uint32_t h[4] = {h0, h1, h2, h3};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        q[2 * i] = __half2float(__ushort_as_half(static_cast<unsigned short>(h[i] & 0xFFFFu)));
-        q[2 * i + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(h[i] >> 16)));
+        const uint32_t h = e2m1_decode_byte(w, i);
+        q[2 * i] = __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+        q[2 * i + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
     }
 }
 
@@ -112,20 +115,50 @@ __device__ __forceinline__ void sr_words16(uint64_t idx0, uint64_t seed, uint64_
 }
 
 // Stochastic rounding of one value to a 4-bit code ("fp4-train", Method): with
-// G[k] <= |v| < G[k+1], pick k+1 when u < p, p = (|v| - G[k]) / (G[k+1] - G[k])
-// (exact: Sterbenz subtraction, power-of-two gap), u = (word >> 8) * 2^-24.
+// G[k] <= |v| < G[k+1], pick k+1 when u < p, p = (|v| - G[k]) / (G[k+1] - G[k]),
+// u = (word >> 8) * 2^-24.  The grid has spacing 0.5 on [0,2), 1 on [2,4) and
+// 2 on [4,6), so t = |v| / spacing is exact, floor(t) indexes the lower point
+// and p = t - floor(t) is exact (Sterbenz); u < p is compared as
+// (word >> 8) < p * 2^24, both sides exact.
 __device__ __forceinline__ uint32_t e2m1_encode_sr(float v, uint32_t word) {
-    if (v != v) return 7u;                              // NaN -> +6
     const float a = fabsf(v);
     const uint32_t sign = (__float_as_uint(v) >> 31) << 3;
-    if (a >= 6.0f) return sign | 7u;
-    const uint32_t k = (a >= 0.5f) + (a >= 1.0f) + (a >= 1.5f) + (a >= 2.0f) + (a >= 3.0f) +
-                       (a >= 4.0f);
-    const float lo = (k < 4) ? 0.5f * static_cast<float>(k) : static_cast<float>(k - 2);
-    const float inv_gap = (k < 4) ? 2.0f : ((k < 6) ? 1.0f : 0.5f);
-    const float p = mul_rn(sub_rn(a, lo), inv_gap);
-    const float u = mul_rn(static_cast<float>(word >> 8), 5.9604644775390625e-08f);  // 2^-24
-    return sign | (k + (u < p ? 1u : 0u));
+    if (!(a < 6.0f)) return (v != v) ? 7u : (sign | 7u);   // NaN -> +6; saturate
+    const float mul = (a < 2.0f) ? 2.0f : ((a < 4.0f) ? 1.0f : 0.5f);
+    const uint32_t off = (a < 2.0f) ? 0u : ((a < 4.0f) ? 2u : 4u);
+    const float t = mul_rn(a, mul);
+    const float fl = floorf(t);
+    const float p24 = mul_rn(sub_rn(t, fl), 16777216.0f);
+    const uint32_t up = (static_cast<float>(word >> 8) < p24) ? 1u : 0u;
+    return sign | (static_cast<uint32_t>(fl) + off + up);
+}
+
+// ---- exact division from a reciprocal ---------------------------------------------------
+// RN(a / b) given r = RN(1 / b): q0 = a*r, then two correction steps
+// q <- q + (a - b*q) * r with fused multiply-adds (P. Markstein, IBM J. R&D 34(1),
+// 1990; Muller et al., Handbook of Floating-Point Arithmetic, ch. 4).  The first
+// step makes q faithful, so the second remainder is exact and the second step
+// returns the correctly rounded quotient.  Valid while b, a / b and the
+// remainders stay normal (the callers' guards keep them so), with the sign of
+// a restored on a zero result.  Checked against IEEE
+// division exhaustively over the mantissas of every E4M3 divisor.
+__device__ __forceinline__ float div_by_recip(float a, float b, float r) {
+    float q = mul_rn(a, r);
+    float e = __fmaf_rn(-q, b, a);
+    q = __fmaf_rn(e, r, q);
+    e = __fmaf_rn(-q, b, a);
+    return __fmaf_rn(e, r, q);
+}
+
+__device__ __forceinline__ float copysign_bits(float mag, float s) {
+    return __uint_as_float((__float_as_uint(mag) & 0x7FFFFFFFu) | (__float_as_uint(s) & 0x80000000u));
+}
+
+// RN(b / 6) for a block amax b >= 0 (the fast path when b is in range).
+__device__ __forceinline__ float div6(float b) {
+    if (b >= 7.8886090522101181e-31f && b < 8.5070591730234616e+37f)   // [2^-100, 2^126)
+        return div_by_recip(b, 6.0f, 0.16666667163372040f);              // RN(1/6)
+    return div_rn(b, 6.0f);
 }
 
 // ---- global scales ("Add NVFP4 four-over-six ...", What) ------------------------------
@@ -135,6 +168,76 @@ __device__ __forceinline__ void global_scales(float A, float bound, float& enc, 
     if (!(A > 0.0f) || isinf(A)) enc = 1.0f;
     else enc = min_nd(div_rn(mul_rn(6.0f, bound), A), FLT_MAX);
     dec = div_rn(1.0f, enc);
+}
+
+// ---- four-over-six candidate data ----------------------------------------------------------
+// For one candidate scale byte sf (decoded d): the encode reciprocal
+// enc = min(1/(d*S_dec), FLT_MAX) and the error values of the grid points.
+// The error value of code q is ((q*d)*A)/C with C = 6*bound.  q*d is exact and
+// q = 2^e * m with m in {1, 1.5}, e in -1..2, so while RN(m*d*A) stays normal
+// far from the range ends, ((q*d)*A)/C = 2^e * X_m exactly, with
+// X_1 = RN(RN(d*A)/C) and X_1.5 = RN(RN(1.5*d*A)/C).  `fast` records whether
+// that holds (also for zero, infinite or NaN products, where the scaling is
+// exact as well); when it does not, the error value is computed literally.
+struct Cand {
+    float enc, X1, X15;
+    uint32_t fast;
+};
+
+__device__ __forceinline__ bool scalable(float Y) {
+    const float a = fabsf(Y);
+    return a == 0.0f || !(a < INFINITY) || (a >= 7.8886090522101181e-31f && a <= 1.2676506002282294e+30f);
+}
+
+__device__ __forceinline__ Cand make_cand(uint32_t sf, float Sdec, float A, float C) {
+    const float d = e4m3_decode(sf);
+    Cand c;
+    c.enc = min_nd(div_rn(1.0f, mul_rn(d, Sdec)), FLT_MAX);
+    const float Y1 = mul_rn(d, A);
+    const float Y15 = mul_rn(mul_rn(1.5f, d), A);
+    c.X1 = div_rn(Y1, C);
+    c.X15 = div_rn(Y15, C);
+    c.fast = (scalable(Y1) && scalable(Y15)) ? 1u : 0u;
+    return c;
+}
+
+// Error values for the 8 codes in word w (one code byte -> an f16 pair of grid
+// values): dq = p * (m == 1.5 ? X15 : X1), p = q with the 1.5 bit cleared.
+__device__ __forceinline__ void error_values8(uint32_t w, float X1, float X15, float* dq) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t h = e2m1_decode_byte(w, i);
+        const uint32_t pw = h & ~0x02000200u;             // clear the 1.5 bit of both halves
+        const float plo = __half2float(__ushort_as_half(static_cast<unsigned short>(pw & 0xFFFFu)));
+        const float phi = __half2float(__ushort_as_half(static_cast<unsigned short>(pw >> 16)));
+        dq[2 * i] = mul_rn(plo, (h & 0x00000200u) ? X15 : X1);
+        dq[2 * i + 1] = mul_rn(phi, (h & 0x02000000u) ? X15 : X1);
+    }
+}
+
+// ---- 16x16 nibble transpose -----------------------------------------------------------------
+// An 8x8 matrix of 4-bit codes, row r in w[r] (column c in nibble c), is
+// transposed in place by swapping 4x4, 2x2 and 1x1 blocks (masked xor swaps).
+__device__ __forceinline__ void transpose8x8_nibbles(uint32_t* w) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {               // 4x4 blocks: 16-bit fields
+        const uint32_t t = ((w[r] >> 16) ^ w[r + 4]) & 0x0000FFFFu;
+        w[r + 4] ^= t;
+        w[r] ^= t << 16;
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {               // 2x2 blocks: 8-bit fields
+        if (r & 2) continue;
+        const uint32_t t = ((w[r] >> 8) ^ w[r + 2]) & 0x00FF00FFu;
+        w[r + 2] ^= t;
+        w[r] ^= t << 8;
+    }
+#pragma unroll
+    for (int r = 0; r < 8; r += 2) {            // 1x1 blocks: 4-bit fields
+        const uint32_t t = ((w[r] >> 4) ^ w[r + 1]) & 0x0F0F0F0Fu;
+        w[r + 1] ^= t;
+        w[r] ^= t << 4;
+    }
 }
 
 // ---- loads and stores ----------------------------------------------------------------------

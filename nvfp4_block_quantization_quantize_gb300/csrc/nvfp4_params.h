@@ -42,6 +42,7 @@ int launch_quantize_tiles(const QuantArgs& a, void* stream);   // 16x16, or any 
 int launch_dequantize(const DequantArgs& a, void* stream);
 int launch_amax(const void* x, int64_t M, int64_t K, int dtype, const float* residual, int mode,
                 float* out, void* stream);
+int launch_probe_divide(const float* a, const float* b, float* out, int64_t n, void* stream);
 int sm_count();
 
 }  // namespace nvfp4

@@ -1,0 +1,299 @@
+// nvfp4_tiles.cu -- 16x16 blocks and columnwise outputs for sm_103a.
+//
+// k_tiles_rows  one CTA = a 16-row band x 256 columns; lane l of warp w holds
+//               row l%16 of the 16x16 tile 2w + l/16.  16x16 blocks reduce
+//               their amax (and, for four-over-six, their row error sums
+//               with the fixed width-16 tree) over the half warp.  With a
+//               columnwise output the tile is staged in shared memory and
+//               each thread then owns one column (x^T's row) of the band.
+// k_tile_t      four-over-six 16x16 with rowwise AND columnwise output: one
+//               thread owns a whole 16x16 tile and walks its rows three times
+//               (amax; both candidates' errors with the row sums AND the
+//               column sums accumulated in row order, so x^T's element-order
+//               sums are exact too; encode and store).  Row and column
+//               choices are made from the same per-element errors; the
+//               columnwise codes are transposed in registers.  Loads of a
+//               row by a warp cover 32 consecutive tiles: fully coalesced.
+//
+// Method: "Add NVFP4 four-over-six (row-wise) quantization to the training
+// prototype" (What: 16x16 blocks, rowwise / columnwise; CuTe DSL kernel
+// (SM100), Design: width-16 tree, element-order sums; Follow-up fusions: a
+// fused row + col kernel) and "Stable FP4 Training via Transposition-Invariant
+// Block Quantization" (abstract: one 2D block scale for x and x^T).
+#include "nvfp4_block.cuh"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTileCols = 256;
+constexpr int kYsStride = kTileCols + 4;
+
+template <int DT, int BLK, int ERR, int RND, bool EF, bool GS, bool COLW>
+__global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
+    __shared__ float ys[COLW ? 16 * kYsStride : 1];
+    __shared__ Cand tab[ERR != NVFP4_ERR_NONE ? 128 : 1];
+    const int64_t band = blockIdx.x;
+    const int64_t chunk = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = 2 * warp + (lane >> 4);
+    const int rr = lane & 15;
+    const int64_t nb = a.K / 16;
+    const int64_t cb = chunk * 16 + t;
+    const bool valid = cb < nb;
+    const int64_t row = band * 16 + rr;
+
+    GScale g{0.0f, 1.0f, 1.0f};
+    if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
+        g.A = a.gamax[0];
+        global_scales(g.A, a.bound, g.Senc, g.Sdec);
+    }
+    const float C = mul_rn(6.0f, a.bound);
+    if (ERR != NVFP4_ERR_NONE) fill_cand_table(tab, g.Sdec, g.A, C);
+    const Cand* tp = ERR != NVFP4_ERR_NONE ? tab : nullptr;
+
+    const int64_t e0 = row * a.K + cb * 16;
+    float y[16];
+    if (valid) {
+        load16<DT>(a.x, e0, y);
+        if (EF) {
+            float r[16];
+            load16_f32(a.residual, e0, r);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = 0.0f;
+    }
+    float b = absmax16(y);
+    if (BLK == NVFP4_BLOCK_16X16) b = max16_lanes(b);
+
+    // ---- rowwise ----
+    {
+        uint32_t w0, w1, sf;
+        float d;
+        constexpr bool TREE = BLK == NVFP4_BLOCK_16X16;
+        if (ERR == NVFP4_ERR_NONE) {
+            const float s6f = block_s6f<GS>(b, g.Senc);
+            sf = e4m3_encode(min_nd(s6f, 448.0f));
+            d = e4m3_decode(sf);
+            const float D = GS ? mul_rn(d, g.Sdec) : d;
+            const uint64_t idx0 = (static_cast<uint64_t>(a.row_offset) + static_cast<uint64_t>(row)) *
+                                      static_cast<uint64_t>(a.K) + static_cast<uint64_t>(cb * 16);
+            encode_plain16<RND>(y, D, b, idx0, a.seed, a.step, w0, w1);
+        } else {
+            four_over_six16<ERR, TREE>(y, b, g, C, tp, w0, w1, sf, d);
+        }
+        if (valid) {
+            if (a.codes) reinterpret_cast<uint2*>(a.codes)[e0 / 16] = make_uint2(w0, w1);
+            if (a.scales) a.scales[row * nb + cb] = static_cast<uint8_t>(sf);
+            if (EF || a.dq_bf16) {
+                float dq[16];
+                dequant16<GS || ERR != NVFP4_ERR_NONE>(w0, w1, d, g.Sdec, dq);
+                if (EF) {
+                    float r[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) r[i] = sub_rn(y[i], dq[i]);
+                    store16_f32(a.residual, e0, r);
+                }
+                if (a.dq_bf16) store16_bf16(a.dq_bf16, e0, dq);
+            }
+        }
+    }
+    if constexpr (COLW) {
+    // ---- columnwise: the rowwise quantization of x^T, from the staged band ----
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ys[rr * kYsStride + t * 16 + i] = y[i];
+    __syncthreads();
+    const int j = threadIdx.x;                  // column within the chunk (its tile is t)
+    const int64_t col = chunk * kTileCols + j;
+    float c[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) c[r] = ys[r * kYsStride + j];
+    float bc = absmax16(c);
+    if (BLK == NVFP4_BLOCK_16X16) bc = max16_lanes(bc);
+    uint32_t w0, w1, sf;
+    float d;
+    if (ERR == NVFP4_ERR_NONE) {
+        const float s6f = block_s6f<GS>(bc, g.Senc);
+        sf = e4m3_encode(min_nd(s6f, 448.0f));
+        d = e4m3_decode(sf);
+        const float D = GS ? mul_rn(d, g.Sdec) : d;
+        encode_plain16<NVFP4_RTN>(c, D, bc, 0, 0, 0, w0, w1);
+    } else {
+        four_over_six16<ERR, BLK == NVFP4_BLOCK_16X16>(c, bc, g, C, tp, w0, w1, sf, d);
+    }
+    if (col < a.K) {
+        reinterpret_cast<uint2*>(a.codes_col)[(col * a.M + band * 16) / 16] = make_uint2(w0, w1);
+        a.scales_col[col * (a.M / 16) + band] = static_cast<uint8_t>(sf);
+    }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+constexpr int kTileThreads = 128;
+
+template <int DT, int ERR>
+__global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
+    __shared__ Cand tab[128];
+    GScale g{0.0f, 1.0f, 1.0f};
+    if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
+        g.A = a.gamax[0];
+        global_scales(g.A, a.bound, g.Senc, g.Sdec);
+    }
+    const float C = mul_rn(6.0f, a.bound);
+    fill_cand_table(tab, g.Sdec, g.A, C);
+
+    const int64_t band = blockIdx.x;
+    const int64_t tile = static_cast<int64_t>(blockIdx.y) * kTileThreads + threadIdx.x;
+    const int64_t nb = a.K / 16;
+    if (tile >= nb) return;                     // no barrier follows
+    const int64_t K = a.K;
+    const int64_t base = band * 16 * K + tile * 16;
+
+    // pass 0: tile amax
+    float y[16];
+    float b = 0.0f;
+#pragma unroll 1
+    for (int r = 0; r < 16; ++r) {
+        load16<DT>(a.x, base + r * K, y);
+        b = max_nd(b, absmax16(y));
+    }
+    const float s6f = block_s6f<true>(b, g.Senc);
+    const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
+    const uint32_t sf4 = e4m3_encode(min_nd(mul_rn(s6f, 1.5f), 448.0f));
+    const Cand c6 = tab[sf6], c4 = tab[sf4];
+    const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
+
+    // pass 1: per-element errors; row sums (pairs r, r+8 for the tree) and
+    // column sums, both accumulated in element order
+    float F6[16], F4[16], P6[8], P4[8];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        load16<DT>(a.x, base + r * K, y);
+        float e[16];
+        uint32_t w0, w1;
+        encode_scaled16(y, c6.enc, w0, w1);
+        candidate_errors16<ERR>(y, w0, w1, c6, d6, g.A, C, e);
+        const float r6 = seq_sum16(e);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) F6[i] = add_rn(F6[i], e[i]);
+        encode_scaled16(y, c4.enc, w0, w1);
+        candidate_errors16<ERR>(y, w0, w1, c4, d4, g.A, C, e);
+        const float r4 = seq_sum16(e);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) F4[i] = add_rn(F4[i], e[i]);
+        if (r < 8) {
+            P6[r] = r6;
+            P4[r] = r4;
+        } else {
+            P6[r - 8] = add_rn(P6[r - 8], r6);
+            P4[r - 8] = add_rn(P4[r - 8], r4);
+        }
+    }
+    // (((e0+e8)+(e4+e12))+((e2+e10)+(e6+e14))) + (((e1+e9)+(e5+e13))+((e3+e11)+(e7+e15)))
+    const float E6r = add_rn(add_rn(add_rn(P6[0], P6[4]), add_rn(P6[2], P6[6])),
+                             add_rn(add_rn(P6[1], P6[5]), add_rn(P6[3], P6[7])));
+    const float E4r = add_rn(add_rn(add_rn(P4[0], P4[4]), add_rn(P4[2], P4[6])),
+                             add_rn(add_rn(P4[1], P4[5]), add_rn(P4[3], P4[7])));
+    const float E6c = tree16_regs(F6), E4c = tree16_regs(F4);
+    const bool row4 = E4r < E6r, col4 = E4c < E6c;       // ties and NaN keep map-to-6
+    const float enc_r = row4 ? c4.enc : c6.enc, enc_c = col4 ? c4.enc : c6.enc;
+    const uint8_t sf_r = static_cast<uint8_t>(row4 ? sf4 : sf6);
+    const uint8_t sf_c = static_cast<uint8_t>(col4 ? sf4 : sf6);
+
+    // pass 2: encode, store rowwise, collect columnwise codes
+    uint32_t lo[16], hi[16];
+    const int64_t nbr = K / 16;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        load16<DT>(a.x, base + r * K, y);
+        uint32_t w0, w1;
+        encode_scaled16(y, enc_r, w0, w1);
+        const int64_t rowg = band * 16 + r;
+        reinterpret_cast<uint2*>(a.codes)[(rowg * K + tile * 16) / 16] = make_uint2(w0, w1);
+        a.scales[rowg * nbr + tile] = sf_r;
+        if (col4 == row4) {
+            lo[r] = w0;
+            hi[r] = w1;
+        } else {
+            encode_scaled16(y, enc_c, lo[r], hi[r]);
+        }
+    }
+    transpose8x8_nibbles(lo);          // rows 0-7,  cols 0-7
+    transpose8x8_nibbles(lo + 8);      // rows 8-15, cols 0-7
+    transpose8x8_nibbles(hi);          // rows 0-7,  cols 8-15
+    transpose8x8_nibbles(hi + 8);      // rows 8-15, cols 8-15
+    const int64_t M = a.M;
+    uint2* cc = reinterpret_cast<uint2*>(a.codes_col);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const int64_t col0 = tile * 16 + c, col1 = tile * 16 + 8 + c;
+        cc[(col0 * M + band * 16) / 16] = make_uint2(lo[c], lo[8 + c]);
+        cc[(col1 * M + band * 16) / 16] = make_uint2(hi[c], hi[8 + c]);
+        a.scales_col[col0 * (M / 16) + band] = sf_c;
+        a.scales_col[col1 * (M / 16) + band] = sf_c;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+template <typename KernelT>
+int launch_rowowner(KernelT kernel, const QuantArgs& a, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(a.M / 16), static_cast<unsigned>((a.K / 16 + 15) / 16));
+    kernel<<<grid, kThreads, 0, s>>>(a);
+    return static_cast<int>(cudaGetLastError());
+}
+
+template <int DT, int BLK, bool COLW, bool GS>
+int plain_dispatch(const QuantArgs& a, cudaStream_t s) {
+    if (COLW) return launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN, false, GS, COLW>, a, s);
+    const bool ef = a.residual != nullptr;
+    if (a.rounding == NVFP4_RTN)
+        return ef ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN, true, GS, false>, a, s)
+                  : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN, false, GS, false>, a, s);
+    return ef ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, true, GS, false>, a, s)
+              : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, false, GS, false>, a, s);
+}
+
+template <int DT, int ERR>
+int launch_tile_t(const QuantArgs& a, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(a.M / 16),
+                    static_cast<unsigned>((a.K / 16 + kTileThreads - 1) / kTileThreads));
+    k_tile_t<DT, ERR><<<grid, kTileThreads, 0, s>>>(a);
+    return static_cast<int>(cudaGetLastError());
+}
+
+template <int DT, int BLK, bool COLW>
+int tiles_dispatch_blk(const QuantArgs& a, cudaStream_t s) {
+    if (a.err_mode != NVFP4_ERR_NONE) {
+        if (BLK == NVFP4_BLOCK_16X16 && COLW)
+            return a.err_mode == NVFP4_ERR_MAE ? launch_tile_t<DT, NVFP4_ERR_MAE>(a, s)
+                                               : launch_tile_t<DT, NVFP4_ERR_MSE>(a, s);
+        return a.err_mode == NVFP4_ERR_MAE
+                   ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_MAE, NVFP4_RTN, false, true, COLW>, a, s)
+                   : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_MSE, NVFP4_RTN, false, true, COLW>, a, s);
+    }
+    return a.gamax_mode == NVFP4_GAMAX_NONE ? plain_dispatch<DT, BLK, COLW, false>(a, s)
+                                            : plain_dispatch<DT, BLK, COLW, true>(a, s);
+}
+
+template <int DT>
+int tiles_dispatch(const QuantArgs& a, cudaStream_t s) {
+    const bool colw = a.codes_col != nullptr;
+    if (a.block == NVFP4_BLOCK_16X16)
+        return colw ? tiles_dispatch_blk<DT, NVFP4_BLOCK_16X16, true>(a, s)
+                    : tiles_dispatch_blk<DT, NVFP4_BLOCK_16X16, false>(a, s);
+    return tiles_dispatch_blk<DT, NVFP4_BLOCK_1X16, true>(a, s);
+}
+
+}  // namespace
+
+int launch_quantize_tiles(const QuantArgs& a, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return a.dtype == NVFP4_BF16 ? tiles_dispatch<NVFP4_BF16>(a, s) : tiles_dispatch<NVFP4_F32>(a, s);
+}
+
+}  // namespace nvfp4

@@ -87,3 +87,28 @@ def test_philox_all_counter_words(block):
         gpu, o = quantize_both(x, block=block, rounding="sr", seed=seed, step=step,
                                row_offset=row_offset)
         assert_same(gpu["codes"], o["codes"], f"sr codes seed={seed} step={step}")
+
+
+def test_exact_division_routine_exhaustive_mantissas():
+    """The plain path divides each element by the decoded scale with a
+    reciprocal-and-correction sequence; it must equal IEEE division.  Every fp32
+    mantissa of the dividend against every E4M3 divisor mantissa (x 3 divisor
+    exponents, 2 dividend exponents), plus divisor 6 (the b / 6 step), plus
+    random dividend / divisor pairs across the guarded range and beyond it."""
+    mant = (np.arange(1 << 23, dtype=np.uint32) | np.uint32(0x3F800000)).view(np.float32)
+    divisors = [np.float32((1 + k / 8) * 2.0 ** e) for k in range(8) for e in (-9, 0, 8)]
+    divisors += [np.float32(6.0)]
+    for dv in divisors:
+        for scale in (np.float32(1.0), np.float32(-2.0 ** -7)):
+            a = mant * scale
+            b = np.full(a.shape, dv, np.float32)
+            got = to_np(nv.nvfp4_probe_divide(to_dev(a), to_dev(b)))
+            assert_same(got, a / b, f"divisor {dv} scale {scale}")
+    rng = np.random.default_rng(17)
+    n = 4_000_000
+    a = (rng.standard_normal(n) * np.exp2(rng.uniform(-90, 70, n))).astype(np.float32)
+    b = np.exp2(rng.uniform(-30, 30, n)).astype(np.float32) * rng.uniform(1, 2, n).astype(np.float32)
+    a[:1000] = np.float32(0.0)
+    a[1000:2000] = np.float32(-0.0)
+    got = to_np(nv.nvfp4_probe_divide(to_dev(a), to_dev(b)))
+    assert_same(got, a / b, "random pairs")
