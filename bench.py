@@ -309,8 +309,13 @@ def run_gpu(args, rank, world, local_rank):
     barrier()
     clocks = clocks_sampler_stop(proc, fh, clk_path, local_rank)
     total_ms = start.elapsed_time(stop)
+    ran = [not args.only or args.only in name for name, _, _ in plan]
     per_call_ms = [statistics.mean(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(nsteps))
-                   for i in range(len(plan))]
+                   if ran[i] else 0.0 for i in range(len(plan))]
+    if args.only:
+        plan = [p if r else (p[0], 0, 0) for p, r in zip(plan, ran)]
+        bytes_step = sum(b for _, _, b in plan)
+        elems_step = sum(e for _, e, _ in plan)
     if dist is not None:
         tt = torch.tensor([total_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -378,7 +383,7 @@ def run_gpu(args, rank, world, local_rank):
                 "algorithmic_bytes_per_launch": int(nbytes), "ms_per_launch": round(per_call_ms[dom], 4)}
     calls = [{"call": n, "ms": round(ms, 4), "GB/s": round(b / (ms * 1e-3) / GB, 1),
               "frac_of_peak": round(b / (ms * 1e-3) / GB / peak, 3)}
-             for (n, _, b), ms in zip(plan, per_call_ms)]
+             for (n, _, b), ms in zip(plan, per_call_ms) if ms > 0]
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline()

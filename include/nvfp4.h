@@ -161,7 +161,8 @@ int nvfp4_amax(const void* x, int64_t M, int64_t K, int dtype, const float* resi
  * nvfp4_probe_divide -- diagnostic.  out[i] = a[i] / b[i] computed by the
  * device routine the plain quantizer uses for "every element is divided by the
  * decoded scale" [fp4-train, Method] (its stochastic-rounding form, which must
- * equal IEEE round-to-nearest division for every input).  Device pointers,
+ * equal IEEE round-to-nearest division for every input; a divisor that is an
+ * E4M3 value takes the shorter form used without a global scale).  Device pointers,
  * n >= 0 elements, 4-byte aligned; EINVAL on bad arguments.  It exists so the
  * routine can be checked exhaustively against IEEE division.
  */

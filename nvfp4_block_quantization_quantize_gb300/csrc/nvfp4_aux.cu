@@ -69,6 +69,28 @@ __global__ void __launch_bounds__(kThreads) k_amax_rows(const void* x, const flo
 }
 
 template <int ODT>
+__device__ __forceinline__ void dequant_block(const DequantArgs& a, int64_t blk, uint32_t w0, uint32_t w1,
+                                              uint32_t sf, float Sdec, bool per_row, int64_t bpr) {
+    float Sd = Sdec;
+    if (per_row) {
+        float se;
+        global_scales(a.gamax[blk / bpr], a.bound, se, Sd);
+    }
+    const float d = e4m3_decode(sf);
+    float q[16];
+    e2m1_decode8(w0, q);
+    e2m1_decode8(w1, q + 8);
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = mul_rn(mul_rn(q[i], d), Sd);
+    if (ODT == NVFP4_BF16) store16_bf16(static_cast<uint16_t*>(a.out), blk * 16, v);
+    else store16_f32(static_cast<float*>(a.out), blk * 16, v);
+}
+
+// Four blocks per thread per step, interleaved across the warp (lane l takes
+// blocks base + l, +32, +64, +96) so every load and store instruction covers
+// consecutive blocks; all four blocks' codes and scales are loaded first.
+template <int ODT>
 __global__ void __launch_bounds__(kThreads) k_dequant(const DequantArgs a) {
     const int64_t bpr = a.K / 16;
     const int64_t nblk = a.M * bpr;
@@ -76,37 +98,45 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DequantArgs a) {
     const bool per_tensor = a.gamax_mode == NVFP4_GAMAX_TENSOR || a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN;
     const bool per_row = a.gamax_mode == NVFP4_GAMAX_ROW || a.gamax_mode == NVFP4_GAMAX_ROW_GIVEN;
     if (per_tensor) global_scales(a.gamax[0], a.bound, Senc, Sdec);
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; blk < nblk;
-         blk += stride) {
-        const uint2 w = reinterpret_cast<const uint2*>(a.codes)[blk];
-        const float d = e4m3_decode(a.scales[blk]);
-        float Sd = Sdec;
-        if (per_row) {
-            float se;
-            global_scales(a.gamax[blk / bpr], a.bound, se, Sd);
-        }
-        float q[16];
-        e2m1_decode8(w.x, q);
-        e2m1_decode8(w.y, q + 8);
-        float v[16];
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const uint2* codes = reinterpret_cast<const uint2*>(a.codes);
+    for (int64_t base = warp * 128; base < nblk; base += nwarps * 128) {
+        uint2 w[4];
+        uint32_t sf[4];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = mul_rn(mul_rn(q[i], d), Sd);
-        if (ODT == NVFP4_BF16) store16_bf16(static_cast<uint16_t*>(a.out), blk * 16, v);
-        else store16_f32(static_cast<float*>(a.out), blk * 16, v);
+        for (int k = 0; k < 4; ++k) {
+            const int64_t blk = base + 32 * k + lane;
+            if (blk < nblk) {
+                w[k] = __ldg(codes + blk);
+                sf[k] = __ldg(a.scales + blk);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t blk = base + 32 * k + lane;
+            if (blk < nblk) dequant_block<ODT>(a, blk, w[k].x, w[k].y, sf[k], Sdec, per_row, bpr);
+        }
     }
 }
 
 // out[i] = the plain path's division a[i] / b[i] (its exact, stochastic-
-// rounding form), with the block amax taken as |a[i]|.
+// rounding form), with the block amax taken as |a[i]|; an E4M3-valued divisor
+// takes the one-step form the kernels use without a global scale.
 __global__ void __launch_bounds__(kThreads) k_probe_divide(const float* a, const float* b,
                                                            float* out, int64_t n) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
         const float y = a[i], D = b[i];
         const bool fast = plain_fast(D, fabsf(y));
-        const float r = fast ? div_rn(1.0f, D) : 0.0f;
-        out[i] = plain_quotient<true>(y, D, r, fast);
+        const uint32_t sf = e4m3_encode(D);
+        if (fast && D > 0.0f && D <= 448.0f && e4m3_decode(sf) == D) {
+            out[i] = plain_quotient<true, true>(y, D, div_rn(1.0f, D), fast);   // E4M3 divisor form
+        } else {
+            const float r = fast ? div_rn(1.0f, D) : 0.0f;
+            out[i] = plain_quotient<true>(y, D, r, fast);
+        }
     }
 }
 
@@ -173,7 +203,7 @@ int launch_dequantize(const DequantArgs& a, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t nblk = a.M * (a.K / 16);
     if (nblk == 0) return 0;
-    const int g = grid_for(nblk);
+    const int g = grid_for((nblk + 3) / 4);   // 4 blocks per thread
     if (a.out_dtype == NVFP4_BF16) k_dequant<NVFP4_BF16><<<g, kThreads, 0, s>>>(a);
     else k_dequant<NVFP4_F32><<<g, kThreads, 0, s>>>(a);
     return static_cast<int>(cudaGetLastError());

@@ -73,25 +73,42 @@ __device__ __forceinline__ bool plain_fast(float D, float b) {
     return D >= 9.5367431640625e-07f && D <= 1048576.0f && b <= 1.152921504606847e+18f;
 }
 
-template <bool EXACT>
+// E4: D is a decoded E4M3 scale (no global scale), so one correction step is
+// exact; otherwise D is arbitrary and two steps are taken.
+template <bool EXACT, bool E4 = false>
 __device__ __forceinline__ float plain_quotient(float y, float D, float r, bool fast) {
     if (!fast) return div_rn(y, D);
-    float q = div_by_recip(y, D, r);
+    float q = E4 ? div_by_recip1(y, D, r) : div_by_recip(y, D, r);
     if (EXACT && fabsf(y) < 8.271806125530277e-25f) q = div_rn(y, D);
     return (q == 0.0f) ? copysign_bits(q, y) : q;      // a zero keeps y's sign
 }
 
+// RN(1/d) for every non-negative E4M3 byte (entry 0 unused: a zero scale
+// zeroes the block), filled once per CTA.
+__device__ __forceinline__ void fill_recip_table(float* rt) {
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) rt[i] = div_rn(1.0f, e4m3_decode(static_cast<uint32_t>(i)));
+    __syncthreads();
+}
+
 // codes of y / D (D = decoded scale * S_dec), nearest or stochastic; a zero
-// divisor zeroes the block.  b is the block amax (bounds |y|).
+// divisor zeroes the block.  b is the block amax (bounds |y|).  rt: the
+// reciprocal table when D is a bare E4M3 scale sf (no global scale), else null.
 template <int RND>
 __device__ __forceinline__ void encode_plain16(const float* y, float D, float b, uint64_t idx0,
                                                uint64_t seed, uint64_t step, uint32_t& w0,
-                                               uint32_t& w1) {
+                                               uint32_t& w1, const float* rt = nullptr,
+                                               uint32_t sf = 0) {
     float v[16];
     const bool fast = plain_fast(D, b);
-    const float r = fast ? div_rn(1.0f, D) : 0.0f;
+    if (rt) {
+        const float r = rt[sf];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = plain_quotient<RND == NVFP4_SR>(y[i], D, r, fast);
+        for (int i = 0; i < 16; ++i) v[i] = plain_quotient<RND == NVFP4_SR, true>(y[i], D, r, fast);
+    } else {
+        const float r = fast ? div_rn(1.0f, D) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = plain_quotient<RND == NVFP4_SR>(y[i], D, r, fast);
+    }
     if (RND == NVFP4_RTN) {
         w0 = e2m1_encode8(v);
         w1 = e2m1_encode8(v + 8);

@@ -150,14 +150,25 @@ __device__ __forceinline__ float div_by_recip(float a, float b, float r) {
     return __fmaf_rn(e, r, q);
 }
 
+// RN(a / b) given r = RN(1 / b) with ONE correction step.  Exact when b's
+// significand is one of the eight E4M3 significands 1 + k/8 (checked
+// exhaustively over every fp32 significand of a, both quotient binades), under
+// the same range conditions as div_by_recip.
+__device__ __forceinline__ float div_by_recip1(float a, float b, float r) {
+    const float q = mul_rn(a, r);
+    const float e = __fmaf_rn(-q, b, a);
+    return __fmaf_rn(e, r, q);
+}
+
 __device__ __forceinline__ float copysign_bits(float mag, float s) {
     return __uint_as_float((__float_as_uint(mag) & 0x7FFFFFFFu) | (__float_as_uint(s) & 0x80000000u));
 }
 
-// RN(b / 6) for a block amax b >= 0 (the fast path when b is in range).
+// RN(b / 6) for a block amax b >= 0 (6 = 1.5 * 4 has an E4M3 significand, so
+// one correction step is exact while b is in range).
 __device__ __forceinline__ float div6(float b) {
     if (b >= 7.8886090522101181e-31f && b < 8.5070591730234616e+37f)   // [2^-100, 2^126)
-        return div_by_recip(b, 6.0f, 0.16666667163372040f);              // RN(1/6)
+        return div_by_recip1(b, 6.0f, 0.16666667163372040f);             // RN(1/6)
     return div_rn(b, 6.0f);
 }
 
@@ -240,6 +251,22 @@ __device__ __forceinline__ void transpose8x8_nibbles(uint32_t* w) {
     }
 }
 
+// ---- asynchronous global -> shared copies (per thread) --------------------------------------
+// Each thread copies its own 16-byte pieces and waits only for its own groups
+// (cp.async.wait_group), so a per-thread multi-stage pipeline needs neither a
+// barrier nor a spin-wait.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---- loads and stores ----------------------------------------------------------------------
 template <int DT>
 __device__ __forceinline__ void load16(const void* base, int64_t elem0, float* y) {
@@ -257,6 +284,29 @@ __device__ __forceinline__ void load16(const void* base, int64_t elem0, float* y
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float4 f = __ldg(p + i);
+            y[4 * i] = f.x;
+            y[4 * i + 1] = f.y;
+            y[4 * i + 2] = f.z;
+            y[4 * i + 3] = f.w;
+        }
+    }
+}
+
+// 16 elements from shared memory (the layout load16 reads from global memory)
+template <int DT>
+__device__ __forceinline__ void lds16(const void* p, float* y) {
+    if (DT == NVFP4_BF16) {
+        const uint4 a = reinterpret_cast<const uint4*>(p)[0], b = reinterpret_cast<const uint4*>(p)[1];
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            y[2 * i] = __uint_as_float(w[i] << 16);
+            y[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 f = reinterpret_cast<const float4*>(p)[i];
             y[4 * i] = f.x;
             y[4 * i + 1] = f.y;
             y[4 * i + 2] = f.z;

@@ -2,9 +2,10 @@
 //
 // K % 16 == 0, so the 1x16 blocks of a row-major [M,K] tensor are simply the
 // consecutive 16-element groups of the flat array: the kernel streams them.
-// Each thread owns one block per step, two steps per loop iteration (both
-// blocks' loads are issued before either is computed, doubling the bytes in
-// flight); one persistent wave of CTAs covers the tensor.  Per block:
+// Each thread owns one block per grid-stride step and keeps the next three
+// steps' bytes in flight with its own asynchronous global->shared copies (a
+// per-thread four-stage pipeline: no registers held, no barrier); one
+// persistent wave of CTAs covers the tensor.  Per block:
 // absmax -> (b/6)*S_enc -> E4M3 scale, then either the plain encode (division
 // by the decoded scale through an exact reciprocal-and-correction sequence,
 // nearest or Philox stochastic rounding) or four-over-six (two candidates,
@@ -21,7 +22,7 @@ constexpr int kThreads = 256;
 template <int DT, int ERR, int RND, bool EF, bool GS>
 __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, float* y,
                                            const GScale& g, float C, const Cand* tab,
-                                           uint64_t idx_base, int64_t bpr) {
+                                           const float* rt, uint64_t idx_base, int64_t bpr) {
     GScale gb = g;
     if (a.gamax_mode == NVFP4_GAMAX_ROW_GIVEN) {
         gb.A = a.gamax[blk / bpr];
@@ -36,7 +37,7 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, floa
         d = e4m3_decode(sf);
         const float D = GS ? mul_rn(d, gb.Sdec) : d;
         encode_plain16<RND>(y, D, b, idx_base + static_cast<uint64_t>(blk) * 16u, a.seed, a.step,
-                            w0, w1);
+                            w0, w1, GS ? nullptr : rt, sf);
     } else {
         four_over_six16<ERR, false>(y, b, gb, C, tab, w0, w1, sf, d);
     }
@@ -55,20 +56,26 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, floa
     }
 }
 
+// Per-thread copy pipeline: stage s holds, for each thread, its block's x
+// bytes (and residual bytes under error feedback) for one grid-stride step.
+// With a residual a block moves 96-128 bytes, so one step ahead at a higher
+// occupancy keeps enough in flight; without, three steps ahead (the stage count is per variant).
 template <int DT, bool EF>
-__device__ __forceinline__ void rows_load(const QuantArgs& a, int64_t blk, float* y) {
-    load16<DT>(a.x, blk * 16, y);
-    if (EF) {
-        float r[16];
-        load16_f32(a.residual, blk * 16, r);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
-    }
-}
+struct RowsStage {
+    static constexpr int STAGES = EF ? 2 : 4;
+    static constexpr int XB = DT == NVFP4_BF16 ? 32 : 64;   // x bytes per block
+    static constexpr int RB = EF ? 64 : 0;                    // residual bytes per block
+    static constexpr int BYTES = kThreads * (XB + RB);
+    static constexpr int TOTAL = STAGES * BYTES;
+};
 
 template <int DT, int ERR, int RND, bool EF, bool GS>
 __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
+    using St = RowsStage<DT, EF>;
+    extern __shared__ __align__(16) unsigned char smem[];
     __shared__ Cand tab[ERR != NVFP4_ERR_NONE ? 128 : 1];
+    __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
+    if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
     const int64_t bpr = a.K / 16;
     const int64_t nblk = a.M * bpr;
     GScale g{0.0f, 1.0f, 1.0f};
@@ -83,28 +90,65 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
         tp = tab;
     }
     const uint64_t idx_base = static_cast<uint64_t>(a.row_offset) * static_cast<uint64_t>(a.K);
+    const int tid = threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; blk < nblk;
-         blk += 2 * stride) {
-        const int64_t blk2 = blk + stride;
-        float y[16], y2[16];
-        rows_load<DT, EF>(a, blk, y);
-        if (blk2 < nblk) rows_load<DT, EF>(a, blk2, y2);
-        rows_block<DT, ERR, RND, EF, GS>(a, blk, y, g, C, tp, idx_base, bpr);
-        if (blk2 < nblk) rows_block<DT, ERR, RND, EF, GS>(a, blk2, y2, g, C, tp, idx_base, bpr);
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
+    unsigned char* xs = smem + tid * St::XB;
+    unsigned char* rs = smem + kThreads * St::XB + tid * St::RB;
+
+    auto issue = [&](int64_t blk, int stage) {
+        if (blk < nblk) {
+            const unsigned char* gx = static_cast<const unsigned char*>(a.x) + blk * St::XB;
+#pragma unroll
+            for (int c = 0; c < St::XB / 16; ++c) cp_async16(xs + stage * St::BYTES + 16 * c, gx + 16 * c);
+            if (EF) {
+                const unsigned char* gr = reinterpret_cast<const unsigned char*>(a.residual) + blk * 64;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) cp_async16(rs + stage * St::BYTES + 16 * c, gr + 16 * c);
+            }
+        }
+        cp_async_commit();
+    };
+
+    constexpr int S = St::STAGES;
+#pragma unroll
+    for (int k = 0; k < S - 1; ++k) issue(first + k * stride, k);
+    int stage = 0;
+    for (int64_t blk = first; blk < nblk; blk += stride) {
+        issue(blk + (S - 1) * stride, stage == 0 ? S - 1 : stage - 1);
+        cp_async_wait<S - 1>();
+        float y[16];
+        lds16<DT>(xs + stage * St::BYTES, y);
+        if (EF) {
+            float r[16];
+            lds16<NVFP4_F32>(rs + stage * St::BYTES, r);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
+        }
+        rows_block<DT, ERR, RND, EF, GS>(a, blk, y, g, C, tp, rtab, idx_base, bpr);
+        stage = stage == S - 1 ? 0 : stage + 1;
     }
+    cp_async_wait<0>();
 }
 
-template <typename KernelT>
-int launch_wave(KernelT kernel, const QuantArgs& a, int64_t nblk, cudaStream_t s) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
-        per_sm < 1)
-        per_sm = 1;
-    const int64_t want = (nblk + 2 * kThreads - 1) / (2 * kThreads);
+template <int DT, int ERR, int RND, bool EF, bool GS>
+int launch_rows(const QuantArgs& a, int64_t nblk, cudaStream_t s) {
+    auto kernel = k_rows<DT, ERR, RND, EF, GS>;
+    constexpr int smem = RowsStage<DT, EF>::TOTAL;
+    static thread_local int configured_dev = -1, per_sm = 1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_dev != dev) {
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        configured_dev = dev;
+    }
+    const int64_t want = (nblk + kThreads - 1) / kThreads;
     const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
     const int grid = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
-    kernel<<<grid, kThreads, 0, s>>>(a);
+    kernel<<<grid, kThreads, smem, s>>>(a);
     return static_cast<int>(cudaGetLastError());
 }
 
@@ -112,19 +156,17 @@ template <int DT, bool GS>
 int rows_plain(const QuantArgs& a, int64_t nblk, cudaStream_t s) {
     const bool ef = a.residual != nullptr;
     if (a.rounding == NVFP4_RTN)
-        return ef ? launch_wave(k_rows<DT, NVFP4_ERR_NONE, NVFP4_RTN, true, GS>, a, nblk, s)
-                  : launch_wave(k_rows<DT, NVFP4_ERR_NONE, NVFP4_RTN, false, GS>, a, nblk, s);
-    return ef ? launch_wave(k_rows<DT, NVFP4_ERR_NONE, NVFP4_SR, true, GS>, a, nblk, s)
-              : launch_wave(k_rows<DT, NVFP4_ERR_NONE, NVFP4_SR, false, GS>, a, nblk, s);
+        return ef ? launch_rows<DT, NVFP4_ERR_NONE, NVFP4_RTN, true, GS>(a, nblk, s)
+                  : launch_rows<DT, NVFP4_ERR_NONE, NVFP4_RTN, false, GS>(a, nblk, s);
+    return ef ? launch_rows<DT, NVFP4_ERR_NONE, NVFP4_SR, true, GS>(a, nblk, s)
+              : launch_rows<DT, NVFP4_ERR_NONE, NVFP4_SR, false, GS>(a, nblk, s);
 }
 
 template <int DT>
 int rows_dispatch(const QuantArgs& a, cudaStream_t s) {
     const int64_t nblk = a.M * (a.K / 16);
-    if (a.err_mode == NVFP4_ERR_MAE)
-        return launch_wave(k_rows<DT, NVFP4_ERR_MAE, NVFP4_RTN, false, true>, a, nblk, s);
-    if (a.err_mode == NVFP4_ERR_MSE)
-        return launch_wave(k_rows<DT, NVFP4_ERR_MSE, NVFP4_RTN, false, true>, a, nblk, s);
+    if (a.err_mode == NVFP4_ERR_MAE) return launch_rows<DT, NVFP4_ERR_MAE, NVFP4_RTN, false, true>(a, nblk, s);
+    if (a.err_mode == NVFP4_ERR_MSE) return launch_rows<DT, NVFP4_ERR_MSE, NVFP4_RTN, false, true>(a, nblk, s);
     return a.gamax_mode == NVFP4_GAMAX_NONE ? rows_plain<DT, false>(a, nblk, s)
                                             : rows_plain<DT, true>(a, nblk, s);
 }

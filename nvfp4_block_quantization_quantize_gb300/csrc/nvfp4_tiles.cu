@@ -7,13 +7,19 @@
 //               columnwise output the tile is staged in shared memory and
 //               each thread then owns one column (x^T's row) of the band.
 // k_tile_t      four-over-six 16x16 with rowwise AND columnwise output: one
-//               thread owns a whole 16x16 tile and walks its rows three times
-//               (amax; both candidates' errors with the row sums AND the
-//               column sums accumulated in row order, so x^T's element-order
-//               sums are exact too; encode and store).  Row and column
+//               thread owns a whole 16x16 tile and walks its rows twice
+//               (amax; both candidates' codes and errors with the row sums
+//               AND the column sums accumulated in row order, so x^T's
+//               element-order sums are exact too; then store).  Row and column
 //               choices are made from the same per-element errors; the
 //               columnwise codes are transposed in registers.  Loads of a
 //               row by a warp cover 32 consecutive tiles: fully coalesced.
+//               The row loops stay rolled (an unrolled kernel overflowed the
+//               instruction cache); row sums and code words wait in shared
+//               memory until the tile's choices are known (both
+//               candidates' code words too, so x is read only twice); each
+//               thread streams its 32 row reads through a 4-slot ring of
+//               asynchronous copies, three reads ahead.
 //
 // Method: "Add NVFP4 four-over-six (row-wise) quantization to the training
 // prototype" (What: 16x16 blocks, rowwise / columnwise; CuTe DSL kernel
@@ -33,6 +39,8 @@ template <int DT, int BLK, int ERR, int RND, bool EF, bool GS, bool COLW>
 __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
     __shared__ float ys[COLW ? 16 * kYsStride : 1];
     __shared__ Cand tab[ERR != NVFP4_ERR_NONE ? 128 : 1];
+    __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
+    if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
     const int64_t band = blockIdx.x;
     const int64_t chunk = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -81,7 +89,7 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
             const float D = GS ? mul_rn(d, g.Sdec) : d;
             const uint64_t idx0 = (static_cast<uint64_t>(a.row_offset) + static_cast<uint64_t>(row)) *
                                       static_cast<uint64_t>(a.K) + static_cast<uint64_t>(cb * 16);
-            encode_plain16<RND>(y, D, b, idx0, a.seed, a.step, w0, w1);
+            encode_plain16<RND>(y, D, b, idx0, a.seed, a.step, w0, w1, GS ? nullptr : rtab, sf);
         } else {
             four_over_six16<ERR, TREE>(y, b, g, C, tp, w0, w1, sf, d);
         }
@@ -120,7 +128,7 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
         sf = e4m3_encode(min_nd(s6f, 448.0f));
         d = e4m3_decode(sf);
         const float D = GS ? mul_rn(d, g.Sdec) : d;
-        encode_plain16<NVFP4_RTN>(c, D, bc, 0, 0, 0, w0, w1);
+        encode_plain16<NVFP4_RTN>(c, D, bc, 0, 0, 0, w0, w1, GS ? nullptr : rtab, sf);
     } else {
         four_over_six16<ERR, BLK == NVFP4_BLOCK_16X16>(c, bc, g, C, tp, w0, w1, sf, d);
     }
@@ -134,9 +142,26 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
 // ---------------------------------------------------------------------------------------------
 constexpr int kTileThreads = 128;
 
+constexpr int kRing = 4;                        // tile rows in flight per thread
+
+template <int DT>
+struct TileRing {
+    static constexpr int XB = DT == NVFP4_BF16 ? 32 : 64;    // bytes of one tile row
+    static constexpr int BYTES = kRing * kTileThreads * XB;
+};
+
 template <int DT, int ERR>
 __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
+    using Rg = TileRing<DT>;
     __shared__ Cand tab[128];
+    // per-thread row sums of both candidates and the 16 rows' code words,
+    // [row][thread] so a warp's accesses are conflict-free
+    __shared__ float sR6[16][kTileThreads], sR4[16][kTileThreads];
+    // both candidates' code words of every row (map-to-6: [0..1], map-to-4: [2..3])
+    __shared__ uint32_t sW[4][16][kTileThreads];
+    // ring of tile rows: the thread streams its tile's rows twice (32 row
+    // reads) through kRing slots of asynchronous copies
+    __shared__ __align__(16) unsigned char ring[Rg::BYTES];
     GScale g{0.0f, 1.0f, 1.0f};
     if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
         g.A = a.gamax[0];
@@ -146,18 +171,40 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
     fill_cand_table(tab, g.Sdec, g.A, C);
 
     const int64_t band = blockIdx.x;
-    const int64_t tile = static_cast<int64_t>(blockIdx.y) * kTileThreads + threadIdx.x;
+    const int tid = threadIdx.x;
+    const int64_t tile = static_cast<int64_t>(blockIdx.y) * kTileThreads + tid;
     const int64_t nb = a.K / 16;
     if (tile >= nb) return;                     // no barrier follows
     const int64_t K = a.K;
     const int64_t base = band * 16 * K + tile * 16;
+    const unsigned char* gx = static_cast<const unsigned char*>(a.x) + base * (Rg::XB / 16);
+    const int64_t row_bytes = K * (Rg::XB / 16);
+    unsigned char* slot0 = ring + tid * Rg::XB;
+
+    // row read j (0..31) is tile row j % 16, into slot j % kRing
+    auto issue = [&](int j) {
+        if (j < 32) {
+            const unsigned char* src = gx + static_cast<int64_t>(j & 15) * row_bytes;
+            unsigned char* dst = slot0 + (j % kRing) * (kTileThreads * Rg::XB);
+#pragma unroll
+            for (int c = 0; c < Rg::XB / 16; ++c) cp_async16(dst + 16 * c, src + 16 * c);
+        }
+        cp_async_commit();
+    };
+    auto next_row = [&](int j, float* y) {       // row read j, ready in y
+        issue(j + kRing - 1);
+        cp_async_wait<kRing - 1>();
+        lds16<DT>(slot0 + (j % kRing) * (kTileThreads * Rg::XB), y);
+    };
+#pragma unroll
+    for (int j = 0; j < kRing - 1; ++j) issue(j);
 
     // pass 0: tile amax
     float y[16];
     float b = 0.0f;
 #pragma unroll 1
     for (int r = 0; r < 16; ++r) {
-        load16<DT>(a.x, base + r * K, y);
+        next_row(r, y);
         b = max_nd(b, absmax16(y));
     }
     const float s6f = block_s6f<true>(b, g.Senc);
@@ -166,62 +213,59 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
     const Cand c6 = tab[sf6], c4 = tab[sf4];
     const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
 
-    // pass 1: per-element errors; row sums (pairs r, r+8 for the tree) and
-    // column sums, both accumulated in element order
-    float F6[16], F4[16], P6[8], P4[8];
+    // pass 1: per-element errors; row sums to shared memory, column sums in
+    // registers, both accumulated in element order
+    float F6[16], F4[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
-#pragma unroll
+#pragma unroll 1
     for (int r = 0; r < 16; ++r) {
-        load16<DT>(a.x, base + r * K, y);
+        next_row(16 + r, y);
         float e[16];
         uint32_t w0, w1;
         encode_scaled16(y, c6.enc, w0, w1);
+        sW[0][r][tid] = w0;
+        sW[1][r][tid] = w1;
         candidate_errors16<ERR>(y, w0, w1, c6, d6, g.A, C, e);
-        const float r6 = seq_sum16(e);
+        sR6[r][tid] = seq_sum16(e);
 #pragma unroll
         for (int i = 0; i < 16; ++i) F6[i] = add_rn(F6[i], e[i]);
         encode_scaled16(y, c4.enc, w0, w1);
+        sW[2][r][tid] = w0;
+        sW[3][r][tid] = w1;
         candidate_errors16<ERR>(y, w0, w1, c4, d4, g.A, C, e);
-        const float r4 = seq_sum16(e);
+        sR4[r][tid] = seq_sum16(e);
 #pragma unroll
         for (int i = 0; i < 16; ++i) F4[i] = add_rn(F4[i], e[i]);
-        if (r < 8) {
-            P6[r] = r6;
-            P4[r] = r4;
-        } else {
-            P6[r - 8] = add_rn(P6[r - 8], r6);
-            P4[r - 8] = add_rn(P4[r - 8], r4);
-        }
     }
-    // (((e0+e8)+(e4+e12))+((e2+e10)+(e6+e14))) + (((e1+e9)+(e5+e13))+((e3+e11)+(e7+e15)))
-    const float E6r = add_rn(add_rn(add_rn(P6[0], P6[4]), add_rn(P6[2], P6[6])),
-                             add_rn(add_rn(P6[1], P6[5]), add_rn(P6[3], P6[7])));
-    const float E4r = add_rn(add_rn(add_rn(P4[0], P4[4]), add_rn(P4[2], P4[6])),
-                             add_rn(add_rn(P4[1], P4[5]), add_rn(P4[3], P4[7])));
+    cp_async_wait<0>();
+    float R[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) R[r] = sR6[r][tid];
+    const float E6r = tree16_regs(R);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) R[r] = sR4[r][tid];
+    const float E4r = tree16_regs(R);
     const float E6c = tree16_regs(F6), E4c = tree16_regs(F4);
     const bool row4 = E4r < E6r, col4 = E4c < E6c;       // ties and NaN keep map-to-6
-    const float enc_r = row4 ? c4.enc : c6.enc, enc_c = col4 ? c4.enc : c6.enc;
     const uint8_t sf_r = static_cast<uint8_t>(row4 ? sf4 : sf6);
     const uint8_t sf_c = static_cast<uint8_t>(col4 ? sf4 : sf6);
 
-    // pass 2: encode, store rowwise, collect columnwise codes
-    uint32_t lo[16], hi[16];
+    // store the rowwise codes of the chosen candidate; gather the columnwise one's
     const int64_t nbr = K / 16;
+    const int wr = row4 ? 2 : 0, wc = col4 ? 2 : 0;
+#pragma unroll 1
+    for (int r = 0; r < 16; ++r) {
+        const int64_t rowg = band * 16 + r;
+        reinterpret_cast<uint2*>(a.codes)[(rowg * K + tile * 16) / 16] =
+            make_uint2(sW[wr][r][tid], sW[wr + 1][r][tid]);
+        a.scales[rowg * nbr + tile] = sf_r;
+    }
+    uint32_t lo[16], hi[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-        load16<DT>(a.x, base + r * K, y);
-        uint32_t w0, w1;
-        encode_scaled16(y, enc_r, w0, w1);
-        const int64_t rowg = band * 16 + r;
-        reinterpret_cast<uint2*>(a.codes)[(rowg * K + tile * 16) / 16] = make_uint2(w0, w1);
-        a.scales[rowg * nbr + tile] = sf_r;
-        if (col4 == row4) {
-            lo[r] = w0;
-            hi[r] = w1;
-        } else {
-            encode_scaled16(y, enc_c, lo[r], hi[r]);
-        }
+        lo[r] = sW[wc][r][tid];
+        hi[r] = sW[wc + 1][r][tid];
     }
     transpose8x8_nibbles(lo);          // rows 0-7,  cols 0-7
     transpose8x8_nibbles(lo + 8);      // rows 8-15, cols 0-7

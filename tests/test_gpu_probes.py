@@ -96,7 +96,7 @@ def test_exact_division_routine_exhaustive_mantissas():
     exponents, 2 dividend exponents), plus divisor 6 (the b / 6 step), plus
     random dividend / divisor pairs across the guarded range and beyond it."""
     mant = (np.arange(1 << 23, dtype=np.uint32) | np.uint32(0x3F800000)).view(np.float32)
-    divisors = [np.float32((1 + k / 8) * 2.0 ** e) for k in range(8) for e in (-9, 0, 8)]
+    divisors = [np.float32((1 + k / 8) * 2.0 ** e) for k in range(8) for e in (-9, -6, 0, 8)]
     divisors += [np.float32(6.0)]
     for dv in divisors:
         for scale in (np.float32(1.0), np.float32(-2.0 ** -7)):
