@@ -130,7 +130,7 @@ __device__ __forceinline__ void encode_plain16(const float* y, float D, float b,
 }
 
 // ---- four-over-six --------------------------------------------------------------------------
-// codes of y * enc for one candidate
+// codes of y * enc for one candidate (codes only)
 __device__ __forceinline__ void encode_scaled16(const float* y, float enc, uint32_t& w0, uint32_t& w1) {
     float v[16];
 #pragma unroll
@@ -139,21 +139,29 @@ __device__ __forceinline__ void encode_scaled16(const float* y, float enc, uint3
     w1 = e2m1_encode8(v + 8);
 }
 
-// per-element errors |dq - y| (MAE) or (dq - y)^2 (MSE) of one candidate
+// One candidate over 16 values: codes of y * enc, and the per-element errors
+// |dq - y| (MAE) or (dq - y)^2 (MSE) of its error values dq = ((q*d)*A)/C.
 template <int ERR>
-__device__ __forceinline__ void candidate_errors16(const float* y, uint32_t w0, uint32_t w1,
-                                                   const Cand& c, float d, float A, float C,
-                                                   float* e) {
+__device__ __forceinline__ void candidate16(const float* y, const Cand& c, float d, float A, float C,
+                                            uint32_t& w0, uint32_t& w1, float* e) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = mul_rn(y[i], c.enc);
+    uint32_t h[8];
+    w0 = e2m1_encode8_dec(v, h);
+    w1 = e2m1_encode8_dec(v + 8, h + 4);
     float dq[16];
     if (c.fast) {
-        error_values8(w0, c.X1, c.X15, dq);
-        error_values8(w1, c.X1, c.X15, dq + 8);
+        error_values8(h, c.X1, c.DX, dq);
+        error_values8(h + 4, c.X1, c.DX, dq + 8);
     } else {
-        float q[16];
-        e2m1_decode8(w0, q);
-        e2m1_decode8(w1, q + 8);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) dq[i] = div_rn(mul_rn(mul_rn(q[i], d), A), C);
+        for (int i = 0; i < 8; ++i) {
+            const float qlo = __half2float(__ushort_as_half(static_cast<unsigned short>(h[i] & 0xFFFFu)));
+            const float qhi = __half2float(__ushort_as_half(static_cast<unsigned short>(h[i] >> 16)));
+            dq[2 * i] = div_rn(mul_rn(mul_rn(qlo, d), A), C);
+            dq[2 * i + 1] = div_rn(mul_rn(mul_rn(qhi, d), A), C);
+        }
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -190,12 +198,10 @@ __device__ __forceinline__ void four_over_six16(const float* y, float b, const G
     const Cand c4 = tab ? tab[sf4] : make_cand(sf4, g.Sdec, g.A, C);
     const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
     uint32_t a0, a1, b0, b1;
-    encode_scaled16(y, c6.enc, a0, a1);
-    encode_scaled16(y, c4.enc, b0, b1);
     float e[16];
-    candidate_errors16<ERR>(y, a0, a1, c6, d6, g.A, C, e);
+    candidate16<ERR>(y, c6, d6, g.A, C, a0, a1, e);
     float E6 = seq_sum16(e);
-    candidate_errors16<ERR>(y, b0, b1, c4, d4, g.A, C, e);
+    candidate16<ERR>(y, c4, d4, g.A, C, b0, b1, e);
     float E4 = seq_sum16(e);
     if (TREE) {
         E6 = tree16_lanes(E6);

@@ -191,13 +191,13 @@ __device__ __forceinline__ void global_scales(float A, float bound, float& enc, 
 // that holds (also for zero, infinite or NaN products, where the scaling is
 // exact as well); when it does not, the error value is computed literally.
 struct Cand {
-    float enc, X1, X15;
+    float enc, X1, DX;      // DX = X_1.5 - X_1, exact (Sterbenz: X_1.5 ~ 1.5 X_1)
     uint32_t fast;
 };
 
 __device__ __forceinline__ bool scalable(float Y) {
     const float a = fabsf(Y);
-    return a == 0.0f || !(a < INFINITY) || (a >= 7.8886090522101181e-31f && a <= 1.2676506002282294e+30f);
+    return a == 0.0f || (a >= 7.8886090522101181e-31f && a <= 1.2676506002282294e+30f);
 }
 
 __device__ __forceinline__ Cand make_cand(uint32_t sf, float Sdec, float A, float C) {
@@ -207,22 +207,47 @@ __device__ __forceinline__ Cand make_cand(uint32_t sf, float Sdec, float A, floa
     const float Y1 = mul_rn(d, A);
     const float Y15 = mul_rn(mul_rn(1.5f, d), A);
     c.X1 = div_rn(Y1, C);
-    c.X15 = div_rn(Y15, C);
+    c.DX = sub_rn(div_rn(Y15, C), c.X1);
     c.fast = (scalable(Y1) && scalable(Y15)) ? 1u : 0u;
     return c;
 }
 
-// Error values for the 8 codes in word w (one code byte -> an f16 pair of grid
-// values): dq = p * (m == 1.5 ? X15 : X1), p = q with the 1.5 bit cleared.
-__device__ __forceinline__ void error_values8(uint32_t w, float X1, float X15, float* dq) {
+// Eight values -> eight 4-bit codes (as e2m1_encode8) AND the codes' grid
+// values as four f16 pairs, each byte decoded straight from the register the
+// encode wrote.
+__device__ __forceinline__ uint32_t e2m1_encode8_dec(const float* v, uint32_t* h) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %8, %7;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %10, %9;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %12, %11;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %4, b3;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r), "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return r;
+}
+
+// Error values of 8 codes given as f16 pairs of grid values (q = 2^e * m):
+// dq = p * X_m with p = q without its 1.5 bit and X_m = X_1 + s * DX, s = 1
+// for m = 1.5 (exact: X_1 + DX = X_1.5).  s is built from the 1.5 bit by an
+// integer multiply (bit 9 * 0x1FC000 = the bits of 1.0f; the other half's
+// bit 25 overflows out), so the selection needs no compare or select.
+__device__ __forceinline__ void error_values8(const uint32_t* h, float X1, float DX, float* dq) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t h = e2m1_decode_byte(w, i);
-        const uint32_t pw = h & ~0x02000200u;             // clear the 1.5 bit of both halves
+        const uint32_t sb = h[i] & 0x02000200u;           // the 1.5 bits of both halves
+        const uint32_t pw = h[i] ^ sb;                    // p values
         const float plo = __half2float(__ushort_as_half(static_cast<unsigned short>(pw & 0xFFFFu)));
         const float phi = __half2float(__ushort_as_half(static_cast<unsigned short>(pw >> 16)));
-        dq[2 * i] = mul_rn(plo, (h & 0x00000200u) ? X15 : X1);
-        dq[2 * i + 1] = mul_rn(phi, (h & 0x02000000u) ? X15 : X1);
+        const float slo = __uint_as_float(sb * 0x1FC000u);
+        const float shi = __uint_as_float(__umulhi(sb, 0x10000u) * 0x1FC000u);
+        dq[2 * i] = mul_rn(plo, __fmaf_rn(slo, DX, X1));
+        dq[2 * i + 1] = mul_rn(phi, __fmaf_rn(shi, DX, X1));
     }
 }
 

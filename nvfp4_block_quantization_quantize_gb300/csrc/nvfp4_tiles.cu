@@ -223,17 +223,15 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
         next_row(16 + r, y);
         float e[16];
         uint32_t w0, w1;
-        encode_scaled16(y, c6.enc, w0, w1);
+        candidate16<ERR>(y, c6, d6, g.A, C, w0, w1, e);
         sW[0][r][tid] = w0;
         sW[1][r][tid] = w1;
-        candidate_errors16<ERR>(y, w0, w1, c6, d6, g.A, C, e);
         sR6[r][tid] = seq_sum16(e);
 #pragma unroll
         for (int i = 0; i < 16; ++i) F6[i] = add_rn(F6[i], e[i]);
-        encode_scaled16(y, c4.enc, w0, w1);
+        candidate16<ERR>(y, c4, d4, g.A, C, w0, w1, e);
         sW[2][r][tid] = w0;
         sW[3][r][tid] = w1;
-        candidate_errors16<ERR>(y, w0, w1, c4, d4, g.A, C, e);
         sR4[r][tid] = seq_sum16(e);
 #pragma unroll
         for (int i = 0; i < 16; ++i) F4[i] = add_rn(F4[i], e[i]);
