@@ -62,8 +62,6 @@ __device__ __forceinline__ float absmax16(const float* y) {
 }
 
 // ---- plain path ---------------------------------------------------------------------------
-// codes of y / D (D = decoded scale * S_dec), nearest or stochastic; a zero
-// divisor zeroes the block.  b is the block amax (bounds |y|).
 // The plain path's division y / D.  2^-20 <= D <= 2^20 and |y| <= b <= 2^60
 // keep quotients and remainders normal for |y| >= 2^-80, so the reciprocal
 // sequence is exact there; below that the quotient is under 2^-60 and its
@@ -73,14 +71,32 @@ __device__ __forceinline__ bool plain_fast(float D, float b) {
     return D >= 9.5367431640625e-07f && D <= 1048576.0f && b <= 1.152921504606847e+18f;
 }
 
-// E4: D is a decoded E4M3 scale (no global scale), so one correction step is
-// exact; otherwise D is arbitrary and two steps are taken.
+// RN(y / D) from r = RN(1/D) up to the sign of a zero result; q0 = y * r
+// (the sign source).  One correction step is exact when D is a decoded E4M3
+// scale (E4), two in general.
+template <bool E4>
+__device__ __forceinline__ float recip_quotient(float y, float D, float r, float& q0) {
+    q0 = mul_rn(y, r);
+    float e = __fmaf_rn(-q0, D, y);
+    float q = __fmaf_rn(e, r, q0);
+    if (!E4) {
+        e = __fmaf_rn(-q, D, y);
+        q = __fmaf_rn(e, r, q);
+    }
+    return q;
+}
+
+// One signed quotient RN(y / D), as plain_quotients16 computes it per element.
 template <bool EXACT, bool E4 = false>
 __device__ __forceinline__ float plain_quotient(float y, float D, float r, bool fast) {
-    if (!fast) return div_rn(y, D);
-    float q = E4 ? div_by_recip1(y, D, r) : div_by_recip(y, D, r);
+    if (!fast) {
+        const float q = div_rn(y, D);
+        return q == q ? q : fabsf(q);
+    }
+    float q0;
+    float q = recip_quotient<E4>(y, D, r, q0);
     if (EXACT && fabsf(y) < 8.271806125530277e-25f) q = div_rn(y, D);
-    return (q == 0.0f) ? copysign_bits(q, y) : q;      // a zero keeps y's sign
+    return sign_of_first(q0, q);
 }
 
 // RN(1/d) for every non-negative E4M3 byte (entry 0 unused: a zero scale
@@ -92,40 +108,69 @@ __device__ __forceinline__ void fill_recip_table(float* rt) {
 
 // codes of y / D (D = decoded scale * S_dec), nearest or stochastic; a zero
 // divisor zeroes the block.  b is the block amax (bounds |y|).  rt: the
-// reciprocal table when D is a bare E4M3 scale sf (no global scale), else null.
+// reciprocal table when D is a bare E4M3 scale sf (no global scale), else
+// null.  With wq, stochastic rounding also returns the codes' signed grid
+// values in q (nearest rounding leaves q alone).
 template <int RND>
 __device__ __forceinline__ void encode_plain16(const float* y, float D, float b, uint64_t idx0,
                                                uint64_t seed, uint64_t step, uint32_t& w0,
-                                               uint32_t& w1, const float* rt = nullptr,
-                                               uint32_t sf = 0) {
-    float v[16];
+                                               uint32_t& w1, const float* rt, uint32_t sf,
+                                               float* q, bool wq) {
     const bool fast = plain_fast(D, b);
-    if (rt) {
-        const float r = rt[sf];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = plain_quotient<RND == NVFP4_SR, true>(y[i], D, r, fast);
-    } else {
-        const float r = fast ? div_rn(1.0f, D) : 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = plain_quotient<RND == NVFP4_SR>(y[i], D, r, fast);
-    }
+    const float r = rt ? rt[sf] : (fast ? div_rn(1.0f, D) : 0.0f);
     if (RND == NVFP4_RTN) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            v[i] = rt ? plain_quotient<false, true>(y[i], D, r, fast) : plain_quotient<false>(y[i], D, r, fast);
         w0 = e2m1_encode8(v);
         w1 = e2m1_encode8(v + 8);
     } else {
         uint32_t wd[16];
         sr_words16(idx0, seed, step, wd);
-        w0 = 0;
-        w1 = 0;
+        // blocks holding an element 0 < |y| < 2^-80 (or zeros) take the per-element checked path
+        bool tiny = false;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            w0 |= e2m1_encode_sr(v[i], wd[i]) << (4 * i);
-            w1 |= e2m1_encode_sr(v[8 + i], wd[8 + i]) << (4 * i);
+        for (int i = 0; i < 16; ++i) tiny |= fabsf(y[i]) < 8.271806125530277e-25f;
+        float g[16];
+        if (fast && !tiny) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float q0;
+                const float m = rt ? recip_quotient<true>(y[i], D, r, q0) : recip_quotient<false>(y[i], D, r, q0);
+                g[i] = sign_of_first(q0, sr_grid_value(fabsf(m), wd[i]));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float v = rt ? plain_quotient<true, true>(y[i], D, r, fast) : plain_quotient<true>(y[i], D, r, fast);
+                g[i] = sign_of_first(v, sr_grid_value(fabsf(v), wd[i]));
+            }
+        }
+        w0 = e2m1_encode8(g);
+        w1 = e2m1_encode8(g + 8);
+        if (wq) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) q[i] = g[i];
         }
     }
     if (D == 0.0f) {
         w0 = 0;
         w1 = 0;
+        if (RND == NVFP4_SR && wq) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) q[i] = 0.0f;
+        }
+    }
+}
+
+// dequantized values (q * d) * S_dec from signed grid values
+template <bool GS>
+__device__ __forceinline__ void dequant_q16(const float* q, float d, float Sdec, float* dq) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float v = mul_rn(q[i], d);
+        dq[i] = GS ? mul_rn(v, Sdec) : v;
     }
 }
 

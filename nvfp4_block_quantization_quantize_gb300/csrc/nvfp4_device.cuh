@@ -85,13 +85,20 @@ __device__ __forceinline__ void e2m1_decode8(uint32_t w, float* q) {
 }
 
 // ---- counter-based generator: Philox4x32-10 (Salmon et al., SC'11) -------------------
+__device__ __forceinline__ uint64_t mul_wide_u32(uint32_t a, uint32_t b) {
+    uint64_t p;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p) : "r"(a), "r"(b));
+    return p;
+}
+
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
         if (r) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
-        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        const uint64_t p0 = mul_wide_u32(0xD2511F53u, c.x);
+        const uint64_t p1 = mul_wide_u32(0xCD9E8D57u, c.z);
+        c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(p1),
+                       static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
     }
     return c;
 }
@@ -114,23 +121,33 @@ __device__ __forceinline__ void sr_words16(uint64_t idx0, uint64_t seed, uint64_
     }
 }
 
-// Stochastic rounding of one value to a 4-bit code ("fp4-train", Method): with
-// G[k] <= |v| < G[k+1], pick k+1 when u < p, p = (|v| - G[k]) / (G[k+1] - G[k]),
-// u = (word >> 8) * 2^-24.  The grid has spacing 0.5 on [0,2), 1 on [2,4) and
-// 2 on [4,6), so t = |v| / spacing is exact, floor(t) indexes the lower point
-// and p = t - floor(t) is exact (Sterbenz); u < p is compared as
-// (word >> 8) < p * 2^24, both sides exact.
-__device__ __forceinline__ uint32_t e2m1_encode_sr(float v, uint32_t word) {
-    const float a = fabsf(v);
-    const uint32_t sign = (__float_as_uint(v) >> 31) << 3;
-    if (!(a < 6.0f)) return (v != v) ? 7u : (sign | 7u);   // NaN -> +6; saturate
-    const float mul = (a < 2.0f) ? 2.0f : ((a < 4.0f) ? 1.0f : 0.5f);
-    const uint32_t off = (a < 2.0f) ? 0u : ((a < 4.0f) ? 2u : 4u);
-    const float t = mul_rn(a, mul);
+// 1.0f when a < b, else 0.0f (one compare-and-set)
+__device__ __forceinline__ float lt_one(float a, float b) {
+    float r;
+    asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// Stochastic rounding of one magnitude a = |v| to a grid value ("fp4-train",
+// Method): with G[k] <= a < G[k+1], take G[k+1] when u < p, p = (a - G[k]) /
+// (G[k+1] - G[k]), u = (word >> 8) * 2^-24.  The grid spacing is 0.5 on
+// [0,2), 1 on [2,4) and 2 on [4,6): sp = 2^(max(E,0) - 1) for a's binary
+// exponent E, built from a's exponent bits together with 1/sp.  t = a / sp
+// is exact and lies in [0,4), floor(t) indexes the lower point, p = t -
+// floor(t) is exact (Sterbenz) and u < p is compared as (word >> 8) < p * 2^24
+// (both sides exact).  a >= 6, infinity and NaN give 6 (the NaN-dropping min
+// after clamping a); the caller restores the sign.
+__device__ __forceinline__ float sr_grid_value(float a, uint32_t word) {
+    a = min_nd(a, 6.0f);
+    const uint32_t eb = __float_as_uint(a) & 0x7F800000u;
+    const uint32_t spb = (eb > 0x3F800000u ? eb : 0x3F800000u) - 0x00800000u;   // sp
+    const float sp = __uint_as_float(spb);
+    const float inv = __uint_as_float(0x7F000000u - spb);                         // 1/sp
+    const float t = mul_rn(a, inv);
     const float fl = floorf(t);
     const float p24 = mul_rn(sub_rn(t, fl), 16777216.0f);
-    const uint32_t up = (static_cast<float>(word >> 8) < p24) ? 1u : 0u;
-    return sign | (static_cast<uint32_t>(fl) + off + up);
+    const float up = lt_one(static_cast<float>(word >> 8), p24);
+    return mul_rn(add_rn(fl, up), sp);
 }
 
 // ---- exact division from a reciprocal ---------------------------------------------------
@@ -158,6 +175,14 @@ __device__ __forceinline__ float div_by_recip1(float a, float b, float r) {
     const float q = mul_rn(a, r);
     const float e = __fmaf_rn(-q, b, a);
     return __fmaf_rn(e, r, q);
+}
+
+// RN(|a| / b) and the sign of a / b: the two-step (or, for E4M3 divisors,
+// one-step) sequence on a signed a gives the exact magnitude, while its first
+// product a * r carries the quotient's sign also for a = -0 (where the
+// correction's sum would be +0) and is a positive NaN for NaN a.
+__device__ __forceinline__ float sign_of_first(float q0, float mag) {
+    return __uint_as_float((__float_as_uint(mag) & 0x7FFFFFFFu) | (__float_as_uint(q0) & 0x80000000u));
 }
 
 __device__ __forceinline__ float copysign_bits(float mag, float s) {

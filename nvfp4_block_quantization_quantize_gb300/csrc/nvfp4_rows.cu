@@ -30,22 +30,25 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, floa
     }
     const float b = absmax16(y);
     uint32_t w0, w1, sf;
-    float d;
+    float d, q[16];
+    const bool wq = EF || a.dq_bf16;
+    constexpr bool QV = ERR == NVFP4_ERR_NONE && RND == NVFP4_SR;   // grid values kept
     if (ERR == NVFP4_ERR_NONE) {
         const float s6f = block_s6f<GS>(b, gb.Senc);
         sf = e4m3_encode(min_nd(s6f, 448.0f));
         d = e4m3_decode(sf);
         const float D = GS ? mul_rn(d, gb.Sdec) : d;
         encode_plain16<RND>(y, D, b, idx_base + static_cast<uint64_t>(blk) * 16u, a.seed, a.step,
-                            w0, w1, GS ? nullptr : rt, sf);
+                            w0, w1, GS ? nullptr : rt, sf, q, wq);
     } else {
         four_over_six16<ERR, false>(y, b, gb, C, tab, w0, w1, sf, d);
     }
     if (a.codes) reinterpret_cast<uint2*>(a.codes)[blk] = make_uint2(w0, w1);
     if (a.scales) a.scales[blk] = static_cast<uint8_t>(sf);
-    if (EF || a.dq_bf16) {
+    if (wq) {
         float dq[16];
-        dequant16<GS || ERR != NVFP4_ERR_NONE>(w0, w1, d, gb.Sdec, dq);
+        if (QV) dequant_q16<GS>(q, d, gb.Sdec, dq);
+        else dequant16<GS || ERR != NVFP4_ERR_NONE>(w0, w1, d, gb.Sdec, dq);
         if (EF) {
             float r[16];
 #pragma unroll

@@ -80,7 +80,9 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
     // ---- rowwise ----
     {
         uint32_t w0, w1, sf;
-        float d;
+        float d, q[16];
+        const bool wq = EF || a.dq_bf16;
+        constexpr bool QV = ERR == NVFP4_ERR_NONE && RND == NVFP4_SR;   // grid values kept
         constexpr bool TREE = BLK == NVFP4_BLOCK_16X16;
         if (ERR == NVFP4_ERR_NONE) {
             const float s6f = block_s6f<GS>(b, g.Senc);
@@ -89,16 +91,17 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
             const float D = GS ? mul_rn(d, g.Sdec) : d;
             const uint64_t idx0 = (static_cast<uint64_t>(a.row_offset) + static_cast<uint64_t>(row)) *
                                       static_cast<uint64_t>(a.K) + static_cast<uint64_t>(cb * 16);
-            encode_plain16<RND>(y, D, b, idx0, a.seed, a.step, w0, w1, GS ? nullptr : rtab, sf);
+            encode_plain16<RND>(y, D, b, idx0, a.seed, a.step, w0, w1, GS ? nullptr : rtab, sf, q, wq);
         } else {
             four_over_six16<ERR, TREE>(y, b, g, C, tp, w0, w1, sf, d);
         }
         if (valid) {
             if (a.codes) reinterpret_cast<uint2*>(a.codes)[e0 / 16] = make_uint2(w0, w1);
             if (a.scales) a.scales[row * nb + cb] = static_cast<uint8_t>(sf);
-            if (EF || a.dq_bf16) {
+            if (wq) {
                 float dq[16];
-                dequant16<GS || ERR != NVFP4_ERR_NONE>(w0, w1, d, g.Sdec, dq);
+                if (QV) dequant_q16<GS>(q, d, g.Sdec, dq);
+                else dequant16<GS || ERR != NVFP4_ERR_NONE>(w0, w1, d, g.Sdec, dq);
                 if (EF) {
                     float r[16];
 #pragma unroll
@@ -128,7 +131,8 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
         sf = e4m3_encode(min_nd(s6f, 448.0f));
         d = e4m3_decode(sf);
         const float D = GS ? mul_rn(d, g.Sdec) : d;
-        encode_plain16<NVFP4_RTN>(c, D, bc, 0, 0, 0, w0, w1, GS ? nullptr : rtab, sf);
+        float qc[16];
+        encode_plain16<NVFP4_RTN>(c, D, bc, 0, 0, 0, w0, w1, GS ? nullptr : rtab, sf, qc, false);
     } else {
         four_over_six16<ERR, BLK == NVFP4_BLOCK_16X16>(c, bc, g, C, tp, w0, w1, sf, d);
     }
