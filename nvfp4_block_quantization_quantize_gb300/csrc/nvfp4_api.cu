@@ -88,8 +88,7 @@ int run_quant(nvfp4::QuantArgs a, float* gamax, void* stream) {
         a.gamax_mode = a.gamax_mode == NVFP4_GAMAX_TENSOR ? NVFP4_GAMAX_TENSOR_GIVEN : NVFP4_GAMAX_ROW_GIVEN;
     }
     if (a.M == 0 || a.K == 0) return NVFP4_OK;
-    const bool tiles = a.block == NVFP4_BLOCK_16X16 || a.codes_col != nullptr;
-    err = tiles ? nvfp4::launch_quantize_tiles(a, stream) : nvfp4::launch_quantize_rows(a, stream);
+    err = a.codes_col ? nvfp4::launch_quantize_tiles(a, stream) : nvfp4::launch_quantize_rows(a, stream);
     if (err) return cuda_fail(err, "quantize launch");
     return NVFP4_OK;
 }

@@ -232,10 +232,12 @@ __device__ __forceinline__ void fill_cand_table(Cand* tab, float Sdec, float A, 
 
 // Four-over-six for one 16-value group (1x16 block, or one row of a 16x16 tile
 // when TREE: the row error sums are combined over the half warp).
-template <int ERR, bool TREE>
+// tile_sums(E6, E4) turns one group's error sums into its block's: nothing for
+// a 1x16 block, the width-16 tree over the tile's 16 rows for a 16x16 tile.
+template <int ERR, class TileSums>
 __device__ __forceinline__ void four_over_six16(const float* y, float b, const GScale& g, float C,
                                                 const Cand* tab, uint32_t& w0, uint32_t& w1,
-                                                uint32_t& sf, float& d) {
+                                                uint32_t& sf, float& d, TileSums tile_sums) {
     const float s6f = block_s6f<true>(b, g.Senc);
     const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
     const uint32_t sf4 = e4m3_encode(min_nd(mul_rn(s6f, 1.5f), 448.0f));
@@ -248,15 +250,25 @@ __device__ __forceinline__ void four_over_six16(const float* y, float b, const G
     float E6 = seq_sum16(e);
     candidate16<ERR>(y, c4, d4, g.A, C, b0, b1, e);
     float E4 = seq_sum16(e);
-    if (TREE) {
-        E6 = tree16_lanes(E6);
-        E4 = tree16_lanes(E4);
-    }
+    tile_sums(E6, E4);
     const bool pick4 = E4 < E6;                 // ties and NaN keep map-to-6
     w0 = pick4 ? b0 : a0;
     w1 = pick4 ? b1 : a1;
     sf = pick4 ? sf4 : sf6;
     d = pick4 ? d4 : d6;
+}
+
+// TREE: the tile's 16 rows are the 16 lanes of the caller's half warp.
+template <int ERR, bool TREE>
+__device__ __forceinline__ void four_over_six16(const float* y, float b, const GScale& g, float C,
+                                                const Cand* tab, uint32_t& w0, uint32_t& w1,
+                                                uint32_t& sf, float& d) {
+    four_over_six16<ERR>(y, b, g, C, tab, w0, w1, sf, d, [](float& E6, float& E4) {
+        if (TREE) {
+            E6 = tree16_lanes(E6);
+            E4 = tree16_lanes(E4);
+        }
+    });
 }
 
 // dequantized values (q * d) * S_dec of 16 codes

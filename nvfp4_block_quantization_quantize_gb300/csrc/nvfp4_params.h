@@ -37,8 +37,8 @@ struct DequantArgs {
 };
 
 // launchers (each returns cudaGetLastError() after its launches)
-int launch_quantize_rows(const QuantArgs& a, void* stream);    // 1x16, rowwise only
-int launch_quantize_tiles(const QuantArgs& a, void* stream);   // 16x16, or any columnwise
+int launch_quantize_rows(const QuantArgs& a, void* stream);    // rowwise output only
+int launch_quantize_tiles(const QuantArgs& a, void* stream);   // rowwise + columnwise
 int launch_dequantize(const DequantArgs& a, void* stream);
 int launch_amax(const void* x, int64_t M, int64_t K, int dtype, const float* residual, int mode,
                 float* out, void* stream);

@@ -1,4 +1,5 @@
-// nvfp4_rows.cu -- 1x16 rowwise quantization (and qdq) for sm_103a.
+// nvfp4_rows.cu -- rowwise quantization (and qdq) for sm_103a: 1x16 blocks
+// (k_rows) and 16x16 blocks (k_band16).
 //
 // K % 16 == 0, so the 1x16 blocks of a row-major [M,K] tensor are simply the
 // consecutive 16-element groups of the flat array: the kernel streams them.
@@ -19,16 +20,21 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <int DT, int ERR, int RND, bool EF, bool GS>
-__device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, float* y,
+// One 1x16 group y of block-row blk: its block amax is tile_amax(the group's
+// absmax) and its four-over-six error sums go through tile_sums (identities
+// for 1x16 blocks; the 16x16 tile's reductions otherwise).  Nothing is stored
+// when !live (a group past the tensor's last column block).
+template <int DT, int ERR, int RND, bool EF, bool GS, class TileAmax, class TileSums>
+__device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool live, float* y,
                                            const GScale& g, float C, const Cand* tab,
-                                           const float* rt, uint64_t idx_base, int64_t bpr) {
+                                           const float* rt, uint64_t idx_base, int64_t bpr,
+                                           TileAmax tile_amax, TileSums tile_sums) {
     GScale gb = g;
     if (a.gamax_mode == NVFP4_GAMAX_ROW_GIVEN) {
         gb.A = a.gamax[blk / bpr];
         global_scales(gb.A, a.bound, gb.Senc, gb.Sdec);
     }
-    const float b = absmax16(y);
+    const float b = tile_amax(absmax16(y));
     uint32_t w0, w1, sf;
     float d, q[16];
     const bool wq = EF || a.dq_bf16;
@@ -41,8 +47,9 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, floa
         encode_plain16<RND>(y, D, b, idx_base + static_cast<uint64_t>(blk) * 16u, a.seed, a.step,
                             w0, w1, GS ? nullptr : rt, sf, q, wq);
     } else {
-        four_over_six16<ERR, false>(y, b, gb, C, tab, w0, w1, sf, d);
+        four_over_six16<ERR>(y, b, gb, C, tab, w0, w1, sf, d, tile_sums);
     }
+    if (!live) return;
     if (a.codes) reinterpret_cast<uint2*>(a.codes)[blk] = make_uint2(w0, w1);
     if (a.scales) a.scales[blk] = static_cast<uint8_t>(sf);
     if (wq) {
@@ -128,17 +135,154 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
         }
-        rows_block<DT, ERR, RND, EF, GS>(a, blk, y, g, C, tp, rtab, idx_base, bpr);
+        rows_block<DT, ERR, RND, EF, GS>(a, blk, true, y, g, C, tp, rtab, idx_base, bpr,
+                                         [](float b) { return b; }, [](float&, float&) {});
         stage = stage == S - 1 ? 0 : stage + 1;
     }
     cp_async_wait<0>();
 }
 
+// 16x16 blocks, rowwise output.  One CTA step quantizes a 16-row band x 256
+// columns (16 tiles): warp w holds rows 2w and 2w+1 of the band (lanes 0-15
+// and 16-31), lane l&15 the tile, so a warp's loads and stores run along two
+// rows like the 1x16 walk's.  The tile amax is reduced over the lane pair and
+// then the 8 warps through shared memory; four-over-six's row error sums are
+// combined with the width-16 tree in the same way.  The CTAs walk the steps
+// (band-major) persistently, each thread fetching its group one step ahead
+// (the per-thread copy pipeline of k_rows); the reductions' shared buffers
+// alternate between steps, so one barrier per reduction suffices.
+struct BandCursor {      // CTA-uniform step: (band, 256-column chunk)
+    int64_t band, chunk, nch, dband, dchunk;
+    __device__ void init(int64_t u, int64_t nch_, int64_t stride) {
+        nch = nch_;
+        band = u / nch;
+        chunk = u - band * nch;
+        dband = stride / nch;
+        dchunk = stride - dband * nch;
+    }
+    __device__ void advance() {
+        band += dband;
+        chunk += dchunk;
+        if (chunk >= nch) {
+            chunk -= nch;
+            ++band;
+        }
+    }
+};
+
 template <int DT, int ERR, int RND, bool EF, bool GS>
-int launch_rows(const QuantArgs& a, int64_t nblk, cudaStream_t s) {
-    auto kernel = k_rows<DT, ERR, RND, EF, GS>;
-    constexpr int smem = RowsStage<DT, EF>::TOTAL;
-    static thread_local int configured_dev = -1, per_sm = 1;
+__global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
+    using St = RowsStage<DT, EF>;
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ Cand tab[ERR != NVFP4_ERR_NONE ? 128 : 1];
+    __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
+    __shared__ float red[2][8][16];                                   // [step parity][warp][tile]
+    __shared__ float esum[ERR != NVFP4_ERR_NONE ? 2 : 1][2][16][16];  // [parity][cand][row][tile]
+    if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
+    const int64_t nb = a.K / 16;
+    const int64_t nch = (nb + 15) / 16;
+    const int64_t nbands = a.M / 16;
+    GScale g{0.0f, 1.0f, 1.0f};
+    if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
+        g.A = a.gamax[0];
+        global_scales(g.A, a.bound, g.Senc, g.Sdec);
+    }
+    const float C = mul_rn(6.0f, a.bound);
+    const Cand* tp = nullptr;
+    if (ERR != NVFP4_ERR_NONE) {
+        fill_cand_table(tab, g.Sdec, g.A, C);
+        tp = tab;
+    }
+    const uint64_t idx_base = static_cast<uint64_t>(a.row_offset) * static_cast<uint64_t>(a.K);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rr = 2 * warp + (lane >> 4);       // row within the band
+    const int t = lane & 15;                     // tile within the chunk
+    unsigned char* xs = smem + tid * St::XB;
+    unsigned char* rs = smem + kThreads * St::XB + tid * St::RB;
+
+    auto group = [&](const BandCursor& c, bool& live) {   // this thread's 1x16 block
+        const int64_t cb = c.chunk * 16 + t;
+        live = c.band < nbands && cb < nb;
+        return (c.band * 16 + rr) * nb + cb;
+    };
+    auto issue = [&](const BandCursor& c, int stage) {
+        bool live;
+        const int64_t blk = group(c, live);
+        if (live) {
+            const unsigned char* gx = static_cast<const unsigned char*>(a.x) + blk * St::XB;
+#pragma unroll
+            for (int k = 0; k < St::XB / 16; ++k) cp_async16(xs + stage * St::BYTES + 16 * k, gx + 16 * k);
+            if (EF) {
+                const unsigned char* gr = reinterpret_cast<const unsigned char*>(a.residual) + blk * 64;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) cp_async16(rs + stage * St::BYTES + 16 * k, gr + 16 * k);
+            }
+        }
+        cp_async_commit();
+    };
+
+    constexpr int S = St::STAGES;
+    BandCursor cur, ahead;
+    cur.init(blockIdx.x, nch, gridDim.x);
+    ahead = cur;
+#pragma unroll
+    for (int k = 0; k < S - 1; ++k) {
+        issue(ahead, k);
+        ahead.advance();
+    }
+    int stage = 0, par = 0;
+    for (; cur.band < nbands; cur.advance()) {
+        issue(ahead, stage == 0 ? S - 1 : stage - 1);
+        ahead.advance();
+        cp_async_wait<S - 1>();
+        bool live;
+        const int64_t blk = group(cur, live);
+        float y[16];
+        if (live) {
+            lds16<DT>(xs + stage * St::BYTES, y);
+            if (EF) {
+                float r[16];
+                lds16<NVFP4_F32>(rs + stage * St::BYTES, r);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) y[i] = 0.0f;
+        }
+        auto tile_amax = [&](float b) {
+            b = max_nd(b, __shfl_xor_sync(kFullMask, b, 16));
+            if (lane < 16) red[par][warp][t] = b;
+            __syncthreads();
+            float m = red[par][0][t];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) m = max_nd(m, red[par][w][t]);
+            return m;
+        };
+        auto tile_sums = [&](float& E6, float& E4) {
+            if constexpr (ERR != NVFP4_ERR_NONE) {
+                esum[par][0][rr][t] = E6;
+                esum[par][1][rr][t] = E4;
+                __syncthreads();
+                float e[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) e[r] = esum[par][0][r][t];
+                E6 = tree16_regs(e);
+#pragma unroll
+                for (int r = 0; r < 16; ++r) e[r] = esum[par][1][r][t];
+                E4 = tree16_regs(e);
+            }
+        };
+        rows_block<DT, ERR, RND, EF, GS>(a, blk, live, y, g, C, tp, rtab, idx_base, nb, tile_amax, tile_sums);
+        stage = stage == S - 1 ? 0 : stage + 1;
+        par ^= 1;
+    }
+    cp_async_wait<0>();
+}
+
+template <class KernelT>
+int launch_persistent(KernelT kernel, int smem, int64_t units_per_cta_step, int64_t units, const QuantArgs& a,
+                      cudaStream_t s, int& configured_dev, int& per_sm) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
@@ -148,30 +292,48 @@ int launch_rows(const QuantArgs& a, int64_t nblk, cudaStream_t s) {
             per_sm = 1;
         configured_dev = dev;
     }
-    const int64_t want = (nblk + kThreads - 1) / kThreads;
+    const int64_t want = (units + units_per_cta_step - 1) / units_per_cta_step;
     const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
     const int grid = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
     kernel<<<grid, kThreads, smem, s>>>(a);
     return static_cast<int>(cudaGetLastError());
 }
 
-template <int DT, bool GS>
+// BLK 1x16: k_rows over blocks; 16x16: k_band16 over (band, chunk) steps
+template <int DT, int BLK, int ERR, int RND, bool EF, bool GS>
+int launch_rows(const QuantArgs& a, int64_t nblk, cudaStream_t s) {
+    constexpr int smem = RowsStage<DT, EF>::TOTAL;
+    static thread_local int configured_dev = -1, per_sm = 1;
+    if (BLK == NVFP4_BLOCK_16X16) {
+        const int64_t steps = (a.M / 16) * ((a.K / 16 + 15) / 16);
+        return launch_persistent(k_band16<DT, ERR, RND, EF, GS>, smem, 1, steps, a, s, configured_dev, per_sm);
+    }
+    return launch_persistent(k_rows<DT, ERR, RND, EF, GS>, smem, kThreads, nblk, a, s, configured_dev, per_sm);
+}
+
+template <int DT, int BLK, bool GS>
 int rows_plain(const QuantArgs& a, int64_t nblk, cudaStream_t s) {
     const bool ef = a.residual != nullptr;
     if (a.rounding == NVFP4_RTN)
-        return ef ? launch_rows<DT, NVFP4_ERR_NONE, NVFP4_RTN, true, GS>(a, nblk, s)
-                  : launch_rows<DT, NVFP4_ERR_NONE, NVFP4_RTN, false, GS>(a, nblk, s);
-    return ef ? launch_rows<DT, NVFP4_ERR_NONE, NVFP4_SR, true, GS>(a, nblk, s)
-              : launch_rows<DT, NVFP4_ERR_NONE, NVFP4_SR, false, GS>(a, nblk, s);
+        return ef ? launch_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN, true, GS>(a, nblk, s)
+                  : launch_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN, false, GS>(a, nblk, s);
+    return ef ? launch_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, true, GS>(a, nblk, s)
+              : launch_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, false, GS>(a, nblk, s);
+}
+
+template <int DT, int BLK>
+int rows_dispatch_blk(const QuantArgs& a, cudaStream_t s) {
+    const int64_t nblk = a.M * (a.K / 16);
+    if (a.err_mode == NVFP4_ERR_MAE) return launch_rows<DT, BLK, NVFP4_ERR_MAE, NVFP4_RTN, false, true>(a, nblk, s);
+    if (a.err_mode == NVFP4_ERR_MSE) return launch_rows<DT, BLK, NVFP4_ERR_MSE, NVFP4_RTN, false, true>(a, nblk, s);
+    return a.gamax_mode == NVFP4_GAMAX_NONE ? rows_plain<DT, BLK, false>(a, nblk, s)
+                                            : rows_plain<DT, BLK, true>(a, nblk, s);
 }
 
 template <int DT>
 int rows_dispatch(const QuantArgs& a, cudaStream_t s) {
-    const int64_t nblk = a.M * (a.K / 16);
-    if (a.err_mode == NVFP4_ERR_MAE) return launch_rows<DT, NVFP4_ERR_MAE, NVFP4_RTN, false, true>(a, nblk, s);
-    if (a.err_mode == NVFP4_ERR_MSE) return launch_rows<DT, NVFP4_ERR_MSE, NVFP4_RTN, false, true>(a, nblk, s);
-    return a.gamax_mode == NVFP4_GAMAX_NONE ? rows_plain<DT, false>(a, nblk, s)
-                                            : rows_plain<DT, true>(a, nblk, s);
+    return a.block == NVFP4_BLOCK_16X16 ? rows_dispatch_blk<DT, NVFP4_BLOCK_16X16>(a, s)
+                                        : rows_dispatch_blk<DT, NVFP4_BLOCK_1X16>(a, s);
 }
 
 }  // namespace

@@ -1,11 +1,12 @@
 // nvfp4_tiles.cu -- 16x16 blocks and columnwise outputs for sm_103a.
 //
-// k_tiles_rows  one CTA = a 16-row band x 256 columns; lane l of warp w holds
-//               row l%16 of the 16x16 tile 2w + l/16.  16x16 blocks reduce
-//               their amax (and, for four-over-six, their row error sums
-//               with the fixed width-16 tree) over the half warp.  With a
-//               columnwise output the tile is staged in shared memory and
-//               each thread then owns one column (x^T's row) of the band.
+// k_tiles_rows  rowwise + columnwise output (round to nearest): one CTA = a
+//               16-row band x 256 columns; lane l of warp w holds row l%16
+//               of the 16x16 tile 2w + l/16.  16x16 blocks reduce their amax
+//               (and, for four-over-six, their row error sums with the fixed
+//               width-16 tree) over the half warp.  The band is then staged
+//               in shared memory and each thread owns one column (x^T's row)
+//               of it for the columnwise pass.
 // k_tile_t      four-over-six 16x16 with rowwise AND columnwise output: one
 //               thread owns a whole 16x16 tile and walks its rows twice
 //               (amax; both candidates' codes and errors with the row sums
@@ -35,9 +36,9 @@ constexpr int kThreads = 256;
 constexpr int kTileCols = 256;
 constexpr int kYsStride = kTileCols + 4;
 
-template <int DT, int BLK, int ERR, int RND, bool EF, bool GS, bool COLW>
+template <int DT, int BLK, int ERR, bool GS>
 __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
-    __shared__ float ys[COLW ? 16 * kYsStride : 1];
+    __shared__ float ys[16 * kYsStride];
     __shared__ Cand tab[ERR != NVFP4_ERR_NONE ? 128 : 1];
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
     if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
@@ -64,12 +65,6 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
     float y[16];
     if (valid) {
         load16<DT>(a.x, e0, y);
-        if (EF) {
-            float r[16];
-            load16_f32(a.residual, e0, r);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
-        }
     } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) y[i] = 0.0f;
@@ -80,39 +75,22 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
     // ---- rowwise ----
     {
         uint32_t w0, w1, sf;
-        float d, q[16];
-        const bool wq = EF || a.dq_bf16;
-        constexpr bool QV = ERR == NVFP4_ERR_NONE && RND == NVFP4_SR;   // grid values kept
-        constexpr bool TREE = BLK == NVFP4_BLOCK_16X16;
+        float d;
         if (ERR == NVFP4_ERR_NONE) {
             const float s6f = block_s6f<GS>(b, g.Senc);
             sf = e4m3_encode(min_nd(s6f, 448.0f));
             d = e4m3_decode(sf);
             const float D = GS ? mul_rn(d, g.Sdec) : d;
-            const uint64_t idx0 = (static_cast<uint64_t>(a.row_offset) + static_cast<uint64_t>(row)) *
-                                      static_cast<uint64_t>(a.K) + static_cast<uint64_t>(cb * 16);
-            encode_plain16<RND>(y, D, b, idx0, a.seed, a.step, w0, w1, GS ? nullptr : rtab, sf, q, wq);
+            float q[16];
+            encode_plain16<NVFP4_RTN>(y, D, b, 0, 0, 0, w0, w1, GS ? nullptr : rtab, sf, q, false);
         } else {
-            four_over_six16<ERR, TREE>(y, b, g, C, tp, w0, w1, sf, d);
+            four_over_six16<ERR, BLK == NVFP4_BLOCK_16X16>(y, b, g, C, tp, w0, w1, sf, d);
         }
         if (valid) {
             if (a.codes) reinterpret_cast<uint2*>(a.codes)[e0 / 16] = make_uint2(w0, w1);
             if (a.scales) a.scales[row * nb + cb] = static_cast<uint8_t>(sf);
-            if (wq) {
-                float dq[16];
-                if (QV) dequant_q16<GS>(q, d, g.Sdec, dq);
-                else dequant16<GS || ERR != NVFP4_ERR_NONE>(w0, w1, d, g.Sdec, dq);
-                if (EF) {
-                    float r[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) r[i] = sub_rn(y[i], dq[i]);
-                    store16_f32(a.residual, e0, r);
-                }
-                if (a.dq_bf16) store16_bf16(a.dq_bf16, e0, dq);
-            }
         }
     }
-    if constexpr (COLW) {
     // ---- columnwise: the rowwise quantization of x^T, from the staged band ----
 #pragma unroll
     for (int i = 0; i < 16; ++i) ys[rr * kYsStride + t * 16 + i] = y[i];
@@ -139,7 +117,6 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
     if (col < a.K) {
         reinterpret_cast<uint2*>(a.codes_col)[(col * a.M + band * 16) / 16] = make_uint2(w0, w1);
         a.scales_col[col * (a.M / 16) + band] = static_cast<uint8_t>(sf);
-    }
     }
 }
 
@@ -293,17 +270,6 @@ int launch_rowowner(KernelT kernel, const QuantArgs& a, cudaStream_t s) {
     return static_cast<int>(cudaGetLastError());
 }
 
-template <int DT, int BLK, bool COLW, bool GS>
-int plain_dispatch(const QuantArgs& a, cudaStream_t s) {
-    if (COLW) return launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN, false, GS, COLW>, a, s);
-    const bool ef = a.residual != nullptr;
-    if (a.rounding == NVFP4_RTN)
-        return ef ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN, true, GS, false>, a, s)
-                  : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN, false, GS, false>, a, s);
-    return ef ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, true, GS, false>, a, s)
-              : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, false, GS, false>, a, s);
-}
-
 template <int DT, int ERR>
 int launch_tile_t(const QuantArgs& a, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(a.M / 16),
@@ -312,27 +278,24 @@ int launch_tile_t(const QuantArgs& a, cudaStream_t s) {
     return static_cast<int>(cudaGetLastError());
 }
 
-template <int DT, int BLK, bool COLW>
+// rowwise + columnwise outputs (round to nearest, no residual)
+template <int DT, int BLK>
 int tiles_dispatch_blk(const QuantArgs& a, cudaStream_t s) {
     if (a.err_mode != NVFP4_ERR_NONE) {
-        if (BLK == NVFP4_BLOCK_16X16 && COLW)
+        if (BLK == NVFP4_BLOCK_16X16)
             return a.err_mode == NVFP4_ERR_MAE ? launch_tile_t<DT, NVFP4_ERR_MAE>(a, s)
                                                : launch_tile_t<DT, NVFP4_ERR_MSE>(a, s);
-        return a.err_mode == NVFP4_ERR_MAE
-                   ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_MAE, NVFP4_RTN, false, true, COLW>, a, s)
-                   : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_MSE, NVFP4_RTN, false, true, COLW>, a, s);
+        return a.err_mode == NVFP4_ERR_MAE ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_MAE, true>, a, s)
+                                           : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_MSE, true>, a, s);
     }
-    return a.gamax_mode == NVFP4_GAMAX_NONE ? plain_dispatch<DT, BLK, COLW, false>(a, s)
-                                            : plain_dispatch<DT, BLK, COLW, true>(a, s);
+    return a.gamax_mode == NVFP4_GAMAX_NONE ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, false>, a, s)
+                                            : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, true>, a, s);
 }
 
 template <int DT>
 int tiles_dispatch(const QuantArgs& a, cudaStream_t s) {
-    const bool colw = a.codes_col != nullptr;
-    if (a.block == NVFP4_BLOCK_16X16)
-        return colw ? tiles_dispatch_blk<DT, NVFP4_BLOCK_16X16, true>(a, s)
-                    : tiles_dispatch_blk<DT, NVFP4_BLOCK_16X16, false>(a, s);
-    return tiles_dispatch_blk<DT, NVFP4_BLOCK_1X16, true>(a, s);
+    return a.block == NVFP4_BLOCK_16X16 ? tiles_dispatch_blk<DT, NVFP4_BLOCK_16X16>(a, s)
+                                        : tiles_dispatch_blk<DT, NVFP4_BLOCK_1X16>(a, s);
 }
 
 }  // namespace
