@@ -184,24 +184,22 @@ __device__ __forceinline__ void encode_scaled16(const float* y, float enc, uint3
     w1 = e2m1_encode8(v + 8);
 }
 
-// One candidate over 16 values: codes of y * enc, and the per-element errors
+// One candidate over 8 values: codes of y * enc, and the per-element errors
 // |dq - y| (MAE) or (dq - y)^2 (MSE) of its error values dq = ((q*d)*A)/C.
 template <int ERR>
-__device__ __forceinline__ void candidate16(const float* y, const Cand& c, float d, float A, float C,
-                                            uint32_t& w0, uint32_t& w1, float* e) {
-    float v[16];
+__device__ __forceinline__ void candidate8(const float* y, const Cand& c, float d, float A, float C,
+                                           uint32_t& w, float* e) {
+    float v[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = mul_rn(y[i], c.enc);
-    uint32_t h[8];
-    w0 = e2m1_encode8_dec(v, h);
-    w1 = e2m1_encode8_dec(v + 8, h + 4);
-    float dq[16];
+    for (int i = 0; i < 8; ++i) v[i] = mul_rn(y[i], c.enc);
+    uint32_t h[4];
+    w = e2m1_encode8_dec(v, h);
+    float dq[8];
     if (c.fast) {
         error_values8(h, c.X1, c.DX, dq);
-        error_values8(h + 4, c.X1, c.DX, dq + 8);
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 4; ++i) {
             const float qlo = __half2float(__ushort_as_half(static_cast<unsigned short>(h[i] & 0xFFFFu)));
             const float qhi = __half2float(__ushort_as_half(static_cast<unsigned short>(h[i] >> 16)));
             dq[2 * i] = div_rn(mul_rn(mul_rn(qlo, d), A), C);
@@ -209,10 +207,26 @@ __device__ __forceinline__ void candidate16(const float* y, const Cand& c, float
         }
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
         const float diff = sub_rn(dq[i], y[i]);
         e[i] = (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff);
     }
+}
+
+// The same over 16 values (two 8-value halves).
+template <int ERR>
+__device__ __forceinline__ void candidate16(const float* y, const Cand& c, float d, float A, float C,
+                                            uint32_t& w0, uint32_t& w1, float* e) {
+    candidate8<ERR>(y, c, d, A, C, w0, e);
+    candidate8<ERR>(y + 8, c, d, A, C, w1, e + 8);
+}
+
+// sequential sum start + e[0] + ... + e[7]
+__device__ __forceinline__ float seq_sum8(float start, const float* e) {
+    float E = start;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) E = add_rn(E, e[i]);
+    return E;
 }
 
 // sequential sum e[0] + ... + e[15] from 0
