@@ -134,11 +134,19 @@ __device__ __forceinline__ void encode_plain16(const float* y, float D, float b,
         for (int i = 0; i < 16; ++i) tiny |= fabsf(y[i]) < 8.271806125530277e-25f;
         float g[16];
         if (fast && !tiny) {
+            const uint64_t R2 = pack2(r, r), ND2 = pack2(-D, -D);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float q0;
-                const float m = rt ? recip_quotient<true>(y[i], D, r, q0) : recip_quotient<false>(y[i], D, r, q0);
-                g[i] = sign_of_first(q0, sr_grid_value(fabsf(m), wd[i]));
+            for (int i = 0; i < 16; i += 2) {
+                const uint64_t Y = pack2(y[i], y[i + 1]);
+                const uint64_t Q0 = mul2(Y, R2);
+                uint64_t Q = fma2(fma2(Q0, ND2, Y), R2, Q0);
+                if (!rt) Q = fma2(fma2(Q, ND2, Y), R2, Q);
+                float q0a, q0b, qa, qb, ga, gb;
+                unpack2(Q0, q0a, q0b);
+                unpack2(Q, qa, qb);
+                sr_grid_value2(fabsf(qa), fabsf(qb), wd[i], wd[i + 1], ga, gb);
+                g[i] = sign_of_first(q0a, ga);
+                g[i + 1] = sign_of_first(q0b, gb);
             }
         } else {
 #pragma unroll

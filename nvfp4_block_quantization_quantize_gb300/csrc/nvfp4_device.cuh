@@ -121,6 +121,36 @@ __device__ __forceinline__ void sr_words16(uint64_t idx0, uint64_t seed, uint64_
     }
 }
 
+// ---- packed pairs of fp32 (one instruction, two IEEE round-to-nearest results) ----
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // 1.0f when a < b, else 0.0f (one compare-and-set)
 __device__ __forceinline__ float lt_one(float a, float b) {
     float r;
@@ -148,6 +178,26 @@ __device__ __forceinline__ float sr_grid_value(float a, uint32_t word) {
     const float p24 = mul_rn(sub_rn(t, fl), 16777216.0f);
     const float up = lt_one(static_cast<float>(word >> 8), p24);
     return mul_rn(add_rn(fl, up), sp);
+}
+
+// sr_grid_value on two magnitudes at once (same arithmetic, paired fp32 ops)
+__device__ __forceinline__ void sr_grid_value2(float a0, float a1, uint32_t w0, uint32_t w1, float& g0, float& g1) {
+    a0 = min_nd(a0, 6.0f);
+    a1 = min_nd(a1, 6.0f);
+    const uint32_t e0 = __float_as_uint(a0) & 0x7F800000u, e1 = __float_as_uint(a1) & 0x7F800000u;
+    const uint32_t s0 = (e0 > 0x3F800000u ? e0 : 0x3F800000u) - 0x00800000u;
+    const uint32_t s1 = (e1 > 0x3F800000u ? e1 : 0x3F800000u) - 0x00800000u;
+    const uint64_t SP = pack2(__uint_as_float(s0), __uint_as_float(s1));
+    const uint64_t INV = pack2(__uint_as_float(0x7F000000u - s0), __uint_as_float(0x7F000000u - s1));
+    const uint64_t T = mul2(pack2(a0, a1), INV);
+    float t0, t1;
+    unpack2(T, t0, t1);
+    const uint64_t FL = pack2(floorf(t0), floorf(t1));
+    const uint64_t P = mul2(sub2(T, FL), pack2(16777216.0f, 16777216.0f));
+    float p0, p1;
+    unpack2(P, p0, p1);
+    const uint64_t UP = pack2(lt_one(static_cast<float>(w0 >> 8), p0), lt_one(static_cast<float>(w1 >> 8), p1));
+    unpack2(mul2(add2(FL, UP), SP), g0, g1);
 }
 
 // ---- exact division from a reciprocal ---------------------------------------------------
