@@ -5,14 +5,18 @@ One step = one pass of the whole path over the LLM-shaped bf16 sweep
 with 0.1% outlier channels x100; seed 4):
   1. W1  SR + error feedback, 1x16            (fp32 residual read + written)
   2. W2  SR + error feedback, 16x16
-  3. A   four-over-six MAE, bound 256, 1x16 rowwise, per-tensor amax computed
-  4. W1  four-over-six MAE, bound 256, 16x16 rowwise + columnwise, amax computed
-  5. W2  four-over-six MAE, bound 256, 16x16 rowwise + columnwise, amax computed
+  3. A   per-tensor amax, then four-over-six MAE, bound 256, 1x16 rowwise
+  4. W1  per-tensor amax, then four-over-six MAE, bound 256, 16x16 rowwise + columnwise
+  5. W2  the same as 4
   6. A   round-to-nearest, 1x16
   7. W2  stochastic rounding, 1x16
   8. A   dequantize (codes of 3) to bf16
-Metric: algorithmic GB/s (bytes read + written once each, amax passes counted
-with their real extra read) and Gelem/s, as a fraction of measured HBM peak.
+The amax passes are separate nvfp4_amax calls whose result the quantize call
+takes as given: the same two kernels the quantize call runs by itself with a
+computed amax, timed apart.  Metric: algorithmic GB/s (bytes read + written
+once each, amax passes counted with their real extra read) and Gelem/s
+(elements quantized or dequantized), as a fraction of measured HBM peak; the
+roofline line is for the kernel with the largest time per step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
@@ -54,22 +58,25 @@ def parse():
 WORKLOAD = ("c5 LLM-shaped sweep, bf16: W1[4096,14336], W2[14336,4096] ~ 0.02*N(0,1), "
             "A[16384,4096] ~ Student-t(4) with 4 outlier channels x100 (seed 4); SR+EF 1x16 "
             "and 16x16 (seed 0, step t), four-over-six MAE bound 256 (1x16 rowwise on A, 16x16 "
-            "row+col on W1/W2, per-tensor amax computed), RTN, SR, dequantize")
+            "row+col on W1/W2, per-tensor amax computed by a separate amax call), RTN, SR, dequantize")
 
 
 def step_plan(M1, K1, M2, K2, Ma, Ka):
-    """(name, elements, algorithmic bytes) per call of one step."""
+    """(call, kernel, elements, algorithmic bytes) per call of one step."""
     e1, e2, ea = M1 * K1, M2 * K2, Ma * Ka
     q = 0.5 + 1 / 16                       # codes + scales per element
     return [
-        ("W1 SR+EF 1x16", e1, e1 * (2 + 4 + 4 + q)),
-        ("W2 SR+EF 16x16", e2, e2 * (2 + 4 + 4 + q)),
-        ("A 4o6 1x16 (amax computed)", ea, ea * (2 + 2 + q)),
-        ("W1 4o6 16x16 row+col (amax computed)", e1, e1 * (2 + 2 + 2 * q)),
-        ("W2 4o6 16x16 row+col (amax computed)", e2, e2 * (2 + 2 + 2 * q)),
-        ("A RTN 1x16", ea, ea * (2 + q)),
-        ("W2 SR 1x16", e2, e2 * (2 + q)),
-        ("A dequantize", ea, ea * (q + 2)),
+        ("W1 SR+EF 1x16", "k_rows<bf16, plain, SR, EF>", e1, e1 * (2 + 4 + 4 + q)),
+        ("W2 SR+EF 16x16", "k_band16<bf16, plain, SR, EF>", e2, e2 * (2 + 4 + 4 + q)),
+        ("A amax", "k_amax_tensor<bf16>", 0, ea * 2),
+        ("A 4o6 1x16", "k_rows<bf16, MAE>", ea, ea * (2 + q)),
+        ("W1 amax", "k_amax_tensor<bf16>", 0, e1 * 2),
+        ("W1 4o6 16x16 row+col", "k_tile_t<bf16, MAE>", e1, e1 * (2 + 2 * q)),
+        ("W2 amax", "k_amax_tensor<bf16>", 0, e2 * 2),
+        ("W2 4o6 16x16 row+col", "k_tile_t<bf16, MAE>", e2, e2 * (2 + 2 * q)),
+        ("A RTN 1x16", "k_rows<bf16, plain, RTN>", ea, ea * (2 + q)),
+        ("W2 SR 1x16", "k_rows<bf16, plain, SR>", e2, e2 * (2 + q)),
+        ("A dequantize", "k_dequant<bf16>", ea, ea * (q + 2)),
     ]
 
 
@@ -174,8 +181,8 @@ def cpu_baseline(sample_rows=1024, repeats=1):
         oracle.dequantize(qa["codes"], qa["scales"], *A.shape, gamax_mode=oracle.GAMAX_TENSOR_GIVEN,
                           gamax=qa["gamax"], scale_bound=256.0)
     dt = (time.perf_counter() - t0) / repeats
-    total_bytes = sum(b for _, _, b in plan)
-    total_elems = sum(e for _, e, _ in plan)
+    total_bytes = sum(b for _, _, _, b in plan)
+    total_elems = sum(e for _, _, e, _ in plan)
     return {"value": total_bytes / dt / GB, "unit": "GB/s", "gelem_per_s": total_elems / dt / GB,
             "cores": 1, "kind": "oracle", "seconds_per_sample_step": dt,
             "sample": f"first {sample_rows} rows of W1, W2 and A (every call of the step), "
@@ -226,8 +233,8 @@ def run_gpu(args, rank, world, local_rank):
     W1, W2, A = up(c5.W1), up(c5.W2), up(c5.A)
     (M1, K1), (M2, K2), (Ma, Ka) = W1.shape, W2.shape, A.shape
     plan = step_plan(M1, K1, M2, K2, Ma, Ka)
-    bytes_step = sum(b for _, _, b in plan)
-    elems_step = sum(e for _, e, _ in plan)
+    bytes_step = sum(b for _, _, _, b in plan)
+    elems_step = sum(e for _, _, e, _ in plan)
 
     u8 = lambda *s: torch.empty(s, dtype=torch.uint8, device=dev)   # noqa: E731
     f32 = lambda *s: torch.empty(s, dtype=torch.float32, device=dev)  # noqa: E731
@@ -254,13 +261,16 @@ def run_gpu(args, rank, world, local_rank):
                                       codes=o["c1"], scales=o["s1"]),
             lambda: nv.nvfp4_quantize(W2, block="16x16", rounding="sr", residual=R2, seed=0, step=t,
                                       codes=o["c2"], scales=o["s2"]),
-            lambda: nv.nvfp4_quantize(A, gamax_mode="tensor", gamax=o["ga"], err_mode="mae",
+            lambda: nv.nvfp4_amax(A, out=o["ga"]),
+            lambda: nv.nvfp4_quantize(A, gamax_mode="tensor_given", gamax=o["ga"], err_mode="mae",
                                       scale_bound=256.0, codes=o["ca"], scales=o["sa"]),
-            lambda: nv.nvfp4_quantize(W1, block="16x16", gamax_mode="tensor", gamax=o["g1"],
+            lambda: nv.nvfp4_amax(W1, out=o["g1"]),
+            lambda: nv.nvfp4_quantize(W1, block="16x16", gamax_mode="tensor_given", gamax=o["g1"],
                                       err_mode="mae", scale_bound=256.0, colwise=True,
                                       codes=o["c1r"], scales=o["s1r"], codes_col=o["c1c"],
                                       scales_col=o["s1c"]),
-            lambda: nv.nvfp4_quantize(W2, block="16x16", gamax_mode="tensor", gamax=o["g2"],
+            lambda: nv.nvfp4_amax(W2, out=o["g2"]),
+            lambda: nv.nvfp4_quantize(W2, block="16x16", gamax_mode="tensor_given", gamax=o["g2"],
                                       err_mode="mae", scale_bound=256.0, colwise=True,
                                       codes=o["c2r"], scales=o["s2r"], codes_col=o["c2c"],
                                       scales_col=o["s2c"]),
@@ -309,13 +319,13 @@ def run_gpu(args, rank, world, local_rank):
     barrier()
     clocks = clocks_sampler_stop(proc, fh, clk_path, local_rank)
     total_ms = start.elapsed_time(stop)
-    ran = [not args.only or args.only in name for name, _, _ in plan]
+    ran = [not args.only or args.only in name for name, _, _, _ in plan]
     per_call_ms = [statistics.mean(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(nsteps))
                    if ran[i] else 0.0 for i in range(len(plan))]
     if args.only:
-        plan = [p if r else (p[0], 0, 0) for p, r in zip(plan, ran)]
-        bytes_step = sum(b for _, _, b in plan)
-        elems_step = sum(e for _, e, _ in plan)
+        plan = [p if r else (p[0], p[1], 0, 0) for p, r in zip(plan, ran)]
+        bytes_step = sum(b for _, _, _, b in plan)
+        elems_step = sum(e for _, _, e, _ in plan)
     if dist is not None:
         tt = torch.tensor([total_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -371,19 +381,29 @@ def run_gpu(args, rank, world, local_rank):
 
     if rank != 0:
         return
-    # ---- roofline of the dominant kernel ----
-    dom = int(np.argmax(per_call_ms))
-    name, elems, nbytes = plan[dom]
+    # ---- roofline of the dominant kernel: the largest total time per step ----
+    per_kernel = {}
+    for (_, kern, _, b), ms in zip(plan, per_call_ms):
+        if ms > 0:
+            tot = per_kernel.setdefault(kern, [0.0, 0.0, 0])
+            tot[0] += ms
+            tot[1] += b
+            tot[2] += 1
+    kern = max(per_kernel, key=lambda k: per_kernel[k][0])
+    ms_k, bytes_k, launches_k = per_kernel[kern]
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks else 6800.0
-    achieved = nbytes / (per_call_ms[dom] * 1e-3) / GB
+    achieved = (bytes_k / launches_k) / (ms_k / launches_k * 1e-3) / GB
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(name),
-                "kernel": name, "peak_source": "measured" if peaks else "fallback",
-                "algorithmic_bytes_per_launch": int(nbytes), "ms_per_launch": round(per_call_ms[dom], 4)}
-    calls = [{"call": n, "ms": round(ms, 4), "GB/s": round(b / (ms * 1e-3) / GB, 1),
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(kern),
+                "kernel": kern, "launches_per_step": launches_k,
+                "peak_source": "measured" if peaks else "fallback",
+                "algorithmic_bytes_per_launch": int(bytes_k / launches_k),
+                "ms_per_launch": round(ms_k / launches_k, 4),
+                "share_of_step": round(ms_k / sum(per_call_ms), 3)}
+    calls = [{"call": n, "kernel": k, "ms": round(ms, 4), "GB/s": round(b / (ms * 1e-3) / GB, 1),
               "frac_of_peak": round(b / (ms * 1e-3) / GB / peak, 3)}
-             for (n, _, b), ms in zip(plan, per_call_ms) if ms > 0]
+             for (n, k, _, b), ms in zip(plan, per_call_ms) if ms > 0]
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline()
@@ -402,8 +422,7 @@ def run_gpu(args, rank, world, local_rank):
                          "re-read within 129 MB of other traffic, except the second (quantize) "
                          "pass after an amax pass over the same tensor",
                    "parallelism": f"{world} independent replica(s), no data-path collective"},
-        "gpu_launches": nsteps * sum(n for (name, _, _), n in zip(plan, (1, 1, 2, 2, 2, 1, 1, 1))
-                                     if not args.only or args.only in name),
+        "gpu_launches": nsteps * sum(1 for name, _, _, _ in plan if not args.only or args.only in name),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "calls": calls,
     }
     print(json.dumps(line), flush=True)

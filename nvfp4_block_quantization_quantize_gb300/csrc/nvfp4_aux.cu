@@ -35,16 +35,74 @@ __device__ __forceinline__ float warp_max(float m) {
     return m;
 }
 
-// Per-tensor amax; *out must hold +0 on entry.  The maximum of non-negative
+// Max of |x (+ r)| over one 8-element vector: 16 (bf16) or 32 (fp32) bytes
+// of x, 32 bytes of the residual.
+template <int DT, bool EF>
+struct AmaxVec {
+    uint4 x[DT == NVFP4_BF16 ? 1 : 2];
+    uint4 r[EF ? 2 : 1];
+    __device__ void load(const void* xp, const float* rp, int64_t v) {
+        const uint4* px = static_cast<const uint4*>(xp) + v * (DT == NVFP4_BF16 ? 1 : 2);
+#pragma unroll
+        for (int k = 0; k < (DT == NVFP4_BF16 ? 1 : 2); ++k) x[k] = __ldg(px + k);
+        if (EF) {
+            const uint4* pr = reinterpret_cast<const uint4*>(rp) + v * 2;
+            r[0] = __ldg(pr);
+            r[1] = __ldg(pr + 1);
+        }
+    }
+    __device__ float absmax() const {
+        float y[8];
+        if (DT == NVFP4_BF16) {
+            const uint32_t w[4] = {x[0].x, x[0].y, x[0].z, x[0].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                y[2 * i] = __uint_as_float(w[i] << 16);
+                y[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                y[4 * k] = __uint_as_float(x[k].x);
+                y[4 * k + 1] = __uint_as_float(x[k].y);
+                y[4 * k + 2] = __uint_as_float(x[k].z);
+                y[4 * k + 3] = __uint_as_float(x[k].w);
+            }
+        }
+        if (EF) {
+            const uint32_t rw[8] = {r[0].x, r[0].y, r[0].z, r[0].w, r[1].x, r[1].y, r[1].z, r[1].w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = add_rn(y[i], __uint_as_float(rw[i]));
+        }
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = max_nd(m, fabsf(y[i]));
+        return m;
+    }
+};
+
+// Per-tensor amax; *out must hold +0 on entry.  The tensor is read as 8-element
+// vectors, kAmaxUnroll per thread and step, all loads issued before the max
+// (consecutive lanes on consecutive vectors).  The maximum of non-negative
 // floats orders like their bit patterns, so an unsigned atomic max is exact.
+constexpr int kAmaxUnroll = 4;
+
 template <int DT, bool EF>
 __global__ void __launch_bounds__(kThreads) k_amax_tensor(const void* x, const float* res,
-                                                          int64_t nblk, float* out) {
+                                                          int64_t nvec, float* out) {
     __shared__ float part[kThreads / 32];
     float m = 0.0f;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblk; b += stride)
-        m = max_nd(m, block_absmax<DT, EF>(x, res, b * 16));
+    const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x * kAmaxUnroll;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * kAmaxUnroll + threadIdx.x; base < nvec;
+         base += step) {
+        AmaxVec<DT, EF> v[kAmaxUnroll];
+#pragma unroll
+        for (int k = 0; k < kAmaxUnroll; ++k)
+            if (base + k * kThreads < nvec) v[k].load(x, res, base + k * kThreads);
+#pragma unroll
+        for (int k = 0; k < kAmaxUnroll; ++k)
+            if (base + k * kThreads < nvec) m = max_nd(m, v[k].absmax());
+    }
     m = warp_max(m);
     if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = m;
     __syncthreads();
@@ -166,15 +224,15 @@ int launch_amax(const void* x, int64_t M, int64_t K, int dtype, const float* res
     const bool ef = residual != nullptr;
     if (mode == NVFP4_GAMAX_TENSOR) {
         cudaMemsetAsync(out, 0, sizeof(float), s);
-        const int64_t nblk = M * (K / 16);
-        if (nblk > 0) {
-            const int g = grid_for(nblk);
+        const int64_t nvec = M * (K / 8);
+        if (nvec > 0) {
+            const int g = grid_for((nvec + kAmaxUnroll - 1) / kAmaxUnroll);
             if (dtype == NVFP4_BF16) {
-                if (ef) k_amax_tensor<NVFP4_BF16, true><<<g, kThreads, 0, s>>>(x, residual, nblk, out);
-                else k_amax_tensor<NVFP4_BF16, false><<<g, kThreads, 0, s>>>(x, residual, nblk, out);
+                if (ef) k_amax_tensor<NVFP4_BF16, true><<<g, kThreads, 0, s>>>(x, residual, nvec, out);
+                else k_amax_tensor<NVFP4_BF16, false><<<g, kThreads, 0, s>>>(x, residual, nvec, out);
             } else {
-                if (ef) k_amax_tensor<NVFP4_F32, true><<<g, kThreads, 0, s>>>(x, residual, nblk, out);
-                else k_amax_tensor<NVFP4_F32, false><<<g, kThreads, 0, s>>>(x, residual, nblk, out);
+                if (ef) k_amax_tensor<NVFP4_F32, true><<<g, kThreads, 0, s>>>(x, residual, nvec, out);
+                else k_amax_tensor<NVFP4_F32, false><<<g, kThreads, 0, s>>>(x, residual, nvec, out);
             }
         }
     } else {
