@@ -134,7 +134,10 @@ struct TileRing {
 template <int DT, int ERR>
 __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
     using Rg = TileRing<DT>;
-    __shared__ Cand tab[128];
+    __shared__ float tenc[128];                 // encode reciprocal of every scale byte
+    // per thread and candidate: the error value magnitude |dq| of each grid
+    // index k, [candidate][k][thread] so a warp's lookups are conflict-free
+    __shared__ float dqt[2][8][kTileThreads];
     // per-thread row sums of both candidates and the 16 rows' code words,
     // [row][thread] so a warp's accesses are conflict-free
     __shared__ float sR6[16][kTileThreads], sR4[16][kTileThreads];
@@ -149,7 +152,9 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
         global_scales(g.A, a.bound, g.Senc, g.Sdec);
     }
     const float C = mul_rn(6.0f, a.bound);
-    fill_cand_table(tab, g.Sdec, g.A, C);
+    for (int i = threadIdx.x; i < 128; i += blockDim.x)
+        tenc[i] = min_nd(div_rn(1.0f, mul_rn(e4m3_decode(static_cast<uint32_t>(i)), g.Sdec)), FLT_MAX);
+    __syncthreads();
 
     const int64_t band = blockIdx.x;
     const int tid = threadIdx.x;
@@ -191,26 +196,50 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
     const float s6f = block_s6f<true>(b, g.Senc);
     const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
     const uint32_t sf4 = e4m3_encode(min_nd(mul_rn(s6f, 1.5f), 448.0f));
-    const Cand c6 = tab[sf6], c4 = tab[sf4];
-    const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
+    const float enc6 = tenc[sf6], enc4 = tenc[sf4];
+    // |dq| = ((G[k] * d) * A) / (6 * bound) of each grid magnitude G[k]: the
+    // error value of a code with index k is +-|dq| with the sign of its y, so
+    // |dq - y| = | |dq| - |y| | exactly (and likewise the square)
+    {
+        const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
+        const float G[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            dqt[0][k][tid] = div_rn(mul_rn(mul_rn(G[k], d6), g.A), C);
+            dqt[1][k][tid] = div_rn(mul_rn(mul_rn(G[k], d4), g.A), C);
+        }
+    }
 
     // pass 1: per-element errors; row sums to shared memory, column sums in
     // registers, both accumulated in element order
     float F6[16], F4[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
+    auto candidate = [&](const float* y, float enc, int c, uint32_t& w0, uint32_t& w1, float* e) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = mul_rn(y[i], enc);
+        w0 = e2m1_encode8(v);
+        w1 = e2m1_encode8(v + 8);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t k = ((i < 8 ? w0 : w1) >> (4 * (i & 7))) & 7u;
+            const float diff = sub_rn(dqt[c][k][tid], fabsf(y[i]));
+            e[i] = (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff);
+        }
+    };
 #pragma unroll 1
     for (int r = 0; r < 16; ++r) {
         next_row(16 + r, y);
         float e[16];
         uint32_t w0, w1;
-        candidate16<ERR>(y, c6, d6, g.A, C, w0, w1, e);
+        candidate(y, enc6, 0, w0, w1, e);
         sW[0][r][tid] = w0;
         sW[1][r][tid] = w1;
         sR6[r][tid] = seq_sum16(e);
 #pragma unroll
         for (int i = 0; i < 16; ++i) F6[i] = add_rn(F6[i], e[i]);
-        candidate16<ERR>(y, c4, d4, g.A, C, w0, w1, e);
+        candidate(y, enc4, 1, w0, w1, e);
         sW[2][r][tid] = w0;
         sW[3][r][tid] = w1;
         sR4[r][tid] = seq_sum16(e);
