@@ -8,6 +8,8 @@
 // element-order error sums, the width-16 tree, strict err4 < err6).
 #pragma once
 
+#include <type_traits>
+
 #include "nvfp4_device.cuh"
 
 namespace nvfp4 {
@@ -245,11 +247,52 @@ __device__ __forceinline__ float seq_sum16(const float* e) {
     return E;
 }
 
-// Per-tensor candidate table: entry sf holds the candidate data of scale byte
-// sf (every block scale is a non-negative E4M3 byte <= 0x7E).
-__device__ __forceinline__ void fill_cand_table(Cand* tab, float Sdec, float A, float C) {
-    for (int i = threadIdx.x; i < 128; i += blockDim.x) tab[i] = make_cand(static_cast<uint32_t>(i), Sdec, A, C);
+// Per-tensor four-over-six table, for a global scale shared by the tensor:
+// enc[sf] = min(1/(dec(sf) * S_dec), FLT_MAX) and dq[k][sf] = ((G[k] * dec(sf))
+// * A) / (6 * bound), the error-value magnitude of grid index k under scale
+// byte sf (every block scale is a non-negative E4M3 byte <= 0x7E).  A code
+// with index k stands for +-dq[k][sf] with the sign of its y (y * enc keeps
+// y's sign), so its error |dq - y| is | dq[k][sf] - |y| | exactly, and the
+// square likewise.  The row stride 132 spreads the 8 rows of one scale byte
+// over distinct banks.
+constexpr int kDqStride = 132;
+struct O6Tab {
+    float enc[128];
+    float dq[8 * kDqStride];
+};
+
+// the shared table of a kernel instance, or nothing when it has no four-over-six
+struct NoTab {};
+template <int ERR>
+using O6TabOf = typename std::conditional<ERR != NVFP4_ERR_NONE, O6Tab, NoTab>::type;
+
+__device__ __forceinline__ void fill_o6_table(O6Tab* tab, float Sdec, float A, float C) {
+    const float G[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+        const float d = e4m3_decode(static_cast<uint32_t>(i));
+        tab->enc[i] = min_nd(div_rn(1.0f, mul_rn(d, Sdec)), FLT_MAX);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) tab->dq[k * kDqStride + i] = div_rn(mul_rn(mul_rn(G[k], d), A), C);
+    }
     __syncthreads();
+}
+
+// One candidate over 16 values from the table: codes of y * enc and the
+// per-element errors (dq: the table column of the candidate's scale byte).
+template <int ERR>
+__device__ __forceinline__ void candidate16_tab(const float* y, float enc, const float* dq, uint32_t& w0,
+                                                uint32_t& w1, float* e) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = mul_rn(y[i], enc);
+    w0 = e2m1_encode8(v);
+    w1 = e2m1_encode8(v + 8);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t k = ((i < 8 ? w0 : w1) >> (4 * (i & 7))) & 7u;
+        const float diff = sub_rn(dq[k * kDqStride], fabsf(y[i]));
+        e[i] = (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff);
+    }
 }
 
 // Four-over-six for one 16-value group (1x16 block, or one row of a 16x16 tile
@@ -258,20 +301,26 @@ __device__ __forceinline__ void fill_cand_table(Cand* tab, float Sdec, float A, 
 // a 1x16 block, the width-16 tree over the tile's 16 rows for a 16x16 tile.
 template <int ERR, class TileSums>
 __device__ __forceinline__ void four_over_six16(const float* y, float b, const GScale& g, float C,
-                                                const Cand* tab, uint32_t& w0, uint32_t& w1,
+                                                const O6Tab* tab, uint32_t& w0, uint32_t& w1,
                                                 uint32_t& sf, float& d, TileSums tile_sums) {
     const float s6f = block_s6f<true>(b, g.Senc);
     const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
     const uint32_t sf4 = e4m3_encode(min_nd(mul_rn(s6f, 1.5f), 448.0f));
-    const Cand c6 = tab ? tab[sf6] : make_cand(sf6, g.Sdec, g.A, C);
-    const Cand c4 = tab ? tab[sf4] : make_cand(sf4, g.Sdec, g.A, C);
     const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
     uint32_t a0, a1, b0, b1;
-    float e[16];
-    candidate16<ERR>(y, c6, d6, g.A, C, a0, a1, e);
-    float E6 = seq_sum16(e);
-    candidate16<ERR>(y, c4, d4, g.A, C, b0, b1, e);
-    float E4 = seq_sum16(e);
+    float e[16], E6, E4;
+    if (tab) {                                  // per-tensor global scale: table lookups
+        candidate16_tab<ERR>(y, tab->enc[sf6], tab->dq + sf6, a0, a1, e);
+        E6 = seq_sum16(e);
+        candidate16_tab<ERR>(y, tab->enc[sf4], tab->dq + sf4, b0, b1, e);
+        E4 = seq_sum16(e);
+    } else {                                    // per-row global scale: candidates per block
+        const Cand c6 = make_cand(sf6, g.Sdec, g.A, C), c4 = make_cand(sf4, g.Sdec, g.A, C);
+        candidate16<ERR>(y, c6, d6, g.A, C, a0, a1, e);
+        E6 = seq_sum16(e);
+        candidate16<ERR>(y, c4, d4, g.A, C, b0, b1, e);
+        E4 = seq_sum16(e);
+    }
     tile_sums(E6, E4);
     const bool pick4 = E4 < E6;                 // ties and NaN keep map-to-6
     w0 = pick4 ? b0 : a0;
@@ -283,7 +332,7 @@ __device__ __forceinline__ void four_over_six16(const float* y, float b, const G
 // TREE: the tile's 16 rows are the 16 lanes of the caller's half warp.
 template <int ERR, bool TREE>
 __device__ __forceinline__ void four_over_six16(const float* y, float b, const GScale& g, float C,
-                                                const Cand* tab, uint32_t& w0, uint32_t& w1,
+                                                const O6Tab* tab, uint32_t& w0, uint32_t& w1,
                                                 uint32_t& sf, float& d) {
     four_over_six16<ERR>(y, b, g, C, tab, w0, w1, sf, d, [](float& E6, float& E4) {
         if (TREE) {

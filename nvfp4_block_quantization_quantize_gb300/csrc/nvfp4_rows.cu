@@ -26,7 +26,7 @@ constexpr int kThreads = 256;
 // when !live (a group past the tensor's last column block).
 template <int DT, int ERR, int RND, bool EF, bool GS, class TileAmax, class TileSums>
 __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool live, float* y,
-                                           const GScale& g, float C, const Cand* tab,
+                                           const GScale& g, float C, const O6Tab* tab,
                                            const float* rt, uint64_t idx_base, int64_t bpr,
                                            TileAmax tile_amax, TileSums tile_sums) {
     GScale gb = g;
@@ -83,7 +83,7 @@ template <int DT, int ERR, int RND, bool EF, bool GS>
 __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
     using St = RowsStage<DT, EF>;
     extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ Cand tab[ERR != NVFP4_ERR_NONE ? 128 : 1];
+    __shared__ O6TabOf<ERR> tab;
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
     if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
     const int64_t bpr = a.K / 16;
@@ -94,10 +94,12 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
         global_scales(g.A, a.bound, g.Senc, g.Sdec);
     }
     const float C = mul_rn(6.0f, a.bound);
-    const Cand* tp = nullptr;
-    if (ERR != NVFP4_ERR_NONE && a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
-        fill_cand_table(tab, g.Sdec, g.A, C);
-        tp = tab;
+    const O6Tab* tp = nullptr;
+    if constexpr (ERR != NVFP4_ERR_NONE) {
+        if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
+            fill_o6_table(&tab, g.Sdec, g.A, C);
+            tp = &tab;
+        }
     }
     const uint64_t idx_base = static_cast<uint64_t>(a.row_offset) * static_cast<uint64_t>(a.K);
     const int tid = threadIdx.x;
@@ -174,7 +176,7 @@ template <int DT, int ERR, int RND, bool EF, bool GS>
 __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
     using St = RowsStage<DT, EF>;
     extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ Cand tab[ERR != NVFP4_ERR_NONE ? 128 : 1];
+    __shared__ O6TabOf<ERR> tab;
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
     __shared__ float red[2][8][16];                                   // [step parity][warp][tile]
     __shared__ float esum[ERR != NVFP4_ERR_NONE ? 2 : 1][2][16][16];  // [parity][cand][row][tile]
@@ -188,10 +190,10 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
         global_scales(g.A, a.bound, g.Senc, g.Sdec);
     }
     const float C = mul_rn(6.0f, a.bound);
-    const Cand* tp = nullptr;
-    if (ERR != NVFP4_ERR_NONE) {
-        fill_cand_table(tab, g.Sdec, g.A, C);
-        tp = tab;
+    const O6Tab* tp = nullptr;
+    if constexpr (ERR != NVFP4_ERR_NONE) {
+        fill_o6_table(&tab, g.Sdec, g.A, C);
+        tp = &tab;
     }
     const uint64_t idx_base = static_cast<uint64_t>(a.row_offset) * static_cast<uint64_t>(a.K);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

@@ -39,7 +39,7 @@ constexpr int kYsStride = kTileCols + 4;
 template <int DT, int BLK, int ERR, bool GS>
 __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
     __shared__ float ys[16 * kYsStride];
-    __shared__ Cand tab[ERR != NVFP4_ERR_NONE ? 128 : 1];
+    __shared__ O6TabOf<ERR> tab;
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
     if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
     const int64_t band = blockIdx.x;
@@ -58,8 +58,11 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
         global_scales(g.A, a.bound, g.Senc, g.Sdec);
     }
     const float C = mul_rn(6.0f, a.bound);
-    if (ERR != NVFP4_ERR_NONE) fill_cand_table(tab, g.Sdec, g.A, C);
-    const Cand* tp = ERR != NVFP4_ERR_NONE ? tab : nullptr;
+    const O6Tab* tp = nullptr;
+    if constexpr (ERR != NVFP4_ERR_NONE) {
+        fill_o6_table(&tab, g.Sdec, g.A, C);
+        tp = &tab;
+    }
 
     const int64_t e0 = row * a.K + cb * 16;
     float y[16];
