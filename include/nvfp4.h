@@ -53,8 +53,12 @@ enum nvfp4_dtype { NVFP4_F32 = 0, NVFP4_BF16 = 1 };
  * whose scale is the same for x and x^T [4o6 PR, What; Design] */
 enum nvfp4_block { NVFP4_BLOCK_1X16 = 0, NVFP4_BLOCK_16X16 = 1 };
 
-/* element rounding: nearest (ties to even) or stochastic [fp4-train, Method] */
-enum nvfp4_round { NVFP4_RTN = 0, NVFP4_SR = 1 };
+/* element rounding: nearest (ties to even) or stochastic [fp4-train, Method];
+ * NVFP4_RTN_STD is nearest rounding with the standard NVFP4 block-scale
+ * association b * (S_enc * (1/6)) ("Add NVFP4 four-over-six (row-wise)
+ * quantization to the training prototype", Two load-bearing numeric details:
+ * the recipe's gradient-side quantizer) instead of (b / 6) * S_enc. */
+enum nvfp4_round { NVFP4_RTN = 0, NVFP4_SR = 1, NVFP4_RTN_STD = 2 };
 
 /* global (second-level) scale [4o6 PR, What]:
  *   NONE          S_enc = S_dec = 1 (the fp4-train recipe); gamax unused
@@ -86,9 +90,13 @@ enum nvfp4_status { NVFP4_OK = 0, NVFP4_EINVAL = 1, NVFP4_ECUDA = 2 };
  * Per block of y = x (+ residual when residual != NULL):
  *   b    = max |y| over the block (NaN dropped)
  *   s6f  = (b / 6) * S_enc;  sf6 = E4M3(min(s6f, 448))              [fp4-train, Method]
+ *        (NVFP4_RTN_STD: s6f = b * (S_enc * (1/6)), 1/6 the nearest fp32)
  *   plain (err_mode NONE): code = round(y / (dec(sf6) * S_dec)), nearest or
  *        stochastic with the Philox4x32-10 draw keyed on (seed, step, global
- *        index (row_offset + r) * K + c); a zero scale gives zero codes.
+ *        index (row_offset + r) * K + c) of the element in x -- for the
+ *        columnwise output too, so x and x^T round each element alike
+ *        ("Stable FP4 Training via Transposition-Invariant Block
+ *        Quantization", abstract); a zero scale gives zero codes.
  *   four-over-six (MAE/MSE): also sf4 = E4M3(min(1.5 * s6f, 448)); each
  *        candidate encodes y * min(1/(dec(sf)*S_dec), FLT_MAX) and is scored by
  *        the error of ((q*dec(sf))*A)/(6*bound) against y, summed in element
@@ -99,7 +107,7 @@ enum nvfp4_status { NVFP4_OK = 0, NVFP4_EINVAL = 1, NVFP4_ECUDA = 2 };
  * Arguments
  *   x            device [M,K], dtype F32 or BF16
  *   block        NVFP4_BLOCK_1X16 or NVFP4_BLOCK_16X16
- *   rounding     NVFP4_RTN or NVFP4_SR
+ *   rounding     NVFP4_RTN, NVFP4_SR or NVFP4_RTN_STD
  *   residual     NULL or device [M,K] fp32 (error feedback, in place)
  *   seed, step   SR key and step (unused by RTN)
  *   row_offset   global row index of x's row 0 (SR counter base; 0 for a
@@ -116,9 +124,10 @@ enum nvfp4_status { NVFP4_OK = 0, NVFP4_EINVAL = 1, NVFP4_ECUDA = 2 };
  * columnwise output; a required pointer is NULL or a pointer is not 16-byte
  * aligned; an enum is out of range; ROW modes with 16x16 or columnwise
  * (a row-scaled tensor has no columnwise form [4o6 PR, What]); four-over-six
- * with SR, a residual, gamax NONE or a bound other than 256/448 (the recipe is
- * nearest-rounding only [4o6 PR, What]); columnwise with SR or a residual; a
- * bound outside (0, 448]; only one of codes_col / scales_col given.
+ * with SR or RTN_STD, a residual, gamax NONE or a bound other than 256/448
+ * (the recipe is nearest-rounding only [4o6 PR, What]); columnwise with a
+ * residual (one residual cannot serve two quantizations); a bound outside
+ * (0, 448]; only one of codes_col / scales_col given.
  */
 int nvfp4_quantize(const void* x, int64_t M, int64_t K, int dtype, int block, int rounding,
                    float* residual, uint64_t seed, uint64_t step, int64_t row_offset,

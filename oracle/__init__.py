@@ -30,7 +30,7 @@ _lib = None
 
 F32, BF16 = 0, 1
 BLOCK_1X16, BLOCK_16X16 = 0, 1
-RTN, SR = 0, 1
+RTN, SR, RTN_STD = 0, 1, 2
 GAMAX_NONE, GAMAX_TENSOR, GAMAX_ROW, GAMAX_TENSOR_GIVEN, GAMAX_ROW_GIVEN = 0, 1, 2, 3, 4
 ERR_NONE, ERR_MAE, ERR_MSE = 0, 1, 2
 

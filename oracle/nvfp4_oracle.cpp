@@ -45,6 +45,12 @@ struct GScale {
  * (block_amax / 6) * S_enc association; [4o6 PR, Design] the 448 cap). */
 float block_s6f(float b, float S_enc) { return (b / 6.0f) * S_enc; }
 
+/* The standard NVFP4 association the four-over-six page contrasts with its own
+ * ([4o6 PR, Two load-bearing numeric details]): b * (S_enc * (1/6)), with 1/6
+ * the fp32 constant nearest to it.  It rounds differently from (b / 6) * S_enc
+ * on some blocks. */
+float block_s6f_std(float b, float S_enc) { return b * (S_enc * (1.0f / 6.0f)); }
+
 /* Error sum of one candidate over a block ([4o6 PR, Design]): elements of a
  * 16-group are added strictly in order 0..15 starting from 0; a 16x16 tile
  * combines its 16 row sums with the fixed width-16 tree
@@ -68,6 +74,7 @@ float block_error(const float* e, int n) {
 struct PlaneArgs {
     const float* y;           /* R x C fp32 plane */
     int64_t R, C;
+    bool transposed;          /* the plane is x^T: SR draws are keyed on x's index */
     int block, rounding, err_mode;
     float bound;
     const GScale* gs;         /* per row of the plane (all equal for per-tensor) */
@@ -91,7 +98,7 @@ void quantize_block(const PlaneArgs& P, const int64_t* rows, const int64_t* cols
     float b = 0.0f;
     for (int i = 0; i < n; ++i) b = max_nd(b, std::fabs(P.y[rows[i] * P.C + cols[i]]));
 
-    const float s6f = block_s6f(b, g.S_enc);
+    const float s6f = (P.rounding == ORC_RTN_STD) ? block_s6f_std(b, g.S_enc) : block_s6f(b, g.S_enc);
     const uint8_t sf6 = orc_e4m3_encode(min_nd(s6f, 448.0f));
     const float d6 = orc_e4m3_decode(sf6);
 
@@ -107,11 +114,18 @@ void quantize_block(const PlaneArgs& P, const int64_t* rows, const int64_t* cols
             const float yv = P.y[rows[i] * P.C + cols[i]];
             if (D == 0.0f) { code[i] = 0; continue; }
             const float v = yv / D;
-            if (P.rounding == ORC_RTN) {
+            if (P.rounding != ORC_SR) {
                 code[i] = orc_e2m1_encode_rn(v);
             } else {
-                const uint64_t idx = static_cast<uint64_t>(P.row_offset + rows[i]) *
-                                         static_cast<uint64_t>(P.C) + static_cast<uint64_t>(cols[i]);
+                /* the draw is keyed on the element's global index in x (row-major,
+                 * row_offset rows before this tensor), also for the x^T plane, so
+                 * x and x^T round each element the same way [Stable FP4 Training
+                 * via Transposition-Invariant Block Quantization, abstract] */
+                const int64_t xr = P.transposed ? cols[i] : rows[i];
+                const int64_t xc = P.transposed ? rows[i] : cols[i];
+                const int64_t xK = P.transposed ? P.R : P.C;
+                const uint64_t idx = static_cast<uint64_t>(P.row_offset + xr) * static_cast<uint64_t>(xK) +
+                                     static_cast<uint64_t>(xc);
                 code[i] = orc_e2m1_encode_sr(v, orc_sr_uniform(P.seed, P.step, idx));
             }
         }
@@ -190,7 +204,7 @@ bool args_ok(int64_t M, int64_t K, int dtype, int block, int rounding, const flo
     if (M < 0 || K < 0 || K % 16 != 0) return false;
     if (dtype != ORC_F32 && dtype != ORC_BF16) return false;
     if (block != ORC_BLOCK_1X16 && block != ORC_BLOCK_16X16) return false;
-    if (rounding != ORC_RTN && rounding != ORC_SR) return false;
+    if (rounding != ORC_RTN && rounding != ORC_SR && rounding != ORC_RTN_STD) return false;
     if (gamax_mode < ORC_GAMAX_NONE || gamax_mode > ORC_GAMAX_ROW_GIVEN) return false;
     if (err_mode < ORC_ERR_NONE || err_mode > ORC_ERR_MSE) return false;
     if (!valid_bound(bound)) return false;
@@ -202,7 +216,7 @@ bool args_ok(int64_t M, int64_t K, int dtype, int block, int rounding, const flo
         if (gamax_mode == ORC_GAMAX_NONE) return false;
         if (bound != 256.0f && bound != 448.0f) return false;
     }
-    if (colwise && (rounding != ORC_RTN || residual)) return false;
+    if (colwise && residual) return false;
     return true;
 }
 
@@ -409,7 +423,7 @@ int orc_quantize(const void* x, int64_t M, int64_t K, int dtype, int block, int 
     std::vector<float> dq;
     if (residual) dq.resize(static_cast<size_t>(M * K));
 
-    PlaneArgs P{y.data(), M, K, block, rounding, err_mode, scale_bound, gs.data(),
+    PlaneArgs P{y.data(), M, K, false, block, rounding, err_mode, scale_bound, gs.data(),
                 seed, step, row_offset, codes, scales, residual ? dq.data() : nullptr};
     quantize_plane(P);
 
@@ -424,8 +438,8 @@ int orc_quantize(const void* x, int64_t M, int64_t K, int dtype, int block, int 
         for (int64_t r = 0; r < M; ++r)
             for (int64_t c = 0; c < K; ++c) yt[c * M + r] = y[r * K + c];
         std::vector<GScale> gt(static_cast<size_t>(K > 0 ? K : 1), M > 0 ? gs[0] : GScale{0.0f, 1.0f, 1.0f});
-        PlaneArgs T{yt.data(), K, M, block, rounding, err_mode, scale_bound, gt.data(),
-                    seed, step, 0, codes_col, scales_col, nullptr};
+        PlaneArgs T{yt.data(), K, M, true, block, rounding, err_mode, scale_bound, gt.data(),
+                    seed, step, row_offset, codes_col, scales_col, nullptr};
         quantize_plane(T);
     }
     return 0;

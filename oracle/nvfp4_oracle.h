@@ -41,7 +41,9 @@ extern "C" {
  * the two sides share no file */
 enum { ORC_F32 = 0, ORC_BF16 = 1 };
 enum { ORC_BLOCK_1X16 = 0, ORC_BLOCK_16X16 = 1 };
-enum { ORC_RTN = 0, ORC_SR = 1 };
+/* RTN_STD: round to nearest with the standard NVFP4 block-scale association
+ * b * (S_enc * (1/6)) instead of (b / 6) * S_enc */
+enum { ORC_RTN = 0, ORC_SR = 1, ORC_RTN_STD = 2 };
 enum { ORC_GAMAX_NONE = 0, ORC_GAMAX_TENSOR = 1, ORC_GAMAX_ROW = 2,
        ORC_GAMAX_TENSOR_GIVEN = 3, ORC_GAMAX_ROW_GIVEN = 4 };
 enum { ORC_ERR_NONE = 0, ORC_ERR_MAE = 1, ORC_ERR_MSE = 2 };

@@ -73,6 +73,7 @@ BAD_QUANT = {
     "bad dtype": dict(dtype=7),
     "bad block": dict(block=2),
     "bad rounding": dict(rounding=5),
+    "bad rounding 3": dict(rounding=3),
     "bad gamax mode": dict(gm=9, gamax=A16),
     "bad err mode": dict(err=3, gm=1, gamax=A16),
     "bound zero": dict(bound=0.0),
@@ -84,10 +85,10 @@ BAD_QUANT = {
     "row gamax with 16x16": dict(block=1, gm=2, gamax=A16),
     "row gamax with columnwise": dict(gm=4, gamax=A16, ccol=A16, scol=A16),
     "4o6 with SR": dict(err=1, rounding=1, gm=1, gamax=A16, bound=256.0),
+    "4o6 with standard association": dict(err=1, rounding=2, gm=1, gamax=A16, bound=256.0),
     "4o6 with residual": dict(err=2, residual=A16, gm=1, gamax=A16, bound=256.0),
     "4o6 without global amax": dict(err=1, bound=256.0),
     "4o6 bound 300": dict(err=1, gm=1, gamax=A16, bound=300.0),
-    "columnwise with SR": dict(rounding=1, ccol=A16, scol=A16),
     "columnwise with residual": dict(residual=A16, ccol=A16, scol=A16),
     "x NULL": dict(x=None),
     "codes NULL": dict(codes=None),

@@ -35,6 +35,11 @@ MUTATIONS = {
     "SR counter uses idx, not idx/4": ("const uint64_t blk = idx >> 2;", "const uint64_t blk = idx;"),
     "residual ignores the previous residual": ("residual[i] = y[i] - dq[i];",
                                                "residual[i] = widen(x, dtype, i) - dq[i];"),
+    "standard association grouped like four-over-six": (
+        "return b * (S_enc * (1.0f / 6.0f)); }", "return (b * (1.0f / 6.0f)) * S_enc; }"),
+    "columnwise SR keyed on the x^T index": (
+        "const int64_t xr = P.transposed ? cols[i] : rows[i];\n                const int64_t xc = P.transposed ? rows[i] : cols[i];\n                const int64_t xK = P.transposed ? P.R : P.C;",
+        "const int64_t xr = rows[i];\n                const int64_t xc = cols[i];\n                const int64_t xK = P.C;"),
     "nibbles swapped": ("if (c % 2 == 0) byte = static_cast<uint8_t>((byte & 0xF0) | code);",
                         "if (c % 2 == 1) byte = static_cast<uint8_t>((byte & 0xF0) | code); else if (0) byte = 0;"),
 }

@@ -652,3 +652,106 @@ def test_row_mode_equals_per_row_given():
                             gamax=r["gamax"][i:i + 1], err_mode=oracle.ERR_MAE, scale_bound=256.0)
         assert np.array_equal(s["codes"][0], r["codes"][i])
         assert np.array_equal(s["scales"][0], r["scales"][i])
+
+
+# ---- the standard NVFP4 association (nearest rounding, b * (S_enc * (1/6))) -------------
+def _unpack_codes(c):
+    """[R, C/2] packed bytes -> [R, C] 4-bit codes (even column in the low nibble)."""
+    c = np.asarray(c, np.uint8)
+    out = np.empty((c.shape[0], c.shape[1] * 2), np.uint8)
+    out[:, 0::2] = c & 0x0F
+    out[:, 1::2] = c >> 4
+    return out
+
+
+def _std_scales_numpy(y, S_enc):
+    """Scale bytes of the standard association, evaluated with numpy's fp32
+    arithmetic and the brute-force E4M3 encoder (no oracle code)."""
+    b = np.abs(y.reshape(y.shape[0], -1, 16)).max(axis=2).astype(f32)
+    k6 = f32(S_enc) * f32(1.0 / 6.0)              # S_enc * (1/6), the fp32 constant
+    s = (b * k6).astype(f32)
+    return brute_e4m3(np.minimum(s, f32(448.0))).reshape(b.shape)
+
+
+@pytest.mark.parametrize("gmode", ["none", "tensor"])
+def test_std_association_scales_match_numpy_fp32(gmode):
+    rng = np.random.default_rng(41)
+    y = (rng.standard_normal((64, 256)) * np.exp2(rng.integers(-6, 6, (64, 1)))).astype(f32)
+    if gmode == "none":
+        r = oracle.quantize(y, rounding=oracle.RTN_STD)
+        S_enc = 1.0
+    else:
+        A = np.abs(y).max().astype(f32)
+        r = oracle.quantize(y, rounding=oracle.RTN_STD, gamax_mode=oracle.GAMAX_TENSOR_GIVEN,
+                            gamax=np.array([A], f32), scale_bound=448.0)
+        S_enc = np.minimum(f32(6.0) * f32(448.0) / A, np.finfo(f32).max)   # the page's global scale
+    assert np.array_equal(r["scales"], _std_scales_numpy(y, S_enc))
+
+
+@pytest.mark.parametrize("gmode", ["none", "tensor"])
+def test_std_association_differs_from_four_over_six_on_a_fraction_of_blocks(gmode):
+    # the page: the two associations round differently "on a fraction of
+    # blocks" -- blocks whose scale lands next to an E4M3 rounding midpoint.
+    # Block maxima b sweep +-40 fp32 steps around each midpoint's preimage.
+    tab = torch_e4m3_table()[8:0x7F]              # normal E4M3 values
+    mids = ((tab[:-1] + tab[1:]) / 2).astype(f32)
+    if gmode == "none":
+        S_enc, kw = f32(1.0), {}
+    else:
+        A, bound = f32(10.0), f32(256.0)
+        S_enc = f32(6.0) * bound / A
+        kw = dict(gamax_mode=oracle.GAMAX_TENSOR_GIVEN, gamax=np.array([A], f32), scale_bound=256.0)
+    bs = []
+    for mid in mids:
+        b0 = f32(mid * f32(6.0) / S_enc)
+        up = dn = b0
+        bs.append(b0)
+        for _ in range(40):
+            up, dn = np.nextafter(up, f32(np.inf)), np.nextafter(dn, f32(-np.inf))
+            bs += [up, dn]
+    bs = np.array(bs, f32)
+    bs = bs[: len(bs) // 4 * 4]
+    y = (bs[:, None] * np.linspace(1.0, 0.25, 16, dtype=f32)[None, :]).astype(f32).reshape(-1, 64)
+    std = oracle.quantize(y, rounding=oracle.RTN_STD, **kw)
+    own = oracle.quantize(y, rounding=oracle.RTN, **kw)
+    diff = std["scales"] != own["scales"]
+    assert 0 < diff.mean() < 0.1
+    assert np.array_equal(std["scales"], _std_scales_numpy(y, S_enc))
+    # where the scales agree the element path is the same nearest rounding
+    same = np.repeat(~diff, 16, axis=1)
+    assert np.array_equal(_unpack_codes(std["codes"])[same], _unpack_codes(own["codes"])[same])
+
+
+# ---- stochastic rounding of the columnwise output, keyed on the element in x -------------
+def test_sr_columnwise_16x16_is_the_transpose_of_rowwise():
+    # 16x16 blocks and draws keyed on x's index: Q(x^T) = Q(x)^T ("Stable FP4
+    # Training via Transposition-Invariant Block Quantization", abstract)
+    x = W.matrix((64, 96), seed=47, outlier_frac=0.02, outlier_factor=30.0)
+    r = oracle.quantize(x, block=oracle.BLOCK_16X16, rounding=oracle.SR, seed=9, step=4, colwise=True)
+    assert np.array_equal(_unpack_codes(r["codes_col"]), _unpack_codes(r["codes"]).T)
+    tiles = r["scales"][::16, :]                  # one byte per tile, repeated on its 16 rows
+    assert np.array_equal(r["scales_col"][::16, :], tiles.T)
+
+
+def test_sr_columnwise_1x16_draws_use_the_x_index():
+    x = W.matrix((32, 48), seed=53)
+    seed, step, row_offset = 5, 11, 64
+    r = oracle.quantize(x, rounding=oracle.SR, seed=seed, step=step, row_offset=row_offset, colwise=True)
+    codes_col = _unpack_codes(r["codes_col"])     # [K, M]
+    M, K = x.shape
+    for c in (0, 17, 47):
+        for blk in range(M // 16):
+            rows = np.arange(16 * blk, 16 * blk + 16)
+            d = float(np.asarray(oracle.e4m3_decode(np.array([r["scales_col"][c, blk]], np.uint8))).ravel()[0])
+            v = (x[rows, c] / f32(d)).astype(f32)
+            u = oracle.sr_uniform(seed, step, (row_offset + rows) * K + c)
+            assert np.array_equal(codes_col[c, rows], oracle.e2m1_encode_sr(v, u))
+
+
+def test_sr_columnwise_row_shard_is_a_column_slice():
+    x = W.matrix((64, 32), seed=59)
+    whole = oracle.quantize(x, rounding=oracle.SR, seed=3, step=2, colwise=True)
+    part = oracle.quantize(np.ascontiguousarray(x[32:]), rounding=oracle.SR, seed=3, step=2, row_offset=32,
+                           colwise=True)
+    assert np.array_equal(part["codes_col"], whole["codes_col"][:, 16:])
+    assert np.array_equal(part["scales_col"], whole["scales_col"][:, 2:])
