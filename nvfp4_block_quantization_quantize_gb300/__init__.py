@@ -26,14 +26,14 @@ from .build import LIB_PATH, build  # noqa: F401  (build is re-exported)
 
 F32, BF16 = 0, 1
 BLOCK_1X16, BLOCK_16X16 = 0, 1
-RTN, SR = 0, 1
+RTN, SR, RTN_STD = 0, 1, 2
 GAMAX_NONE, GAMAX_TENSOR, GAMAX_ROW, GAMAX_TENSOR_GIVEN, GAMAX_ROW_GIVEN = 0, 1, 2, 3, 4
 ERR_NONE, ERR_MAE, ERR_MSE = 0, 1, 2
 OK, EINVAL, ECUDA = 0, 1, 2
 
 _NAMES = {
     "block": {"1x16": BLOCK_1X16, "16x16": BLOCK_16X16},
-    "rounding": {"rtn": RTN, "sr": SR},
+    "rounding": {"rtn": RTN, "sr": SR, "rtn_std": RTN_STD},
     "gamax_mode": {"none": GAMAX_NONE, "tensor": GAMAX_TENSOR, "row": GAMAX_ROW,
                    "tensor_given": GAMAX_TENSOR_GIVEN, "row_given": GAMAX_ROW_GIVEN},
     "err_mode": {"none": ERR_NONE, "mae": ERR_MAE, "mse": ERR_MSE},

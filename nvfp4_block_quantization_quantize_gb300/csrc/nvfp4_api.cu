@@ -53,7 +53,8 @@ int check_quant(const void* x, int64_t M, int64_t K, int dtype, int block, int r
     if (rc) return rc;
     if (dtype != NVFP4_F32 && dtype != NVFP4_BF16) return fail(NVFP4_EINVAL, "bad dtype %d", dtype);
     if (block != NVFP4_BLOCK_1X16 && block != NVFP4_BLOCK_16X16) return fail(NVFP4_EINVAL, "bad block %d", block);
-    if (rounding != NVFP4_RTN && rounding != NVFP4_SR) return fail(NVFP4_EINVAL, "bad rounding %d", rounding);
+    if (rounding != NVFP4_RTN && rounding != NVFP4_SR && rounding != NVFP4_RTN_STD)
+        return fail(NVFP4_EINVAL, "bad rounding %d", rounding);
     if (gamax_mode < NVFP4_GAMAX_NONE || gamax_mode > NVFP4_GAMAX_ROW_GIVEN)
         return fail(NVFP4_EINVAL, "bad gamax_mode %d", gamax_mode);
     if (err_mode < NVFP4_ERR_NONE || err_mode > NVFP4_ERR_MSE) return fail(NVFP4_EINVAL, "bad err_mode %d", err_mode);
@@ -63,13 +64,13 @@ int check_quant(const void* x, int64_t M, int64_t K, int dtype, int block, int r
     if (is_row_mode(gamax_mode) && (block == NVFP4_BLOCK_16X16 || colwise))
         return fail(NVFP4_EINVAL, "per-row global scales allow 1x16 rowwise output only");
     if (err_mode != NVFP4_ERR_NONE) {
-        if (rounding != NVFP4_RTN) return fail(NVFP4_EINVAL, "four-over-six is round-to-nearest only");
+        if (rounding != NVFP4_RTN)
+            return fail(NVFP4_EINVAL, "four-over-six is round-to-nearest with its own scale association only");
         if (residual) return fail(NVFP4_EINVAL, "four-over-six takes no residual");
         if (gamax_mode == NVFP4_GAMAX_NONE) return fail(NVFP4_EINVAL, "four-over-six needs a global amax");
         if (bound != 256.0f && bound != 448.0f) return fail(NVFP4_EINVAL, "four-over-six bound must be 256 or 448");
     }
-    if (colwise && (rounding != NVFP4_RTN || residual))
-        return fail(NVFP4_EINVAL, "columnwise output is round-to-nearest without a residual");
+    if (colwise && residual) return fail(NVFP4_EINVAL, "columnwise output takes no residual");
     const bool any = M > 0 && K > 0;
     if ((rc = check_ptr(x, "x", any))) return rc;
     if ((rc = check_ptr(residual, "residual", false))) return rc;

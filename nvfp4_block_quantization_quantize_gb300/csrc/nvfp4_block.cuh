@@ -113,14 +113,15 @@ __device__ __forceinline__ void fill_recip_table(float* rt) {
 // reciprocal table when D is a bare E4M3 scale sf (no global scale), else
 // null.  With wq, stochastic rounding also returns the codes' signed grid
 // values in q (nearest rounding leaves q alone).
-template <int RND>
-__device__ __forceinline__ void encode_plain16(const float* y, float D, float b, uint64_t idx0,
-                                               uint64_t seed, uint64_t step, uint32_t& w0,
-                                               uint32_t& w1, const float* rt, uint32_t sf,
-                                               float* q, bool wq) {
+// get_words(wd) fills the 16 elements' stochastic-rounding words (called
+// only for stochastic rounding, where the words are needed).
+template <int RND, class GetWords>
+__device__ __forceinline__ void encode_plain16_impl(const float* y, float D, float b, GetWords get_words,
+                                                    uint32_t& w0, uint32_t& w1, const float* rt,
+                                                    uint32_t sf, float* q, bool wq) {
     const bool fast = plain_fast(D, b);
     const float r = rt ? rt[sf] : (fast ? div_rn(1.0f, D) : 0.0f);
-    if (RND == NVFP4_RTN) {
+    if (RND != NVFP4_SR) {                      // nearest (either scale association)
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -129,7 +130,7 @@ __device__ __forceinline__ void encode_plain16(const float* y, float D, float b,
         w1 = e2m1_encode8(v + 8);
     } else {
         uint32_t wd[16];
-        sr_words16(idx0, seed, step, wd);
+        get_words(wd);
         // blocks holding an element 0 < |y| < 2^-80 (or zeros) take the per-element checked path
         bool tiny = false;
 #pragma unroll
@@ -172,6 +173,40 @@ __device__ __forceinline__ void encode_plain16(const float* y, float D, float b,
             for (int i = 0; i < 16; ++i) q[i] = 0.0f;
         }
     }
+}
+
+// elements idx0 .. idx0 + 15 of x (the stochastic-rounding counter)
+template <int RND>
+__device__ __forceinline__ void encode_plain16(const float* y, float D, float b, uint64_t idx0,
+                                               uint64_t seed, uint64_t step, uint32_t& w0,
+                                               uint32_t& w1, const float* rt, uint32_t sf,
+                                               float* q, bool wq) {
+    encode_plain16_impl<RND>(
+        y, D, b, [&](uint32_t* wd) { sr_words16(idx0, seed, step, wd); }, w0, w1, rt, sf, q, wq);
+}
+
+// the same with the words given (wd[16], read only for stochastic rounding)
+template <int RND>
+__device__ __forceinline__ void encode_plain16_words(const float* y, float D, float b, const uint32_t* wd,
+                                                     uint32_t& w0, uint32_t& w1, const float* rt,
+                                                     uint32_t sf, float* q, bool wq) {
+    encode_plain16_impl<RND>(
+        y, D, b,
+        [&](uint32_t* out) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) out[i] = wd[i];
+        },
+        w0, w1, rt, sf, q, wq);
+}
+
+// The block scale before E4M3 rounding: (b / 6) * S_enc, or with the standard
+// NVFP4 association (std_assoc) b * (S_enc * (1/6)), 1/6 the nearest fp32
+// ("Add NVFP4 four-over-six (row-wise) quantization to the training
+// prototype", Two load-bearing numeric details).
+template <bool GS>
+__device__ __forceinline__ float block_scale(float b, float Senc, bool std_assoc) {
+    if (std_assoc) return mul_rn(b, mul_rn(Senc, 0.16666667163372040f));
+    return block_s6f<GS>(b, Senc);
 }
 
 // dequantized values (q * d) * S_dec from signed grid values

@@ -40,7 +40,7 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool
     const bool wq = EF || a.dq_bf16;
     constexpr bool QV = ERR == NVFP4_ERR_NONE && RND == NVFP4_SR;   // grid values kept
     if (ERR == NVFP4_ERR_NONE) {
-        const float s6f = block_s6f<GS>(b, gb.Senc);
+        const float s6f = block_scale<GS>(b, gb.Senc, RND == NVFP4_RTN_STD);
         sf = e4m3_encode(min_nd(s6f, 448.0f));
         d = e4m3_decode(sf);
         const float D = GS ? mul_rn(d, gb.Sdec) : d;
@@ -319,6 +319,9 @@ int rows_plain(const QuantArgs& a, int64_t nblk, cudaStream_t s) {
     if (a.rounding == NVFP4_RTN)
         return ef ? launch_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN, true, GS>(a, nblk, s)
                   : launch_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN, false, GS>(a, nblk, s);
+    if (a.rounding == NVFP4_RTN_STD)
+        return ef ? launch_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN_STD, true, GS>(a, nblk, s)
+                  : launch_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN_STD, false, GS>(a, nblk, s);
     return ef ? launch_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, true, GS>(a, nblk, s)
               : launch_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, false, GS>(a, nblk, s);
 }

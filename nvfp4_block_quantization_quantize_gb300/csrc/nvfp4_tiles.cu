@@ -1,6 +1,6 @@
 // nvfp4_tiles.cu -- 16x16 blocks and columnwise outputs for sm_103a.
 //
-// k_tiles_rows  rowwise + columnwise output (round to nearest): one CTA = a
+// k_tiles_rows  rowwise + columnwise output (no residual): one CTA = a
 //               16-row band x 256 columns; lane l of warp w holds row l%16
 //               of the 16x16 tile 2w + l/16.  16x16 blocks reduce their amax
 //               (and, for four-over-six, their row error sums with the fixed
@@ -36,9 +36,12 @@ constexpr int kThreads = 256;
 constexpr int kTileCols = 256;
 constexpr int kYsStride = kTileCols + 4;
 
-template <int DT, int BLK, int ERR, bool GS>
+template <int DT, int BLK, int ERR, int RND, bool GS>
 __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
     __shared__ float ys[16 * kYsStride];
+    // stochastic rounding: the row pass's draws, keyed on x's index, reused by
+    // the column pass
+    __shared__ uint32_t ws[RND == NVFP4_SR ? 16 * kYsStride : 1];
     __shared__ O6TabOf<ERR> tab;
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
     if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
@@ -80,12 +83,20 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
         uint32_t w0, w1, sf;
         float d;
         if (ERR == NVFP4_ERR_NONE) {
-            const float s6f = block_s6f<GS>(b, g.Senc);
+            const float s6f = block_scale<GS>(b, g.Senc, RND == NVFP4_RTN_STD);
             sf = e4m3_encode(min_nd(s6f, 448.0f));
             d = e4m3_decode(sf);
             const float D = GS ? mul_rn(d, g.Sdec) : d;
             float q[16];
-            encode_plain16<NVFP4_RTN>(y, D, b, 0, 0, 0, w0, w1, GS ? nullptr : rtab, sf, q, false);
+            uint32_t wd[16];
+            if (RND == NVFP4_SR) {
+                const uint64_t idx0 = (static_cast<uint64_t>(a.row_offset) + static_cast<uint64_t>(row)) *
+                                          static_cast<uint64_t>(a.K) + static_cast<uint64_t>(cb * 16);
+                sr_words16(idx0, a.seed, a.step, wd);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) ws[rr * kYsStride + t * 16 + i] = wd[i];
+            }
+            encode_plain16_words<RND>(y, D, b, wd, w0, w1, GS ? nullptr : rtab, sf, q, false);
         } else {
             four_over_six16<ERR, BLK == NVFP4_BLOCK_16X16>(y, b, g, C, tp, w0, w1, sf, d);
         }
@@ -108,12 +119,17 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
     uint32_t w0, w1, sf;
     float d;
     if (ERR == NVFP4_ERR_NONE) {
-        const float s6f = block_s6f<GS>(bc, g.Senc);
+        const float s6f = block_scale<GS>(bc, g.Senc, RND == NVFP4_RTN_STD);
         sf = e4m3_encode(min_nd(s6f, 448.0f));
         d = e4m3_decode(sf);
         const float D = GS ? mul_rn(d, g.Sdec) : d;
         float qc[16];
-        encode_plain16<NVFP4_RTN>(c, D, bc, 0, 0, 0, w0, w1, GS ? nullptr : rtab, sf, qc, false);
+        uint32_t wd[16];
+        if (RND == NVFP4_SR) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) wd[r] = ws[r * kYsStride + j];
+        }
+        encode_plain16_words<RND>(c, D, bc, wd, w0, w1, GS ? nullptr : rtab, sf, qc, false);
     } else {
         four_over_six16<ERR, BLK == NVFP4_BLOCK_16X16>(c, bc, g, C, tp, w0, w1, sf, d);
     }
@@ -310,18 +326,25 @@ int launch_tile_t(const QuantArgs& a, cudaStream_t s) {
     return static_cast<int>(cudaGetLastError());
 }
 
-// rowwise + columnwise outputs (round to nearest, no residual)
+// rowwise + columnwise outputs (no residual)
 template <int DT, int BLK>
 int tiles_dispatch_blk(const QuantArgs& a, cudaStream_t s) {
     if (a.err_mode != NVFP4_ERR_NONE) {
         if (BLK == NVFP4_BLOCK_16X16)
             return a.err_mode == NVFP4_ERR_MAE ? launch_tile_t<DT, NVFP4_ERR_MAE>(a, s)
                                                : launch_tile_t<DT, NVFP4_ERR_MSE>(a, s);
-        return a.err_mode == NVFP4_ERR_MAE ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_MAE, true>, a, s)
-                                           : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_MSE, true>, a, s);
+        return a.err_mode == NVFP4_ERR_MAE ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_MAE, NVFP4_RTN, true>, a, s)
+                                           : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_MSE, NVFP4_RTN, true>, a, s);
     }
-    return a.gamax_mode == NVFP4_GAMAX_NONE ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, false>, a, s)
-                                            : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, true>, a, s);
+    const bool gs = a.gamax_mode != NVFP4_GAMAX_NONE;
+    if (a.rounding == NVFP4_SR)
+        return gs ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, true>, a, s)
+                  : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, false>, a, s);
+    if (a.rounding == NVFP4_RTN_STD)
+        return gs ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN_STD, true>, a, s)
+                  : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN_STD, false>, a, s);
+    return gs ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN, true>, a, s)
+              : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN, false>, a, s);
 }
 
 template <int DT>

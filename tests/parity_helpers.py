@@ -9,7 +9,7 @@ import oracle
 
 NAMES = {
     "block": {"1x16": oracle.BLOCK_1X16, "16x16": oracle.BLOCK_16X16},
-    "rounding": {"rtn": oracle.RTN, "sr": oracle.SR},
+    "rounding": {"rtn": oracle.RTN, "sr": oracle.SR, "rtn_std": oracle.RTN_STD},
     "gamax_mode": {"none": oracle.GAMAX_NONE, "tensor": oracle.GAMAX_TENSOR,
                    "row": oracle.GAMAX_ROW, "tensor_given": oracle.GAMAX_TENSOR_GIVEN,
                    "row_given": oracle.GAMAX_ROW_GIVEN},
