@@ -167,6 +167,21 @@ int nvfp4_amax(const void* x, int64_t M, int64_t K, int dtype, const float* resi
                int mode, float* out, void* stream);
 
 /*
+ * nvfp4_scales_to_mma -- re-lay a row-major scale matrix [rows, cols] (one
+ * E4M3 byte per 16 elements along K: cols = K/16) out in the layout the
+ * block-scaled tensor-core matrix multiply reads ("fp4-train", API:
+ * to_fp4_operands returns "the layout NVFP4 tensor cores read"; the format is
+ * the block-scaling-factor layout of NVIDIA's public cuBLAS documentation):
+ *   rows padded to R = 128 * ceil(rows/128), cols to C = 4 * ceil(cols/4),
+ *   padding bytes 0; 128 x 4 tiles of 512 bytes, tile (rt, ct) at byte
+ *   (rt * C/4 + ct) * 512; inside a tile, byte (r, c) at
+ *   (r % 32) * 16 + (r / 32) * 4 + c.
+ * scales  device [rows, cols] bytes;  out  device [R * C] bytes (caller-owned).
+ * EINVAL when rows < 0, cols < 0, or a pointer is NULL (with rows, cols > 0).
+ */
+int nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out, void* stream);
+
+/*
  * nvfp4_probe_divide -- diagnostic.  out[i] = a[i] / b[i] computed by the
  * device routine the plain quantizer uses for "every element is divided by the
  * decoded scale" [fp4-train, Method] (its stochastic-rounding form, which must

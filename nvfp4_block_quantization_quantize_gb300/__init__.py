@@ -80,6 +80,8 @@ def load_library(path: str | None = None):
         lib.nvfp4_amax.argtypes = [P, i64, i64, i32, P, i32, P, P]
         lib.nvfp4_probe_divide.restype = i32
         lib.nvfp4_probe_divide.argtypes = [P, P, P, i64, P]
+        lib.nvfp4_scales_to_mma.restype = i32
+        lib.nvfp4_scales_to_mma.argtypes = [P, i64, i64, P, P]
         lib.nvfp4_last_error.restype = ctypes.c_char_p
         lib.nvfp4_last_error.argtypes = []
         lib.nvfp4_abi_version.restype = i32
@@ -273,6 +275,20 @@ def nvfp4_amax(x: torch.Tensor, *, residual=None, per_row: bool = False, out=Non
     rc = lib.nvfp4_amax(_ptr(xd), M, K, _x_dtype(x), _ptr(rd), GAMAX_ROW if per_row else GAMAX_TENSOR,
                         _ptr(o), _stream(stream))
     _check(lib, rc)
+    return o.cpu() if host else o
+
+
+def nvfp4_scales_to_mma(scales: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+    """Row-major scale bytes [rows, cols] -> the block-scaled matrix-multiply
+    layout, [128*ceil(rows/128), 4*ceil(cols/4)] bytes (see nvfp4.h)."""
+    lib = load_library()
+    host = not scales.is_cuda
+    dev = scales.device if scales.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    s = _stage(scales.contiguous(), dev)
+    rows, cols = s.shape
+    R, C = -(-rows // 128) * 128, -(-cols // 4) * 4
+    o = out if out is not None else _empty((R, C), torch.uint8, dev)
+    _check(lib, lib.nvfp4_scales_to_mma(_ptr(s), rows, cols, _ptr(o), _stream(stream)))
     return o.cpu() if host else o
 
 

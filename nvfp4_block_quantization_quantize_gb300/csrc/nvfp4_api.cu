@@ -177,6 +177,19 @@ int nvfp4_amax(const void* x, int64_t M, int64_t K, int dtype, const float* resi
     return NVFP4_OK;
 }
 
+int nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out, void* stream) {
+    g_msg[0] = '\0';
+    if (rows < 0 || cols < 0) return fail(NVFP4_EINVAL, "rows and cols must be >= 0");
+    const bool any = rows > 0 && cols > 0;
+    int rc;
+    if ((rc = check_ptr(scales, "scales", any, 1))) return rc;
+    if ((rc = check_ptr(out, "out", any, 4))) return rc;
+    if (!any) return NVFP4_OK;
+    const int err = nvfp4::launch_scales_mma(scales, rows, cols, out, stream);
+    if (err) return cuda_fail(err, "scale layout launch");
+    return NVFP4_OK;
+}
+
 int nvfp4_probe_divide(const float* a, const float* b, float* out, int64_t n, void* stream) {
     g_msg[0] = '\0';
     if (n < 0) return fail(NVFP4_EINVAL, "n must be >= 0");

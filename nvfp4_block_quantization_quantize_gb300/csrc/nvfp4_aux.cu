@@ -204,6 +204,29 @@ int grid_for(int64_t nblk) {
     return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
+// Scale re-layout for the block-scaled matrix multiply: one thread per
+// (row, group of 4 columns) of the padded matrix, i.e. one 4-byte word of the
+// output: tile (r/128, c/4), word (r % 32) * 4 + (r % 128) / 32 of the tile.
+__global__ void __launch_bounds__(kThreads) k_scales_mma(const uint8_t* __restrict__ in, int64_t rows,
+                                                         int64_t cols, int64_t R, int64_t C4,
+                                                         uint32_t* __restrict__ out) {
+    const int64_t n = R * C4;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / C4, cg = i - r * C4;
+        uint32_t w = 0;
+        if (r < rows) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int64_t c = 4 * cg + k;
+                if (c < cols) w |= static_cast<uint32_t>(in[r * cols + c]) << (8 * k);
+            }
+        }
+        const int64_t tile = (r / 128) * C4 + cg;
+        out[tile * 128 + (r % 32) * 4 + (r % 128) / 32] = w;
+    }
+}
+
 }  // namespace
 
 int sm_count() {
@@ -247,6 +270,15 @@ int launch_amax(const void* x, int64_t M, int64_t K, int dtype, const float* res
             }
         }
     }
+    return static_cast<int>(cudaGetLastError());
+}
+
+int launch_scales_mma(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out, void* stream) {
+    const int64_t R = (rows + 127) / 128 * 128, C4 = (cols + 3) / 4;
+    const int64_t n = R * C4;
+    if (n <= 0) return 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    k_scales_mma<<<grid_for(n), kThreads, 0, s>>>(in, rows, cols, R, C4, reinterpret_cast<uint32_t*>(out));
     return static_cast<int>(cudaGetLastError());
 }
 

@@ -40,6 +40,7 @@ struct DequantArgs {
 int launch_quantize_rows(const QuantArgs& a, void* stream);    // rowwise output only
 int launch_quantize_tiles(const QuantArgs& a, void* stream);   // rowwise + columnwise
 int launch_dequantize(const DequantArgs& a, void* stream);
+int launch_scales_mma(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out, void* stream);
 int launch_amax(const void* x, int64_t M, int64_t K, int dtype, const float* residual, int mode,
                 float* out, void* stream);
 int launch_probe_divide(const float* a, const float* b, float* out, int64_t n, void* stream);

@@ -80,6 +80,8 @@ def _load():
     lib.orc_global_scales.argtypes = [f32, f32, P, P]
     lib.orc_amax.restype = None
     lib.orc_amax.argtypes = [P, i64, i64, i32, P, i32, P]
+    lib.orc_scales_to_mma.restype = None
+    lib.orc_scales_to_mma.argtypes = [P, i64, i64, P]
     lib.orc_quantize.restype = i32
     lib.orc_quantize.argtypes = [P, i64, i64, i32, i32, i32, P, u64, u64, i64, i32, P, i32, f32,
                                  P, P, P, P]
@@ -236,6 +238,16 @@ def quantize(x: np.ndarray, *, block: int = BLOCK_1X16, rounding: int = RTN,
     if colwise:
         out["codes_col"] = codes_col
         out["scales_col"] = scales_col
+    return out
+
+
+def scales_to_mma(scales: np.ndarray) -> np.ndarray:
+    """Row-major scale bytes [rows, cols] -> the matrix-multiply layout (flat bytes)."""
+    lib = _load()
+    s = np.ascontiguousarray(scales, np.uint8)
+    rows, cols = s.shape
+    out = np.zeros(((rows + 127) // 128 * 128) * ((cols + 3) // 4 * 4), np.uint8)
+    lib.orc_scales_to_mma(_ptr(s), rows, cols, _ptr(out))
     return out
 
 

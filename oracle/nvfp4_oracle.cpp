@@ -445,6 +445,18 @@ int orc_quantize(const void* x, int64_t M, int64_t K, int dtype, int block, int 
     return 0;
 }
 
+/* ---- scale layout for the block-scaled matrix multiply ---------------- */
+void orc_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out) {
+    const int64_t R = (rows + 127) / 128 * 128, C = (cols + 3) / 4 * 4;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            const uint8_t v = (r < rows && c < cols) ? scales[r * cols + c] : 0;
+            const int64_t tile = (r / 128) * (C / 4) + c / 4;
+            const int64_t rr = r % 128, cc = c % 4;
+            out[tile * 512 + (rr % 32) * 16 + (rr / 32) * 4 + cc] = v;
+        }
+}
+
 /* ---- dequantize ------------------------------------------------------- */
 int orc_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int64_t K,
                    int gamax_mode, const float* gamax, float scale_bound,

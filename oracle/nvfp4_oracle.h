@@ -89,6 +89,12 @@ int orc_qdq(const void* x, int64_t M, int64_t K, int dtype, int block, int round
             int gamax_mode, float* gamax, int err_mode, float scale_bound,
             uint8_t* codes, uint8_t* scales, uint16_t* out_bf16);
 
+/* scale bytes [rows, cols] -> the block-scaled matrix-multiply layout:
+ * rows padded to 128, cols to 4 (zero bytes), 128 x 4 tiles of 512 bytes in
+ * row-major tile order, byte (r, c) of a tile at (r % 32) * 16 + (r / 32) * 4 + c
+ * ("fp4-train", API: to_fp4_operands, the layout NVFP4 tensor cores read) */
+void orc_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out);
+
 /* batch forms of the scalar codecs */
 void orc_e4m3_encode_n(const float* s, int64_t n, uint8_t* out);
 void orc_e2m1_encode_rn_n(const float* v, int64_t n, uint8_t* out);

@@ -147,3 +147,13 @@ def test_product_never_touches_the_oracle():
         if f.endswith((".py", ".cpp", ".h")):
             assert "nvfp4_block_quantization_quantize_gb300" not in open(
                 os.path.join(ROOT, "oracle", f)).read()
+
+
+def test_scales_to_mma_rejects(lib):
+    f = lib.nvfp4_scales_to_mma
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    assert f(A16, -1, 4, A16, None) == 1
+    assert f(None, 128, 4, A16, None) == 1
+    assert f(A16, 128, 4, None, None) == 1
+    assert f(A16, 128, 4, ctypes.c_void_p(0x10002), None) == 1      # out needs 4-byte alignment
+    assert f(None, 0, 4, None, None) == 0                              # empty: a no-op

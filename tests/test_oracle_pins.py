@@ -755,3 +755,22 @@ def test_sr_columnwise_row_shard_is_a_column_slice():
                            colwise=True)
     assert np.array_equal(part["codes_col"], whole["codes_col"][:, 16:])
     assert np.array_equal(part["scales_col"], whole["scales_col"][:, 2:])
+
+
+# ---- scale layout for the block-scaled matrix multiply -------------------------------------
+@pytest.mark.parametrize("rows,cols", [(128, 4), (256, 12), (300, 7), (1, 1), (129, 5)])
+def test_scales_to_mma_is_the_blocked_permutation(rows, cols):
+    # the layout as a reshape of the zero-padded matrix: [R/128, 4, 32, C/4, 4]
+    # (row = 128 a + 32 b + r32, col = 4 t + j) stored as [a, t, r32, b, j]
+    rng = np.random.default_rng(rows * 7 + cols)
+    s = rng.integers(0, 127, (rows, cols), dtype=np.uint8)
+    R, C = -(-rows // 128) * 128, -(-cols // 4) * 4
+    pad = np.zeros((R, C), np.uint8)
+    pad[:rows, :cols] = s
+    want = pad.reshape(R // 128, 4, 32, C // 4, 4).transpose(0, 3, 2, 1, 4).ravel()
+    got = oracle.scales_to_mma(s)
+    assert np.array_equal(got, want)
+    # a bijection of the padded matrix: every byte lands once
+    idx = np.arange(R * C, dtype=np.int64).reshape(R, C)
+    assert np.array_equal(np.sort(idx.reshape(R // 128, 4, 32, C // 4, 4).transpose(0, 3, 2, 1, 4).ravel()),
+                          np.arange(R * C))
