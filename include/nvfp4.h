@@ -182,6 +182,25 @@ int nvfp4_amax(const void* x, int64_t M, int64_t K, int dtype, const float* resi
 int nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out, void* stream);
 
 /*
+ * nvfp4_mm -- out = (A B^T) * S_dec(A) * S_dec(B) on the block-scaled FP4
+ * tensor cores ("fp4-train", API: fp4_mm, a @ b^T on the NVFP4 tensor cores;
+ * Correctness: the tensor-core result agrees with the dequantize path).
+ *   codes_a [M, K/2], codes_b [N, K/2]: rowwise 1x16 codes from nvfp4_quantize
+ *   scales_a, scales_b: their scale bytes in the nvfp4_scales_to_mma layout
+ *   gamax_a, gamax_b: NULL (no global scale) or the per-tensor amax the codes
+ *     were made with (device fp32 [1]); scale_bound the bound they used
+ *   out: device [M, N], NVFP4_F32 or NVFP4_BF16 (RNE), row-major
+ * Products are exact and accumulate in fp32 in tensor memory, 64 K-elements
+ * per step.  EINVAL when M % 128, N % 128 or K % 64 is not 0, M, N or K is
+ * negative, a pointer is NULL or misaligned (16 bytes; gamax 4), or the bound
+ * is outside (0, 448].  A CTA that stops waiting for its tensor-core work
+ * writes NaN to its 128 x 128 tile of out.
+ */
+int nvfp4_mm(const uint8_t* codes_a, const uint8_t* scales_a, const uint8_t* codes_b, const uint8_t* scales_b,
+             int64_t M, int64_t N, int64_t K, const float* gamax_a, const float* gamax_b, float scale_bound,
+             void* out, int out_dtype, void* stream);
+
+/*
  * nvfp4_probe_divide -- diagnostic.  out[i] = a[i] / b[i] computed by the
  * device routine the plain quantizer uses for "every element is divided by the
  * decoded scale" [fp4-train, Method] (its stochastic-rounding form, which must

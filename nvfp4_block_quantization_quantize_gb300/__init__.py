@@ -82,6 +82,8 @@ def load_library(path: str | None = None):
         lib.nvfp4_probe_divide.argtypes = [P, P, P, i64, P]
         lib.nvfp4_scales_to_mma.restype = i32
         lib.nvfp4_scales_to_mma.argtypes = [P, i64, i64, P, P]
+        lib.nvfp4_mm.restype = i32
+        lib.nvfp4_mm.argtypes = [P, P, P, P, i64, i64, i64, P, P, f32, P, i32, P]
         lib.nvfp4_last_error.restype = ctypes.c_char_p
         lib.nvfp4_last_error.argtypes = []
         lib.nvfp4_abi_version.restype = i32
@@ -290,6 +292,20 @@ def nvfp4_scales_to_mma(scales: torch.Tensor, out=None, stream=None) -> torch.Te
     o = out if out is not None else _empty((R, C), torch.uint8, dev)
     _check(lib, lib.nvfp4_scales_to_mma(_ptr(s), rows, cols, _ptr(o), _stream(stream)))
     return o.cpu() if host else o
+
+
+def nvfp4_mm(codes_a, scales_a, codes_b, scales_b, M: int, N: int, K: int, *, gamax_a=None, gamax_b=None,
+             scale_bound: float = 448.0, out_dtype="bf16", out=None, stream=None) -> torch.Tensor:
+    """(A B^T) * S_dec(A) * S_dec(B) on the block-scaled FP4 tensor cores;
+    scales in the nvfp4_scales_to_mma layout (see nvfp4.h).  Device tensors."""
+    lib = load_library()
+    odt = _enum("dtype", out_dtype)
+    dev = codes_a.device
+    o = out if out is not None else _empty((M, N), torch.float32 if odt == F32 else torch.bfloat16, dev)
+    rc = lib.nvfp4_mm(_ptr(codes_a), _ptr(scales_a), _ptr(codes_b), _ptr(scales_b), M, N, K, _ptr(gamax_a),
+                      _ptr(gamax_b), scale_bound, _ptr(o), odt, _stream(stream))
+    _check(lib, rc)
+    return o
 
 
 def nvfp4_probe_divide(a: torch.Tensor, b: torch.Tensor, stream=None) -> torch.Tensor:

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libnvfp4_gb300.so")
-SOURCES = ["nvfp4_rows.cu", "nvfp4_tiles.cu", "nvfp4_aux.cu", "nvfp4_api.cu"]
+SOURCES = ["nvfp4_rows.cu", "nvfp4_tiles.cu", "nvfp4_aux.cu", "nvfp4_mm.cu", "nvfp4_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-ftz=false",
          "-prec-div=true", "-prec-sqrt=true", "-fmad=false", "-I", INCLUDE]

@@ -190,6 +190,37 @@ int nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t cols, uint8
     return NVFP4_OK;
 }
 
+int nvfp4_mm(const uint8_t* codes_a, const uint8_t* scales_a, const uint8_t* codes_b, const uint8_t* scales_b,
+             int64_t M, int64_t N, int64_t K, const float* gamax_a, const float* gamax_b, float scale_bound,
+             void* out, int out_dtype, void* stream) {
+    g_msg[0] = '\0';
+    if (M < 0 || N < 0 || K < 0) return fail(NVFP4_EINVAL, "M, N and K must be >= 0");
+    if (M % 128 || N % 128 || K % 64)
+        return fail(NVFP4_EINVAL, "nvfp4_mm needs M %% 128 == 0, N %% 128 == 0 and K %% 64 == 0");
+    if (out_dtype != NVFP4_F32 && out_dtype != NVFP4_BF16) return fail(NVFP4_EINVAL, "bad out_dtype %d", out_dtype);
+    if (!(scale_bound > 0.0f && scale_bound <= 448.0f)) return fail(NVFP4_EINVAL, "scale_bound must be in (0, 448]");
+    const bool any = M > 0 && N > 0;
+    const bool anyk = any && K > 0;
+    int rc;
+    if ((rc = check_ptr(codes_a, "codes_a", anyk))) return rc;
+    if ((rc = check_ptr(scales_a, "scales_a", anyk))) return rc;
+    if ((rc = check_ptr(codes_b, "codes_b", anyk))) return rc;
+    if ((rc = check_ptr(scales_b, "scales_b", anyk))) return rc;
+    if ((rc = check_ptr(gamax_a, "gamax_a", false, 4))) return rc;
+    if ((rc = check_ptr(gamax_b, "gamax_b", false, 4))) return rc;
+    if ((rc = check_ptr(out, "out", any))) return rc;
+    if (!any) return NVFP4_OK;
+    if (K == 0) {
+        const size_t bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * (out_dtype == NVFP4_F32 ? 4 : 2);
+        const int err = static_cast<int>(cudaMemsetAsync(out, 0, bytes, static_cast<cudaStream_t>(stream)));
+        return err ? cuda_fail(err, "mm zero fill") : NVFP4_OK;
+    }
+    const int err = nvfp4::launch_mm(codes_a, scales_a, codes_b, scales_b, M, N, K, gamax_a, gamax_b, scale_bound,
+                                     out, out_dtype, stream);
+    if (err) return cuda_fail(err, "mm launch");
+    return NVFP4_OK;
+}
+
 int nvfp4_probe_divide(const float* a, const float* b, float* out, int64_t n, void* stream) {
     g_msg[0] = '\0';
     if (n < 0) return fail(NVFP4_EINVAL, "n must be >= 0");

@@ -41,6 +41,9 @@ int launch_quantize_rows(const QuantArgs& a, void* stream);    // rowwise output
 int launch_quantize_tiles(const QuantArgs& a, void* stream);   // rowwise + columnwise
 int launch_dequantize(const DequantArgs& a, void* stream);
 int launch_scales_mma(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* out, void* stream);
+int launch_mm(const uint8_t* A, const uint8_t* SA, const uint8_t* B, const uint8_t* SB, int64_t M, int64_t N,
+              int64_t K, const float* gamax_a, const float* gamax_b, float bound, void* out, int out_dtype,
+              void* stream);
 int launch_amax(const void* x, int64_t M, int64_t K, int dtype, const float* residual, int mode,
                 float* out, void* stream);
 int launch_probe_divide(const float* a, const float* b, float* out, int64_t n, void* stream);

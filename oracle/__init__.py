@@ -251,6 +251,21 @@ def scales_to_mma(scales: np.ndarray) -> np.ndarray:
     return out
 
 
+def mm_reference(codes_a: np.ndarray, scales_a: np.ndarray, codes_b: np.ndarray, scales_b: np.ndarray,
+                 M: int, N: int, K: int, gamax_a=None, gamax_b=None, scale_bound: float = 448.0):
+    """The plain definition of the FP4 product ("fp4-train", API: fp4_mm, a @ b^T,
+    and Correctness: equal to the dequantize path): (deq(A) deq(B)^T) with each
+    operand dequantized without its global scale, in float64, times both fp32
+    decode scales.  Row-major scales [M, K/16], [N, K/16]; returns float64 [M, N]."""
+    da = dequantize(codes_a, scales_a, M, K, out_dtype=F32).astype(np.float64)
+    db = dequantize(codes_b, scales_b, N, K, out_dtype=F32).astype(np.float64)
+    alpha = 1.0
+    for g in (gamax_a, gamax_b):
+        if g is not None:
+            alpha *= float(global_scales(float(np.asarray(g).ravel()[0]), scale_bound)[1])
+    return (da @ db.T) * alpha
+
+
 def dequantize(codes: np.ndarray, scales: np.ndarray, M: int, K: int, *,
                gamax_mode: int = GAMAX_NONE, gamax=None, scale_bound: float = 448.0,
                out_dtype: int = BF16) -> np.ndarray:

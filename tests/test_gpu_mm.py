@@ -1,0 +1,108 @@
+"""The block-scaled FP4 tensor-core product (nvfp4_mm) against its plain
+definition (oracle.mm_reference: the product of the dequantized operands in
+float64).
+
+With unit scales and small grid values every partial sum is a multiple of 1/4
+below 2^22, so any fp32 accumulation order is exact and the result must equal
+the reference bit for bit; with real scales the products are still exact in
+fp32 and only the accumulation of K terms can round, which bounds the error
+by K * 2^-23 * (|A| |B|^T).
+"""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_workloads as W
+import oracle
+from parity_helpers import to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+nv = pytest.importorskip("nvfp4_block_quantization_quantize_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    nv.build()
+    nv.load_library()
+
+
+def _mm_both(ca, sa, cb, sb, M, N, K, ga=None, gb=None, out_dtype="f32"):
+    y = nv.nvfp4_mm(to_dev(ca), nv.nvfp4_scales_to_mma(to_dev(sa)), to_dev(cb), nv.nvfp4_scales_to_mma(to_dev(sb)),
+                    M, N, K, gamax_a=None if ga is None else to_dev(ga), gamax_b=None if gb is None else to_dev(gb),
+                    out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    ref = oracle.mm_reference(ca, sa, cb, sb, M, N, K, gamax_a=ga, gamax_b=gb)
+    return to_np(y.float()).astype(np.float64), ref
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (128, 256, 192), (256, 128, 512)])
+def test_mm_unit_scales_exact(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    ca = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    cb = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = np.full((M, K // 16), 0x38, np.uint8)        # E4M3 1.0
+    sb = np.full((N, K // 16), 0x38, np.uint8)
+    y, ref = _mm_both(ca, sa, cb, sb, M, N, K)
+    assert np.array_equal(y, ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (256, 384, 1024)])
+def test_mm_scales_exact_per_block(M, N, K):
+    # one scale per block row, powers of two: still exact in any order
+    rng = np.random.default_rng(3 * M + N)
+    ca = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    cb = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = (0x38 + 8 * rng.integers(-2, 3, (M, K // 16))).astype(np.uint8)      # 2^-2 .. 2^2
+    sb = (0x38 + 8 * rng.integers(-2, 3, (N, K // 16))).astype(np.uint8)
+    y, ref = _mm_both(ca, sa, cb, sb, M, N, K)
+    assert np.array_equal(y, ref)
+
+
+@pytest.mark.parametrize("gm", ["none", "tensor"])
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_mm_quantized_operands(gm, out_dtype):
+    M, N, K = 256, 384, 1024
+    a = W.matrix((M, K), seed=83, dtype="bf16", dist="t")
+    b = W.matrix((N, K), seed=89, dtype="bf16")
+    qa = nv.nvfp4_quantize(to_dev(a), gamax_mode=gm)
+    qb = nv.nvfp4_quantize(to_dev(b), gamax_mode=gm)
+    ga = None if gm == "none" else to_np(qa["gamax"])
+    gb = None if gm == "none" else to_np(qb["gamax"])
+    y, ref = _mm_both(to_np(qa["codes"]), to_np(qa["scales"]), to_np(qb["codes"]), to_np(qb["scales"]), M, N, K,
+                      ga, gb, out_dtype)
+    da = oracle.dequantize(to_np(qa["codes"]), to_np(qa["scales"]), M, K, out_dtype=oracle.F32).astype(np.float64)
+    db = oracle.dequantize(to_np(qb["codes"]), to_np(qb["scales"]), N, K, out_dtype=oracle.F32).astype(np.float64)
+    scale = abs(ref).max() / max(abs(da @ db.T).max(), 1e-300)
+    bound = (np.abs(da) @ np.abs(db).T) * scale * K * 2.0 ** -23
+    if out_dtype == "bf16":
+        bound = bound + np.abs(ref) * 2.0 ** -8
+    err = np.abs(y - ref)
+    assert (err <= bound + 1e-30).all(), f"max err {err.max()}"
+
+
+def test_mm_matches_library_gemm():
+    from nvfp4_block_quantization_quantize_gb300.consumers import fp4_mm, to_fp4_operands
+    M, N, K = 256, 256, 2048
+    a = to_dev(W.matrix((M, K), seed=97, dtype="bf16"))
+    b = to_dev(W.matrix((N, K), seed=101, dtype="bf16"))
+    qa, qb = nv.nvfp4_quantize(a), nv.nvfp4_quantize(b)
+    ours = nv.nvfp4_mm(qa["codes"], nv.nvfp4_scales_to_mma(qa["scales"]), qb["codes"],
+                       nv.nvfp4_scales_to_mma(qb["scales"]), M, N, K, out_dtype="f32")
+    try:
+        lib = fp4_mm(to_fp4_operands(qa), to_fp4_operands(qb), out_dtype=torch.float32)
+    except (RuntimeError, NotImplementedError, TypeError, AttributeError) as e:
+        pytest.skip(f"no library block-scaled FP4 GEMM: {e}")
+    torch.cuda.synchronize()
+    rel = float(((ours - lib).abs().max() / lib.abs().max()).item())
+    assert rel < 1e-5
+
+
+def test_mm_rejects_bad_shapes():
+    z = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(nv.NVFP4Error):
+        nv.nvfp4_mm(z, z, z, z, 100, 128, 64)
+    with pytest.raises(nv.NVFP4Error):
+        nv.nvfp4_mm(z, z, z, z, 128, 128, 48)
