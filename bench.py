@@ -214,6 +214,52 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def mm_measurement(nv, torch, out, Ma, Ka, M2, K2, peaks, iters=5):
+    """The FP4 product consumer (not part of the step): C = A W2^T with the
+    step's round-to-nearest A codes and stochastic-rounding W2 codes, timed with
+    CUDA events; against the fp4 dense peak taken as the measured bf16 peak x
+    the nominal fp4 / bf16 ratio (13.5 / 2.25)."""
+    sa = nv.nvfp4_scales_to_mma(out["sar"])
+    sb = nv.nvfp4_scales_to_mma(out["s2s"])
+    M, N, K = Ma, M2, Ka
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=out["car"].device)
+    run = lambda: nv.nvfp4_mm(out["car"], sa, out["c2s"], sb, M, N, K, out=y)   # noqa: E731
+    for _ in range(2):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    flops = 2.0 * M * N * K
+    peak = (peaks["bf16_tflops"] if peaks else 1900.0) * 13.5 / 2.25
+    res = {"kernel": "k_mm<bf16 out>", "shape_mnk": [M, N, K], "ms": round(ms, 4),
+           "tflops": round(flops / ms / 1e9, 1), "peak_tflops": round(peak, 1),
+           "frac": round(flops / ms / 1e9 / peak, 4),
+           "peak_source": ("measured" if peaks else "fallback") + " bf16 x nominal fp4/bf16 ratio 6"}
+    try:
+        from nvfp4_block_quantization_quantize_gb300.consumers import fp4_mm, to_fp4_operands
+        qa, qb = to_fp4_operands({"codes": out["car"], "scales": out["sar"]}), \
+            to_fp4_operands({"codes": out["c2s"], "scales": out["s2s"]})
+        for _ in range(2):
+            fp4_mm(qa, qb)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(iters):
+            fp4_mm(qa, qb)
+        e1.record()
+        torch.cuda.synchronize()
+        lms = e0.elapsed_time(e1) / iters
+        res["library_scaled_mm_tflops"] = round(flops / lms / 1e9, 1)
+    except Exception as e:                                    # noqa: BLE001
+        res["library_scaled_mm_tflops"] = None
+        res["library_note"] = str(e).splitlines()[0][:120]
+    return res
+
+
 # ---------------------------------------------------------------------------------------
 def run_gpu(args, rank, world, local_rank):
     import torch
@@ -404,6 +450,9 @@ def run_gpu(args, rank, world, local_rank):
     calls = [{"call": n, "kernel": k, "ms": round(ms, 4), "GB/s": round(b / (ms * 1e-3) / GB, 1),
               "frac_of_peak": round(b / (ms * 1e-3) / GB / peak, 3)}
              for (n, k, _, b), ms in zip(plan, per_call_ms) if ms > 0]
+    mm = None
+    if not args.only:
+        mm = mm_measurement(nv, torch, o, Ma, Ka, M2, K2, peaks)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline()
@@ -424,6 +473,7 @@ def run_gpu(args, rank, world, local_rank):
                    "parallelism": f"{world} independent replica(s), no data-path collective"},
         "gpu_launches": nsteps * sum(1 for name, _, _, _ in plan if not args.only or args.only in name),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "calls": calls,
+        "fp4_mm": mm,
     }
     print(json.dumps(line), flush=True)
 

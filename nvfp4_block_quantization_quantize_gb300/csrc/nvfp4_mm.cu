@@ -28,7 +28,7 @@ constexpr int kMmThreads = 128;
 constexpr int kTileM = 128, kTileN = 128, kStepK = 64;   // K elements per MMA
 constexpr int kOpBytes = kTileM * kStepK / 2;            // 4 KB per operand slice
 constexpr uint32_t kTmemCols = 256;                       // accumulator 128 + scale columns
-constexpr uint32_t kColSfa = 128, kColSfb = 132;
+constexpr uint32_t kColSfa = 128;                         // first scale column
 constexpr long kWaitLimit = 1L << 22;                     // try_wait rounds before giving up
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -89,24 +89,34 @@ __device__ __forceinline__ float decode_scale(const float* gamax, float bound) {
     return __fdiv_rn(1.0f, enc);
 }
 
+// Pipeline: a stage holds kStageK K-steps of both operands and their scale
+// tiles; kStages stages rotate, the loads for stage t + kAhead are issued while
+// stage t is multiplied, into the slot stage t + kAhead - kStages last used,
+// whose MMAs were committed kStages - kAhead stages earlier.
+constexpr int kStageK = 2;                                // MMA K-steps (64 elements each) per stage
+constexpr int kStages = 6, kAhead = 4;
+constexpr int kSlotA = kStageK * kOpBytes;               // 8 KB
+constexpr int kSlotSf = kStageK * 512;                   // 1 KB
+constexpr int kSlotBytes = 2 * kSlotA + 2 * kSlotSf;     // 18 KB
+constexpr int kMmSmem = kStages * kSlotBytes;             // 108 KB
+constexpr uint32_t kSfColsPerStage = 2 * 4 * kStageK;    // SFA and SFB, 4 columns per K-step each
+
 template <int ODT>
 __global__ void __launch_bounds__(kMmThreads) k_mm(const uint8_t* __restrict__ A, const uint8_t* __restrict__ SA,
                                                    const uint8_t* __restrict__ B, const uint8_t* __restrict__ SB,
                                                    int64_t M, int64_t N, int64_t K, const float* gamax_a,
                                                    const float* gamax_b, float bound, void* out) {
-    __shared__ __align__(128) uint8_t sA[kOpBytes];
-    __shared__ __align__(128) uint8_t sB[kOpBytes];
-    __shared__ __align__(128) uint8_t sSA[512];
-    __shared__ __align__(128) uint8_t sSB[512];
-    __shared__ __align__(8) uint64_t bar;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ __align__(8) uint64_t done[kStages];       // MMAs of the stage in the slot have completed
     __shared__ uint32_t tmem_base;
     __shared__ int timed_out;
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTileM, n0 = static_cast<int64_t>(blockIdx.x) * kTileN;
     const int64_t row_bytes = K / 2;
-    const int64_t ksteps = K / kStepK;
-    const int64_t sf_tiles_k = K / kStepK;                // 4-column scale tiles along K (K / 16 / 4)
+    const int64_t ksteps = K / kStepK;                    // 64-element steps
+    const int64_t nstages = (ksteps + kStageK - 1) / kStageK;
+    const int64_t sf_tiles_k = ksteps;                    // 128 x 4 scale tiles along K
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -115,7 +125,7 @@ __global__ void __launch_bounds__(kMmThreads) k_mm(const uint8_t* __restrict__ A
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == 0) {
-        mbar_init(&bar);
+        for (int i = 0; i < kStages; ++i) mbar_init(&done[i]);
         timed_out = 0;
         asm volatile("fence.mbarrier_init.release.cluster;");
     }
@@ -125,56 +135,89 @@ __global__ void __launch_bounds__(kMmThreads) k_mm(const uint8_t* __restrict__ A
     const uint32_t tmem = tmem_base;
     const uint32_t idesc = instr_desc(kTileM, kTileN);
     const float alpha = __fmul_rn(decode_scale(gamax_a, bound), decode_scale(gamax_b, bound));
-    uint32_t last_parity = 0;
 
-    for (int64_t ks = 0; ks < ksteps; ++ks) {
-        // stage the A and B slices: row r's 32 bytes are core matrices (r/8, 0) and
-        // (r/8, 1), each 8 rows x 16 bytes; core (g, j) sits at (2 g + j) * 128
-        for (int c = tid; c < 2 * kTileM * 2; c += kMmThreads) {
-            const int op = c / (kTileM * 2), rc = c % (kTileM * 2);
-            const int r = rc >> 1, j = rc & 1;
-            const uint8_t* src = (op == 0 ? A + (m0 + r) * row_bytes : B + (n0 + r) * row_bytes) + ks * 32 + 16 * j;
-            uint8_t* dst = (op == 0 ? sA : sB) + ((r >> 3) * 2 + j) * 128 + (r & 7) * 16;
-            cp16(dst, src);
+    // copies of stage t into slot t % kStages: row r's 32 bytes of K-step kk are
+    // core matrices (r/8, 0), (r/8, 1) of that K-step's 4 KB block; consecutive
+    // threads read one row's contiguous bytes
+    auto issue = [&](int64_t t) {
+        if (t < nstages) {
+            uint8_t* slot = smem + (t % kStages) * kSlotBytes;
+            const int64_t k0 = t * kStageK;
+            const int nk = static_cast<int>(ksteps - k0 < kStageK ? ksteps - k0 : kStageK);
+            constexpr int kRowChunks = 2 * kStageK;        // 16-byte chunks of one row per stage
+            for (int c = tid; c < 2 * kTileM * kRowChunks; c += kMmThreads) {
+                const int op = c / (kTileM * kRowChunks), rc = c % (kTileM * kRowChunks);
+                const int r = rc / kRowChunks, q = rc % kRowChunks, kk = q >> 1, j = q & 1;
+                if (kk < nk) {
+                    const uint8_t* src =
+                        (op == 0 ? A + (m0 + r) * row_bytes : B + (n0 + r) * row_bytes) + (k0 + kk) * 32 + 16 * j;
+                    uint8_t* dst = slot + op * kSlotA + kk * kOpBytes + ((r >> 3) * 2 + j) * 128 + (r & 7) * 16;
+                    cp16(dst, src);
+                }
+            }
+            for (int c = tid; c < 2 * kStageK * 32; c += kMmThreads) {
+                const int op = c / (kStageK * 32), rc = c % (kStageK * 32), kk = rc >> 5, q = rc & 31;
+                if (kk < nk) {
+                    const uint8_t* src = (op == 0 ? SA + ((m0 / 128) * sf_tiles_k + k0 + kk) * 512
+                                                  : SB + ((n0 / 128) * sf_tiles_k + k0 + kk) * 512) + 16 * q;
+                    cp16(slot + 2 * kSlotA + op * kSlotSf + kk * 512 + 16 * q, src);
+                }
+            }
         }
-        // the step's 128 x 4 scale tiles (512 contiguous bytes each)
-        if (tid < 64) {
-            const int op = tid >> 5, q = tid & 31;
-            const uint8_t* src = (op == 0 ? SA + ((m0 / 128) * sf_tiles_k + ks) * 512
-                                          : SB + ((n0 / 128) * sf_tiles_k + ks) * 512) + 16 * q;
-            cp16((op == 0 ? sSA : sSB) + 16 * q, src);
-        }
-        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // make the stores visible to the tensor core
-        __syncthreads();
-        if (tid == 0 && !timed_out) {
-            asm volatile("tcgen05.fence::after_thread_sync;");
-            const uint64_t dsa = smem_desc(smem_addr(sSA), 0, 128);
-            const uint64_t dsb = smem_desc(smem_addr(sSB), 0, 128);
-            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + kColSfa), "l"(dsa));
-            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + kColSfb), "l"(dsb));
-            const uint64_t da = smem_desc(smem_addr(sA), 128, 256);
-            const uint64_t db = smem_desc(smem_addr(sB), 128, 256);
-            const uint32_t acc = ks > 0 ? 1u : 0u;
-            asm volatile(
-                "{\n\t.reg .pred p;\n\t"
-                "setp.ne.b32 p, %6, 0;\n\t"
-                "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(tmem),
-                "l"(da), "l"(db), "r"(idesc), "r"(tmem + kColSfa), "r"(tmem + kColSfb), "r"(acc));
-            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                smem_addr(&bar)));
-        }
-        // the MMA has read the staged slices before they are overwritten
-        last_parity = static_cast<uint32_t>(ks & 1);
-        if (!timed_out && !mbar_wait(&bar, last_parity)) timed_out = 1;
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    int64_t committed = -1;                               // last stage whose MMAs were committed
+    for (int64_t t = 0; t < kAhead; ++t) issue(t);
+    for (int64_t t = 0; t < nstages; ++t) {
+        // the slot of stage t + kAhead last held stage t + kAhead - kStages
+        const int64_t prev = t + kAhead - kStages;
+        if (prev >= 0 && !timed_out &&
+            !mbar_wait(&done[prev % kStages], static_cast<uint32_t>((prev / kStages) & 1)))
+            timed_out = 1;
+        issue(t + kAhead);
+        asm volatile("cp.async.wait_group %0;" ::"n"(kAhead) : "memory");   // stage t's own copies landed
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         if (timed_out) break;
+        if (tid == 0) {
+            asm volatile("tcgen05.fence::after_thread_sync;");
+            const uint8_t* slot = smem + (t % kStages) * kSlotBytes;
+            const uint32_t sfcol = kColSfa + static_cast<uint32_t>(t % kStages) * kSfColsPerStage;
+            const int64_t k0 = t * kStageK;
+            const int nk = static_cast<int>(ksteps - k0 < kStageK ? ksteps - k0 : kStageK);
+            for (int kk = 0; kk < nk; ++kk) {
+                const uint32_t ca = sfcol + 8 * kk, cb = ca + 4;
+                const uint64_t dsa = smem_desc(smem_addr(slot + 2 * kSlotA + kk * 512), 0, 128);
+                const uint64_t dsb = smem_desc(smem_addr(slot + 2 * kSlotA + kSlotSf + kk * 512), 0, 128);
+                asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + ca), "l"(dsa));
+                asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + cb), "l"(dsb));
+                const uint64_t da = smem_desc(smem_addr(slot + kk * kOpBytes), 128, 256);
+                const uint64_t db = smem_desc(smem_addr(slot + kSlotA + kk * kOpBytes), 128, 256);
+                const uint32_t acc = (k0 + kk) > 0 ? 1u : 0u;
+                asm volatile(
+                    "{\n\t.reg .pred p;\n\t"
+                    "setp.ne.b32 p, %6, 0;\n\t"
+                    "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(tmem),
+                    "l"(da), "l"(db), "r"(idesc), "r"(tmem + ca), "r"(tmem + cb), "r"(acc));
+            }
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                smem_addr(&done[t % kStages])));
+        }
+        committed = t;
     }
-    if (timed_out) mbar_wait(&bar, last_parity);        // once more (bounded) before tensor memory is freed
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // every MMA has completed once the last commit has arrived (a commit tracks
+    // all earlier tensor-core work of the issuing thread)
+    if (committed >= 0 &&
+        !mbar_wait(&done[committed % kStages], static_cast<uint32_t>((committed / kStages) & 1)))
+        timed_out = 1;
+    __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;");
 
     // epilogue: warp w reads accumulator lanes 32w .. 32w+31 (rows m0 + 32w + lane)
     const int64_t row = m0 + 32 * warp + (tid & 31);
+    const bool bad = timed_out != 0;
     for (int c0 = 0; c0 < kTileN; c0 += 16) {
         uint32_t v[16];
         asm volatile(
@@ -185,7 +228,7 @@ __global__ void __launch_bounds__(kMmThreads) k_mm(const uint8_t* __restrict__ A
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         float f[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) f[i] = timed_out ? __int_as_float(0x7FC00000) : __fmul_rn(__uint_as_float(v[i]), alpha);
+        for (int i = 0; i < 16; ++i) f[i] = bad ? __int_as_float(0x7FC00000) : __fmul_rn(__uint_as_float(v[i]), alpha);
         if (ODT == NVFP4_F32) {
             float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + row * N + n0 + c0);
 #pragma unroll
@@ -214,10 +257,16 @@ int launch_mm(const uint8_t* A, const uint8_t* SA, const uint8_t* B, const uint8
               void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid(static_cast<unsigned>(N / kTileN), static_cast<unsigned>(M / kTileM));
+    static bool configured = false;
+    if (!configured) {
+        cudaFuncSetAttribute(k_mm<NVFP4_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmSmem);
+        cudaFuncSetAttribute(k_mm<NVFP4_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmSmem);
+        configured = true;
+    }
     if (out_dtype == NVFP4_F32)
-        k_mm<NVFP4_F32><<<grid, kMmThreads, 0, s>>>(A, SA, B, SB, M, N, K, gamax_a, gamax_b, bound, out);
+        k_mm<NVFP4_F32><<<grid, kMmThreads, kMmSmem, s>>>(A, SA, B, SB, M, N, K, gamax_a, gamax_b, bound, out);
     else
-        k_mm<NVFP4_BF16><<<grid, kMmThreads, 0, s>>>(A, SA, B, SB, M, N, K, gamax_a, gamax_b, bound, out);
+        k_mm<NVFP4_BF16><<<grid, kMmThreads, kMmSmem, s>>>(A, SA, B, SB, M, N, K, gamax_a, gamax_b, bound, out);
     return static_cast<int>(cudaGetLastError());
 }
 
