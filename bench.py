@@ -52,6 +52,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--only", default=None,
                    help="run only the step's calls whose name contains this text (profiling)")
+    p.add_argument("--mm-only", action="store_true",
+                   help="only the FP4 product measurement (quantize A and W2, then time nvfp4_mm)")
     return p.parse_args()
 
 
@@ -258,6 +260,25 @@ def mm_measurement(nv, torch, out, Ma, Ka, M2, K2, peaks, iters=5):
         res["library_scaled_mm_tflops"] = None
         res["library_note"] = str(e).splitlines()[0][:120]
     return res
+
+
+def run_mm_only(args, local_rank):
+    import torch
+    import nvfp4_block_quantization_quantize_gb300 as nv
+    torch.cuda.set_device(local_rank)
+    nv.build()
+    nv.load_library()
+    c5 = c5_inputs()
+    dev = torch.device("cuda", local_rank)
+    up = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)   # noqa: E731
+    A, W2 = up(c5.A), up(c5.W2)
+    qa = nv.nvfp4_quantize(A)
+    q2 = nv.nvfp4_quantize(W2, rounding="sr", seed=0, step=7)
+    out = {"car": qa["codes"], "sar": qa["scales"], "c2s": q2["codes"], "s2s": q2["scales"]}
+    mm = mm_measurement(nv, torch, out, A.shape[0], A.shape[1], W2.shape[0], W2.shape[1], measured_peaks(),
+                        iters=args.steps)
+    print(json.dumps({"metric": "fp4 GEMM TFLOP/s", "value": mm["tflops"], "unit": "TFLOP/s",
+                      "higher_is_better": True, "fp4_mm": mm}), flush=True)
 
 
 # ---------------------------------------------------------------------------------------
@@ -487,6 +508,10 @@ def main():
         if world > 1 and rank != 0:
             return
         run_reference(args, rank, world)
+        return
+    if args.mm_only:
+        if rank == 0:
+            run_mm_only(args, local_rank)
         return
     if world > 1:
         import torch
