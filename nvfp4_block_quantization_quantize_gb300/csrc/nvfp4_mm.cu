@@ -16,6 +16,8 @@
 // wait runs out writes NaN to its tile.  The epilogue reads the accumulator
 // with tcgen05.ld and multiplies by both per-tensor decode scales.
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -25,25 +27,26 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kMmThreads = 128;
-constexpr int kTileM = 128, kTileN = 128, kStepK = 64;   // K elements per MMA
-constexpr int kOpBytes = kTileM * kStepK / 2;            // 4 KB per operand slice
-constexpr uint32_t kTmemCols = 256;                       // accumulator 128 + scale columns
-constexpr uint32_t kColSfa = 128;                         // first scale column
+constexpr int kTileM = 128, kStepK = 64;                 // K elements per MMA
+constexpr uint32_t kColSfa = 256;                         // first scale column (after the two accumulators)
 constexpr long kWaitLimit = 1L << 22;                     // try_wait rounds before giving up
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// shared-memory matrix descriptor: no swizzle, K-major core matrices of 8 rows
-// x 16 bytes; lbo = byte step between core matrices along K, sbo = along M/N
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// shared-memory matrix descriptor, K-major: lbo = byte step between core
+// matrices along K, sbo = between 8-row groups along M/N; layout 0 = no
+// swizzle (core matrices of 8 rows x 16 bytes), 2 = 128-byte swizzle (rows
+// of 128 bytes, 8-row atoms of 1 KB, 1 KB-aligned)
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout = 0) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
     d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
     d |= 1ull << 46;                                      // descriptor version for sm_100 family
-    return d;                                             // base offset 0, layout type 0 (no swizzle)
+    d |= static_cast<uint64_t>(layout & 7u) << 61;        // base offset 0
+    return d;
 }
 
 // instruction descriptor for .kind::mxf4nvf4: A and B e2m1 (format 1), both
@@ -76,9 +79,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return false;
 }
 
-__device__ __forceinline__ void cp16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
 
 // decode scale S_dec = 1 / min(6 * bound / A, FLT_MAX) of a per-tensor amax
 // (1 without one, and when A is not a positive finite number)
@@ -89,136 +89,165 @@ __device__ __forceinline__ float decode_scale(const float* gamax, float bound) {
     return __fdiv_rn(1.0f, enc);
 }
 
-// Pipeline: a stage holds kStageK K-steps of both operands and their scale
-// tiles; kStages stages rotate, the loads for stage t + kAhead are issued while
-// stage t is multiplied, into the slot stage t + kAhead - kStages last used,
-// whose MMAs were committed kStages - kAhead stages earlier.
-constexpr int kStageK = 2;                                // MMA K-steps (64 elements each) per stage
-constexpr int kStages = 6, kAhead = 4;
-constexpr int kSlotA = kStageK * kOpBytes;               // 8 KB
-constexpr int kSlotSf = kStageK * 512;                   // 1 KB
-constexpr int kSlotBytes = 2 * kSlotA + 2 * kSlotSf;     // 18 KB
-constexpr int kMmSmem = kStages * kSlotBytes;             // 108 KB
-constexpr uint32_t kSfColsPerStage = 2 * 4 * kStageK;    // SFA and SFB, 4 columns per K-step each
+// Pipeline (warp-specialised).  A CTA owns a 128 x 256 tile of C as two
+// 128 x 128 accumulators in tensor memory.  Thread 0 (the producer) loads a
+// stage -- kStageK K-steps (128 bytes of every row) of A (128 rows) and B (256
+// rows), one TMA box each with the 128-byte swizzle, which is the layout the
+// MMA descriptor's 128-byte-swizzle mode reads (a K-step starts 32 bytes
+// further into the 1 KB atoms), and the matching 512-byte scale tiles by bulk
+// copies -- into one of kStages slots, signalling the slot's `full` barrier by
+// transaction count.  Thread 32 (the MMA issuer) waits for `full`, copies the
+// scale tiles to tensor memory and issues two MMAs per K-step, then commits to
+// the slot's `empty` barrier, which the producer waits on before refilling the
+// slot.  A last commit signals `acc`; all four warps then read the
+// accumulators.  When N is not a multiple of 256 the last CTA of a row of
+// tiles computes only its first half (TMA fills the rows past N with zeros).
+constexpr int kTileN2 = 256;                              // two 128-column halves
+constexpr int kStageK = 4;                                // MMA K-steps (64 elements = 32 bytes each) per stage
+constexpr int kStages = 4;
+constexpr int kSlotA = kTileM * 128;                      // 128 rows x 128 bytes (128-byte swizzle): 16 KB
+constexpr int kSlotB = kTileN2 * 128;                     // 32 KB
+constexpr int kSlotSfa = kStageK * 512, kSlotSfb = 2 * kStageK * 512;
+constexpr int kSlotBytes = kSlotA + kSlotB + kSlotSfa + kSlotSfb;   // 54 KB
+constexpr int kMmSmem = kStages * kSlotBytes + 1024;                 // + alignment slack
+constexpr uint32_t kSfColsPerStep = 12;                   // SFA, SFB half 0, SFB half 1: 4 columns each
+constexpr uint32_t kTmemCols2 = 512;
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_f4(uint32_t d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                       uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+        "l"(da), "l"(db), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc));
+}
 
 template <int ODT>
-__global__ void __launch_bounds__(kMmThreads) k_mm(const uint8_t* __restrict__ A, const uint8_t* __restrict__ SA,
-                                                   const uint8_t* __restrict__ B, const uint8_t* __restrict__ SB,
-                                                   int64_t M, int64_t N, int64_t K, const float* gamax_a,
-                                                   const float* gamax_b, float bound, void* out) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ __align__(8) uint64_t done[kStages];       // MMAs of the stage in the slot have completed
+__global__ void __launch_bounds__(kMmThreads, 1)
+    k_mm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+         const uint8_t* __restrict__ SA, const uint8_t* __restrict__ SB, int64_t M, int64_t N, int64_t K,
+         const float* gamax_a, const float* gamax_b, float bound, void* out) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], accb;
     __shared__ uint32_t tmem_base;
     __shared__ int timed_out;
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTileM, n0 = static_cast<int64_t>(blockIdx.x) * kTileN;
-    const int64_t row_bytes = K / 2;
-    const int64_t ksteps = K / kStepK;                    // 64-element steps
+    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTileM, n0 = static_cast<int64_t>(blockIdx.x) * kTileN2;
+    const bool half1 = n0 + 128 < N;                     // the second 128-column half exists
+    const int64_t ksteps = K / kStepK;
     const int64_t nstages = (ksteps + kStageK - 1) / kStageK;
-    const int64_t sf_tiles_k = ksteps;                    // 128 x 4 scale tiles along K
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(&tmem_base)),
-                     "r"(kTmemCols));
+                     "r"(kTmemCols2));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) mbar_init(&done[i]);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i]);
+            mbar_init(&empty[i]);
+        }
+        mbar_init(&accb);
         timed_out = 0;
         asm volatile("fence.mbarrier_init.release.cluster;");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapA)));
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapB)));
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;");
     const uint32_t tmem = tmem_base;
-    const uint32_t idesc = instr_desc(kTileM, kTileN);
-    const float alpha = __fmul_rn(decode_scale(gamax_a, bound), decode_scale(gamax_b, bound));
+    const uint32_t idesc = instr_desc(kTileM, 128);
 
-    // copies of stage t into slot t % kStages: row r's 32 bytes of K-step kk are
-    // core matrices (r/8, 0), (r/8, 1) of that K-step's 4 KB block; consecutive
-    // threads read one row's contiguous bytes
-    auto issue = [&](int64_t t) {
-        if (t < nstages) {
-            uint8_t* slot = smem + (t % kStages) * kSlotBytes;
+    if (tid == 0) {
+        // ---- producer ----
+        for (int64_t t = 0; t < nstages; ++t) {
+            const int s = static_cast<int>(t % kStages);
+            if (t >= kStages && !mbar_wait(&empty[s], static_cast<uint32_t>(((t / kStages) - 1) & 1))) {
+                timed_out = 1;
+                break;
+            }
             const int64_t k0 = t * kStageK;
             const int nk = static_cast<int>(ksteps - k0 < kStageK ? ksteps - k0 : kStageK);
-            constexpr int kRowChunks = 2 * kStageK;        // 16-byte chunks of one row per stage
-            for (int c = tid; c < 2 * kTileM * kRowChunks; c += kMmThreads) {
-                const int op = c / (kTileM * kRowChunks), rc = c % (kTileM * kRowChunks);
-                const int r = rc / kRowChunks, q = rc % kRowChunks, kk = q >> 1, j = q & 1;
-                if (kk < nk) {
-                    const uint8_t* src =
-                        (op == 0 ? A + (m0 + r) * row_bytes : B + (n0 + r) * row_bytes) + (k0 + kk) * 32 + 16 * j;
-                    uint8_t* dst = slot + op * kSlotA + kk * kOpBytes + ((r >> 3) * 2 + j) * 128 + (r & 7) * 16;
-                    cp16(dst, src);
-                }
-            }
-            for (int c = tid; c < 2 * kStageK * 32; c += kMmThreads) {
-                const int op = c / (kStageK * 32), rc = c % (kStageK * 32), kk = rc >> 5, q = rc & 31;
-                if (kk < nk) {
-                    const uint8_t* src = (op == 0 ? SA + ((m0 / 128) * sf_tiles_k + k0 + kk) * 512
-                                                  : SB + ((n0 / 128) * sf_tiles_k + k0 + kk) * 512) + 16 * q;
-                    cp16(slot + 2 * kSlotA + op * kSlotSf + kk * 512 + 16 * q, src);
-                }
-            }
+            uint8_t* slot = smem + s * kSlotBytes;
+            mbar_expect_tx(&full[s], static_cast<uint32_t>(kSlotA + kSlotB + nk * (512 + (half1 ? 1024 : 512))));
+            tma_2d(slot, &mapA, static_cast<int>(k0 * 32), static_cast<int>(m0), &full[s]);
+            tma_2d(slot + kSlotA, &mapB, static_cast<int>(k0 * 32), static_cast<int>(n0), &full[s]);
+            bulk_copy(slot + kSlotA + kSlotB, SA + ((m0 / 128) * ksteps + k0) * 512, nk * 512, &full[s]);
+            bulk_copy(slot + kSlotA + kSlotB + kSlotSfa, SB + ((n0 / 128) * ksteps + k0) * 512, nk * 512, &full[s]);
+            if (half1)
+                bulk_copy(slot + kSlotA + kSlotB + kSlotSfa + kStageK * 512, SB + ((n0 / 128 + 1) * ksteps + k0) * 512,
+                          nk * 512, &full[s]);
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-
-    int64_t committed = -1;                               // last stage whose MMAs were committed
-    for (int64_t t = 0; t < kAhead; ++t) issue(t);
-    for (int64_t t = 0; t < nstages; ++t) {
-        // the slot of stage t + kAhead last held stage t + kAhead - kStages
-        const int64_t prev = t + kAhead - kStages;
-        if (prev >= 0 && !timed_out &&
-            !mbar_wait(&done[prev % kStages], static_cast<uint32_t>((prev / kStages) & 1)))
-            timed_out = 1;
-        issue(t + kAhead);
-        asm volatile("cp.async.wait_group %0;" ::"n"(kAhead) : "memory");   // stage t's own copies landed
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
-        if (timed_out) break;
-        if (tid == 0) {
+    } else if (tid == 32) {
+        // ---- MMA issuer ----
+        int64_t t = 0;
+        for (; t < nstages; ++t) {
+            const int s = static_cast<int>(t % kStages);
+            if (timed_out || !mbar_wait(&full[s], static_cast<uint32_t>((t / kStages) & 1))) {
+                timed_out = 1;
+                break;
+            }
             asm volatile("tcgen05.fence::after_thread_sync;");
-            const uint8_t* slot = smem + (t % kStages) * kSlotBytes;
-            const uint32_t sfcol = kColSfa + static_cast<uint32_t>(t % kStages) * kSfColsPerStage;
+            const uint8_t* slot = smem + s * kSlotBytes;
             const int64_t k0 = t * kStageK;
             const int nk = static_cast<int>(ksteps - k0 < kStageK ? ksteps - k0 : kStageK);
             for (int kk = 0; kk < nk; ++kk) {
-                const uint32_t ca = sfcol + 8 * kk, cb = ca + 4;
-                const uint64_t dsa = smem_desc(smem_addr(slot + 2 * kSlotA + kk * 512), 0, 128);
-                const uint64_t dsb = smem_desc(smem_addr(slot + 2 * kSlotA + kSlotSf + kk * 512), 0, 128);
-                asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + ca), "l"(dsa));
-                asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + cb), "l"(dsb));
-                const uint64_t da = smem_desc(smem_addr(slot + kk * kOpBytes), 128, 256);
-                const uint64_t db = smem_desc(smem_addr(slot + kSlotA + kk * kOpBytes), 128, 256);
+                const uint32_t c = kColSfa + static_cast<uint32_t>(s * kStageK + kk) * kSfColsPerStep;
+                const uint8_t* sf = slot + kSlotA + kSlotB;
+                asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + c),
+                             "l"(smem_desc(smem_addr(sf + kk * 512), 0, 128)));
+                asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + c + 4),
+                             "l"(smem_desc(smem_addr(sf + kSlotSfa + kk * 512), 0, 128)));
+                if (half1)
+                    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + c + 8),
+                                 "l"(smem_desc(smem_addr(sf + kSlotSfa + kStageK * 512 + kk * 512), 0, 128)));
+                const uint64_t da = smem_desc(smem_addr(slot + kk * 32), 16, 1024, 2);
                 const uint32_t acc = (k0 + kk) > 0 ? 1u : 0u;
-                asm volatile(
-                    "{\n\t.reg .pred p;\n\t"
-                    "setp.ne.b32 p, %6, 0;\n\t"
-                    "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(tmem),
-                    "l"(da), "l"(db), "r"(idesc), "r"(tmem + ca), "r"(tmem + cb), "r"(acc));
+                mma_f4(tmem, da, smem_desc(smem_addr(slot + kSlotA + kk * 32), 16, 1024, 2), idesc, tmem + c,
+                       tmem + c + 4, acc);
+                if (half1)
+                    mma_f4(tmem + 128, da, smem_desc(smem_addr(slot + kSlotA + 128 * 128 + kk * 32), 16, 1024, 2),
+                           idesc, tmem + c, tmem + c + 8, acc);
             }
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                smem_addr(&done[t % kStages])));
+                smem_addr(&empty[s])));
         }
-        committed = t;
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(&accb)));
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    // every MMA has completed once the last commit has arrived (a commit tracks
-    // all earlier tensor-core work of the issuing thread)
-    if (committed >= 0 &&
-        !mbar_wait(&done[committed % kStages], static_cast<uint32_t>((committed / kStages) & 1)))
-        timed_out = 1;
-    __syncthreads();
+    // ---- epilogue: every warp reads its 32 accumulator lanes ----
+    if (!mbar_wait(&accb, 0)) timed_out = 1;
+    __syncwarp();
     asm volatile("tcgen05.fence::after_thread_sync;");
-
-    // epilogue: warp w reads accumulator lanes 32w .. 32w+31 (rows m0 + 32w + lane)
+    const float alpha = __fmul_rn(decode_scale(gamax_a, bound), decode_scale(gamax_b, bound));
     const int64_t row = m0 + 32 * warp + (tid & 31);
     const bool bad = timed_out != 0;
-    for (int c0 = 0; c0 < kTileN; c0 += 16) {
+    const int ncols = half1 ? kTileN2 : 128;
+    for (int c0 = 0; c0 < ncols; c0 += 16) {
         uint32_t v[16];
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
@@ -247,7 +276,26 @@ __global__ void __launch_bounds__(kMmThreads) k_mm(const uint8_t* __restrict__ A
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols2));
+}
+
+// 2D map of a [rows, K/2]-byte code matrix, boxes of box_rows x 128 bytes, 128-byte swizzle
+bool encode_codes_map(CUtensorMap* map, const uint8_t* codes, int64_t rows, int64_t K, int box_rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void**>(&encode), 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return false;
+    }
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -256,7 +304,10 @@ int launch_mm(const uint8_t* A, const uint8_t* SA, const uint8_t* B, const uint8
               int64_t K, const float* gamax_a, const float* gamax_b, float bound, void* out, int out_dtype,
               void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const dim3 grid(static_cast<unsigned>(N / kTileN), static_cast<unsigned>(M / kTileM));
+    CUtensorMap mapA, mapB;
+    if (!encode_codes_map(&mapA, A, M, K, kTileM) || !encode_codes_map(&mapB, B, N, K, kTileN2))
+        return static_cast<int>(cudaErrorInvalidValue);
+    const dim3 grid(static_cast<unsigned>((N + kTileN2 - 1) / kTileN2), static_cast<unsigned>(M / kTileM));
     static bool configured = false;
     if (!configured) {
         cudaFuncSetAttribute(k_mm<NVFP4_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmSmem);
@@ -264,9 +315,9 @@ int launch_mm(const uint8_t* A, const uint8_t* SA, const uint8_t* B, const uint8
         configured = true;
     }
     if (out_dtype == NVFP4_F32)
-        k_mm<NVFP4_F32><<<grid, kMmThreads, kMmSmem, s>>>(A, SA, B, SB, M, N, K, gamax_a, gamax_b, bound, out);
+        k_mm<NVFP4_F32><<<grid, kMmThreads, kMmSmem, s>>>(mapA, mapB, SA, SB, M, N, K, gamax_a, gamax_b, bound, out);
     else
-        k_mm<NVFP4_BF16><<<grid, kMmThreads, kMmSmem, s>>>(A, SA, B, SB, M, N, K, gamax_a, gamax_b, bound, out);
+        k_mm<NVFP4_BF16><<<grid, kMmThreads, kMmSmem, s>>>(mapA, mapB, SA, SB, M, N, K, gamax_a, gamax_b, bound, out);
     return static_cast<int>(cudaGetLastError());
 }
 
