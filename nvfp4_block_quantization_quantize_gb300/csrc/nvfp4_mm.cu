@@ -5,16 +5,13 @@
 // Correctness: the tensor-core path agrees with the dequantize path).  A and B
 // are the quantizer's rowwise outputs: codes [M, K/2] and [N, K/2] (two e2m1
 // codes per byte, element 2j in the low nibble) and their scale bytes re-laid
-// out by nvfp4_scales_to_mma (128 x 4 tiles).  One CTA of 128 threads owns a
-// 128 x 128 tile of C; for each 64-element step of K it stages the A and B
-// slices in shared memory in the no-swizzle K-major core-matrix layout (8 rows
-// x 16 bytes per core matrix), copies the step's two 512-byte scale tiles into
-// tensor memory (tcgen05.cp 32x128b.warpx4: each lane quadrant gets the 128 x
-// 4 tile, a lane finds its row's four scales in the column of its quadrant),
-// and one thread issues the MMA, accumulating in fp32 in tensor memory.
-// Completion is tracked with an mbarrier whose waits are bounded; a CTA whose
-// wait runs out writes NaN to its tile.  The epilogue reads the accumulator
-// with tcgen05.ld and multiplies by both per-tensor decode scales.
+// out by nvfp4_scales_to_mma (128 x 4 tiles).  Each 512-byte scale tile goes
+// to tensor memory with tcgen05.cp 32x128b.warpx4: every lane quadrant gets
+// the 128 x 4 tile, and a lane finds its row's four scales in the column of
+// its quadrant.  Products accumulate in fp32 in tensor memory.  Every wait on
+// an mbarrier is bounded; a CTA whose wait runs out writes NaN to its tile.
+// The epilogue reads the accumulator with tcgen05.ld and multiplies by both
+// per-tensor decode scales.
 #include <cstdint>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -89,19 +86,20 @@ __device__ __forceinline__ float decode_scale(const float* gamax, float bound) {
     return __fdiv_rn(1.0f, enc);
 }
 
-// Pipeline (warp-specialised).  A CTA owns a 128 x 256 tile of C as two
-// 128 x 128 accumulators in tensor memory.  Thread 0 (the producer) loads a
+// Pipeline (warp-specialised).  A CTA owns a 128 x 256 tile of C, one fp32
+// accumulator of 256 tensor-memory columns.  Thread 0 (the producer) loads a
 // stage -- kStageK K-steps (128 bytes of every row) of A (128 rows) and B (256
 // rows), one TMA box each with the 128-byte swizzle, which is the layout the
 // MMA descriptor's 128-byte-swizzle mode reads (a K-step starts 32 bytes
 // further into the 1 KB atoms), and the matching 512-byte scale tiles by bulk
 // copies -- into one of kStages slots, signalling the slot's `full` barrier by
 // transaction count.  Thread 32 (the MMA issuer) waits for `full`, copies the
-// scale tiles to tensor memory and issues two MMAs per K-step, then commits to
-// the slot's `empty` barrier, which the producer waits on before refilling the
-// slot.  A last commit signals `acc`; all four warps then read the
-// accumulators.  When N is not a multiple of 256 the last CTA of a row of
-// tiles computes only its first half (TMA fills the rows past N with zeros).
+// scale tiles to tensor memory (B's rows 128-255 four columns after rows
+// 0-127) and issues one N = 256 MMA per K-step, then commits to the slot's
+// `empty` barrier, which the producer waits on before refilling the slot.  A
+// last commit signals `acc`; all four warps then read the accumulator.  When
+// N is not a multiple of 256 the last CTA of a row of tiles computes only its
+// first 128 columns (N = 128 MMAs; TMA fills the rows past N with zeros).
 constexpr int kTileN2 = 256;                              // two 128-column halves
 constexpr int kStageK = 4;                                // MMA K-steps (64 elements = 32 bytes each) per stage
 constexpr int kStages = 4;
@@ -180,7 +178,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;");
     const uint32_t tmem = tmem_base;
-    const uint32_t idesc = instr_desc(kTileM, 128);
+    const uint32_t idesc = instr_desc(kTileM, half1 ? kTileN2 : 128);
 
     if (tid == 0) {
         // ---- producer ----
@@ -227,11 +225,9 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                                  "l"(smem_desc(smem_addr(sf + kSlotSfa + kStageK * 512 + kk * 512), 0, 128)));
                 const uint64_t da = smem_desc(smem_addr(slot + kk * 32), 16, 1024, 2);
                 const uint32_t acc = (k0 + kk) > 0 ? 1u : 0u;
+                // one MMA over both halves (N = 256; B's scales for rows 128-255 in the next 4 columns)
                 mma_f4(tmem, da, smem_desc(smem_addr(slot + kSlotA + kk * 32), 16, 1024, 2), idesc, tmem + c,
                        tmem + c + 4, acc);
-                if (half1)
-                    mma_f4(tmem + 128, da, smem_desc(smem_addr(slot + kSlotA + 128 * 128 + kk * 32), 16, 1024, 2),
-                           idesc, tmem + c, tmem + c + 8, acc);
             }
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                 smem_addr(&empty[s])));
