@@ -146,6 +146,27 @@ def _empty(shape, dtype, dev):
     return torch.empty(shape, dtype=dtype, device=dev)
 
 
+def _to_host(ts: dict, stream=None) -> dict:
+    """Device tensors -> pinned host tensors: asynchronous copies on the call's
+    stream, then one wait for that stream, so the results are ready on return."""
+    out = {}
+    for k, v in ts.items():
+        h = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+        h.copy_(v, non_blocking=True)
+        out[k] = h
+    _sync(stream)
+    return out
+
+
+def _sync(stream=None):
+    if stream is None:
+        torch.cuda.current_stream().synchronize()
+    elif isinstance(stream, torch.cuda.Stream):
+        stream.synchronize()
+    else:
+        torch.cuda.synchronize()
+
+
 def _default_bound(err_mode: int, scale_bound):
     if scale_bound is not None:
         return float(scale_bound)
@@ -199,9 +220,9 @@ def nvfp4_quantize(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=No
     if g is not None:
         out["gamax"] = g
     if host:
-        out = {k: v.cpu() for k, v in out.items()}
         if residual is not None and rd is not residual:
-            residual.copy_(rd.cpu())
+            residual.copy_(rd, non_blocking=True)
+        out = _to_host(out, stream)
     return out
 
 
@@ -232,9 +253,9 @@ def nvfp4_qdq(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=None, s
     if g is not None:
         res["gamax"] = g
     if host:
-        res = {k: v.cpu() for k, v in res.items()}
         if residual is not None and rd is not residual:
-            residual.copy_(rd.cpu())
+            residual.copy_(rd, non_blocking=True)
+        res = _to_host(res, stream)
         if out is not None:
             out.copy_(res["out"])
             res["out"] = out
@@ -262,7 +283,7 @@ def nvfp4_dequantize(codes: torch.Tensor, scales: torch.Tensor, M: int, K: int, 
     rc = lib.nvfp4_dequantize(_ptr(c), _ptr(s), M, K, gm, _ptr(g), bound, _ptr(o), od,
                               _stream(stream))
     _check(lib, rc)
-    return o.cpu() if host else o
+    return _to_host({"o": o}, stream)["o"] if host else o
 
 
 def nvfp4_amax(x: torch.Tensor, *, residual=None, per_row: bool = False, out=None,
