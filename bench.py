@@ -32,6 +32,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -372,7 +373,7 @@ def run_gpu(args, rank, world, local_rank):
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in plan] for _ in range(nsteps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clk_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_rank{rank}.csv")
+    clk_path = os.path.join(tempfile.gettempdir(), f"nvfp4_bench_clocks_rank{rank}.csv")
     os.makedirs(os.path.dirname(clk_path), exist_ok=True)
     proc, fh = clocks_sampler_start(clk_path)
     time.sleep(0.5 if proc else 0)
