@@ -304,11 +304,13 @@ int launch_mm(const uint8_t* A, const uint8_t* SA, const uint8_t* B, const uint8
     if (!encode_codes_map(&mapA, A, M, K, kTileM) || !encode_codes_map(&mapB, B, N, K, kTileN2))
         return static_cast<int>(cudaErrorInvalidValue);
     const dim3 grid(static_cast<unsigned>((N + kTileN2 - 1) / kTileN2), static_cast<unsigned>(M / kTileM));
-    static bool configured = false;
-    if (!configured) {
+    static thread_local int configured_dev = -1;         // the attribute is per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_dev != dev) {
         cudaFuncSetAttribute(k_mm<NVFP4_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmSmem);
         cudaFuncSetAttribute(k_mm<NVFP4_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmSmem);
-        configured = true;
+        configured_dev = dev;
     }
     if (out_dtype == NVFP4_F32)
         k_mm<NVFP4_F32><<<grid, kMmThreads, kMmSmem, s>>>(mapA, mapB, SA, SB, M, N, K, gamax_a, gamax_b, bound, out);
