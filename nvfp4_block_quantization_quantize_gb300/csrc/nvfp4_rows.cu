@@ -20,21 +20,36 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// One 1x16 group y of block-row blk: its block amax is tile_amax(the group's
-// absmax) and its four-over-six error sums go through tile_sums (identities
-// for 1x16 blocks; the 16x16 tile's reductions otherwise).  Nothing is stored
-// when !live (a group past the tensor's last column block).
+// The block amax of a 1x16 group is its own absmax.
+struct OwnAmax {
+    static constexpr bool kSplit = false;
+    float v;
+    __device__ void post(float b) { v = b; }
+    __device__ float get() const { return v; }
+};
+
+// One 1x16 group y of block-row blk: tile_amax.post(the group's absmax) then
+// tile_amax.get() gives its block amax, and its four-over-six error sums go
+// through tile_sums (identities for 1x16 blocks; the 16x16 tile's reductions
+// otherwise).  With a split tile amax (kSplit) the stochastic-rounding draws,
+// which do not depend on the scale, are made between post and get.  Nothing
+// is stored when !live (a group past the tensor's last column block).
 template <int DT, int ERR, int RND, bool EF, bool GS, class TileAmax, class TileSums>
 __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool live, float* y,
                                            const GScale& g, float C, const O6Tab* tab,
                                            const float* rt, uint64_t idx_base, int64_t bpr,
-                                           TileAmax tile_amax, TileSums tile_sums) {
+                                           TileAmax& tile_amax, TileSums tile_sums) {
     GScale gb = g;
     if (a.gamax_mode == NVFP4_GAMAX_ROW_GIVEN) {
         gb.A = a.gamax[blk / bpr];
         global_scales(gb.A, a.bound, gb.Senc, gb.Sdec);
     }
-    const float b = tile_amax(absmax16(y));
+    constexpr bool EARLY = TileAmax::kSplit && ERR == NVFP4_ERR_NONE && RND == NVFP4_SR;
+    const uint64_t idx0 = idx_base + static_cast<uint64_t>(blk) * 16u;
+    tile_amax.post(absmax16(y));
+    uint32_t wd[16];
+    if constexpr (EARLY) sr_words16(idx0, a.seed, a.step, wd);
+    const float b = tile_amax.get();
     uint32_t w0, w1, sf;
     float d, q[16];
     const bool wq = EF || a.dq_bf16;
@@ -44,8 +59,10 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool
         sf = e4m3_encode(min_nd(s6f, 448.0f));
         d = e4m3_decode(sf);
         const float D = GS ? mul_rn(d, gb.Sdec) : d;
-        encode_plain16<RND>(y, D, b, idx_base + static_cast<uint64_t>(blk) * 16u, a.seed, a.step,
-                            w0, w1, GS ? nullptr : rt, sf, q, wq);
+        if constexpr (EARLY)
+            encode_plain16_words<RND>(y, D, b, wd, w0, w1, GS ? nullptr : rt, sf, q, wq);
+        else
+            encode_plain16<RND>(y, D, b, idx0, a.seed, a.step, w0, w1, GS ? nullptr : rt, sf, q, wq);
     } else {
         four_over_six16<ERR>(y, b, gb, C, tab, w0, w1, sf, d, tile_sums);
     }
@@ -137,8 +154,9 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
         }
-        rows_block<DT, ERR, RND, EF, GS>(a, blk, true, y, g, C, tp, rtab, idx_base, bpr,
-                                         [](float b) { return b; }, [](float&, float&) {});
+        OwnAmax own;
+        rows_block<DT, ERR, RND, EF, GS>(a, blk, true, y, g, C, tp, rtab, idx_base, bpr, own,
+                                         [](float&, float&) {});
         stage = stage == S - 1 ? 0 : stage + 1;
     }
     cp_async_wait<0>();
@@ -153,6 +171,46 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
 // (band-major) persistently, each thread fetching its group one step ahead
 // (the per-thread copy pipeline of k_rows); the reductions' shared buffers
 // alternate between steps, so one barrier per reduction suffices.
+// The tile amax of k_band16, split in two phases on an mbarrier that all
+// threads arrive on once per step: post() reduces the lane pair and publishes
+// the warp's maximum, then arrives; get() waits for the step's phase (with an
+// iteration limit) and reduces the 8 warps.  The partial maxima alternate
+// between two buffers by step parity: a thread writes a step's buffer only
+// after it arrived for the previous step, which it did after reading the
+// buffer two steps back.
+struct BandAmax {
+    static constexpr bool kSplit = true;
+    float (*red)[8][16];
+    uint64_t* bar;
+    int warp, lane, t;
+    uint32_t step;                               // this thread's step count
+    __device__ void post(float b) {
+        b = max_nd(b, __shfl_xor_sync(kFullMask, b, 16));
+        if (lane < 16) red[step & 1][warp][t] = b;
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
+                     : "memory");
+    }
+    __device__ float get() {
+        const uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+        for (int it = 0; it < (1 << 22); ++it) {
+            uint32_t ok;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(ok)
+                : "r"(addr), "r"(step & 1u)
+                : "memory");
+            if (ok) break;
+        }
+        float m = red[step & 1][0][t];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) m = max_nd(m, red[step & 1][w][t]);
+        ++step;
+        return m;
+    }
+};
+
 struct BandCursor {      // CTA-uniform step: (band, 256-column chunk)
     int64_t band, chunk, nch, dband, dchunk;
     __device__ void init(int64_t u, int64_t nch_, int64_t stride) {
@@ -180,6 +238,14 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
     __shared__ float red[2][8][16];                                   // [step parity][warp][tile]
     __shared__ float esum[ERR != NVFP4_ERR_NONE ? 2 : 1][2][16][16];  // [parity][cand][row][tile]
+    __shared__ __align__(8) uint64_t amax_bar;
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(
+                         static_cast<uint32_t>(__cvta_generic_to_shared(&amax_bar))),
+                     "r"(static_cast<uint32_t>(blockDim.x)));
+        asm volatile("fence.mbarrier_init.release.cluster;");
+    }
+    __syncthreads();
     if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
     const int64_t nb = a.K / 16;
     const int64_t nch = (nb + 15) / 16;
@@ -233,6 +299,7 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
         ahead.advance();
     }
     int stage = 0, par = 0;
+    BandAmax tile_amax{red, &amax_bar, warp, lane, t, 0u};
     for (; cur.band < nbands; cur.advance()) {
         issue(ahead, stage == 0 ? S - 1 : stage - 1);
         ahead.advance();
@@ -252,15 +319,6 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) y[i] = 0.0f;
         }
-        auto tile_amax = [&](float b) {
-            b = max_nd(b, __shfl_xor_sync(kFullMask, b, 16));
-            if (lane < 16) red[par][warp][t] = b;
-            __syncthreads();
-            float m = red[par][0][t];
-#pragma unroll
-            for (int w = 1; w < 8; ++w) m = max_nd(m, red[par][w][t]);
-            return m;
-        };
         auto tile_sums = [&](float& E6, float& E4) {
             if constexpr (ERR != NVFP4_ERR_NONE) {
                 esum[par][0][rr][t] = E6;
