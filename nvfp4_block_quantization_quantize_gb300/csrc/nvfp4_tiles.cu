@@ -13,14 +13,17 @@
 //               AND the column sums accumulated in row order, so x^T's
 //               element-order sums are exact too; then store).  Row and column
 //               choices are made from the same per-element errors; the
-//               columnwise codes are transposed in registers.  Loads of a
-//               row by a warp cover 32 consecutive tiles: fully coalesced.
-//               The row loops stay rolled (an unrolled kernel overflowed the
-//               instruction cache); row sums and code words wait in shared
-//               memory until the tile's choices are known (both
-//               candidates' code words too, so x is read only twice); each
-//               thread streams its 32 row reads through a 4-slot ring of
-//               asynchronous copies, three reads ahead.
+//               columnwise codes are transposed in registers.  A CTA is 4
+//               bands (one per warp) x 32 tiles: loads of a row by a warp
+//               cover 32 consecutive tiles (fully coalesced), and the
+//               columnwise output, staged in shared memory, leaves as one
+//               32-byte run per column (4 bands x 8 bytes) instead of 8-byte
+//               pieces 32 to a warp store.  The row loops stay rolled (an
+//               unrolled kernel overflowed the instruction cache); row sums
+//               and code words wait in shared memory until the tile's choices
+//               are known (both candidates' code words too, so x is read only
+//               twice); each thread streams its 32 row reads through a 4-slot
+//               ring of asynchronous copies, three reads ahead.
 //
 // Method: "Add NVFP4 four-over-six (row-wise) quantization to the training
 // prototype" (What: 16x16 blocks, rowwise / columnwise; CuTe DSL kernel
@@ -150,6 +153,17 @@ struct TileRing {
     static constexpr int BYTES = kRing * kTileThreads * XB;
 };
 
+constexpr int kBands = kTileThreads / 32;       // 16-row bands per CTA, one per warp
+
+// Staging slot of (band b of the CTA, column j of the CTA's 512) for the
+// columnwise words: band-major, the column's low four bits XORed with its
+// tile's (j / 16) and with 8 for odd bands, so that a warp's writes (one
+// column of each of 32 tiles) and its reads (8 columns x 4 bands) both take
+// the minimum of two shared-memory wavefronts.
+__device__ __forceinline__ int stage_index(int b, int j) {
+    return b * 512 + (j ^ ((j >> 4) & 15) ^ ((b & 1) << 3));
+}
+
 template <int DT, int ERR>
 __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
     using Rg = TileRing<DT>;
@@ -165,6 +179,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
     // ring of tile rows: the thread streams its tile's rows twice (32 row
     // reads) through kRing slots of asynchronous copies
     __shared__ __align__(16) unsigned char ring[Rg::BYTES];
+    __shared__ uint8_t scol[kBands][32];        // columnwise scale byte of each tile
     GScale g{0.0f, 1.0f, 1.0f};
     if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
         g.A = a.gamax[0];
@@ -175,138 +190,157 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
         tenc[i] = min_nd(div_rn(1.0f, mul_rn(e4m3_decode(static_cast<uint32_t>(i)), g.Sdec)), FLT_MAX);
     __syncthreads();
 
-    const int64_t band = blockIdx.x;
-    const int tid = threadIdx.x;
-    const int64_t tile = static_cast<int64_t>(blockIdx.y) * kTileThreads + tid;
-    const int64_t nb = a.K / 16;
-    if (tile >= nb) return;                     // no barrier follows
-    const int64_t K = a.K;
-    const int64_t base = band * 16 * K + tile * 16;
-    const unsigned char* gx = static_cast<const unsigned char*>(a.x) + base * (Rg::XB / 16);
-    const int64_t row_bytes = K * (Rg::XB / 16);
-    unsigned char* slot0 = ring + tid * Rg::XB;
+    // warp w: band kBands * blockIdx.x + w; lane l: tile 32 * blockIdx.y + l
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t M = a.M, K = a.K;
+    const int64_t band0 = static_cast<int64_t>(blockIdx.x) * kBands, band = band0 + warp;
+    const int64_t tile0 = static_cast<int64_t>(blockIdx.y) * 32, tile = tile0 + lane;
+    const int64_t nb = K / 16, nbands = M / 16;
+    uint32_t lo[16], hi[16];                    // columnwise code words, transposed
+    uint32_t sf_c = 0;
+    if (band < nbands && tile < nb) {
+        const int64_t base = band * 16 * K + tile * 16;
+        const unsigned char* gx = static_cast<const unsigned char*>(a.x) + base * (Rg::XB / 16);
+        const int64_t row_bytes = K * (Rg::XB / 16);
+        unsigned char* slot0 = ring + tid * Rg::XB;
 
-    // row read j (0..31) is tile row j % 16, into slot j % kRing
-    auto issue = [&](int j) {
-        if (j < 32) {
-            const unsigned char* src = gx + static_cast<int64_t>(j & 15) * row_bytes;
-            unsigned char* dst = slot0 + (j % kRing) * (kTileThreads * Rg::XB);
+        // row read j (0..31) is tile row j % 16, into slot j % kRing
+        auto issue = [&](int j) {
+            if (j < 32) {
+                const unsigned char* src = gx + static_cast<int64_t>(j & 15) * row_bytes;
+                unsigned char* dst = slot0 + (j % kRing) * (kTileThreads * Rg::XB);
 #pragma unroll
-            for (int c = 0; c < Rg::XB / 16; ++c) cp_async16(dst + 16 * c, src + 16 * c);
-        }
-        cp_async_commit();
-    };
-    auto next_row = [&](int j, float* y) {       // row read j, ready in y
-        issue(j + kRing - 1);
-        cp_async_wait<kRing - 1>();
-        lds16<DT>(slot0 + (j % kRing) * (kTileThreads * Rg::XB), y);
-    };
+                for (int c = 0; c < Rg::XB / 16; ++c) cp_async16(dst + 16 * c, src + 16 * c);
+            }
+            cp_async_commit();
+        };
+        auto next_row = [&](int j, float* y) {       // row read j, ready in y
+            issue(j + kRing - 1);
+            cp_async_wait<kRing - 1>();
+            lds16<DT>(slot0 + (j % kRing) * (kTileThreads * Rg::XB), y);
+        };
 #pragma unroll
-    for (int j = 0; j < kRing - 1; ++j) issue(j);
+        for (int j = 0; j < kRing - 1; ++j) issue(j);
 
-    // pass 0: tile amax
-    float y[16];
-    float b = 0.0f;
+        // pass 0: tile amax
+        float y[16];
+        float b = 0.0f;
 #pragma unroll 1
-    for (int r = 0; r < 16; ++r) {
-        next_row(r, y);
-        b = max_nd(b, absmax16(y));
-    }
-    const float s6f = block_s6f<true>(b, g.Senc);
-    const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
-    const uint32_t sf4 = e4m3_encode(min_nd(mul_rn(s6f, 1.5f), 448.0f));
-    const float enc6 = tenc[sf6], enc4 = tenc[sf4];
-    // |dq| = ((G[k] * d) * A) / (6 * bound) of each grid magnitude G[k]: the
-    // error value of a code with index k is +-|dq| with the sign of its y, so
-    // |dq - y| = | |dq| - |y| | exactly (and likewise the square)
-    {
-        const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
-        const float G[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+        for (int r = 0; r < 16; ++r) {
+            next_row(r, y);
+            b = max_nd(b, absmax16(y));
+        }
+        const float s6f = block_s6f<true>(b, g.Senc);
+        const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
+        const uint32_t sf4 = e4m3_encode(min_nd(mul_rn(s6f, 1.5f), 448.0f));
+        const float enc6 = tenc[sf6], enc4 = tenc[sf4];
+        // |dq| = ((G[k] * d) * A) / (6 * bound) of each grid magnitude G[k]: the
+        // error value of a code with index k is +-|dq| with the sign of its y, so
+        // |dq - y| = | |dq| - |y| | exactly (and likewise the square)
+        {
+            const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
+            const float G[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            dqt[0][k][tid] = div_rn(mul_rn(mul_rn(G[k], d6), g.A), C);
-            dqt[1][k][tid] = div_rn(mul_rn(mul_rn(G[k], d4), g.A), C);
+            for (int k = 0; k < 8; ++k) {
+                dqt[0][k][tid] = div_rn(mul_rn(mul_rn(G[k], d6), g.A), C);
+                dqt[1][k][tid] = div_rn(mul_rn(mul_rn(G[k], d4), g.A), C);
+            }
+        }
+
+        // pass 1: per-element errors; row sums to shared memory, column sums in
+        // registers, both accumulated in element order
+        float F6[16], F4[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
+        auto candidate = [&](const float* y, float enc, int c, uint32_t& w0, uint32_t& w1, float* e) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = mul_rn(y[i], enc);
+            w0 = e2m1_encode8(v);
+            w1 = e2m1_encode8(v + 8);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t k = ((i < 8 ? w0 : w1) >> (4 * (i & 7))) & 7u;
+                const float diff = sub_rn(dqt[c][k][tid], fabsf(y[i]));
+                e[i] = (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff);
+            }
+        };
+#pragma unroll 1
+        for (int r = 0; r < 16; ++r) {
+            next_row(16 + r, y);
+            float e[16];
+            uint32_t w0, w1;
+            candidate(y, enc6, 0, w0, w1, e);
+            sW[0][r][tid] = w0;
+            sW[1][r][tid] = w1;
+            sR6[r][tid] = seq_sum16(e);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) F6[i] = add_rn(F6[i], e[i]);
+            candidate(y, enc4, 1, w0, w1, e);
+            sW[2][r][tid] = w0;
+            sW[3][r][tid] = w1;
+            sR4[r][tid] = seq_sum16(e);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) F4[i] = add_rn(F4[i], e[i]);
+        }
+        cp_async_wait<0>();
+        float R[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) R[r] = sR6[r][tid];
+        const float E6r = tree16_regs(R);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) R[r] = sR4[r][tid];
+        const float E4r = tree16_regs(R);
+        const float E6c = tree16_regs(F6), E4c = tree16_regs(F4);
+        const bool row4 = E4r < E6r, col4 = E4c < E6c;       // ties and NaN keep map-to-6
+        const uint8_t sf_r = static_cast<uint8_t>(row4 ? sf4 : sf6);
+
+        // store the rowwise codes of the chosen candidate; gather the columnwise one's
+        const int64_t nbr = K / 16;
+        const int wr = row4 ? 2 : 0, wc = col4 ? 2 : 0;
+#pragma unroll 1
+        for (int r = 0; r < 16; ++r) {
+            const int64_t rowg = band * 16 + r;
+            reinterpret_cast<uint2*>(a.codes)[(rowg * K + tile * 16) / 16] =
+                make_uint2(sW[wr][r][tid], sW[wr + 1][r][tid]);
+            a.scales[rowg * nbr + tile] = sf_r;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            lo[r] = sW[wc][r][tid];
+            hi[r] = sW[wc + 1][r][tid];
+        }
+        transpose8x8_nibbles(lo);          // rows 0-7,  cols 0-7
+        transpose8x8_nibbles(lo + 8);      // rows 8-15, cols 0-7
+        transpose8x8_nibbles(hi);          // rows 0-7,  cols 8-15
+        transpose8x8_nibbles(hi + 8);      // rows 8-15, cols 8-15
+        sf_c = col4 ? sf4 : sf6;
+    }
+    // columnwise output: x^T's row (tile0 * 16 + j) holds 8 code bytes of each
+    // band, so the CTA's kBands bands give each of its 512 columns 32
+    // consecutive bytes (one sector) and kBands consecutive scale bytes.  The
+    // transposed words are staged in the code-word buffer (free once every
+    // thread has read its own) and written column by column.
+    __syncthreads();
+    uint2* stg = reinterpret_cast<uint2*>(&sW[0][0][0]);
+    if (band < nbands && tile < nb) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            stg[stage_index(warp, lane * 16 + c)] = make_uint2(lo[c], lo[8 + c]);
+            stg[stage_index(warp, lane * 16 + 8 + c)] = make_uint2(hi[c], hi[8 + c]);
         }
     }
-
-    // pass 1: per-element errors; row sums to shared memory, column sums in
-    // registers, both accumulated in element order
-    float F6[16], F4[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
-    auto candidate = [&](const float* y, float enc, int c, uint32_t& w0, uint32_t& w1, float* e) {
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = mul_rn(y[i], enc);
-        w0 = e2m1_encode8(v);
-        w1 = e2m1_encode8(v + 8);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t k = ((i < 8 ? w0 : w1) >> (4 * (i & 7))) & 7u;
-            const float diff = sub_rn(dqt[c][k][tid], fabsf(y[i]));
-            e[i] = (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff);
-        }
-    };
-#pragma unroll 1
-    for (int r = 0; r < 16; ++r) {
-        next_row(16 + r, y);
-        float e[16];
-        uint32_t w0, w1;
-        candidate(y, enc6, 0, w0, w1, e);
-        sW[0][r][tid] = w0;
-        sW[1][r][tid] = w1;
-        sR6[r][tid] = seq_sum16(e);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) F6[i] = add_rn(F6[i], e[i]);
-        candidate(y, enc4, 1, w0, w1, e);
-        sW[2][r][tid] = w0;
-        sW[3][r][tid] = w1;
-        sR4[r][tid] = seq_sum16(e);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) F4[i] = add_rn(F4[i], e[i]);
-    }
-    cp_async_wait<0>();
-    float R[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) R[r] = sR6[r][tid];
-    const float E6r = tree16_regs(R);
-#pragma unroll
-    for (int r = 0; r < 16; ++r) R[r] = sR4[r][tid];
-    const float E4r = tree16_regs(R);
-    const float E6c = tree16_regs(F6), E4c = tree16_regs(F4);
-    const bool row4 = E4r < E6r, col4 = E4c < E6c;       // ties and NaN keep map-to-6
-    const uint8_t sf_r = static_cast<uint8_t>(row4 ? sf4 : sf6);
-    const uint8_t sf_c = static_cast<uint8_t>(col4 ? sf4 : sf6);
-
-    // store the rowwise codes of the chosen candidate; gather the columnwise one's
-    const int64_t nbr = K / 16;
-    const int wr = row4 ? 2 : 0, wc = col4 ? 2 : 0;
-#pragma unroll 1
-    for (int r = 0; r < 16; ++r) {
-        const int64_t rowg = band * 16 + r;
-        reinterpret_cast<uint2*>(a.codes)[(rowg * K + tile * 16) / 16] =
-            make_uint2(sW[wr][r][tid], sW[wr + 1][r][tid]);
-        a.scales[rowg * nbr + tile] = sf_r;
-    }
-    uint32_t lo[16], hi[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        lo[r] = sW[wc][r][tid];
-        hi[r] = sW[wc + 1][r][tid];
-    }
-    transpose8x8_nibbles(lo);          // rows 0-7,  cols 0-7
-    transpose8x8_nibbles(lo + 8);      // rows 8-15, cols 0-7
-    transpose8x8_nibbles(hi);          // rows 0-7,  cols 8-15
-    transpose8x8_nibbles(hi + 8);      // rows 8-15, cols 8-15
-    const int64_t M = a.M;
+    scol[warp][lane] = static_cast<uint8_t>(sf_c);
+    __syncthreads();
     uint2* cc = reinterpret_cast<uint2*>(a.codes_col);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const int64_t col0 = tile * 16 + c, col1 = tile * 16 + 8 + c;
-        cc[(col0 * M + band * 16) / 16] = make_uint2(lo[c], lo[8 + c]);
-        cc[(col1 * M + band * 16) / 16] = make_uint2(hi[c], hi[8 + c]);
-        a.scales_col[col0 * (M / 16) + band] = sf_c;
-        a.scales_col[col1 * (M / 16) + band] = sf_c;
+#pragma unroll 4
+    for (int q = tid; q < 512 * kBands; q += kTileThreads) {
+        const int j = q / kBands, bb = q % kBands;          // column of the CTA, band of the CTA
+        const int64_t col = tile0 * 16 + j, bnd = band0 + bb;
+        if (col < K && bnd < nbands) {
+            cc[col * nbands + bnd] = stg[stage_index(bb, j)];
+            a.scales_col[col * nbands + bnd] = scol[bb][j >> 4];
+        }
     }
 }
 
@@ -320,8 +354,8 @@ int launch_rowowner(KernelT kernel, const QuantArgs& a, cudaStream_t s) {
 
 template <int DT, int ERR>
 int launch_tile_t(const QuantArgs& a, cudaStream_t s) {
-    const dim3 grid(static_cast<unsigned>(a.M / 16),
-                    static_cast<unsigned>((a.K / 16 + kTileThreads - 1) / kTileThreads));
+    const dim3 grid(static_cast<unsigned>((a.M / 16 + kBands - 1) / kBands),
+                    static_cast<unsigned>((a.K / 16 + 31) / 32));
     k_tile_t<DT, ERR><<<grid, kTileThreads, 0, s>>>(a);
     return static_cast<int>(cudaGetLastError());
 }
