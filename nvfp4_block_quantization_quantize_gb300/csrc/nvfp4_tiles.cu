@@ -1,12 +1,14 @@
 // nvfp4_tiles.cu -- 16x16 blocks and columnwise outputs for sm_103a.
 //
-// k_tiles_rows  rowwise + columnwise output (no residual): one CTA = a
-//               16-row band x 256 columns; lane l of warp w holds row l%16
-//               of the 16x16 tile 2w + l/16.  16x16 blocks reduce their amax
-//               (and, for four-over-six, their row error sums with the fixed
-//               width-16 tree) over the half warp.  The band is then staged
-//               in shared memory and each thread owns one column (x^T's row)
-//               of it for the columnwise pass.
+// k_tiles_rows  rowwise + columnwise output (no residual): one CTA = 256
+//               columns of 4 consecutive 16-row bands, walked in turn; lane
+//               l of warp w holds row l%16 of the 16x16 tile 2w + l/16.
+//               16x16 blocks reduce their amax (and, for four-over-six, their
+//               row error sums with the fixed width-16 tree) over the half
+//               warp.  The band is then staged in shared memory and each
+//               thread owns one column (x^T's row) of it for the columnwise
+//               pass; the 4 bands' columnwise codes wait in shared memory and
+//               leave as one 32-byte run per column.
 // k_tile_t      four-over-six 16x16 with rowwise AND columnwise output: one
 //               thread owns a whole 16x16 tile and walks its rows twice
 //               (amax; both candidates' codes and errors with the row sums
@@ -39,6 +41,8 @@ constexpr int kThreads = 256;
 constexpr int kTileCols = 256;
 constexpr int kYsStride = kTileCols + 4;
 
+constexpr int kRowBands = 4;                    // bands per CTA of k_tiles_rows
+
 template <int DT, int BLK, int ERR, int RND, bool GS>
 __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
     __shared__ float ys[16 * kYsStride];
@@ -47,16 +51,19 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
     __shared__ uint32_t ws[RND == NVFP4_SR ? 16 * kYsStride : 1];
     __shared__ O6TabOf<ERR> tab;
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
+    // columnwise codes and scale bytes of the CTA's bands, [band][column]
+    __shared__ uint2 ccs[kRowBands][kTileCols];
+    __shared__ uint8_t scs[kRowBands][kTileCols];
     if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
-    const int64_t band = blockIdx.x;
     const int64_t chunk = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = 2 * warp + (lane >> 4);
     const int rr = lane & 15;
     const int64_t nb = a.K / 16;
+    const int64_t nbands = a.M / 16;
+    const int64_t band0 = static_cast<int64_t>(blockIdx.x) * kRowBands;
     const int64_t cb = chunk * 16 + t;
     const bool valid = cb < nb;
-    const int64_t row = band * 16 + rr;
 
     GScale g{0.0f, 1.0f, 1.0f};
     if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
@@ -70,75 +77,91 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
         tp = &tab;
     }
 
-    const int64_t e0 = row * a.K + cb * 16;
-    float y[16];
-    if (valid) {
-        load16<DT>(a.x, e0, y);
-    } else {
+    const int j = threadIdx.x;                  // column within the chunk (its tile is t)
+    for (int bi = 0; bi < kRowBands; ++bi) {
+        const int64_t band = band0 + bi;
+        if (band >= nbands) break;              // CTA-uniform
+        const int64_t row = band * 16 + rr;
+        const int64_t e0 = row * a.K + cb * 16;
+        float y[16];
+        if (valid) {
+            load16<DT>(a.x, e0, y);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] = 0.0f;
-    }
-    float b = absmax16(y);
-    if (BLK == NVFP4_BLOCK_16X16) b = max16_lanes(b);
+            for (int i = 0; i < 16; ++i) y[i] = 0.0f;
+        }
+        float b = absmax16(y);
+        if (BLK == NVFP4_BLOCK_16X16) b = max16_lanes(b);
 
-    // ---- rowwise ----
-    {
+        // ---- rowwise ----
+        {
+            uint32_t w0, w1, sf;
+            float d;
+            if (ERR == NVFP4_ERR_NONE) {
+                const float s6f = block_scale<GS>(b, g.Senc, RND == NVFP4_RTN_STD);
+                sf = e4m3_encode(min_nd(s6f, 448.0f));
+                d = e4m3_decode(sf);
+                const float D = GS ? mul_rn(d, g.Sdec) : d;
+                float q[16];
+                uint32_t wd[16];
+                if (RND == NVFP4_SR) {
+                    const uint64_t idx0 = (static_cast<uint64_t>(a.row_offset) + static_cast<uint64_t>(row)) *
+                                              static_cast<uint64_t>(a.K) + static_cast<uint64_t>(cb * 16);
+                    sr_words16(idx0, a.seed, a.step, wd);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) ws[rr * kYsStride + t * 16 + i] = wd[i];
+                }
+                encode_plain16_words<RND>(y, D, b, wd, w0, w1, GS ? nullptr : rtab, sf, q, false);
+            } else {
+                four_over_six16<ERR, BLK == NVFP4_BLOCK_16X16>(y, b, g, C, tp, w0, w1, sf, d);
+            }
+            if (valid) {
+                if (a.codes) reinterpret_cast<uint2*>(a.codes)[e0 / 16] = make_uint2(w0, w1);
+                if (a.scales) a.scales[row * nb + cb] = static_cast<uint8_t>(sf);
+            }
+        }
+        // ---- columnwise: the rowwise quantization of x^T, from the staged band ----
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ys[rr * kYsStride + t * 16 + i] = y[i];
+        __syncthreads();
+        float c[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) c[r] = ys[r * kYsStride + j];
+        float bc = absmax16(c);
+        if (BLK == NVFP4_BLOCK_16X16) bc = max16_lanes(bc);
         uint32_t w0, w1, sf;
         float d;
         if (ERR == NVFP4_ERR_NONE) {
-            const float s6f = block_scale<GS>(b, g.Senc, RND == NVFP4_RTN_STD);
+            const float s6f = block_scale<GS>(bc, g.Senc, RND == NVFP4_RTN_STD);
             sf = e4m3_encode(min_nd(s6f, 448.0f));
             d = e4m3_decode(sf);
             const float D = GS ? mul_rn(d, g.Sdec) : d;
-            float q[16];
+            float qc[16];
             uint32_t wd[16];
             if (RND == NVFP4_SR) {
-                const uint64_t idx0 = (static_cast<uint64_t>(a.row_offset) + static_cast<uint64_t>(row)) *
-                                          static_cast<uint64_t>(a.K) + static_cast<uint64_t>(cb * 16);
-                sr_words16(idx0, a.seed, a.step, wd);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) ws[rr * kYsStride + t * 16 + i] = wd[i];
+                for (int r = 0; r < 16; ++r) wd[r] = ws[r * kYsStride + j];
             }
-            encode_plain16_words<RND>(y, D, b, wd, w0, w1, GS ? nullptr : rtab, sf, q, false);
+            encode_plain16_words<RND>(c, D, bc, wd, w0, w1, GS ? nullptr : rtab, sf, qc, false);
         } else {
-            four_over_six16<ERR, BLK == NVFP4_BLOCK_16X16>(y, b, g, C, tp, w0, w1, sf, d);
+            four_over_six16<ERR, BLK == NVFP4_BLOCK_16X16>(c, bc, g, C, tp, w0, w1, sf, d);
         }
-        if (valid) {
-            if (a.codes) reinterpret_cast<uint2*>(a.codes)[e0 / 16] = make_uint2(w0, w1);
-            if (a.scales) a.scales[row * nb + cb] = static_cast<uint8_t>(sf);
-        }
+        ccs[bi][j] = make_uint2(w0, w1);
+        scs[bi][j] = static_cast<uint8_t>(sf);
+        __syncthreads();                        // ys and ws are rewritten by the next band
     }
-    // ---- columnwise: the rowwise quantization of x^T, from the staged band ----
-#pragma unroll
-    for (int i = 0; i < 16; ++i) ys[rr * kYsStride + t * 16 + i] = y[i];
-    __syncthreads();
-    const int j = threadIdx.x;                  // column within the chunk (its tile is t)
-    const int64_t col = chunk * kTileCols + j;
-    float c[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) c[r] = ys[r * kYsStride + j];
-    float bc = absmax16(c);
-    if (BLK == NVFP4_BLOCK_16X16) bc = max16_lanes(bc);
-    uint32_t w0, w1, sf;
-    float d;
-    if (ERR == NVFP4_ERR_NONE) {
-        const float s6f = block_scale<GS>(bc, g.Senc, RND == NVFP4_RTN_STD);
-        sf = e4m3_encode(min_nd(s6f, 448.0f));
-        d = e4m3_decode(sf);
-        const float D = GS ? mul_rn(d, g.Sdec) : d;
-        float qc[16];
-        uint32_t wd[16];
-        if (RND == NVFP4_SR) {
-#pragma unroll
-            for (int r = 0; r < 16; ++r) wd[r] = ws[r * kYsStride + j];
+    // x^T's row col holds 8 code bytes and one scale byte per band: the CTA's
+    // bands give each of its columns one run of consecutive bytes, written
+    // by consecutive threads
+    const int64_t nbc = nbands - band0 < kRowBands ? nbands - band0 : kRowBands;
+    uint2* cc = reinterpret_cast<uint2*>(a.codes_col);
+    for (int q = threadIdx.x; q < kRowBands * kTileCols; q += kThreads) {
+        const int jj = q / kRowBands, bb = q % kRowBands;
+        const int64_t cj = chunk * kTileCols + jj;
+        if (bb < nbc && cj < a.K) {
+            cc[cj * nbands + band0 + bb] = ccs[bb][jj];
+            a.scales_col[cj * nbands + band0 + bb] = scs[bb][jj];
         }
-        encode_plain16_words<RND>(c, D, bc, wd, w0, w1, GS ? nullptr : rtab, sf, qc, false);
-    } else {
-        four_over_six16<ERR, BLK == NVFP4_BLOCK_16X16>(c, bc, g, C, tp, w0, w1, sf, d);
-    }
-    if (col < a.K) {
-        reinterpret_cast<uint2*>(a.codes_col)[(col * a.M + band * 16) / 16] = make_uint2(w0, w1);
-        a.scales_col[col * (a.M / 16) + band] = static_cast<uint8_t>(sf);
     }
 }
 
@@ -347,7 +370,8 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
 // ---------------------------------------------------------------------------------------------
 template <typename KernelT>
 int launch_rowowner(KernelT kernel, const QuantArgs& a, cudaStream_t s) {
-    const dim3 grid(static_cast<unsigned>(a.M / 16), static_cast<unsigned>((a.K / 16 + 15) / 16));
+    const dim3 grid(static_cast<unsigned>((a.M / 16 + kRowBands - 1) / kRowBands),
+                    static_cast<unsigned>((a.K / 16 + 15) / 16));
     kernel<<<grid, kThreads, 0, s>>>(a);
     return static_cast<int>(cudaGetLastError());
 }
