@@ -263,6 +263,44 @@ def mm_measurement(nv, torch, out, Ma, Ka, M2, K2, peaks, iters=5):
     return res
 
 
+def c4_measurement(nv, torch, dev, peaks, iters=10):
+    """The other large graded configuration, timed beside the step (not part of
+    it): fp32 [8192,8192] Student-t(3) (seed 3), four-over-six 16x16 MSE with a
+    given per-tensor amax, rowwise + columnwise outputs from one read, bounds
+    256 and 448.  The input (256 MiB) is larger than L2."""
+    import nvfp4_workloads as wl
+    x = torch.from_numpy(wl.c4()).to(dev)
+    M, K = x.shape
+    g = nv.nvfp4_amax(x)
+    outs = dict(codes=torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+                scales=torch.empty((M, K // 16), dtype=torch.uint8, device=dev),
+                codes_col=torch.empty((K, M // 2), dtype=torch.uint8, device=dev),
+                scales_col=torch.empty((K, M // 16), dtype=torch.uint8, device=dev))
+    q = 0.5 + 1 / 16
+    nbytes = M * K * (4 + 2 * q)
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    res = []
+    for bound in (256.0, 448.0):
+        run = lambda: nv.nvfp4_quantize(x, block="16x16", err_mode="mse", gamax_mode="tensor_given",   # noqa: E731
+                                        gamax=g, scale_bound=bound, colwise=True, **outs)
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        res.append({"bound": bound, "ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / GB, 1),
+                    "frac_of_peak": round(nbytes / (ms * 1e-3) / GB / peak, 3)})
+    del x, outs
+    return {"workload": "c4: fp32 [8192,8192] Student-t(3) seed 3, four-over-six 16x16 MSE, "
+                        "per-tensor amax given, rowwise + columnwise", "kernel": "k_tile_t<f32, MSE>",
+            "algorithmic_bytes": int(nbytes), "runs": res}
+
+
 def run_mm_only(args, local_rank):
     import torch
     import nvfp4_block_quantization_quantize_gb300 as nv
@@ -472,9 +510,10 @@ def run_gpu(args, rank, world, local_rank):
     calls = [{"call": n, "kernel": k, "ms": round(ms, 4), "GB/s": round(b / (ms * 1e-3) / GB, 1),
               "frac_of_peak": round(b / (ms * 1e-3) / GB / peak, 3)}
              for (n, k, _, b), ms in zip(plan, per_call_ms) if ms > 0]
-    mm = None
+    mm = c4 = None
     if not args.only:
         mm = mm_measurement(nv, torch, o, Ma, Ka, M2, K2, peaks)
+        c4 = c4_measurement(nv, torch, dev, peaks)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline()
@@ -495,7 +534,7 @@ def run_gpu(args, rank, world, local_rank):
                    "parallelism": f"{world} independent replica(s), no data-path collective"},
         "gpu_launches": nsteps * sum(1 for name, _, _, _ in plan if not args.only or args.only in name),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "calls": calls,
-        "fp4_mm": mm,
+        "fp4_mm": mm, "c4_rowcol": c4,
     }
     print(json.dumps(line), flush=True)
 

@@ -168,13 +168,21 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
 // ---------------------------------------------------------------------------------------------
 constexpr int kTileThreads = 128;
 
-constexpr int kRing = 4;                        // tile rows in flight per thread
-
+// Ring of tile rows per thread: 4 slots of bf16 rows, 3 of fp32 rows (the
+// same bytes in flight; 3 CTAs fit on an SM either way).
 template <int DT>
 struct TileRing {
     static constexpr int XB = DT == NVFP4_BF16 ? 32 : 64;    // bytes of one tile row
-    static constexpr int BYTES = kRing * kTileThreads * XB;
+    static constexpr int SLOTS = DT == NVFP4_BF16 ? 4 : 3;
+    static constexpr int BYTES = SLOTS * kTileThreads * XB;
 };
+
+// The width-16 tree's upper levels over the first level's eight pair sums
+// s[i] = R[i] + R[i + 8] of the row sums R.
+__device__ __forceinline__ float tree16_upper(const float* s) {
+    return add_rn(add_rn(add_rn(s[0], s[4]), add_rn(s[2], s[6])),
+                  add_rn(add_rn(s[1], s[5]), add_rn(s[3], s[7])));
+}
 
 constexpr int kBands = kTileThreads / 32;       // 16-row bands per CTA, one per warp
 
@@ -194,13 +202,14 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
     // per thread and candidate: the error value magnitude |dq| of each grid
     // index k, [candidate][k][thread] so a warp's lookups are conflict-free
     __shared__ float dqt[2][8][kTileThreads];
-    // per-thread row sums of both candidates and the 16 rows' code words,
-    // [row][thread] so a warp's accesses are conflict-free
-    __shared__ float sR6[16][kTileThreads], sR4[16][kTileThreads];
+    // per thread and candidate: row sums of rows 0-7, then the width-16
+    // tree's first level (row i + row i + 8), [candidate][i][thread] so a
+    // warp's accesses are conflict-free
+    __shared__ float sR[2][8][kTileThreads];
     // both candidates' code words of every row (map-to-6: [0..1], map-to-4: [2..3])
     __shared__ uint32_t sW[4][16][kTileThreads];
     // ring of tile rows: the thread streams its tile's rows twice (32 row
-    // reads) through kRing slots of asynchronous copies
+    // reads) through Rg::SLOTS slots of asynchronous copies
     __shared__ __align__(16) unsigned char ring[Rg::BYTES];
     __shared__ uint8_t scol[kBands][32];        // columnwise scale byte of each tile
     GScale g{0.0f, 1.0f, 1.0f};
@@ -227,23 +236,23 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
         const int64_t row_bytes = K * (Rg::XB / 16);
         unsigned char* slot0 = ring + tid * Rg::XB;
 
-        // row read j (0..31) is tile row j % 16, into slot j % kRing
+        // row read j (0..31) is tile row j % 16, into slot j % Rg::SLOTS
         auto issue = [&](int j) {
             if (j < 32) {
                 const unsigned char* src = gx + static_cast<int64_t>(j & 15) * row_bytes;
-                unsigned char* dst = slot0 + (j % kRing) * (kTileThreads * Rg::XB);
+                unsigned char* dst = slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB);
 #pragma unroll
                 for (int c = 0; c < Rg::XB / 16; ++c) cp_async16(dst + 16 * c, src + 16 * c);
             }
             cp_async_commit();
         };
         auto next_row = [&](int j, float* y) {       // row read j, ready in y
-            issue(j + kRing - 1);
-            cp_async_wait<kRing - 1>();
-            lds16<DT>(slot0 + (j % kRing) * (kTileThreads * Rg::XB), y);
+            issue(j + Rg::SLOTS - 1);
+            cp_async_wait<Rg::SLOTS - 1>();
+            lds16<DT>(slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB), y);
         };
 #pragma unroll
-        for (int j = 0; j < kRing - 1; ++j) issue(j);
+        for (int j = 0; j < Rg::SLOTS - 1; ++j) issue(j);
 
         // pass 0: tile amax
         float y[16];
@@ -296,24 +305,31 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             candidate(y, enc6, 0, w0, w1, e);
             sW[0][r][tid] = w0;
             sW[1][r][tid] = w1;
-            sR6[r][tid] = seq_sum16(e);
+            float R6 = seq_sum16(e);
 #pragma unroll
             for (int i = 0; i < 16; ++i) F6[i] = add_rn(F6[i], e[i]);
             candidate(y, enc4, 1, w0, w1, e);
             sW[2][r][tid] = w0;
             sW[3][r][tid] = w1;
-            sR4[r][tid] = seq_sum16(e);
+            float R4 = seq_sum16(e);
 #pragma unroll
             for (int i = 0; i < 16; ++i) F4[i] = add_rn(F4[i], e[i]);
+            const int i8 = r & 7;
+            if (r >= 8) {
+                R6 = add_rn(sR[0][i8][tid], R6);
+                R4 = add_rn(sR[1][i8][tid], R4);
+            }
+            sR[0][i8][tid] = R6;
+            sR[1][i8][tid] = R4;
         }
         cp_async_wait<0>();
-        float R[16];
+        float S[8];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) R[r] = sR6[r][tid];
-        const float E6r = tree16_regs(R);
+        for (int i = 0; i < 8; ++i) S[i] = sR[0][i][tid];
+        const float E6r = tree16_upper(S);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) R[r] = sR4[r][tid];
-        const float E4r = tree16_regs(R);
+        for (int i = 0; i < 8; ++i) S[i] = sR[1][i][tid];
+        const float E4r = tree16_upper(S);
         const float E6c = tree16_regs(F6), E4c = tree16_regs(F4);
         const bool row4 = E4r < E6r, col4 = E4c < E6c;       // ties and NaN keep map-to-6
         const uint8_t sf_r = static_cast<uint8_t>(row4 ? sf4 : sf6);
