@@ -29,6 +29,14 @@ __device__ __forceinline__ float sub_rn(float a, float b) { return __fsub_rn(a, 
 __device__ __forceinline__ float div_rn(float a, float b) { return __fdiv_rn(a, b); }
 __device__ __forceinline__ float max_nd(float a, float b) { return fmaxf(a, b); }
 __device__ __forceinline__ float min_nd(float a, float b) { return fminf(a, b); }
+// NaN-dropping maximum of two pairs of bf16 magnitudes: max.bf16x2 (no .NaN)
+// returns the other operand where one is NaN, and keeps subnormals; the
+// maximum is one of its inputs, so it is exact.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(w & 0x7FFF7FFFu));
+    return r;
+}
 
 // ---- E4M3 block scales -----------------------------------------------------------------
 // RN-even to E4M3FN with saturation to +-448 (NaN stays NaN).

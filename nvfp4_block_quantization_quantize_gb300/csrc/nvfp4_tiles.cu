@@ -254,13 +254,27 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
 #pragma unroll
         for (int j = 0; j < Rg::SLOTS - 1; ++j) issue(j);
 
-        // pass 0: tile amax
+        // pass 0: tile amax (bf16: on the packed pairs)
         float y[16];
         float b = 0.0f;
+        if constexpr (DT == NVFP4_BF16) {
+            uint32_t m2 = 0u;
 #pragma unroll 1
-        for (int r = 0; r < 16; ++r) {
-            next_row(r, y);
-            b = max_nd(b, absmax16(y));
+            for (int r = 0; r < 16; ++r) {
+                issue(r + Rg::SLOTS - 1);
+                cp_async_wait<Rg::SLOTS - 1>();
+                const uint4* p = reinterpret_cast<const uint4*>(slot0 + (r % Rg::SLOTS) * (kTileThreads * Rg::XB));
+                const uint4 u = p[0], v = p[1];
+                m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, u.x), u.y), u.z), u.w);
+                m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, v.x), v.y), v.z), v.w);
+            }
+            b = max_nd(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
+        } else {
+#pragma unroll 1
+            for (int r = 0; r < 16; ++r) {
+                next_row(r, y);
+                b = max_nd(b, absmax16(y));
+            }
         }
         const float s6f = block_s6f<true>(b, g.Senc);
         const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
@@ -290,10 +304,17 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             for (int i = 0; i < 16; ++i) v[i] = mul_rn(y[i], enc);
             w0 = e2m1_encode8(v);
             w1 = e2m1_encode8(v + 8);
+            // byte offset of dqt[c][k][tid] from dqt: k * 512 ORed into
+            // c * 4096 + tid * 4 (whose bits 9-11 are clear)
+            const uint32_t coff = static_cast<uint32_t>(c * 4096 + tid * 4);
+            const unsigned char* dbase = reinterpret_cast<const unsigned char*>(&dqt[0][0][0]);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const uint32_t k = ((i < 8 ? w0 : w1) >> (4 * (i & 7))) & 7u;
-                const float diff = sub_rn(dqt[c][k][tid], fabsf(y[i]));
+                const uint32_t w = i < 8 ? w0 : w1;
+                const int sh = 4 * (i & 7);
+                const uint32_t k512 = (sh >= 9 ? w >> (sh - 9) : w << (9 - sh)) & 0xE00u;
+                const float dq = *reinterpret_cast<const float*>(dbase + (k512 | coff));
+                const float diff = sub_rn(dq, fabsf(y[i]));
                 e[i] = (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff);
             }
         };
