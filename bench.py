@@ -55,6 +55,8 @@ def parse():
                    help="run only the step's calls whose name contains this text (profiling)")
     p.add_argument("--mm-only", action="store_true",
                    help="only the FP4 product measurement (quantize A and W2, then time nvfp4_mm)")
+    p.add_argument("--c4-only", action="store_true",
+                   help="only the fp32 [8192,8192] four-over-six 16x16 row+col measurement")
     return p.parse_args()
 
 
@@ -263,7 +265,7 @@ def mm_measurement(nv, torch, out, Ma, Ka, M2, K2, peaks, iters=5):
     return res
 
 
-def c4_measurement(nv, torch, dev, peaks, iters=10):
+def c4_measurement(nv, torch, dev, peaks, iters=10, bounds=(256.0, 448.0)):
     """The other large graded configuration, timed beside the step (not part of
     it): fp32 [8192,8192] Student-t(3) (seed 3), four-over-six 16x16 MSE with a
     given per-tensor amax, rowwise + columnwise outputs from one read, bounds
@@ -280,7 +282,7 @@ def c4_measurement(nv, torch, dev, peaks, iters=10):
     nbytes = M * K * (4 + 2 * q)
     peak = peaks["hbm_gbs"] if peaks else 6800.0
     res = []
-    for bound in (256.0, 448.0):
+    for bound in bounds:
         run = lambda: nv.nvfp4_quantize(x, block="16x16", err_mode="mse", gamax_mode="tensor_given",   # noqa: E731
                                         gamax=g, scale_bound=bound, colwise=True, **outs)
         for _ in range(3):
@@ -318,6 +320,19 @@ def run_mm_only(args, local_rank):
                         iters=args.steps)
     print(json.dumps({"metric": "fp4 GEMM TFLOP/s", "value": mm["tflops"], "unit": "TFLOP/s",
                       "higher_is_better": True, "fp4_mm": mm}), flush=True)
+
+
+def run_c4_only(args, local_rank):
+    import torch
+    import nvfp4_block_quantization_quantize_gb300 as nv
+    torch.cuda.set_device(local_rank)
+    nv.build()
+    nv.load_library()
+    dev = torch.device("cuda", local_rank)
+    c4 = c4_measurement(nv, torch, dev, measured_peaks(), iters=args.steps, bounds=(256.0,))
+    run = c4["runs"][0]
+    print(json.dumps({"metric": "NVFP4 quantize GB/s", "value": run["GB/s"], "unit": "GB/s",
+                      "higher_is_better": True, "c4_rowcol": c4}), flush=True)
 
 
 # ---------------------------------------------------------------------------------------
@@ -552,6 +567,10 @@ def main():
     if args.mm_only:
         if rank == 0:
             run_mm_only(args, local_rank)
+        return
+    if args.c4_only:
+        if rank == 0:
+            run_c4_only(args, local_rank)
         return
     if world > 1:
         import torch

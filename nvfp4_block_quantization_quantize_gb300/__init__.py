@@ -11,8 +11,10 @@ Functions (same names as the C ABI):
   nvfp4_dequantize(codes, scales, M, K, ...) -> tensor
   nvfp4_qdq(x, ...)        -> dict(out[, codes, scales][, gamax])
   nvfp4_amax(x, ...)       -> tensor
-Inputs on the CPU are staged to the current CUDA device and the results are
-copied back (the host-buffer path); CUDA inputs stay on their device.
+Calls on CUDA tensors stay on their device.  Calls on CPU tensors (the
+host-buffer path) stage their inputs on the current CUDA device and copy the
+results back (into the caller's host tensors when given, else into new pinned
+ones); they return with their results ready.
 """
 from __future__ import annotations
 
@@ -146,15 +148,64 @@ def _empty(shape, dtype, dev):
     return torch.empty(shape, dtype=dtype, device=dev)
 
 
-def _to_host(ts: dict, stream=None) -> dict:
-    """Device tensors -> pinned host tensors: asynchronous copies on the call's
-    stream, then one wait for that stream, so the results are ready on return."""
-    out = {}
-    for k, v in ts.items():
-        h = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-        h.copy_(v, non_blocking=True)
-        out[k] = h
+# ---- host buffers ---------------------------------------------------------------------------
+# A call whose tensors live in host memory runs the same kernels on staged
+# device copies: inputs (and the residual) are copied to the device, outputs
+# are made in device memory and copied back, into the caller's host tensors
+# when given, else into new pinned ones.  Host calls return with their
+# results ready.  (Kernels reading and writing mapped pinned memory in place
+# over the host link measured 2-2.5x slower than these bulk copies.)
+def _host_in(t, dev):
+    """An input (or the in-place residual) of a host call."""
+    if t is None or t.is_cuda:
+        return t
+    return _stage(t.contiguous(), dev)
+
+
+def _out_buf(shape, dtype, given, dev, host):
+    """An output: the given device tensor or a new device one (copied back
+    into a given host tensor by _finish_host); a call on device tensors
+    refuses host outputs."""
+    if given is not None and given.is_cuda:
+        return given
+    if given is not None and not host:
+        raise ValueError("nvfp4: the outputs of a call on device tensors must be device tensors")
+    return _empty(shape, dtype, dev)
+
+
+def _dev_residual(residual, dev):
+    """The in-place residual of a call on device tensors: it must live on the
+    call's device (a staged copy would lose the update)."""
+    if residual is not None and residual.device != dev:
+        raise ValueError("nvfp4: the residual of a call on device tensors must be on x's device")
+    return residual
+
+
+def _inputs_ready(stream):
+    """Staging copies run on torch's current stream; a call on another stream
+    waits for them."""
+    if stream is not None:
+        torch.cuda.current_stream().synchronize()
+
+
+def _finish_host(res: dict, given: dict, stream=None) -> dict:
+    """End of a host call: results still in device memory are copied into the
+    caller's host tensor or a new pinned one, after the call's stream is done;
+    then one wait, so everything is ready on return."""
     _sync(stream)
+    out = {}
+    for k, v in res.items():
+        g = given.get(k)
+        if not v.is_cuda or (g is not None and g.is_cuda):
+            out[k] = v
+        elif g is not None:
+            g.copy_(v, non_blocking=True)
+            out[k] = g
+        else:
+            h = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+            h.copy_(v, non_blocking=True)
+            out[k] = h
+    torch.cuda.current_stream().synchronize()
     return out
 
 
@@ -202,14 +253,17 @@ def nvfp4_quantize(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=No
     blk, rnd = _enum("block", block), _enum("rounding", rounding)
     gm, em = _enum("gamax_mode", gamax_mode), _enum("err_mode", err_mode)
     bound = _default_bound(em, scale_bound)
-    xd = _stage(x.contiguous(), dev)
-    rd = _stage(residual, dev)
+    given = {"codes": codes, "scales": scales, "codes_col": codes_col, "scales_col": scales_col}
+    xd = _host_in(x, dev) if host else x.contiguous()
+    rd = _host_in(residual, dev) if host else _dev_residual(residual, dev)
     g = _gamax_buffer(gm, gamax, M, dev)
-    codes = codes if codes is not None else _empty((M, K // 2), torch.uint8, dev)
-    scales = scales if scales is not None else _empty((M, K // 16), torch.uint8, dev)
+    codes = _out_buf((M, K // 2), torch.uint8, codes, dev, host)
+    scales = _out_buf((M, K // 16), torch.uint8, scales, dev, host)
     if colwise:
-        codes_col = codes_col if codes_col is not None else _empty((K, M // 2), torch.uint8, dev)
-        scales_col = scales_col if scales_col is not None else _empty((K, M // 16), torch.uint8, dev)
+        codes_col = _out_buf((K, M // 2), torch.uint8, codes_col, dev, host)
+        scales_col = _out_buf((K, M // 16), torch.uint8, scales_col, dev, host)
+    if host:
+        _inputs_ready(stream)
     rc = lib.nvfp4_quantize(_ptr(xd), M, K, _x_dtype(x), blk, rnd, _ptr(rd), seed, step,
                             row_offset, gm, _ptr(g), em, bound, _ptr(codes), _ptr(scales),
                             _ptr(codes_col), _ptr(scales_col), _stream(stream))
@@ -221,8 +275,10 @@ def nvfp4_quantize(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=No
         out["gamax"] = g
     if host:
         if residual is not None and rd is not residual:
-            residual.copy_(rd, non_blocking=True)
-        out = _to_host(out, stream)
+            given["residual"] = residual
+            out["residual"] = rd
+        out = _finish_host(out, given, stream)
+        out.pop("residual", None)
     return out
 
 
@@ -237,12 +293,14 @@ def nvfp4_qdq(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=None, s
     blk, rnd = _enum("block", block), _enum("rounding", rounding)
     gm, em = _enum("gamax_mode", gamax_mode), _enum("err_mode", err_mode)
     bound = _default_bound(em, scale_bound)
-    xd = _stage(x.contiguous(), dev)
-    rd = _stage(residual, dev)
+    xd = _host_in(x, dev) if host else x.contiguous()
+    rd = _host_in(residual, dev) if host else _dev_residual(residual, dev)
     g = _gamax_buffer(gm, gamax, M, dev)
-    o = out if out is not None and out.is_cuda else _empty((M, K), torch.bfloat16, dev)
-    codes = _empty((M, K // 2), torch.uint8, dev) if want_codes else None
-    scales = _empty((M, K // 16), torch.uint8, dev) if want_codes else None
+    o = _out_buf((M, K), torch.bfloat16, out, dev, host)
+    codes = _out_buf((M, K // 2), torch.uint8, None, dev, host) if want_codes else None
+    scales = _out_buf((M, K // 16), torch.uint8, None, dev, host) if want_codes else None
+    if host:
+        _inputs_ready(stream)
     rc = lib.nvfp4_qdq(_ptr(xd), M, K, _x_dtype(x), blk, rnd, _ptr(rd), seed, step, row_offset,
                        gm, _ptr(g), em, bound, _ptr(codes), _ptr(scales), _ptr(o),
                        _stream(stream))
@@ -253,12 +311,12 @@ def nvfp4_qdq(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=None, s
     if g is not None:
         res["gamax"] = g
     if host:
+        given = {"out": out}
         if residual is not None and rd is not residual:
-            residual.copy_(rd, non_blocking=True)
-        res = _to_host(res, stream)
-        if out is not None:
-            out.copy_(res["out"])
-            res["out"] = out
+            given["residual"] = residual
+            res["residual"] = rd
+        res = _finish_host(res, given, stream)
+        res.pop("residual", None)
     return res
 
 
@@ -271,19 +329,20 @@ def nvfp4_dequantize(codes: torch.Tensor, scales: torch.Tensor, M: int, K: int, 
     gm = _enum("gamax_mode", gamax_mode)
     od = _enum("dtype", out_dtype)
     bound = 448.0 if scale_bound is None else float(scale_bound)
-    c = _stage(codes.contiguous(), dev)
-    s = _stage(scales.contiguous(), dev)
+    c = _host_in(codes, dev) if host else codes.contiguous()
+    s = _host_in(scales, dev) if host else scales.contiguous()
     g = None
     if gm != GAMAX_NONE:
         if gamax is None:
             raise ValueError("gamax_mode needs gamax")
         g = (gamax if torch.is_tensor(gamax) else torch.tensor([float(gamax)])).to(dev, torch.float32)
-    o = out if out is not None and out.is_cuda else _empty(
-        (M, K), torch.bfloat16 if od == BF16 else torch.float32, dev)
+    o = _out_buf((M, K), torch.bfloat16 if od == BF16 else torch.float32, out, dev, host)
+    if host:
+        _inputs_ready(stream)
     rc = lib.nvfp4_dequantize(_ptr(c), _ptr(s), M, K, gm, _ptr(g), bound, _ptr(o), od,
                               _stream(stream))
     _check(lib, rc)
-    return _to_host({"o": o}, stream)["o"] if host else o
+    return _finish_host({"o": o}, {"o": out}, stream)["o"] if host else o
 
 
 def nvfp4_amax(x: torch.Tensor, *, residual=None, per_row: bool = False, out=None,
@@ -292,13 +351,19 @@ def nvfp4_amax(x: torch.Tensor, *, residual=None, per_row: bool = False, out=Non
     host = not x.is_cuda
     dev = _device_of(x, residual)
     M, K = x.shape
-    xd = _stage(x.contiguous(), dev)
-    rd = _stage(residual, dev)
-    o = out if out is not None else _empty((max(M, 1),) if per_row else (1,), torch.float32, dev)
+    xd = _host_in(x, dev) if host else x.contiguous()
+    rd = _host_in(residual, dev) if host else _dev_residual(residual, dev)
+    # the amax is reduced with device atomics: always a device buffer
+    o = out if out is not None and out.is_cuda else _empty((max(M, 1),) if per_row else (1,),
+                                                           torch.float32, dev)
+    if host:
+        _inputs_ready(stream)
     rc = lib.nvfp4_amax(_ptr(xd), M, K, _x_dtype(x), _ptr(rd), GAMAX_ROW if per_row else GAMAX_TENSOR,
                         _ptr(o), _stream(stream))
     _check(lib, rc)
-    return o.cpu() if host else o
+    if host or (out is not None and not out.is_cuda):
+        return _finish_host({"o": o}, {"o": out}, stream)["o"]
+    return o
 
 
 def nvfp4_scales_to_mma(scales: torch.Tensor, out=None, stream=None) -> torch.Tensor:

@@ -221,6 +221,38 @@ def test_host_buffer_path():
     assert_same(r["codes"].numpy(), o["codes"], "codes")
 
 
+def test_host_pinned_buffers_and_residual():
+    """Host tensors (pinned here) through the staged path: results, the
+    in-place residual and a host dequantize match the oracle byte for byte."""
+    x = mat((64, 256), seed=14)
+    xh = torch.from_numpy(x).pin_memory()
+    r0 = mat((64, 256), seed=15) * np.float32(0.01)
+    rh = torch.from_numpy(r0.copy()).pin_memory()
+    g = nv.nvfp4_quantize(xh, rounding="sr", seed=5, step=2, residual=rh)
+    assert g["codes"].device.type == "cpu"
+    ro = r0.copy()
+    o = oracle.quantize(x, rounding=oracle.SR, seed=5, step=2, residual=ro)
+    assert_same(g["codes"].numpy(), o["codes"], "codes")
+    assert_same(g["scales"].numpy(), o["scales"], "scales")
+    assert_same(rh.numpy(), ro, "residual")
+    dq = nv.nvfp4_dequantize(g["codes"], g["scales"], 64, 256)
+    assert dq.device.type == "cpu"
+    assert_same(dq.view(torch.int16).numpy().view(np.uint16), oracle.dequantize(o["codes"], o["scales"], 64, 256),
+                "dequantized")
+
+
+def test_host_pageable_outputs_and_device_call_refusal():
+    x = mat((64, 128), seed=16)
+    codes = torch.empty((64, 64), dtype=torch.uint8)
+    g = nv.nvfp4_quantize(torch.from_numpy(x), codes=codes)
+    assert g["codes"] is codes
+    assert_same(codes.numpy(), oracle.quantize(x)["codes"], "codes")
+    with pytest.raises(ValueError):
+        nv.nvfp4_quantize(to_dev(x), codes=torch.empty((64, 64), dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        nv.nvfp4_quantize(to_dev(x), rounding="sr", residual=torch.zeros((64, 128)))
+
+
 def test_stream_argument_is_honoured():
     x = to_dev(mat((256, 256), seed=13))
     s = torch.cuda.Stream()
