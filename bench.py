@@ -322,6 +322,39 @@ def run_mm_only(args, local_rank):
                       "higher_is_better": True, "fp4_mm": mm}), flush=True)
 
 
+def rowcol_measurement(nv, torch, W1, peaks, iters=10):
+    """Plain quantization with rowwise AND columnwise outputs from one read
+    (timed beside the step, not part of it), on the step's W1 [4096,14336]
+    bf16: round-to-nearest 1x16 and 16x16, stochastic rounding 1x16 (draws
+    keyed on x's index, shared by both outputs)."""
+    M, K = W1.shape
+    dev = W1.device
+    outs = dict(codes=torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+                scales=torch.empty((M, K // 16), dtype=torch.uint8, device=dev),
+                codes_col=torch.empty((K, M // 2), dtype=torch.uint8, device=dev),
+                scales_col=torch.empty((K, M // 16), dtype=torch.uint8, device=dev))
+    nbytes = M * K * (2 + 2 * (0.5 + 1 / 16))
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    res = []
+    for name, kw in (("RTN 1x16", dict(block="1x16")), ("RTN 16x16", dict(block="16x16")),
+                     ("SR 1x16", dict(block="1x16", rounding="sr", seed=0, step=7))):
+        run = lambda: nv.nvfp4_quantize(W1, colwise=True, **kw, **outs)   # noqa: E731
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        res.append({"variant": name, "ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / GB, 1),
+                    "frac_of_peak": round(nbytes / (ms * 1e-3) / GB / peak, 3)})
+    return {"workload": "W1 [4096,14336] bf16, rowwise + columnwise, no global scale",
+            "algorithmic_bytes": int(nbytes), "runs": res}
+
+
 def run_c4_only(args, local_rank):
     import torch
     import nvfp4_block_quantization_quantize_gb300 as nv
@@ -525,10 +558,11 @@ def run_gpu(args, rank, world, local_rank):
     calls = [{"call": n, "kernel": k, "ms": round(ms, 4), "GB/s": round(b / (ms * 1e-3) / GB, 1),
               "frac_of_peak": round(b / (ms * 1e-3) / GB / peak, 3)}
              for (n, k, _, b), ms in zip(plan, per_call_ms) if ms > 0]
-    mm = c4 = None
+    mm = c4 = rc = None
     if not args.only:
         mm = mm_measurement(nv, torch, o, Ma, Ka, M2, K2, peaks)
         c4 = c4_measurement(nv, torch, dev, peaks)
+        rc = rowcol_measurement(nv, torch, W1, peaks)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline()
@@ -549,7 +583,7 @@ def run_gpu(args, rank, world, local_rank):
                    "parallelism": f"{world} independent replica(s), no data-path collective"},
         "gpu_launches": nsteps * sum(1 for name, _, _, _ in plan if not args.only or args.only in name),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "calls": calls,
-        "fp4_mm": mm, "c4_rowcol": c4,
+        "fp4_mm": mm, "c4_rowcol": c4, "rowcol_plain": rc,
     }
     print(json.dumps(line), flush=True)
 

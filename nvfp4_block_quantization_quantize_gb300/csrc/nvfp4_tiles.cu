@@ -404,6 +404,144 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
     }
 }
 
+// Plain (map-to-6) 16x16 quantization with rowwise AND columnwise output:
+// the tile's one scale serves both outputs and x^T's codes are x's codes
+// transposed (stochastic rounding draws are keyed on x's index), so a thread
+// owns a tile as in k_tile_t, finds the tile amax in a first walk over its
+// rows and encodes each row in a second (from L2), storing the row's codes
+// and shifting its nibbles into the column words: rows come in pairs, whose
+// nibbles are interleaved into one byte per column (low nibble the even row)
+// and moved in at the top of that column's word, so after rows 0-7 (and
+// again 8-15) word c holds column c with row r in nibble r % 8.  The
+// columnwise output is staged and written as in k_tile_t.
+template <int DT, int RND, bool GS>
+__global__ void __launch_bounds__(kTileThreads) k_tile_p(const QuantArgs a) {
+    using Rg = TileRing<DT>;
+    __shared__ __align__(16) unsigned char ring[Rg::BYTES];
+    __shared__ uint2 stg[kBands * 512];          // columnwise words, [stage_index]
+    __shared__ uint8_t scol[kBands][32];
+    __shared__ float rtab[GS ? 1 : 128];
+    if (!GS) fill_recip_table(rtab);
+    GScale g{0.0f, 1.0f, 1.0f};
+    if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
+        g.A = a.gamax[0];
+        global_scales(g.A, a.bound, g.Senc, g.Sdec);
+    }
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t M = a.M, K = a.K;
+    const int64_t band0 = static_cast<int64_t>(blockIdx.x) * kBands, band = band0 + warp;
+    const int64_t tile0 = static_cast<int64_t>(blockIdx.y) * 32, tile = tile0 + lane;
+    const int64_t nb = K / 16, nbands = M / 16;
+    uint32_t colw[16], top[16];
+    uint32_t sf = 0;
+    if (band < nbands && tile < nb) {
+        const int64_t base = band * 16 * K + tile * 16;
+        const unsigned char* gx = static_cast<const unsigned char*>(a.x) + base * (Rg::XB / 16);
+        const int64_t row_bytes = K * (Rg::XB / 16);
+        unsigned char* slot0 = ring + tid * Rg::XB;
+        auto issue = [&](int j) {                // row read j (0..31) is tile row j % 16
+            if (j < 32) {
+                const unsigned char* src = gx + static_cast<int64_t>(j & 15) * row_bytes;
+                unsigned char* dst = slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB);
+#pragma unroll
+                for (int c = 0; c < Rg::XB / 16; ++c) cp_async16(dst + 16 * c, src + 16 * c);
+            }
+            cp_async_commit();
+        };
+        auto next_row = [&](int j, float* y) {
+            issue(j + Rg::SLOTS - 1);
+            cp_async_wait<Rg::SLOTS - 1>();
+            lds16<DT>(slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB), y);
+        };
+#pragma unroll
+        for (int j = 0; j < Rg::SLOTS - 1; ++j) issue(j);
+
+        // pass 0: tile amax (bf16: on the packed pairs)
+        float y[16];
+        float b = 0.0f;
+        if constexpr (DT == NVFP4_BF16) {
+            uint32_t m2 = 0u;
+#pragma unroll 1
+            for (int r = 0; r < 16; ++r) {
+                issue(r + Rg::SLOTS - 1);
+                cp_async_wait<Rg::SLOTS - 1>();
+                const uint4* p = reinterpret_cast<const uint4*>(slot0 + (r % Rg::SLOTS) * (kTileThreads * Rg::XB));
+                const uint4 u = p[0], v = p[1];
+                m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, u.x), u.y), u.z), u.w);
+                m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, v.x), v.y), v.z), v.w);
+            }
+            b = max_nd(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
+        } else {
+#pragma unroll 1
+            for (int r = 0; r < 16; ++r) {
+                next_row(r, y);
+                b = max_nd(b, absmax16(y));
+            }
+        }
+        const float s6f = block_scale<GS>(b, g.Senc, RND == NVFP4_RTN_STD);
+        sf = e4m3_encode(min_nd(s6f, 448.0f));
+        const float d = e4m3_decode(sf);
+        const float D = GS ? mul_rn(d, g.Sdec) : d;
+
+        // pass 1: encode each row; rowwise codes stored, columnwise gathered
+#pragma unroll
+        for (int c = 0; c < 16; ++c) colw[c] = top[c] = 0u;
+        uint32_t pw0 = 0u, pw1 = 0u;             // the pair's even row
+        const uint64_t idx_row0 = (static_cast<uint64_t>(a.row_offset) + static_cast<uint64_t>(band * 16)) *
+                                      static_cast<uint64_t>(K) + static_cast<uint64_t>(tile * 16);
+#pragma unroll 1
+        for (int r = 0; r < 16; ++r) {
+            next_row(16 + r, y);
+            uint32_t wd[16];
+            if (RND == NVFP4_SR) sr_words16(idx_row0 + static_cast<uint64_t>(r) * static_cast<uint64_t>(K),
+                                            a.seed, a.step, wd);
+            uint32_t w0, w1;
+            float q[16];
+            encode_plain16_words<RND>(y, D, b, wd, w0, w1, GS ? nullptr : rtab, sf, q, false);
+            const int64_t rowg = band * 16 + r;
+            reinterpret_cast<uint2*>(a.codes)[(rowg * K + tile * 16) / 16] = make_uint2(w0, w1);
+            a.scales[rowg * nb + tile] = static_cast<uint8_t>(sf);
+            if ((r & 1) == 0) {
+                pw0 = w0;
+                pw1 = w1;
+            } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t e = h ? pw1 : pw0, o = h ? w1 : w0;
+                    // byte k of ev: column 2k of both rows; of od: column 2k + 1
+                    const uint32_t ev = (e & 0x0F0F0F0Fu) | ((o & 0x0F0F0F0Fu) << 4);
+                    const uint32_t od = ((e >> 4) & 0x0F0F0F0Fu) | (o & 0xF0F0F0F0u);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        // word >> 8 with byte k of the pair's bytes on top
+                        colw[8 * h + 2 * k] = __byte_perm(colw[8 * h + 2 * k], ev, 0x0321u | ((4u + k) << 12));
+                        colw[8 * h + 2 * k + 1] = __byte_perm(colw[8 * h + 2 * k + 1], od, 0x0321u | ((4u + k) << 12));
+                    }
+                }
+                if (r == 7) {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) top[c] = colw[c];
+                }
+            }
+        }
+        cp_async_wait<0>();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) stg[stage_index(warp, lane * 16 + c)] = make_uint2(top[c], colw[c]);
+    }
+    scol[warp][lane] = static_cast<uint8_t>(sf);
+    __syncthreads();
+    uint2* cc = reinterpret_cast<uint2*>(a.codes_col);
+#pragma unroll 4
+    for (int q = tid; q < 512 * kBands; q += kTileThreads) {
+        const int j = q / kBands, bb = q % kBands;          // column of the CTA, band of the CTA
+        const int64_t col = tile0 * 16 + j, bnd = band0 + bb;
+        if (col < K && bnd < nbands) {
+            cc[col * nbands + bnd] = stg[stage_index(bb, j)];
+            a.scales_col[col * nbands + bnd] = scol[bb][j >> 4];
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------------------------
 template <typename KernelT>
 int launch_rowowner(KernelT kernel, const QuantArgs& a, cudaStream_t s) {
@@ -413,12 +551,18 @@ int launch_rowowner(KernelT kernel, const QuantArgs& a, cudaStream_t s) {
     return static_cast<int>(cudaGetLastError());
 }
 
-template <int DT, int ERR>
-int launch_tile_t(const QuantArgs& a, cudaStream_t s) {
+// the thread-per-tile kernels: CTA = kBands bands x 32 tiles
+template <typename KernelT>
+int launch_tile(KernelT kernel, const QuantArgs& a, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>((a.M / 16 + kBands - 1) / kBands),
                     static_cast<unsigned>((a.K / 16 + 31) / 32));
-    k_tile_t<DT, ERR><<<grid, kTileThreads, 0, s>>>(a);
+    kernel<<<grid, kTileThreads, 0, s>>>(a);
     return static_cast<int>(cudaGetLastError());
+}
+
+template <int DT, int ERR>
+int launch_tile_t(const QuantArgs& a, cudaStream_t s) {
+    return launch_tile(k_tile_t<DT, ERR>, a, s);
 }
 
 // rowwise + columnwise outputs (no residual)
@@ -432,6 +576,14 @@ int tiles_dispatch_blk(const QuantArgs& a, cudaStream_t s) {
                                            : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_MSE, NVFP4_RTN, true>, a, s);
     }
     const bool gs = a.gamax_mode != NVFP4_GAMAX_NONE;
+    if (BLK == NVFP4_BLOCK_16X16) {
+        if (a.rounding == NVFP4_SR)
+            return gs ? launch_tile(k_tile_p<DT, NVFP4_SR, true>, a, s) : launch_tile(k_tile_p<DT, NVFP4_SR, false>, a, s);
+        if (a.rounding == NVFP4_RTN_STD)
+            return gs ? launch_tile(k_tile_p<DT, NVFP4_RTN_STD, true>, a, s)
+                      : launch_tile(k_tile_p<DT, NVFP4_RTN_STD, false>, a, s);
+        return gs ? launch_tile(k_tile_p<DT, NVFP4_RTN, true>, a, s) : launch_tile(k_tile_p<DT, NVFP4_RTN, false>, a, s);
+    }
     if (a.rounding == NVFP4_SR)
         return gs ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, true>, a, s)
                   : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, false>, a, s);
