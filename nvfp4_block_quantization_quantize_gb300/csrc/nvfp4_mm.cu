@@ -25,7 +25,7 @@ namespace {
 
 constexpr int kMmThreads = 128;
 constexpr int kTileM = 128, kStepK = 64;                 // K elements per MMA
-constexpr uint32_t kColSfa = 256;                         // first scale column (after the two accumulators)
+constexpr uint32_t kColSfa = 128;                         // first scale column (after the accumulator)
 constexpr long kWaitLimit = 1L << 22;                     // try_wait rounds before giving up
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -86,30 +86,31 @@ __device__ __forceinline__ float decode_scale(const float* gamax, float bound) {
     return __fdiv_rn(1.0f, enc);
 }
 
-// Pipeline (warp-specialised).  A CTA owns a 128 x 256 tile of C, one fp32
-// accumulator of 256 tensor-memory columns.  Thread 0 (the producer) loads a
-// stage -- kStageK K-steps (128 bytes of every row) of A (128 rows) and B (256
-// rows), one TMA box each with the 128-byte swizzle, which is the layout the
+// Pipeline (warp-specialised).  A CTA owns a 128 x 128 tile of C, one fp32
+// accumulator of 128 tensor-memory columns.  Thread 0 (the producer) loads a
+// stage -- kStageK K-steps (128 bytes of every row) of A and B (128 rows
+// each), one TMA box each with the 128-byte swizzle, which is the layout the
 // MMA descriptor's 128-byte-swizzle mode reads (a K-step starts 32 bytes
 // further into the 1 KB atoms), and the matching 512-byte scale tiles by bulk
 // copies -- into one of kStages slots, signalling the slot's `full` barrier by
 // transaction count.  Thread 32 (the MMA issuer) waits for `full`, copies the
-// scale tiles to tensor memory (B's rows 128-255 four columns after rows
-// 0-127) and issues one N = 256 MMA per K-step, then commits to the slot's
-// `empty` barrier, which the producer waits on before refilling the slot.  A
-// last commit signals `acc`; all four warps then read the accumulator.  When
-// N is not a multiple of 256 the last CTA of a row of tiles computes only its
-// first 128 columns (N = 128 MMAs; TMA fills the rows past N with zeros).
-constexpr int kTileN2 = 256;                              // two 128-column halves
+// scale tiles to tensor memory and issues one N = 128 MMA per K-step, then
+// commits to the slot's `empty` barrier, which the producer waits on before
+// refilling the slot.  A last commit signals `acc`; all four warps then read
+// the accumulator.  Two CTAs fit on an SM (108 KB of shared memory and 256
+// tensor-memory columns each), so one CTA's epilogue and start-up overlap the
+// other's MMAs; with one CTA of 128 x 256 tiles per SM (N = 256 MMAs, 512
+// columns) the product ran 6 % slower.  TMA fills rows past M or N with zeros.
+constexpr int kTileN = 128;
 constexpr int kStageK = 4;                                // MMA K-steps (64 elements = 32 bytes each) per stage
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kSlotA = kTileM * 128;                      // 128 rows x 128 bytes (128-byte swizzle): 16 KB
-constexpr int kSlotB = kTileN2 * 128;                     // 32 KB
-constexpr int kSlotSfa = kStageK * 512, kSlotSfb = 2 * kStageK * 512;
-constexpr int kSlotBytes = kSlotA + kSlotB + kSlotSfa + kSlotSfb;   // 54 KB
+constexpr int kSlotB = kTileN * 128;                      // 16 KB
+constexpr int kSlotSfa = kStageK * 512, kSlotSfb = kStageK * 512;
+constexpr int kSlotBytes = kSlotA + kSlotB + kSlotSfa + kSlotSfb;   // 36 KB
 constexpr int kMmSmem = kStages * kSlotBytes + 1024;                 // + alignment slack
-constexpr uint32_t kSfColsPerStep = 12;                   // SFA, SFB half 0, SFB half 1: 4 columns each
-constexpr uint32_t kTmemCols2 = 512;
+constexpr uint32_t kSfColsPerStep = 8;                    // SFA, SFB: 4 columns each
+constexpr uint32_t kTmemCols = 256;
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
@@ -141,7 +142,7 @@ __device__ __forceinline__ void mma_f4(uint32_t d, uint64_t da, uint64_t db, uin
 }
 
 template <int ODT>
-__global__ void __launch_bounds__(kMmThreads, 1)
+__global__ void __launch_bounds__(kMmThreads, 2)
     k_mm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
          const uint8_t* __restrict__ SA, const uint8_t* __restrict__ SB, int64_t M, int64_t N, int64_t K,
          const float* gamax_a, const float* gamax_b, float bound, void* out) {
@@ -152,15 +153,14 @@ __global__ void __launch_bounds__(kMmThreads, 1)
     __shared__ int timed_out;
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTileM, n0 = static_cast<int64_t>(blockIdx.x) * kTileN2;
-    const bool half1 = n0 + 128 < N;                     // the second 128-column half exists
+    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTileM, n0 = static_cast<int64_t>(blockIdx.x) * kTileN;
     const int64_t ksteps = K / kStepK;
     const int64_t nstages = (ksteps + kStageK - 1) / kStageK;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(&tmem_base)),
-                     "r"(kTmemCols2));
+                     "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == 0) {
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;");
     const uint32_t tmem = tmem_base;
-    const uint32_t idesc = instr_desc(kTileM, half1 ? kTileN2 : 128);
+    const uint32_t idesc = instr_desc(kTileM, kTileN);
 
     if (tid == 0) {
         // ---- producer ----
@@ -191,14 +191,11 @@ __global__ void __launch_bounds__(kMmThreads, 1)
             const int64_t k0 = t * kStageK;
             const int nk = static_cast<int>(ksteps - k0 < kStageK ? ksteps - k0 : kStageK);
             uint8_t* slot = smem + s * kSlotBytes;
-            mbar_expect_tx(&full[s], static_cast<uint32_t>(kSlotA + kSlotB + nk * (512 + (half1 ? 1024 : 512))));
+            mbar_expect_tx(&full[s], static_cast<uint32_t>(kSlotA + kSlotB + nk * 1024));
             tma_2d(slot, &mapA, static_cast<int>(k0 * 32), static_cast<int>(m0), &full[s]);
             tma_2d(slot + kSlotA, &mapB, static_cast<int>(k0 * 32), static_cast<int>(n0), &full[s]);
             bulk_copy(slot + kSlotA + kSlotB, SA + ((m0 / 128) * ksteps + k0) * 512, nk * 512, &full[s]);
             bulk_copy(slot + kSlotA + kSlotB + kSlotSfa, SB + ((n0 / 128) * ksteps + k0) * 512, nk * 512, &full[s]);
-            if (half1)
-                bulk_copy(slot + kSlotA + kSlotB + kSlotSfa + kStageK * 512, SB + ((n0 / 128 + 1) * ksteps + k0) * 512,
-                          nk * 512, &full[s]);
         }
     } else if (tid == 32) {
         // ---- MMA issuer ----
@@ -220,12 +217,8 @@ __global__ void __launch_bounds__(kMmThreads, 1)
                              "l"(smem_desc(smem_addr(sf + kk * 512), 0, 128)));
                 asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + c + 4),
                              "l"(smem_desc(smem_addr(sf + kSlotSfa + kk * 512), 0, 128)));
-                if (half1)
-                    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem + c + 8),
-                                 "l"(smem_desc(smem_addr(sf + kSlotSfa + kStageK * 512 + kk * 512), 0, 128)));
                 const uint64_t da = smem_desc(smem_addr(slot + kk * 32), 16, 1024, 2);
                 const uint32_t acc = (k0 + kk) > 0 ? 1u : 0u;
-                // one MMA over both halves (N = 256; B's scales for rows 128-255 in the next 4 columns)
                 mma_f4(tmem, da, smem_desc(smem_addr(slot + kSlotA + kk * 32), 16, 1024, 2), idesc, tmem + c,
                        tmem + c + 4, acc);
             }
@@ -242,7 +235,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
     const float alpha = __fmul_rn(decode_scale(gamax_a, bound), decode_scale(gamax_b, bound));
     const int64_t row = m0 + 32 * warp + (tid & 31);
     const bool bad = timed_out != 0;
-    const int ncols = half1 ? kTileN2 : 128;
+    const int ncols = kTileN;
     for (int c0 = 0; c0 < ncols; c0 += 16) {
         uint32_t v[16];
         asm volatile(
@@ -272,7 +265,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols2));
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
 // 2D map of a [rows, K/2]-byte code matrix, boxes of box_rows x 128 bytes, 128-byte swizzle
@@ -301,9 +294,9 @@ int launch_mm(const uint8_t* A, const uint8_t* SA, const uint8_t* B, const uint8
               void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     CUtensorMap mapA, mapB;
-    if (!encode_codes_map(&mapA, A, M, K, kTileM) || !encode_codes_map(&mapB, B, N, K, kTileN2))
+    if (!encode_codes_map(&mapA, A, M, K, kTileM) || !encode_codes_map(&mapB, B, N, K, kTileN))
         return static_cast<int>(cudaErrorInvalidValue);
-    const dim3 grid(static_cast<unsigned>((N + kTileN2 - 1) / kTileN2), static_cast<unsigned>(M / kTileM));
+    const dim3 grid(static_cast<unsigned>((N + kTileN - 1) / kTileN), static_cast<unsigned>(M / kTileM));
     static thread_local int configured_dev = -1;         // the attribute is per device
     int dev = 0;
     cudaGetDevice(&dev);
