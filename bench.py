@@ -18,7 +18,13 @@ once each, amax passes counted with their real extra read) and Gelem/s
 (elements quantized or dequantized), as a fraction of measured HBM peak; the
 roofline line is for the kernel with the largest time per step.
 
+Beside the step (not in its value) the line also reports the FP4 GEMM
+consumer (fp4_mm), the fp32 [8192,8192] four-over-six 16x16 MSE row+col
+configuration (c4_rowcol) and plain rowwise + columnwise quantization of W1
+(rowcol_plain).
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                  [--mm-only | --c4-only]
 
 N > 1 runs under torchrun: every rank processes its own copy of the sweep
 (independent problems, no collective on the data path; weak scaling).
