@@ -24,7 +24,7 @@ configuration (c4_rowcol) and plain rowwise + columnwise quantization of W1
 (rowcol_plain).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--mm-only | --c4-only]
+                  [--mm-only | --c4-only | --rowcol-only [--only VARIANT]]
 
 N > 1 runs under torchrun: every rank processes its own copy of the sweep
 (independent problems, no collective on the data path; weak scaling).
@@ -63,6 +63,8 @@ def parse():
                    help="only the FP4 product measurement (quantize A and W2, then time nvfp4_mm)")
     p.add_argument("--c4-only", action="store_true",
                    help="only the fp32 [8192,8192] four-over-six 16x16 row+col measurement")
+    p.add_argument("--rowcol-only", action="store_true",
+                   help="only the plain rowwise + columnwise measurement on W1 (--only picks a variant)")
     return p.parse_args()
 
 
@@ -328,7 +330,7 @@ def run_mm_only(args, local_rank):
                       "higher_is_better": True, "fp4_mm": mm}), flush=True)
 
 
-def rowcol_measurement(nv, torch, W1, peaks, iters=10):
+def rowcol_measurement(nv, torch, W1, peaks, iters=10, variants=None):
     """Plain quantization with rowwise AND columnwise outputs from one read
     (timed beside the step, not part of it), on the step's W1 [4096,14336]
     bf16: round-to-nearest 1x16 and 16x16, stochastic rounding 1x16 (draws
@@ -344,6 +346,8 @@ def rowcol_measurement(nv, torch, W1, peaks, iters=10):
     res = []
     for name, kw in (("RTN 1x16", dict(block="1x16")), ("RTN 16x16", dict(block="16x16")),
                      ("SR 1x16", dict(block="1x16", rounding="sr", seed=0, step=7))):
+        if variants and name not in variants:
+            continue
         run = lambda: nv.nvfp4_quantize(W1, colwise=True, **kw, **outs)   # noqa: E731
         for _ in range(3):
             run()
@@ -372,6 +376,20 @@ def run_c4_only(args, local_rank):
     run = c4["runs"][0]
     print(json.dumps({"metric": "NVFP4 quantize GB/s", "value": run["GB/s"], "unit": "GB/s",
                       "higher_is_better": True, "c4_rowcol": c4}), flush=True)
+
+
+def run_rowcol_only(args, local_rank):
+    import torch
+    import nvfp4_block_quantization_quantize_gb300 as nv
+    torch.cuda.set_device(local_rank)
+    nv.build()
+    nv.load_library()
+    dev = torch.device("cuda", local_rank)
+    W1 = torch.from_numpy(c5_inputs().W1.view(np.int16)).view(torch.bfloat16).to(dev)
+    rc = rowcol_measurement(nv, torch, W1, measured_peaks(), iters=args.steps,
+                            variants=(args.only,) if args.only else None)
+    print(json.dumps({"metric": "NVFP4 quantize GB/s", "value": rc["runs"][0]["GB/s"], "unit": "GB/s",
+                      "higher_is_better": True, "rowcol_plain": rc}), flush=True)
 
 
 # ---------------------------------------------------------------------------------------
@@ -611,6 +629,10 @@ def main():
     if args.c4_only:
         if rank == 0:
             run_c4_only(args, local_rank)
+        return
+    if args.rowcol_only:
+        if rank == 0:
+            run_rowcol_only(args, local_rank)
         return
     if world > 1:
         import torch

@@ -54,6 +54,10 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
     // columnwise codes and scale bytes of the CTA's bands, [band][column]
     __shared__ uint2 ccs[kRowBands][kTileCols];
     __shared__ uint8_t scs[kRowBands][kTileCols];
+    // the thread's block of the current and the next band, copied ahead
+    // asynchronously (each thread reads only its own slot)
+    constexpr int XB = DT == NVFP4_BF16 ? 32 : 64;
+    __shared__ __align__(16) unsigned char xb[2][kThreads * XB];
     if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
     const int64_t chunk = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -78,14 +82,27 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
     }
 
     const int j = threadIdx.x;                  // column within the chunk (its tile is t)
+    auto fetch = [&](int bi) {
+        const int64_t band = band0 + bi;
+        if (valid && bi < kRowBands && band < nbands) {
+            const unsigned char* src = static_cast<const unsigned char*>(a.x) +
+                                       ((band * 16 + rr) * a.K + cb * 16) * (XB / 16);
+#pragma unroll
+            for (int c = 0; c < XB / 16; ++c) cp_async16(&xb[bi & 1][threadIdx.x * XB + 16 * c], src + 16 * c);
+        }
+        cp_async_commit();
+    };
+    fetch(0);
     for (int bi = 0; bi < kRowBands; ++bi) {
         const int64_t band = band0 + bi;
         if (band >= nbands) break;              // CTA-uniform
         const int64_t row = band * 16 + rr;
         const int64_t e0 = row * a.K + cb * 16;
+        fetch(bi + 1);
+        cp_async_wait<1>();
         float y[16];
         if (valid) {
-            load16<DT>(a.x, e0, y);
+            lds16<DT>(&xb[bi & 1][threadIdx.x * XB], y);
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) y[i] = 0.0f;
@@ -150,6 +167,7 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
         scs[bi][j] = static_cast<uint8_t>(sf);
         __syncthreads();                        // ys and ws are rewritten by the next band
     }
+    cp_async_wait<0>();
     // x^T's row col holds 8 code bytes and one scale byte per band: the CTA's
     // bands give each of its columns one run of consecutive bytes, written
     // by consecutive threads
