@@ -126,9 +126,9 @@ __global__ void __launch_bounds__(kThreads) k_amax_rows(const void* x, const flo
     if (lane == 0) out[row] = m;
 }
 
-template <int ODT>
-__device__ __forceinline__ void dequant_block(const DequantArgs& a, int64_t blk, uint32_t w0, uint32_t w1,
-                                              uint32_t sf, float Sdec, bool per_row, int64_t bpr) {
+// dequantized values (q * d) * S_dec of one block
+__device__ __forceinline__ void dequant_values(const DequantArgs& a, int64_t blk, uint32_t w0, uint32_t w1,
+                                               uint32_t sf, float Sdec, bool per_row, int64_t bpr, float* v) {
     float Sd = Sdec;
     if (per_row) {
         float se;
@@ -138,18 +138,22 @@ __device__ __forceinline__ void dequant_block(const DequantArgs& a, int64_t blk,
     float q[16];
     e2m1_decode8(w0, q);
     e2m1_decode8(w1, q + 8);
-    float v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = mul_rn(mul_rn(q[i], d), Sd);
-    if (ODT == NVFP4_BF16) store16_bf16(static_cast<uint16_t*>(a.out), blk * 16, v);
-    else store16_f32(static_cast<float*>(a.out), blk * 16, v);
 }
 
 // Four blocks per thread per step, interleaved across the warp (lane l takes
-// blocks base + l, +32, +64, +96) so every load and store instruction covers
-// consecutive blocks; all four blocks' codes and scales are loaded first.
+// blocks base + l, +32, +64, +96) so every load covers consecutive blocks;
+// all four blocks' codes and scales are loaded first.  The 32 blocks of one
+// group are contiguous in the output too: the warp passes them through a
+// shared buffer (16-byte chunk c of lane l at CH*l + (c ^ swz(l)), which
+// keeps both the writes and the reads at the minimum of shared-memory
+// wavefronts) so that store instruction c of lane l writes chunk 32 c + l,
+// 512 consecutive bytes per instruction.
 template <int ODT>
 __global__ void __launch_bounds__(kThreads) k_dequant(const DequantArgs a) {
+    constexpr int CH = ODT == NVFP4_BF16 ? 2 : 4;          // 16-byte output chunks per block
+    __shared__ uint4 wst[kThreads / 32][32 * CH];
     const int64_t bpr = a.K / 16;
     const int64_t nblk = a.M * bpr;
     float Senc = 1.0f, Sdec = 1.0f;
@@ -157,10 +161,13 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DequantArgs a) {
     const bool per_row = a.gamax_mode == NVFP4_GAMAX_ROW || a.gamax_mode == NVFP4_GAMAX_ROW_GIVEN;
     if (per_tensor) global_scales(a.gamax[0], a.bound, Senc, Sdec);
     const int lane = threadIdx.x & 31;
+    uint4* buf = wst[threadIdx.x >> 5];
+    auto pos = [](int l, int c) { return CH * l + (c ^ ((l / (8 / CH)) & (CH - 1))); };
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const uint2* codes = reinterpret_cast<const uint2*>(a.codes);
-    for (int64_t base = warp * 128; base < nblk; base += nwarps * 128) {
+    uint4* out = static_cast<uint4*>(a.out);
+    for (int64_t base = warp * 128; base < nblk; base += nwarps * 128) {   // warp-uniform
         uint2 w[4];
         uint32_t sf[4];
 #pragma unroll
@@ -173,8 +180,32 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DequantArgs a) {
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int64_t blk = base + 32 * k + lane;
-            if (blk < nblk) dequant_block<ODT>(a, blk, w[k].x, w[k].y, sf[k], Sdec, per_row, bpr);
+            const int64_t blk0 = base + 32 * k;                 // the group's first block
+            if (blk0 + lane < nblk) {
+                float v[16];
+                dequant_values(a, blk0 + lane, w[k].x, w[k].y, sf[k], Sdec, per_row, bpr, v);
+                if (ODT == NVFP4_BF16) {
+                    uint32_t h[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        h[i] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i]))) |
+                               (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i + 1]))) << 16);
+                    buf[pos(lane, 0)] = make_uint4(h[0], h[1], h[2], h[3]);
+                    buf[pos(lane, 1)] = make_uint4(h[4], h[5], h[6], h[7]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        buf[pos(lane, c)] = make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
+                                                       __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int q = 32 * c + lane;
+                if (blk0 + q / CH < nblk) out[blk0 * CH + q] = buf[pos(q / CH, q % CH)];
+            }
+            __syncwarp();
         }
     }
 }
