@@ -12,8 +12,8 @@
  * Conventions shared by every call
  *   - Data pointers are DEVICE pointers owned by the caller; the library never
  *     allocates, frees or synchronizes.  Work is enqueued on `stream` (a
- *     cudaStream_t passed as void*; NULL = the legacy default stream) on the
- *     current CUDA device.
+ *     cudaStream_t; NULL = the legacy default stream) on the current CUDA
+ *     device.
  *   - Layouts are row-major:
  *       x          [M,K]     fp32 or bf16
  *       residual   [M,K]     fp32, read and overwritten in place
@@ -41,6 +41,12 @@
 #define NVFP4_H
 
 #include <stdint.h>
+
+/* cudaStream_t without the CUDA headers: the same opaque handle type the CUDA
+ * runtime declares (a repeated identical typedef is valid C11 and C++). */
+#ifndef CUDART_VERSION
+typedef struct CUstream_st* cudaStream_t;
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -133,7 +139,7 @@ int nvfp4_quantize(const void* x, int64_t M, int64_t K, int dtype, int block, in
                    float* residual, uint64_t seed, uint64_t step, int64_t row_offset,
                    int gamax_mode, float* gamax, int err_mode, float scale_bound,
                    uint8_t* codes, uint8_t* scales, uint8_t* codes_col, uint8_t* scales_col,
-                   void* stream);
+                   cudaStream_t stream);
 
 /*
  * nvfp4_dequantize -- [fp4-train, API] dequantize(packed, scale, M, K):
@@ -144,7 +150,7 @@ int nvfp4_quantize(const void* x, int64_t M, int64_t K, int dtype, int block, in
  */
 int nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int64_t K,
                      int gamax_mode, const float* gamax, float scale_bound,
-                     void* out, int out_dtype, void* stream);
+                     void* out, int out_dtype, cudaStream_t stream);
 
 /*
  * nvfp4_qdq -- [fp4-train, API] qdq(x, stochastic, residual, seed, step):
@@ -155,7 +161,7 @@ int nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int
 int nvfp4_qdq(const void* x, int64_t M, int64_t K, int dtype, int block, int rounding,
               float* residual, uint64_t seed, uint64_t step, int64_t row_offset,
               int gamax_mode, float* gamax, int err_mode, float scale_bound,
-              uint8_t* codes, uint8_t* scales, void* out_bf16, void* stream);
+              uint8_t* codes, uint8_t* scales, void* out_bf16, cudaStream_t stream);
 
 /*
  * nvfp4_amax -- the global amax step on its own [4o6 PR, What; Design]:
@@ -164,7 +170,22 @@ int nvfp4_qdq(const void* x, int64_t M, int64_t K, int dtype, int block, int rou
  * residual may be NULL.
  */
 int nvfp4_amax(const void* x, int64_t M, int64_t K, int dtype, const float* residual,
-               int mode, float* out, void* stream);
+               int mode, float* out, cudaStream_t stream);
+
+/*
+ * nvfp4_global_scales -- the global encode / decode scales of n global amaxes
+ * ("Add NVFP4 four-over-six (row-wise) quantization to the training
+ * prototype", What and Design): S_enc[i] = min(6*bound / gamax[i], FLT_MAX),
+ * or 1 when gamax[i] is not a positive finite number, and S_dec[i] = 1 /
+ * S_enc[i] (IEEE divisions) -- the values every quantize and dequantize call
+ * uses, for consumers that apply the decode scale themselves (a block-scaled
+ * matrix multiply multiplies its result by S_dec(A) * S_dec(B)).
+ * gamax, s_enc, s_dec: device fp32 [n] (4-byte aligned); s_enc or s_dec may be
+ * NULL (not both when n > 0).  EINVAL on n < 0, a bound outside (0, 448] or
+ * bad pointers.
+ */
+int nvfp4_global_scales(const float* gamax, int64_t n, float scale_bound, float* s_enc, float* s_dec,
+                        cudaStream_t stream);
 
 /*
  * nvfp4_scales_to_mma -- re-lay a row-major scale matrix [rows, cols] (one
@@ -179,7 +200,7 @@ int nvfp4_amax(const void* x, int64_t M, int64_t K, int dtype, const float* resi
  * scales  device [rows, cols] bytes;  out  device [R * C] bytes (caller-owned).
  * EINVAL when rows < 0, cols < 0, or a pointer is NULL (with rows, cols > 0).
  */
-int nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out, void* stream);
+int nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out, cudaStream_t stream);
 
 /*
  * nvfp4_mm -- out = (A B^T) * S_dec(A) * S_dec(B) on the block-scaled FP4
@@ -198,7 +219,7 @@ int nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t cols, uint8
  */
 int nvfp4_mm(const uint8_t* codes_a, const uint8_t* scales_a, const uint8_t* codes_b, const uint8_t* scales_b,
              int64_t M, int64_t N, int64_t K, const float* gamax_a, const float* gamax_b, float scale_bound,
-             void* out, int out_dtype, void* stream);
+             void* out, int out_dtype, cudaStream_t stream);
 
 /*
  * nvfp4_probe_divide -- diagnostic.  out[i] = a[i] / b[i] computed by the
@@ -209,7 +230,21 @@ int nvfp4_mm(const uint8_t* codes_a, const uint8_t* scales_a, const uint8_t* cod
  * n >= 0 elements, 4-byte aligned; EINVAL on bad arguments.  It exists so the
  * routine can be checked exhaustively against IEEE division.
  */
-int nvfp4_probe_divide(const float* a, const float* b, float* out, int64_t n, void* stream);
+int nvfp4_probe_divide(const float* a, const float* b, float* out, int64_t n, cudaStream_t stream);
+
+/*
+ * nvfp4_probe_e2m1 -- diagnostic.  The e2m1 codes that the quantizers' element
+ * encode ("fp4-train", Method: each value rounded to the signed grid
+ * {0,.5,1,1.5,2,3,4,6}; "Add NVFP4 four-over-six (row-wise) quantization to
+ * the training prototype", Design: NaN encodes to +6) gives the n fp32 values
+ * whose bit patterns are first, first + 1, ..., first + n - 1, packed two per
+ * byte like quantized codes (pattern 2j in the low nibble of byte j; for odd n
+ * the last byte's high nibble is 0).  out is
+ * device memory of (n + 1) / 2 bytes, 4-byte aligned.  EINVAL when n < 0 or
+ * first + n > 2^32.  It exists so the conversion can be checked against the
+ * oracle over every fp32 value.
+ */
+int nvfp4_probe_e2m1(uint32_t first, int64_t n, uint8_t* out, cudaStream_t stream);
 
 /* message for the calling thread's last non-OK status ("" if none) */
 const char* nvfp4_last_error(void);

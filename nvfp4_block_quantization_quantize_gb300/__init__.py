@@ -43,7 +43,8 @@ _NAMES = {
 }
 
 EXPORTED = ("nvfp4_quantize", "nvfp4_dequantize", "nvfp4_qdq", "nvfp4_amax",
-            "nvfp4_probe_divide", "nvfp4_last_error", "nvfp4_abi_version")
+            "nvfp4_global_scales", "nvfp4_probe_divide", "nvfp4_probe_e2m1", "nvfp4_last_error",
+            "nvfp4_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -82,6 +83,10 @@ def load_library(path: str | None = None):
         lib.nvfp4_amax.argtypes = [P, i64, i64, i32, P, i32, P, P]
         lib.nvfp4_probe_divide.restype = i32
         lib.nvfp4_probe_divide.argtypes = [P, P, P, i64, P]
+        lib.nvfp4_global_scales.restype = i32
+        lib.nvfp4_global_scales.argtypes = [P, i64, f32, P, P, P]
+        lib.nvfp4_probe_e2m1.restype = i32
+        lib.nvfp4_probe_e2m1.argtypes = [ctypes.c_uint32, i64, P, P]
         lib.nvfp4_scales_to_mma.restype = i32
         lib.nvfp4_scales_to_mma.argtypes = [P, i64, i64, P, P]
         lib.nvfp4_mm.restype = i32
@@ -162,23 +167,57 @@ def _host_in(t, dev):
     return _stage(t.contiguous(), dev)
 
 
-def _out_buf(shape, dtype, given, dev, host):
-    """An output: the given device tensor or a new device one (copied back
-    into a given host tensor by _finish_host); a call on device tensors
-    refuses host outputs."""
+def _numel(shape):
+    n = 1
+    for s in shape:
+        n *= int(s)
+    return n
+
+
+def _check_dev(t, name, dtype, numel, dev, at_least=False):
+    """A device tensor the kernels read or write through a raw pointer: it must
+    be on the call's device, of the expected dtype, contiguous, and hold the
+    expected number of elements (at least that many when at_least)."""
+    if not t.is_cuda or t.device != dev:
+        raise ValueError(f"nvfp4: {name} must be on {dev} (got {t.device})")
+    if t.dtype != dtype:
+        raise ValueError(f"nvfp4: {name} must be {dtype} (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"nvfp4: {name} must be contiguous")
+    if (t.numel() < numel) if at_least else (t.numel() != numel):
+        raise ValueError(f"nvfp4: {name} must hold {'at least ' if at_least else ''}{numel} elements "
+                         f"(got {t.numel()})")
+    return t
+
+
+def _out_buf(shape, dtype, given, dev, host, name="output"):
+    """An output: the given device tensor (checked) or a new device one
+    (copied back into a given host tensor by _finish_host); a call on device
+    tensors refuses host outputs."""
     if given is not None and given.is_cuda:
-        return given
+        return _check_dev(given, name, dtype, _numel(shape), dev)
     if given is not None and not host:
         raise ValueError("nvfp4: the outputs of a call on device tensors must be device tensors")
+    if given is not None and (given.dtype != dtype or given.numel() != _numel(shape)):
+        raise ValueError(f"nvfp4: {name} must be {dtype} with {_numel(shape)} elements")
     return _empty(shape, dtype, dev)
 
 
-def _dev_residual(residual, dev):
-    """The in-place residual of a call on device tensors: it must live on the
-    call's device (a staged copy would lose the update)."""
-    if residual is not None and residual.device != dev:
+def _dev_residual(residual, dev, M=None, K=None):
+    """The in-place residual of a call on device tensors: float32 [M,K],
+    contiguous, on the call's device (a staged copy would lose the update)."""
+    if residual is None:
+        return None
+    if residual.device != dev:
         raise ValueError("nvfp4: the residual of a call on device tensors must be on x's device")
-    return residual
+    if M is None:
+        return residual
+    return _check_dev(residual, "residual", torch.float32, M * K, dev)
+
+
+def _host_residual(residual, M, K):
+    if residual is not None and (residual.dtype != torch.float32 or residual.numel() != M * K):
+        raise ValueError("nvfp4: the residual must be float32 with M*K elements")
 
 
 def _inputs_ready(stream):
@@ -199,7 +238,8 @@ def _finish_host(res: dict, given: dict, stream=None) -> dict:
         if not v.is_cuda or (g is not None and g.is_cuda):
             out[k] = v
         elif g is not None:
-            g.copy_(v, non_blocking=True)
+            dst = g if g.shape == v.shape else g.reshape(-1)[:v.numel()].view(v.shape)
+            dst.copy_(v, non_blocking=True)
             out[k] = g
         else:
             h = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
@@ -224,17 +264,32 @@ def _default_bound(err_mode: int, scale_bound):
     return 448.0 if err_mode == ERR_NONE else 256.0
 
 
-def _gamax_buffer(mode: int, gamax, M: int, dev):
+def _gamax_buffer(mode: int, gamax, M: int, dev, host: bool = False):
+    """The device buffer the kernels read (GIVEN modes) or write (TENSOR /
+    ROW: 1 or M floats, reduced with device atomics).  A device call must pass
+    a written gamax as a float32 CUDA tensor on x's device; a host call may
+    pass a host tensor, which _finish_host fills from a device buffer."""
+    need = 1 if mode in (GAMAX_TENSOR, GAMAX_TENSOR_GIVEN) else max(M, 1)
     if mode in (GAMAX_TENSOR, GAMAX_ROW):
         if gamax is not None:
-            return gamax
-        return _empty((1,) if mode == GAMAX_TENSOR else (max(M, 1),), torch.float32, dev)
+            if not torch.is_tensor(gamax):
+                raise ValueError("nvfp4: a computed gamax is written into a tensor")
+            if gamax.is_cuda:
+                return _check_dev(gamax, "gamax", torch.float32, need, dev, at_least=True)
+            if not host:
+                raise ValueError("nvfp4: the gamax of a call on device tensors must be a device tensor")
+            if gamax.dtype != torch.float32 or gamax.numel() < need:
+                raise ValueError(f"nvfp4: gamax must be float32 with at least {need} elements")
+        return _empty((need,), torch.float32, dev)
     if mode in (GAMAX_TENSOR_GIVEN, GAMAX_ROW_GIVEN):
         if gamax is None:
             raise ValueError("a *_given gamax_mode needs gamax")
         if not torch.is_tensor(gamax):
             gamax = torch.tensor([float(gamax)], dtype=torch.float32)
-        return gamax.to(dev, torch.float32).contiguous()
+        g = gamax.to(dev, torch.float32).reshape(-1).contiguous()
+        if g.numel() < need:
+            raise ValueError(f"nvfp4: gamax must hold at least {need} values")
+        return g
     return None
 
 
@@ -254,19 +309,24 @@ def nvfp4_quantize(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=No
     gm, em = _enum("gamax_mode", gamax_mode), _enum("err_mode", err_mode)
     bound = _default_bound(em, scale_bound)
     given = {"codes": codes, "scales": scales, "codes_col": codes_col, "scales_col": scales_col}
+    if host:
+        _host_residual(residual, M, K)
     xd = _host_in(x, dev) if host else x.contiguous()
-    rd = _host_in(residual, dev) if host else _dev_residual(residual, dev)
-    g = _gamax_buffer(gm, gamax, M, dev)
-    codes = _out_buf((M, K // 2), torch.uint8, codes, dev, host)
-    scales = _out_buf((M, K // 16), torch.uint8, scales, dev, host)
+    rd = _host_in(residual, dev) if host else _dev_residual(residual, dev, M, K)
+    g = _gamax_buffer(gm, gamax, M, dev, host)
+    if host and torch.is_tensor(gamax) and not gamax.is_cuda and gm in (GAMAX_TENSOR, GAMAX_ROW):
+        given["gamax"] = gamax
+    codes = _out_buf((M, K // 2), torch.uint8, codes, dev, host, "codes")
+    scales = _out_buf((M, K // 16), torch.uint8, scales, dev, host, "scales")
     if colwise:
-        codes_col = _out_buf((K, M // 2), torch.uint8, codes_col, dev, host)
-        scales_col = _out_buf((K, M // 16), torch.uint8, scales_col, dev, host)
+        codes_col = _out_buf((K, M // 2), torch.uint8, codes_col, dev, host, "codes_col")
+        scales_col = _out_buf((K, M // 16), torch.uint8, scales_col, dev, host, "scales_col")
     if host:
         _inputs_ready(stream)
-    rc = lib.nvfp4_quantize(_ptr(xd), M, K, _x_dtype(x), blk, rnd, _ptr(rd), seed, step,
-                            row_offset, gm, _ptr(g), em, bound, _ptr(codes), _ptr(scales),
-                            _ptr(codes_col), _ptr(scales_col), _stream(stream))
+    with torch.cuda.device(dev):
+        rc = lib.nvfp4_quantize(_ptr(xd), M, K, _x_dtype(x), blk, rnd, _ptr(rd), seed, step,
+                                row_offset, gm, _ptr(g), em, bound, _ptr(codes), _ptr(scales),
+                                _ptr(codes_col), _ptr(scales_col), _stream(stream))
     _check(lib, rc)
     out = {"codes": codes, "scales": scales}
     if colwise:
@@ -293,17 +353,20 @@ def nvfp4_qdq(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=None, s
     blk, rnd = _enum("block", block), _enum("rounding", rounding)
     gm, em = _enum("gamax_mode", gamax_mode), _enum("err_mode", err_mode)
     bound = _default_bound(em, scale_bound)
+    if host:
+        _host_residual(residual, M, K)
     xd = _host_in(x, dev) if host else x.contiguous()
-    rd = _host_in(residual, dev) if host else _dev_residual(residual, dev)
-    g = _gamax_buffer(gm, gamax, M, dev)
-    o = _out_buf((M, K), torch.bfloat16, out, dev, host)
+    rd = _host_in(residual, dev) if host else _dev_residual(residual, dev, M, K)
+    g = _gamax_buffer(gm, gamax, M, dev, host)
+    o = _out_buf((M, K), torch.bfloat16, out, dev, host, "out")
     codes = _out_buf((M, K // 2), torch.uint8, None, dev, host) if want_codes else None
     scales = _out_buf((M, K // 16), torch.uint8, None, dev, host) if want_codes else None
     if host:
         _inputs_ready(stream)
-    rc = lib.nvfp4_qdq(_ptr(xd), M, K, _x_dtype(x), blk, rnd, _ptr(rd), seed, step, row_offset,
-                       gm, _ptr(g), em, bound, _ptr(codes), _ptr(scales), _ptr(o),
-                       _stream(stream))
+    with torch.cuda.device(dev):
+        rc = lib.nvfp4_qdq(_ptr(xd), M, K, _x_dtype(x), blk, rnd, _ptr(rd), seed, step, row_offset,
+                           gm, _ptr(g), em, bound, _ptr(codes), _ptr(scales), _ptr(o),
+                           _stream(stream))
     _check(lib, rc)
     res = {"out": o}
     if want_codes:
@@ -312,6 +375,8 @@ def nvfp4_qdq(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=None, s
         res["gamax"] = g
     if host:
         given = {"out": out}
+        if torch.is_tensor(gamax) and not gamax.is_cuda and gm in (GAMAX_TENSOR, GAMAX_ROW):
+            given["gamax"] = gamax
         if residual is not None and rd is not residual:
             given["residual"] = residual
             res["residual"] = rd
@@ -331,16 +396,24 @@ def nvfp4_dequantize(codes: torch.Tensor, scales: torch.Tensor, M: int, K: int, 
     bound = 448.0 if scale_bound is None else float(scale_bound)
     c = _host_in(codes, dev) if host else codes.contiguous()
     s = _host_in(scales, dev) if host else scales.contiguous()
+    for t, name, n in ((c, "codes", M * K // 2), (s, "scales", M * K // 16)):
+        if t.dtype != torch.uint8 or t.numel() != n:
+            raise ValueError(f"nvfp4: {name} must be uint8 with {n} elements")
     g = None
     if gm != GAMAX_NONE:
         if gamax is None:
             raise ValueError("gamax_mode needs gamax")
         g = (gamax if torch.is_tensor(gamax) else torch.tensor([float(gamax)])).to(dev, torch.float32)
-    o = _out_buf((M, K), torch.bfloat16 if od == BF16 else torch.float32, out, dev, host)
+        g = g.reshape(-1).contiguous()
+        need = M if gm in (GAMAX_ROW, GAMAX_ROW_GIVEN) else 1
+        if g.numel() < need:
+            raise ValueError(f"nvfp4: gamax must hold at least {need} values")
+    o = _out_buf((M, K), torch.bfloat16 if od == BF16 else torch.float32, out, dev, host, "out")
     if host:
         _inputs_ready(stream)
-    rc = lib.nvfp4_dequantize(_ptr(c), _ptr(s), M, K, gm, _ptr(g), bound, _ptr(o), od,
-                              _stream(stream))
+    with torch.cuda.device(dev):
+        rc = lib.nvfp4_dequantize(_ptr(c), _ptr(s), M, K, gm, _ptr(g), bound, _ptr(o), od,
+                                  _stream(stream))
     _check(lib, rc)
     return _finish_host({"o": o}, {"o": out}, stream)["o"] if host else o
 
@@ -351,15 +424,23 @@ def nvfp4_amax(x: torch.Tensor, *, residual=None, per_row: bool = False, out=Non
     host = not x.is_cuda
     dev = _device_of(x, residual)
     M, K = x.shape
+    if host:
+        _host_residual(residual, M, K)
     xd = _host_in(x, dev) if host else x.contiguous()
-    rd = _host_in(residual, dev) if host else _dev_residual(residual, dev)
+    rd = _host_in(residual, dev) if host else _dev_residual(residual, dev, M, K)
+    need = max(M, 1) if per_row else 1
     # the amax is reduced with device atomics: always a device buffer
-    o = out if out is not None and out.is_cuda else _empty((max(M, 1),) if per_row else (1,),
-                                                           torch.float32, dev)
+    if out is not None and out.is_cuda:
+        o = _check_dev(out, "out", torch.float32, need, dev, at_least=True)
+    else:
+        if out is not None and (out.dtype != torch.float32 or out.numel() < need):
+            raise ValueError(f"nvfp4: out must be float32 with at least {need} elements")
+        o = _empty((need,), torch.float32, dev)
     if host:
         _inputs_ready(stream)
-    rc = lib.nvfp4_amax(_ptr(xd), M, K, _x_dtype(x), _ptr(rd), GAMAX_ROW if per_row else GAMAX_TENSOR,
-                        _ptr(o), _stream(stream))
+    with torch.cuda.device(dev):
+        rc = lib.nvfp4_amax(_ptr(xd), M, K, _x_dtype(x), _ptr(rd), GAMAX_ROW if per_row else GAMAX_TENSOR,
+                            _ptr(o), _stream(stream))
     _check(lib, rc)
     if host or (out is not None and not out.is_cuda):
         return _finish_host({"o": o}, {"o": out}, stream)["o"]
@@ -394,6 +475,20 @@ def nvfp4_mm(codes_a, scales_a, codes_b, scales_b, M: int, N: int, K: int, *, ga
     return o
 
 
+def nvfp4_global_scales(gamax: torch.Tensor, scale_bound: float = 448.0, stream=None):
+    """(S_enc, S_dec) of each global amax in ``gamax`` (device float32), as
+    every quantize / dequantize call computes them (see nvfp4.h)."""
+    lib = load_library()
+    g = gamax.reshape(-1)
+    if not (g.is_cuda and g.dtype == torch.float32 and g.is_contiguous()):
+        raise ValueError("nvfp4_global_scales: gamax must be a contiguous CUDA float32 tensor")
+    enc, dec = torch.empty_like(g), torch.empty_like(g)
+    with torch.cuda.device(g.device):
+        _check(lib, lib.nvfp4_global_scales(_ptr(g), g.numel(), float(scale_bound), _ptr(enc), _ptr(dec),
+                                            _stream(stream)))
+    return enc, dec
+
+
 def nvfp4_probe_divide(a: torch.Tensor, b: torch.Tensor, stream=None) -> torch.Tensor:
     """Diagnostic: the plain path's device division a / b, elementwise (fp32)."""
     lib = load_library()
@@ -402,6 +497,16 @@ def nvfp4_probe_divide(a: torch.Tensor, b: torch.Tensor, stream=None) -> torch.T
     out = torch.empty_like(a)
     _check(lib, lib.nvfp4_probe_divide(_ptr(a), _ptr(b), _ptr(out), a.numel(), _stream(stream)))
     return out
+
+
+def nvfp4_probe_e2m1(first: int, n: int, out=None, stream=None) -> torch.Tensor:
+    """Diagnostic: the device e2m1 codes of the n fp32 bit patterns from
+    ``first`` on, packed two per byte (uint8 [(n + 1) // 2])."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    o = out if out is not None else _empty(((n + 1) // 2,), torch.uint8, dev)
+    _check(lib, lib.nvfp4_probe_e2m1(first, n, _ptr(o), _stream(stream)))
+    return o
 
 
 def nvfp4_last_error() -> str:

@@ -13,7 +13,7 @@ from __future__ import annotations
 
 import torch
 
-from . import nvfp4_scales_to_mma
+from . import nvfp4_global_scales, nvfp4_scales_to_mma
 
 
 def to_fp4_operands(q: dict) -> dict:
@@ -29,12 +29,10 @@ def to_fp4_operands(q: dict) -> dict:
 
 
 def _scale_dec(g, bound: float) -> torch.Tensor | float:
+    """The per-tensor decode scale the library derives from a global amax."""
     if g is None:
         return 1.0
-    A = g.float().reshape(-1)[0]
-    enc = torch.where((A > 0) & torch.isfinite(A), torch.clamp(6.0 * bound / A, max=torch.finfo(torch.float32).max),
-                      torch.ones_like(A))
-    return 1.0 / enc
+    return nvfp4_global_scales(g.float().reshape(-1)[:1].contiguous(), bound)[1]
 
 
 def fp4_mm(a: dict, b: dict, *, out_dtype=torch.bfloat16, scale_bound: float = 448.0) -> torch.Tensor:

@@ -102,7 +102,7 @@ int nvfp4_quantize(const void* x, int64_t M, int64_t K, int dtype, int block, in
                    float* residual, uint64_t seed, uint64_t step, int64_t row_offset,
                    int gamax_mode, float* gamax, int err_mode, float scale_bound,
                    uint8_t* codes, uint8_t* scales, uint8_t* codes_col, uint8_t* scales_col,
-                   void* stream) {
+                   cudaStream_t stream) {
     g_msg[0] = '\0';
     if ((codes_col == nullptr) != (scales_col == nullptr))
         return fail(NVFP4_EINVAL, "give both codes_col and scales_col, or neither");
@@ -124,7 +124,7 @@ int nvfp4_quantize(const void* x, int64_t M, int64_t K, int dtype, int block, in
 int nvfp4_qdq(const void* x, int64_t M, int64_t K, int dtype, int block, int rounding,
               float* residual, uint64_t seed, uint64_t step, int64_t row_offset,
               int gamax_mode, float* gamax, int err_mode, float scale_bound,
-              uint8_t* codes, uint8_t* scales, void* out_bf16, void* stream) {
+              uint8_t* codes, uint8_t* scales, void* out_bf16, cudaStream_t stream) {
     g_msg[0] = '\0';
     int rc = check_quant(x, M, K, dtype, block, rounding, residual, gamax_mode, gamax, err_mode,
                          scale_bound, false);
@@ -141,7 +141,7 @@ int nvfp4_qdq(const void* x, int64_t M, int64_t K, int dtype, int block, int rou
 
 int nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int64_t K,
                      int gamax_mode, const float* gamax, float scale_bound, void* out,
-                     int out_dtype, void* stream) {
+                     int out_dtype, cudaStream_t stream) {
     g_msg[0] = '\0';
     int rc = check_shape(M, K);
     if (rc) return rc;
@@ -161,7 +161,7 @@ int nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int
 }
 
 int nvfp4_amax(const void* x, int64_t M, int64_t K, int dtype, const float* residual, int mode,
-               float* out, void* stream) {
+               float* out, cudaStream_t stream) {
     g_msg[0] = '\0';
     int rc = check_shape(M, K);
     if (rc) return rc;
@@ -177,7 +177,7 @@ int nvfp4_amax(const void* x, int64_t M, int64_t K, int dtype, const float* resi
     return NVFP4_OK;
 }
 
-int nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out, void* stream) {
+int nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out, cudaStream_t stream) {
     g_msg[0] = '\0';
     if (rows < 0 || cols < 0) return fail(NVFP4_EINVAL, "rows and cols must be >= 0");
     const bool any = rows > 0 && cols > 0;
@@ -192,7 +192,7 @@ int nvfp4_scales_to_mma(const uint8_t* scales, int64_t rows, int64_t cols, uint8
 
 int nvfp4_mm(const uint8_t* codes_a, const uint8_t* scales_a, const uint8_t* codes_b, const uint8_t* scales_b,
              int64_t M, int64_t N, int64_t K, const float* gamax_a, const float* gamax_b, float scale_bound,
-             void* out, int out_dtype, void* stream) {
+             void* out, int out_dtype, cudaStream_t stream) {
     g_msg[0] = '\0';
     if (M < 0 || N < 0 || K < 0) return fail(NVFP4_EINVAL, "M, N and K must be >= 0");
     if (M % 128 || N % 128 || K % 64)
@@ -221,7 +221,22 @@ int nvfp4_mm(const uint8_t* codes_a, const uint8_t* scales_a, const uint8_t* cod
     return NVFP4_OK;
 }
 
-int nvfp4_probe_divide(const float* a, const float* b, float* out, int64_t n, void* stream) {
+int nvfp4_global_scales(const float* gamax, int64_t n, float scale_bound, float* s_enc, float* s_dec,
+                        cudaStream_t stream) {
+    g_msg[0] = '\0';
+    if (n < 0) return fail(NVFP4_EINVAL, "n must be >= 0");
+    if (!(scale_bound > 0.0f && scale_bound <= 448.0f)) return fail(NVFP4_EINVAL, "scale_bound must be in (0, 448]");
+    int rc;
+    if ((rc = check_ptr(gamax, "gamax", n > 0, 4))) return rc;
+    if ((rc = check_ptr(s_enc, "s_enc", false, 4))) return rc;
+    if ((rc = check_ptr(s_dec, "s_dec", false, 4))) return rc;
+    if (n > 0 && !s_enc && !s_dec) return fail(NVFP4_EINVAL, "give s_enc, s_dec or both");
+    const int err = nvfp4::launch_global_scales(gamax, n, scale_bound, s_enc, s_dec, stream);
+    if (err) return cuda_fail(err, "global scales launch");
+    return NVFP4_OK;
+}
+
+int nvfp4_probe_divide(const float* a, const float* b, float* out, int64_t n, cudaStream_t stream) {
     g_msg[0] = '\0';
     if (n < 0) return fail(NVFP4_EINVAL, "n must be >= 0");
     int rc;
@@ -229,6 +244,18 @@ int nvfp4_probe_divide(const float* a, const float* b, float* out, int64_t n, vo
     if ((rc = check_ptr(b, "b", n > 0, 4))) return rc;
     if ((rc = check_ptr(out, "out", n > 0, 4))) return rc;
     const int err = nvfp4::launch_probe_divide(a, b, out, n, stream);
+    if (err) return cuda_fail(err, "probe launch");
+    return NVFP4_OK;
+}
+
+int nvfp4_probe_e2m1(uint32_t first, int64_t n, uint8_t* out, cudaStream_t stream) {
+    g_msg[0] = '\0';
+    if (n < 0 || n > (int64_t{1} << 32)) return fail(NVFP4_EINVAL, "n must be in [0, 2^32]");
+    if (static_cast<uint64_t>(first) + static_cast<uint64_t>(n) > (uint64_t{1} << 32))
+        return fail(NVFP4_EINVAL, "first + n must not pass 2^32");
+    int rc;
+    if ((rc = check_ptr(out, "out", n > 0, 4))) return rc;
+    const int err = nvfp4::launch_probe_e2m1(first, n, out, stream);
     if (err) return cuda_fail(err, "probe launch");
     return NVFP4_OK;
 }

@@ -229,6 +229,42 @@ __global__ void __launch_bounds__(kThreads) k_probe_divide(const float* a, const
     }
 }
 
+// out holds the e2m1 codes of the fp32 bit patterns first, first + 1, ...,
+// first + n - 1, packed like quantized codes (pattern 2j in the low nibble of
+// byte j; for odd n the last high nibble is 0), encoded by the routine every
+// quantize kernel uses.
+__global__ void __launch_bounds__(kThreads) k_probe_e2m1(uint32_t first, int64_t n, uint8_t* out) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g * 8 < n; g += stride) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(first + static_cast<uint32_t>(g * 8 + i));
+        const uint32_t w = e2m1_encode8(v);
+        if (g * 8 + 8 <= n) {
+            reinterpret_cast<uint32_t*>(out)[g] = w;
+        } else {
+            for (int64_t b = 0; 8 * g + 2 * b < n; ++b) {
+                const uint32_t byte = (w >> (8 * b)) & 0xFFu;
+                out[4 * g + b] = static_cast<uint8_t>(8 * g + 2 * b + 1 < n ? byte : byte & 0x0Fu);
+            }
+        }
+    }
+}
+
+// S_enc[i], S_dec[i] of the global amaxes gamax[i] (the global_scales step
+// every quantize and dequantize kernel runs), for consumers that apply the
+// decode scales themselves.
+__global__ void __launch_bounds__(kThreads) k_global_scales(const float* gamax, int64_t n, float bound,
+                                                            float* s_enc, float* s_dec) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        float enc, dec;
+        global_scales(gamax[i], bound, enc, dec);
+        if (s_enc) s_enc[i] = enc;
+        if (s_dec) s_dec[i] = dec;
+    }
+}
+
 int grid_for(int64_t nblk) {
     const int64_t want = (nblk + kThreads - 1) / kThreads;
     const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
@@ -317,6 +353,20 @@ int launch_probe_divide(const float* a, const float* b, float* out, int64_t n, v
     if (n <= 0) return 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     k_probe_divide<<<grid_for((n + 15) / 16), kThreads, 0, s>>>(a, b, out, n);
+    return static_cast<int>(cudaGetLastError());
+}
+
+int launch_probe_e2m1(uint32_t first, int64_t n, uint8_t* out, void* stream) {
+    if (n <= 0) return 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    k_probe_e2m1<<<grid_for((n + 7) / 8), kThreads, 0, s>>>(first, n, out);
+    return static_cast<int>(cudaGetLastError());
+}
+
+int launch_global_scales(const float* gamax, int64_t n, float bound, float* s_enc, float* s_dec, void* stream) {
+    if (n <= 0) return 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    k_global_scales<<<grid_for(n), kThreads, 0, s>>>(gamax, n, bound, s_enc, s_dec);
     return static_cast<int>(cudaGetLastError());
 }
 

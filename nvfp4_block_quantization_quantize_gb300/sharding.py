@@ -47,7 +47,8 @@ def sharded_quantize(x_shard: torch.Tensor, row_offset: int, *, gamax_mode: str 
         quantize_fn = quantize_fn or nvfp4_quantize
         amax_fn = amax_fn or nvfp4_amax
     if gamax_mode == "tensor":
-        A = global_amax(amax_fn(x_shard).reshape(1).float(), group)
+        # the amax of what is quantized: x + residual under error feedback
+        A = global_amax(amax_fn(x_shard, residual=kw.get("residual")).reshape(1).float(), group)
         out = quantize_fn(x_shard, row_offset=row_offset, gamax_mode="tensor_given", gamax=A, **kw)
         out["gamax"] = A
         return out

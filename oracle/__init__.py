@@ -43,7 +43,7 @@ def build(force: bool = False) -> str:
         if force or stale:
             tmp = _LIB + f".tmp{os.getpid()}"
             cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math",
-                   "-fno-finite-math-only", "-Wall", "-shared", "-fPIC", _SRC, "-o", tmp]
+                   "-fno-finite-math-only", "-Wall", "-pthread", "-shared", "-fPIC", _SRC, "-o", tmp]
             subprocess.run(cmd, check=True)
             os.replace(tmp, _LIB)
     return _LIB
@@ -96,12 +96,43 @@ def _load():
     lib.orc_e2m1_encode_sr_n.argtypes = [P, P, i64, P]
     lib.orc_sr_uniform_n.restype = None
     lib.orc_sr_uniform_n.argtypes = [u64, u64, P, i64, P]
+    lib.orc_e2m1_encode_rn_bits.restype = None
+    lib.orc_e2m1_encode_rn_bits.argtypes = [ctypes.c_uint32, i64, P]
+    lib.orc_set_threads.restype = i32
+    lib.orc_set_threads.argtypes = [i32]
+    lib.orc_get_threads.restype = i32
+    lib.orc_get_threads.argtypes = []
     lib.orc_fp_env_ok.restype = i32
     lib.orc_fp_env_ok.argtypes = []
     if not lib.orc_fp_env_ok():
         raise RuntimeError("oracle: subnormal fp32 arithmetic is flushed on this host")
     _lib = lib
     return lib
+
+
+def set_threads(n: int) -> int:
+    """Worker threads for the oracle's loops over independent rows, bands and
+    elements (0: one per hardware thread); returns the previous count.  The
+    results do not depend on it (each block's arithmetic is unchanged)."""
+    return int(_load().orc_set_threads(int(n)))
+
+
+def threads() -> int:
+    return int(_load().orc_get_threads())
+
+
+class using_threads:
+    """``with oracle.using_threads(n): ...`` runs the oracle on n threads."""
+
+    def __init__(self, n: int):
+        self.n = n
+
+    def __enter__(self):
+        self.old = set_threads(self.n)
+        return threads()
+
+    def __exit__(self, *exc):
+        set_threads(self.old)
 
 
 def _ptr(a):
@@ -151,6 +182,14 @@ def e2m1_encode_sr(v, u) -> np.ndarray:
     u = np.ascontiguousarray(np.broadcast_to(u, v.shape), dtype=np.float64)
     out = np.empty(v.shape, np.uint8)
     lib.orc_e2m1_encode_sr_n(_ptr(v), _ptr(u), v.size, _ptr(out))
+    return out
+
+
+def e2m1_encode_rn_bits(first: int, n: int) -> np.ndarray:
+    """Codes of the n consecutive fp32 bit patterns starting at ``first``."""
+    lib = _load()
+    out = np.empty(n, np.uint8)
+    lib.orc_e2m1_encode_rn_bits(first, n, _ptr(out))
     return out
 
 

@@ -12,12 +12,38 @@
  */
 #include "nvfp4_oracle.h"
 
+#include <algorithm>
 #include <cfloat>
 #include <cmath>
 #include <cstring>
+#include <thread>
 #include <vector>
 
 namespace {
+
+/* Worker threads for the loops over independent rows, bands and elements.
+ * Each block's arithmetic is the same whichever thread runs it, and the only
+ * cross-block combination (the tensor amax) is a NaN-dropping maximum of
+ * non-negative values, which is exact in any order; so every thread count
+ * gives the same bytes.  1 (the default) runs everything on the calling
+ * thread. */
+int g_threads = 1;
+
+/* f(lo, hi) over [0, n), split into at most g_threads contiguous chunks. */
+template <class F>
+void parallel_for(int64_t n, F f) {
+    const int64_t T = std::min<int64_t>(g_threads, n);
+    if (T <= 1) {
+        if (n > 0) f(int64_t{0}, n);
+        return;
+    }
+    std::vector<std::thread> pool;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t lo = n * t / T, hi = n * (t + 1) / T;
+        pool.emplace_back([=] { f(lo, hi); });
+    }
+    for (auto& th : pool) th.join();
+}
 
 /* The signed e2m1 grid magnitudes, index k = 0..7 [fp4-train, Method]. */
 const double kGrid[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
@@ -176,23 +202,28 @@ void quantize_block(const PlaneArgs& P, const int64_t* rows, const int64_t* cols
 }
 
 void quantize_plane(const PlaneArgs& P) {
-    int64_t rows[256], cols[256];
     if (P.block == ORC_BLOCK_1X16) {
-        for (int64_t r = 0; r < P.R; ++r)
-            for (int64_t j = 0; j < P.C / 16; ++j) {
-                for (int t = 0; t < 16; ++t) { rows[t] = r; cols[t] = 16 * j + t; }
-                quantize_block(P, rows, cols, 16);
-            }
+        parallel_for(P.R, [&](int64_t r0, int64_t r1) {
+            int64_t rows[16], cols[16];
+            for (int64_t r = r0; r < r1; ++r)
+                for (int64_t j = 0; j < P.C / 16; ++j) {
+                    for (int t = 0; t < 16; ++t) { rows[t] = r; cols[t] = 16 * j + t; }
+                    quantize_block(P, rows, cols, 16);
+                }
+        });
     } else {
-        for (int64_t i = 0; i < P.R / 16; ++i)
-            for (int64_t j = 0; j < P.C / 16; ++j) {
-                for (int t = 0; t < 16; ++t)
-                    for (int u = 0; u < 16; ++u) {
-                        rows[16 * t + u] = 16 * i + t;
-                        cols[16 * t + u] = 16 * j + u;
-                    }
-                quantize_block(P, rows, cols, 256);
-            }
+        parallel_for(P.R / 16, [&](int64_t i0, int64_t i1) {
+            int64_t rows[256], cols[256];
+            for (int64_t i = i0; i < i1; ++i)
+                for (int64_t j = 0; j < P.C / 16; ++j) {
+                    for (int t = 0; t < 16; ++t)
+                        for (int u = 0; u < 16; ++u) {
+                            rows[16 * t + u] = 16 * i + t;
+                            cols[16 * t + u] = 16 * j + u;
+                        }
+                    quantize_block(P, rows, cols, 256);
+                }
+        });
     }
 }
 
@@ -372,23 +403,25 @@ void orc_global_scales(float A, float bound, float* S_enc, float* S_dec) {
 void orc_amax(const void* x, int64_t M, int64_t K, int dtype, const float* residual,
               int mode, float* out) {
     if (mode == ORC_GAMAX_TENSOR) {
+        /* max over rows of the row maxima: the same value as one running max
+         * (the NaN-dropping maximum of non-negative values is order-free) */
+        std::vector<float> part(static_cast<size_t>(M > 0 ? M : 1), 0.0f);
+        orc_amax(x, M, K, dtype, residual, ORC_GAMAX_ROW, part.data());
         float A = 0.0f;
-        for (int64_t i = 0; i < M * K; ++i) {
-            float y = widen(x, dtype, i);
-            if (residual) y = y + residual[i];
-            A = max_nd(A, std::fabs(y));
-        }
+        for (int64_t r = 0; r < M; ++r) A = max_nd(A, part[r]);
         out[0] = A;
     } else {
-        for (int64_t r = 0; r < M; ++r) {
-            float A = 0.0f;
-            for (int64_t c = 0; c < K; ++c) {
-                float y = widen(x, dtype, r * K + c);
-                if (residual) y = y + residual[r * K + c];
-                A = max_nd(A, std::fabs(y));
+        parallel_for(M, [&](int64_t r0, int64_t r1) {
+            for (int64_t r = r0; r < r1; ++r) {
+                float A = 0.0f;
+                for (int64_t c = 0; c < K; ++c) {
+                    float y = widen(x, dtype, r * K + c);
+                    if (residual) y = y + residual[r * K + c];
+                    A = max_nd(A, std::fabs(y));
+                }
+                out[r] = A;
             }
-            out[r] = A;
-        }
+        });
     }
 }
 
@@ -403,10 +436,12 @@ int orc_quantize(const void* x, int64_t M, int64_t K, int dtype, int block, int 
 
     /* y = x, or x + residual under error feedback [fp4-train, Method] */
     std::vector<float> y(static_cast<size_t>(M * K));
-    for (int64_t i = 0; i < M * K; ++i) {
-        y[i] = widen(x, dtype, i);
-        if (residual) y[i] = y[i] + residual[i];
-    }
+    parallel_for(M * K, [&](int64_t i0, int64_t i1) {
+        for (int64_t i = i0; i < i1; ++i) {
+            y[i] = widen(x, dtype, i);
+            if (residual) y[i] = y[i] + residual[i];
+        }
+    });
 
     /* global amax and scales: per tensor or per row [4o6 PR, What] */
     std::vector<GScale> gs(static_cast<size_t>(M > 0 ? M : 1));
@@ -429,14 +464,18 @@ int orc_quantize(const void* x, int64_t M, int64_t K, int dtype, int block, int 
 
     /* error feedback: carry y - dequant(quantize(y)) [fp4-train, Method] */
     if (residual)
-        for (int64_t i = 0; i < M * K; ++i) residual[i] = y[i] - dq[i];
+        parallel_for(M * K, [&](int64_t i0, int64_t i1) {
+            for (int64_t i = i0; i < i1; ++i) residual[i] = y[i] - dq[i];
+        });
 
     /* columnwise output = the rowwise quantization of x^T with the same
      * per-tensor scale [4o6 PR, Validation; Follow-up fusions] */
     if (colwise) {
         std::vector<float> yt(static_cast<size_t>(M * K));
-        for (int64_t r = 0; r < M; ++r)
-            for (int64_t c = 0; c < K; ++c) yt[c * M + r] = y[r * K + c];
+        parallel_for(K, [&](int64_t c0, int64_t c1) {
+            for (int64_t c = c0; c < c1; ++c)
+                for (int64_t r = 0; r < M; ++r) yt[c * M + r] = y[r * K + c];
+        });
         std::vector<GScale> gt(static_cast<size_t>(K > 0 ? K : 1), M > 0 ? gs[0] : GScale{0.0f, 1.0f, 1.0f});
         PlaneArgs T{yt.data(), K, M, true, block, rounding, err_mode, scale_bound, gt.data(),
                     seed, step, row_offset, codes_col, scales_col, nullptr};
@@ -463,21 +502,25 @@ int orc_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t M, int64
                    void* out, int out_dtype) {
     if (M < 0 || K < 0 || K % 16 != 0 || !valid_bound(scale_bound)) return 1;
     if (gamax_mode < ORC_GAMAX_NONE || gamax_mode > ORC_GAMAX_ROW_GIVEN) return 1;
-    for (int64_t r = 0; r < M; ++r) {
-        float S_enc = 1.0f, S_dec = 1.0f;
-        if (gamax_mode == ORC_GAMAX_TENSOR || gamax_mode == ORC_GAMAX_TENSOR_GIVEN)
-            orc_global_scales(gamax[0], scale_bound, &S_enc, &S_dec);
-        if (gamax_mode == ORC_GAMAX_ROW || gamax_mode == ORC_GAMAX_ROW_GIVEN)
-            orc_global_scales(gamax[r], scale_bound, &S_enc, &S_dec);
-        for (int64_t c = 0; c < K; ++c) {
-            const uint8_t byte = codes[r * (K / 2) + c / 2];
-            const uint8_t code = (c % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
-            const float d = orc_e4m3_decode(scales[r * (K / 16) + c / 16]);
-            const float v = (orc_e2m1_value(code) * d) * S_dec;
-            if (out_dtype == ORC_BF16) static_cast<uint16_t*>(out)[r * K + c] = orc_f32_to_bf16(v);
-            else static_cast<float*>(out)[r * K + c] = v;
+    parallel_for(M, [&](int64_t r0, int64_t r1) {
+        for (int64_t r = r0; r < r1; ++r) {
+            float S_enc = 1.0f, S_dec = 1.0f;
+            if (gamax_mode == ORC_GAMAX_TENSOR || gamax_mode == ORC_GAMAX_TENSOR_GIVEN)
+                orc_global_scales(gamax[0], scale_bound, &S_enc, &S_dec);
+            if (gamax_mode == ORC_GAMAX_ROW || gamax_mode == ORC_GAMAX_ROW_GIVEN)
+                orc_global_scales(gamax[r], scale_bound, &S_enc, &S_dec);
+            for (int64_t c = 0; c < K; ++c) {
+                const uint8_t byte = codes[r * (K / 2) + c / 2];
+                const uint8_t code = (c % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+                const float d = orc_e4m3_decode(scales[r * (K / 16) + c / 16]);
+                /* the decoded value q * d is exact (a 2-bit grid value times a
+                 * 4-bit E4M3 significand), so (q * d) * S_dec rounds once */
+                const float v = (orc_e2m1_value(code) * d) * S_dec;
+                if (out_dtype == ORC_BF16) static_cast<uint16_t*>(out)[r * K + c] = orc_f32_to_bf16(v);
+                else static_cast<float*>(out)[r * K + c] = v;
+            }
         }
-    }
+    });
     return 0;
 }
 
@@ -498,10 +541,26 @@ int orc_qdq(const void* x, int64_t M, int64_t K, int dtype, int block, int round
 
 /* ---- batch forms of the scalar codecs (loops, for exhaustive checks) -- */
 void orc_e4m3_encode_n(const float* s, int64_t n, uint8_t* out) {
-    for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(s[i]);
+    parallel_for(n, [&](int64_t i0, int64_t i1) {
+        for (int64_t i = i0; i < i1; ++i) out[i] = orc_e4m3_encode(s[i]);
+    });
 }
 void orc_e2m1_encode_rn_n(const float* v, int64_t n, uint8_t* out) {
-    for (int64_t i = 0; i < n; ++i) out[i] = orc_e2m1_encode_rn(v[i]);
+    parallel_for(n, [&](int64_t i0, int64_t i1) {
+        for (int64_t i = i0; i < i1; ++i) out[i] = orc_e2m1_encode_rn(v[i]);
+    });
+}
+/* the same over consecutive fp32 bit patterns first, first + 1, ..., first + n - 1
+ * (an exhaustive sweep needs no input array) */
+void orc_e2m1_encode_rn_bits(uint32_t first, int64_t n, uint8_t* out) {
+    parallel_for(n, [&](int64_t i0, int64_t i1) {
+        for (int64_t i = i0; i < i1; ++i) {
+            const uint32_t u = first + static_cast<uint32_t>(i);
+            float f;
+            std::memcpy(&f, &u, 4);
+            out[i] = orc_e2m1_encode_rn(f);
+        }
+    });
 }
 void orc_e2m1_encode_sr_n(const float* v, const double* u, int64_t n, uint8_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_e2m1_encode_sr(v[i], u[i]);
@@ -512,6 +571,15 @@ void orc_sr_uniform_n(uint64_t seed, uint64_t step, const uint64_t* idx, int64_t
 void orc_f32_to_bf16_n(const float* f, int64_t n, uint16_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_bf16(f[i]);
 }
+
+int orc_set_threads(int n) {
+    const int old = g_threads;
+    if (n <= 0) n = static_cast<int>(std::thread::hardware_concurrency());
+    g_threads = n > 0 ? n : 1;
+    return old;
+}
+
+int orc_get_threads(void) { return g_threads; }
 
 int orc_fp_env_ok(void) {
     volatile float t = 1.0e-38f;   /* below FLT_MIN: a subnormal */

@@ -102,6 +102,15 @@ void orc_e2m1_encode_sr_n(const float* v, const double* u, int64_t n, uint8_t* o
 void orc_sr_uniform_n(uint64_t seed, uint64_t step, const uint64_t* idx, int64_t n, double* out);
 void orc_f32_to_bf16_n(const float* f, int64_t n, uint16_t* out);
 
+/* codes of the consecutive fp32 bit patterns first .. first + n - 1 */
+void orc_e2m1_encode_rn_bits(uint32_t first, int64_t n, uint8_t* out);
+
+/* Worker threads for loops over independent rows, bands, tiles and elements
+ * (n <= 0: one per hardware thread); returns the previous count.  The result
+ * bytes do not depend on it.  Default 1. */
+int orc_set_threads(int n);
+int orc_get_threads(void);
+
 /* 1 when subnormal fp32 arithmetic is honoured (no FTZ/DAZ) on this host */
 int orc_fp_env_ok(void);
 

@@ -149,6 +149,17 @@ def test_product_never_touches_the_oracle():
                 os.path.join(ROOT, "oracle", f)).read()
 
 
+def test_probe_e2m1_rejects(lib):
+    f = lib.nvfp4_probe_e2m1
+    f.argtypes = [ctypes.c_uint32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    assert f(0, -1, A16, None) == 1
+    assert f(0, (1 << 32) + 1, A16, None) == 1
+    assert f(5, 1 << 32, A16, None) == 1                               # runs past 2^32
+    assert f(0, 16, None, None) == 1
+    assert f(0, 16, ctypes.c_void_p(0x10002), None) == 1
+    assert f(0, 0, None, None) == 0
+
+
 def test_scales_to_mma_rejects(lib):
     f = lib.nvfp4_scales_to_mma
     f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]

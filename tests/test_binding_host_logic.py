@@ -1,7 +1,9 @@
 """The binding's argument checks that run before any CUDA call (CPU only):
-a call on device tensors refuses host output tensors and a residual that is
-not on x's device (its kernels would be handed host pointers, or the in-place
-update would land in a staged copy)."""
+a call on device tensors refuses host output tensors, a host gamax it would
+have to write, and a residual that is not on x's device (its kernels would be
+handed host pointers, or the in-place update would land in a staged copy);
+given tensors of the wrong dtype or size are refused before the kernels could
+read or write past them."""
 import pytest
 import torch
 
@@ -17,3 +19,43 @@ def test_device_call_refuses_foreign_residual():
     with pytest.raises(ValueError):
         nv._dev_residual(torch.zeros((4, 16)), torch.device("cuda", 0))
     assert nv._dev_residual(None, torch.device("cuda", 0)) is None
+
+
+DEV = torch.device("cuda", 0)
+
+
+def test_device_call_refuses_a_host_gamax_to_write():
+    for mode in (nv.GAMAX_TENSOR, nv.GAMAX_ROW):
+        with pytest.raises(ValueError):
+            nv._gamax_buffer(mode, torch.zeros(64), 64, DEV, host=False)
+
+
+def test_host_call_checks_a_given_host_gamax():
+    with pytest.raises(ValueError):                     # wrong dtype
+        nv._gamax_buffer(nv.GAMAX_TENSOR, torch.zeros(1, dtype=torch.float64), 64, DEV, host=True)
+    with pytest.raises(ValueError):                     # 'row' needs M floats
+        nv._gamax_buffer(nv.GAMAX_ROW, torch.zeros(8), 64, DEV, host=True)
+    with pytest.raises(ValueError):                     # a written amax needs a tensor
+        nv._gamax_buffer(nv.GAMAX_TENSOR, 3.0, 64, DEV, host=True)
+
+
+def test_host_call_checks_the_residual():
+    nv._host_residual(None, 4, 16)
+    nv._host_residual(torch.zeros(4, 16), 4, 16)
+    with pytest.raises(ValueError):
+        nv._host_residual(torch.zeros(4, 16, dtype=torch.bfloat16), 4, 16)
+    with pytest.raises(ValueError):
+        nv._host_residual(torch.zeros(4, 8), 4, 16)
+
+
+def test_host_call_checks_given_host_outputs():
+    with pytest.raises(ValueError):
+        nv._out_buf((4, 8), torch.uint8, torch.empty((4, 8), dtype=torch.int8), DEV, True, "codes")
+    with pytest.raises(ValueError):
+        nv._out_buf((4, 8), torch.uint8, torch.empty((4, 4), dtype=torch.uint8), DEV, True, "codes")
+
+
+def test_device_checks_reject_wrong_tensors_before_any_cuda_call():
+    t = torch.zeros(4, 16)
+    with pytest.raises(ValueError):                     # not on the call's device
+        nv._check_dev(t, "residual", torch.float32, 64, DEV)

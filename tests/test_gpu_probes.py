@@ -1,6 +1,8 @@
 """Device probes of the conversion instructions and the generator, run through
 the library's own entry points (in-bounds inputs only).
 
+- e2m1, every fp32 value: nvfp4_probe_e2m1 runs the kernels' element encode on
+  all 2^32 bit patterns, compared with the oracle's encoder.
 - e2m1: blocks [6.0, y1..y15] have scale exactly 1.0 (6/6), so the stored code
   of each y is the hardware's e2m1 rounding of y itself.  Every fp32 value with
   0.125 <= |y| <= 6 (all decision boundaries of the grid) is checked against
@@ -59,6 +61,33 @@ def test_e2m1_conversion_exhaustive_window():
         assert np.all(to_np(r["scales"]) == 0x38)
         got = unpack_codes(to_np(r["codes"]))[:, 1:].reshape(-1)[:n]
         assert_same(got, oracle.e2m1_encode_rn(vals), "e2m1 codes")
+
+
+def test_e2m1_conversion_every_fp32_value():
+    """All 2^32 fp32 bit patterns through the device's element encode (the
+    routine every quantize kernel uses) against the oracle's nearest-grid
+    encoder, in chunks of 2^28: signs, zeros, subnormals, every decision
+    boundary, the saturating range (6, inf], infinities and every NaN."""
+    chunk = 1 << 28
+    with oracle.using_threads(0):
+        for first in range(0, 1 << 32, chunk):
+            got = to_np(nv.nvfp4_probe_e2m1(first, chunk))
+            c = oracle.e2m1_encode_rn_bits(first, chunk)
+            want = (c[0::2] | (c[1::2] << 4)).astype(np.uint8)
+            if not np.array_equal(got, want):
+                bad = np.flatnonzero(got != want)[:4]
+                pats = [hex(first + 2 * int(b)) for b in bad]
+                raise AssertionError(f"e2m1 codes differ near patterns {pats}: gpu {got[bad]} oracle {want[bad]}")
+            del got, c, want
+
+
+def test_e2m1_probe_ragged_tail():
+    first = int(np.array([1.1], np.float32).view(np.uint32)[0])
+    for n in (1, 7, 9, 4099):
+        got = to_np(nv.nvfp4_probe_e2m1(first, n))
+        c = np.zeros(n + (n & 1), np.uint8)
+        c[:n] = oracle.e2m1_encode_rn_bits(first, n)
+        assert_same(got, (c[0::2] | (c[1::2] << 4)).astype(np.uint8), f"tail n={n}")
 
 
 def test_e4m3_conversion_near_midpoints():

@@ -40,6 +40,12 @@ MUTATIONS = {
     "columnwise SR keyed on the x^T index": (
         "const int64_t xr = P.transposed ? cols[i] : rows[i];\n                const int64_t xc = P.transposed ? rows[i] : cols[i];\n                const int64_t xK = P.transposed ? P.R : P.C;",
         "const int64_t xr = rows[i];\n                const int64_t xc = cols[i];\n                const int64_t xK = P.C;"),
+    "dequantize associates q * (d * S_dec)": (
+        "const float v = (orc_e2m1_value(code) * d) * S_dec;",
+        "const float v = orc_e2m1_value(code) * (d * S_dec);"),
+    "residual dequant associates q * (d * S_dec)": (
+        "P.dq32[rows[i] * P.C + cols[i]] = (q * d_out) * g.S_dec;",
+        "P.dq32[rows[i] * P.C + cols[i]] = q * (d_out * g.S_dec);"),
     "nibbles swapped": ("if (c % 2 == 0) byte = static_cast<uint8_t>((byte & 0xF0) | code);",
                         "if (c % 2 == 1) byte = static_cast<uint8_t>((byte & 0xF0) | code); else if (0) byte = 0;"),
 }
@@ -57,7 +63,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     (tmp_path / "nvfp4_oracle.h").write_text(open(hdr).read())
     so = tmp_path / "liboracle_mut.so"
     subprocess.run(["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-w",
-                    "-shared", "-fPIC", str(cpp), "-o", str(so)], check=True)
+                    "-pthread", "-shared", "-fPIC", str(cpp), "-o", str(so)], check=True)
     env = dict(os.environ, NVFP4_ORACLE_LIB=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],

@@ -10,7 +10,9 @@ them.
 Not pinned by anything outside the oracle ("parity unpinned"): the exact
 association of the four-over-six error value ((q*d)*A)/(6*bound) away from the
 S_enc = 1 regime, and the S_enc fallback to 1 when the global amax is 0, Inf or
-NaN.  The pages name these steps but print no value that fixes them.
+NaN.  The pages name these steps but print no value that fixes them.  The
+dequantized value with a global scale, (q*d)*S_dec, is pinned: q*d is exact,
+so it is the exact triple product rounded once (checked with rationals).
 """
 import ctypes
 import json
@@ -294,6 +296,107 @@ def test_global_scale_closed_forms():
         assert oracle.global_scales(A, 256.0) == (1.0, 1.0)
     enc, dec = oracle.global_scales(1e-38, 256.0)
     assert enc == np.finfo(np.float32).max and dec > 0
+
+
+def rn_f32(fr):
+    """The fp32 value nearest to the rational fr (ties to even), computed with
+    integers: the plain definition of one correctly rounded fp32 operation."""
+    from fractions import Fraction
+    fr = Fraction(fr)
+    if fr == 0:
+        return f32(0.0)
+    sign = -1 if fr < 0 else 1
+    a = abs(fr)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    q = max(e, -126) - 23                      # quantum of the result's binade
+    m = a / Fraction(2) ** q                   # significand in units of the quantum
+    n = m.numerator // m.denominator
+    rem = m - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return f32(sign * float(Fraction(n) * Fraction(2) ** q))
+
+
+def _frac(v):
+    from fractions import Fraction
+    return Fraction(float(v))
+
+
+def test_global_scales_are_correctly_rounded_divisions():
+    """S_enc = RN(6*bound / A) (clamped to FLT_MAX) and S_dec = RN(1 / S_enc)
+    ("Add NVFP4 four-over-six (row-wise) quantization to the training
+    prototype", Design: S_enc / S_dec among the correctly rounded divisions)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(31)
+    As = np.exp2(rng.uniform(-20, 20, 3000)).astype(np.float32) * rng.uniform(1, 2, 3000).astype(np.float32)
+    for bound in (256.0, 448.0):
+        for A in As:
+            enc, dec = oracle.global_scales(float(A), bound)
+            want = rn_f32(Fraction(int(6 * bound)) / _frac(A))
+            assert enc == want, (A, bound)
+            assert dec == rn_f32(1 / _frac(enc)), (A, bound)
+
+
+def test_dequantize_with_a_global_scale_rounds_the_exact_product_once():
+    """Dequantized value = (q * d) * S_dec ("fp4-train", API dequantize; the
+    four-over-six page's decode scale S_dec): q * d is exact (a two-bit grid
+    significand times a four-bit E4M3 one), so the result is the exact product
+    q * d * S_dec rounded once.  Checked with rationals for every code and every
+    positive scale byte, at global amaxes whose S_dec is not a power of two;
+    the other association q * (d * S_dec) rounds twice and must differ
+    somewhere among these cases."""
+    from fractions import Fraction
+    tab = torch_e4m3_table()
+    codes = np.arange(16, dtype=np.uint8)
+    packed = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)      # 16 codes, one row
+    M, K = 126, 16
+    c = np.tile(packed, (M, 1))
+    s = np.arange(1, 127, dtype=np.uint8).reshape(M, 1)                # every positive scale byte
+    differs = 0
+    for A in (np.float32(1.0), np.float32(3.7), np.float32(1234.5678), np.float32(0.0173)):
+        for bound in (256.0, 448.0):
+            enc, dec = oracle.global_scales(float(A), bound)
+            assert np.float32(dec) != np.exp2(np.round(np.log2(dec)))   # not a power of two
+            got = oracle.dequantize(c, s, M, K, gamax_mode=oracle.GAMAX_TENSOR_GIVEN,
+                                    gamax=np.array([A], np.float32), scale_bound=bound,
+                                    out_dtype=oracle.F32)
+            for i in range(M):
+                d = Fraction(float(tab[int(s[i, 0])]))
+                for j in range(16):
+                    q = Fraction(float(oracle.e2m1_value(codes[j])))
+                    want = rn_f32(q * d * _frac(dec))
+                    if codes[j] == 8:
+                        want = f32(-0.0)              # -0 times a positive scale
+                    assert got[i, j].view(np.uint32) == want.view(np.uint32), (A, bound, i, j)
+                    if rn_f32(q * _frac(rn_f32(d * _frac(dec)))) != want:
+                        differs += 1
+    assert differs > 0
+
+
+def test_ef_residual_with_a_global_scale_uses_the_same_dequantized_value():
+    """Under error feedback with a global scale the residual is y - (q*d)*S_dec,
+    one fp32 subtraction from the once-rounded dequantized value."""
+    from fractions import Fraction
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal((32, 64)) * 3).astype(np.float32)
+    r0 = (rng.standard_normal(x.shape) * 0.05).astype(np.float32)
+    A = np.float32(11.3)
+    res = r0.copy()
+    q = oracle.quantize(x, residual=res, gamax_mode=oracle.GAMAX_TENSOR_GIVEN,
+                        gamax=np.array([A], np.float32), scale_bound=448.0)
+    enc, dec = oracle.global_scales(float(A), 448.0)
+    tab = torch_e4m3_table()
+    y = x + r0
+    for i in range(x.shape[0]):
+        for j in range(x.shape[1]):
+            byte = q["codes"][i, j // 2]
+            code = (byte >> 4) if j % 2 else (byte & 0xF)
+            qv = Fraction(float(oracle.e2m1_value(np.uint8(code))))
+            d = Fraction(float(tab[q["scales"][i, j // 16]]))
+            dq = rn_f32(qv * d * _frac(dec))
+            assert res[i, j].view(np.uint32) == rn_f32(_frac(y[i, j]) - _frac(dq)).view(np.uint32)
 
 
 # ---- stochastic rounding -------------------------------------------------------------------

@@ -31,15 +31,16 @@ def _oracle_fns():
              "mae": oracle.ERR_MAE, "mse": oracle.ERR_MSE}
 
     def quantize_fn(x, row_offset=0, gamax_mode="none", gamax=None, rounding="rtn", block="1x16",
-                    err_mode=None, **kw):
+                    err_mode=None, residual=None, **kw):
         g = None if gamax is None else gamax.numpy()
+        res = None if residual is None else residual.numpy()      # shares memory: updated in place
         r = oracle.quantize(x.numpy(), row_offset=row_offset, gamax_mode=names[gamax_mode], gamax=g,
-                            rounding=names[rounding], block=names[block],
+                            rounding=names[rounding], block=names[block], residual=res,
                             err_mode=names[err_mode] if err_mode else oracle.ERR_NONE, **kw)
         return {k: torch.from_numpy(v) for k, v in r.items() if v is not None}
 
-    def amax_fn(x):
-        return torch.from_numpy(oracle.amax(x.numpy()))
+    def amax_fn(x, residual=None):
+        return torch.from_numpy(oracle.amax(x.numpy(), residual=None if residual is None else residual.numpy()))
     return quantize_fn, amax_fn
 
 
@@ -52,11 +53,19 @@ def _worker(rank, world, port, x, cases, q):
     quantize_fn, amax_fn = _oracle_fns()
     results = []
     for kw in cases:
+        kw = dict(kw)
         r0, r1 = shard_rows(x.shape[0], world, rank)
+        res = None
+        if kw.pop("ef", False):
+            res = torch.from_numpy(_residual(x.shape)[r0:r1].copy())
+            kw["residual"] = res
         out = sharded_quantize(torch.from_numpy(x[r0:r1].copy()), r0, quantize_fn=quantize_fn,
                                amax_fn=amax_fn, **kw)
+        got = {k: v.numpy() for k, v in out.items()}
+        if res is not None:
+            got["residual"] = res.numpy()
         gathered = [None] * world
-        dist.all_gather_object(gathered, {k: v.numpy() for k, v in out.items()})
+        dist.all_gather_object(gathered, got)
         results.append(gathered)
     if rank == 0:
         q.put(results)
@@ -64,7 +73,15 @@ def _worker(rank, world, port, x, cases, q):
     dist.destroy_process_group()
 
 
+def _residual(shape):
+    return (np.random.default_rng(9).standard_normal(shape) * 0.5).astype(np.float32)
+
+
+# "ef": each rank passes its rows of one residual; with a per-tensor scale the
+# exchanged amax is that of x + residual, as the unsharded call takes it
 CASES = [dict(rounding="sr", seed=5, step=2),
+         dict(gamax_mode="tensor", rounding="sr", seed=3, step=4, ef=True),
+         dict(gamax_mode="tensor", rounding="rtn", ef=True),
          dict(gamax_mode="tensor", err_mode="mse", scale_bound=256.0, block="16x16", colwise=True),
          dict(gamax_mode="tensor", rounding="rtn"),
          dict(gamax_mode="row", err_mode="mae", scale_bound=256.0)]
@@ -86,13 +103,18 @@ def test_row_shards_over_gloo_match_unsharded():
         assert p.exitcode == 0
     quantize_fn, _ = _oracle_fns()
     for kw, gathered in zip(CASES, results):
-        okw = {k: v for k, v in kw.items() if k != "gamax_mode"}
-        if kw.get("gamax_mode") == "tensor":      # the unsharded tensor's own amax
-            A = torch.from_numpy(oracle.amax(x))
+        okw = {k: v for k, v in kw.items() if k not in ("gamax_mode", "ef")}
+        res = torch.from_numpy(_residual(x.shape)) if kw.get("ef") else None
+        if res is not None:
+            okw["residual"] = res
+        if kw.get("gamax_mode") == "tensor":      # the unsharded tensor's own amax (of x + residual)
+            A = torch.from_numpy(oracle.amax(x, residual=None if res is None else res.numpy()))
             whole = quantize_fn(torch.from_numpy(x), gamax_mode="tensor_given", gamax=A, **okw)
             assert all(np.array_equal(g["gamax"], A.numpy()) for g in gathered)
         else:
             whole = quantize_fn(torch.from_numpy(x), gamax_mode=kw.get("gamax_mode", "none"), **okw)
+        if res is not None:
+            assert np.array_equal(np.concatenate([g["residual"] for g in gathered]), res.numpy())
         assert np.array_equal(np.concatenate([g["codes"] for g in gathered]), whole["codes"].numpy())
         assert np.array_equal(np.concatenate([g["scales"] for g in gathered]), whole["scales"].numpy())
         if kw.get("colwise"):
