@@ -28,7 +28,8 @@ configuration (c4_rowcol) and plain rowwise + columnwise quantization of W1
 
 N > 1 runs under torchrun: every rank processes its own copy of the sweep
 (independent problems, no collective on the data path; weak scaling).
---impl reference times the CPU oracle on a bounded sample of the same step.
+--impl reference times the CPU oracle, on every host core, on a bounded sample
+of the same step.
 """
 from __future__ import annotations
 
@@ -170,36 +171,56 @@ def c5_inputs():
     return _C5
 
 
-def cpu_baseline(sample_rows=1024, repeats=1):
-    """The oracle as it stands, single-threaded, on a bounded sample of the step:
-    the first `sample_rows` rows of each tensor (16-row aligned), every call."""
+def _oracle_step(oracle, W1, W2, A):
+    """Every call of the step on the oracle; returns the outputs."""
+    r1 = np.zeros(W1.shape, np.float32)
+    r2 = np.zeros(W2.shape, np.float32)
+    out = [oracle.quantize(W1, rounding=oracle.SR, residual=r1, seed=0, step=7),
+           oracle.quantize(W2, block=oracle.BLOCK_16X16, rounding=oracle.SR, residual=r2, seed=0, step=7)]
+    qa = oracle.quantize(A, gamax_mode=oracle.GAMAX_TENSOR, err_mode=oracle.ERR_MAE, scale_bound=256.0)
+    out.append(qa)
+    out.append(oracle.quantize(W1, block=oracle.BLOCK_16X16, gamax_mode=oracle.GAMAX_TENSOR,
+                               err_mode=oracle.ERR_MAE, scale_bound=256.0, colwise=True))
+    out.append(oracle.quantize(W2, block=oracle.BLOCK_16X16, gamax_mode=oracle.GAMAX_TENSOR,
+                               err_mode=oracle.ERR_MAE, scale_bound=256.0, colwise=True))
+    out.append(oracle.quantize(A))
+    out.append(oracle.quantize(W2, rounding=oracle.SR, seed=0, step=7))
+    out.append({"dq": oracle.dequantize(qa["codes"], qa["scales"], *A.shape, gamax_mode=oracle.GAMAX_TENSOR_GIVEN,
+                                        gamax=qa["gamax"], scale_bound=256.0), "r1": r1, "r2": r2})
+    return out
+
+
+def cpu_baseline(sample_rows=2048, threads=(1, 0)):
+    """The oracle as it stands on a bounded sample of the step -- the first
+    `sample_rows` rows of each tensor (16-row aligned), every call -- once per
+    thread count in `threads` (0 = every host core); the runs must give the
+    same bytes.  Returns the all-core figure with the single-thread one beside it."""
     import oracle
     c5 = c5_inputs()
     W1, W2, A = (np.ascontiguousarray(c5.W1[:sample_rows]), np.ascontiguousarray(c5.W2[:sample_rows]),
                  np.ascontiguousarray(c5.A[:sample_rows]))
     plan = step_plan(*W1.shape, *W2.shape, *A.shape)
-    r1 = np.zeros(W1.shape, np.float32)
-    r2 = np.zeros(W2.shape, np.float32)
-    t0 = time.perf_counter()
-    for _ in range(repeats):
-        oracle.quantize(W1, rounding=oracle.SR, residual=r1, seed=0, step=7)
-        oracle.quantize(W2, block=oracle.BLOCK_16X16, rounding=oracle.SR, residual=r2, seed=0, step=7)
-        qa = oracle.quantize(A, gamax_mode=oracle.GAMAX_TENSOR, err_mode=oracle.ERR_MAE, scale_bound=256.0)
-        oracle.quantize(W1, block=oracle.BLOCK_16X16, gamax_mode=oracle.GAMAX_TENSOR,
-                        err_mode=oracle.ERR_MAE, scale_bound=256.0, colwise=True)
-        oracle.quantize(W2, block=oracle.BLOCK_16X16, gamax_mode=oracle.GAMAX_TENSOR,
-                        err_mode=oracle.ERR_MAE, scale_bound=256.0, colwise=True)
-        oracle.quantize(A)
-        oracle.quantize(W2, rounding=oracle.SR, seed=0, step=7)
-        oracle.dequantize(qa["codes"], qa["scales"], *A.shape, gamax_mode=oracle.GAMAX_TENSOR_GIVEN,
-                          gamax=qa["gamax"], scale_bound=256.0)
-    dt = (time.perf_counter() - t0) / repeats
     total_bytes = sum(b for _, _, _, b in plan)
     total_elems = sum(e for _, _, e, _ in plan)
+    runs, ref = {}, None
+    for t in threads:
+        with oracle.using_threads(t) as n:
+            t0 = time.perf_counter()
+            out = _oracle_step(oracle, W1, W2, A)
+            dt = time.perf_counter() - t0
+        flat = [v for d in out for v in d.values() if v is not None]
+        if ref is None:
+            ref = flat
+        elif not all(np.array_equal(a.view(np.uint8), b.view(np.uint8)) for a, b in zip(ref, flat)):
+            raise AssertionError("oracle: thread counts gave different bytes")
+        runs[n] = dt
+    cores = max(runs)
+    dt = runs[cores]
     return {"value": total_bytes / dt / GB, "unit": "GB/s", "gelem_per_s": total_elems / dt / GB,
-            "cores": 1, "kind": "oracle", "seconds_per_sample_step": dt,
-            "sample": f"first {sample_rows} rows of W1, W2 and A (every call of the step), "
-                      f"single-threaded C++ oracle"}
+            "cores": cores, "kind": "oracle", "seconds_per_sample_step": dt,
+            "single_thread_value": total_bytes / runs[min(runs)] / GB,
+            "sample": f"first {sample_rows} rows of W1, W2 and A (every call of the step), C++ oracle on "
+                      f"{cores} threads (single-thread run beside it: bit-identical)"}
 
 
 def run_reference(args, rank, world):
@@ -207,11 +228,11 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     if args.warmup > 0:
-        cpu_baseline(sample_rows=16)
+        cpu_baseline(sample_rows=16, threads=(0,))
     times = []
     res = None
     for _ in range(args.steps):
-        res = cpu_baseline(sample_rows=64)
+        res = cpu_baseline(sample_rows=256, threads=(0,))
         times.append(res["seconds_per_sample_step"])
     val = res["value"]
     line = {"impl": "reference", "metric": "NVFP4 quantize GB/s (Gelem/s alongside); % of HBM roofline",
@@ -220,7 +241,7 @@ def run_reference(args, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "gelem_per_s": round(res["gelem_per_s"], 6),
             "config": {"workload": WORKLOAD, "sample": res["sample"]},
-            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": res["cores"], "kind": "oracle",
                              "sample": res["sample"]},
             "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -591,7 +612,8 @@ def run_gpu(args, rank, world, local_rank):
     if world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline()
         cpu = {"value": round(cb["value"], 4), "unit": "GB/s", "cores": cb["cores"],
-               "kind": "oracle", "sample": cb["sample"]}
+               "kind": "oracle", "sample": cb["sample"],
+               "single_thread_value": round(cb["single_thread_value"], 4)}
     line = {
         "metric": "NVFP4 quantize GB/s (Gelem/s alongside); % of HBM roofline",
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": nsteps,
