@@ -23,22 +23,26 @@ constexpr int kThreads = 256;
 // The block amax of a 1x16 group is its own absmax.
 struct OwnAmax {
     static constexpr bool kSplit = false;
+    static constexpr bool failed = false;
     float v;
     __device__ void post(float b) { v = b; }
     __device__ float get() const { return v; }
 };
 
 // One 1x16 group y of block-row blk: tile_amax.post(the group's absmax) then
-// tile_amax.get() gives its block amax, and its four-over-six error sums go
-// through tile_sums (identities for 1x16 blocks; the 16x16 tile's reductions
-// otherwise).  With a split tile amax (kSplit) the stochastic-rounding draws,
-// which do not depend on the scale, are made between post and get.  Nothing
-// is stored when !live (a group past the tensor's last column block).
-template <int DT, int ERR, int RND, bool EF, bool GS, class TileAmax, class TileSums>
+// tile_amax.get() gives its block amax (after_amax() runs right after it),
+// and its four-over-six error sums go through tile_sums (identities for 1x16
+// blocks; the 16x16 tile's reductions otherwise).  With a split tile amax
+// (kSplit) the stochastic-rounding draws, which do not depend on the scale,
+// are made between post and get.  Nothing is stored when !live (a group past
+// the tensor's last column block).  When the tile amax reports a failed wait
+// the block's scale byte is the E4M3 NaN 0x7F (its bf16 output NaN) and
+// nothing else is written.
+template <int DT, int ERR, int RND, bool EF, bool GS, class TileAmax, class TileSums, class AfterAmax>
 __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool live, float* y,
                                            const GScale& g, float C, const O6Tab* tab,
                                            const float* rt, uint64_t idx_base, int64_t bpr,
-                                           TileAmax& tile_amax, TileSums tile_sums) {
+                                           TileAmax& tile_amax, TileSums tile_sums, AfterAmax after_amax) {
     GScale gb = g;
     if (a.gamax_mode == NVFP4_GAMAX_ROW_GIVEN) {
         gb.A = a.gamax[blk / bpr];
@@ -50,6 +54,7 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool
     uint32_t wd[16];
     if constexpr (EARLY) sr_words16(idx0, a.seed, a.step, wd);
     const float b = tile_amax.get();
+    after_amax();
     uint32_t w0, w1, sf;
     float d, q[16];
     const bool wq = EF || a.dq_bf16;
@@ -67,6 +72,16 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool
         four_over_six16<ERR>(y, b, gb, C, tab, w0, w1, sf, d, tile_sums);
     }
     if (!live) return;
+    if (tile_amax.failed) {
+        if (a.scales) a.scales[blk] = 0x7F;
+        if (a.dq_bf16) {
+            float nan16[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) nan16[i] = __int_as_float(0x7FC00000);
+            store16_bf16(a.dq_bf16, blk * 16, nan16);
+        }
+        return;
+    }
     if (a.codes) reinterpret_cast<uint2*>(a.codes)[blk] = make_uint2(w0, w1);
     if (a.scales) a.scales[blk] = static_cast<uint8_t>(sf);
     if (wq) {
@@ -156,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
         }
         OwnAmax own;
         rows_block<DT, ERR, RND, EF, GS>(a, blk, true, y, g, C, tp, rtab, idx_base, bpr, own,
-                                         [](float&, float&) {});
+                                         [](float&, float&) {}, [] {});
         stage = stage == S - 1 ? 0 : stage + 1;
     }
     cp_async_wait<0>();
@@ -165,43 +180,51 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
 // 16x16 blocks, rowwise output.  One CTA step quantizes a 16-row band x 256
 // columns (16 tiles): warp w holds rows 2w and 2w+1 of the band (lanes 0-15
 // and 16-31), lane l&15 the tile, so a warp's loads and stores run along two
-// rows like the 1x16 walk's.  The tile amax is reduced over the lane pair and
-// then the 8 warps through shared memory; four-over-six's row error sums are
-// combined with the width-16 tree in the same way.  The CTAs walk the steps
-// (band-major) persistently, each thread fetching its group one step ahead
-// (the per-thread copy pipeline of k_rows); the reductions' shared buffers
-// alternate between steps, so one barrier per reduction suffices.
-// The tile amax of k_band16, split in two phases on an mbarrier that all
-// threads arrive on once per step: post() reduces the lane pair and publishes
-// the warp's maximum, then arrives; get() waits for the step's phase (with an
-// iteration limit) and reduces the 8 warps.  The partial maxima alternate
-// between two buffers by step parity: a thread writes a step's buffer only
-// after it arrived for the previous step, which it did after reading the
-// buffer two steps back.
+// rows like the 1x16 walk's.  The CTAs walk the steps (band-major)
+// persistently.  Warp 0 stages each step's band (x, and the residual under
+// error feedback) in shared memory with bulk copies, one per row and tensor,
+// completing on the slot's `full` mbarrier by transaction count, STAGES
+// steps ahead.  The tile amax is reduced over the lane pair and then the 8
+// warps through shared memory on the `amax` mbarrier, which every thread
+// arrives on once per step after reading its group from the slot; so when a
+// step's amax phase completes the slot is free and warp 0 refills it with
+// the step STAGES ahead.  Four-over-six's row error sums are combined
+// with the width-16 tree through shared memory as well.
+//
+// Every wait is bounded.  A thread whose wait runs out raises the CTA's fail
+// flag; every thread reads the flag after each wait, and from then on waits no
+// more and writes the E4M3 NaN byte 0x7F (which no quantization produces) as
+// the scale of each block it still owns, so a timed-out call is visible in its
+// scales and the kernel always ends.  Warp 0 stops issuing copies and, at
+// the end, thread 0 waits (bounded) for the copies still in flight.
+template <int DT, bool EF>
+struct BandStage {
+    static constexpr int XROW = 256 * (DT == NVFP4_BF16 ? 2 : 4);   // x bytes of one band row
+    static constexpr int RROW = EF ? 256 * 4 : 0;                     // residual bytes of one band row
+    static constexpr int BYTES = 16 * (XROW + RROW);
+    // stages: as many as keep two CTAs per SM (bf16 with a residual: 24 KB
+    // a stage), capped at 6
+    static constexpr int STAGES = (96 * 1024) / BYTES < 6 ? (96 * 1024) / BYTES : 6;
+    static constexpr int TOTAL = STAGES * BYTES;
+};
+
 struct BandAmax {
     static constexpr bool kSplit = true;
     float (*red)[8][16];
     uint64_t* bar;
+    volatile int* fail;
     int warp, lane, t;
     uint32_t step;                               // this thread's step count
+    bool failed;
     __device__ void post(float b) {
         b = max_nd(b, __shfl_xor_sync(kFullMask, b, 16));
         if (lane < 16) red[step & 1][warp][t] = b;
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
-                     : "memory");
+        mbar_arrive(bar);
     }
     __device__ float get() {
-        const uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
-        for (int it = 0; it < (1 << 22); ++it) {
-            uint32_t ok;
-            asm volatile(
-                "{\n\t.reg .pred p;\n\t"
-                "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                "selp.u32 %0, 1, 0, p;\n\t}"
-                : "=r"(ok)
-                : "r"(addr), "r"(step & 1u)
-                : "memory");
-            if (ok) break;
+        if (!failed) {
+            if (!mbar_wait(bar, step & 1u)) *fail = 1;
+            if (*fail) failed = true;
         }
         float m = red[step & 1][0][t];
 #pragma unroll
@@ -232,18 +255,23 @@ struct BandCursor {      // CTA-uniform step: (band, 256-column chunk)
 
 template <int DT, int ERR, int RND, bool EF, bool GS>
 __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
-    using St = RowsStage<DT, EF>;
-    extern __shared__ __align__(16) unsigned char smem[];
+    using St = BandStage<DT, EF>;
+    constexpr int S = St::STAGES;
+    extern __shared__ __align__(128) unsigned char smem[];
     __shared__ O6TabOf<ERR> tab;
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
     __shared__ float red[2][8][16];                                   // [step parity][warp][tile]
     __shared__ float esum[ERR != NVFP4_ERR_NONE ? 2 : 1][2][16][16];  // [parity][cand][row][tile]
+    __shared__ __align__(8) uint64_t full[S];
     __shared__ __align__(8) uint64_t amax_bar;
-    if (threadIdx.x == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(
-                         static_cast<uint32_t>(__cvta_generic_to_shared(&amax_bar))),
-                     "r"(static_cast<uint32_t>(blockDim.x)));
-        asm volatile("fence.mbarrier_init.release.cluster;");
+    __shared__ int fail_flag;
+    volatile int& fail = fail_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
+        mbar_init(&amax_bar, blockDim.x);
+        fail = 0;
+        mbar_fence_init();
     }
     __syncthreads();
     if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
@@ -262,56 +290,54 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
         tp = &tab;
     }
     const uint64_t idx_base = static_cast<uint64_t>(a.row_offset) * static_cast<uint64_t>(a.K);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rr = 2 * warp + (lane >> 4);       // row within the band
     const int t = lane & 15;                     // tile within the chunk
-    unsigned char* xs = smem + tid * St::XB;
-    unsigned char* rs = smem + kThreads * St::XB + tid * St::RB;
+    constexpr int EB = DT == NVFP4_BF16 ? 2 : 4;  // bytes of one x element
 
-    auto group = [&](const BandCursor& c, bool& live) {   // this thread's 1x16 block
-        const int64_t cb = c.chunk * 16 + t;
-        live = c.band < nbands && cb < nb;
-        return (c.band * 16 + rr) * nb + cb;
-    };
-    auto issue = [&](const BandCursor& c, int stage) {
-        bool live;
-        const int64_t blk = group(c, live);
-        if (live) {
-            const unsigned char* gx = static_cast<const unsigned char*>(a.x) + blk * St::XB;
-#pragma unroll
-            for (int k = 0; k < St::XB / 16; ++k) cp_async16(xs + stage * St::BYTES + 16 * k, gx + 16 * k);
-            if (EF) {
-                const unsigned char* gr = reinterpret_cast<const unsigned char*>(a.residual) + blk * 64;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) cp_async16(rs + stage * St::BYTES + 16 * k, gr + 16 * k);
-            }
+    // warp 0: stage the band of step c into slot s (lane 0 sets the expected
+    // bytes, lane r < 16 copies row r)
+    auto issue = [&](const BandCursor& c, int s) {
+        const int64_t col0 = c.chunk * 256;
+        const int64_t ncols = a.K - col0 < 256 ? a.K - col0 : 256;
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(16 * ncols * (EB + (EF ? 4 : 0))));
+        __syncwarp();
+        if (lane < 16) {
+            const int64_t e0 = (c.band * 16 + lane) * a.K + col0;
+            unsigned char* xs = smem + s * St::BYTES;
+            bulk_g2s(xs + lane * St::XROW, static_cast<const unsigned char*>(a.x) + e0 * EB,
+                     static_cast<uint32_t>(ncols * EB), &full[s]);
+            if (EF)
+                bulk_g2s(xs + 16 * St::XROW + lane * St::RROW, a.residual + e0, static_cast<uint32_t>(ncols * 4),
+                         &full[s]);
         }
-        cp_async_commit();
     };
 
-    constexpr int S = St::STAGES;
     BandCursor cur, ahead;
     cur.init(blockIdx.x, nch, gridDim.x);
     ahead = cur;
-#pragma unroll
-    for (int k = 0; k < S - 1; ++k) {
-        issue(ahead, k);
-        ahead.advance();
+    int issued = 0;                              // steps warp 0 has staged
+    if (warp == 0) {
+        for (; issued < S && ahead.band < nbands; ++issued, ahead.advance()) issue(ahead, issued);
     }
-    int stage = 0, par = 0;
-    BandAmax tile_amax{red, &amax_bar, warp, lane, t, 0u};
-    for (; cur.band < nbands; cur.advance()) {
-        issue(ahead, stage == 0 ? S - 1 : stage - 1);
-        ahead.advance();
-        cp_async_wait<S - 1>();
-        bool live;
-        const int64_t blk = group(cur, live);
+    BandAmax tile_amax{red, &amax_bar, &fail_flag, warp, lane, t, 0u, false};
+    int par = 0;
+    uint32_t k = 0;                              // step count
+    for (; cur.band < nbands; cur.advance(), ++k) {
+        const int s = static_cast<int>(k % S);
+        const int64_t cb = cur.chunk * 16 + t;
+        const bool live = cb < nb;
+        const int64_t blk = (cur.band * 16 + rr) * nb + cb;
+        if (!tile_amax.failed) {
+            if (!mbar_wait(&full[s], (k / S) & 1u)) fail = 1;
+            if (fail) tile_amax.failed = true;
+        }
         float y[16];
-        if (live) {
-            lds16<DT>(xs + stage * St::BYTES, y);
+        if (live && !tile_amax.failed) {
+            const unsigned char* xs = smem + s * St::BYTES;
+            lds16<DT>(xs + rr * St::XROW + t * 16 * EB, y);
             if (EF) {
                 float r[16];
-                lds16<NVFP4_F32>(rs + stage * St::BYTES, r);
+                lds16<NVFP4_F32>(xs + 16 * St::XROW + rr * St::RROW + t * 64, r);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
             }
@@ -333,11 +359,23 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
                 E4 = tree16_regs(e);
             }
         };
-        rows_block<DT, ERR, RND, EF, GS>(a, blk, live, y, g, C, tp, rtab, idx_base, nb, tile_amax, tile_sums);
-        stage = stage == S - 1 ? 0 : stage + 1;
+        // after the step's amax phase every thread has read slot s: refill it
+        auto refill = [&]() {
+            if (warp == 0 && !fail && ahead.band < nbands) {
+                issue(ahead, s);
+                ahead.advance();
+                ++issued;
+            }
+        };
+        rows_block<DT, ERR, RND, EF, GS>(a, blk, live, y, g, C, tp, rtab, idx_base, nb, tile_amax, tile_sums,
+                                         refill);
         par ^= 1;
     }
-    cp_async_wait<0>();
+    // copies warp 0 issued that no step consumed (only after a failure)
+    if (tid == 0) {
+        for (uint32_t j = k; j < static_cast<uint32_t>(issued); ++j)
+            if (!mbar_wait(&full[j % S], (j / S) & 1u)) break;
+    }
 }
 
 template <class KernelT>
@@ -362,13 +400,14 @@ int launch_persistent(KernelT kernel, int smem, int64_t units_per_cta_step, int6
 // BLK 1x16: k_rows over blocks; 16x16: k_band16 over (band, chunk) steps
 template <int DT, int BLK, int ERR, int RND, bool EF, bool GS>
 int launch_rows(const QuantArgs& a, int64_t nblk, cudaStream_t s) {
-    constexpr int smem = RowsStage<DT, EF>::TOTAL;
     static thread_local int configured_dev = -1, per_sm = 1;
     if (BLK == NVFP4_BLOCK_16X16) {
         const int64_t steps = (a.M / 16) * ((a.K / 16 + 15) / 16);
-        return launch_persistent(k_band16<DT, ERR, RND, EF, GS>, smem, 1, steps, a, s, configured_dev, per_sm);
+        return launch_persistent(k_band16<DT, ERR, RND, EF, GS>, BandStage<DT, EF>::TOTAL, 1, steps, a, s,
+                                 configured_dev, per_sm);
     }
-    return launch_persistent(k_rows<DT, ERR, RND, EF, GS>, smem, kThreads, nblk, a, s, configured_dev, per_sm);
+    return launch_persistent(k_rows<DT, ERR, RND, EF, GS>, RowsStage<DT, EF>::TOTAL, kThreads, nblk, a, s,
+                             configured_dev, per_sm);
 }
 
 template <int DT, int BLK, bool GS>
