@@ -181,55 +181,69 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
 // columns (16 tiles): warp w holds rows 2w and 2w+1 of the band (lanes 0-15
 // and 16-31), lane l&15 the tile, so a warp's loads and stores run along two
 // rows like the 1x16 walk's.  The CTAs walk the steps (band-major)
-// persistently.  Warp 0 stages each step's band (x, and the residual under
-// error feedback) in shared memory with bulk copies, one per row and tensor,
-// completing on the slot's `full` mbarrier by transaction count, STAGES
-// steps ahead.  The tile amax is reduced over the lane pair and then the 8
-// warps through shared memory on the `amax` mbarrier, which every thread
-// arrives on once per step after reading its group from the slot; so when a
-// step's amax phase completes the slot is free and warp 0 refills it with
-// the step STAGES ahead.  Four-over-six's row error sums are combined
-// with the width-16 tree through shared memory as well.
+// persistently; each thread streams its own group of every step through a
+// per-thread ring of BandRing::SLOTS asynchronous-copy slots (no producer, no
+// copy barrier), SLOTS - 1 steps ahead.
 //
-// Every wait is bounded.  A thread whose wait runs out raises the CTA's fail
-// flag; every thread reads the flag after each wait, and from then on waits no
-// more and writes the E4M3 NaN byte 0x7F (which no quantization produces) as
-// the scale of each block it still owns, so a timed-out call is visible in its
-// scales and the kernel always ends.  Warp 0 stops issuing copies and, at
-// the end, thread 0 waits (bounded) for the copies still in flight.
+// The tile amax is software-pipelined one step ahead: while step j is
+// encoded, its tile maxima were published during step j - 1.  Each iteration
+// reads step j + 1's group, reduces its maximum over the lane pair, writes the
+// warp's value to red[(j + 1) % 4] and arrives on amax barrier (j + 1) % 2;
+// then it waits for barrier j % 2 (all warps published step j an iteration
+// ago, so the wait rarely blocks), reduces red[j % 4] over the 8 warps and
+// encodes step j.  Four buffers and two barriers keep a thread that runs
+// ahead from overwriting maxima another thread still reads, and from
+// counting its arrival towards the wrong step.  Under error feedback y = x + r
+// of step j + 1 is written back over its residual slot, so the encode reads
+// it from there.  Four-over-six's row error sums are combined with the
+// width-16 tree through shared memory (one block barrier per step).
+//
+// Every barrier wait is bounded.  A thread whose wait runs out raises the
+// CTA's fail flag; every thread reads the flag after each wait, and from then
+// on waits no more and writes the E4M3 NaN byte 0x7F (which no quantization
+// produces) as the scale of each block it still owns, so a timed-out call is
+// visible in its scales and the kernel always ends.
 template <int DT, bool EF>
-struct BandStage {
-    static constexpr int XROW = 256 * (DT == NVFP4_BF16 ? 2 : 4);   // x bytes of one band row
-    static constexpr int RROW = EF ? 256 * 4 : 0;                     // residual bytes of one band row
-    static constexpr int BYTES = 16 * (XROW + RROW);
-    // stages: as many as keep two CTAs per SM (bf16 with a residual: 24 KB
-    // a stage), capped at 6
-    static constexpr int STAGES = (96 * 1024) / BYTES < 6 ? (96 * 1024) / BYTES : 6;
-    static constexpr int TOTAL = STAGES * BYTES;
+struct BandRing {
+    static constexpr int SLOTS = (EF || DT == NVFP4_F32) ? 3 : 4;
+    static constexpr int XB = DT == NVFP4_BF16 ? 32 : 64;   // x bytes per group
+    static constexpr int RB = EF ? 64 : 0;                    // residual bytes per group
+    static constexpr int BYTES = kThreads * (XB + RB);        // one slot, all threads
+    static constexpr int TOTAL = SLOTS * BYTES;
 };
 
-struct BandAmax {
+struct BandShared {
+    float red[4][8][16];                         // [step % 4][warp][tile]
+    uint64_t bar[2];                             // amax barriers, step % 2
+    int fail;
+};
+
+// The maxima of step j + 1: reduce over the lane pair, publish the warp's
+// value, arrive.
+__device__ __forceinline__ void band_publish(BandShared& sh, float b, uint32_t step, int warp, int lane, int t) {
+    b = max_nd(b, __shfl_xor_sync(kFullMask, b, 16));
+    if (lane < 16) sh.red[step & 3][warp][t] = b;
+    mbar_arrive(&sh.bar[step & 1]);
+}
+
+// rows_block's tile amax for the step being encoded: its maxima were
+// published an iteration earlier, so post() has nothing to do.
+struct LaggedAmax {
     static constexpr bool kSplit = true;
-    float (*red)[8][16];
-    uint64_t* bar;
-    volatile int* fail;
-    int warp, lane, t;
-    uint32_t step;                               // this thread's step count
+    BandShared* sh;
+    int t;
+    uint32_t step;
     bool failed;
-    __device__ void post(float b) {
-        b = max_nd(b, __shfl_xor_sync(kFullMask, b, 16));
-        if (lane < 16) red[step & 1][warp][t] = b;
-        mbar_arrive(bar);
-    }
+    __device__ void post(float) {}
     __device__ float get() {
+        volatile int* fail = &sh->fail;
         if (!failed) {
-            if (!mbar_wait(bar, step & 1u)) *fail = 1;
+            if (!mbar_wait(&sh->bar[step & 1], (step >> 1) & 1u)) *fail = 1;
             if (*fail) failed = true;
         }
-        float m = red[step & 1][0][t];
+        float m = sh->red[step & 3][0][t];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) m = max_nd(m, red[step & 1][w][t]);
-        ++step;
+        for (int w = 1; w < 8; ++w) m = max_nd(m, sh->red[step & 3][w][t]);
         return m;
     }
 };
@@ -255,22 +269,18 @@ struct BandCursor {      // CTA-uniform step: (band, 256-column chunk)
 
 template <int DT, int ERR, int RND, bool EF, bool GS>
 __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
-    using St = BandStage<DT, EF>;
-    constexpr int S = St::STAGES;
-    extern __shared__ __align__(128) unsigned char smem[];
+    using Rg = BandRing<DT, EF>;
+    constexpr int S = Rg::SLOTS;
+    extern __shared__ __align__(16) unsigned char smem[];
     __shared__ O6TabOf<ERR> tab;
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
-    __shared__ float red[2][8][16];                                   // [step parity][warp][tile]
     __shared__ float esum[ERR != NVFP4_ERR_NONE ? 2 : 1][2][16][16];  // [parity][cand][row][tile]
-    __shared__ __align__(8) uint64_t full[S];
-    __shared__ __align__(8) uint64_t amax_bar;
-    __shared__ int fail_flag;
-    volatile int& fail = fail_flag;
+    __shared__ __align__(8) BandShared sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
-        mbar_init(&amax_bar, blockDim.x);
-        fail = 0;
+        mbar_init(&sh.bar[0], blockDim.x);
+        mbar_init(&sh.bar[1], blockDim.x);
+        sh.fail = 0;
         mbar_fence_init();
     }
     __syncthreads();
@@ -292,55 +302,86 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
     const uint64_t idx_base = static_cast<uint64_t>(a.row_offset) * static_cast<uint64_t>(a.K);
     const int rr = 2 * warp + (lane >> 4);       // row within the band
     const int t = lane & 15;                     // tile within the chunk
-    constexpr int EB = DT == NVFP4_BF16 ? 2 : 4;  // bytes of one x element
+    unsigned char* xs = smem + tid * Rg::XB;
+    unsigned char* rs = smem + kThreads * Rg::XB + tid * Rg::RB;
 
-    // warp 0: stage the band of step c into slot s (lane 0 sets the expected
-    // bytes, lane r < 16 copies row r)
-    auto issue = [&](const BandCursor& c, int s) {
-        const int64_t col0 = c.chunk * 256;
-        const int64_t ncols = a.K - col0 < 256 ? a.K - col0 : 256;
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(16 * ncols * (EB + (EF ? 4 : 0))));
-        __syncwarp();
-        if (lane < 16) {
-            const int64_t e0 = (c.band * 16 + lane) * a.K + col0;
-            unsigned char* xs = smem + s * St::BYTES;
-            bulk_g2s(xs + lane * St::XROW, static_cast<const unsigned char*>(a.x) + e0 * EB,
-                     static_cast<uint32_t>(ncols * EB), &full[s]);
-            if (EF)
-                bulk_g2s(xs + 16 * St::XROW + lane * St::RROW, a.residual + e0, static_cast<uint32_t>(ncols * 4),
-                         &full[s]);
-        }
+    auto group = [&](const BandCursor& c, bool& live) {   // this thread's 1x16 block
+        const int64_t cb = c.chunk * 16 + t;
+        live = c.band < nbands && cb < nb;
+        return (c.band * 16 + rr) * nb + cb;
     };
-
-    BandCursor cur, ahead;
-    cur.init(blockIdx.x, nch, gridDim.x);
-    ahead = cur;
-    int issued = 0;                              // steps warp 0 has staged
-    if (warp == 0) {
-        for (; issued < S && ahead.band < nbands; ++issued, ahead.advance()) issue(ahead, issued);
-    }
-    BandAmax tile_amax{red, &amax_bar, &fail_flag, warp, lane, t, 0u, false};
-    int par = 0;
-    uint32_t k = 0;                              // step count
-    for (; cur.band < nbands; cur.advance(), ++k) {
-        const int s = static_cast<int>(k % S);
-        const int64_t cb = cur.chunk * 16 + t;
-        const bool live = cb < nb;
-        const int64_t blk = (cur.band * 16 + rr) * nb + cb;
-        if (!tile_amax.failed) {
-            if (!mbar_wait(&full[s], (k / S) & 1u)) fail = 1;
-            if (fail) tile_amax.failed = true;
+    auto issue = [&](const BandCursor& c, int slot) {
+        bool live;
+        const int64_t blk = group(c, live);
+        if (live) {
+            const unsigned char* gx = static_cast<const unsigned char*>(a.x) + blk * Rg::XB;
+#pragma unroll
+            for (int k = 0; k < Rg::XB / 16; ++k) cp_async16(xs + slot * Rg::BYTES + 16 * k, gx + 16 * k);
+            if (EF) {
+                const unsigned char* gr = reinterpret_cast<const unsigned char*>(a.residual) + blk * 64;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) cp_async16(rs + slot * Rg::BYTES + 16 * k, gr + 16 * k);
+            }
         }
+        cp_async_commit();
+    };
+    // read the group of a step from its slot (zeros when it lies past the
+    // tensor), publish its maxima; under error feedback keep y = x + r in the
+    // residual slot for the encode
+    auto load_publish = [&](const BandCursor& c, int slot, uint32_t step) {
+        bool live;
+        group(c, live);
         float y[16];
-        if (live && !tile_amax.failed) {
-            const unsigned char* xs = smem + s * St::BYTES;
-            lds16<DT>(xs + rr * St::XROW + t * 16 * EB, y);
+        if (live) {
+            lds16<DT>(xs + slot * Rg::BYTES, y);
             if (EF) {
                 float r[16];
-                lds16<NVFP4_F32>(xs + 16 * St::XROW + rr * St::RROW + t * 64, r);
+                lds16<NVFP4_F32>(rs + slot * Rg::BYTES, r);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
+                float4* yp = reinterpret_cast<float4*>(rs + slot * Rg::BYTES);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) yp[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
             }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) y[i] = 0.0f;
+        }
+        band_publish(sh, absmax16(y), step, warp, lane, t);
+    };
+
+    BandCursor cur, nxt, ahead;
+    cur.init(blockIdx.x, nch, gridDim.x);
+    ahead = cur;
+#pragma unroll
+    for (int k = 0; k < S - 1; ++k) {
+        issue(ahead, k);
+        ahead.advance();
+    }
+    if (cur.band < nbands) {
+        cp_async_wait<S - 2>();
+        load_publish(cur, 0, 0u);
+    }
+    nxt = cur;
+    nxt.advance();
+    LaggedAmax tile_amax{&sh, t, 0u, false};
+    int par = 0;
+    uint32_t j = 0;
+    for (; cur.band < nbands; cur.advance(), nxt.advance(), ++j) {
+        const int slot = static_cast<int>(j % S);
+        // the step S - 1 ahead goes to the slot of step j - 1, encoded last iteration
+        issue(ahead, static_cast<int>((j + S - 1) % S));
+        ahead.advance();
+        if (nxt.band < nbands) {                 // CTA-uniform
+            cp_async_wait<S - 2>();
+            load_publish(nxt, static_cast<int>((j + 1) % S), j + 1);
+        }
+        bool live;
+        const int64_t blk = group(cur, live);
+        float y[16];
+        if (live) {
+            if (EF) lds16<NVFP4_F32>(rs + slot * Rg::BYTES, y);
+            else lds16<DT>(xs + slot * Rg::BYTES, y);
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) y[i] = 0.0f;
@@ -359,23 +400,12 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
                 E4 = tree16_regs(e);
             }
         };
-        // after the step's amax phase every thread has read slot s: refill it
-        auto refill = [&]() {
-            if (warp == 0 && !fail && ahead.band < nbands) {
-                issue(ahead, s);
-                ahead.advance();
-                ++issued;
-            }
-        };
+        tile_amax.step = j;
         rows_block<DT, ERR, RND, EF, GS>(a, blk, live, y, g, C, tp, rtab, idx_base, nb, tile_amax, tile_sums,
-                                         refill);
+                                         [] {});
         par ^= 1;
     }
-    // copies warp 0 issued that no step consumed (only after a failure)
-    if (tid == 0) {
-        for (uint32_t j = k; j < static_cast<uint32_t>(issued); ++j)
-            if (!mbar_wait(&full[j % S], (j / S) & 1u)) break;
-    }
+    cp_async_wait<0>();
 }
 
 template <class KernelT>
@@ -403,7 +433,7 @@ int launch_rows(const QuantArgs& a, int64_t nblk, cudaStream_t s) {
     static thread_local int configured_dev = -1, per_sm = 1;
     if (BLK == NVFP4_BLOCK_16X16) {
         const int64_t steps = (a.M / 16) * ((a.K / 16 + 15) / 16);
-        return launch_persistent(k_band16<DT, ERR, RND, EF, GS>, BandStage<DT, EF>::TOTAL, 1, steps, a, s,
+        return launch_persistent(k_band16<DT, ERR, RND, EF, GS>, BandRing<DT, EF>::TOTAL, 1, steps, a, s,
                                  configured_dev, per_sm);
     }
     return launch_persistent(k_rows<DT, ERR, RND, EF, GS>, RowsStage<DT, EF>::TOTAL, kThreads, nblk, a, s,

@@ -316,22 +316,19 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
         float F6[16], F4[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
-        auto candidate = [&](const float* y, float enc, int c, uint32_t& w0, uint32_t& w1, float* e) {
+        const uint64_t ENC6 = pack2(enc6, enc6), ENC4 = pack2(enc4, enc4);
+        // shared-memory byte address of dqt[c][0][tid]; entry k is 512 bytes further
+        const uint32_t tab6 = smem_u32(&dqt[0][0][tid]), tab4 = smem_u32(&dqt[1][0][tid]);
+        auto candidate = [&](const float* y, uint64_t enc2, uint32_t tab, uint32_t& w0, uint32_t& w1, float* e) {
             float v[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = mul_rn(y[i], enc);
+            for (int i = 0; i < 16; i += 2) unpack2(mul2(pack2(y[i], y[i + 1]), enc2), v[i], v[i + 1]);
             w0 = e2m1_encode8(v);
             w1 = e2m1_encode8(v + 8);
-            // byte offset of dqt[c][k][tid] from dqt: k * 512 ORed into
-            // c * 4096 + tid * 4 (whose bits 9-11 are clear)
-            const uint32_t coff = static_cast<uint32_t>(c * 4096 + tid * 4);
-            const unsigned char* dbase = reinterpret_cast<const unsigned char*>(&dqt[0][0][0]);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const uint32_t w = i < 8 ? w0 : w1;
-                const int sh = 4 * (i & 7);
-                const uint32_t k512 = (sh >= 9 ? w >> (sh - 9) : w << (9 - sh)) & 0xE00u;
-                const float dq = *reinterpret_cast<const float*>(dbase + (k512 | coff));
+                const uint32_t k = bfe3(i < 8 ? w0 : w1, 4 * (i & 7));     // grid index of the code
+                const float dq = lds_f32(tab + (k << 9));
                 const float diff = sub_rn(dq, fabsf(y[i]));
                 e[i] = (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff);
             }
@@ -341,13 +338,13 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             next_row(16 + r, y);
             float e[16];
             uint32_t w0, w1;
-            candidate(y, enc6, 0, w0, w1, e);
+            candidate(y, ENC6, tab6, w0, w1, e);
             sW[0][r][tid] = w0;
             sW[1][r][tid] = w1;
             float R6 = seq_sum16(e);
 #pragma unroll
             for (int i = 0; i < 16; ++i) F6[i] = add_rn(F6[i], e[i]);
-            candidate(y, enc4, 1, w0, w1, e);
+            candidate(y, ENC4, tab4, w0, w1, e);
             sW[2][r][tid] = w0;
             sW[3][r][tid] = w1;
             float R4 = seq_sum16(e);
