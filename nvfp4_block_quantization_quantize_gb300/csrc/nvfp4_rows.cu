@@ -183,29 +183,31 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
 // rows like the 1x16 walk's.  The CTAs walk the steps (band-major)
 // persistently; each thread streams its own group of every step through a
 // per-thread ring of BandRing::SLOTS asynchronous-copy slots (no producer, no
-// copy barrier), SLOTS - 1 steps ahead.
+// copy barrier), SLOTS steps ahead of the one it encodes.
 //
 // The tile amax is software-pipelined one step ahead: while step j is
 // encoded, its tile maxima were published during step j - 1.  Each iteration
-// reads step j + 1's group, reduces its maximum over the lane pair, writes the
-// warp's value to red[(j + 1) % 4] and arrives on amax barrier (j + 1) % 2;
-// then it waits for barrier j % 2 (all warps published step j an iteration
-// ago, so the wait rarely blocks), reduces red[j % 4] over the 8 warps and
-// encodes step j.  Four buffers and two barriers keep a thread that runs
-// ahead from overwriting maxima another thread still reads, and from
-// counting its arrival towards the wrong step.  Under error feedback y = x + r
-// of step j + 1 is written back over its residual slot, so the encode reads
-// it from there.  Four-over-six's row error sums are combined with the
-// width-16 tree through shared memory (one block barrier per step).
+// reads step j + 1's group into registers, reduces its maximum over the lane
+// pair, writes the warp's value to red[(j + 1) % 4] and arrives on amax
+// barrier (j + 1) % 2; then it waits for barrier j % 2 (all warps published
+// step j an iteration ago, so the wait rarely blocks), reduces red[j % 4]
+// over the 8 warps and encodes step j.  Four buffers and two barriers keep a
+// thread that runs ahead from overwriting maxima another thread still reads,
+// and from counting its arrival towards the wrong step.  Four-over-six's row
+// error sums are combined with the width-16 tree through shared memory (one
+// block barrier per step).
 //
 // Every barrier wait is bounded.  A thread whose wait runs out raises the
 // CTA's fail flag; every thread reads the flag after each wait, and from then
 // on waits no more and writes the E4M3 NaN byte 0x7F (which no quantization
 // produces) as the scale of each block it still owns, so a timed-out call is
 // visible in its scales and the kernel always ends.
+#ifndef NVFP4_BAND_SLOTS
+#define NVFP4_BAND_SLOTS 2
+#endif
 template <int DT, bool EF>
 struct BandRing {
-    static constexpr int SLOTS = (EF || DT == NVFP4_F32) ? 3 : 4;
+    static constexpr int SLOTS = NVFP4_BAND_SLOTS;
     static constexpr int XB = DT == NVFP4_BF16 ? 32 : 64;   // x bytes per group
     static constexpr int RB = EF ? 64 : 0;                    // residual bytes per group
     static constexpr int BYTES = kThreads * (XB + RB);        // one slot, all threads
@@ -325,13 +327,11 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
         }
         cp_async_commit();
     };
-    // read the group of a step from its slot (zeros when it lies past the
-    // tensor), publish its maxima; under error feedback keep y = x + r in the
-    // residual slot for the encode
-    auto load_publish = [&](const BandCursor& c, int slot, uint32_t step) {
+    // read the group y (x, plus r under error feedback) of a step from its
+    // slot (zeros when it lies past the tensor) and publish its maxima
+    auto load_publish = [&](const BandCursor& c, int slot, uint32_t step, float* y) {
         bool live;
         group(c, live);
-        float y[16];
         if (live) {
             lds16<DT>(xs + slot * Rg::BYTES, y);
             if (EF) {
@@ -339,9 +339,6 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
                 lds16<NVFP4_F32>(rs + slot * Rg::BYTES, r);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
-                float4* yp = reinterpret_cast<float4*>(rs + slot * Rg::BYTES);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) yp[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
             }
         } else {
 #pragma unroll
@@ -350,17 +347,20 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
         band_publish(sh, absmax16(y), step, warp, lane, t);
     };
 
+    // step m is copied into slot m % S; a slot is refilled once its group is
+    // in registers
     BandCursor cur, nxt, ahead;
     cur.init(blockIdx.x, nch, gridDim.x);
     ahead = cur;
 #pragma unroll
-    for (int k = 0; k < S - 1; ++k) {
+    for (int k = 0; k < S; ++k) {
         issue(ahead, k);
         ahead.advance();
     }
+    float ynext[16];
     if (cur.band < nbands) {
-        cp_async_wait<S - 2>();
-        load_publish(cur, 0, 0u);
+        cp_async_wait<S - 1>();
+        load_publish(cur, 0, 0u, ynext);
     }
     nxt = cur;
     nxt.advance();
@@ -368,24 +368,18 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
     int par = 0;
     uint32_t j = 0;
     for (; cur.band < nbands; cur.advance(), nxt.advance(), ++j) {
-        const int slot = static_cast<int>(j % S);
-        // the step S - 1 ahead goes to the slot of step j - 1, encoded last iteration
-        issue(ahead, static_cast<int>((j + S - 1) % S));
+        float y[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = ynext[i];
+        // step j + S goes to the slot of step j, read last iteration
+        issue(ahead, static_cast<int>(j % S));
         ahead.advance();
         if (nxt.band < nbands) {                 // CTA-uniform
-            cp_async_wait<S - 2>();
-            load_publish(nxt, static_cast<int>((j + 1) % S), j + 1);
+            cp_async_wait<S - 1>();
+            load_publish(nxt, static_cast<int>((j + 1) % S), j + 1, ynext);
         }
         bool live;
         const int64_t blk = group(cur, live);
-        float y[16];
-        if (live) {
-            if (EF) lds16<NVFP4_F32>(rs + slot * Rg::BYTES, y);
-            else lds16<DT>(xs + slot * Rg::BYTES, y);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) y[i] = 0.0f;
-        }
         auto tile_sums = [&](float& E6, float& E4) {
             if constexpr (ERR != NVFP4_ERR_NONE) {
                 esum[par][0][rr][t] = E6;

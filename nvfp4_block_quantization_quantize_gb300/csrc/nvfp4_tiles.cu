@@ -186,10 +186,20 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
 // ---------------------------------------------------------------------------------------------
 constexpr int kTileThreads = 128;
 
-// Ring of tile rows per thread: 4 slots of bf16 rows, 3 of fp32 rows (the
-// same bytes in flight; 3 CTAs fit on an SM either way).
+// Ring of tile rows per thread for fp32 input (3 slots of 64-byte rows).
+// bf16 rows (32 bytes) are loaded straight into registers instead, which
+// leaves the shared memory of four CTAs per SM.
 template <int DT>
 struct TileRing {
+    static constexpr int XB = DT == NVFP4_BF16 ? 32 : 64;    // bytes of one tile row
+    static constexpr int SLOTS = DT == NVFP4_BF16 ? 0 : 3;
+    static constexpr int BYTES = SLOTS * kTileThreads * XB;
+};
+
+// Ring of tile rows per thread of k_tile_p: 4 slots of bf16 rows, 3 of fp32
+// rows (the same bytes in flight).
+template <int DT>
+struct TilePRing {
     static constexpr int XB = DT == NVFP4_BF16 ? 32 : 64;    // bytes of one tile row
     static constexpr int SLOTS = DT == NVFP4_BF16 ? 4 : 3;
     static constexpr int BYTES = SLOTS * kTileThreads * XB;
@@ -228,7 +238,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
     __shared__ uint32_t sW[4][16][kTileThreads];
     // ring of tile rows: the thread streams its tile's rows twice (32 row
     // reads) through Rg::SLOTS slots of asynchronous copies
-    __shared__ __align__(16) unsigned char ring[Rg::BYTES];
+    __shared__ __align__(16) unsigned char ring[Rg::BYTES > 0 ? Rg::BYTES : 16];
     __shared__ uint8_t scol[kBands][32];        // columnwise scale byte of each tile
     GScale g{0.0f, 1.0f, 1.0f};
     if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
@@ -254,39 +264,69 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
         const int64_t row_bytes = K * (Rg::XB / 16);
         unsigned char* slot0 = ring + tid * Rg::XB;
 
-        // row read j (0..31) is tile row j % 16, into slot j % Rg::SLOTS
+        // fp32: row read j (0..31) is tile row j % 16, into slot j % Rg::SLOTS
         auto issue = [&](int j) {
-            if (j < 32) {
-                const unsigned char* src = gx + static_cast<int64_t>(j & 15) * row_bytes;
-                unsigned char* dst = slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB);
+            if constexpr (Rg::SLOTS > 0) {
+                if (j < 32) {
+                    const unsigned char* src = gx + static_cast<int64_t>(j & 15) * row_bytes;
+                    unsigned char* dst = slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB);
 #pragma unroll
-                for (int c = 0; c < Rg::XB / 16; ++c) cp_async16(dst + 16 * c, src + 16 * c);
+                    for (int c = 0; c < Rg::XB / 16; ++c) cp_async16(dst + 16 * c, src + 16 * c);
+                }
+                cp_async_commit();
             }
-            cp_async_commit();
         };
+        // bf16: row r's 32 bytes, loaded one row ahead into registers
+        const uint4* grow = reinterpret_cast<const uint4*>(gx);
+        const int64_t row_u4 = row_bytes / 16;
+        uint4 pre0 = make_uint4(0, 0, 0, 0), pre1 = pre0;
         auto next_row = [&](int j, float* y) {       // row read j, ready in y
-            issue(j + Rg::SLOTS - 1);
-            cp_async_wait<Rg::SLOTS - 1>();
-            lds16<DT>(slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB), y);
-        };
+            if constexpr (Rg::SLOTS > 0) {
+                issue(j + Rg::SLOTS - 1);
+                cp_async_wait<Rg::SLOTS - 1>();
+                lds16<DT>(slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB), y);
+            } else {
+                const uint4 u = pre0, v = pre1;
+                if (j + 1 < 32) {
+                    const uint4* p = grow + static_cast<int64_t>((j + 1) & 15) * row_u4;
+                    pre0 = __ldg(p);
+                    pre1 = __ldg(p + 1);
+                }
+                const uint32_t w[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < Rg::SLOTS - 1; ++j) issue(j);
+                for (int i = 0; i < 8; ++i) {
+                    y[2 * i] = __uint_as_float(w[i] << 16);
+                    y[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                }
+            }
+        };
+        if constexpr (Rg::SLOTS > 0) {
+#pragma unroll
+            for (int j = 0; j < Rg::SLOTS - 1; ++j) issue(j);
+        }
 
-        // pass 0: tile amax (bf16: on the packed pairs)
+        // pass 0: tile amax (bf16: on the packed pairs, four rows' loads in flight)
         float y[16];
         float b = 0.0f;
         if constexpr (DT == NVFP4_BF16) {
             uint32_t m2 = 0u;
 #pragma unroll 1
-            for (int r = 0; r < 16; ++r) {
-                issue(r + Rg::SLOTS - 1);
-                cp_async_wait<Rg::SLOTS - 1>();
-                const uint4* p = reinterpret_cast<const uint4*>(slot0 + (r % Rg::SLOTS) * (kTileThreads * Rg::XB));
-                const uint4 u = p[0], v = p[1];
-                m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, u.x), u.y), u.z), u.w);
-                m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, v.x), v.y), v.z), v.w);
+            for (int r = 0; r < 16; r += 4) {
+                uint4 u[4], v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    u[q] = __ldg(grow + static_cast<int64_t>(r + q) * row_u4);
+                    v[q] = __ldg(grow + static_cast<int64_t>(r + q) * row_u4 + 1);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, u[q].x), u[q].y), u[q].z), u[q].w);
+                    m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, v[q].x), v[q].y), v[q].z), v[q].w);
+                }
             }
             b = max_nd(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
+            pre0 = __ldg(grow);                     // row 0 for pass 1 (read 16)
+            pre1 = __ldg(grow + 1);
         } else {
 #pragma unroll 1
             for (int r = 0; r < 16; ++r) {
@@ -358,7 +398,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             sR[0][i8][tid] = R6;
             sR[1][i8][tid] = R4;
         }
-        cp_async_wait<0>();
+        if constexpr (Rg::SLOTS > 0) cp_async_wait<0>();
         float S[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) S[i] = sR[0][i][tid];
@@ -431,7 +471,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
 // columnwise output is staged and written as in k_tile_t.
 template <int DT, int RND, bool GS>
 __global__ void __launch_bounds__(kTileThreads) k_tile_p(const QuantArgs a) {
-    using Rg = TileRing<DT>;
+    using Rg = TilePRing<DT>;
     __shared__ __align__(16) unsigned char ring[Rg::BYTES];
     __shared__ uint2 stg[kBands * 512];          // columnwise words, [stage_index]
     __shared__ uint8_t scol[kBands][32];
