@@ -20,11 +20,13 @@ roofline line is for the kernel with the largest time per step.
 
 Beside the step (not in its value) the line also reports the FP4 GEMM
 consumer (fp4_mm), the fp32 [8192,8192] four-over-six 16x16 MSE row+col
-configuration (c4_rowcol) and plain rowwise + columnwise quantization of W1
-(rowcol_plain).
+configuration (c4_rowcol), plain rowwise + columnwise quantization of W1
+(rowcol_plain) and the other graded variants (variants: SR + error feedback
+on every c5 tensor in both block shapes, c3 four-over-six MAE/MSE with
+per-tensor and per-row amax, the c2 stored-weight step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--mm-only | --c4-only | --rowcol-only [--only VARIANT]]
+                  [--mm-only | --c4-only | --rowcol-only | --variants-only [--only VARIANT]]
 
 N > 1 runs under torchrun: every rank processes its own copy of the sweep
 (independent problems, no collective on the data path; weak scaling).
@@ -66,6 +68,8 @@ def parse():
                    help="only the fp32 [8192,8192] four-over-six 16x16 row+col measurement")
     p.add_argument("--rowcol-only", action="store_true",
                    help="only the plain rowwise + columnwise measurement on W1 (--only picks a variant)")
+    p.add_argument("--variants-only", action="store_true",
+                   help="only the graded variants outside the step (--only picks by name)")
     return p.parse_args()
 
 
@@ -386,6 +390,99 @@ def rowcol_measurement(nv, torch, W1, peaks, iters=10, variants=None):
             "algorithmic_bytes": int(nbytes), "runs": res}
 
 
+def _time_calls(torch, run, iters, warm=3):
+    for _ in range(warm):
+        run(0)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(iters):
+        run(i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def variants_measurement(nv, torch, W1, W2, A, peaks, iters=10, only=None):
+    """Graded variants outside the step, each timed alone with CUDA events
+    (mean of `iters` back-to-back calls; algorithmic bytes as in the step):
+    SR + error feedback on every c5 tensor in both block shapes, and the c3
+    four-over-six 1x16 configuration (bf16 [2048,7168], 72 columns x50, seed
+    2: MAE and MSE, bound 256, per-tensor and per-row amax given) over 8
+    rotating copies (235 MB, larger than L2).  Also the c2 stored-weight step
+    (qdq of a bf16 [1024,1024] weight with an fp32 residual), which is
+    launch-bound and reported in microseconds."""
+    import nvfp4_workloads as wl
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    q = 0.5 + 1 / 16
+    res = []
+
+    def add(name, kernel, nbytes, ms, elems):
+        res.append({"variant": name, "kernel": kernel, "ms": round(ms, 4),
+                    "GB/s": round(nbytes / (ms * 1e-3) / GB, 1),
+                    "frac_of_peak": round(nbytes / (ms * 1e-3) / GB / peak, 3),
+                    "gelem_per_s": round(elems / (ms * 1e-3) / GB, 2)})
+
+    for tname, x in (("W1", W1), ("W2", W2), ("A", A)):
+        M, K = x.shape
+        r = torch.zeros((M, K), dtype=torch.float32, device=x.device)
+        c = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
+        s = torch.empty((M, K // 16), dtype=torch.uint8, device=x.device)
+        for blk in ("1x16", "16x16"):
+            name = f"{tname} SR+EF {blk}"
+            if only and only not in name:
+                continue
+            ms = _time_calls(torch, lambda i: nv.nvfp4_quantize(x, block=blk, rounding="sr", residual=r, seed=0,
+                                                                 step=i, codes=c, scales=s), iters)
+            add(name, f"{'k_rows' if blk == '1x16' else 'k_band16'}<bf16, plain, SR, EF>",
+                M * K * (2 + 4 + 4 + q), ms, M * K)
+        del r, c, s
+    dev = A.device
+    c3 = wl.c3()
+    copies = [torch.from_numpy(c3.view(np.int16)).view(torch.bfloat16).to(dev) for _ in range(8)]
+    M, K = c3.shape
+    amax_t = nv.nvfp4_amax(copies[0])
+    amax_r = nv.nvfp4_amax(copies[0], per_row=True)
+    c = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    s = torch.empty((M, K // 16), dtype=torch.uint8, device=dev)
+    for err in ("mae", "mse"):
+        for gm, g in (("tensor_given", amax_t), ("row_given", amax_r)):
+            name = f"c3 4o6 {err.upper()} 1x16 {'per-tensor' if gm == 'tensor_given' else 'per-row'}"
+            if only and only not in name:
+                continue
+            ms = _time_calls(torch, lambda i: nv.nvfp4_quantize(copies[i % 8], gamax_mode=gm, gamax=g, err_mode=err,
+                                                                 scale_bound=256.0, codes=c, scales=s), 4 * iters)
+            add(name, f"k_rows<bf16, {err.upper()}>", M * K * (2 + q), ms, M * K)
+    del copies
+    if not only or "c2" in only:
+        cfg = wl.C2()
+        Wt = torch.from_numpy(cfg.W0.view(np.int16)).view(torch.bfloat16).to(dev)
+        r = torch.zeros(cfg.shape, dtype=torch.float32, device=dev)
+        o = torch.empty(cfg.shape, dtype=torch.bfloat16, device=dev)
+        ms = _time_calls(torch, lambda i: nv.nvfp4_qdq(Wt, rounding="sr", residual=r, seed=0, step=i, out=o),
+                         20 * iters)
+        n = cfg.shape[0] * cfg.shape[1]
+        add("c2 SR+EF qdq 1024x1024 (one stored-weight step)", "k_rows<bf16, plain, SR, EF, qdq>",
+            n * (2 + 4 + 4 + 2), ms, n)
+        res[-1]["us"] = round(ms * 1e3, 2)
+    return {"note": "each variant alone, mean of back-to-back calls with CUDA events", "runs": res}
+
+
+def run_variants_only(args, local_rank):
+    import torch
+    import nvfp4_block_quantization_quantize_gb300 as nv
+    torch.cuda.set_device(local_rank)
+    nv.build()
+    nv.load_library()
+    dev = torch.device("cuda", local_rank)
+    c5 = c5_inputs()
+    up = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)   # noqa: E731
+    v = variants_measurement(nv, torch, up(c5.W1), up(c5.W2), up(c5.A), measured_peaks(), iters=args.steps,
+                             only=args.only)
+    print(json.dumps({"metric": "NVFP4 quantize GB/s", "value": v["runs"][0]["GB/s"], "unit": "GB/s",
+                      "higher_is_better": True, "variants": v}), flush=True)
+
+
 def run_c4_only(args, local_rank):
     import torch
     import nvfp4_block_quantization_quantize_gb300 as nv
@@ -501,6 +598,9 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
 
     nsteps = args.steps
+    # per-call events come from a separate set of steps: an event recorded
+    # between two kernels keeps the second from starting while the first
+    # finishes (programmatic dependent launch), so the timed steps carry none
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in plan] for _ in range(nsteps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -512,12 +612,15 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     start.record(stream)
     for k in range(nsteps):
-        step(args.warmup + k, evs[k])
+        step(args.warmup + k)
     stop.record(stream)
     torch.cuda.synchronize()
     barrier()
     clocks = clocks_sampler_stop(proc, fh, clk_path, local_rank)
     total_ms = start.elapsed_time(stop)
+    for k in range(nsteps):                     # the per-call breakdown
+        step(args.warmup + nsteps + k, evs[k])
+    torch.cuda.synchronize()
     ran = [not args.only or args.only in name for name, _, _, _ in plan]
     per_call_ms = [statistics.mean(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(nsteps))
                    if ran[i] else 0.0 for i in range(len(plan))]
@@ -603,11 +706,12 @@ def run_gpu(args, rank, world, local_rank):
     calls = [{"call": n, "kernel": k, "ms": round(ms, 4), "GB/s": round(b / (ms * 1e-3) / GB, 1),
               "frac_of_peak": round(b / (ms * 1e-3) / GB / peak, 3)}
              for (n, k, _, b), ms in zip(plan, per_call_ms) if ms > 0]
-    mm = c4 = rc = None
+    mm = c4 = rc = var = None
     if not args.only:
         mm = mm_measurement(nv, torch, o, Ma, Ka, M2, K2, peaks)
         c4 = c4_measurement(nv, torch, dev, peaks)
         rc = rowcol_measurement(nv, torch, W1, peaks)
+        var = variants_measurement(nv, torch, W1, W2, A, peaks)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline()
@@ -629,7 +733,7 @@ def run_gpu(args, rank, world, local_rank):
                    "parallelism": f"{world} independent replica(s), no data-path collective"},
         "gpu_launches": nsteps * sum(1 for name, _, _, _ in plan if not args.only or args.only in name),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "calls": calls,
-        "fp4_mm": mm, "c4_rowcol": c4, "rowcol_plain": rc,
+        "fp4_mm": mm, "c4_rowcol": c4, "rowcol_plain": rc, "variants": var,
     }
     print(json.dumps(line), flush=True)
 
@@ -655,6 +759,10 @@ def main():
     if args.rowcol_only:
         if rank == 0:
             run_rowcol_only(args, local_rank)
+        return
+    if args.variants_only:
+        if rank == 0:
+            run_variants_only(args, local_rank)
         return
     if world > 1:
         import torch

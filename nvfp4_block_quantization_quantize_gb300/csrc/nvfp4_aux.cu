@@ -91,6 +91,7 @@ template <int DT, bool EF>
 __global__ void __launch_bounds__(kThreads) k_amax_tensor(const void* x, const float* res,
                                                           int64_t nvec, float* out) {
     __shared__ float part[kThreads / 32];
+    pdl_wait();
     float m = 0.0f;
     const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x * kAmaxUnroll;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * kAmaxUnroll + threadIdx.x; base < nvec;
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(kThreads) k_amax_tensor(const void* x, const f
         for (int k = 0; k < kAmaxUnroll; ++k)
             if (base + k * kThreads < nvec) m = max_nd(m, v[k].absmax());
     }
+    pdl_trigger();
     m = warp_max(m);
     if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = m;
     __syncthreads();
@@ -118,10 +120,12 @@ template <int DT, bool EF>
 __global__ void __launch_bounds__(kThreads) k_amax_rows(const void* x, const float* res, int64_t M,
                                                         int64_t K, float* out) {
     const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+    pdl_wait();
     if (row >= M) return;
     const int lane = threadIdx.x & 31;
     float m = 0.0f;
     for (int64_t b = lane; b < K / 16; b += 32) m = max_nd(m, block_absmax<DT, EF>(x, res, row * K + b * 16));
+    pdl_trigger();
     m = warp_max(m);
     if (lane == 0) out[row] = m;
 }
@@ -154,6 +158,7 @@ template <int ODT>
 __global__ void __launch_bounds__(kThreads) k_dequant(const DequantArgs a) {
     constexpr int CH = ODT == NVFP4_BF16 ? 2 : 4;          // 16-byte output chunks per block
     __shared__ uint4 wst[kThreads / 32][32 * CH];
+    pdl_wait();
     const int64_t bpr = a.K / 16;
     const int64_t nblk = a.M * bpr;
     float Senc = 1.0f, Sdec = 1.0f;
@@ -208,6 +213,7 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DequantArgs a) {
             __syncwarp();
         }
     }
+    pdl_trigger();
 }
 
 // out[i] = the plain path's division a[i] / b[i] (its exact, stochastic-
@@ -215,6 +221,7 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DequantArgs a) {
 // takes the one-step form the kernels use without a global scale.
 __global__ void __launch_bounds__(kThreads) k_probe_divide(const float* a, const float* b,
                                                            float* out, int64_t n) {
+    pdl_wait();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
         const float y = a[i], D = b[i];
@@ -234,6 +241,7 @@ __global__ void __launch_bounds__(kThreads) k_probe_divide(const float* a, const
 // byte j; for odd n the last high nibble is 0), encoded by the routine every
 // quantize kernel uses.
 __global__ void __launch_bounds__(kThreads) k_probe_e2m1(uint32_t first, int64_t n, uint8_t* out) {
+    pdl_wait();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g * 8 < n; g += stride) {
         float v[8];
@@ -256,6 +264,7 @@ __global__ void __launch_bounds__(kThreads) k_probe_e2m1(uint32_t first, int64_t
 // decode scales themselves.
 __global__ void __launch_bounds__(kThreads) k_global_scales(const float* gamax, int64_t n, float bound,
                                                             float* s_enc, float* s_dec) {
+    pdl_wait();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
         float enc, dec;
@@ -277,6 +286,7 @@ int grid_for(int64_t nblk) {
 __global__ void __launch_bounds__(kThreads) k_scales_mma(const uint8_t* __restrict__ in, int64_t rows,
                                                          int64_t cols, int64_t R, int64_t C4,
                                                          uint32_t* __restrict__ out) {
+    pdl_wait();
     const int64_t n = R * C4;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -318,22 +328,22 @@ int launch_amax(const void* x, int64_t M, int64_t K, int dtype, const float* res
         if (nvec > 0) {
             const int g = grid_for((nvec + kAmaxUnroll - 1) / kAmaxUnroll);
             if (dtype == NVFP4_BF16) {
-                if (ef) k_amax_tensor<NVFP4_BF16, true><<<g, kThreads, 0, s>>>(x, residual, nvec, out);
-                else k_amax_tensor<NVFP4_BF16, false><<<g, kThreads, 0, s>>>(x, residual, nvec, out);
+                if (ef) launch_pdl(k_amax_tensor<NVFP4_BF16, true>, g, kThreads, 0, s, x, residual, nvec, out);
+                else launch_pdl(k_amax_tensor<NVFP4_BF16, false>, g, kThreads, 0, s, x, residual, nvec, out);
             } else {
-                if (ef) k_amax_tensor<NVFP4_F32, true><<<g, kThreads, 0, s>>>(x, residual, nvec, out);
-                else k_amax_tensor<NVFP4_F32, false><<<g, kThreads, 0, s>>>(x, residual, nvec, out);
+                if (ef) launch_pdl(k_amax_tensor<NVFP4_F32, true>, g, kThreads, 0, s, x, residual, nvec, out);
+                else launch_pdl(k_amax_tensor<NVFP4_F32, false>, g, kThreads, 0, s, x, residual, nvec, out);
             }
         }
     } else {
         if (M > 0) {
             const int g = static_cast<int>((M + kThreads / 32 - 1) / (kThreads / 32));
             if (dtype == NVFP4_BF16) {
-                if (ef) k_amax_rows<NVFP4_BF16, true><<<g, kThreads, 0, s>>>(x, residual, M, K, out);
-                else k_amax_rows<NVFP4_BF16, false><<<g, kThreads, 0, s>>>(x, residual, M, K, out);
+                if (ef) launch_pdl(k_amax_rows<NVFP4_BF16, true>, g, kThreads, 0, s, x, residual, M, K, out);
+                else launch_pdl(k_amax_rows<NVFP4_BF16, false>, g, kThreads, 0, s, x, residual, M, K, out);
             } else {
-                if (ef) k_amax_rows<NVFP4_F32, true><<<g, kThreads, 0, s>>>(x, residual, M, K, out);
-                else k_amax_rows<NVFP4_F32, false><<<g, kThreads, 0, s>>>(x, residual, M, K, out);
+                if (ef) launch_pdl(k_amax_rows<NVFP4_F32, true>, g, kThreads, 0, s, x, residual, M, K, out);
+                else launch_pdl(k_amax_rows<NVFP4_F32, false>, g, kThreads, 0, s, x, residual, M, K, out);
             }
         }
     }
@@ -345,28 +355,28 @@ int launch_scales_mma(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* ou
     const int64_t n = R * C4;
     if (n <= 0) return 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    k_scales_mma<<<grid_for(n), kThreads, 0, s>>>(in, rows, cols, R, C4, reinterpret_cast<uint32_t*>(out));
+    launch_pdl(k_scales_mma, grid_for(n), kThreads, 0, s, in, rows, cols, R, C4, reinterpret_cast<uint32_t*>(out));
     return static_cast<int>(cudaGetLastError());
 }
 
 int launch_probe_divide(const float* a, const float* b, float* out, int64_t n, void* stream) {
     if (n <= 0) return 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    k_probe_divide<<<grid_for((n + 15) / 16), kThreads, 0, s>>>(a, b, out, n);
+    launch_pdl(k_probe_divide, grid_for((n + 15) / 16), kThreads, 0, s, a, b, out, n);
     return static_cast<int>(cudaGetLastError());
 }
 
 int launch_probe_e2m1(uint32_t first, int64_t n, uint8_t* out, void* stream) {
     if (n <= 0) return 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    k_probe_e2m1<<<grid_for((n + 7) / 8), kThreads, 0, s>>>(first, n, out);
+    launch_pdl(k_probe_e2m1, grid_for((n + 7) / 8), kThreads, 0, s, first, n, out);
     return static_cast<int>(cudaGetLastError());
 }
 
 int launch_global_scales(const float* gamax, int64_t n, float bound, float* s_enc, float* s_dec, void* stream) {
     if (n <= 0) return 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    k_global_scales<<<grid_for(n), kThreads, 0, s>>>(gamax, n, bound, s_enc, s_dec);
+    launch_pdl(k_global_scales, grid_for(n), kThreads, 0, s, gamax, n, bound, s_enc, s_dec);
     return static_cast<int>(cudaGetLastError());
 }
 
@@ -375,8 +385,8 @@ int launch_dequantize(const DequantArgs& a, void* stream) {
     const int64_t nblk = a.M * (a.K / 16);
     if (nblk == 0) return 0;
     const int g = grid_for((nblk + 3) / 4);   // 4 blocks per thread
-    if (a.out_dtype == NVFP4_BF16) k_dequant<NVFP4_BF16><<<g, kThreads, 0, s>>>(a);
-    else k_dequant<NVFP4_F32><<<g, kThreads, 0, s>>>(a);
+    if (a.out_dtype == NVFP4_BF16) launch_pdl(k_dequant<NVFP4_BF16>, g, kThreads, 0, s, a);
+    else launch_pdl(k_dequant<NVFP4_F32>, g, kThreads, 0, s, a);
     return static_cast<int>(cudaGetLastError());
 }
 

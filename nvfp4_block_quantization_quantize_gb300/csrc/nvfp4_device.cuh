@@ -375,6 +375,34 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// ---- programmatic dependent launch -------------------------------------------------------------
+// Every kernel is launched with programmatic stream serialization allowed
+// (launch_pdl): it may start while the previous kernel in the stream is
+// finishing, so its launch and its input-independent set-up (shared tables
+// that need no input, barrier initialisation) overlap that kernel's last
+// CTAs.  pdl_wait() blocks until the previous kernel has completed and its
+// memory is visible; a kernel calls it before its first global-memory access.
+// pdl_trigger() lets the next kernel launch; a kernel calls it once its CTA
+// has no work left.  Launched without the attribute, both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- bit fields and shared-memory loads ------------------------------------------------------
 // the 3 bits of w at bit pos (a code's grid index when pos is a nibble start)
 __device__ __forceinline__ uint32_t bfe3(uint32_t w, int pos) {

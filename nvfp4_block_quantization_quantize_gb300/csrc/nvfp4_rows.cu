@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
     __shared__ O6TabOf<ERR> tab;
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
     if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
+    pdl_wait();
     const int64_t bpr = a.K / 16;
     const int64_t nblk = a.M * bpr;
     GScale g{0.0f, 1.0f, 1.0f};
@@ -174,78 +175,59 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
                                          [](float&, float&) {}, [] {});
         stage = stage == S - 1 ? 0 : stage + 1;
     }
+    pdl_trigger();
     cp_async_wait<0>();
 }
 
 // 16x16 blocks, rowwise output.  One CTA step quantizes a 16-row band x 256
 // columns (16 tiles): warp w holds rows 2w and 2w+1 of the band (lanes 0-15
 // and 16-31), lane l&15 the tile, so a warp's loads and stores run along two
-// rows like the 1x16 walk's.  The CTAs walk the steps (band-major)
-// persistently; each thread streams its own group of every step through a
-// per-thread ring of BandRing::SLOTS asynchronous-copy slots (no producer, no
-// copy barrier), SLOTS steps ahead of the one it encodes.
+// rows like the 1x16 walk's.  The tile amax is reduced over the lane pair and
+// then the 8 warps through shared memory; four-over-six's row error sums are
+// combined with the width-16 tree in the same way.  The CTAs walk the steps
+// (band-major) persistently, each thread fetching its group one step ahead
+// (the per-thread copy pipeline of k_rows); the reductions' shared buffers
+// alternate between steps, so one barrier per reduction suffices.  (Staging
+// whole bands with bulk copies several steps ahead, and publishing each
+// step's tile maxima one step early, were both measured slower: fewer CTAs
+// fit per SM and the extra shared-memory traffic outweighed the shorter
+// waits.)
 //
-// The tile amax is software-pipelined one step ahead: while step j is
-// encoded, its tile maxima were published during step j - 1.  Each iteration
-// reads step j + 1's group into registers, reduces its maximum over the lane
-// pair, writes the warp's value to red[(j + 1) % 4] and arrives on amax
-// barrier (j + 1) % 2; then it waits for barrier j % 2 (all warps published
-// step j an iteration ago, so the wait rarely blocks), reduces red[j % 4]
-// over the 8 warps and encodes step j.  Four buffers and two barriers keep a
-// thread that runs ahead from overwriting maxima another thread still reads,
-// and from counting its arrival towards the wrong step.  Four-over-six's row
-// error sums are combined with the width-16 tree through shared memory (one
-// block barrier per step).
+// The tile amax of k_band16, split in two phases on an mbarrier that all
+// threads arrive on once per step: post() reduces the lane pair and publishes
+// the warp's maximum, then arrives; get() waits for the step's phase and
+// reduces the 8 warps.  The partial maxima alternate between two buffers by
+// step parity: a thread writes a step's buffer only after it arrived for the
+// previous step, which it did after reading the buffer two steps back.
 //
-// Every barrier wait is bounded.  A thread whose wait runs out raises the
-// CTA's fail flag; every thread reads the flag after each wait, and from then
-// on waits no more and writes the E4M3 NaN byte 0x7F (which no quantization
-// produces) as the scale of each block it still owns, so a timed-out call is
-// visible in its scales and the kernel always ends.
-#ifndef NVFP4_BAND_SLOTS
-#define NVFP4_BAND_SLOTS 2
-#endif
-template <int DT, bool EF>
-struct BandRing {
-    static constexpr int SLOTS = NVFP4_BAND_SLOTS;
-    static constexpr int XB = DT == NVFP4_BF16 ? 32 : 64;   // x bytes per group
-    static constexpr int RB = EF ? 64 : 0;                    // residual bytes per group
-    static constexpr int BYTES = kThreads * (XB + RB);        // one slot, all threads
-    static constexpr int TOTAL = SLOTS * BYTES;
-};
-
-struct BandShared {
-    float red[4][8][16];                         // [step % 4][warp][tile]
-    uint64_t bar[2];                             // amax barriers, step % 2
-    int fail;
-};
-
-// The maxima of step j + 1: reduce over the lane pair, publish the warp's
-// value, arrive.
-__device__ __forceinline__ void band_publish(BandShared& sh, float b, uint32_t step, int warp, int lane, int t) {
-    b = max_nd(b, __shfl_xor_sync(kFullMask, b, 16));
-    if (lane < 16) sh.red[step & 3][warp][t] = b;
-    mbar_arrive(&sh.bar[step & 1]);
-}
-
-// rows_block's tile amax for the step being encoded: its maxima were
-// published an iteration earlier, so post() has nothing to do.
-struct LaggedAmax {
+// The wait is bounded.  A thread whose wait runs out raises the CTA's fail
+// flag; every thread reads the flag after each wait, and from then on waits
+// no more (it still arrives, so the others' waits end) and writes the E4M3
+// NaN byte 0x7F -- which no quantization produces -- as the scale of each
+// block it still owns: a timed-out call is visible in its scales, and the
+// kernel always ends.
+struct BandAmax {
     static constexpr bool kSplit = true;
-    BandShared* sh;
-    int t;
-    uint32_t step;
+    float (*red)[8][16];
+    uint64_t* bar;
+    volatile int* fail;
+    int warp, lane, t;
+    uint32_t step;                               // this thread's step count
     bool failed;
-    __device__ void post(float) {}
+    __device__ void post(float b) {
+        b = max_nd(b, __shfl_xor_sync(kFullMask, b, 16));
+        if (lane < 16) red[step & 1][warp][t] = b;
+        mbar_arrive(bar);
+    }
     __device__ float get() {
-        volatile int* fail = &sh->fail;
         if (!failed) {
-            if (!mbar_wait(&sh->bar[step & 1], (step >> 1) & 1u)) *fail = 1;
+            if (!mbar_wait(bar, step & 1u)) *fail = 1;
             if (*fail) failed = true;
         }
-        float m = sh->red[step & 3][0][t];
+        float m = red[step & 1][0][t];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) m = max_nd(m, sh->red[step & 3][w][t]);
+        for (int w = 1; w < 8; ++w) m = max_nd(m, red[step & 1][w][t]);
+        ++step;
         return m;
     }
 };
@@ -271,22 +253,22 @@ struct BandCursor {      // CTA-uniform step: (band, 256-column chunk)
 
 template <int DT, int ERR, int RND, bool EF, bool GS>
 __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
-    using Rg = BandRing<DT, EF>;
-    constexpr int S = Rg::SLOTS;
+    using St = RowsStage<DT, EF>;
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ O6TabOf<ERR> tab;
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
+    __shared__ float red[2][8][16];                                   // [step parity][warp][tile]
     __shared__ float esum[ERR != NVFP4_ERR_NONE ? 2 : 1][2][16][16];  // [parity][cand][row][tile]
-    __shared__ __align__(8) BandShared sh;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0) {
-        mbar_init(&sh.bar[0], blockDim.x);
-        mbar_init(&sh.bar[1], blockDim.x);
-        sh.fail = 0;
+    __shared__ __align__(8) uint64_t amax_bar;
+    __shared__ int fail_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&amax_bar, blockDim.x);
+        fail_flag = 0;
         mbar_fence_init();
     }
     __syncthreads();
     if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
+    pdl_wait();
     const int64_t nb = a.K / 16;
     const int64_t nch = (nb + 15) / 16;
     const int64_t nbands = a.M / 16;
@@ -302,41 +284,56 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
         tp = &tab;
     }
     const uint64_t idx_base = static_cast<uint64_t>(a.row_offset) * static_cast<uint64_t>(a.K);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rr = 2 * warp + (lane >> 4);       // row within the band
     const int t = lane & 15;                     // tile within the chunk
-    unsigned char* xs = smem + tid * Rg::XB;
-    unsigned char* rs = smem + kThreads * Rg::XB + tid * Rg::RB;
+    unsigned char* xs = smem + tid * St::XB;
+    unsigned char* rs = smem + kThreads * St::XB + tid * St::RB;
 
     auto group = [&](const BandCursor& c, bool& live) {   // this thread's 1x16 block
         const int64_t cb = c.chunk * 16 + t;
         live = c.band < nbands && cb < nb;
         return (c.band * 16 + rr) * nb + cb;
     };
-    auto issue = [&](const BandCursor& c, int slot) {
+    auto issue = [&](const BandCursor& c, int stage) {
         bool live;
         const int64_t blk = group(c, live);
         if (live) {
-            const unsigned char* gx = static_cast<const unsigned char*>(a.x) + blk * Rg::XB;
+            const unsigned char* gx = static_cast<const unsigned char*>(a.x) + blk * St::XB;
 #pragma unroll
-            for (int k = 0; k < Rg::XB / 16; ++k) cp_async16(xs + slot * Rg::BYTES + 16 * k, gx + 16 * k);
+            for (int k = 0; k < St::XB / 16; ++k) cp_async16(xs + stage * St::BYTES + 16 * k, gx + 16 * k);
             if (EF) {
                 const unsigned char* gr = reinterpret_cast<const unsigned char*>(a.residual) + blk * 64;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) cp_async16(rs + slot * Rg::BYTES + 16 * k, gr + 16 * k);
+                for (int k = 0; k < 4; ++k) cp_async16(rs + stage * St::BYTES + 16 * k, gr + 16 * k);
             }
         }
         cp_async_commit();
     };
-    // read the group y (x, plus r under error feedback) of a step from its
-    // slot (zeros when it lies past the tensor) and publish its maxima
-    auto load_publish = [&](const BandCursor& c, int slot, uint32_t step, float* y) {
+
+    constexpr int S = St::STAGES;
+    BandCursor cur, ahead;
+    cur.init(blockIdx.x, nch, gridDim.x);
+    ahead = cur;
+#pragma unroll
+    for (int k = 0; k < S - 1; ++k) {
+        issue(ahead, k);
+        ahead.advance();
+    }
+    int stage = 0, par = 0;
+    BandAmax tile_amax{red, &amax_bar, &fail_flag, warp, lane, t, 0u, false};
+    for (; cur.band < nbands; cur.advance()) {
+        issue(ahead, stage == 0 ? S - 1 : stage - 1);
+        ahead.advance();
+        cp_async_wait<S - 1>();
         bool live;
-        group(c, live);
+        const int64_t blk = group(cur, live);
+        float y[16];
         if (live) {
-            lds16<DT>(xs + slot * Rg::BYTES, y);
+            lds16<DT>(xs + stage * St::BYTES, y);
             if (EF) {
                 float r[16];
-                lds16<NVFP4_F32>(rs + slot * Rg::BYTES, r);
+                lds16<NVFP4_F32>(rs + stage * St::BYTES, r);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
             }
@@ -344,42 +341,6 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) y[i] = 0.0f;
         }
-        band_publish(sh, absmax16(y), step, warp, lane, t);
-    };
-
-    // step m is copied into slot m % S; a slot is refilled once its group is
-    // in registers
-    BandCursor cur, nxt, ahead;
-    cur.init(blockIdx.x, nch, gridDim.x);
-    ahead = cur;
-#pragma unroll
-    for (int k = 0; k < S; ++k) {
-        issue(ahead, k);
-        ahead.advance();
-    }
-    float ynext[16];
-    if (cur.band < nbands) {
-        cp_async_wait<S - 1>();
-        load_publish(cur, 0, 0u, ynext);
-    }
-    nxt = cur;
-    nxt.advance();
-    LaggedAmax tile_amax{&sh, t, 0u, false};
-    int par = 0;
-    uint32_t j = 0;
-    for (; cur.band < nbands; cur.advance(), nxt.advance(), ++j) {
-        float y[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] = ynext[i];
-        // step j + S goes to the slot of step j, read last iteration
-        issue(ahead, static_cast<int>(j % S));
-        ahead.advance();
-        if (nxt.band < nbands) {                 // CTA-uniform
-            cp_async_wait<S - 1>();
-            load_publish(nxt, static_cast<int>((j + 1) % S), j + 1, ynext);
-        }
-        bool live;
-        const int64_t blk = group(cur, live);
         auto tile_sums = [&](float& E6, float& E4) {
             if constexpr (ERR != NVFP4_ERR_NONE) {
                 esum[par][0][rr][t] = E6;
@@ -394,11 +355,12 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
                 E4 = tree16_regs(e);
             }
         };
-        tile_amax.step = j;
         rows_block<DT, ERR, RND, EF, GS>(a, blk, live, y, g, C, tp, rtab, idx_base, nb, tile_amax, tile_sums,
                                          [] {});
+        stage = stage == S - 1 ? 0 : stage + 1;
         par ^= 1;
     }
+    pdl_trigger();
     cp_async_wait<0>();
 }
 
@@ -417,7 +379,7 @@ int launch_persistent(KernelT kernel, int smem, int64_t units_per_cta_step, int6
     const int64_t want = (units + units_per_cta_step - 1) / units_per_cta_step;
     const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
     const int grid = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
-    kernel<<<grid, kThreads, smem, s>>>(a);
+    launch_pdl(kernel, grid, kThreads, smem, s, a);
     return static_cast<int>(cudaGetLastError());
 }
 
@@ -427,7 +389,7 @@ int launch_rows(const QuantArgs& a, int64_t nblk, cudaStream_t s) {
     static thread_local int configured_dev = -1, per_sm = 1;
     if (BLK == NVFP4_BLOCK_16X16) {
         const int64_t steps = (a.M / 16) * ((a.K / 16 + 15) / 16);
-        return launch_persistent(k_band16<DT, ERR, RND, EF, GS>, BandRing<DT, EF>::TOTAL, 1, steps, a, s,
+        return launch_persistent(k_band16<DT, ERR, RND, EF, GS>, RowsStage<DT, EF>::TOTAL, 1, steps, a, s,
                                  configured_dev, per_sm);
     }
     return launch_persistent(k_rows<DT, ERR, RND, EF, GS>, RowsStage<DT, EF>::TOTAL, kThreads, nblk, a, s,

@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
     constexpr int XB = DT == NVFP4_BF16 ? 32 : 64;
     __shared__ __align__(16) unsigned char xb[2][kThreads * XB];
     if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
+    pdl_wait();
     const int64_t chunk = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = 2 * warp + (lane >> 4);
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
             a.scales_col[cj * nbands + band0 + bb] = scs[bb][jj];
         }
     }
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -240,6 +242,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
     // reads) through Rg::SLOTS slots of asynchronous copies
     __shared__ __align__(16) unsigned char ring[Rg::BYTES > 0 ? Rg::BYTES : 16];
     __shared__ uint8_t scol[kBands][32];        // columnwise scale byte of each tile
+    pdl_wait();
     GScale g{0.0f, 1.0f, 1.0f};
     if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
         g.A = a.gamax[0];
@@ -457,6 +460,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             a.scales_col[col * nbands + bnd] = scol[bb][j >> 4];
         }
     }
+    pdl_trigger();
 }
 
 // Plain (map-to-6) 16x16 quantization with rowwise AND columnwise output:
@@ -477,6 +481,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_p(const QuantArgs a) {
     __shared__ uint8_t scol[kBands][32];
     __shared__ float rtab[GS ? 1 : 128];
     if (!GS) fill_recip_table(rtab);
+    pdl_wait();
     GScale g{0.0f, 1.0f, 1.0f};
     if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
         g.A = a.gamax[0];
@@ -595,6 +600,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_p(const QuantArgs a) {
             a.scales_col[col * nbands + bnd] = scol[bb][j >> 4];
         }
     }
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -602,7 +608,7 @@ template <typename KernelT>
 int launch_rowowner(KernelT kernel, const QuantArgs& a, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>((a.M / 16 + kRowBands - 1) / kRowBands),
                     static_cast<unsigned>((a.K / 16 + 15) / 16));
-    kernel<<<grid, kThreads, 0, s>>>(a);
+    launch_pdl(kernel, grid, kThreads, 0, s, a);
     return static_cast<int>(cudaGetLastError());
 }
 
@@ -611,7 +617,7 @@ template <typename KernelT>
 int launch_tile(KernelT kernel, const QuantArgs& a, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>((a.M / 16 + kBands - 1) / kBands),
                     static_cast<unsigned>((a.K / 16 + 31) / 32));
-    kernel<<<grid, kTileThreads, 0, s>>>(a);
+    launch_pdl(kernel, grid, kTileThreads, 0, s, a);
     return static_cast<int>(cudaGetLastError());
 }
 
