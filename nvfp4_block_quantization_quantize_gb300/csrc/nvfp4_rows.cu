@@ -102,12 +102,12 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool
 // bytes (and residual bytes under error feedback) for one grid-stride step.
 // With a residual a block moves 96-128 bytes, so one step ahead at a higher
 // occupancy keeps enough in flight; without, three steps ahead (the stage count is per variant).
-template <int DT, bool EF>
+template <int DT, bool EF, int NT = kThreads>
 struct RowsStage {
     static constexpr int STAGES = EF ? 2 : 4;
     static constexpr int XB = DT == NVFP4_BF16 ? 32 : 64;   // x bytes per block
     static constexpr int RB = EF ? 64 : 0;                    // residual bytes per block
-    static constexpr int BYTES = kThreads * (XB + RB);
+    static constexpr int BYTES = NT * (XB + RB);
     static constexpr int TOTAL = STAGES * BYTES;
 };
 
@@ -179,11 +179,12 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
     cp_async_wait<0>();
 }
 
-// 16x16 blocks, rowwise output.  One CTA step quantizes a 16-row band x 256
-// columns (16 tiles): warp w holds rows 2w and 2w+1 of the band (lanes 0-15
-// and 16-31), lane l&15 the tile, so a warp's loads and stores run along two
-// rows like the 1x16 walk's.  The tile amax is reduced over the lane pair and
-// then the 8 warps through shared memory; four-over-six's row error sums are
+// 16x16 blocks, rowwise output.  One CTA step quantizes a 16-row band x T
+// tiles (BandGeom: T = 16 for 256 threads): warp w holds RPW consecutive rows
+// of the band (2 for 256 threads: lanes 0-15 and 16-31), lane l % T the tile,
+// so a warp's loads and stores run along its rows like the 1x16 walk's.  The
+// tile amax is reduced over the warp's rows with shuffles and then over the
+// warps through shared memory; four-over-six's row error sums are
 // combined with the width-16 tree in the same way.  The CTAs walk the steps
 // (band-major) persistently, each thread fetching its group one step ahead
 // (the per-thread copy pipeline of k_rows); the reductions' shared buffers
@@ -206,17 +207,31 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
 // NaN byte 0x7F -- which no quantization produces -- as the scale of each
 // block it still owns: a timed-out call is visible in its scales, and the
 // kernel always ends.
+// Band geometry for a CTA of NT threads: a step covers 16 rows x T tiles
+// (T = NT / 16); warp w holds rows w*RPW .. w*RPW + RPW - 1 (RPW = 32 / T),
+// lane l row w*RPW + l / T and tile l % T, so a warp's loads run along RPW
+// rows, T * 32 bytes (bf16) each.
+template <int NT>
+struct BandGeom {
+    static constexpr int T = NT / 16;            // tiles per step
+    static constexpr int RPW = 32 / T;           // rows per warp
+    static constexpr int NW = NT / 32;           // warps
+};
+
+template <int NT>
 struct BandAmax {
+    using Gm = BandGeom<NT>;
     static constexpr bool kSplit = true;
-    float (*red)[8][16];
+    float (*red)[Gm::NW][Gm::T];
     uint64_t* bar;
     volatile int* fail;
     int warp, lane, t;
     uint32_t step;                               // this thread's step count
     bool failed;
     __device__ void post(float b) {
-        b = max_nd(b, __shfl_xor_sync(kFullMask, b, 16));
-        if (lane < 16) red[step & 1][warp][t] = b;
+#pragma unroll
+        for (int o = Gm::T; o < 32; o <<= 1) b = max_nd(b, __shfl_xor_sync(kFullMask, b, o));
+        if (lane < Gm::T) red[step & 1][warp][t] = b;
         mbar_arrive(bar);
     }
     __device__ float get() {
@@ -226,7 +241,7 @@ struct BandAmax {
         }
         float m = red[step & 1][0][t];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) m = max_nd(m, red[step & 1][w][t]);
+        for (int w = 1; w < Gm::NW; ++w) m = max_nd(m, red[step & 1][w][t]);
         ++step;
         return m;
     }
@@ -251,14 +266,21 @@ struct BandCursor {      // CTA-uniform step: (band, 256-column chunk)
     }
 };
 
+#ifndef NVFP4_BAND_THREADS
+#define NVFP4_BAND_THREADS 256
+#endif
+constexpr int kBandThreads = NVFP4_BAND_THREADS;
+
 template <int DT, int ERR, int RND, bool EF, bool GS>
-__global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
-    using St = RowsStage<DT, EF>;
+__global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
+    constexpr int NT = kBandThreads;
+    using Gm = BandGeom<NT>;
+    using St = RowsStage<DT, EF, NT>;
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ O6TabOf<ERR> tab;
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
-    __shared__ float red[2][8][16];                                   // [step parity][warp][tile]
-    __shared__ float esum[ERR != NVFP4_ERR_NONE ? 2 : 1][2][16][16];  // [parity][cand][row][tile]
+    __shared__ float red[2][Gm::NW][Gm::T];                           // [step parity][warp][tile]
+    __shared__ float esum[ERR != NVFP4_ERR_NONE ? 2 : 1][2][16][Gm::T];  // [parity][cand][row][tile]
     __shared__ __align__(8) uint64_t amax_bar;
     __shared__ int fail_flag;
     if (threadIdx.x == 0) {
@@ -270,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
     if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
     pdl_wait();
     const int64_t nb = a.K / 16;
-    const int64_t nch = (nb + 15) / 16;
+    const int64_t nch = (nb + Gm::T - 1) / Gm::T;
     const int64_t nbands = a.M / 16;
     GScale g{0.0f, 1.0f, 1.0f};
     if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
@@ -285,13 +307,13 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
     }
     const uint64_t idx_base = static_cast<uint64_t>(a.row_offset) * static_cast<uint64_t>(a.K);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rr = 2 * warp + (lane >> 4);       // row within the band
-    const int t = lane & 15;                     // tile within the chunk
+    const int rr = warp * Gm::RPW + lane / Gm::T;   // row within the band
+    const int t = lane % Gm::T;                  // tile within the chunk
     unsigned char* xs = smem + tid * St::XB;
-    unsigned char* rs = smem + kThreads * St::XB + tid * St::RB;
+    unsigned char* rs = smem + NT * St::XB + tid * St::RB;
 
     auto group = [&](const BandCursor& c, bool& live) {   // this thread's 1x16 block
-        const int64_t cb = c.chunk * 16 + t;
+        const int64_t cb = c.chunk * Gm::T + t;
         live = c.band < nbands && cb < nb;
         return (c.band * 16 + rr) * nb + cb;
     };
@@ -321,7 +343,7 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
         ahead.advance();
     }
     int stage = 0, par = 0;
-    BandAmax tile_amax{red, &amax_bar, &fail_flag, warp, lane, t, 0u, false};
+    BandAmax<NT> tile_amax{red, &amax_bar, &fail_flag, warp, lane, t, 0u, false};
     for (; cur.band < nbands; cur.advance()) {
         issue(ahead, stage == 0 ? S - 1 : stage - 1);
         ahead.advance();
@@ -366,12 +388,12 @@ __global__ void __launch_bounds__(kThreads) k_band16(const QuantArgs a) {
 
 template <class KernelT>
 int launch_persistent(KernelT kernel, int smem, int64_t units_per_cta_step, int64_t units, const QuantArgs& a,
-                      cudaStream_t s, int& configured_dev, int& per_sm) {
+                      cudaStream_t s, int& configured_dev, int& per_sm, int threads = kThreads) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess ||
             per_sm < 1)
             per_sm = 1;
         configured_dev = dev;
@@ -379,7 +401,7 @@ int launch_persistent(KernelT kernel, int smem, int64_t units_per_cta_step, int6
     const int64_t want = (units + units_per_cta_step - 1) / units_per_cta_step;
     const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
     const int grid = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
-    launch_pdl(kernel, grid, kThreads, smem, s, a);
+    launch_pdl(kernel, grid, threads, smem, s, a);
     return static_cast<int>(cudaGetLastError());
 }
 
@@ -388,9 +410,10 @@ template <int DT, int BLK, int ERR, int RND, bool EF, bool GS>
 int launch_rows(const QuantArgs& a, int64_t nblk, cudaStream_t s) {
     static thread_local int configured_dev = -1, per_sm = 1;
     if (BLK == NVFP4_BLOCK_16X16) {
-        const int64_t steps = (a.M / 16) * ((a.K / 16 + 15) / 16);
-        return launch_persistent(k_band16<DT, ERR, RND, EF, GS>, RowsStage<DT, EF>::TOTAL, 1, steps, a, s,
-                                 configured_dev, per_sm);
+        constexpr int T = BandGeom<kBandThreads>::T;
+        const int64_t steps = (a.M / 16) * ((a.K / 16 + T - 1) / T);
+        return launch_persistent(k_band16<DT, ERR, RND, EF, GS>, RowsStage<DT, EF, kBandThreads>::TOTAL, 1, steps,
+                                 a, s, configured_dev, per_sm, kBandThreads);
     }
     return launch_persistent(k_rows<DT, ERR, RND, EF, GS>, RowsStage<DT, EF>::TOTAL, kThreads, nblk, a, s,
                              configured_dev, per_sm);
