@@ -201,13 +201,12 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
 // step parity: a thread writes a step's buffer only after it arrived for the
 // previous step, which it did after reading the buffer two steps back.
 //
-// The wait is bounded.  A warp whose wait runs out raises the CTA's fail
-// flag; every warp reads the flag after each wait, and from then on waits no
-// more (it still arrives, so the others' waits end) and writes the E4M3 NaN
-// byte 0x7F -- which no quantization produces -- as the scale of each block
-// it still owns: a timed-out call is visible in its scales, and the kernel
-// always ends.
-
+// The wait is bounded.  A thread whose wait runs out raises the CTA's fail
+// flag; every thread reads the flag after each wait, and from then on waits
+// no more (it still arrives, so the others' waits end) and writes the E4M3
+// NaN byte 0x7F -- which no quantization produces -- as the scale of each
+// block it still owns: a timed-out call is visible in its scales, and the
+// kernel always ends.
 // Band geometry for a CTA of NT threads: a step covers 16 rows x T tiles
 // (T = NT / 16); warp w holds rows w*RPW .. w*RPW + RPW - 1 (RPW = 32 / T),
 // lane l row w*RPW + l / T and tile l % T, so a warp's loads run along RPW
@@ -229,24 +228,17 @@ struct BandAmax {
     int warp, lane, t;
     uint32_t step;                               // this thread's step count
     bool failed;
-    // one arrival and one wait per warp: lane 0 arrives after the warp's
-    // maxima are written (__syncwarp orders them before it) and waits; the
-    // warp's other lanes read the maxima after a __syncwarp with lane 0
     __device__ void post(float b) {
 #pragma unroll
         for (int o = Gm::T; o < 32; o <<= 1) b = max_nd(b, __shfl_xor_sync(kFullMask, b, o));
         if (lane < Gm::T) red[step & 1][warp][t] = b;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar);
+        mbar_arrive(bar);
     }
     __device__ float get() {
-        int ok = 1;
-        if (lane == 0 && !failed) {
+        if (!failed) {
             if (!mbar_wait(bar, step & 1u)) *fail = 1;
-            ok = *fail == 0;
+            if (*fail) failed = true;
         }
-        ok = __shfl_sync(kFullMask, ok, 0);
-        if (!ok) failed = true;
         float m = red[step & 1][0][t];
 #pragma unroll
         for (int w = 1; w < Gm::NW; ++w) m = max_nd(m, red[step & 1][w][t]);
@@ -292,7 +284,7 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
     __shared__ __align__(8) uint64_t amax_bar;
     __shared__ int fail_flag;
     if (threadIdx.x == 0) {
-        mbar_init(&amax_bar, Gm::NW);            // one arrival per warp and step
+        mbar_init(&amax_bar, blockDim.x);
         fail_flag = 0;
         mbar_fence_init();
     }
