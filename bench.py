@@ -61,7 +61,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--only", default=None,
-                   help="run only the step's calls whose name contains this text (profiling)")
+                   help="time only the step's calls whose name contains this text (profiling); the "
+                        "warm-up steps run every call")
     p.add_argument("--mm-only", action="store_true",
                    help="only the FP4 product measurement (quantize A and W2, then time nvfp4_mm)")
     p.add_argument("--c4-only", action="store_true",
@@ -70,6 +71,8 @@ def parse():
                    help="only the plain rowwise + columnwise measurement on W1 (--only picks a variant)")
     p.add_argument("--variants-only", action="store_true",
                    help="only the graded variants outside the step (--only picks by name)")
+    p.add_argument("--single", default=None, choices=sorted(SINGLE),
+                   help="time one kernel variant the step does not run (profiling)")
     return p.parse_args()
 
 
@@ -511,6 +514,66 @@ def run_variants_only(args, local_rank):
                       "higher_is_better": True, "variants": v}), flush=True)
 
 
+# One call each, for profiling the kernel variants the step does not run
+# (bench.py --single NAME: warm-up calls, then --steps calls, CUDA-event time).
+SINGLE = {
+    "f32 SR+EF 1x16": ("k_rows<f32, plain, SR, EF>", "W2f", dict(rounding="sr", seed=0, ef=True)),
+    "4o6 MAE 1x16 per-row": ("k_rows<bf16, MAE> (per-row scale)", "A", dict(err_mode="mae", gamax_mode="row_given",
+                                                                          scale_bound=256.0, amax="row")),
+    "RTN 16x16": ("k_band16<bf16, plain, RTN>", "A", dict(block="16x16")),
+    "4o6 MAE 16x16 rowwise": ("k_band16<bf16, MAE>", "W2", dict(block="16x16", err_mode="mae",
+                                                                gamax_mode="tensor_given", scale_bound=256.0,
+                                                                amax="tensor")),
+    "RTN_STD 1x16 per-tensor": ("k_rows<bf16, plain, RTN_STD, GS>", "A", dict(rounding="rtn_std",
+                                                                           gamax_mode="tensor_given",
+                                                                           amax="tensor")),
+    "amax per-row": ("k_amax_rows<bf16>", "A", dict(amax_only="row")),
+    "qdq SR+EF 1x16": ("k_rows<bf16, plain, SR, EF, qdq>", "W2", dict(rounding="sr", seed=0, ef=True, qdq=True)),
+}
+
+
+def run_single(args, local_rank):
+    import torch
+    import nvfp4_block_quantization_quantize_gb300 as nv
+    torch.cuda.set_device(local_rank)
+    nv.build()
+    nv.load_library()
+    dev = torch.device("cuda", local_rank)
+    kern, tname, kw = SINGLE[args.single]
+    kw = dict(kw)
+    c5 = c5_inputs()
+    src = c5.W2 if tname in ("W2", "W2f") else getattr(c5, tname)
+    x = torch.from_numpy(src.view(np.int16)).view(torch.bfloat16).to(dev)
+    if tname == "W2f":
+        x = x.float()
+    M, K = x.shape
+    amax = kw.pop("amax", None)
+    if amax:
+        kw["gamax"] = nv.nvfp4_amax(x, per_row=amax == "row")
+    ef, qdq, amax_only = kw.pop("ef", False), kw.pop("qdq", False), kw.pop("amax_only", None)
+    r = torch.zeros((M, K), dtype=torch.float32, device=dev) if ef else None
+    c = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    s = torch.empty((M, K // 16), dtype=torch.uint8, device=dev)
+    o = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    g = torch.empty((M,), dtype=torch.float32, device=dev)
+    q = 0.5 + 1 / 16
+    eb = x.element_size()
+    if amax_only:
+        run = lambda i: nv.nvfp4_amax(x, per_row=True, out=g)   # noqa: E731
+        nbytes = M * K * eb
+    elif qdq:
+        run = lambda i: nv.nvfp4_qdq(x, residual=r, step=i, out=o, **kw)   # noqa: E731
+        nbytes = M * K * (eb + 4 + 4 + 2)
+    else:
+        run = lambda i: nv.nvfp4_quantize(x, residual=r, step=i, codes=c, scales=s, **kw)   # noqa: E731
+        nbytes = M * K * (eb + (8 if ef else 0) + q)
+    ms = _time_calls(torch, run, args.steps, warm=args.warmup)
+    peak = (measured_peaks() or {}).get("hbm_gbs", 6800.0)
+    print(json.dumps({"single": args.single, "kernel": kern, "tensor": tname, "ms": round(ms, 4),
+                      "GB/s": round(nbytes / (ms * 1e-3) / GB, 1),
+                      "frac_of_peak": round(nbytes / (ms * 1e-3) / GB / peak, 3)}), flush=True)
+
+
 def run_c4_only(args, local_rank):
     import torch
     import nvfp4_block_quantization_quantize_gb300 as nv
@@ -579,7 +642,7 @@ def run_gpu(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     o = out
 
-    def step(t, ev=None):
+    def step(t, ev=None, only=args.only):
         calls = [
             lambda: nv.nvfp4_quantize(W1, rounding="sr", residual=R1, seed=0, step=t,
                                       codes=o["c1"], scales=o["s1"]),
@@ -605,7 +668,7 @@ def run_gpu(args, rank, world, local_rank):
                                         gamax=o["ga"], scale_bound=256.0, out=o["da"]),
         ]
         for i, c in enumerate(calls):
-            if args.only and args.only not in plan[i][0]:
+            if only and only not in plan[i][0]:
                 continue
             if ev is not None:
                 ev[i][0].record(stream)
@@ -621,8 +684,8 @@ def run_gpu(args, rank, world, local_rank):
         if dist is not None:
             dist.barrier()
 
-    for t in range(args.warmup):
-        step(t)
+    for t in range(args.warmup):             # every call, so the amaxes a selected call reads exist
+        step(t, only=None)
     torch.cuda.synchronize()
 
     nsteps = args.steps
@@ -791,6 +854,10 @@ def main():
     if args.variants_only:
         if rank == 0:
             run_variants_only(args, local_rank)
+        return
+    if args.single:
+        if rank == 0:
+            run_single(args, local_rank)
         return
     if world > 1:
         import torch

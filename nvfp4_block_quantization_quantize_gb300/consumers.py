@@ -1,5 +1,5 @@
 """Consumers of the quantizer's outputs: torch FP4 / FP8 views in the layout
-block-scaled tensor cores read, and the matrix multiply on them.
+block-scaled tensor cores read, the matrix multiply on them, and fp4_linear.
 
 "fp4-train" (API: to_fp4_operands, fp4_mm) hands quantized operands to the
 native NVFP4 tensor-core matmul; here the codes are viewed as
@@ -13,7 +13,8 @@ from __future__ import annotations
 
 import torch
 
-from . import nvfp4_global_scales, nvfp4_scales_to_mma
+from . import (nvfp4_dequantize, nvfp4_global_scales, nvfp4_mm, nvfp4_quantize,
+               nvfp4_scales_to_mma)
 
 
 def to_fp4_operands(q: dict) -> dict:
@@ -41,3 +42,63 @@ def fp4_mm(a: dict, b: dict, *, out_dtype=torch.bfloat16, scale_bound: float = 4
     y = torch._scaled_mm(a["fp4"], b["fp4"].t(), a["scales"], b["scales"], out_dtype=torch.float32)
     s = _scale_dec(a.get("scale_dec"), scale_bound) * _scale_dec(b.get("scale_dec"), scale_bound)
     return (y * s).to(out_dtype)
+
+
+# ---- fp4_linear -------------------------------------------------------------------------------
+def _pad_rows(t: torch.Tensor, mult: int) -> torch.Tensor:
+    pad = (-t.shape[0]) % mult
+    if pad == 0:
+        return t.contiguous()
+    return torch.cat([t, t.new_zeros((pad, t.shape[1]))]).contiguous()
+
+
+def _quantize_operand(t: torch.Tensor, stochastic: bool, seed: int, step: int) -> dict:
+    """1x16 rowwise quantization of a [rows, K] operand (rows padded to 128
+    with zeros, which quantize to zero codes and add nothing to a product),
+    its scales re-laid for the tensor cores, and its dequantized value."""
+    rows = t.shape[0]
+    tp = _pad_rows(t, 128)
+    q = nvfp4_quantize(tp, rounding="sr" if stochastic else "rtn", seed=seed, step=step)
+    deq = nvfp4_dequantize(q["codes"], q["scales"], tp.shape[0], tp.shape[1], out_dtype="f32")[:rows]
+    return {"codes": q["codes"], "scales_mma": nvfp4_scales_to_mma(q["scales"]), "rows": tp.shape[0], "deq": deq}
+
+
+class _FP4Linear(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, weight, stochastic, seed, step):
+        M, K = x.shape
+        N = weight.shape[0]
+        qx = _quantize_operand(x, stochastic, seed, step)
+        qw = _quantize_operand(weight, stochastic, seed + 1, step)
+        y = nvfp4_mm(qx["codes"], qx["scales_mma"], qw["codes"], qw["scales_mma"], qx["rows"], qw["rows"], K,
+                     out_dtype="f32")[:M, :N]
+        ctx.save_for_backward(qx["deq"], qw["deq"])
+        ctx.dtypes = (x.dtype, weight.dtype)
+        return y.to(x.dtype)
+
+    @staticmethod
+    def backward(ctx, gy):
+        dx_q, dw_q = ctx.saved_tensors
+        g = gy.float()
+        gx = (g @ dw_q).to(ctx.dtypes[0]) if ctx.needs_input_grad[0] else None
+        gw = (g.t() @ dx_q).to(ctx.dtypes[1]) if ctx.needs_input_grad[1] else None
+        return gx, gw, None, None, None
+
+
+def fp4_linear(x: torch.Tensor, weight: torch.Tensor, stochastic: bool = False, seed: int = 0,
+               step: int = 0) -> torch.Tensor:
+    """y = Q(x) Q(weight)^T ("fp4-train", API: fp4_linear, a quantized-operand
+    linear with a straight-through gradient).
+
+    Both operands are quantized rowwise in 1x16 blocks (the page's recipe: no
+    global scale; round-to-nearest, or stochastic rounding keyed on (seed,
+    step) for x and (seed + 1, step) for the weight) and multiplied on the
+    block-scaled FP4 tensor cores (nvfp4_mm, fp32 accumulation).  The
+    backward pass treats quantization as the identity: dL/dx = dL/dy Q(w)
+    and dL/dw = dL/dy^T Q(x), with the dequantized operands.
+    x [M, K], weight [N, K]: CUDA float32 / bfloat16, K a multiple of 64."""
+    if x.dim() != 2 or weight.dim() != 2 or x.shape[1] != weight.shape[1]:
+        raise ValueError("fp4_linear: x [M, K] and weight [N, K]")
+    if x.shape[1] % 64:
+        raise ValueError("fp4_linear: K must be a multiple of 64")
+    return _FP4Linear.apply(x, weight, stochastic, seed, step)

@@ -87,12 +87,16 @@ struct AmaxVec {
 // floats orders like their bit patterns, so an unsigned atomic max is exact.
 constexpr int kAmaxUnroll = 4;
 
+// bf16 without a residual keeps its running maximum as a packed pair of bf16
+// magnitudes (absmax_bf16x2: exact, NaN-dropping) and widens it once at the end.
 template <int DT, bool EF>
 __global__ void __launch_bounds__(kThreads) k_amax_tensor(const void* x, const float* res,
                                                           int64_t nvec, float* out) {
     __shared__ float part[kThreads / 32];
+    constexpr bool PACKED = DT == NVFP4_BF16 && !EF;
     pdl_wait();
     float m = 0.0f;
+    uint32_t m2 = 0u;
     const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x * kAmaxUnroll;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * kAmaxUnroll + threadIdx.x; base < nvec;
          base += step) {
@@ -101,9 +105,18 @@ __global__ void __launch_bounds__(kThreads) k_amax_tensor(const void* x, const f
         for (int k = 0; k < kAmaxUnroll; ++k)
             if (base + k * kThreads < nvec) v[k].load(x, res, base + k * kThreads);
 #pragma unroll
-        for (int k = 0; k < kAmaxUnroll; ++k)
-            if (base + k * kThreads < nvec) m = max_nd(m, v[k].absmax());
+        for (int k = 0; k < kAmaxUnroll; ++k) {
+            if (base + k * kThreads < nvec) {
+                if constexpr (PACKED) {
+                    m2 = absmax_bf16x2(absmax_bf16x2(m2, v[k].x[0].x), v[k].x[0].y);
+                    m2 = absmax_bf16x2(absmax_bf16x2(m2, v[k].x[0].z), v[k].x[0].w);
+                } else {
+                    m = max_nd(m, v[k].absmax());
+                }
+            }
+        }
     }
+    if constexpr (PACKED) m = max_nd(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
     pdl_trigger();
     m = warp_max(m);
     if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = m;

@@ -106,3 +106,41 @@ def test_mm_rejects_bad_shapes():
         nv.nvfp4_mm(z, z, z, z, 100, 128, 64)
     with pytest.raises(nv.NVFP4Error):
         nv.nvfp4_mm(z, z, z, z, 128, 128, 48)
+
+
+@pytest.mark.parametrize("stochastic", [False, True])
+def test_fp4_linear_forward_and_straight_through_backward(stochastic):
+    """fp4_linear's output is the product of the two operands' quantizations
+    (each the oracle's, rows padded to the tensor cores' 128 with zeros),
+    within the fp32 accumulation bound; its gradients are the straight-through
+    ones, dL/dx = g Q(w) and dL/dw = g^T Q(x)."""
+    from nvfp4_block_quantization_quantize_gb300.consumers import fp4_linear
+    M, N, K = 200, 136, 512                       # neither multiple of 128: padded
+    x = W.matrix((M, K), seed=131, dtype="bf16", dist="t")
+    w = W.matrix((N, K), seed=137, dtype="bf16")
+    xd, wd = to_dev(x).requires_grad_(True), to_dev(w).requires_grad_(True)
+    y = fp4_linear(xd, wd, stochastic=stochastic, seed=5, step=3)
+    rnd = oracle.SR if stochastic else oracle.RTN
+    ox = oracle.quantize(x, rounding=rnd, seed=5, step=3)
+    ow = oracle.quantize(w, rounding=rnd, seed=6, step=3)
+    dx = oracle.dequantize(ox["codes"], ox["scales"], M, K, out_dtype=oracle.F32).astype(np.float64)
+    dw = oracle.dequantize(ow["codes"], ow["scales"], N, K, out_dtype=oracle.F32).astype(np.float64)
+    ref = dx @ dw.T
+    got = to_np(y.float()).astype(np.float64)
+    bound = (np.abs(dx) @ np.abs(dw).T) * K * 2.0 ** -23 + np.abs(ref) * 2.0 ** -8   # bf16 output
+    assert (np.abs(got - ref) <= bound + 1e-30).all()
+    g = torch.from_numpy(np.random.default_rng(7).standard_normal((M, N)).astype(np.float32)).cuda()
+    y.backward(g.to(y.dtype))
+    gx_ref = g.double().cpu().numpy() @ dw
+    gw_ref = g.double().cpu().numpy().T @ dx
+    gx = xd.grad.float().cpu().numpy().astype(np.float64)
+    gw = wd.grad.float().cpu().numpy().astype(np.float64)
+    gy = np.abs(to_np(g.to(y.dtype).float()).astype(np.float64))
+    assert (np.abs(gx - gx_ref) <= (gy @ np.abs(dw)) * (N * 2.0 ** -20 + 2.0 ** -7) + 1e-30).all()
+    assert (np.abs(gw - gw_ref) <= (gy.T @ np.abs(dx)) * (M * 2.0 ** -20 + 2.0 ** -7) + 1e-30).all()
+
+
+def test_fp4_linear_rejects_bad_shapes():
+    from nvfp4_block_quantization_quantize_gb300.consumers import fp4_linear
+    with pytest.raises(ValueError):
+        fp4_linear(torch.zeros(128, 48, device="cuda"), torch.zeros(128, 48, device="cuda"))
