@@ -194,19 +194,6 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
 // fit per SM and the extra shared-memory traffic outweighed the shorter
 // waits.)
 //
-// The tile amax of k_band16, split in two phases on an mbarrier that all
-// threads arrive on once per step: post() reduces the lane pair and publishes
-// the warp's maximum, then arrives; get() waits for the step's phase and
-// reduces the 8 warps.  The partial maxima alternate between two buffers by
-// step parity: a thread writes a step's buffer only after it arrived for the
-// previous step, which it did after reading the buffer two steps back.
-//
-// The wait is bounded.  A thread whose wait runs out raises the CTA's fail
-// flag; every thread reads the flag after each wait, and from then on waits
-// no more (it still arrives, so the others' waits end) and writes the E4M3
-// NaN byte 0x7F -- which no quantization produces -- as the scale of each
-// block it still owns: a timed-out call is visible in its scales, and the
-// kernel always ends.
 // Band geometry for a CTA of NT threads: a step covers 16 rows x T tiles
 // (T = NT / 16); warp w holds rows w*RPW .. w*RPW + RPW - 1 (RPW = 32 / T),
 // lane l row w*RPW + l / T and tile l % T, so a warp's loads run along RPW
@@ -218,27 +205,29 @@ struct BandGeom {
     static constexpr int NW = NT / 32;           // warps
 };
 
+// The tile amax of k_band16: post() reduces the group maxima over the warp's
+// rows with shuffles and publishes the warp's value; get() passes the CTA
+// barrier (a hardware barrier: waiting warps issue nothing) and reduces over
+// the warps.  The stochastic-rounding draws are made between the two.  The
+// partial maxima alternate between two buffers by step parity: a thread
+// writes a step's buffer only after it passed the previous step's barrier,
+// which every thread reaches after reading the buffer two steps back.  Every
+// thread runs the same CTA-uniform steps, so every barrier completes.
 template <int NT>
 struct BandAmax {
     using Gm = BandGeom<NT>;
     static constexpr bool kSplit = true;
+    static constexpr bool failed = false;
     float (*red)[Gm::NW][Gm::T];
-    uint64_t* bar;
-    volatile int* fail;
     int warp, lane, t;
     uint32_t step;                               // this thread's step count
-    bool failed;
     __device__ void post(float b) {
 #pragma unroll
         for (int o = Gm::T; o < 32; o <<= 1) b = max_nd(b, __shfl_xor_sync(kFullMask, b, o));
         if (lane < Gm::T) red[step & 1][warp][t] = b;
-        mbar_arrive(bar);
     }
     __device__ float get() {
-        if (!failed) {
-            if (!mbar_wait(bar, step & 1u)) *fail = 1;
-            if (*fail) failed = true;
-        }
+        __syncthreads();
         float m = red[step & 1][0][t];
 #pragma unroll
         for (int w = 1; w < Gm::NW; ++w) m = max_nd(m, red[step & 1][w][t]);
@@ -281,14 +270,6 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
     __shared__ float red[2][Gm::NW][Gm::T];                           // [step parity][warp][tile]
     __shared__ float esum[ERR != NVFP4_ERR_NONE ? 2 : 1][2][16][Gm::T];  // [parity][cand][row][tile]
-    __shared__ __align__(8) uint64_t amax_bar;
-    __shared__ int fail_flag;
-    if (threadIdx.x == 0) {
-        mbar_init(&amax_bar, blockDim.x);
-        fail_flag = 0;
-        mbar_fence_init();
-    }
-    __syncthreads();
     if (ERR == NVFP4_ERR_NONE && !GS) fill_recip_table(rtab);
     pdl_wait();
     const int64_t nb = a.K / 16;
@@ -343,7 +324,7 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
         ahead.advance();
     }
     int stage = 0, par = 0;
-    BandAmax<NT> tile_amax{red, &amax_bar, &fail_flag, warp, lane, t, 0u, false};
+    BandAmax<NT> tile_amax{red, warp, lane, t, 0u};
     for (; cur.band < nbands; cur.advance()) {
         issue(ahead, stage == 0 ? S - 1 : stage - 1);
         ahead.advance();
