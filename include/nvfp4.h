@@ -33,6 +33,7 @@
  *   - M == 0 or K == 0 is a valid empty call (a per-tensor amax of an empty
  *     tensor is +0).  K must be a multiple of 16 [fp4-train, Requirements and
  *     limits]; 16x16 blocks and columnwise outputs also need M % 16 == 0.
+ *     M and K are each below 2^35.
  *
  * Arithmetic: fp32, round-to-nearest-even, correctly rounded division, no
  * fused multiply-add and no flush-to-zero on the pinned steps [4o6 PR, Design].

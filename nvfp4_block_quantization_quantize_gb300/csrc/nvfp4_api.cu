@@ -40,6 +40,8 @@ int check_shape(int64_t M, int64_t K) {
                                     (long long)M, (long long)K);
     if (K % 16 != 0) return fail(NVFP4_EINVAL, "K must be a multiple of 16 (got %lld)", (long long)K);
     if (K > 0 && M > INT64_MAX / 4 / K) return fail(NVFP4_EINVAL, "M*K is too large");
+    if (M >= (int64_t{1} << 35) || K >= (int64_t{1} << 35))
+        return fail(NVFP4_EINVAL, "M and K must each be below 2^35");
     return NVFP4_OK;
 }
 

@@ -236,21 +236,34 @@ struct BandAmax {
     }
 };
 
-struct BandCursor {      // CTA-uniform step: (band, 256-column chunk)
-    int64_t band, chunk, nch, dband, dchunk;
-    __device__ void init(int64_t u, int64_t nch_, int64_t stride) {
+// CTA-uniform step (band, column chunk) and this thread's 1x16 block in it.
+// The band and chunk counters are 32-bit; the block index (64-bit) is kept
+// up to date by additions only: a chunk is T blocks along the row, a band 16
+// rows of nb blocks.
+struct BandCursor {
+    int32_t band, chunk, nch, dband, dchunk;
+    int64_t blk;                                 // block index of (band*16 + rr, chunk*T + t)
+    int64_t dblk_band, dblk_step;                // blk increments: one band, one regular step
+    __device__ void init(int64_t u, int32_t nch_, int64_t stride, int64_t nb, int rr, int t, int T) {
         nch = nch_;
-        band = u / nch;
-        chunk = u - band * nch;
-        dband = stride / nch;
-        dchunk = stride - dband * nch;
+        band = static_cast<int32_t>(u / nch);
+        chunk = static_cast<int32_t>(u - static_cast<int64_t>(band) * nch);
+        dband = static_cast<int32_t>(stride / nch);
+        dchunk = static_cast<int32_t>(stride - static_cast<int64_t>(dband) * nch);
+        dblk_band = 16 * nb;
+        dblk_step = dband * dblk_band + static_cast<int64_t>(dchunk) * T;
+        blk = (static_cast<int64_t>(band) * 16 + rr) * nb + static_cast<int64_t>(chunk) * T + t;
+        wrap = dblk_band - static_cast<int64_t>(nch) * T;
     }
+    int64_t wrap;                                // blk correction when the chunk wraps to the next band
     __device__ void advance() {
         band += dband;
         chunk += dchunk;
+        blk += dblk_step;
         if (chunk >= nch) {
             chunk -= nch;
             ++band;
+            blk += wrap;
         }
     }
 };
@@ -293,10 +306,10 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
     unsigned char* xs = smem + tid * St::XB;
     unsigned char* rs = smem + NT * St::XB + tid * St::RB;
 
+    const int32_t nbands32 = static_cast<int32_t>(nbands), nb32 = static_cast<int32_t>(nb);
     auto group = [&](const BandCursor& c, bool& live) {   // this thread's 1x16 block
-        const int64_t cb = c.chunk * Gm::T + t;
-        live = c.band < nbands && cb < nb;
-        return (c.band * 16 + rr) * nb + cb;
+        live = c.band < nbands32 && c.chunk * Gm::T + t < nb32;
+        return c.blk;
     };
     auto issue = [&](const BandCursor& c, int stage) {
         bool live;
@@ -316,7 +329,7 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
 
     constexpr int S = St::STAGES;
     BandCursor cur, ahead;
-    cur.init(blockIdx.x, nch, gridDim.x);
+    cur.init(blockIdx.x, static_cast<int32_t>(nch), gridDim.x, nb, rr, t, Gm::T);
     ahead = cur;
 #pragma unroll
     for (int k = 0; k < S - 1; ++k) {
@@ -325,7 +338,7 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
     }
     int stage = 0, par = 0;
     BandAmax<NT> tile_amax{red, warp, lane, t, 0u};
-    for (; cur.band < nbands; cur.advance()) {
+    for (; cur.band < nbands32; cur.advance()) {
         issue(ahead, stage == 0 ? S - 1 : stage - 1);
         ahead.advance();
         cp_async_wait<S - 1>();
