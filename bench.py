@@ -71,6 +71,8 @@ def parse():
                    help="only the plain rowwise + columnwise measurement on W1 (--only picks a variant)")
     p.add_argument("--variants-only", action="store_true",
                    help="only the graded variants outside the step (--only picks by name)")
+    p.add_argument("--graph", type=int, default=1,
+                   help="1: the timed steps replay as one captured CUDA graph; 0: issued call by call")
     p.add_argument("--single", default=None, choices=sorted(SINGLE),
                    help="time one kernel variant the step does not run (profiling)")
     return p.parse_args()
@@ -697,13 +699,29 @@ def run_gpu(args, rank, world, local_rank):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clk_path = os.path.join(tempfile.gettempdir(), f"nvfp4_bench_clocks_rank{rank}.csv")
     os.makedirs(os.path.dirname(clk_path), exist_ok=True)
+    graph = None
+    if args.graph:
+        # the K timed steps (their own step indices) captured as one CUDA
+        # graph: the same launches, issued without the host's per-call work
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for k in range(nsteps):
+                    step(args.warmup + k)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
     proc, fh = clocks_sampler_start(clk_path)
     time.sleep(0.5 if proc else 0)
     barrier()
     torch.cuda.synchronize()
     start.record(stream)
-    for k in range(nsteps):
-        step(args.warmup + k)
+    if graph is not None:
+        graph.replay()
+    else:
+        for k in range(nsteps):
+            step(args.warmup + k)
     stop.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -821,7 +839,10 @@ def run_gpu(args, rank, world, local_rank):
                    "l2": "inputs larger than L2: each step streams ~2.7 GB and no tensor is "
                          "re-read within 129 MB of other traffic, except the second (quantize) "
                          "pass after an amax pass over the same tensor",
-                   "parallelism": f"{world} independent replica(s), no data-path collective"},
+                   "parallelism": f"{world} independent replica(s), no data-path collective",
+                   "launch": ("the K timed steps captured once as a CUDA graph and replayed (same kernels and "
+                              "arguments, each step its own step index)" if args.graph else
+                              "calls issued one by one from Python")},
         "gpu_launches": nsteps * sum(1 for name, _, _, _ in plan if not args.only or args.only in name),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "calls": calls,
         "fp4_mm": mm, "c4_rowcol": c4, "rowcol_plain": rc, "variants": var,
