@@ -113,11 +113,10 @@ __device__ __forceinline__ void fill_recip_table(float* rt) {
 // reciprocal table when D is a bare E4M3 scale sf (no global scale), else
 // null.  With wq, stochastic rounding also returns the codes' signed grid
 // values in q (nearest rounding leaves q alone).
-// get_words4(j, w) fills the four stochastic-rounding words of elements
-// 4j .. 4j + 3 (called only for stochastic rounding, group by group, so the
-// generator's work interleaves with the rounding and only four words are live).
-template <int RND, class GetWords4>
-__device__ __forceinline__ void encode_plain16_impl(const float* y, float D, float b, GetWords4 get_words4,
+// get_words(wd) fills the 16 elements' stochastic-rounding words (called
+// only for stochastic rounding, where the words are needed).
+template <int RND, class GetWords>
+__device__ __forceinline__ void encode_plain16_impl(const float* y, float D, float b, GetWords get_words,
                                                     uint32_t& w0, uint32_t& w1, const float* rt,
                                                     uint32_t sf, float* q, bool wq) {
     const bool fast = plain_fast(D, b);
@@ -130,6 +129,8 @@ __device__ __forceinline__ void encode_plain16_impl(const float* y, float D, flo
         w0 = e2m1_encode8(v);
         w1 = e2m1_encode8(v + 8);
     } else {
+        uint32_t wd[16];
+        get_words(wd);
         // blocks holding an element 0 < |y| < 2^-80 (or zeros) take the per-element checked path
         bool tiny = false;
 #pragma unroll
@@ -138,35 +139,23 @@ __device__ __forceinline__ void encode_plain16_impl(const float* y, float D, flo
         if (fast && !tiny) {
             const uint64_t R2 = pack2(r, r), ND2 = pack2(-D, -D);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t wd[4];
-                get_words4(j, wd);
-#pragma unroll
-                for (int h = 0; h < 4; h += 2) {
-                    const int i = 4 * j + h;
-                    const uint64_t Y = pack2(y[i], y[i + 1]);
-                    const uint64_t Q0 = mul2(Y, R2);
-                    uint64_t Q = fma2(fma2(Q0, ND2, Y), R2, Q0);
-                    if (!rt) Q = fma2(fma2(Q, ND2, Y), R2, Q);
-                    float q0a, q0b, qa, qb, ga, gb;
-                    unpack2(Q0, q0a, q0b);
-                    unpack2(Q, qa, qb);
-                    sr_grid_value2(fabsf(qa), fabsf(qb), wd[h], wd[h + 1], ga, gb);
-                    g[i] = sign_of_first(q0a, ga);
-                    g[i + 1] = sign_of_first(q0b, gb);
-                }
+            for (int i = 0; i < 16; i += 2) {
+                const uint64_t Y = pack2(y[i], y[i + 1]);
+                const uint64_t Q0 = mul2(Y, R2);
+                uint64_t Q = fma2(fma2(Q0, ND2, Y), R2, Q0);
+                if (!rt) Q = fma2(fma2(Q, ND2, Y), R2, Q);
+                float q0a, q0b, qa, qb, ga, gb;
+                unpack2(Q0, q0a, q0b);
+                unpack2(Q, qa, qb);
+                sr_grid_value2(fabsf(qa), fabsf(qb), wd[i], wd[i + 1], ga, gb);
+                g[i] = sign_of_first(q0a, ga);
+                g[i + 1] = sign_of_first(q0b, gb);
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t wd[4];
-                get_words4(j, wd);
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const int i = 4 * j + h;
-                    const float v = rt ? plain_quotient<true, true>(y[i], D, r, fast) : plain_quotient<true>(y[i], D, r, fast);
-                    g[i] = sign_of_first(v, sr_grid_value(fabsf(v), wd[h]));
-                }
+            for (int i = 0; i < 16; ++i) {
+                const float v = rt ? plain_quotient<true, true>(y[i], D, r, fast) : plain_quotient<true>(y[i], D, r, fast);
+                g[i] = sign_of_first(v, sr_grid_value(fabsf(v), wd[i]));
             }
         }
         w0 = e2m1_encode8(g);
@@ -193,7 +182,7 @@ __device__ __forceinline__ void encode_plain16(const float* y, float D, float b,
                                                uint32_t& w1, const float* rt, uint32_t sf,
                                                float* q, bool wq) {
     encode_plain16_impl<RND>(
-        y, D, b, [&](int j, uint32_t* w) { sr_words4(idx0, j, seed, step, w); }, w0, w1, rt, sf, q, wq);
+        y, D, b, [&](uint32_t* wd) { sr_words16(idx0, seed, step, wd); }, w0, w1, rt, sf, q, wq);
 }
 
 // the same with the words given (wd[16], read only for stochastic rounding)
@@ -203,9 +192,9 @@ __device__ __forceinline__ void encode_plain16_words(const float* y, float D, fl
                                                      uint32_t sf, float* q, bool wq) {
     encode_plain16_impl<RND>(
         y, D, b,
-        [&](int j, uint32_t* out) {
+        [&](uint32_t* out) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) out[i] = wd[4 * j + i];
+            for (int i = 0; i < 16; ++i) out[i] = wd[i];
         },
         w0, w1, rt, sf, q, wq);
 }

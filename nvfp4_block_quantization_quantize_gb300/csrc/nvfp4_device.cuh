@@ -111,20 +111,6 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
     return c;
 }
 
-// The four words of the counter block holding global element indices
-// idx0 + 4j .. idx0 + 4j + 3 (idx0 a multiple of 16): element idx uses word
-// idx % 4 of the block with counter (idx / 4, step).
-__device__ __forceinline__ void sr_words4(uint64_t idx0, int j, uint64_t seed, uint64_t step, uint32_t* w) {
-    const uint64_t blk = (idx0 >> 2) + static_cast<uint64_t>(j);
-    const uint4 o = philox4x32_10(make_uint4(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32),
-                                             static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32)),
-                                  static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
-    w[0] = o.x;
-    w[1] = o.y;
-    w[2] = o.z;
-    w[3] = o.w;
-}
-
 // Words for global element indices idx0 .. idx0+15 (idx0 a multiple of 16):
 // element idx uses word idx % 4 of the block with counter (idx / 4, step).
 __device__ __forceinline__ void sr_words16(uint64_t idx0, uint64_t seed, uint64_t step,
