@@ -102,9 +102,9 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool
 // bytes (and residual bytes under error feedback) for one grid-stride step.
 // With a residual a block moves 96-128 bytes, so one step ahead at a higher
 // occupancy keeps enough in flight; without, three steps ahead (the stage count is per variant).
-template <int DT, bool EF, int NT = kThreads>
+template <int DT, bool EF, int NT = kThreads, int EF_STAGES = 2>
 struct RowsStage {
-    static constexpr int STAGES = EF ? 2 : 4;
+    static constexpr int STAGES = EF ? EF_STAGES : 4;
     static constexpr int XB = DT == NVFP4_BF16 ? 32 : 64;   // x bytes per block
     static constexpr int RB = EF ? 64 : 0;                    // residual bytes per block
     static constexpr int BYTES = NT * (XB + RB);
@@ -269,15 +269,19 @@ struct BandCursor {
 };
 
 #ifndef NVFP4_BAND_THREADS
-#define NVFP4_BAND_THREADS 256
+#define NVFP4_BAND_THREADS 128
+#endif
+#ifndef NVFP4_BAND_EF_STAGES
+#define NVFP4_BAND_EF_STAGES 2
 #endif
 constexpr int kBandThreads = NVFP4_BAND_THREADS;
+constexpr int kBandEfStages = NVFP4_BAND_EF_STAGES;
 
 template <int DT, int ERR, int RND, bool EF, bool GS>
 __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
     constexpr int NT = kBandThreads;
     using Gm = BandGeom<NT>;
-    using St = RowsStage<DT, EF, NT>;
+    using St = RowsStage<DT, EF, NT, kBandEfStages>;
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ O6TabOf<ERR> tab;
     __shared__ float rtab[(ERR == NVFP4_ERR_NONE && !GS) ? 128 : 1];
@@ -406,8 +410,9 @@ int launch_rows(const QuantArgs& a, int64_t nblk, cudaStream_t s) {
     if (BLK == NVFP4_BLOCK_16X16) {
         constexpr int T = BandGeom<kBandThreads>::T;
         const int64_t steps = (a.M / 16) * ((a.K / 16 + T - 1) / T);
-        return launch_persistent(k_band16<DT, ERR, RND, EF, GS>, RowsStage<DT, EF, kBandThreads>::TOTAL, 1, steps,
-                                 a, s, configured_dev, per_sm, kBandThreads);
+        return launch_persistent(k_band16<DT, ERR, RND, EF, GS>,
+                                 RowsStage<DT, EF, kBandThreads, kBandEfStages>::TOTAL, 1, steps, a, s,
+                                 configured_dev, per_sm, kBandThreads);
     }
     return launch_persistent(k_rows<DT, ERR, RND, EF, GS>, RowsStage<DT, EF>::TOTAL, kThreads, nblk, a, s,
                              configured_dev, per_sm);
