@@ -85,6 +85,7 @@ int check_quant(const void* x, int64_t M, int64_t K, int dtype, int block, int r
 // The amax pass (TENSOR / ROW) then the quantize kernel with the amax given.
 int run_quant(nvfp4::QuantArgs a, float* gamax, void* stream) {
     int err;
+    a.pk = nvfp4::philox_keys(a.seed, a.step);
     if (a.gamax_mode == NVFP4_GAMAX_TENSOR || a.gamax_mode == NVFP4_GAMAX_ROW) {
         err = nvfp4::launch_amax(a.x, a.M, a.K, a.dtype, a.residual, a.gamax_mode, gamax, stream);
         if (err) return cuda_fail(err, "amax launch");

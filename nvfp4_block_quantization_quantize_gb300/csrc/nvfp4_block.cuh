@@ -178,11 +178,11 @@ __device__ __forceinline__ void encode_plain16_impl(const float* y, float D, flo
 // elements idx0 .. idx0 + 15 of x (the stochastic-rounding counter)
 template <int RND>
 __device__ __forceinline__ void encode_plain16(const float* y, float D, float b, uint64_t idx0,
-                                               uint64_t seed, uint64_t step, uint32_t& w0,
+                                               const PhiloxKeys& pk, uint32_t& w0,
                                                uint32_t& w1, const float* rt, uint32_t sf,
                                                float* q, bool wq) {
     encode_plain16_impl<RND>(
-        y, D, b, [&](uint32_t* wd) { sr_words16(idx0, seed, step, wd); }, w0, w1, rt, sf, q, wq);
+        y, D, b, [&](uint32_t* wd) { sr_words16(idx0, pk, wd); }, w0, w1, rt, sf, q, wq);
 }
 
 // the same with the words given (wd[16], read only for stochastic rounding)

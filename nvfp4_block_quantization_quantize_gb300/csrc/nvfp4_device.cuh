@@ -99,33 +99,28 @@ __device__ __forceinline__ uint64_t mul_wide_u32(uint32_t a, uint32_t b) {
     return p;
 }
 
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        if (r) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
-        const uint64_t p0 = mul_wide_u32(0xD2511F53u, c.x);
-        const uint64_t p1 = mul_wide_u32(0xCD9E8D57u, c.z);
-        c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(p1),
-                       static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
-    }
-    return c;
-}
-
 // Words for global element indices idx0 .. idx0+15 (idx0 a multiple of 16):
 // element idx uses word idx % 4 of the block with counter (idx / 4, step).
-__device__ __forceinline__ void sr_words16(uint64_t idx0, uint64_t seed, uint64_t step,
-                                           uint32_t* w) {
-    const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
-    const uint32_t s0 = static_cast<uint32_t>(step), s1 = static_cast<uint32_t>(step >> 32);
+// Round r: (x, y, z, w) <- (hi(M1 z) ^ y ^ k0[r], lo(M1 z), hi(M0 x) ^ w ^ k1[r],
+// lo(M0 x)); round 0's step terms and the round keys come from pk.
+__device__ __forceinline__ void sr_words16(uint64_t idx0, const PhiloxKeys& pk, uint32_t* w) {
+    const uint64_t b0 = idx0 >> 2;                         // a multiple of 4
+    const uint32_t hi = static_cast<uint32_t>(b0 >> 32);   // shared by the four counters
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint64_t blk = (idx0 >> 2) + j;
-        const uint4 o = philox4x32_10(
-            make_uint4(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), s0, s1), k0, k1);
-        w[4 * j + 0] = o.x;
-        w[4 * j + 1] = o.y;
-        w[4 * j + 2] = o.z;
-        w[4 * j + 3] = o.w;
+        const uint64_t p = mul_wide_u32(kPhiloxM0, static_cast<uint32_t>(b0) + j);
+        uint4 c = make_uint4(pk.r0x ^ hi, pk.r0y, static_cast<uint32_t>(p >> 32) ^ pk.r0z, static_cast<uint32_t>(p));
+#pragma unroll
+        for (int r = 1; r < 10; ++r) {
+            const uint64_t p0 = mul_wide_u32(kPhiloxM0, c.x);
+            const uint64_t p1 = mul_wide_u32(kPhiloxM1, c.z);
+            c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ pk.k0[r], static_cast<uint32_t>(p1),
+                           static_cast<uint32_t>(p0 >> 32) ^ c.w ^ pk.k1[r], static_cast<uint32_t>(p0));
+        }
+        w[4 * j + 0] = c.x;
+        w[4 * j + 1] = c.y;
+        w[4 * j + 2] = c.z;
+        w[4 * j + 3] = c.w;
     }
 }
 
@@ -159,53 +154,48 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
     return d;
 }
 
-// 1.0f when a < b, else 0.0f (one compare-and-set)
-__device__ __forceinline__ float lt_one(float a, float b) {
-    float r;
-    asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
-
 // Stochastic rounding of one magnitude a = |v| to a grid value ("fp4-train",
 // Method): with G[k] <= a < G[k+1], take G[k+1] when u < p, p = (a - G[k]) /
 // (G[k+1] - G[k]), u = (word >> 8) * 2^-24.  The grid spacing is 0.5 on
-// [0,2), 1 on [2,4) and 2 on [4,6): sp = 2^(max(E,0) - 1) for a's binary
-// exponent E, built from a's exponent bits together with 1/sp.  t = a / sp
-// is exact and lies in [0,4), floor(t) indexes the lower point, p = t -
-// floor(t) is exact (Sterbenz) and u < p is compared as (word >> 8) < p * 2^24
-// (both sides exact).  a >= 6, infinity and NaN give 6 (the NaN-dropping min
-// after clamping a); the caller restores the sign.
+// [0,2), 1 on [2,4) and 2 on [4,6]: sp = 2^(max(E,0) - 1) for a's binary
+// exponent E.  Its reciprocal's bits are min(~bits(a) & 0x7F800000, bits(2)):
+// the complemented exponent field is 0x7F800000 minus the field.  t = a / sp
+// is exact and lies in [0,4); with fl = floor(t) and p = t - fl, the rounded
+// index fl + [u < p] equals ceil(t - u) (t - u lies in (fl, fl+1) when u < p,
+// in (fl-1, fl] otherwise), and ceil(RU(t - u)) = ceil(t - u) because
+// rounding upward never passes the integer above, so one fused multiply-add
+// rounded upward, t - (word >> 8) * 2^-24, and a ceiling give the index.  a >= 6,
+// infinity and NaN give 6 (the NaN-dropping min after clamping a); the
+// caller restores the sign (a zero result may come out as -0).
+__device__ __forceinline__ uint32_t sr_inv_bits(float a) {
+    return min(~__float_as_uint(a) & 0x7F800000u, 0x40000000u);
+}
+
 __device__ __forceinline__ float sr_grid_value(float a, uint32_t word) {
     a = min_nd(a, 6.0f);
-    const uint32_t eb = __float_as_uint(a) & 0x7F800000u;
-    const uint32_t spb = (eb > 0x3F800000u ? eb : 0x3F800000u) - 0x00800000u;   // sp
-    const float sp = __uint_as_float(spb);
-    const float inv = __uint_as_float(0x7F000000u - spb);                         // 1/sp
-    const float t = mul_rn(a, inv);
-    const float fl = floorf(t);
-    const float p24 = mul_rn(sub_rn(t, fl), 16777216.0f);
-    const float up = lt_one(static_cast<float>(word >> 8), p24);
-    return mul_rn(add_rn(fl, up), sp);
+    const uint32_t ib = sr_inv_bits(a);
+    const float t = mul_rn(a, __uint_as_float(ib));
+    const float k = ceilf(__fmaf_ru(static_cast<float>(word >> 8), -5.9604644775390625e-08f, t));
+    return mul_rn(k, __uint_as_float(0x7F000000u - ib));
+}
+
+__device__ __forceinline__ uint64_t fma2_ru(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rp.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
 }
 
 // sr_grid_value on two magnitudes at once (same arithmetic, paired fp32 ops)
 __device__ __forceinline__ void sr_grid_value2(float a0, float a1, uint32_t w0, uint32_t w1, float& g0, float& g1) {
     a0 = min_nd(a0, 6.0f);
     a1 = min_nd(a1, 6.0f);
-    const uint32_t e0 = __float_as_uint(a0) & 0x7F800000u, e1 = __float_as_uint(a1) & 0x7F800000u;
-    const uint32_t s0 = (e0 > 0x3F800000u ? e0 : 0x3F800000u) - 0x00800000u;
-    const uint32_t s1 = (e1 > 0x3F800000u ? e1 : 0x3F800000u) - 0x00800000u;
-    const uint64_t SP = pack2(__uint_as_float(s0), __uint_as_float(s1));
-    const uint64_t INV = pack2(__uint_as_float(0x7F000000u - s0), __uint_as_float(0x7F000000u - s1));
-    const uint64_t T = mul2(pack2(a0, a1), INV);
-    float t0, t1;
-    unpack2(T, t0, t1);
-    const uint64_t FL = pack2(floorf(t0), floorf(t1));
-    const uint64_t P = mul2(sub2(T, FL), pack2(16777216.0f, 16777216.0f));
-    float p0, p1;
-    unpack2(P, p0, p1);
-    const uint64_t UP = pack2(lt_one(static_cast<float>(w0 >> 8), p0), lt_one(static_cast<float>(w1 >> 8), p1));
-    unpack2(mul2(add2(FL, UP), SP), g0, g1);
+    const uint32_t i0 = sr_inv_bits(a0), i1 = sr_inv_bits(a1);
+    const uint64_t T = mul2(pack2(a0, a1), pack2(__uint_as_float(i0), __uint_as_float(i1)));
+    const uint64_t U = pack2(static_cast<float>(w0 >> 8), static_cast<float>(w1 >> 8));
+    float k0, k1;
+    unpack2(fma2_ru(U, pack2(-5.9604644775390625e-08f, -5.9604644775390625e-08f), T), k0, k1);
+    const uint64_t SP = pack2(__uint_as_float(0x7F000000u - i0), __uint_as_float(0x7F000000u - i1));
+    unpack2(mul2(pack2(ceilf(k0), ceilf(k1)), SP), g0, g1);
 }
 
 // ---- exact division from a reciprocal ---------------------------------------------------

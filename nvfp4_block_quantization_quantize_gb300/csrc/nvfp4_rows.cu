@@ -52,7 +52,7 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool
     const uint64_t idx0 = idx_base + static_cast<uint64_t>(blk) * 16u;
     tile_amax.post(absmax16(y));
     uint32_t wd[16];
-    if constexpr (EARLY) sr_words16(idx0, a.seed, a.step, wd);
+    if constexpr (EARLY) sr_words16(idx0, a.pk, wd);
     const float b = tile_amax.get();
     after_amax();
     uint32_t w0, w1, sf;
@@ -67,7 +67,7 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool
         if constexpr (EARLY)
             encode_plain16_words<RND>(y, D, b, wd, w0, w1, GS ? nullptr : rt, sf, q, wq);
         else
-            encode_plain16<RND>(y, D, b, idx0, a.seed, a.step, w0, w1, GS ? nullptr : rt, sf, q, wq);
+            encode_plain16<RND>(y, D, b, idx0, a.pk, w0, w1, GS ? nullptr : rt, sf, q, wq);
     } else {
         four_over_six16<ERR>(y, b, gb, C, tab, w0, w1, sf, d, tile_sums);
     }

@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
                 if (RND == NVFP4_SR) {
                     const uint64_t idx0 = (static_cast<uint64_t>(a.row_offset) + static_cast<uint64_t>(row)) *
                                               static_cast<uint64_t>(a.K) + static_cast<uint64_t>(cb * 16);
-                    sr_words16(idx0, a.seed, a.step, wd);
+                    sr_words16(idx0, a.pk, wd);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) ws[rr * kYsStride + t * 16 + i] = wd[i];
                 }
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_p(const QuantArgs a) {
             next_row(16 + r, y);
             uint32_t wd[16];
             if (RND == NVFP4_SR) sr_words16(idx_row0 + static_cast<uint64_t>(r) * static_cast<uint64_t>(K),
-                                            a.seed, a.step, wd);
+                                            a.pk, wd);
             uint32_t w0, w1;
             float q[16];
             encode_plain16_words<RND>(y, D, b, wd, w0, w1, GS ? nullptr : rtab, sf, q, false);
