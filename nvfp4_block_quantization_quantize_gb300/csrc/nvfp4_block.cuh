@@ -209,6 +209,23 @@ __device__ __forceinline__ float block_scale(float b, float Senc, bool std_assoc
     return block_s6f<GS>(b, Senc);
 }
 
+// y[i] += r[i] (the error-feedback sum), two elements per instruction
+__device__ __forceinline__ void add16(float* y, const float* r) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) unpack2(add2(pack2(y[i], y[i + 1]), pack2(r[i], r[i + 1])), y[i], y[i + 1]);
+}
+
+// Error-feedback residual r = y - q * d of a block without a global scale,
+// from the codes' signed grid values q: q * d has at most 7 significant bits
+// (a grid value times an E4M3 value, both normal or zero), so it is exact and
+// the fused y + (-q) * d rounds once, as y - RN(q * d) does.
+__device__ __forceinline__ void residual_q16(const float* y, const float* q, float d, float* r) {
+    const uint64_t ND = pack2(-d, -d);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2)
+        unpack2(fma2(pack2(q[i], q[i + 1]), ND, pack2(y[i], y[i + 1])), r[i], r[i + 1]);
+}
+
 // dequantized values (q * d) * S_dec from signed grid values
 template <bool GS>
 __device__ __forceinline__ void dequant_q16(const float* q, float d, float Sdec, float* dq) {

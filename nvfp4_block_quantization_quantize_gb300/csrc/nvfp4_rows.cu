@@ -85,16 +85,25 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool
     if (a.codes) reinterpret_cast<uint2*>(a.codes)[blk] = make_uint2(w0, w1);
     if (a.scales) a.scales[blk] = static_cast<uint8_t>(sf);
     if (wq) {
-        float dq[16];
-        if (QV) dequant_q16<GS>(q, d, gb.Sdec, dq);
-        else dequant16<GS || ERR != NVFP4_ERR_NONE>(w0, w1, d, gb.Sdec, dq);
-        if (EF) {
+        // stochastic rounding without a global scale: the residual straight from the grid values
+        constexpr bool FUSED = EF && QV && !GS;
+        if (FUSED) {
             float r[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) r[i] = sub_rn(y[i], dq[i]);
+            residual_q16(y, q, d, r);
             store16_f32(a.residual, blk * 16, r);
         }
-        if (a.dq_bf16) store16_bf16(a.dq_bf16, blk * 16, dq);
+        if (!FUSED || a.dq_bf16) {
+            float dq[16];
+            if (QV) dequant_q16<GS>(q, d, gb.Sdec, dq);
+            else dequant16<GS || ERR != NVFP4_ERR_NONE>(w0, w1, d, gb.Sdec, dq);
+            if (EF && !FUSED) {
+                float r[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) r[i] = sub_rn(y[i], dq[i]);
+                store16_f32(a.residual, blk * 16, r);
+            }
+            if (a.dq_bf16) store16_bf16(a.dq_bf16, blk * 16, dq);
+        }
     }
 }
 
@@ -167,8 +176,7 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
         if (EF) {
             float r[16];
             lds16<NVFP4_F32>(rs + stage * St::BYTES, r);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
+            add16(y, r);
         }
         OwnAmax own;
         rows_block<DT, ERR, RND, EF, GS>(a, blk, true, y, g, C, tp, rtab, idx_base, bpr, own,
@@ -354,8 +362,7 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
             if (EF) {
                 float r[16];
                 lds16<NVFP4_F32>(rs + stage * St::BYTES, r);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) y[i] = add_rn(y[i], r[i]);
+                add16(y, r);
             }
         } else {
 #pragma unroll
