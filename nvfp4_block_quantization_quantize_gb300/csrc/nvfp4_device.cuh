@@ -393,21 +393,6 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// ---- bit fields and shared-memory loads ------------------------------------------------------
-// the 3 bits of w at bit pos (a code's grid index when pos is a nibble start)
-__device__ __forceinline__ uint32_t bfe3(uint32_t w, int pos) {
-    uint32_t r;
-    asm("bfe.u32 %0, %1, %2, 3;" : "=r"(r) : "r"(w), "r"(pos));
-    return r;
-}
-// fp32 load from a shared-memory byte address (the data was written by the
-// same thread earlier, or published by a barrier)
-__device__ __forceinline__ float lds_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 // ---- mbarriers and bulk (TMA) copies ---------------------------------------------------------
 constexpr int kWaitTries = 1 << 22;              // bounded waits: tries before giving up
 

@@ -360,9 +360,12 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
         const uint64_t ENC6 = pack2(enc6, enc6), ENC4 = pack2(enc4, enc4);
-        // shared-memory byte address of dqt[c][0][tid]; entry k is 512 bytes further
-        const uint32_t tab6 = smem_u32(&dqt[0][0][tid]), tab4 = smem_u32(&dqt[1][0][tid]);
-        auto candidate = [&](const float* y, uint64_t enc2, uint32_t tab, uint32_t& w0, uint32_t& w1, float* e) {
+        // entry [c][k][tid] of dqt sits at byte (k << 9) | (tid << 2) of the
+        // candidate's 4 KB (tid < 128), so the byte offset of a code's entry is
+        // its nibble's magnitude bits moved to bits 9-11, or-ed with tid << 2
+        static_assert(kTileThreads == 128, "dqt entry offsets assume 128 threads");
+        const uint32_t tid4 = static_cast<uint32_t>(tid) << 2;
+        auto candidate = [&](const float* y, uint64_t enc2, const float* tab, uint32_t& w0, uint32_t& w1, float* e) {
             float v[16];
 #pragma unroll
             for (int i = 0; i < 16; i += 2) unpack2(mul2(pack2(y[i], y[i + 1]), enc2), v[i], v[i + 1]);
@@ -370,10 +373,33 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             w1 = e2m1_encode8(v + 8);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const uint32_t k = bfe3(i < 8 ? w0 : w1, 4 * (i & 7));     // grid index of the code
-                const float dq = lds_f32(tab + (k << 9));
-                const float diff = sub_rn(dq, fabsf(y[i]));
-                e[i] = (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff);
+                const uint32_t w = i < 8 ? w0 : w1;
+                constexpr int kField = 9;               // bit of the entry offset that takes the nibble's bit 0
+                const int s = 4 * (i & 7) - kField;
+                const uint32_t f = s >= 0 ? (w >> s) : (w << -s);
+                const float dq = *reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(tab) +
+                                                                 ((f & 0xE00u) | tid4));
+                e[i] = sub_rn(dq, fabsf(y[i]));
+            }
+            // MAE: |diff| (taken where the sums read it); MSE: diff^2 in pairs
+            if (ERR == NVFP4_ERR_MAE) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) e[i] = fabsf(e[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; i += 2) {
+                    const uint64_t D = pack2(e[i], e[i + 1]);
+                    unpack2(mul2(D, D), e[i], e[i + 1]);
+                }
+            }
+        };
+        // column sums F[i] += e[i] (MSE: two columns per instruction)
+        auto col_sums = [&](float* F, const float* e) {
+            if (ERR == NVFP4_ERR_MAE) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) F[i] = add_rn(F[i], e[i]);
+            } else {
+                add16(F, e);
             }
         };
 #pragma unroll 1
@@ -381,18 +407,16 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             next_row(16 + r, y);
             float e[16];
             uint32_t w0, w1;
-            candidate(y, ENC6, tab6, w0, w1, e);
+            candidate(y, ENC6, &dqt[0][0][0], w0, w1, e);
             sW[0][r][tid] = w0;
             sW[1][r][tid] = w1;
             float R6 = seq_sum16(e);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) F6[i] = add_rn(F6[i], e[i]);
-            candidate(y, ENC4, tab4, w0, w1, e);
+            col_sums(F6, e);
+            candidate(y, ENC4, &dqt[1][0][0], w0, w1, e);
             sW[2][r][tid] = w0;
             sW[3][r][tid] = w1;
             float R4 = seq_sum16(e);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) F4[i] = add_rn(F4[i], e[i]);
+            col_sums(F4, e);
             const int i8 = r & 7;
             if (r >= 8) {
                 R6 = add_rn(sR[0][i8][tid], R6);
