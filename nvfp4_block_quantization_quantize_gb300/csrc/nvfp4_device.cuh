@@ -461,6 +461,39 @@ __device__ __forceinline__ void load16(const void* base, int64_t elem0, float* y
     }
 }
 
+// A thread's slot of P 16-byte pieces (P = 2 or 4) in a per-thread copy ring,
+// with piece c stored at position c ^ swz: each 32-byte sector keeps its two
+// pieces together (so the copies fill whole sectors), while a quarter warp's
+// 16-byte reads of one piece fall into eight distinct 16-byte bank groups.
+template <int P>
+__device__ __forceinline__ uint32_t piece_swizzle(int tid) {
+    return static_cast<uint32_t>(tid >> (P == 2 ? 2 : 1)) & (P - 1);
+}
+
+// 16 elements from a swizzled slot (piece c of the group at c ^ swz)
+template <int DT>
+__device__ __forceinline__ void lds16_swz(const unsigned char* slot, uint32_t swz, float* y) {
+    if (DT == NVFP4_BF16) {
+        const uint4 a = *reinterpret_cast<const uint4*>(slot + ((0 ^ swz) << 4));
+        const uint4 b = *reinterpret_cast<const uint4*>(slot + ((1 ^ swz) << 4));
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            y[2 * i] = __uint_as_float(w[i] << 16);
+            y[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 f = *reinterpret_cast<const float4*>(slot + ((i ^ swz) << 4));
+            y[4 * i] = f.x;
+            y[4 * i + 1] = f.y;
+            y[4 * i + 2] = f.z;
+            y[4 * i + 3] = f.w;
+        }
+    }
+}
+
 // 16 elements from shared memory (the layout load16 reads from global memory)
 template <int DT>
 __device__ __forceinline__ void lds16(const void* p, float* y) {

@@ -108,7 +108,8 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool
 }
 
 // Per-thread copy pipeline: stage s holds, for each thread, its block's x
-// bytes (and residual bytes under error feedback) for one grid-stride step.
+// bytes (and residual bytes under error feedback) for one grid-stride step,
+// each in a slot of its own with the 16-byte pieces swizzled (piece_swizzle).
 // With a residual a block moves 96-128 bytes, so one step ahead at a higher
 // occupancy keeps enough in flight; without, three steps ahead (the stage count is per variant).
 template <int DT, bool EF, int NT = kThreads, int EF_STAGES = 2>
@@ -149,16 +150,17 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
     const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
     unsigned char* xs = smem + tid * St::XB;
     unsigned char* rs = smem + kThreads * St::XB + tid * St::RB;
+    const uint32_t swx = piece_swizzle<St::XB / 16>(tid), swr = piece_swizzle<4>(tid);
 
     auto issue = [&](int64_t blk, int stage) {
         if (blk < nblk) {
             const unsigned char* gx = static_cast<const unsigned char*>(a.x) + blk * St::XB;
 #pragma unroll
-            for (int c = 0; c < St::XB / 16; ++c) cp_async16(xs + stage * St::BYTES + 16 * c, gx + 16 * c);
+            for (int c = 0; c < St::XB / 16; ++c) cp_async16(xs + stage * St::BYTES + ((c ^ swx) << 4), gx + 16 * c);
             if (EF) {
                 const unsigned char* gr = reinterpret_cast<const unsigned char*>(a.residual) + blk * 64;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) cp_async16(rs + stage * St::BYTES + 16 * c, gr + 16 * c);
+                for (int c = 0; c < 4; ++c) cp_async16(rs + stage * St::BYTES + ((c ^ swr) << 4), gr + 16 * c);
             }
         }
         cp_async_commit();
@@ -172,10 +174,10 @@ __global__ void __launch_bounds__(kThreads) k_rows(const QuantArgs a) {
         issue(blk + (S - 1) * stride, stage == 0 ? S - 1 : stage - 1);
         cp_async_wait<S - 1>();
         float y[16];
-        lds16<DT>(xs + stage * St::BYTES, y);
+        lds16_swz<DT>(xs + stage * St::BYTES, swx, y);
         if (EF) {
             float r[16];
-            lds16<NVFP4_F32>(rs + stage * St::BYTES, r);
+            lds16_swz<NVFP4_F32>(rs + stage * St::BYTES, swr, r);
             add16(y, r);
         }
         OwnAmax own;
@@ -317,6 +319,7 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
     const int t = lane % Gm::T;                  // tile within the chunk
     unsigned char* xs = smem + tid * St::XB;
     unsigned char* rs = smem + NT * St::XB + tid * St::RB;
+    const uint32_t swx = piece_swizzle<St::XB / 16>(tid), swr = piece_swizzle<4>(tid);
 
     const int32_t nbands32 = static_cast<int32_t>(nbands), nb32 = static_cast<int32_t>(nb);
     auto group = [&](const BandCursor& c, bool& live) {   // this thread's 1x16 block
@@ -329,11 +332,11 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
         if (live) {
             const unsigned char* gx = static_cast<const unsigned char*>(a.x) + blk * St::XB;
 #pragma unroll
-            for (int k = 0; k < St::XB / 16; ++k) cp_async16(xs + stage * St::BYTES + 16 * k, gx + 16 * k);
+            for (int k = 0; k < St::XB / 16; ++k) cp_async16(xs + stage * St::BYTES + ((k ^ swx) << 4), gx + 16 * k);
             if (EF) {
                 const unsigned char* gr = reinterpret_cast<const unsigned char*>(a.residual) + blk * 64;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) cp_async16(rs + stage * St::BYTES + 16 * k, gr + 16 * k);
+                for (int k = 0; k < 4; ++k) cp_async16(rs + stage * St::BYTES + ((k ^ swr) << 4), gr + 16 * k);
             }
         }
         cp_async_commit();
@@ -358,10 +361,10 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
         const int64_t blk = group(cur, live);
         float y[16];
         if (live) {
-            lds16<DT>(xs + stage * St::BYTES, y);
+            lds16_swz<DT>(xs + stage * St::BYTES, swx, y);
             if (EF) {
                 float r[16];
-                lds16<NVFP4_F32>(rs + stage * St::BYTES, r);
+                lds16_swz<NVFP4_F32>(rs + stage * St::BYTES, swr, r);
                 add16(y, r);
             }
         } else {
