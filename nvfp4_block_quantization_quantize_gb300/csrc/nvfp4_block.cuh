@@ -347,11 +347,88 @@ __device__ __forceinline__ void candidate16_tab(const float* y, float enc, const
     }
 }
 
+// The exact error sum of one candidate from its codes (the per-element
+// errors of candidate16_tab, summed in element order from 0 as seq_sum16).
+template <int ERR>
+__device__ __forceinline__ float errsum16_tab(const float* y, uint32_t w0, uint32_t w1, const float* dq) {
+    float E = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t k = ((i < 8 ? w0 : w1) >> (4 * (i & 7))) & 7u;
+        const float diff = sub_rn(dq[k * kDqStride], fabsf(y[i]));
+        E = add_rn(E, (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff));
+    }
+    return E;
+}
+
+// Approximate error sum of one candidate, no table lookups: a code of grid
+// value q (signed like its y) stands for q * K, K = the error value of q = 1
+// (((1 * d) * A) / C), so an element's error is |y - q * K| from one fused
+// multiply-add (squared for MSE), summed in element order.  The codes are
+// the candidate's exact codes.
+template <int ERR>
+__device__ __forceinline__ float errsum16_approx(const float* y, float enc, float K, uint32_t& w0,
+                                                 uint32_t& w1) {
+    float v[16];
+    const uint64_t ENC2 = pack2(enc, enc), NK2 = pack2(-K, -K);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) unpack2(mul2(pack2(y[i], y[i + 1]), ENC2), v[i], v[i + 1]);
+    uint32_t h[8];
+    w0 = e2m1_encode8_dec(v, h);
+    w1 = e2m1_encode8_dec(v + 8, h + 4);
+    float E = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float q0 = __half2float(__ushort_as_half(static_cast<unsigned short>(h[j] & 0xFFFFu)));
+        const float q1 = __half2float(__ushort_as_half(static_cast<unsigned short>(h[j] >> 16)));
+        uint64_t D = fma2(pack2(q0, q1), NK2, pack2(y[2 * j], y[2 * j + 1]));   // y - q * K
+        if (ERR == NVFP4_ERR_MSE) D = mul2(D, D);
+        float e0, e1;
+        unpack2(D, e0, e1);
+        E = add_rn(E, fabsf(e0));
+        E = add_rn(E, fabsf(e1));
+    }
+    return E;
+}
+
+// Whether approximate sums S6, S4 (errsum16_approx) decide E4 < E6 as the
+// exact sums E6, E4 do.  With u = 2^-24, K_r = d*A/C and q an element's grid
+// value (|q| <= 6): an error value dq = ((q*d)*A)/C (q*d exact, two
+// roundings) lies within (2u + u^2)|q| K_r of |q| K_r, and K (the same two
+// roundings) within as much of K_r, so |dq - |q| K| <= 4.02u |q| K.  The
+// differences d_t = dq - |y| and d_a = y - q*K are each rounded once, so
+// ||d_t| - |d_a|| <= 4.02u |q| K + u (|d_t| + |d_a|) (1 + u).
+//   MAE: summing over the block and adding gamma_15 <= 15.01u of each
+//   element-order sum, |E - S| <= 386u K + 32.1u S (to first order in u).
+//   MSE: |d_t^2 - d_a^2| = ||d_t| - |d_a|| (|d_t| + |d_a|), the squares'
+//   roundings add u each, and sum |d| <= 4 sqrt(sum d^2) over 16 terms, so
+//   |E - S| <= 193u K sqrt(S) + 36u S.
+// The threshold is twice these bounds with the constants rounded up to
+// powers of two (2^9 u K + 2^6 u S, and 2^8 u K sqrt(S) + 2^6 u S per
+// candidate), plus 2^-120 for the absolute errors of subnormal results; the
+// square root is rounded upward.  A NaN or infinite sum or K gives a NaN
+// difference or an infinite threshold: the test fails and the caller takes
+// the exact sums.
+template <int ERR>
+__device__ __forceinline__ bool approx_decides(float S6, float S4, float K6, float K4) {
+    float T;
+    if (ERR == NVFP4_ERR_MAE) {
+        T = add_rn(mul_rn(add_rn(K6, K4), 6.103515625e-05f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
+    } else {
+        const float R = add_rn(mul_rn(K6, __fsqrt_ru(S6)), mul_rn(K4, __fsqrt_ru(S4)));
+        T = add_rn(mul_rn(R, 3.0517578125e-05f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
+    }
+    T = add_rn(T, 7.52316384526264e-37f);
+    return fabsf(sub_rn(S6, S4)) > T;
+}
+
 // Four-over-six for one 16-value group (1x16 block, or one row of a 16x16 tile
 // when TREE: the row error sums are combined over the half warp).
 // tile_sums(E6, E4) turns one group's error sums into its block's: nothing for
 // a 1x16 block, the width-16 tree over the tile's 16 rows for a 16x16 tile.
-template <int ERR, class TileSums>
+// CERT (a 1x16 block, whose error sums are its own): the sums come from
+// errsum16_approx wherever approx_decides, from the table otherwise.
+template <int ERR, bool CERT = false, class TileSums>
 __device__ __forceinline__ void four_over_six16(const float* y, float b, const GScale& g, float C,
                                                 const O6Tab* tab, uint32_t& w0, uint32_t& w1,
                                                 uint32_t& sf, float& d, TileSums tile_sums) {
@@ -361,7 +438,15 @@ __device__ __forceinline__ void four_over_six16(const float* y, float b, const G
     const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
     uint32_t a0, a1, b0, b1;
     float e[16], E6, E4;
-    if (tab) {                                  // per-tensor global scale: table lookups
+    if (CERT && tab) {                          // per-tensor global scale, 1x16
+        const float K6 = tab->dq[2 * kDqStride + sf6], K4 = tab->dq[2 * kDqStride + sf4];
+        E6 = errsum16_approx<ERR>(y, tab->enc[sf6], K6, a0, a1);
+        E4 = errsum16_approx<ERR>(y, tab->enc[sf4], K4, b0, b1);
+        if (!approx_decides<ERR>(E6, E4, K6, K4)) {
+            E6 = errsum16_tab<ERR>(y, a0, a1, tab->dq + sf6);
+            E4 = errsum16_tab<ERR>(y, b0, b1, tab->dq + sf4);
+        }
+    } else if (tab) {                           // per-tensor global scale: table lookups
         candidate16_tab<ERR>(y, tab->enc[sf6], tab->dq + sf6, a0, a1, e);
         E6 = seq_sum16(e);
         candidate16_tab<ERR>(y, tab->enc[sf4], tab->dq + sf4, b0, b1, e);
