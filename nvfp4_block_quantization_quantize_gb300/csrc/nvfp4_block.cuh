@@ -426,6 +426,26 @@ __device__ __forceinline__ bool approx_decides(float S6, float S4, float K6, flo
 // when TREE: the row error sums are combined over the half warp).
 // tile_sums(E6, E4) turns one group's error sums into its block's: nothing for
 // a 1x16 block, the width-16 tree over the tile's 16 rows for a 16x16 tile.
+// The same test for a 16x16 tile's sums over its 256 elements (rowwise: the
+// width-16 tree of the rows' element-order sums; columnwise: of the
+// columns'), each element's error passing at most 15 + 4 additions: with
+// sum |q| <= 1536 and gamma_19, |E - S| <= 6175u K + 40u S for MAE and, with
+// sum |d| <= 16 sqrt(sum d^2) over 256 terms, <= 772u K sqrt(S) + 44u S for
+// MSE; per candidate 2^13 u K + 2^6 u S and 2^10 u K sqrt(S) + 2^6 u S, and
+// the threshold twice the two candidates' bounds together plus 2^-120.
+template <int ERR>
+__device__ __forceinline__ bool tile_sums_decide(float S6, float S4, float K6, float K4) {
+    float T;
+    if (ERR == NVFP4_ERR_MAE) {
+        T = add_rn(mul_rn(add_rn(K6, K4), 9.765625e-04f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
+    } else {
+        const float R = add_rn(mul_rn(K6, __fsqrt_ru(S6)), mul_rn(K4, __fsqrt_ru(S4)));
+        T = add_rn(mul_rn(R, 1.220703125e-04f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
+    }
+    T = add_rn(T, 7.52316384526264e-37f);
+    return fabsf(sub_rn(S6, S4)) > T;
+}
+
 // CERT (a 1x16 block, whose error sums are its own): the sums come from
 // errsum16_approx wherever approx_decides, from the table otherwise.
 template <int ERR, bool CERT = false, class TileSums>

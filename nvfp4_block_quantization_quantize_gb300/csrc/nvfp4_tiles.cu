@@ -341,56 +341,37 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
         const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
         const uint32_t sf4 = e4m3_encode(min_nd(mul_rn(s6f, 1.5f), 448.0f));
         const float enc6 = tenc[sf6], enc4 = tenc[sf4];
-        // |dq| = ((G[k] * d) * A) / (6 * bound) of each grid magnitude G[k]: the
-        // error value of a code with index k is +-|dq| with the sign of its y, so
-        // |dq - y| = | |dq| - |y| | exactly (and likewise the square)
-        {
-            const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
-            const float G[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                dqt[0][k][tid] = div_rn(mul_rn(mul_rn(G[k], d6), g.A), C);
-                dqt[1][k][tid] = div_rn(mul_rn(mul_rn(G[k], d4), g.A), C);
-            }
-        }
+        const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
+        // K: the error value of grid value 1, ((1 * d) * A) / (6 * bound)
+        const float K6 = div_rn(mul_rn(d6, g.A), C), K4 = div_rn(mul_rn(d4, g.A), C);
 
-        // pass 1: per-element errors; row sums to shared memory, column sums in
-        // registers, both accumulated in element order
+        // pass 1: both candidates' codes, and approximate per-element errors
+        // |y - q K| (squared for MSE; q the code's signed grid value, so this is
+        // | |q| K - |y| |) with no table lookup; row sums to shared memory,
+        // column sums in registers, both accumulated in element order
         float F6[16], F4[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
         const uint64_t ENC6 = pack2(enc6, enc6), ENC4 = pack2(enc4, enc4);
-        // entry [c][k][tid] of dqt sits at byte (k << 9) | (tid << 2) of the
-        // candidate's 4 KB (tid < 128), so the byte offset of a code's entry is
-        // its nibble's magnitude bits moved to bits 9-11, or-ed with tid << 2
-        static_assert(kTileThreads == 128, "dqt entry offsets assume 128 threads");
-        const uint32_t tid4 = static_cast<uint32_t>(tid) << 2;
-        auto candidate = [&](const float* y, uint64_t enc2, const float* tab, uint32_t& w0, uint32_t& w1, float* e) {
+        auto candidate = [&](const float* y, uint64_t enc2, float K, uint32_t& w0, uint32_t& w1, float* e) {
             float v[16];
 #pragma unroll
             for (int i = 0; i < 16; i += 2) unpack2(mul2(pack2(y[i], y[i + 1]), enc2), v[i], v[i + 1]);
-            w0 = e2m1_encode8(v);
-            w1 = e2m1_encode8(v + 8);
+            uint32_t h[8];
+            w0 = e2m1_encode8_dec(v, h);
+            w1 = e2m1_encode8_dec(v + 8, h + 4);
+            const uint64_t NK2 = pack2(-K, -K);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t w = i < 8 ? w0 : w1;
-                constexpr int kField = 9;               // bit of the entry offset that takes the nibble's bit 0
-                const int s = 4 * (i & 7) - kField;
-                const uint32_t f = s >= 0 ? (w >> s) : (w << -s);
-                const float dq = *reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(tab) +
-                                                                 ((f & 0xE00u) | tid4));
-                e[i] = sub_rn(dq, fabsf(y[i]));
+            for (int j = 0; j < 8; ++j) {
+                const float q0 = __half2float(__ushort_as_half(static_cast<unsigned short>(h[j] & 0xFFFFu)));
+                const float q1 = __half2float(__ushort_as_half(static_cast<unsigned short>(h[j] >> 16)));
+                uint64_t D = fma2(pack2(q0, q1), NK2, pack2(y[2 * j], y[2 * j + 1]));
+                if (ERR != NVFP4_ERR_MAE) D = mul2(D, D);
+                unpack2(D, e[2 * j], e[2 * j + 1]);
             }
-            // MAE: |diff| (taken where the sums read it); MSE: diff^2 in pairs
             if (ERR == NVFP4_ERR_MAE) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) e[i] = fabsf(e[i]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; i += 2) {
-                    const uint64_t D = pack2(e[i], e[i + 1]);
-                    unpack2(mul2(D, D), e[i], e[i + 1]);
-                }
             }
         };
         // column sums F[i] += e[i] (MSE: two columns per instruction)
@@ -402,21 +383,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
                 add16(F, e);
             }
         };
-#pragma unroll 1
-        for (int r = 0; r < 16; ++r) {
-            next_row(16 + r, y);
-            float e[16];
-            uint32_t w0, w1;
-            candidate(y, ENC6, &dqt[0][0][0], w0, w1, e);
-            sW[0][r][tid] = w0;
-            sW[1][r][tid] = w1;
-            float R6 = seq_sum16(e);
-            col_sums(F6, e);
-            candidate(y, ENC4, &dqt[1][0][0], w0, w1, e);
-            sW[2][r][tid] = w0;
-            sW[3][r][tid] = w1;
-            float R4 = seq_sum16(e);
-            col_sums(F4, e);
+        auto row_sums = [&](int r, float R6, float R4) {
             const int i8 = r & 7;
             if (r >= 8) {
                 R6 = add_rn(sR[0][i8][tid], R6);
@@ -424,16 +391,76 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             }
             sR[0][i8][tid] = R6;
             sR[1][i8][tid] = R4;
+        };
+#pragma unroll 1
+        for (int r = 0; r < 16; ++r) {
+            next_row(16 + r, y);
+            float e[16];
+            uint32_t w0, w1;
+            candidate(y, ENC6, K6, w0, w1, e);
+            sW[0][r][tid] = w0;
+            sW[1][r][tid] = w1;
+            const float R6 = seq_sum16(e);
+            col_sums(F6, e);
+            candidate(y, ENC4, K4, w0, w1, e);
+            sW[2][r][tid] = w0;
+            sW[3][r][tid] = w1;
+            const float R4 = seq_sum16(e);
+            col_sums(F4, e);
+            row_sums(r, R6, R4);
         }
         if constexpr (Rg::SLOTS > 0) cp_async_wait<0>();
-        float S[8];
+        float E6r, E4r, E6c, E4c;
+        auto tree_sums = [&]() {
+            float S[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) S[i] = sR[0][i][tid];
-        const float E6r = tree16_upper(S);
+            for (int i = 0; i < 8; ++i) S[i] = sR[0][i][tid];
+            E6r = tree16_upper(S);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) S[i] = sR[1][i][tid];
-        const float E4r = tree16_upper(S);
-        const float E6c = tree16_regs(F6), E4c = tree16_regs(F4);
+            for (int i = 0; i < 8; ++i) S[i] = sR[1][i][tid];
+            E4r = tree16_upper(S);
+            E6c = tree16_regs(F6);
+            E4c = tree16_regs(F4);
+        };
+        tree_sums();
+        if (!(tile_sums_decide<ERR>(E6r, E4r, K6, K4) && tile_sums_decide<ERR>(E6c, E4c, K6, K4))) {
+            // the exact sums: error values |dq| = ((G[k] * d) * A) / (6 * bound)
+            // of each grid magnitude G[k] from a per-thread table (a code of
+            // index k stands for +-|dq| with the sign of its y, so |dq - y| =
+            // | |dq| - |y| | exactly, and likewise the square), the codes kept
+            // in sW, the rows read again
+            const float G[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                dqt[0][k][tid] = div_rn(mul_rn(mul_rn(G[k], d6), g.A), C);
+                dqt[1][k][tid] = div_rn(mul_rn(mul_rn(G[k], d4), g.A), C);
+            }
+            auto exact = [&](const float* y, uint32_t w0, uint32_t w1, int c, float* e) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const uint32_t k = ((i < 8 ? w0 : w1) >> (4 * (i & 7))) & 7u;
+                    const float diff = sub_rn(dqt[c][k][tid], fabsf(y[i]));
+                    e[i] = (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff);
+                }
+            };
+#pragma unroll
+            for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
+#pragma unroll 1
+            for (int r = 0; r < 16; ++r) {
+                load16<DT>(a.x, base + static_cast<int64_t>(r) * K, y);
+                float e[16];
+                exact(y, sW[0][r][tid], sW[1][r][tid], 0, e);
+                const float R6 = seq_sum16(e);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) F6[i] = add_rn(F6[i], e[i]);
+                exact(y, sW[2][r][tid], sW[3][r][tid], 1, e);
+                const float R4 = seq_sum16(e);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) F4[i] = add_rn(F4[i], e[i]);
+                row_sums(r, R6, R4);
+            }
+            tree_sums();
+        }
         const bool row4 = E4r < E6r, col4 = E4c < E6c;       // ties and NaN keep map-to-6
         const uint8_t sf_r = static_cast<uint8_t>(row4 ? sf4 : sf6);
 
