@@ -99,6 +99,37 @@ def test_four_over_six_matrix(dtype, err, bound, block, gm, colwise):
         compare_quant(gpu, o)
 
 
+def _tie_inputs():
+    """Inputs on which the two four-over-six candidates' error sums are often
+    equal or within a few ulps: small multiples of 1/4 (many values lie on
+    both candidates' grids, all-zero blocks included), the same nudged by one
+    ulp in random places, and blocks repeating one value."""
+    rng = np.random.default_rng(61)
+    a = (rng.integers(-6, 7, (256, 512)) * 0.25).astype(np.float32)
+    b = a.copy()
+    m = rng.random(b.shape) < 0.3
+    b[m] = np.nextafter(b[m], np.float32(np.inf) * rng.choice([-1, 1], m.sum()).astype(np.float32))
+    c = np.repeat(rng.standard_normal((256, 32)).astype(np.float32), 16, axis=1)
+    c[:16] = 0.0
+    return a, b, c
+
+
+@pytest.mark.parametrize("err,bound", [("mae", 256.0), ("mse", 256.0), ("mae", 448.0), ("mse", 448.0)])
+def test_four_over_six_ties(err, bound):
+    """Where the candidates' sums tie or nearly tie, the decision falls back to
+    the exact sums: those blocks and tiles must still match the oracle.  With
+    bound 448 every block whose amax equals the tensor's has s6f = 448 and a
+    map-to-4 scale that saturates to the same byte: identical candidates,
+    equal nonzero sums, so the exact path decides for most blocks of the
+    first two inputs (their maximum magnitude recurs in most blocks)."""
+    for x in _tie_inputs():
+        for kw in (dict(), dict(block="16x16", colwise=True), dict(block="16x16"),
+                   dict(colwise=True)):
+            for xx in (x, W.to_bf16_bits(x)):
+                gpu, o = quantize_both(xx, gamax_mode="tensor", err_mode=err, scale_bound=bound, **kw)
+                compare_quant(gpu, o)
+
+
 @pytest.mark.parametrize("shape", [(16, 16), (1, 16), (3, 48), (32, 272), (48, 4112), (2048, 1024),
                                    (64, 1024)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -135,6 +166,9 @@ def test_special_values():
                    dict(gamax_mode="tensor", err_mode="mse", block="16x16", colwise=True,
                         scale_bound=448.0),
                    dict(gamax_mode="row", err_mode="mae"),
+                   dict(gamax_mode="tensor", err_mode="mae"),
+                   dict(gamax_mode="tensor", err_mode="mse"),
+                   dict(gamax_mode="tensor", err_mode="mae", block="16x16", colwise=True),
                    dict(gamax_mode="tensor", err_mode="mae", colwise=True)):
             gpu, o = quantize_both(xx, **kw)
             compare_quant(gpu, o)
