@@ -69,7 +69,7 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool
         else
             encode_plain16<RND>(y, D, b, idx0, a.pk, w0, w1, GS ? nullptr : rt, sf, q, wq);
     } else {
-        four_over_six16<ERR>(y, b, gb, C, tab, w0, w1, sf, d, tile_sums);
+        four_over_six16<ERR, std::is_same<TileAmax, OwnAmax>::value>(y, b, gb, C, tab, w0, w1, sf, d, tile_sums);
     }
     if (!live) return;
     if (tile_amax.failed) {
