@@ -405,18 +405,19 @@ __device__ __forceinline__ float errsum16_approx(const float* y, float enc, floa
 //   |E - S| <= 193u K sqrt(S) + 36u S.
 // The threshold is twice these bounds with the constants rounded up to
 // powers of two (2^9 u K + 2^6 u S, and 2^8 u K sqrt(S) + 2^6 u S per
-// candidate), plus 2^-120 for the absolute errors of subnormal results; the
-// square root is rounded upward.  A NaN or infinite sum or K gives a NaN
-// difference or an infinite threshold: the test fails and the caller takes
-// the exact sums.
+// candidate), plus 2^-120 for the absolute errors of subnormal results.
+// K sqrt(S) is bounded without a square root by the AM-GM inequality,
+// K sqrt(S) <= (S + K^2) / 2 (close, since S is of the order of K^2).  A NaN
+// or infinite sum or K gives a NaN difference or an infinite threshold: the
+// test fails and the caller takes the exact sums.
 template <int ERR>
 __device__ __forceinline__ bool approx_decides(float S6, float S4, float K6, float K4) {
     float T;
     if (ERR == NVFP4_ERR_MAE) {
         T = add_rn(mul_rn(add_rn(K6, K4), 6.103515625e-05f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
     } else {
-        const float R = add_rn(mul_rn(K6, __fsqrt_ru(S6)), mul_rn(K4, __fsqrt_ru(S4)));
-        T = add_rn(mul_rn(R, 3.0517578125e-05f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
+        const float R = add_rn(__fmaf_rn(K6, K6, S6), __fmaf_rn(K4, K4, S4));   // 2 * (K sqrt(S)) bound
+        T = add_rn(mul_rn(R, 1.52587890625e-05f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
     }
     T = add_rn(T, 7.52316384526264e-37f);
     return fabsf(sub_rn(S6, S4)) > T;
@@ -432,15 +433,17 @@ __device__ __forceinline__ bool approx_decides(float S6, float S4, float K6, flo
 // sum |q| <= 1536 and gamma_19, |E - S| <= 6175u K + 40u S for MAE and, with
 // sum |d| <= 16 sqrt(sum d^2) over 256 terms, <= 772u K sqrt(S) + 44u S for
 // MSE; per candidate 2^13 u K + 2^6 u S and 2^10 u K sqrt(S) + 2^6 u S, and
-// the threshold twice the two candidates' bounds together plus 2^-120.
+// the threshold twice the two candidates' bounds together plus 2^-120, with
+// K sqrt(S) <= (S + 16 K^2) / 8 (AM-GM; a tile's S is of the order of 16 K^2).
 template <int ERR>
 __device__ __forceinline__ bool tile_sums_decide(float S6, float S4, float K6, float K4) {
     float T;
     if (ERR == NVFP4_ERR_MAE) {
         T = add_rn(mul_rn(add_rn(K6, K4), 9.765625e-04f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
     } else {
-        const float R = add_rn(mul_rn(K6, __fsqrt_ru(S6)), mul_rn(K4, __fsqrt_ru(S4)));
-        T = add_rn(mul_rn(R, 1.220703125e-04f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
+        const float K6s = mul_rn(4.0f, K6), K4s = mul_rn(4.0f, K4);
+        const float R = add_rn(__fmaf_rn(K6s, K6s, S6), __fmaf_rn(K4s, K4s, S4));   // 8 * (K sqrt(S)) bound
+        T = add_rn(mul_rn(R, 1.52587890625e-05f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
     }
     T = add_rn(T, 7.52316384526264e-37f);
     return fabsf(sub_rn(S6, S4)) > T;
