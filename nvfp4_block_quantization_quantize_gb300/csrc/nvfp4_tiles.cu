@@ -20,8 +20,9 @@
 //               cover 32 consecutive tiles (fully coalesced), and the
 //               columnwise output, staged in shared memory, leaves as one
 //               32-byte run per column (4 bands x 8 bytes) instead of 8-byte
-//               pieces 32 to a warp store.  The row loops stay rolled (an
-//               unrolled kernel overflowed the instruction cache); row sums
+//               pieces 32 to a warp store.  The row loops stay rolled (a
+//               fully unrolled kernel overflowed the instruction cache; the
+//               error pass takes two rows per iteration); row sums
 //               and code words wait in shared memory until the tile's choices
 //               are known (both candidates' code words too, so x is read only
 //               twice); each thread streams its 32 row reads through a 4-slot
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             sR[0][i8][tid] = R6;
             sR[1][i8][tid] = R4;
         };
-#pragma unroll 1
+#pragma unroll 2
         for (int r = 0; r < 16; ++r) {
             next_row(16 + r, y);
             float e[16];
