@@ -731,7 +731,13 @@ def run_gpu(args, rank, world, local_rank):
     barrier()
     clocks = clocks_sampler_stop(proc, fh, clk_path, local_rank)
     total_ms = start.elapsed_time(stop)
-    for k in range(nsteps):                     # the per-call breakdown
+    # the per-call breakdown: each instrumented step starts behind a ~1 ms
+    # device spin, so the host has issued every call (and its events) before
+    # the first one runs and no call's time includes the host's issue latency
+    spin = getattr(torch.cuda, "_sleep", None)
+    for k in range(nsteps):
+        if spin is not None:
+            spin(2_000_000)
         step(args.warmup + nsteps + k, evs[k])
     torch.cuda.synchronize()
     ran = [not args.only or args.only in name for name, _, _, _ in plan]
