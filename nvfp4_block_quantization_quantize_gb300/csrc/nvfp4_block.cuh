@@ -489,12 +489,13 @@ __device__ __forceinline__ void four_over_six16(const float* y, float b, const G
     d = pick4 ? d4 : d6;
 }
 
-// TREE: the tile's 16 rows are the 16 lanes of the caller's half warp.
+// TREE: the tile's 16 rows are the 16 lanes of the caller's half warp;
+// otherwise a 1x16 block (certified sums).
 template <int ERR, bool TREE>
 __device__ __forceinline__ void four_over_six16(const float* y, float b, const GScale& g, float C,
                                                 const O6Tab* tab, uint32_t& w0, uint32_t& w1,
                                                 uint32_t& sf, float& d) {
-    four_over_six16<ERR>(y, b, g, C, tab, w0, w1, sf, d, [](float& E6, float& E4) {
+    four_over_six16<ERR, !TREE>(y, b, g, C, tab, w0, w1, sf, d, [](float& E6, float& E4) {
         if (TREE) {
             E6 = tree16_lanes(E6);
             E4 = tree16_lanes(E4);
