@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             sR[0][i8][tid] = R6;
             sR[1][i8][tid] = R4;
         };
-#pragma unroll 2
+#pragma unroll(DT == NVFP4_BF16 ? 4 : 2)
         for (int r = 0; r < 16; ++r) {
             next_row(16 + r, y);
             float e[16];
