@@ -22,7 +22,7 @@
 //               32-byte run per column (4 bands x 8 bytes) instead of 8-byte
 //               pieces 32 to a warp store.  The row loops stay rolled (a
 //               fully unrolled kernel overflowed the instruction cache; the
-//               error pass takes two rows per iteration); row sums
+//               error pass takes four bf16 or two fp32 rows per iteration); row sums
 //               and code words wait in shared memory until the tile's choices
 //               are known (both candidates' code words too, so x is read only
 //               twice); each thread streams its 32 row reads through a 4-slot
