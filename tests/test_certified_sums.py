@@ -1,0 +1,157 @@
+"""The certified four-over-six error sums, checked on the CPU.
+
+With a per-tensor global scale the kernels first form approximate error sums
+S (a code of grid value q stands for q*K, K the error value of grid value 1,
+so an element's error is |y - q*K| from one fused multiply-add) and accept
+the comparison of the approximations only when it is separated by more than
+a rounding bound; otherwise they take the exact table sums.  The outputs
+are the method's as long as |E - S| <= B for every candidate, E the method's
+error sum ("Add NVFP4 four-over-six (row-wise) quantization to the training
+prototype", Two load-bearing numeric details: error values ((q*d)*A)/C,
+element-order sums, the width-16 tree).  This test computes both sums in
+IEEE fp32 (numpy float32 arithmetic; the fused multiply-add rounded once
+from its exact rational value) on many blocks and tiles and checks the
+per-candidate bounds the kernels' thresholds are built from (the threshold
+is twice the two candidates' bounds together):
+
+  1x16 MAE  2^-15 K + 2^-18 S          1x16 MSE  2^-16 K sqrt(S) + 2^-18 S
+  tile MAE  2^-11 K + 2^-18 S          tile MSE  2^-14 K sqrt(S) + 2^-18 S
+
+each plus 2^-121 for subnormal results.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+f32 = np.float32
+FLT_MAX = f32(3.4028234663852886e38)
+
+
+def _rn32(fr: Fraction) -> np.float32:
+    """fp32 round-to-nearest-even of an exact rational."""
+    x = f32(float(fr))                       # near; fixed up below
+    best = x
+    for cand in (np.nextafter(x, f32(-np.inf)), np.nextafter(x, f32(np.inf))):
+        if not np.isfinite(cand):
+            continue
+        dc, db = abs(Fraction(float(cand)) - fr), abs(Fraction(float(best)) - fr)
+        if dc < db or (dc == db and (int(np.array(cand, f32).view(np.uint32)) & 1) == 0):
+            best = cand
+    return f32(best)
+
+
+def _fma_neg(q: np.ndarray, K: np.float32, y: np.ndarray) -> np.ndarray:
+    """RN32(y - q*K) elementwise, rounded once."""
+    fk = Fraction(float(K))
+    return np.array([_rn32(Fraction(float(yy)) - Fraction(float(qq)) * fk) for qq, yy in zip(q, y)], f32)
+
+
+def _seq(e: np.ndarray) -> np.float32:
+    s = f32(0.0)
+    for v in e:
+        s = f32(s + v)
+    return s
+
+
+def _tree16(r) -> np.float32:
+    a = [f32(r[i] + r[i + 8]) for i in range(8)]
+    b = [f32(a[i] + a[i + 4]) for i in range(4)]
+    c = [f32(b[i] + b[i + 2]) for i in range(2)]
+    return f32(c[0] + c[1])
+
+
+def _candidates(b, Senc):
+    s6f = f32(f32(b / f32(6.0)) * Senc)
+    sf6 = oracle.e4m3_encode(np.minimum(np.float32(s6f), f32(448.0)))
+    sf4 = oracle.e4m3_encode(np.minimum(f32(s6f * f32(1.5)), f32(448.0)))
+    return sf6, sf4
+
+
+def _block_errors(y, sf, A, Sdec, C, err):
+    """Exact and approximate per-element errors of one candidate on the
+    values y (any shape), and K."""
+    d = oracle.e4m3_decode(sf).astype(f32)
+    enc = np.minimum(f32(f32(1.0) / f32(d * Sdec)), FLT_MAX)
+    with np.errstate(over="ignore"):         # enc = FLT_MAX for a zero scale; the encode saturates
+        v = (y * enc).astype(f32)
+    q = oracle.e2m1_value(oracle.e2m1_encode_rn(v)).astype(f32)
+    dq = (((np.abs(q) * d).astype(f32) * A).astype(f32) / C).astype(f32)
+    diff_t = (dq - np.abs(y)).astype(f32)
+    K = f32(f32(f32(f32(1.0) * d) * A) / C)
+    diff_a = _fma_neg(q.ravel(), K, y.ravel()).reshape(y.shape)
+    if err == "mae":
+        return np.abs(diff_t), np.abs(diff_a), K
+    return (diff_t * diff_t).astype(f32), (diff_a * diff_a).astype(f32), K
+
+
+def _bound(K, S, err, tile):
+    K, S = float(K), float(S)
+    if err == "mae":
+        return (2.0 ** (-11 if tile else -15)) * K + 2.0 ** -18 * S + 2.0 ** -121
+    return (2.0 ** (-14 if tile else -16)) * K * np.sqrt(S) + 2.0 ** -18 * S + 2.0 ** -121
+
+
+def _inputs(rng, shape):
+    n = int(np.prod(shape))
+    yield "normal", rng.standard_normal(n).astype(f32).reshape(shape)
+    t = rng.standard_t(3, n).astype(f32).reshape(shape)
+    t.reshape(-1, shape[-1])[:, :2] *= 50.0                     # outlier columns
+    yield "t3 outliers", t
+    yield "quarter grid", (rng.integers(-6, 7, n) * 0.25).astype(f32).reshape(shape)
+    small = (rng.standard_normal(n) * 1e-30).astype(f32).reshape(shape)
+    yield "tiny", small
+    mixed = rng.standard_normal(n).astype(f32) * np.exp2(rng.integers(-30, 30, n)).astype(f32)
+    yield "wide exponents", mixed.reshape(shape)
+
+
+@pytest.mark.parametrize("err", ["mae", "mse"])
+@pytest.mark.parametrize("bound", [256.0, 448.0])
+def test_certified_bound_1x16(err, bound):
+    rng = np.random.default_rng(71)
+    worst = 0.0
+    for name, x in _inputs(rng, (96, 64)):
+        A = f32(np.max(np.abs(x)))
+        Senc, Sdec = oracle.global_scales(float(A), bound)
+        C = f32(f32(6.0) * f32(bound))
+        blocks = x.reshape(-1, 16)
+        b = np.max(np.abs(blocks), axis=1).astype(f32)
+        sf6, sf4 = _candidates(b, Senc)
+        for i, y in enumerate(blocks):
+            for sf in (sf6[i], sf4[i]):
+                et, ea, K = _block_errors(y, np.uint8(sf), A, Sdec, C, err)
+                E, S = _seq(et), _seq(ea)
+                gap = abs(float(E) - float(S))
+                B = _bound(K, S, err, tile=False)
+                assert gap <= B, f"{name} block {i}: |E - S| = {gap} > {B} (K {K}, S {S})"
+                worst = max(worst, gap / B)
+    print(err, bound, "worst |E - S| / B:", worst)
+    assert 0.0 < worst <= 1.0                # the approximation is not exact everywhere
+
+
+@pytest.mark.parametrize("err", ["mae", "mse"])
+def test_certified_bound_tile(err):
+    rng = np.random.default_rng(72)
+    worst = 0.0
+    for name, x in _inputs(rng, (64, 64)):
+        A = f32(np.max(np.abs(x)))
+        Senc, Sdec = oracle.global_scales(float(A), 256.0)
+        C = f32(f32(6.0) * f32(256.0))
+        for t0 in range(0, 64, 16):
+            for c0 in range(0, 64, 16):
+                y = x[t0:t0 + 16, c0:c0 + 16]
+                b = np.array([np.max(np.abs(y))], f32)
+                sf6, sf4 = _candidates(b, Senc)
+                for sf in (sf6[0], sf4[0]):
+                    et, ea, K = _block_errors(y, np.uint8(sf), A, Sdec, C, err)
+                    for tr in (False, True):          # rowwise sums, then x^T's (columnwise)
+                        mt, ma = (et.T, ea.T) if tr else (et, ea)
+                        E = _tree16([_seq(r) for r in mt])
+                        S = _tree16([_seq(r) for r in ma])
+                        gap = abs(float(E) - float(S))
+                        B = _bound(K, S, err, tile=True)
+                        assert gap <= B, f"{name} tile ({t0},{c0}) {'col' if tr else 'row'}: {gap} > {B}"
+                        worst = max(worst, gap / B)
+    assert 0.0 < worst <= 1.0
