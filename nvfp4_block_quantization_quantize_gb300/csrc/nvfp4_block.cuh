@@ -237,15 +237,6 @@ __device__ __forceinline__ void dequant_q16(const float* q, float d, float Sdec,
 }
 
 // ---- four-over-six --------------------------------------------------------------------------
-// codes of y * enc for one candidate (codes only)
-__device__ __forceinline__ void encode_scaled16(const float* y, float enc, uint32_t& w0, uint32_t& w1) {
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = mul_rn(y[i], enc);
-    w0 = e2m1_encode8(v);
-    w1 = e2m1_encode8(v + 8);
-}
-
 // One candidate over 8 values: codes of y * enc, and the per-element errors
 // |dq - y| (MAE) or (dq - y)^2 (MSE) of its error values dq = ((q*d)*A)/C.
 template <int ERR>
@@ -281,14 +272,6 @@ __device__ __forceinline__ void candidate16(const float* y, const Cand& c, float
                                             uint32_t& w0, uint32_t& w1, float* e) {
     candidate8<ERR>(y, c, d, A, C, w0, e);
     candidate8<ERR>(y + 8, c, d, A, C, w1, e + 8);
-}
-
-// sequential sum start + e[0] + ... + e[7]
-__device__ __forceinline__ float seq_sum8(float start, const float* e) {
-    float E = start;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) E = add_rn(E, e[i]);
-    return E;
 }
 
 // sequential sum e[0] + ... + e[15] from 0
