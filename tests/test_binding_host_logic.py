@@ -59,3 +59,17 @@ def test_device_checks_reject_wrong_tensors_before_any_cuda_call():
     t = torch.zeros(4, 16)
     with pytest.raises(ValueError):                     # not on the call's device
         nv._check_dev(t, "residual", torch.float32, 64, DEV)
+
+
+def test_pipelined_row_chunks_cover_the_rows_in_whole_tiles():
+    """The pipelined host path's chunks: at most eight, contiguous, covering
+    every row once, each starting on a multiple of 16 rows (whole 16x16
+    tiles, and the chunk's row_offset keeps the stochastic-rounding index)."""
+    for M in (256, 300, 1040, 4096, 14336, 16384, 16400):
+        ch = nv._row_chunks(M)
+        assert 1 <= len(ch) <= 8
+        assert ch[0][0] == 0 and ch[-1][1] == M
+        for (a, b), (c, _) in zip(ch, ch[1:]):
+            assert b == c
+        for a, b in ch:
+            assert a % 16 == 0 and b > a

@@ -287,6 +287,62 @@ def test_host_pageable_outputs_and_device_call_refusal():
         nv.nvfp4_quantize(to_dev(x), rounding="sr", residual=torch.zeros((64, 128)))
 
 
+def _host(x: np.ndarray, pinned: bool = True) -> torch.Tensor:
+    t = (torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16) if x.dtype == np.uint16
+         else torch.from_numpy(x.copy()))
+    return t.pin_memory() if pinned else t
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_host_pipelined_calls(dtype):
+    """Host calls of at least 256 rows run in row chunks on three streams
+    (copies in, kernels, copies out overlapping): every byte, the in-place
+    residual and the stochastic draws (keyed on row_offset + the chunk's
+    first row) must equal the oracle's for the whole tensor."""
+    M, K = 1040, 512                                   # chunks of 144 rows and a 32-row tail
+    x = mat((M, K), seed=81, dtype=dtype, outliers=0.01)
+    r0 = mat((M, K), seed=82) * np.float32(0.01)
+    for blk in ("1x16", "16x16"):
+        rh = _host(r0)
+        g = nv.nvfp4_quantize(_host(x), block=blk, rounding="sr", seed=7, step=3, row_offset=48,
+                              residual=rh)
+        assert g["codes"].device.type == "cpu"
+        ro = r0.copy()
+        o = oracle.quantize(x, block=oracle.BLOCK_16X16 if blk == "16x16" else oracle.BLOCK_1X16,
+                            rounding=oracle.SR, seed=7, step=3, row_offset=48, residual=ro)
+        assert_same(g["codes"].numpy(), o["codes"], f"{blk} codes")
+        assert_same(g["scales"].numpy(), o["scales"], f"{blk} scales")
+        assert_same(rh.numpy(), ro, f"{blk} residual")
+    ga = oracle.amax(x)
+    gr = oracle.amax(x, per_row=True)
+    for err in ("mae", "mse"):
+        for gm, gv, ogm in (("tensor_given", ga, oracle.GAMAX_TENSOR_GIVEN),
+                            ("row_given", gr, oracle.GAMAX_ROW_GIVEN)):
+            g = nv.nvfp4_quantize(_host(x, pinned=False), gamax_mode=gm, gamax=torch.from_numpy(gv.copy()),
+                                  err_mode=err, scale_bound=256.0)
+            o = oracle.quantize(x, gamax_mode=ogm, gamax=gv, err_mode=oracle.ERR_MAE if err == "mae"
+                                else oracle.ERR_MSE, scale_bound=256.0)
+            assert_same(g["codes"].numpy(), o["codes"], f"{err} {gm} codes")
+            assert_same(g["scales"].numpy(), o["scales"], f"{err} {gm} scales")
+    rh = _host(r0)
+    q = nv.nvfp4_qdq(_host(x), rounding="sr", seed=2, step=5, residual=rh, want_codes=True)
+    ro = r0.copy()
+    oq = oracle.qdq(x, rounding=oracle.SR, seed=2, step=5, residual=ro)
+    assert_same(q["out"].view(torch.int16).numpy().view(np.uint16), oq["out"], "qdq out")
+    assert_same(q["codes"].numpy(), oq["codes"], "qdq codes")
+    assert_same(rh.numpy(), ro, "qdq residual")
+    o = oracle.quantize(x, gamax_mode=oracle.GAMAX_TENSOR_GIVEN, gamax=ga, err_mode=oracle.ERR_MAE,
+                        scale_bound=256.0)
+    for od, ood in (("bf16", oracle.BF16), ("f32", oracle.F32)):
+        d = nv.nvfp4_dequantize(torch.from_numpy(o["codes"]), torch.from_numpy(o["scales"]), M, K,
+                                gamax_mode="tensor_given", gamax=torch.from_numpy(ga.copy()), scale_bound=256.0,
+                                out_dtype=od)
+        e = oracle.dequantize(o["codes"], o["scales"], M, K, gamax_mode=oracle.GAMAX_TENSOR_GIVEN, gamax=ga,
+                              scale_bound=256.0, out_dtype=ood)
+        dn = d.view(torch.int16).numpy().view(np.uint16) if od == "bf16" else d.numpy()
+        assert_same(dn, e, f"dequantize {od}")
+
+
 def test_stream_argument_is_honoured():
     x = to_dev(mat((256, 256), seed=13))
     s = torch.cuda.Stream()
