@@ -115,7 +115,15 @@ __device__ __forceinline__ void fill_recip_table(float* rt) {
 // values in q (nearest rounding leaves q alone).
 // get_words(wd) fills the 16 elements' stochastic-rounding words (called
 // only for stochastic rounding, where the words are needed).
-template <int RND, class GetWords>
+// BF16_E4: y is a bf16 input value (no residual added) and D a bare E4M3
+// scale (no global scale).  Then a nonzero y is at least 2^-133 (the least
+// bf16 subnormal) and D at most 448, so y / D is at least 2^-142 and the
+// reciprocal sequence's quotient is nonzero exactly when y is; below 2^-25 a
+// quotient's stochastic rounding depends on nothing else (the distance to
+// the grid, 2|q| * 2^24, is under 1, so it rounds up only on the zero draw,
+// and only if q != 0), and from 2^-25 up y is at least 2^-34, where the
+// sequence is exact.  So the tiny-element check is not needed.
+template <int RND, bool BF16_E4 = false, class GetWords>
 __device__ __forceinline__ void encode_plain16_impl(const float* y, float D, float b, GetWords get_words,
                                                     uint32_t& w0, uint32_t& w1, const float* rt,
                                                     uint32_t sf, float* q, bool wq) {
@@ -133,8 +141,10 @@ __device__ __forceinline__ void encode_plain16_impl(const float* y, float D, flo
         get_words(wd);
         // blocks holding an element 0 < |y| < 2^-80 (or zeros) take the per-element checked path
         bool tiny = false;
+        if (!BF16_E4) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) tiny |= fabsf(y[i]) < 8.271806125530277e-25f;
+            for (int i = 0; i < 16; ++i) tiny |= fabsf(y[i]) < 8.271806125530277e-25f;
+        }
         float g[16];
         if (fast && !tiny) {
             const uint64_t R2 = pack2(r, r), ND2 = pack2(-D, -D);
@@ -176,21 +186,21 @@ __device__ __forceinline__ void encode_plain16_impl(const float* y, float D, flo
 }
 
 // elements idx0 .. idx0 + 15 of x (the stochastic-rounding counter)
-template <int RND>
+template <int RND, bool BF16_E4 = false>
 __device__ __forceinline__ void encode_plain16(const float* y, float D, float b, uint64_t idx0,
                                                const PhiloxKeys& pk, uint32_t& w0,
                                                uint32_t& w1, const float* rt, uint32_t sf,
                                                float* q, bool wq) {
-    encode_plain16_impl<RND>(
+    encode_plain16_impl<RND, BF16_E4>(
         y, D, b, [&](uint32_t* wd) { sr_words16(idx0, pk, wd); }, w0, w1, rt, sf, q, wq);
 }
 
 // the same with the words given (wd[16], read only for stochastic rounding)
-template <int RND>
+template <int RND, bool BF16_E4 = false>
 __device__ __forceinline__ void encode_plain16_words(const float* y, float D, float b, const uint32_t* wd,
                                                      uint32_t& w0, uint32_t& w1, const float* rt,
                                                      uint32_t sf, float* q, bool wq) {
-    encode_plain16_impl<RND>(
+    encode_plain16_impl<RND, BF16_E4>(
         y, D, b,
         [&](uint32_t* out) {
 #pragma unroll

@@ -64,10 +64,11 @@ __device__ __forceinline__ void rows_block(const QuantArgs& a, int64_t blk, bool
         sf = e4m3_encode(min_nd(s6f, 448.0f));
         d = e4m3_decode(sf);
         const float D = GS ? mul_rn(d, gb.Sdec) : d;
+        constexpr bool BF16_E4 = DT == NVFP4_BF16 && !EF && !GS;   // y a bf16 input, D an E4M3 scale
         if constexpr (EARLY)
-            encode_plain16_words<RND>(y, D, b, wd, w0, w1, GS ? nullptr : rt, sf, q, wq);
+            encode_plain16_words<RND, BF16_E4>(y, D, b, wd, w0, w1, GS ? nullptr : rt, sf, q, wq);
         else
-            encode_plain16<RND>(y, D, b, idx0, a.pk, w0, w1, GS ? nullptr : rt, sf, q, wq);
+            encode_plain16<RND, BF16_E4>(y, D, b, idx0, a.pk, w0, w1, GS ? nullptr : rt, sf, q, wq);
     } else {
         four_over_six16<ERR, std::is_same<TileAmax, OwnAmax>::value>(y, b, gb, C, tab, w0, w1, sf, d, tile_sums);
     }

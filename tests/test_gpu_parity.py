@@ -187,6 +187,23 @@ def test_subnormal_and_large_plain_scales():
         compare_quant(gpu, o)
 
 
+@pytest.mark.parametrize("block", ["1x16", "16x16"])
+def test_sr_bf16_tiny_values(block):
+    """Stochastic rounding of bf16 input without a residual or a global scale
+    skips the tiny-element check (a nonzero bf16 value over an E4M3 scale
+    never gives a zero quotient): blocks mixing bf16 subnormals, zeros and
+    values up to 2^20 must still match the oracle, draw for draw."""
+    rng = np.random.default_rng(91)
+    x = rng.standard_normal((256, 512)).astype(np.float32)
+    x *= np.exp2(rng.integers(-140, 20, (256, 512))).astype(np.float32)
+    x[rng.random(x.shape) < 0.05] = 0.0
+    x[:, :16] = np.float32(2.0 ** -133) * rng.integers(-3, 4, (256, 16)).astype(np.float32)
+    xb = W.to_bf16_bits(x)
+    for seed, step in ((1, 0), (2, 7)):
+        gpu, o = quantize_both(xb, block=block, rounding="sr", seed=seed, step=step)
+        compare_quant(gpu, o)
+
+
 def test_dequantize_global_modes():
     x = mat((128, 256), seed=5, outliers=0.05)
     for gm, given in (("tensor", "tensor_given"), ("row", "row_given")):
