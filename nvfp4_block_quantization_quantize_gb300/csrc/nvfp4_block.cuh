@@ -131,9 +131,24 @@ __device__ __forceinline__ void encode_plain16_impl(const float* y, float D, flo
     const float r = rt ? rt[sf] : (fast ? div_rn(1.0f, D) : 0.0f);
     if (RND != NVFP4_SR) {                      // nearest (either scale association)
         float v[16];
+        if (fast) {                             // the reciprocal sequence on pairs (per-lane IEEE)
+            const uint64_t R2 = pack2(r, r), ND2 = pack2(-D, -D);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            v[i] = rt ? plain_quotient<false, true>(y[i], D, r, fast) : plain_quotient<false>(y[i], D, r, fast);
+            for (int i = 0; i < 16; i += 2) {
+                const uint64_t Y = pack2(y[i], y[i + 1]);
+                const uint64_t Q0 = mul2(Y, R2);
+                uint64_t Q = fma2(fma2(Q0, ND2, Y), R2, Q0);
+                if (!rt) Q = fma2(fma2(Q, ND2, Y), R2, Q);
+                float q0a, q0b, qa, qb;
+                unpack2(Q0, q0a, q0b);
+                unpack2(Q, qa, qb);
+                v[i] = sign_of_first(q0a, qa);
+                v[i + 1] = sign_of_first(q0b, qb);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = plain_quotient<false>(y[i], D, r, false);
+        }
         w0 = e2m1_encode8(v);
         w1 = e2m1_encode8(v + 8);
     } else {
