@@ -458,7 +458,8 @@ __device__ __forceinline__ bool tile_sums_decide(float S6, float S4, float K6, f
 }
 
 // CERT (a 1x16 block, whose error sums are its own): the sums come from
-// errsum16_approx wherever approx_decides, from the table otherwise.
+// errsum16_approx wherever approx_decides, otherwise from the table
+// (per-tensor scale) or the per-block exact form (per-row scale).
 template <int ERR, bool CERT = false, class TileSums>
 __device__ __forceinline__ void four_over_six16(const float* y, float b, const GScale& g, float C,
                                                 const O6Tab* tab, uint32_t& w0, uint32_t& w1,
@@ -482,6 +483,21 @@ __device__ __forceinline__ void four_over_six16(const float* y, float b, const G
         E6 = seq_sum16(e);
         candidate16_tab<ERR>(y, tab->enc[sf4], tab->dq + sf4, b0, b1, e);
         E4 = seq_sum16(e);
+    } else if (CERT) {                          // per-row global scale, 1x16, certified
+        // K and enc as make_cand's X1 and enc (the error value of grid value
+        // 1, and the encode reciprocal); the exact form only where undecided
+        const float K6 = div_rn(mul_rn(d6, g.A), C), K4 = div_rn(mul_rn(d4, g.A), C);
+        const float enc6 = min_nd(div_rn(1.0f, mul_rn(d6, g.Sdec)), FLT_MAX);
+        const float enc4 = min_nd(div_rn(1.0f, mul_rn(d4, g.Sdec)), FLT_MAX);
+        E6 = errsum16_approx<ERR>(y, enc6, K6, a0, a1);
+        E4 = errsum16_approx<ERR>(y, enc4, K4, b0, b1);
+        if (!approx_decides<ERR>(E6, E4, K6, K4)) {
+            const Cand c6 = make_cand(sf6, g.Sdec, g.A, C), c4 = make_cand(sf4, g.Sdec, g.A, C);
+            candidate16<ERR>(y, c6, d6, g.A, C, a0, a1, e);
+            E6 = seq_sum16(e);
+            candidate16<ERR>(y, c4, d4, g.A, C, b0, b1, e);
+            E4 = seq_sum16(e);
+        }
     } else {                                    // per-row global scale: candidates per block
         const Cand c6 = make_cand(sf6, g.Sdec, g.A, C), c4 = make_cand(sf4, g.Sdec, g.A, C);
         candidate16<ERR>(y, c6, d6, g.A, C, a0, a1, e);
