@@ -234,6 +234,18 @@ int nvfp4_mm(const uint8_t* codes_a, const uint8_t* scales_a, const uint8_t* cod
 int nvfp4_probe_divide(const float* a, const float* b, float* out, int64_t n, cudaStream_t stream);
 
 /*
+ * nvfp4_probe_sub_f16 -- diagnostic.  For i < n, out[2i] and out[2i+1] are the
+ * low and high f16 halves of q[i] minus v[2i] and v[2i+1], each rounded once to
+ * fp32 by the mixed-precision subtract the certified four-over-six error sums
+ * use (the grid value of a code, decoded to f16, minus the scaled value the
+ * encode rounded; "Add NVFP4 four-over-six (row-wise) quantization to the
+ * training prototype", Design: the candidates' errors).  Device pointers: q
+ * n words, v and out 2n floats, 4-byte aligned; EINVAL on bad arguments.  It
+ * exists so the rounding the sums' error bound assumes can be checked.
+ */
+int nvfp4_probe_sub_f16(const uint32_t* q, const float* v, float* out, int64_t n, cudaStream_t stream);
+
+/*
  * nvfp4_probe_e2m1 -- diagnostic.  The e2m1 codes that the quantizers' element
  * encode ("fp4-train", Method: each value rounded to the signed grid
  * {0,.5,1,1.5,2,3,4,6}; "Add NVFP4 four-over-six (row-wise) quantization to

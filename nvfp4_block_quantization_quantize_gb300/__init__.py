@@ -45,7 +45,7 @@ _NAMES = {
 }
 
 EXPORTED = ("nvfp4_quantize", "nvfp4_dequantize", "nvfp4_qdq", "nvfp4_amax",
-            "nvfp4_global_scales", "nvfp4_probe_divide", "nvfp4_probe_e2m1", "nvfp4_last_error",
+            "nvfp4_global_scales", "nvfp4_probe_divide", "nvfp4_probe_e2m1", "nvfp4_probe_sub_f16", "nvfp4_last_error",
             "nvfp4_abi_version")
 
 _lock = threading.Lock()
@@ -85,6 +85,8 @@ def load_library(path: str | None = None):
         lib.nvfp4_amax.argtypes = [P, i64, i64, i32, P, i32, P, P]
         lib.nvfp4_probe_divide.restype = i32
         lib.nvfp4_probe_divide.argtypes = [P, P, P, i64, P]
+        lib.nvfp4_probe_sub_f16.restype = i32
+        lib.nvfp4_probe_sub_f16.argtypes = [P, P, P, i64, P]
         lib.nvfp4_global_scales.restype = i32
         lib.nvfp4_global_scales.argtypes = [P, i64, f32, P, P, P]
         lib.nvfp4_probe_e2m1.restype = i32
@@ -692,6 +694,19 @@ def nvfp4_probe_divide(a: torch.Tensor, b: torch.Tensor, stream=None) -> torch.T
     b = b.contiguous()
     out = torch.empty_like(a)
     _check(lib, lib.nvfp4_probe_divide(_ptr(a), _ptr(b), _ptr(out), a.numel(), _stream(stream)))
+    return out
+
+
+def nvfp4_probe_sub_f16(q: torch.Tensor, v: torch.Tensor, stream=None) -> torch.Tensor:
+    """Diagnostic: f16 halves of the int32 words q minus the float32 pairs v,
+    rounded once (float32 [2 * q.numel()])."""
+    lib = load_library()
+    q = q.contiguous()
+    v = v.contiguous()
+    if q.dtype != torch.int32 or v.dtype != torch.float32 or v.numel() != 2 * q.numel():
+        raise ValueError("nvfp4: q must be int32 words and v float32 with two values per word")
+    out = torch.empty_like(v)
+    _check(lib, lib.nvfp4_probe_sub_f16(_ptr(q), _ptr(v), _ptr(out), q.numel(), _stream(stream)))
     return out
 
 

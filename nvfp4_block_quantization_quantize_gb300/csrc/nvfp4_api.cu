@@ -251,6 +251,18 @@ int nvfp4_probe_divide(const float* a, const float* b, float* out, int64_t n, cu
     return NVFP4_OK;
 }
 
+int nvfp4_probe_sub_f16(const uint32_t* q, const float* v, float* out, int64_t n, cudaStream_t stream) {
+    g_msg[0] = '\0';
+    if (n < 0) return fail(NVFP4_EINVAL, "n must be >= 0");
+    int rc;
+    if ((rc = check_ptr(q, "q", n > 0, 4))) return rc;
+    if ((rc = check_ptr(v, "v", n > 0, 4))) return rc;
+    if ((rc = check_ptr(out, "out", n > 0, 4))) return rc;
+    const int err = nvfp4::launch_probe_sub_f16(q, v, out, n, stream);
+    if (err) return cuda_fail(err, "probe launch");
+    return NVFP4_OK;
+}
+
 int nvfp4_probe_e2m1(uint32_t first, int64_t n, uint8_t* out, cudaStream_t stream) {
     g_msg[0] = '\0';
     if (n < 0 || n > (int64_t{1} << 32)) return fail(NVFP4_EINVAL, "n must be in [0, 2^32]");

@@ -232,6 +232,21 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DequantArgs a) {
 // out[i] = the plain path's division a[i] / b[i] (its exact, stochastic-
 // rounding form), with the block amax taken as |a[i]|; an E4M3-valued divisor
 // takes the one-step form the kernels use without a global scale.
+// out[2i], out[2i+1] = the two f16 halves of q[i] minus v[2i], v[2i+1], as
+// the certified four-over-six sums take them
+__global__ void __launch_bounds__(kThreads) k_probe_sub_f16(const uint32_t* q, const float* v, float* out,
+                                                            int64_t n) {
+    pdl_wait();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        float d0, d1;
+        sub_f16x2_f32(q[i], v[2 * i], v[2 * i + 1], d0, d1);
+        out[2 * i] = d0;
+        out[2 * i + 1] = d1;
+    }
+    pdl_trigger();
+}
+
 __global__ void __launch_bounds__(kThreads) k_probe_divide(const float* a, const float* b,
                                                            float* out, int64_t n) {
     pdl_wait();
@@ -369,6 +384,13 @@ int launch_scales_mma(const uint8_t* in, int64_t rows, int64_t cols, uint8_t* ou
     if (n <= 0) return 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     launch_pdl(k_scales_mma, grid_for(n), kThreads, 0, s, in, rows, cols, R, C4, reinterpret_cast<uint32_t*>(out));
+    return static_cast<int>(cudaGetLastError());
+}
+
+int launch_probe_sub_f16(const uint32_t* q, const float* v, float* out, int64_t n, void* stream) {
+    if (n <= 0) return 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    launch_pdl(k_probe_sub_f16, grid_for(n), kThreads, 0, s, q, v, out, n);
     return static_cast<int>(cudaGetLastError());
 }
 

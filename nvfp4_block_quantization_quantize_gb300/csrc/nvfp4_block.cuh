@@ -369,92 +369,98 @@ __device__ __forceinline__ float errsum16_tab(const float* y, uint32_t w0, uint3
     return E;
 }
 
-// Approximate error sum of one candidate, no table lookups: a code of grid
-// value q (signed like its y) stands for q * K, K = the error value of q = 1
-// (((1 * d) * A) / C), so an element's error is |y - q * K| from one fused
-// multiply-add (squared for MSE), summed in element order.  The codes are
-// the candidate's exact codes.
+// Approximate error sum of one candidate, no table lookups, in the scaled
+// domain: v = RN(y * enc) is the value the encode rounds to a grid value q
+// (signed like y), an element's approximate error is |RN(q - v)| (one mixed
+// f16/f32 subtract; squared for MSE), summed in element order, and the sum
+// S' is scaled back by K, the error value of grid value 1 (((1 * d) * A) /
+// C): E^ = RN(K * S'), or RN(RN(K * K) * S') for MSE.  The codes are the
+// candidate's exact codes.
 template <int ERR>
 __device__ __forceinline__ float errsum16_approx(const float* y, float enc, float K, uint32_t& w0,
                                                  uint32_t& w1) {
     float v[16];
-    const uint64_t ENC2 = pack2(enc, enc), NK2 = pack2(-K, -K);
+    const uint64_t ENC2 = pack2(enc, enc);
 #pragma unroll
     for (int i = 0; i < 16; i += 2) unpack2(mul2(pack2(y[i], y[i + 1]), ENC2), v[i], v[i + 1]);
     uint32_t h[8];
     w0 = e2m1_encode8_dec(v, h);
     w1 = e2m1_encode8_dec(v + 8, h + 4);
-    float E = 0.0f;
+    float S = 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const float q0 = __half2float(__ushort_as_half(static_cast<unsigned short>(h[j] & 0xFFFFu)));
-        const float q1 = __half2float(__ushort_as_half(static_cast<unsigned short>(h[j] >> 16)));
-        uint64_t D = fma2(pack2(q0, q1), NK2, pack2(y[2 * j], y[2 * j + 1]));   // y - q * K
-        if (ERR == NVFP4_ERR_MSE) D = mul2(D, D);
         float e0, e1;
-        unpack2(D, e0, e1);
-        E = add_rn(E, fabsf(e0));
-        E = add_rn(E, fabsf(e1));
+        sub_f16x2_f32(h[j], v[2 * j], v[2 * j + 1], e0, e1);
+        if (ERR == NVFP4_ERR_MSE) {
+            const uint64_t D = pack2(e0, e1);
+            unpack2(mul2(D, D), e0, e1);
+        }
+        S = add_rn(S, fabsf(e0));
+        S = add_rn(S, fabsf(e1));
     }
-    return E;
+    return ERR == NVFP4_ERR_MAE ? mul_rn(K, S) : mul_rn(mul_rn(K, K), S);
 }
 
-// Whether approximate sums S6, S4 (errsum16_approx) decide E4 < E6 as the
-// exact sums E6, E4 do.  With u = 2^-24, K_r = d*A/C and q an element's grid
-// value (|q| <= 6): an error value dq = ((q*d)*A)/C (q*d exact, two
-// roundings) lies within (2u + u^2)|q| K_r of |q| K_r, and K (the same two
-// roundings) within as much of K_r, so |dq - |q| K| <= 4.02u |q| K.  The
-// differences d_t = dq - |y| and d_a = y - q*K are each rounded once, so
-// ||d_t| - |d_a|| <= 4.02u |q| K + u (|d_t| + |d_a|) (1 + u).
-//   MAE: summing over the block and adding gamma_15 <= 15.01u of each
-//   element-order sum, |E - S| <= 386u K + 32.1u S (to first order in u).
-//   MSE: |d_t^2 - d_a^2| = ||d_t| - |d_a|| (|d_t| + |d_a|), the squares'
-//   roundings add u each, and sum |d| <= 4 sqrt(sum d^2) over 16 terms, so
-//   |E - S| <= 193u K sqrt(S) + 36u S.
-// The threshold is twice these bounds with the constants rounded up to
-// powers of two (2^9 u K + 2^6 u S, and 2^8 u K sqrt(S) + 2^6 u S per
-// candidate), plus 2^-120 for the absolute errors of subnormal results.
-// K sqrt(S) is bounded without a square root by the AM-GM inequality,
-// K sqrt(S) <= (S + K^2) / 2 (close, since S is of the order of K^2).  A NaN
-// or infinite sum or K gives a NaN difference or an infinite threshold: the
-// test fails and the caller takes the exact sums.
+// Whether approximate sums E6^, E4^ (errsum16_approx) decide E4 < E6 as the
+// exact sums E6, E4 do.  With u = 2^-24, K_r = d*A/C, q an element's grid
+// value (|q| <= 6) and b the block amax (>= |y|):
+//   an error value dq = ((q*d)*A)/C (q*d exact, two roundings) lies within
+//   2.01u |q| K_r of |q| K_r, and its difference with |y| is rounded once;
+//   v = y * enc with enc = RN(1 / RN(d * S_dec)) and S_dec = RN(1 / RN(C / A))
+//   is y / K_r within 5.05u |y| / K_r, q - v is rounded once, the sums in
+//   element order add gamma_15 <= 15.01u of their terms, and K * S' (K within
+//   2.01u of K_r) adds 3.02u:
+//   MAE  |E - E^| <= 35.04u E^ + 193u K + 80.8u b   (sum |q| <= 96, sum |y| <= 16 b);
+//   MSE  |d_t^2 - (K_r d_a)^2| = ||d_t| - K_r|d_a|| (|d_t| + K_r|d_a|), with the
+//        first factor <= 12.06u K + 5.05u b + u (|d_t| + K_r|d_a|) and sum |d|
+//        <= 4 sqrt(sum d^2) over 16 terms:
+//        |E - E^| <= 96.5u K sqrt(E^) + 40.4u b sqrt(E^) + 42u E^.
+// Per candidate, with the constants rounded up to powers of two,
+// 2^6 u E^ + 2^8 u K + 2^7 u b and 2^7 u K sqrt(E^) + 2^6 u b sqrt(E^) +
+// 2^6 u E^; the threshold is twice the two candidates' bounds together plus
+// 2^-120 for the absolute errors of subnormal results, with the square roots
+// bounded by the AM-GM inequality: K sqrt(E^) <= (E^ + K^2) / 2 and
+// b sqrt(E^) <= 3 E^ + b^2 / 12.  A NaN or infinite sum, K or b gives a NaN
+// difference or an infinite threshold: the test fails and the caller takes
+// the exact sums.
 template <int ERR>
-__device__ __forceinline__ bool approx_decides(float S6, float S4, float K6, float K4) {
+__device__ __forceinline__ bool approx_decides(float E6, float E4, float K6, float K4, float b) {
     float T;
     if (ERR == NVFP4_ERR_MAE) {
-        T = add_rn(mul_rn(add_rn(K6, K4), 6.103515625e-05f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
+        T = add_rn(mul_rn(add_rn(E6, E4), 7.62939453125e-06f),
+                   mul_rn(add_rn(add_rn(K6, K4), b), 3.0517578125e-05f));
     } else {
-        const float R = add_rn(__fmaf_rn(K6, K6, S6), __fmaf_rn(K4, K4, S4));   // 2 * (K sqrt(S)) bound
-        T = add_rn(mul_rn(R, 1.52587890625e-05f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
+        const float R = add_rn(add_rn(mul_rn(5.0f, add_rn(E6, E4)), __fmaf_rn(K6, K6, mul_rn(K4, K4))),
+                               mul_rn(mul_rn(b, b), 0.1875f));
+        T = mul_rn(R, 7.62939453125e-06f);
     }
     T = add_rn(T, 7.52316384526264e-37f);
-    return fabsf(sub_rn(S6, S4)) > T;
+    return fabsf(sub_rn(E6, E4)) > T;
 }
 
-// Four-over-six for one 16-value group (1x16 block, or one row of a 16x16 tile
-// when TREE: the row error sums are combined over the half warp).
-// tile_sums(E6, E4) turns one group's error sums into its block's: nothing for
-// a 1x16 block, the width-16 tree over the tile's 16 rows for a 16x16 tile.
 // The same test for a 16x16 tile's sums over its 256 elements (rowwise: the
 // width-16 tree of the rows' element-order sums; columnwise: of the
 // columns'), each element's error passing at most 15 + 4 additions: with
-// sum |q| <= 1536 and gamma_19, |E - S| <= 6175u K + 40u S for MAE and, with
-// sum |d| <= 16 sqrt(sum d^2) over 256 terms, <= 772u K sqrt(S) + 44u S for
-// MSE; per candidate 2^13 u K + 2^6 u S and 2^10 u K sqrt(S) + 2^6 u S, and
-// the threshold twice the two candidates' bounds together plus 2^-120, with
-// K sqrt(S) <= (S + 16 K^2) / 8 (AM-GM; a tile's S is of the order of 16 K^2).
+// sum |q| <= 1536, sum |y| <= 256 b and gamma_19, |E - E^| <= 43.04u E^ +
+// 3087u K + 1293u b for MAE and, with sum |d| <= 16 sqrt(sum d^2) over 256
+// terms, <= 386u K sqrt(E^) + 162u b sqrt(E^) + 50u E^ for MSE; per
+// candidate 2^6 u E^ + 2^12 u K + 2^11 u b and 2^9 u K sqrt(E^) + 2^8 u b
+// sqrt(E^) + 2^6 u E^, the threshold twice the two candidates' bounds
+// together plus 2^-120, with K sqrt(E^) <= (E^ + 16 K^2) / 8 and
+// b sqrt(E^) <= (E^ + b^2) / 2.
 template <int ERR>
-__device__ __forceinline__ bool tile_sums_decide(float S6, float S4, float K6, float K4) {
+__device__ __forceinline__ bool tile_sums_decide(float E6, float E4, float K6, float K4, float b) {
     float T;
     if (ERR == NVFP4_ERR_MAE) {
-        T = add_rn(mul_rn(add_rn(K6, K4), 9.765625e-04f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
+        T = add_rn(mul_rn(add_rn(E6, E4), 7.62939453125e-06f),
+                   mul_rn(add_rn(add_rn(K6, K4), b), 4.8828125e-04f));
     } else {
-        const float K6s = mul_rn(4.0f, K6), K4s = mul_rn(4.0f, K4);
-        const float R = add_rn(__fmaf_rn(K6s, K6s, S6), __fmaf_rn(K4s, K4s, S4));   // 8 * (K sqrt(S)) bound
-        T = add_rn(mul_rn(R, 1.52587890625e-05f), mul_rn(add_rn(S6, S4), 7.62939453125e-06f));
+        const float R = add_rn(add_rn(add_rn(E6, E4), mul_rn(4.0f, __fmaf_rn(K6, K6, mul_rn(K4, K4)))),
+                               mul_rn(b, b));
+        T = mul_rn(R, 3.0517578125e-05f);
     }
     T = add_rn(T, 7.52316384526264e-37f);
-    return fabsf(sub_rn(S6, S4)) > T;
+    return fabsf(sub_rn(E6, E4)) > T;
 }
 
 // CERT (a 1x16 block, whose error sums are its own): the sums come from
@@ -474,7 +480,7 @@ __device__ __forceinline__ void four_over_six16(const float* y, float b, const G
         const float K6 = tab->dq[2 * kDqStride + sf6], K4 = tab->dq[2 * kDqStride + sf4];
         E6 = errsum16_approx<ERR>(y, tab->enc[sf6], K6, a0, a1);
         E4 = errsum16_approx<ERR>(y, tab->enc[sf4], K4, b0, b1);
-        if (!approx_decides<ERR>(E6, E4, K6, K4)) {
+        if (!approx_decides<ERR>(E6, E4, K6, K4, b)) {
             E6 = errsum16_tab<ERR>(y, a0, a1, tab->dq + sf6);
             E4 = errsum16_tab<ERR>(y, b0, b1, tab->dq + sf4);
         }
@@ -491,7 +497,7 @@ __device__ __forceinline__ void four_over_six16(const float* y, float b, const G
         const float enc4 = min_nd(div_rn(1.0f, mul_rn(d4, g.Sdec)), FLT_MAX);
         E6 = errsum16_approx<ERR>(y, enc6, K6, a0, a1);
         E4 = errsum16_approx<ERR>(y, enc4, K4, b0, b1);
-        if (!approx_decides<ERR>(E6, E4, K6, K4)) {
+        if (!approx_decides<ERR>(E6, E4, K6, K4, b)) {
             const Cand c6 = make_cand(sf6, g.Sdec, g.A, C), c4 = make_cand(sf4, g.Sdec, g.A, C);
             candidate16<ERR>(y, c6, d6, g.A, C, a0, a1, e);
             E6 = seq_sum16(e);

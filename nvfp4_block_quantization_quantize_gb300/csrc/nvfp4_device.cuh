@@ -277,6 +277,16 @@ __device__ __forceinline__ Cand make_cand(uint32_t sf, float Sdec, float A, floa
     return c;
 }
 
+// q - v for the two halves of an f16 pair q (a code pair's grid values) and
+// two fp32 values v, each rounded once to fp32: the mixed-precision subtract
+// takes its f16 operand exactly (no separate conversion).
+__device__ __forceinline__ void sub_f16x2_f32(uint32_t q, float v0, float v1, float& d0, float& d1) {
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "sub.rn.f32.f16 %0, lo, %3;\n\tsub.rn.f32.f16 %1, hi, %4;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(q), "f"(v0), "f"(v1));
+}
+
 // Eight values -> eight 4-bit codes (as e2m1_encode8) AND the codes' grid
 // values as four f16 pairs, each byte decoded straight from the register the
 // encode wrote.

@@ -79,6 +79,7 @@ int launch_mm(const uint8_t* A, const uint8_t* SA, const uint8_t* B, const uint8
 int launch_amax(const void* x, int64_t M, int64_t K, int dtype, const float* residual, int mode,
                 float* out, void* stream);
 int launch_probe_divide(const float* a, const float* b, float* out, int64_t n, void* stream);
+int launch_probe_sub_f16(const uint32_t* q, const float* v, float* out, int64_t n, void* stream);
 int launch_probe_e2m1(uint32_t first, int64_t n, uint8_t* out, void* stream);
 int launch_global_scales(const float* gamax, int64_t n, float bound, float* s_enc, float* s_dec, void* stream);
 int sm_count();

@@ -346,29 +346,30 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
         // K: the error value of grid value 1, ((1 * d) * A) / (6 * bound)
         const float K6 = div_rn(mul_rn(d6, g.A), C), K4 = div_rn(mul_rn(d4, g.A), C);
 
-        // pass 1: both candidates' codes, and approximate per-element errors
-        // |y - q K| (squared for MSE; q the code's signed grid value, so this is
-        // | |q| K - |y| |) with no table lookup; row sums to shared memory,
-        // column sums in registers, both accumulated in element order
+        // pass 1: both candidates' codes, and approximate per-element errors in
+        // the scaled domain, |q - v| with v = y * enc (squared for MSE; q the
+        // code's signed grid value) from one mixed f16/f32 subtract, no table
+        // lookup; row sums to shared memory, column sums in registers, both
+        // accumulated in element order and scaled back by K (K^2 for MSE) at
+        // the end
         float F6[16], F4[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
         const uint64_t ENC6 = pack2(enc6, enc6), ENC4 = pack2(enc4, enc4);
-        auto candidate = [&](const float* y, uint64_t enc2, float K, uint32_t& w0, uint32_t& w1, float* e) {
+        auto candidate = [&](const float* y, uint64_t enc2, uint32_t& w0, uint32_t& w1, float* e) {
             float v[16];
 #pragma unroll
             for (int i = 0; i < 16; i += 2) unpack2(mul2(pack2(y[i], y[i + 1]), enc2), v[i], v[i + 1]);
             uint32_t h[8];
             w0 = e2m1_encode8_dec(v, h);
             w1 = e2m1_encode8_dec(v + 8, h + 4);
-            const uint64_t NK2 = pack2(-K, -K);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const float q0 = __half2float(__ushort_as_half(static_cast<unsigned short>(h[j] & 0xFFFFu)));
-                const float q1 = __half2float(__ushort_as_half(static_cast<unsigned short>(h[j] >> 16)));
-                uint64_t D = fma2(pack2(q0, q1), NK2, pack2(y[2 * j], y[2 * j + 1]));
-                if (ERR != NVFP4_ERR_MAE) D = mul2(D, D);
-                unpack2(D, e[2 * j], e[2 * j + 1]);
+                sub_f16x2_f32(h[j], v[2 * j], v[2 * j + 1], e[2 * j], e[2 * j + 1]);
+                if (ERR != NVFP4_ERR_MAE) {
+                    const uint64_t D = pack2(e[2 * j], e[2 * j + 1]);
+                    unpack2(mul2(D, D), e[2 * j], e[2 * j + 1]);
+                }
             }
             if (ERR == NVFP4_ERR_MAE) {
 #pragma unroll
@@ -398,12 +399,12 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             next_row(16 + r, y);
             float e[16];
             uint32_t w0, w1;
-            candidate(y, ENC6, K6, w0, w1, e);
+            candidate(y, ENC6, w0, w1, e);
             sW[0][r][tid] = w0;
             sW[1][r][tid] = w1;
             const float R6 = seq_sum16(e);
             col_sums(F6, e);
-            candidate(y, ENC4, K4, w0, w1, e);
+            candidate(y, ENC4, w0, w1, e);
             sW[2][r][tid] = w0;
             sW[3][r][tid] = w1;
             const float R4 = seq_sum16(e);
@@ -424,7 +425,15 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             E4c = tree16_regs(F4);
         };
         tree_sums();
-        if (!(tile_sums_decide<ERR>(E6r, E4r, K6, K4) && tile_sums_decide<ERR>(E6c, E4c, K6, K4))) {
+        {   // back from the scaled domain: E^ = RN(K * S'), or RN(RN(K * K) * S')
+            const float k6 = ERR == NVFP4_ERR_MAE ? K6 : mul_rn(K6, K6);
+            const float k4 = ERR == NVFP4_ERR_MAE ? K4 : mul_rn(K4, K4);
+            E6r = mul_rn(k6, E6r);
+            E6c = mul_rn(k6, E6c);
+            E4r = mul_rn(k4, E4r);
+            E4c = mul_rn(k4, E4c);
+        }
+        if (!(tile_sums_decide<ERR>(E6r, E4r, K6, K4, b) && tile_sums_decide<ERR>(E6c, E4c, K6, K4, b))) {
             // the exact sums: error values |dq| = ((G[k] * d) * A) / (6 * bound)
             // of each grid magnitude G[k] from a per-thread table (a code of
             // index k stands for +-|dq| with the sign of its y, so |dq - y| =

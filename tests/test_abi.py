@@ -160,6 +160,15 @@ def test_probe_e2m1_rejects(lib):
     assert f(0, 0, None, None) == 0
 
 
+def test_probe_sub_f16_rejects(lib):
+    f = lib.nvfp4_probe_sub_f16
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    assert f(A16, A16, A16, -1, None) == 1
+    assert f(None, A16, A16, 4, None) == 1
+    assert f(A16, ctypes.c_void_p(0x10002), A16, 4, None) == 1          # misaligned
+    assert f(None, None, None, 0, None) == 0
+
+
 def test_scales_to_mma_rejects(lib):
     f = lib.nvfp4_scales_to_mma
     f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]

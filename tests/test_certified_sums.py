@@ -1,26 +1,28 @@
 """The certified four-over-six error sums, checked on the CPU.
 
-With a per-tensor global scale the kernels first form approximate error sums
-S (a code of grid value q stands for q*K, K the error value of grid value 1,
-so an element's error is |y - q*K| from one fused multiply-add) and accept
-the comparison of the approximations only when it is separated by more than
-a rounding bound; otherwise they take the exact table sums.  The outputs
-are the method's as long as |E - S| <= B for every candidate, E the method's
+With a global scale the kernels first form approximate error sums in the
+scaled domain: v = RN(y * enc) is the value the encode rounds to a grid
+value q (signed like y), an element's approximate error is |RN(q - v)|
+(squared for MSE), and the block's (or tile's) sum S' of those, in the
+method's summation order, is scaled back by K (K^2 for MSE), K the error
+value of grid value 1, ((1 * d) * A) / C: E^ = RN(K * S').  The comparison of
+the two candidates' E^ is accepted only when it is separated by more than a
+rounding bound; otherwise the kernels take the exact sums.  The outputs are
+the method's as long as |E - E^| <= B for every candidate, E the method's
 error sum ("Add NVFP4 four-over-six (row-wise) quantization to the training
 prototype", Two load-bearing numeric details: error values ((q*d)*A)/C,
-element-order sums, the width-16 tree).  This test computes both sums in
-IEEE fp32 (numpy float32 arithmetic; the fused multiply-add rounded once
-from its exact rational value) on many blocks and tiles and checks the
+element-order sums, the width-16 tree).  This test computes both in IEEE
+fp32 (numpy float32 arithmetic) on many blocks and tiles and checks the
 per-candidate bounds the kernels' thresholds are built from (the threshold
-is twice the two candidates' bounds together):
+is twice the two candidates' bounds together), b the block's amax:
 
-  1x16 MAE  2^-15 K + 2^-18 S          1x16 MSE  2^-16 K sqrt(S) + 2^-18 S
-  tile MAE  2^-11 K + 2^-18 S          tile MSE  2^-14 K sqrt(S) + 2^-18 S
+  1x16 MAE  2^-18 E^ + 2^-16 K + 2^-17 b
+  1x16 MSE  2^-17 K sqrt(E^) + 2^-18 b sqrt(E^) + 2^-18 E^
+  tile MAE  2^-18 E^ + 2^-12 K + 2^-13 b
+  tile MSE  2^-15 K sqrt(E^) + 2^-16 b sqrt(E^) + 2^-18 E^
 
 each plus 2^-121 for subnormal results.
 """
-from fractions import Fraction
-
 import numpy as np
 import pytest
 
@@ -28,25 +30,6 @@ import oracle
 
 f32 = np.float32
 FLT_MAX = f32(3.4028234663852886e38)
-
-
-def _rn32(fr: Fraction) -> np.float32:
-    """fp32 round-to-nearest-even of an exact rational."""
-    x = f32(float(fr))                       # near; fixed up below
-    best = x
-    for cand in (np.nextafter(x, f32(-np.inf)), np.nextafter(x, f32(np.inf))):
-        if not np.isfinite(cand):
-            continue
-        dc, db = abs(Fraction(float(cand)) - fr), abs(Fraction(float(best)) - fr)
-        if dc < db or (dc == db and (int(np.array(cand, f32).view(np.uint32)) & 1) == 0):
-            best = cand
-    return f32(best)
-
-
-def _fma_neg(q: np.ndarray, K: np.float32, y: np.ndarray) -> np.ndarray:
-    """RN32(y - q*K) elementwise, rounded once."""
-    fk = Fraction(float(K))
-    return np.array([_rn32(Fraction(float(yy)) - Fraction(float(qq)) * fk) for qq, yy in zip(q, y)], f32)
 
 
 def _seq(e: np.ndarray) -> np.float32:
@@ -71,8 +54,8 @@ def _candidates(b, Senc):
 
 
 def _block_errors(y, sf, A, Sdec, C, err):
-    """Exact and approximate per-element errors of one candidate on the
-    values y (any shape), and K."""
+    """Exact per-element errors of one candidate on the values y (any shape),
+    the approximate ones in the scaled domain, and K."""
     d = oracle.e4m3_decode(sf).astype(f32)
     enc = np.minimum(f32(f32(1.0) / f32(d * Sdec)), FLT_MAX)
     with np.errstate(over="ignore"):         # enc = FLT_MAX for a zero scale; the encode saturates
@@ -81,17 +64,26 @@ def _block_errors(y, sf, A, Sdec, C, err):
     dq = (((np.abs(q) * d).astype(f32) * A).astype(f32) / C).astype(f32)
     diff_t = (dq - np.abs(y)).astype(f32)
     K = f32(f32(f32(f32(1.0) * d) * A) / C)
-    diff_a = _fma_neg(q.ravel(), K, y.ravel()).reshape(y.shape)
+    with np.errstate(over="ignore", invalid="ignore"):
+        diff_a = (q - v).astype(f32)                              # one rounding, as the mixed subtract
     if err == "mae":
         return np.abs(diff_t), np.abs(diff_a), K
     return (diff_t * diff_t).astype(f32), (diff_a * diff_a).astype(f32), K
 
 
-def _bound(K, S, err, tile):
-    K, S = float(K), float(S)
+def _scaled(Sp, K, err):
+    """E^ from the scaled-domain sum: RN(K * S'), or RN(RN(K * K) * S')."""
+    with np.errstate(over="ignore"):
+        return f32(K * Sp) if err == "mae" else f32(f32(K * K) * Sp)
+
+
+def _bound(K, E, b, err, tile):
+    K, E, b = float(K), float(E), float(b)
     if err == "mae":
-        return (2.0 ** (-11 if tile else -15)) * K + 2.0 ** -18 * S + 2.0 ** -121
-    return (2.0 ** (-14 if tile else -16)) * K * np.sqrt(S) + 2.0 ** -18 * S + 2.0 ** -121
+        return 2.0 ** -18 * E + 2.0 ** (-12 if tile else -16) * K + 2.0 ** (-13 if tile else -17) * b + 2.0 ** -121
+    r = np.sqrt(E)
+    return (2.0 ** (-15 if tile else -17) * K * r + 2.0 ** (-16 if tile else -18) * b * r + 2.0 ** -18 * E
+            + 2.0 ** -121)
 
 
 def _inputs(rng, shape):
@@ -122,10 +114,12 @@ def test_certified_bound_1x16(err, bound):
         for i, y in enumerate(blocks):
             for sf in (sf6[i], sf4[i]):
                 et, ea, K = _block_errors(y, np.uint8(sf), A, Sdec, C, err)
-                E, S = _seq(et), _seq(ea)
-                gap = abs(float(E) - float(S))
-                B = _bound(K, S, err, tile=False)
-                assert gap <= B, f"{name} block {i}: |E - S| = {gap} > {B} (K {K}, S {S})"
+                E, Eh = _seq(et), _scaled(_seq(ea), K, err)
+                if not (np.isfinite(E) and np.isfinite(Eh)):
+                    continue                 # the kernels take the exact sums
+                gap = abs(float(E) - float(Eh))
+                B = _bound(K, Eh, b[i], err, tile=False)
+                assert gap <= B, f"{name} block {i}: |E - E^| = {gap} > {B} (K {K}, E^ {Eh})"
                 worst = max(worst, gap / B)
     print(err, bound, "worst |E - S| / B:", worst)
     assert 0.0 < worst <= 1.0                # the approximation is not exact everywhere
@@ -149,9 +143,11 @@ def test_certified_bound_tile(err):
                     for tr in (False, True):          # rowwise sums, then x^T's (columnwise)
                         mt, ma = (et.T, ea.T) if tr else (et, ea)
                         E = _tree16([_seq(r) for r in mt])
-                        S = _tree16([_seq(r) for r in ma])
-                        gap = abs(float(E) - float(S))
-                        B = _bound(K, S, err, tile=True)
+                        Eh = _scaled(_tree16([_seq(r) for r in ma]), K, err)
+                        if not (np.isfinite(E) and np.isfinite(Eh)):
+                            continue
+                        gap = abs(float(E) - float(Eh))
+                        B = _bound(K, Eh, b[0], err, tile=True)
                         assert gap <= B, f"{name} tile ({t0},{c0}) {'col' if tr else 'row'}: {gap} > {B}"
                         worst = max(worst, gap / B)
     assert 0.0 < worst <= 1.0

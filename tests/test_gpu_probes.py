@@ -11,6 +11,8 @@ the library's own entry points (in-bounds inputs only).
   6x every e4m3 midpoint, plus random values over the whole scale range.
 - Philox: stochastic rounding at global indices whose counter uses all four
   words (row_offset beyond 2^32 blocks, steps beyond 2^32, a 64-bit seed).
+- the mixed f16/f32 subtract of the certified four-over-six sums rounds once
+  (nvfp4_probe_sub_f16 against IEEE fp32 subtraction).
 """
 import numpy as np
 import pytest
@@ -141,3 +143,28 @@ def test_exact_division_routine_exhaustive_mantissas():
     a[1000:2000] = np.float32(-0.0)
     got = to_np(nv.nvfp4_probe_divide(to_dev(a), to_dev(b)))
     assert_same(got, a / b, "random pairs")
+
+
+def test_mixed_f16_subtract_rounds_once():
+    """The certified four-over-six sums take each element's scaled error as
+    RN(q - v), q a grid value held in f16 and v fp32, from one mixed-precision
+    subtract; their rounding bound assumes q is taken exactly and the
+    difference rounded once to fp32 — the IEEE fp32 subtraction of q and v."""
+    rng = np.random.default_rng(93)
+    n = 1 << 16
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float32)
+    q = grid[rng.integers(0, 8, 2 * n)] * rng.choice(np.array([-1, 1], np.float32), 2 * n)
+    kind = rng.integers(0, 5, 2 * n)
+    v = np.empty(2 * n, np.float32)
+    near = q * (1 + rng.standard_normal(2 * n).astype(np.float32) * np.float32(1e-3))
+    v[kind == 0] = near[kind == 0]
+    v[kind == 1] = (rng.standard_normal(2 * n) * 3).astype(np.float32)[kind == 1]
+    v[kind == 2] = (rng.standard_normal(2 * n) * 1e-30).astype(np.float32)[kind == 2]
+    v[kind == 3] = (rng.standard_normal(2 * n) * 1e30).astype(np.float32)[kind == 3]
+    v[kind == 4] = np.nextafter(q, np.float32(np.inf))[kind == 4]
+    h = q.astype(np.float16).view(np.uint16).astype(np.uint32)
+    words = (h[0::2] | (h[1::2] << 16)).view(np.int32)
+    got = to_np(nv.nvfp4_probe_sub_f16(torch.from_numpy(words.copy()).cuda(), to_dev(v)))
+    with np.errstate(over="ignore"):
+        want = (q - v).astype(np.float32)
+    assert_same(got, want, "q - v")
