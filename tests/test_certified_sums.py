@@ -57,8 +57,8 @@ def _block_errors(y, sf, A, Sdec, C, err):
     """Exact per-element errors of one candidate on the values y (any shape),
     the approximate ones in the scaled domain, and K."""
     d = oracle.e4m3_decode(sf).astype(f32)
-    enc = np.minimum(f32(f32(1.0) / f32(d * Sdec)), FLT_MAX)
-    with np.errstate(over="ignore"):         # enc = FLT_MAX for a zero scale; the encode saturates
+    with np.errstate(divide="ignore", over="ignore"):   # a zero scale: enc = FLT_MAX, the encode saturates
+        enc = np.minimum(f32(f32(1.0) / f32(d * Sdec)), FLT_MAX)
         v = (y * enc).astype(f32)
     q = oracle.e2m1_value(oracle.e2m1_encode_rn(v)).astype(f32)
     dq = (((np.abs(q) * d).astype(f32) * A).astype(f32) / C).astype(f32)
@@ -73,7 +73,7 @@ def _block_errors(y, sf, A, Sdec, C, err):
 
 def _scaled(Sp, K, err):
     """E^ from the scaled-domain sum: RN(K * S'), or RN(RN(K * K) * S')."""
-    with np.errstate(over="ignore"):
+    with np.errstate(over="ignore", invalid="ignore"):      # 0 * inf: a NaN the kernels fall back on
         return f32(K * Sp) if err == "mae" else f32(f32(K * K) * Sp)
 
 
