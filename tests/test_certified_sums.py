@@ -68,7 +68,8 @@ def _block_errors(y, sf, A, Sdec, C, err):
         diff_a = (q - v).astype(f32)                              # one rounding, as the mixed subtract
     if err == "mae":
         return np.abs(diff_t), np.abs(diff_a), K
-    return (diff_t * diff_t).astype(f32), (diff_a * diff_a).astype(f32), K
+    with np.errstate(over="ignore"):                          # squares of huge differences: inf, exact path
+        return (diff_t * diff_t).astype(f32), (diff_a * diff_a).astype(f32), K
 
 
 def _scaled(Sp, K, err):
