@@ -354,7 +354,9 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
     }
     int stage = 0, par = 0;
     BandAmax<NT> tile_amax{red, warp, lane, t, 0u};
-    for (; cur.band < nbands32; cur.advance()) {
+    while (cur.band < nbands32) {
+        // with two stages the next step is the one just issued: copied, not advanced
+        const BandCursor next = ahead;
         issue(ahead, stage == 0 ? S - 1 : stage - 1);
         ahead.advance();
         cp_async_wait<S - 1>();
@@ -390,6 +392,8 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
                                          [] {});
         stage = stage == S - 1 ? 0 : stage + 1;
         par ^= 1;
+        if (S == 2) cur = next;
+        else cur.advance();
     }
     pdl_trigger();
     cp_async_wait<0>();
