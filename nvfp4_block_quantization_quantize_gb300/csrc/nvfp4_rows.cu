@@ -323,11 +323,12 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
     const uint32_t swx = piece_swizzle<St::XB / 16>(tid), swr = piece_swizzle<4>(tid);
 
     const int32_t nbands32 = static_cast<int32_t>(nbands), nb32 = static_cast<int32_t>(nb);
+    const bool whole = nb32 % Gm::T == 0;        // every chunk full: a column is never past the row
     auto group = [&](const BandCursor& c, bool& live) {   // this thread's 1x16 block
-        live = c.band < nbands32 && c.chunk * Gm::T + t < nb32;
+        live = c.band < nbands32 && (whole || c.chunk * Gm::T + t < nb32);
         return c.blk;
     };
-    auto issue = [&](const BandCursor& c, int stage) {
+    auto issue = [&](const BandCursor& c, int stage) {   // returns the group's liveness
         bool live;
         const int64_t blk = group(c, live);
         if (live) {
@@ -341,15 +342,17 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
             }
         }
         cp_async_commit();
+        return live;
     };
 
     constexpr int S = St::STAGES;
     BandCursor cur, ahead;
     cur.init(blockIdx.x, static_cast<int32_t>(nch), gridDim.x, nb, rr, t, Gm::T);
     ahead = cur;
+    bool live_cur = false;                       // S == 2: the current group's liveness, from its issue
 #pragma unroll
     for (int k = 0; k < S - 1; ++k) {
-        issue(ahead, k);
+        live_cur = issue(ahead, k);
         ahead.advance();
     }
     int stage = 0, par = 0;
@@ -357,11 +360,11 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
     while (cur.band < nbands32) {
         // with two stages the next step is the one just issued: copied, not advanced
         const BandCursor next = ahead;
-        issue(ahead, stage == 0 ? S - 1 : stage - 1);
+        const bool live_next = issue(ahead, stage == 0 ? S - 1 : stage - 1);
         ahead.advance();
         cp_async_wait<S - 1>();
-        bool live;
-        const int64_t blk = group(cur, live);
+        bool live = live_cur;
+        const int64_t blk = S == 2 ? cur.blk : group(cur, live);
         float y[16];
         if (live) {
             lds16_swz<DT>(xs + stage * St::BYTES, swx, y);
@@ -392,8 +395,12 @@ __global__ void __launch_bounds__(kBandThreads) k_band16(const QuantArgs a) {
                                          [] {});
         stage = stage == S - 1 ? 0 : stage + 1;
         par ^= 1;
-        if (S == 2) cur = next;
-        else cur.advance();
+        if (S == 2) {
+            cur = next;
+            live_cur = live_next;
+        } else {
+            cur.advance();
+        }
     }
     pdl_trigger();
     cp_async_wait<0>();
