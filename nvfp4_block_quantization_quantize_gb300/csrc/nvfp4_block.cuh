@@ -319,6 +319,7 @@ constexpr int kDqStride = 132;
 struct O6Tab {
     float enc[128];
     float dq[8 * kDqStride];
+    float2 ek[128];                             // (enc[sf], dq[grid value 1][sf]): one load per candidate
 };
 
 // the shared table of a kernel instance, or nothing when it has no four-over-six
@@ -333,6 +334,7 @@ __device__ __forceinline__ void fill_o6_table(O6Tab* tab, float Sdec, float A, f
         tab->enc[i] = min_nd(div_rn(1.0f, mul_rn(d, Sdec)), FLT_MAX);
 #pragma unroll
         for (int k = 0; k < 8; ++k) tab->dq[k * kDqStride + i] = div_rn(mul_rn(mul_rn(G[k], d), A), C);
+        tab->ek[i] = make_float2(tab->enc[i], tab->dq[2 * kDqStride + i]);
     }
     __syncthreads();
 }
@@ -471,15 +473,17 @@ __device__ __forceinline__ void four_over_six16(const float* y, float b, const G
                                                 const O6Tab* tab, uint32_t& w0, uint32_t& w1,
                                                 uint32_t& sf, float& d, TileSums tile_sums) {
     const float s6f = block_s6f<true>(b, g.Senc);
-    const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
-    const uint32_t sf4 = e4m3_encode(min_nd(mul_rn(s6f, 1.5f), 448.0f));
-    const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
+    uint32_t sf6, sf4;
+    e4m3_encode2(min_nd(s6f, 448.0f), min_nd(mul_rn(s6f, 1.5f), 448.0f), sf6, sf4);
+    float d6, d4;
+    e4m3_decode2(sf6, sf4, d6, d4);
     uint32_t a0, a1, b0, b1;
     float e[16], E6, E4;
     if (CERT && tab) {                          // per-tensor global scale, 1x16
-        const float K6 = tab->dq[2 * kDqStride + sf6], K4 = tab->dq[2 * kDqStride + sf4];
-        E6 = errsum16_approx<ERR>(y, tab->enc[sf6], K6, a0, a1);
-        E4 = errsum16_approx<ERR>(y, tab->enc[sf4], K4, b0, b1);
+        const float2 ek6 = tab->ek[sf6], ek4 = tab->ek[sf4];
+        const float K6 = ek6.y, K4 = ek4.y;
+        E6 = errsum16_approx<ERR>(y, ek6.x, K6, a0, a1);
+        E4 = errsum16_approx<ERR>(y, ek4.x, K4, b0, b1);
         if (!approx_decides<ERR>(E6, E4, K6, K4, b)) {
             E6 = errsum16_tab<ERR>(y, a0, a1, tab->dq + sf6);
             E4 = errsum16_tab<ERR>(y, b0, b1, tab->dq + sf4);

@@ -46,6 +46,23 @@ __device__ __forceinline__ uint32_t e4m3_encode(float s) {
     return r & 0xFFu;
 }
 
+// Two scales in one conversion: the bytes of sa and sb.
+__device__ __forceinline__ void e4m3_encode2(float sa, float sb, uint32_t& a, uint32_t& b) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(sb), "f"(sa));
+    a = r & 0xFFu;
+    b = static_cast<uint32_t>(r) >> 8;
+}
+
+// The exact values of two E4M3 bytes in one conversion.
+__device__ __forceinline__ void e4m3_decode2(uint32_t a, uint32_t b, float& da, float& db) {
+    uint32_t h2;
+    const uint16_t in = static_cast<uint16_t>((a & 0xFFu) | ((b & 0xFFu) << 8));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    da = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+    db = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+}
+
 // Exact value of an E4M3 byte (every E4M3 value is an fp16 normal or zero).
 __device__ __forceinline__ float e4m3_decode(uint32_t b) {
     uint32_t h2;
