@@ -9,24 +9,26 @@
 //               thread owns one column (x^T's row) of it for the columnwise
 //               pass; the 4 bands' columnwise codes wait in shared memory and
 //               leave as one 32-byte run per column.
-// k_tile_t      four-over-six 16x16 with rowwise AND columnwise output: one
-//               thread owns a whole 16x16 tile and walks its rows twice
-//               (amax; both candidates' codes and errors with the row sums
-//               AND the column sums accumulated in row order, so x^T's
-//               element-order sums are exact too; then store).  Row and column
-//               choices are made from the same per-element errors; the
-//               columnwise codes are transposed in registers.  A CTA is 4
-//               bands (one per warp) x 32 tiles: loads of a row by a warp
-//               cover 32 consecutive tiles (fully coalesced), and the
-//               columnwise output, staged in shared memory, leaves as one
-//               32-byte run per column (4 bands x 8 bytes) instead of 8-byte
-//               pieces 32 to a warp store.  The row loops stay rolled (a
-//               fully unrolled kernel overflowed the instruction cache; the
-//               error pass takes four bf16 or two fp32 rows per iteration); row sums
-//               and code words wait in shared memory until the tile's choices
-//               are known (both candidates' code words too, so x is read only
-//               twice); each thread streams its 32 row reads through a 4-slot
-//               ring of asynchronous copies, three reads ahead.
+// k_tile_ts     four-over-six 16x16 with rowwise AND columnwise output, bf16
+//               input: one thread owns a whole 16x16 tile, copies its 16 rows
+//               into shared memory up front, and walks them twice (amax; both
+//               candidates' codes and approximate errors, the column sums
+//               accumulated in row order).  One approximate sum per candidate
+//               certifies both the row and the column choice; where it does
+//               not, the exact row sums and x^T's element-order column sums
+//               are taken from the error-value table.  The columnwise codes
+//               are transposed in registers.  A CTA is 4 bands (one per warp)
+//               x 32 tiles: a warp's copies of a row cover 32 consecutive
+//               tiles (fully coalesced), and the columnwise output, staged in
+//               shared memory, leaves as one 32-byte run per column (4 bands
+//               x 8 bytes) instead of 8-byte pieces 32 to a warp store.
+// k_tile_t      the same for fp32 input, whose 1 KB tiles are too large to
+//               stage whole: each thread streams its 32 row reads through a
+//               3-slot ring of asynchronous copies, two reads ahead, and the
+//               code words wait in shared memory until the tile's choices
+//               are known (both candidates' code words, so x is read only
+//               twice).  The row loops stay rolled (a fully unrolled kernel
+//               overflowed the instruction cache).
 //
 // Method: "Add NVFP4 four-over-six (row-wise) quantization to the training
 // prototype" (What: 16x16 blocks, rowwise / columnwise; CuTe DSL kernel
@@ -189,13 +191,10 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
 // ---------------------------------------------------------------------------------------------
 constexpr int kTileThreads = 128;
 
-// Ring of tile rows per thread for fp32 input (3 slots of 64-byte rows).
-// bf16 rows (32 bytes) are loaded straight into registers instead, which
-// leaves the shared memory of four CTAs per SM.
-template <int DT>
+// Ring of fp32 tile rows per thread of k_tile_t (3 slots of 64-byte rows).
 struct TileRing {
-    static constexpr int XB = DT == NVFP4_BF16 ? 32 : 64;    // bytes of one tile row
-    static constexpr int SLOTS = DT == NVFP4_BF16 ? 0 : 3;
+    static constexpr int XB = 64;               // bytes of one tile row
+    static constexpr int SLOTS = 3;
     static constexpr int BYTES = SLOTS * kTileThreads * XB;
 };
 
@@ -228,20 +227,21 @@ __device__ __forceinline__ int stage_index(int b, int j) {
 
 template <int DT, int ERR>
 __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
-    using Rg = TileRing<DT>;
+    static_assert(DT == NVFP4_F32, "bf16 input takes k_tile_ts");
+    using Rg = TileRing;
     __shared__ float tenc[128];                 // encode reciprocal of every scale byte
     // per thread and candidate: the error value magnitude |dq| of each grid
     // index k, [candidate][k][thread] so a warp's lookups are conflict-free
     __shared__ float dqt[2][8][kTileThreads];
-    // per thread and candidate: row sums of rows 0-7, then the width-16
-    // tree's first level (row i + row i + 8), [candidate][i][thread] so a
-    // warp's accesses are conflict-free
+    // exact path, per thread and candidate: row sums of rows 0-7, then the
+    // width-16 tree's first level (row i + row i + 8), [candidate][i][thread]
+    // so a warp's accesses are conflict-free
     __shared__ float sR[2][8][kTileThreads];
     // both candidates' code words of every row (map-to-6: [0..1], map-to-4: [2..3])
     __shared__ uint32_t sW[4][16][kTileThreads];
     // ring of tile rows: the thread streams its tile's rows twice (32 row
     // reads) through Rg::SLOTS slots of asynchronous copies
-    __shared__ __align__(16) unsigned char ring[Rg::BYTES > 0 ? Rg::BYTES : 16];
+    __shared__ __align__(16) unsigned char ring[Rg::BYTES];
     __shared__ uint8_t scol[kBands][32];        // columnwise scale byte of each tile
     pdl_wait();
     GScale g{0.0f, 1.0f, 1.0f};
@@ -268,75 +268,31 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
         const int64_t row_bytes = K * (Rg::XB / 16);
         unsigned char* slot0 = ring + tid * Rg::XB;
 
-        // fp32: row read j (0..31) is tile row j % 16, into slot j % Rg::SLOTS
+        // row read j (0..31) is tile row j % 16, into slot j % Rg::SLOTS
         auto issue = [&](int j) {
-            if constexpr (Rg::SLOTS > 0) {
-                if (j < 32) {
-                    const unsigned char* src = gx + static_cast<int64_t>(j & 15) * row_bytes;
-                    unsigned char* dst = slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB);
+            if (j < 32) {
+                const unsigned char* src = gx + static_cast<int64_t>(j & 15) * row_bytes;
+                unsigned char* dst = slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB);
 #pragma unroll
-                    for (int c = 0; c < Rg::XB / 16; ++c) cp_async16(dst + 16 * c, src + 16 * c);
-                }
-                cp_async_commit();
+                for (int c = 0; c < Rg::XB / 16; ++c) cp_async16(dst + 16 * c, src + 16 * c);
             }
+            cp_async_commit();
         };
-        // bf16: row r's 32 bytes, loaded one row ahead into registers
-        const uint4* grow = reinterpret_cast<const uint4*>(gx);
-        const int64_t row_u4 = row_bytes / 16;
-        uint4 pre0 = make_uint4(0, 0, 0, 0), pre1 = pre0;
         auto next_row = [&](int j, float* y) {       // row read j, ready in y
-            if constexpr (Rg::SLOTS > 0) {
-                issue(j + Rg::SLOTS - 1);
-                cp_async_wait<Rg::SLOTS - 1>();
-                lds16<DT>(slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB), y);
-            } else {
-                const uint4 u = pre0, v = pre1;
-                if (j + 1 < 32) {
-                    const uint4* p = grow + static_cast<int64_t>((j + 1) & 15) * row_u4;
-                    pre0 = __ldg(p);
-                    pre1 = __ldg(p + 1);
-                }
-                const uint32_t w[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    y[2 * i] = __uint_as_float(w[i] << 16);
-                    y[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-                }
-            }
+            issue(j + Rg::SLOTS - 1);
+            cp_async_wait<Rg::SLOTS - 1>();
+            lds16<DT>(slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB), y);
         };
-        if constexpr (Rg::SLOTS > 0) {
 #pragma unroll
-            for (int j = 0; j < Rg::SLOTS - 1; ++j) issue(j);
-        }
+        for (int j = 0; j < Rg::SLOTS - 1; ++j) issue(j);
 
-        // pass 0: tile amax (bf16: on the packed pairs, four rows' loads in flight)
+        // pass 0: tile amax
         float y[16];
         float b = 0.0f;
-        if constexpr (DT == NVFP4_BF16) {
-            uint32_t m2 = 0u;
 #pragma unroll 1
-            for (int r = 0; r < 16; r += 4) {
-                uint4 u[4], v[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    u[q] = __ldg(grow + static_cast<int64_t>(r + q) * row_u4);
-                    v[q] = __ldg(grow + static_cast<int64_t>(r + q) * row_u4 + 1);
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, u[q].x), u[q].y), u[q].z), u[q].w);
-                    m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, v[q].x), v[q].y), v[q].z), v[q].w);
-                }
-            }
-            b = max_nd(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
-            pre0 = __ldg(grow);                     // row 0 for pass 1 (read 16)
-            pre1 = __ldg(grow + 1);
-        } else {
-#pragma unroll 1
-            for (int r = 0; r < 16; ++r) {
-                next_row(r, y);
-                b = max_nd(b, absmax16(y));
-            }
+        for (int r = 0; r < 16; ++r) {
+            next_row(r, y);
+            b = max_nd(b, absmax16(y));
         }
         const float s6f = block_s6f<true>(b, g.Senc);
         const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
@@ -349,9 +305,8 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
         // pass 1: both candidates' codes, and approximate per-element errors in
         // the scaled domain, |q - v| with v = y * enc (squared for MSE; q the
         // code's signed grid value) from one mixed f16/f32 subtract, no table
-        // lookup; row sums to shared memory, column sums in registers, both
-        // accumulated in element order and scaled back by K (K^2 for MSE) at
-        // the end
+        // lookup; column sums in registers, accumulated in row order, their
+        // tree scaled back by K (K^2 for MSE) at the end
         float F6[16], F4[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
@@ -394,7 +349,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             sR[0][i8][tid] = R6;
             sR[1][i8][tid] = R4;
         };
-#pragma unroll(DT == NVFP4_BF16 ? 4 : 2)
+#pragma unroll 2
         for (int r = 0; r < 16; ++r) {
             next_row(16 + r, y);
             float e[16];
@@ -402,16 +357,13 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             candidate(y, ENC6, w0, w1, e);
             sW[0][r][tid] = w0;
             sW[1][r][tid] = w1;
-            const float R6 = seq_sum16(e);
             col_sums(F6, e);
             candidate(y, ENC4, w0, w1, e);
             sW[2][r][tid] = w0;
             sW[3][r][tid] = w1;
-            const float R4 = seq_sum16(e);
             col_sums(F4, e);
-            row_sums(r, R6, R4);
         }
-        if constexpr (Rg::SLOTS > 0) cp_async_wait<0>();
+        cp_async_wait<0>();
         float E6r, E4r, E6c, E4c;
         auto tree_sums = [&]() {
             float S[8];
@@ -424,16 +376,16 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
             E6c = tree16_regs(F6);
             E4c = tree16_regs(F4);
         };
-        tree_sums();
         {   // back from the scaled domain: E^ = RN(K * S'), or RN(RN(K * K) * S')
             const float k6 = ERR == NVFP4_ERR_MAE ? K6 : mul_rn(K6, K6);
             const float k4 = ERR == NVFP4_ERR_MAE ? K4 : mul_rn(K4, K4);
-            E6r = mul_rn(k6, E6r);
-            E6c = mul_rn(k6, E6c);
-            E4r = mul_rn(k4, E4r);
-            E4c = mul_rn(k4, E4c);
+            E6r = E6c = mul_rn(k6, tree16_regs(F6));
+            E4r = E4c = mul_rn(k4, tree16_regs(F4));
         }
-        if (!(tile_sums_decide<ERR>(E6r, E4r, K6, K4, b) && tile_sums_decide<ERR>(E6c, E4c, K6, K4, b))) {
+        // one approximate sum per candidate serves both choices: the rowwise
+        // and the columnwise exact sums add the same 256 terms, each through
+        // at most 19 additions, so both lie within the tile bound of it
+        if (!tile_sums_decide<ERR>(E6c, E4c, K6, K4, b)) {
             // the exact sums: error values |dq| = ((G[k] * d) * A) / (6 * bound)
             // of each grid magnitude G[k] from a per-thread table (a code of
             // index k stands for +-|dq| with the sign of its y, so |dq - y| =
@@ -503,6 +455,248 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
     __syncthreads();
     uint2* stg = reinterpret_cast<uint2*>(&sW[0][0][0]);
     if (band < nbands && tile < nb) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            stg[stage_index(warp, lane * 16 + c)] = make_uint2(lo[c], lo[8 + c]);
+            stg[stage_index(warp, lane * 16 + 8 + c)] = make_uint2(hi[c], hi[8 + c]);
+        }
+    }
+    scol[warp][lane] = static_cast<uint8_t>(sf_c);
+    __syncthreads();
+    uint2* cc = reinterpret_cast<uint2*>(a.codes_col);
+#pragma unroll 4
+    for (int q = tid; q < 512 * kBands; q += kTileThreads) {
+        const int j = q / kBands, bb = q % kBands;          // column of the CTA, band of the CTA
+        const int64_t col = tile0 * 16 + j, bnd = band0 + bb;
+        if (col < K && bnd < nbands) {
+            cc[col * nbands + bnd] = stg[stage_index(bb, j)];
+            a.scales_col[col * nbands + bnd] = scol[bb][j >> 4];
+        }
+    }
+    pdl_trigger();
+}
+
+// Four-over-six 16x16 with rowwise and columnwise output, bf16 input, the
+// whole tile staged: the same per-tile work as k_tile_t (one thread per tile,
+// both candidates' row and column sums from one walk, the certified sums with
+// the exact fallback), but each thread copies its tile's 16 rows (512 bytes)
+// into shared memory with asynchronous copies as soon as it starts, so the
+// error pass reads shared memory instead of waiting on L2 one row ahead.  The
+// 64 KB of a CTA's tiles leaves room for three CTAs per SM, so the other
+// CTAs' error passes cover a CTA's copies.  A thread's slot of row r (32
+// bytes, its 16-byte pieces swizzled by piece_swizzle<2>) is reused once row
+// r has been read: its first piece takes the row's code words of both
+// candidates (map-to-6 then map-to-4), the second piece of rows 0-7 the row
+// sums (the width-16 tree's first level), and the exact fallback's error
+// values wait in the second piece of rows 8-15 (the fallback reads x again
+// from global memory).  The columnwise output is staged in the same buffer
+// once every thread is done with its slots.
+constexpr int kStagedTileBytes = 16 * kTileThreads * 32;
+
+template <int ERR>
+__global__ void __launch_bounds__(kTileThreads) k_tile_ts(const QuantArgs a) {
+    extern __shared__ __align__(16) unsigned char tile_s[];   // [row][thread][32 bytes]
+    __shared__ float tenc[128];                 // encode reciprocal of every scale byte
+    __shared__ uint8_t scol[kBands][32];        // columnwise scale byte of each tile
+    pdl_wait();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t M = a.M, K = a.K;
+    const int64_t band0 = static_cast<int64_t>(blockIdx.x) * kBands, band = band0 + warp;
+    const int64_t tile0 = static_cast<int64_t>(blockIdx.y) * 32, tile = tile0 + lane;
+    const int64_t nb = K / 16, nbands = M / 16;
+    const bool own = band < nbands && tile < nb;
+    const int64_t base = band * 16 * K + tile * 16;
+    const uint32_t swz = piece_swizzle<2>(tid);
+    auto slot = [&](int r) { return tile_s + (r * kTileThreads + tid) * 32; };
+    auto piece = [&](int r, uint32_t c) { return slot(r) + ((c ^ swz) << 4); };
+    if (own) {                                  // the tile's rows, four per copy group
+        const unsigned char* gx = static_cast<const unsigned char*>(a.x) + base * 2;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            cp_async16(piece(r, 0), gx + static_cast<int64_t>(r) * K * 2);
+            cp_async16(piece(r, 1), gx + static_cast<int64_t>(r) * K * 2 + 16);
+            if ((r & 3) == 3) cp_async_commit();
+        }
+    }
+    GScale g{0.0f, 1.0f, 1.0f};
+    if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
+        g.A = a.gamax[0];
+        global_scales(g.A, a.bound, g.Senc, g.Sdec);
+    }
+    const float C = mul_rn(6.0f, a.bound);
+    for (int i = tid; i < 128; i += blockDim.x)
+        tenc[i] = min_nd(div_rn(1.0f, mul_rn(e4m3_decode(static_cast<uint32_t>(i)), g.Sdec)), FLT_MAX);
+    __syncthreads();
+
+    uint32_t lo[16], hi[16];                    // columnwise code words, transposed
+    uint32_t sf_c = 0;
+    if (own) {
+        // pass 0: tile amax on the packed pairs, each copy group as it lands
+        uint32_t m2 = 0u;
+        auto amax4 = [&](int r0) {
+#pragma unroll
+            for (int r = r0; r < r0 + 4; ++r) {
+                const uint4 u = *reinterpret_cast<const uint4*>(piece(r, 0));
+                const uint4 v = *reinterpret_cast<const uint4*>(piece(r, 1));
+                m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, u.x), u.y), u.z), u.w);
+                m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, v.x), v.y), v.z), v.w);
+            }
+        };
+        cp_async_wait<3>();
+        amax4(0);
+        cp_async_wait<2>();
+        amax4(4);
+        cp_async_wait<1>();
+        amax4(8);
+        cp_async_wait<0>();
+        amax4(12);
+        const float b = max_nd(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
+        const float s6f = block_s6f<true>(b, g.Senc);
+        const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
+        const uint32_t sf4 = e4m3_encode(min_nd(mul_rn(s6f, 1.5f), 448.0f));
+        const float enc6 = tenc[sf6], enc4 = tenc[sf4];
+        const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
+        // K: the error value of grid value 1, ((1 * d) * A) / (6 * bound)
+        const float K6 = div_rn(mul_rn(d6, g.A), C), K4 = div_rn(mul_rn(d4, g.A), C);
+
+        // pass 1: as k_tile_t's (scaled-domain approximate errors, row sums
+        // and column sums in row order), reading the staged rows
+        float F6[16], F4[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
+        const uint64_t ENC6 = pack2(enc6, enc6), ENC4 = pack2(enc4, enc4);
+        auto candidate = [&](const float* y, uint64_t enc2, uint32_t& w0, uint32_t& w1, float* e) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) unpack2(mul2(pack2(y[i], y[i + 1]), enc2), v[i], v[i + 1]);
+            uint32_t h[8];
+            w0 = e2m1_encode8_dec(v, h);
+            w1 = e2m1_encode8_dec(v + 8, h + 4);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                sub_f16x2_f32(h[j], v[2 * j], v[2 * j + 1], e[2 * j], e[2 * j + 1]);
+                if (ERR != NVFP4_ERR_MAE) {
+                    const uint64_t D = pack2(e[2 * j], e[2 * j + 1]);
+                    unpack2(mul2(D, D), e[2 * j], e[2 * j + 1]);
+                }
+            }
+            if (ERR == NVFP4_ERR_MAE) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) e[i] = fabsf(e[i]);
+            }
+        };
+        auto col_sums = [&](float* F, const float* e) {
+            if (ERR == NVFP4_ERR_MAE) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) F[i] = add_rn(F[i], e[i]);
+            } else {
+                add16(F, e);
+            }
+        };
+        // row sums: rows 0-7 stored, row r >= 8 added to row r - 8's
+        auto row_sums = [&](int r, float R6, float R4) {
+            float2* p = reinterpret_cast<float2*>(piece(r & 7, 1));
+            if (r >= 8) {
+                const float2 s = *p;
+                R6 = add_rn(s.x, R6);
+                R4 = add_rn(s.y, R4);
+            }
+            *p = make_float2(R6, R4);
+        };
+        float y[16];
+#pragma unroll 4
+        for (int r = 0; r < 16; ++r) {
+            lds16_swz<NVFP4_BF16>(slot(r), swz, y);
+            float e[16];
+            uint32_t a0, a1, b0, b1;
+            candidate(y, ENC6, a0, a1, e);
+            col_sums(F6, e);
+            candidate(y, ENC4, b0, b1, e);
+            col_sums(F4, e);
+            *reinterpret_cast<uint4*>(piece(r, 0)) = make_uint4(a0, a1, b0, b1);
+        }
+        float E6r, E4r, E6c, E4c;
+        auto tree_sums = [&]() {
+            float S6[8], S4[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float2 s = *reinterpret_cast<const float2*>(piece(i, 1));
+                S6[i] = s.x;
+                S4[i] = s.y;
+            }
+            E6r = tree16_upper(S6);
+            E4r = tree16_upper(S4);
+            E6c = tree16_regs(F6);
+            E4c = tree16_regs(F4);
+        };
+        {   // back from the scaled domain, one sum per candidate for both choices
+            const float k6 = ERR == NVFP4_ERR_MAE ? K6 : mul_rn(K6, K6);
+            const float k4 = ERR == NVFP4_ERR_MAE ? K4 : mul_rn(K4, K4);
+            E6r = E6c = mul_rn(k6, tree16_regs(F6));
+            E4r = E4c = mul_rn(k4, tree16_regs(F4));
+        }
+        if (!tile_sums_decide<ERR>(E6c, E4c, K6, K4, b)) {
+            // the exact sums as in k_tile_t: error values |dq| of each grid
+            // magnitude (row 8 + k's second piece: map-to-6, map-to-4), the
+            // codes kept in the first pieces, x read again
+            const float G[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<float2*>(piece(8 + k, 1)) =
+                    make_float2(div_rn(mul_rn(mul_rn(G[k], d6), g.A), C), div_rn(mul_rn(mul_rn(G[k], d4), g.A), C));
+            auto exact = [&](const float* y, uint32_t w0, uint32_t w1, int c, float* e) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const uint32_t k = ((i < 8 ? w0 : w1) >> (4 * (i & 7))) & 7u;
+                    const float dq = reinterpret_cast<const float*>(piece(8 + k, 1))[c];
+                    const float diff = sub_rn(dq, fabsf(y[i]));
+                    e[i] = (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff);
+                }
+            };
+#pragma unroll
+            for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
+#pragma unroll 1
+            for (int r = 0; r < 16; ++r) {
+                load16<NVFP4_BF16>(a.x, base + static_cast<int64_t>(r) * K, y);
+                const uint4 w = *reinterpret_cast<const uint4*>(piece(r, 0));
+                float e[16];
+                exact(y, w.x, w.y, 0, e);
+                const float R6 = seq_sum16(e);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) F6[i] = add_rn(F6[i], e[i]);
+                exact(y, w.z, w.w, 1, e);
+                const float R4 = seq_sum16(e);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) F4[i] = add_rn(F4[i], e[i]);
+                row_sums(r, R6, R4);
+            }
+            tree_sums();
+        }
+        const bool row4 = E4r < E6r, col4 = E4c < E6c;       // ties and NaN keep map-to-6
+        const uint8_t sf_r = static_cast<uint8_t>(row4 ? sf4 : sf6);
+
+        // store the rowwise codes of the chosen candidate; gather the columnwise one's
+        const int64_t nbr = K / 16;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const uint4 w = *reinterpret_cast<const uint4*>(piece(r, 0));
+            const int64_t rowg = band * 16 + r;
+            reinterpret_cast<uint2*>(a.codes)[(rowg * K + tile * 16) / 16] =
+                row4 ? make_uint2(w.z, w.w) : make_uint2(w.x, w.y);
+            a.scales[rowg * nbr + tile] = sf_r;
+            lo[r] = col4 ? w.z : w.x;
+            hi[r] = col4 ? w.w : w.y;
+        }
+        transpose8x8_nibbles(lo);          // rows 0-7,  cols 0-7
+        transpose8x8_nibbles(lo + 8);      // rows 8-15, cols 0-7
+        transpose8x8_nibbles(hi);          // rows 0-7,  cols 8-15
+        transpose8x8_nibbles(hi + 8);      // rows 8-15, cols 8-15
+        sf_c = col4 ? sf4 : sf6;
+    }
+    // columnwise output as in k_tile_t, staged in the tile buffer
+    __syncthreads();
+    uint2* stg = reinterpret_cast<uint2*>(tile_s);
+    if (own) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             stg[stage_index(warp, lane * 16 + c)] = make_uint2(lo[c], lo[8 + c]);
@@ -684,7 +878,23 @@ int launch_tile(KernelT kernel, const QuantArgs& a, cudaStream_t s) {
 
 template <int DT, int ERR>
 int launch_tile_t(const QuantArgs& a, cudaStream_t s) {
-    return launch_tile(k_tile_t<DT, ERR>, a, s);
+    if constexpr (DT == NVFP4_BF16) {
+        static int configured_dev = -1;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (configured_dev != dev) {
+            cudaFuncSetAttribute(k_tile_ts<ERR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStagedTileBytes);
+            cudaFuncSetAttribute(k_tile_ts<ERR>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+            configured_dev = dev;
+        }
+        const dim3 grid(static_cast<unsigned>((a.M / 16 + kBands - 1) / kBands),
+                        static_cast<unsigned>((a.K / 16 + 31) / 32));
+        launch_pdl(k_tile_ts<ERR>, grid, kTileThreads, kStagedTileBytes, s, a);
+        return static_cast<int>(cudaGetLastError());
+    } else {
+        return launch_tile(k_tile_t<DT, ERR>, a, s);
+    }
 }
 
 // rowwise + columnwise outputs (no residual)

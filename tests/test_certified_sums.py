@@ -14,7 +14,9 @@ prototype", Two load-bearing numeric details: error values ((q*d)*A)/C,
 element-order sums, the width-16 tree).  This test computes both in IEEE
 fp32 (numpy float32 arithmetic) on many blocks and tiles and checks the
 per-candidate bounds the kernels' thresholds are built from (the threshold
-is twice the two candidates' bounds together), b the block's amax:
+is twice the two candidates' bounds together), b the block's amax.  A
+16x16 tile's one approximate sum per candidate (x^T's order) is checked
+against the exact sums in both orders, since both choices are taken from it:
 
   1x16 MAE  2^-18 E^ + 2^-16 K + 2^-17 b
   1x16 MSE  2^-17 K sqrt(E^) + 2^-18 b sqrt(E^) + 2^-18 E^
@@ -141,10 +143,12 @@ def test_certified_bound_tile(err):
                 sf6, sf4 = _candidates(b, Senc)
                 for sf in (sf6[0], sf4[0]):
                     et, ea, K = _block_errors(y, np.uint8(sf), A, Sdec, C, err)
-                    for tr in (False, True):          # rowwise sums, then x^T's (columnwise)
-                        mt, ma = (et.T, ea.T) if tr else (et, ea)
-                        E = _tree16([_seq(r) for r in mt])
-                        Eh = _scaled(_tree16([_seq(r) for r in ma]), K, err)
+                    # the kernel's one approximate sum per candidate, in x^T's
+                    # order (column sums, then the tree), against the exact
+                    # sums in both orders: the rowwise choice uses it too
+                    Eh = _scaled(_tree16([_seq(r) for r in ea.T]), K, err)
+                    for tr in (False, True):          # rowwise exact sums, then x^T's (columnwise)
+                        E = _tree16([_seq(r) for r in (et.T if tr else et)])
                         if not (np.isfinite(E) and np.isfinite(Eh)):
                             continue
                         gap = abs(float(E) - float(Eh))
