@@ -761,27 +761,33 @@ def run_gpu(args, rank, world, local_rank):
         pin = lambda t: t.cpu().pin_memory()   # noqa: E731
         hW1, hW2, hA = pin(W1), pin(W2), pin(A)
         hR1, hR2 = pin(R1), pin(R2)
-        h2d = sum(t.numel() * t.element_size() for t in (hW1, hW2, hA, hR1, hR2))
-        d2h = [0]
+        nbytes = lambda *ts: sum(t.numel() * t.element_size() for t in ts)   # noqa: E731
+        h2d, d2h = [0], [0]
 
         def e2e_step(t):
+            # every call of the step on host buffers, non-blocking: each call's
+            # inputs go in while the previous calls' results come back; the
+            # step ends when every result is in host memory
+            nb = dict(non_blocking=True)
             outs = []
-            outs.append(nv.nvfp4_quantize(hW1, rounding="sr", residual=hR1, seed=0, step=t))
+            outs.append(nv.nvfp4_quantize(hW1, rounding="sr", residual=hR1, seed=0, step=t, **nb))
             outs.append(nv.nvfp4_quantize(hW2, block="16x16", rounding="sr", residual=hR2, seed=0,
-                                          step=t))
-            qa = nv.nvfp4_quantize(hA, gamax_mode="tensor", err_mode="mae", scale_bound=256.0)
+                                          step=t, **nb))
+            qa = nv.nvfp4_quantize(hA, gamax_mode="tensor", err_mode="mae", scale_bound=256.0, **nb)
             outs.append(qa)
             outs.append(nv.nvfp4_quantize(hW1, block="16x16", gamax_mode="tensor", err_mode="mae",
-                                          scale_bound=256.0, colwise=True))
+                                          scale_bound=256.0, colwise=True, **nb))
             outs.append(nv.nvfp4_quantize(hW2, block="16x16", gamax_mode="tensor", err_mode="mae",
-                                          scale_bound=256.0, colwise=True))
-            outs.append(nv.nvfp4_quantize(hA))
-            outs.append(nv.nvfp4_quantize(hW2, rounding="sr", seed=0, step=t))
+                                          scale_bound=256.0, colwise=True, **nb))
+            outs.append(nv.nvfp4_quantize(hA, **nb))
+            outs.append(nv.nvfp4_quantize(hW2, rounding="sr", seed=0, step=t, **nb))
             dq = nv.nvfp4_dequantize(qa["codes"], qa["scales"], Ma, Ka, gamax_mode="tensor_given",
-                                     gamax=qa["gamax"], scale_bound=256.0)
-            n = sum(v.numel() * v.element_size() for d in outs for v in d.values())
-            n += dq.numel() * dq.element_size() + hR1.numel() * 4 + hR2.numel() * 4
-            d2h[0] = n
+                                     gamax=qa["gamax"], scale_bound=256.0, **nb)
+            nv.nvfp4_synchronize()
+            # bytes copied in: each call's own inputs (W1 twice, W2 three
+            # times, A twice, both residuals, A's codes and scales again)
+            h2d[0] = (nbytes(hW1, hR1, hW2, hR2, hA, hW1, hW2, hA, hW2) + nbytes(qa["codes"], qa["scales"]))
+            d2h[0] = (sum(nbytes(v) for d in outs for v in d.values()) + nbytes(dq, hR1, hR2))
 
         e2e_step(0)
         torch.cuda.synchronize()
@@ -797,7 +803,7 @@ def run_gpu(args, rank, world, local_rank):
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
             dt = float(tt.item())
         e2e = {"value": round(world * bytes_step / dt / GB, 3), "unit": "GB/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h[0]),
+               "h2d_bytes_per_step": int(h2d[0]), "d2h_bytes_per_step": int(d2h[0]),
                "ms_per_step": round(dt * 1e3, 3)}
 
     if rank != 0:

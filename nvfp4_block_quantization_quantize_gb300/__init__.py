@@ -16,7 +16,12 @@ host-buffer path) stage their inputs on the current CUDA device and copy the
 results back (into the caller's host tensors when given, else into new pinned
 ones); they return with their results ready.  Host calls of 256 rows or more
 whose rows are independent run in row chunks, with the copies in, the
-kernels and the copies out of successive chunks overlapping.
+kernels and the copies out of successive chunks overlapping.  With
+``non_blocking=True`` a host call returns once its copies and kernels are
+enqueued, so successive calls overlap too (one call's inputs going in while
+an earlier call's results come back); nvfp4_synchronize() waits for them.  A
+host tensor that a pending call writes is read by later calls only after
+that write.
 """
 from __future__ import annotations
 
@@ -150,6 +155,8 @@ def _device_of(*ts):
 def _stage(t, dev):
     if t is None or t.device == dev:
         return t
+    if not t.is_cuda:                           # after any pending write of it
+        _wait_pending(dev, torch.cuda.current_stream(dev), [t])
     return t.to(dev, non_blocking=True)
 
 
@@ -162,7 +169,8 @@ def _empty(shape, dtype, dev):
 # device copies: inputs (and the residual) are copied to the device, outputs
 # are made in device memory and copied back, into the caller's host tensors
 # when given, else into new pinned ones.  Host calls return with their
-# results ready.  (Kernels reading and writing mapped pinned memory in place
+# results ready unless they are non-blocking (below).  (Kernels reading and
+# writing mapped pinned memory in place
 # over the host link measured 2-2.5x slower than these bulk copies.)
 def _host_in(t, dev):
     """An input (or the in-place residual) of a host call."""
@@ -236,6 +244,8 @@ def _finish_host(res: dict, given: dict, stream=None) -> dict:
     caller's host tensor or a new pinned one, after the call's stream is done;
     then one wait, so everything is ready on return."""
     _sync(stream)
+    dev = next(iter(res.values())).device
+    _wait_pending(dev, torch.cuda.current_stream(dev), [g for g in given.values() if torch.is_tensor(g) and not g.is_cuda])
     out = {}
     for k, v in res.items():
         g = given.get(k)
@@ -266,6 +276,13 @@ _PIPE_CHUNKS = 8
 _PIPE_MIN_ROWS = 256
 _pipe_lock = threading.Lock()
 _pipe_streams = {}
+# Non-blocking host calls (non_blocking=True) enqueue the same three streams
+# and return at once; their host outputs are written when the copies out
+# finish.  _pending[dev] lists (first byte, end byte, event) of host memory
+# still being written: a later host call whose input overlaps one waits for
+# that event before copying it in.  nvfp4_synchronize() (or any device-wide
+# synchronize) makes every result of the device's host calls ready.
+_pending = {}
 
 
 def _row_chunks(M: int):
@@ -295,20 +312,66 @@ def _rows_view(t, M):
     return t.view(M, -1)
 
 
-def _pipelined(dev, M: int, ins, outs, launch, lib):
+def _host_range(t):
+    """[first byte, end byte) of a host tensor's storage."""
+    st = t.untyped_storage()
+    return st.data_ptr(), st.data_ptr() + st.nbytes()
+
+
+def _ranges_overlap(a, b) -> bool:
+    return a[0] < b[1] and b[0] < a[1]
+
+
+def _wait_pending(dev, stream, hosts):
+    """Make stream wait for the unfinished non-blocking copies out that write
+    host memory overlapping any of hosts; finished ones are dropped."""
+    with _pipe_lock:
+        pend = [p for p in _pending.get(dev, []) if not p[2].query()]
+        _pending[dev] = pend
+        if not pend:
+            return
+        for h in hosts:
+            r = _host_range(h)
+            for lo, hi, ev in pend:
+                if _ranges_overlap(r, (lo, hi)):
+                    stream.wait_event(ev)
+
+
+def _add_pending(dev, hosts, ev):
+    with _pipe_lock:
+        _pending.setdefault(dev, []).extend((*_host_range(h), ev) for h in hosts)
+
+
+def nvfp4_synchronize(device=None) -> None:
+    """Wait until every host call on the device (the current one by default),
+    non-blocking ones included, has finished and its results are in host
+    memory."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    for st in _pipe_streams_for(dev):
+        st.synchronize()
+    torch.cuda.current_stream(dev).synchronize()
+    with _pipe_lock:
+        _pending.pop(dev, None)
+
+
+def _pipelined(dev, M: int, ins, outs, launch, lib, blocking: bool = True, whole: bool = False, keep=()):
     """ins: (host, device) row-major pairs copied in chunk by chunk; outs:
     (device, host) pairs copied back; launch(r0, r1, stream) enqueues the
-    kernels of rows [r0, r1) and returns the library status.  Returns with
-    everything done."""
+    kernels of rows [r0, r1) and returns the library status.  whole: one
+    chunk, the tensors copied whole (any shapes).  Returns with everything
+    done, or (not blocking) with everything enqueued: the device buffers are
+    kept from reuse until the streams pass them, and the host outputs are
+    recorded as pending.  keep: device buffers the kernels use besides those."""
     cur = torch.cuda.current_stream(dev)
     s_in, s_cmp, s_out = _pipe_streams_for(dev)
     for st in (s_in, s_cmp, s_out):
         st.wait_stream(cur)
+    _wait_pending(dev, s_in, [h for h, _ in ins])
     rc = OK
-    for r0, r1 in _row_chunks(M):
+    for r0, r1 in ([(0, M)] if whole else _row_chunks(M)):
         with torch.cuda.stream(s_in):
             for h, d in ins:
-                d[r0:r1].copy_(h[r0:r1], non_blocking=True)
+                (d if whole else d[r0:r1]).copy_(h if whole else h[r0:r1], non_blocking=True)
         s_cmp.wait_stream(s_in)
         with torch.cuda.device(dev):
             rc = launch(r0, r1, s_cmp)
@@ -317,10 +380,18 @@ def _pipelined(dev, M: int, ins, outs, launch, lib):
         s_out.wait_stream(s_cmp)
         with torch.cuda.stream(s_out):
             for d, h in outs:
-                h[r0:r1].copy_(d[r0:r1], non_blocking=True)
-    for st in (s_in, s_cmp, s_out):
-        st.synchronize()
-    _check(lib, rc)
+                (h if whole else h[r0:r1]).copy_(d if whole else d[r0:r1], non_blocking=True)
+    if blocking or rc != OK:
+        for st in (s_in, s_cmp, s_out):
+            st.synchronize()
+        _check(lib, rc)
+        return
+    for d in [d for _, d in ins] + [d for d, _ in outs] + [d for d in keep if d is not None]:
+        for st in (s_in, s_cmp, s_out):
+            d.record_stream(st)
+    ev = torch.cuda.Event()
+    ev.record(s_out)
+    _add_pending(dev, [h for _, h in outs], ev)
 
 
 def _host_out(given, shape, dtype):
@@ -328,6 +399,26 @@ def _host_out(given, shape, dtype):
     if given is not None:
         return given
     return torch.empty(shape, dtype=dtype, pin_memory=True)
+
+
+def _host_given(t, name, dtype, n):
+    """A caller's host output of a pipelined call: None when it cannot be
+    written by whole or row-range copies (a device tensor, not contiguous)."""
+    if t is None:
+        return True
+    if t.is_cuda or not t.is_contiguous():
+        return False
+    if t.dtype != dtype or t.numel() != n:
+        raise ValueError(f"nvfp4: {name} must be {dtype} with {n} elements")
+    return True
+
+
+def _gamax_host(gm, gamax, need):
+    """Host tensor a computed gamax (tensor / row) is copied into: the
+    caller's (its first need values) or a new pinned one."""
+    if torch.is_tensor(gamax) and not gamax.is_cuda:
+        return gamax.reshape(-1)[:need]
+    return torch.empty((need,), dtype=torch.float32, pin_memory=True)
 
 
 def _sync(stream=None):
@@ -367,7 +458,7 @@ def _gamax_buffer(mode: int, gamax, M: int, dev, host: bool = False):
             raise ValueError("a *_given gamax_mode needs gamax")
         if not torch.is_tensor(gamax):
             gamax = torch.tensor([float(gamax)], dtype=torch.float32)
-        g = gamax.to(dev, torch.float32).reshape(-1).contiguous()
+        g = _stage(gamax, dev).to(torch.float32).reshape(-1).contiguous()
         if g.numel() < need:
             raise ValueError(f"nvfp4: gamax must hold at least {need} values")
         return g
@@ -377,11 +468,15 @@ def _gamax_buffer(mode: int, gamax, M: int, dev, host: bool = False):
 def nvfp4_quantize(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=None, seed: int = 0,
                    step: int = 0, row_offset: int = 0, gamax_mode="none", gamax=None,
                    err_mode="none", scale_bound=None, colwise: bool = False, codes=None,
-                   scales=None, codes_col=None, scales_col=None, stream=None) -> dict:
+                   scales=None, codes_col=None, scales_col=None, stream=None,
+                   non_blocking: bool = False) -> dict:
     """NVFP4 quantize of a row-major [M,K] float32/bfloat16 tensor (see nvfp4.h).
 
     ``residual`` (float32 [M,K]) is updated in place.  Output tensors may be
-    passed in; otherwise they are allocated with torch on x's device."""
+    passed in; otherwise they are allocated with torch on x's device.  A host
+    call with ``non_blocking`` returns once its copies and kernels are
+    enqueued: its outputs (and the residual) hold the results after
+    nvfp4_synchronize(), and its inputs must stay unchanged until then."""
     lib = load_library()
     host = not x.is_cuda
     dev = _device_of(x, residual)
@@ -392,12 +487,15 @@ def nvfp4_quantize(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=No
     given = {"codes": codes, "scales": scales, "codes_col": codes_col, "scales_col": scales_col}
     if host:
         _host_residual(residual, M, K)
-        if (not colwise and stream is None and M >= _PIPE_MIN_ROWS
-                and gm in (GAMAX_NONE, GAMAX_TENSOR_GIVEN, GAMAX_ROW_GIVEN)):
+        _non_blocking_stream(non_blocking, stream)
+        rows = not colwise and M >= _PIPE_MIN_ROWS and gm in (GAMAX_NONE, GAMAX_TENSOR_GIVEN, GAMAX_ROW_GIVEN)
+        if stream is None and (rows or non_blocking):
             r = _quantize_pipelined(lib, x, dev, M, K, blk, rnd, residual, seed, step, row_offset, gm,
-                                    gamax, em, bound, codes, scales)
+                                    gamax, em, bound, codes, scales, codes_col, scales_col, colwise,
+                                    not non_blocking, not rows)
             if r is not None:
                 return r
+        _non_blocking_refused(non_blocking)
     xd = _host_in(x, dev) if host else x.contiguous()
     rd = _host_in(residual, dev) if host else _dev_residual(residual, dev, M, K)
     g = _gamax_buffer(gm, gamax, M, dev, host)
@@ -429,19 +527,32 @@ def nvfp4_quantize(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=No
     return out
 
 
+def _non_blocking_stream(non_blocking, stream):
+    if non_blocking and stream is not None:
+        raise ValueError("nvfp4: a non-blocking host call runs on the library's own streams (stream=None)")
+
+
+def _non_blocking_refused(non_blocking):
+    if non_blocking:
+        raise ValueError("nvfp4: a non-blocking host call takes contiguous host tensors")
+
+
 def _quantize_pipelined(lib, x, dev, M, K, blk, rnd, residual, seed, step, row_offset, gm, gamax, em, bound,
-                        codes, scales):
-    """The host path of nvfp4_quantize in row chunks (see _pipelined); None
-    when a given host tensor is not a contiguous [M, ...] view."""
+                        codes, scales, codes_col=None, scales_col=None, colwise=False, blocking=True,
+                        whole=False):
+    """The host path of nvfp4_quantize through _pipelined: in row chunks, or
+    (whole) as one chunk for a call whose rows are not independent; None
+    when a host tensor cannot be copied that way (not contiguous, a device
+    output)."""
     xh, rh = _rows_view(x, M), _rows_view(residual, M)
-    for t in (codes, scales):
-        if t is not None and (t.is_cuda or _rows_view(t, M) is None):
-            return None
     if xh is None or (residual is not None and rh is None):
         return None
-    for t, name, dt, n in ((codes, "codes", torch.uint8, M * K // 2), (scales, "scales", torch.uint8, M * K // 16)):
-        if t is not None and (t.dtype != dt or t.numel() != n):
-            raise ValueError(f"nvfp4: {name} must be {dt} with {n} elements")
+    outs_given = [(codes, "codes", M * K // 2), (scales, "scales", M * K // 16)]
+    if colwise:
+        outs_given += [(codes_col, "codes_col", K * M // 2), (scales_col, "scales_col", K * M // 16)]
+    for t, name, n in outs_given:
+        if not _host_given(t, name, torch.uint8, n):
+            return None
     g = _gamax_buffer(gm, gamax, M, dev, True)
     ch = _host_out(codes, (M, K // 2), torch.uint8)
     sh = _host_out(scales, (M, K // 16), torch.uint8)
@@ -450,32 +561,43 @@ def _quantize_pipelined(lib, x, dev, M, K, blk, rnd, residual, seed, step, row_o
     cd, sd = _empty((M, K // 2), torch.uint8, dev), _empty((M, K // 16), torch.uint8, dev)
     ins = [(xh, xd)] + ([(rh, rd)] if rd is not None else [])
     outs = [(cd, _rows_view(ch, M)), (sd, _rows_view(sh, M))] + ([(rd, rh)] if rd is not None else [])
+    ccd = scd = cch = sch = gh = None
+    if colwise:
+        ccd, scd = _empty((K, M // 2), torch.uint8, dev), _empty((K, M // 16), torch.uint8, dev)
+        cch = _host_out(codes_col, (K, M // 2), torch.uint8)
+        sch = _host_out(scales_col, (K, M // 16), torch.uint8)
+        outs += [(ccd, cch.view(K, M // 2)), (scd, sch.view(K, M // 16))]
+    computed = gm in (GAMAX_TENSOR, GAMAX_ROW)
+    if computed:
+        gh = _gamax_host(gm, gamax, g.numel())
+        outs.append((g, gh))
 
     def launch(r0, r1, st):
         gp = g if (g is None or gm != GAMAX_ROW_GIVEN) else g[r0:]
         return lib.nvfp4_quantize(_ptr(xd[r0]), r1 - r0, K, _x_dtype(x), blk, rnd,
                                   _ptr(None if rd is None else rd[r0]), seed, step, row_offset + r0, gm,
-                                  _ptr(gp), em, bound, _ptr(cd[r0]), _ptr(sd[r0]), None, None,
+                                  _ptr(gp), em, bound, _ptr(cd[r0]), _ptr(sd[r0]), _ptr(ccd), _ptr(scd),
                                   ctypes.c_void_p(st.cuda_stream))
 
-    _pipelined(dev, M, ins, outs, launch, lib)
+    _pipelined(dev, M, ins, outs, launch, lib, blocking, whole, keep=(g,))
     out = {"codes": ch, "scales": sh}
-    if g is not None:
+    if colwise:
+        out["codes_col"], out["scales_col"] = cch, sch
+    if computed:
+        out["gamax"] = gamax if torch.is_tensor(gamax) and not gamax.is_cuda else gh
+    elif g is not None:
         out["gamax"] = g.cpu()
     return out
 
 
 def _qdq_pipelined(lib, x, dev, M, K, blk, rnd, residual, seed, step, row_offset, gm, gamax, em, bound,
-                   out, want_codes):
-    """The host path of nvfp4_qdq in row chunks; None as _quantize_pipelined."""
+                   out, want_codes, blocking=True, whole=False):
+    """The host path of nvfp4_qdq through _pipelined; None as _quantize_pipelined."""
     xh, rh = _rows_view(x, M), _rows_view(residual, M)
     if xh is None or (residual is not None and rh is None):
         return None
-    if out is not None:
-        if out.is_cuda or _rows_view(out, M) is None:
-            return None
-        if out.dtype != torch.bfloat16 or out.numel() != M * K:
-            raise ValueError(f"nvfp4: out must be {torch.bfloat16} with {M * K} elements")
+    if not _host_given(out, "out", torch.bfloat16, M * K):
+        return None
     g = _gamax_buffer(gm, gamax, M, dev, True)
     oh = _host_out(out, (M, K), torch.bfloat16)
     xd = _empty((M, K), x.dtype, dev)
@@ -489,6 +611,11 @@ def _qdq_pipelined(lib, x, dev, M, K, blk, rnd, residual, seed, step, row_offset
     outs = [(od, _rows_view(oh, M))] + ([(rd, rh)] if rd is not None else [])
     if want_codes:
         outs += [(cd, ch), (sd, sh)]
+    computed = gm in (GAMAX_TENSOR, GAMAX_ROW)
+    gh = None
+    if computed:
+        gh = _gamax_host(gm, gamax, g.numel())
+        outs.append((g, gh))
 
     def launch(r0, r1, st):
         gp = g if (g is None or gm != GAMAX_ROW_GIVEN) else g[r0:]
@@ -497,27 +624,27 @@ def _qdq_pipelined(lib, x, dev, M, K, blk, rnd, residual, seed, step, row_offset
                              em, bound, _ptr(None if cd is None else cd[r0]), _ptr(None if sd is None else sd[r0]),
                              _ptr(od[r0]), ctypes.c_void_p(st.cuda_stream))
 
-    _pipelined(dev, M, ins, outs, launch, lib)
+    _pipelined(dev, M, ins, outs, launch, lib, blocking, whole, keep=(g,))
     res = {"out": oh}
     if want_codes:
         res["codes"], res["scales"] = ch, sh
-    if g is not None:
+    if computed:
+        res["gamax"] = gamax if torch.is_tensor(gamax) and not gamax.is_cuda else gh
+    elif g is not None:
         res["gamax"] = g.cpu()
     return res
 
 
-def _dequantize_pipelined(lib, codes, scales, dev, M, K, gm, g, bound, od_enum, out):
-    """The host path of nvfp4_dequantize in row chunks; None when a given
-    tensor is not a contiguous row view."""
+def _dequantize_pipelined(lib, codes, scales, dev, M, K, gm, g, bound, od_enum, out, blocking=True,
+                          whole=False):
+    """The host path of nvfp4_dequantize through _pipelined; None when a
+    given tensor is not a contiguous row view."""
     chv, shv = _rows_view(codes, M), _rows_view(scales, M)
     odt = torch.bfloat16 if od_enum == BF16 else torch.float32
     if chv is None or shv is None:
         return None
-    if out is not None:
-        if out.is_cuda or _rows_view(out, M) is None:
-            return None
-        if out.dtype != odt or out.numel() != M * K:
-            raise ValueError(f"nvfp4: out must be {odt} with {M * K} elements")
+    if not _host_given(out, "out", odt, M * K):
+        return None
     oh = _host_out(out, (M, K), odt)
     cd, sd = _empty((M, K // 2), torch.uint8, dev), _empty((M, K // 16), torch.uint8, dev)
     od = _empty((M, K), odt, dev)
@@ -527,14 +654,17 @@ def _dequantize_pipelined(lib, codes, scales, dev, M, K, gm, g, bound, od_enum, 
         return lib.nvfp4_dequantize(_ptr(cd[r0]), _ptr(sd[r0]), r1 - r0, K, gm, _ptr(gp), bound, _ptr(od[r0]),
                                     od_enum, ctypes.c_void_p(st.cuda_stream))
 
-    _pipelined(dev, M, [(chv, cd), (shv, sd)], [(od, _rows_view(oh, M))], launch, lib)
+    _pipelined(dev, M, [(chv, cd), (shv, sd)], [(od, _rows_view(oh, M))], launch, lib, blocking, whole,
+               keep=(g,))
     return oh
 
 
 def nvfp4_qdq(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=None, seed: int = 0,
               step: int = 0, row_offset: int = 0, gamax_mode="none", gamax=None, err_mode="none",
-              scale_bound=None, want_codes: bool = False, out=None, stream=None) -> dict:
-    """quantize then dequantize to bf16 in one pass; ``out`` is bf16 [M,K]."""
+              scale_bound=None, want_codes: bool = False, out=None, stream=None,
+              non_blocking: bool = False) -> dict:
+    """quantize then dequantize to bf16 in one pass; ``out`` is bf16 [M,K].
+    ``non_blocking`` as for nvfp4_quantize."""
     lib = load_library()
     host = not x.is_cuda
     dev = _device_of(x, residual)
@@ -544,11 +674,14 @@ def nvfp4_qdq(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=None, s
     bound = _default_bound(em, scale_bound)
     if host:
         _host_residual(residual, M, K)
-        if stream is None and M >= _PIPE_MIN_ROWS and gm in (GAMAX_NONE, GAMAX_TENSOR_GIVEN, GAMAX_ROW_GIVEN):
+        _non_blocking_stream(non_blocking, stream)
+        rows = M >= _PIPE_MIN_ROWS and gm in (GAMAX_NONE, GAMAX_TENSOR_GIVEN, GAMAX_ROW_GIVEN)
+        if stream is None and (rows or non_blocking):
             r = _qdq_pipelined(lib, x, dev, M, K, blk, rnd, residual, seed, step, row_offset, gm, gamax, em,
-                               bound, out, want_codes)
+                               bound, out, want_codes, not non_blocking, not rows)
             if r is not None:
                 return r
+        _non_blocking_refused(non_blocking)
     xd = _host_in(x, dev) if host else x.contiguous()
     rd = _host_in(residual, dev) if host else _dev_residual(residual, dev, M, K)
     g = _gamax_buffer(gm, gamax, M, dev, host)
@@ -581,7 +714,9 @@ def nvfp4_qdq(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=None, s
 
 def nvfp4_dequantize(codes: torch.Tensor, scales: torch.Tensor, M: int, K: int, *,
                      gamax_mode="none", gamax=None, scale_bound=None, out_dtype="bf16", out=None,
-                     stream=None) -> torch.Tensor:
+                     stream=None, non_blocking: bool = False) -> torch.Tensor:
+    """Codes and scale bytes back to values (see nvfp4.h); ``non_blocking`` as
+    for nvfp4_quantize."""
     lib = load_library()
     host = not codes.is_cuda
     dev = _device_of(codes, scales)
@@ -595,15 +730,20 @@ def nvfp4_dequantize(codes: torch.Tensor, scales: torch.Tensor, M: int, K: int, 
     if gm != GAMAX_NONE:
         if gamax is None:
             raise ValueError("gamax_mode needs gamax")
-        g = (gamax if torch.is_tensor(gamax) else torch.tensor([float(gamax)])).to(dev, torch.float32)
-        g = g.reshape(-1).contiguous()
+        g = _stage(gamax if torch.is_tensor(gamax) else torch.tensor([float(gamax)]), dev)
+        g = g.to(torch.float32).reshape(-1).contiguous()
         need = M if gm in (GAMAX_ROW, GAMAX_ROW_GIVEN) else 1
         if g.numel() < need:
             raise ValueError(f"nvfp4: gamax must hold at least {need} values")
-    if host and not scales.is_cuda and stream is None and M >= _PIPE_MIN_ROWS:
-        r = _dequantize_pipelined(lib, codes, scales, dev, M, K, gm, g, bound, od, out)
+    if host:
+        _non_blocking_stream(non_blocking, stream)
+    if host and not scales.is_cuda and stream is None and (M >= _PIPE_MIN_ROWS or non_blocking):
+        r = _dequantize_pipelined(lib, codes, scales, dev, M, K, gm, g, bound, od, out, not non_blocking,
+                                  M < _PIPE_MIN_ROWS)
         if r is not None:
             return r
+    if host:
+        _non_blocking_refused(non_blocking)
     c = _host_in(codes, dev) if host else codes.contiguous()
     s = _host_in(scales, dev) if host else scales.contiguous()
     o = _out_buf((M, K), torch.bfloat16 if od == BF16 else torch.float32, out, dev, host, "out")

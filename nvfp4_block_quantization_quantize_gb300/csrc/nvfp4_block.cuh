@@ -374,10 +374,11 @@ __device__ __forceinline__ float errsum16_tab(const float* y, uint32_t w0, uint3
 // Approximate error sum of one candidate, no table lookups, in the scaled
 // domain: v = RN(y * enc) is the value the encode rounds to a grid value q
 // (signed like y), an element's approximate error is |RN(q - v)| (one mixed
-// f16/f32 subtract; squared for MSE), summed in element order, and the sum
-// S' is scaled back by K, the error value of grid value 1 (((1 * d) * A) /
-// C): E^ = RN(K * S'), or RN(RN(K * K) * S') for MSE.  The codes are the
-// candidate's exact codes.
+// f16/f32 subtract; squared for MSE, fused into its addition), summed as two
+// interleaved chains (even and odd elements, paired instructions) that are
+// then added, and the sum S' is scaled back by K, the error value of grid
+// value 1 (((1 * d) * A) / C): E^ = RN(K * S'), or RN(RN(K * K) * S') for
+// MSE.  The codes are the candidate's exact codes.
 template <int ERR>
 __device__ __forceinline__ float errsum16_approx(const float* y, float enc, float K, uint32_t& w0,
                                                  uint32_t& w1) {
@@ -388,18 +389,17 @@ __device__ __forceinline__ float errsum16_approx(const float* y, float enc, floa
     uint32_t h[8];
     w0 = e2m1_encode8_dec(v, h);
     w1 = e2m1_encode8_dec(v + 8, h + 4);
-    float S = 0.0f;
+    uint64_t S2 = pack2(0.0f, 0.0f);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         float e0, e1;
         sub_f16x2_f32(h[j], v[2 * j], v[2 * j + 1], e0, e1);
-        if (ERR == NVFP4_ERR_MSE) {
-            const uint64_t D = pack2(e0, e1);
-            unpack2(mul2(D, D), e0, e1);
-        }
-        S = add_rn(S, fabsf(e0));
-        S = add_rn(S, fabsf(e1));
+        const uint64_t D = ERR == NVFP4_ERR_MSE ? pack2(e0, e1) : pack2(fabsf(e0), fabsf(e1));
+        S2 = ERR == NVFP4_ERR_MSE ? fma2(D, D, S2) : add2(S2, D);
     }
+    float s0, s1;
+    unpack2(S2, s0, s1);
+    const float S = add_rn(s0, s1);
     return ERR == NVFP4_ERR_MAE ? mul_rn(K, S) : mul_rn(mul_rn(K, K), S);
 }
 
@@ -409,9 +409,10 @@ __device__ __forceinline__ float errsum16_approx(const float* y, float enc, floa
 //   an error value dq = ((q*d)*A)/C (q*d exact, two roundings) lies within
 //   2.01u |q| K_r of |q| K_r, and its difference with |y| is rounded once;
 //   v = y * enc with enc = RN(1 / RN(d * S_dec)) and S_dec = RN(1 / RN(C / A))
-//   is y / K_r within 5.05u |y| / K_r, q - v is rounded once, the sums in
-//   element order add gamma_15 <= 15.01u of their terms, and K * S' (K within
-//   2.01u of K_r) adds 3.02u:
+//   is y / K_r within 5.05u |y| / K_r, q - v is rounded once, the sums add
+//   gamma_15 <= 15.01u of their terms (the exact sum in element order; the
+//   approximate one passes each term through at most 9 additions, its MSE
+//   squares fused into them), and K * S' (K within 2.01u of K_r) adds 3.02u:
 //   MAE  |E - E^| <= 35.04u E^ + 193u K + 80.8u b   (sum |q| <= 96, sum |y| <= 16 b);
 //   MSE  |d_t^2 - (K_r d_a)^2| = ||d_t| - K_r|d_a|| (|d_t| + K_r|d_a|), with the
 //        first factor <= 12.06u K + 5.05u b + u (|d_t| + K_r|d_a|) and sum |d|

@@ -331,15 +331,8 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
                 for (int i = 0; i < 16; ++i) e[i] = fabsf(e[i]);
             }
         };
-        // column sums F[i] += e[i] (MSE: two columns per instruction)
-        auto col_sums = [&](float* F, const float* e) {
-            if (ERR == NVFP4_ERR_MAE) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) F[i] = add_rn(F[i], e[i]);
-            } else {
-                add16(F, e);
-            }
-        };
+        // column sums F[i] += e[i], two columns per instruction
+        auto col_sums = [&](float* F, const float* e) { add16(F, e); };
         auto row_sums = [&](int r, float R6, float R4) {
             const int i8 = r & 7;
             if (r >= 8) {
@@ -585,14 +578,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_ts(const QuantArgs a) {
                 for (int i = 0; i < 16; ++i) e[i] = fabsf(e[i]);
             }
         };
-        auto col_sums = [&](float* F, const float* e) {
-            if (ERR == NVFP4_ERR_MAE) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) F[i] = add_rn(F[i], e[i]);
-            } else {
-                add16(F, e);
-            }
-        };
+        auto col_sums = [&](float* F, const float* e) { add16(F, e); };
         // row sums: rows 0-7 stored, row r >= 8 added to row r - 8's
         auto row_sums = [&](int r, float R6, float R4) {
             float2* p = reinterpret_cast<float2*>(piece(r & 7, 1));

@@ -73,3 +73,57 @@ def test_pipelined_row_chunks_cover_the_rows_in_whole_tiles():
             assert b == c
         for a, b in ch:
             assert a % 16 == 0 and b > a
+
+
+class _Event:
+    def __init__(self, done):
+        self.done = done
+
+    def query(self):
+        return self.done
+
+
+class _Stream:
+    def __init__(self):
+        self.waited = []
+
+    def wait_event(self, ev):
+        self.waited.append(ev)
+
+
+def test_non_blocking_reads_wait_for_overlapping_pending_writes():
+    """A host tensor that an unfinished non-blocking call writes is read by a
+    later call only after that write's event: the reading stream waits for
+    exactly the events whose host byte ranges overlap the tensors it reads
+    (views of the same storage included); finished writes are dropped."""
+    dev = torch.device("cuda", 7)                       # a key only: nothing runs on it
+    a, b, c = torch.zeros(64), torch.zeros(64), torch.zeros(16)
+    view = a[32:]
+    e1, e2, e3 = _Event(False), _Event(False), _Event(True)
+    nv._pending.pop(dev, None)
+    try:
+        nv._add_pending(dev, [a], e1)
+        nv._add_pending(dev, [b], e2)
+        nv._add_pending(dev, [c], e3)
+        st = _Stream()
+        nv._wait_pending(dev, st, [view])
+        assert st.waited == [e1]
+        st = _Stream()
+        nv._wait_pending(dev, st, [c, torch.zeros(8)])
+        assert st.waited == []                          # c's write finished; a new tensor has none
+        assert [p[2] for p in nv._pending[dev]] == [e1, e2]
+        e1.done = e2.done = True
+        nv._wait_pending(dev, _Stream(), [a])
+        assert nv._pending[dev] == []
+    finally:
+        nv._pending.pop(dev, None)
+    assert nv._ranges_overlap((0, 10), (9, 20)) and not nv._ranges_overlap((0, 10), (10, 20))
+
+
+def test_non_blocking_host_calls_refuse_a_stream():
+    with pytest.raises(ValueError):
+        nv._non_blocking_stream(True, object())
+    nv._non_blocking_stream(True, None)
+    nv._non_blocking_stream(False, object())
+    with pytest.raises(ValueError):
+        nv._non_blocking_refused(True)

@@ -3,8 +3,9 @@
 With a global scale the kernels first form approximate error sums in the
 scaled domain: v = RN(y * enc) is the value the encode rounds to a grid
 value q (signed like y), an element's approximate error is |RN(q - v)|
-(squared for MSE), and the block's (or tile's) sum S' of those, in the
-method's summation order, is scaled back by K (K^2 for MSE), K the error
+(squared for MSE), and the block's (or tile's) sum S' of those (1x16: two
+interleaved chains, then their sum; tiles: column sums in row order, then
+the width-16 tree) is scaled back by K (K^2 for MSE), K the error
 value of grid value 1, ((1 * d) * A) / C: E^ = RN(K * S').  The comparison of
 the two candidates' E^ is accepted only when it is separated by more than a
 rounding bound; otherwise the kernels take the exact sums.  The outputs are
@@ -41,6 +42,20 @@ def _seq(e: np.ndarray) -> np.float32:
     return s
 
 
+def _pairs(d: np.ndarray, err: str) -> np.float32:
+    """The 1x16 kernels' approximate sum: two chains over the even and the
+    odd elements, then their sum; for MSE each square is fused into its
+    chain's addition (emulated in fp64, whose d*d + S is exact or nearly so
+    before the one rounding to fp32)."""
+    s = [f32(0.0), f32(0.0)]
+    for i, x in enumerate(d):
+        if err == "mae":
+            s[i & 1] = f32(s[i & 1] + abs(x))
+        else:
+            s[i & 1] = f32(np.float64(x) * np.float64(x) + np.float64(s[i & 1]))
+    return f32(s[0] + s[1])
+
+
 def _tree16(r) -> np.float32:
     a = [f32(r[i] + r[i + 8]) for i in range(8)]
     b = [f32(a[i] + a[i + 4]) for i in range(4)]
@@ -55,9 +70,10 @@ def _candidates(b, Senc):
     return sf6, sf4
 
 
-def _block_errors(y, sf, A, Sdec, C, err):
+def _block_errors(y, sf, A, Sdec, C, err, signed=False):
     """Exact per-element errors of one candidate on the values y (any shape),
-    the approximate ones in the scaled domain, and K."""
+    the approximate ones in the scaled domain (signed: the differences q - v
+    themselves), and K."""
     d = oracle.e4m3_decode(sf).astype(f32)
     with np.errstate(divide="ignore", over="ignore"):   # a zero scale: enc = FLT_MAX, the encode saturates
         enc = np.minimum(f32(f32(1.0) / f32(d * Sdec)), FLT_MAX)
@@ -68,6 +84,8 @@ def _block_errors(y, sf, A, Sdec, C, err):
     K = f32(f32(f32(f32(1.0) * d) * A) / C)
     with np.errstate(over="ignore", invalid="ignore"):
         diff_a = (q - v).astype(f32)                              # one rounding, as the mixed subtract
+    if signed:
+        return (np.abs(diff_t) if err == "mae" else (diff_t * diff_t).astype(f32)), diff_a, K
     if err == "mae":
         return np.abs(diff_t), np.abs(diff_a), K
     with np.errstate(over="ignore"):                          # squares of huge differences: inf, exact path
@@ -116,8 +134,9 @@ def test_certified_bound_1x16(err, bound):
         sf6, sf4 = _candidates(b, Senc)
         for i, y in enumerate(blocks):
             for sf in (sf6[i], sf4[i]):
-                et, ea, K = _block_errors(y, np.uint8(sf), A, Sdec, C, err)
-                E, Eh = _seq(et), _scaled(_seq(ea), K, err)
+                with np.errstate(over="ignore", invalid="ignore"):
+                    et, da, K = _block_errors(y, np.uint8(sf), A, Sdec, C, err, signed=True)
+                    E, Eh = _seq(et), _scaled(_pairs(da, err), K, err)
                 if not (np.isfinite(E) and np.isfinite(Eh)):
                     continue                 # the kernels take the exact sums
                 gap = abs(float(E) - float(Eh))

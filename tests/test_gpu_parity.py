@@ -360,6 +360,57 @@ def test_host_pipelined_calls(dtype):
         assert_same(dn, e, f"dequantize {od}")
 
 
+def test_host_non_blocking_calls():
+    """Non-blocking host calls (returning once enqueued, so successive calls
+    overlap) give the oracle's bytes: row-chunked calls, whole calls
+    (columnwise output, a computed amax, fewer than 256 rows), a residual
+    carried from one call to the next, a call whose inputs are a pending
+    call's host outputs (codes, scales, gamax), and outputs written into
+    given host tensors."""
+    M, K = 528, 256
+    x = mat((M, K), seed=91, dtype="bf16", outliers=0.01)
+    xs = mat((64, 128), seed=92)                       # under 256 rows: one chunk
+    r0 = mat((M, K), seed=93) * np.float32(0.01)
+    xh, xsh, rh = _host(x), _host(xs), _host(r0)
+    ro = r0.copy()
+    given = torch.empty((M, K // 2), dtype=torch.uint8).pin_memory()
+    sr = []
+    for t in range(3):                                 # the residual read by the next call
+        sr.append(nv.nvfp4_quantize(xh, rounding="sr", seed=5, step=t, residual=rh,
+                                    codes=given if t == 2 else None, non_blocking=True))
+    rc = nv.nvfp4_quantize(xh, block="16x16", gamax_mode="tensor", err_mode="mse", scale_bound=256.0,
+                           colwise=True, non_blocking=True)
+    q1 = nv.nvfp4_quantize(xsh, gamax_mode="tensor", err_mode="mae", scale_bound=256.0, non_blocking=True)
+    dq = nv.nvfp4_dequantize(q1["codes"], q1["scales"], 64, 128, gamax_mode="tensor_given",
+                             gamax=q1["gamax"], scale_bound=256.0, out_dtype="f32", non_blocking=True)
+    qd = nv.nvfp4_qdq(xh, rounding="sr", seed=9, step=1, want_codes=True, non_blocking=True)
+    nv.nvfp4_synchronize()
+    assert sr[2]["codes"] is given
+    for t in range(3):
+        o = oracle.quantize(x, rounding=oracle.SR, seed=5, step=t, residual=ro)
+        assert_same(sr[t]["codes"].numpy(), o["codes"], f"sr step {t} codes")
+        assert_same(sr[t]["scales"].numpy(), o["scales"], f"sr step {t} scales")
+    assert_same(rh.numpy(), ro, "residual after three steps")
+    ga = oracle.amax(x)
+    assert_same(rc["gamax"].numpy(), ga, "computed gamax")
+    o = oracle.quantize(x, block=oracle.BLOCK_16X16, gamax_mode=oracle.GAMAX_TENSOR_GIVEN, gamax=ga,
+                        err_mode=oracle.ERR_MSE, scale_bound=256.0, colwise=True)
+    for k in ("codes", "scales", "codes_col", "scales_col"):
+        assert_same(rc[k].numpy(), o[k], f"row+col {k}")
+    gs = oracle.amax(xs)
+    o1 = oracle.quantize(xs, gamax_mode=oracle.GAMAX_TENSOR_GIVEN, gamax=gs, err_mode=oracle.ERR_MAE,
+                         scale_bound=256.0)
+    assert_same(q1["codes"].numpy(), o1["codes"], "small call codes")
+    e = oracle.dequantize(o1["codes"], o1["scales"], 64, 128, gamax_mode=oracle.GAMAX_TENSOR_GIVEN, gamax=gs,
+                          scale_bound=256.0, out_dtype=oracle.F32)
+    assert_same(dq.numpy(), e, "dequantize of pending outputs")
+    oq = oracle.qdq(x, rounding=oracle.SR, seed=9, step=1)
+    assert_same(qd["out"].view(torch.int16).numpy().view(np.uint16), oq["out"], "qdq out")
+    assert_same(qd["codes"].numpy(), oq["codes"], "qdq codes")
+    with pytest.raises(ValueError):
+        nv.nvfp4_quantize(xh, non_blocking=True, stream=torch.cuda.Stream())
+
+
 def test_stream_argument_is_honoured():
     x = to_dev(mat((256, 256), seed=13))
     s = torch.cuda.Stream()
