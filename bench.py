@@ -98,9 +98,9 @@ def step_plan(M1, K1, M2, K2, Ma, Ka):
         ("W1 SR+EF 1x16", "k_rows<bf16, plain, SR, EF>", e1, e1 * (2 + 4 + 4 + q)),
         ("A 4o6 1x16", "k_rows<bf16, MAE>", ea, ea * (2 + q)),
         ("W2 SR+EF 16x16", "k_band16<bf16, plain, SR, EF>", e2, e2 * (2 + 4 + 4 + q)),
-        ("W1 4o6 16x16 row+col", "k_tile_t<bf16, MAE>", e1, e1 * (2 + 2 * q)),
+        ("W1 4o6 16x16 row+col", "k_tile_ts<bf16, MAE>", e1, e1 * (2 + 2 * q)),
         ("A RTN 1x16", "k_rows<bf16, plain, RTN>", ea, ea * (2 + q)),
-        ("W2 4o6 16x16 row+col", "k_tile_t<bf16, MAE>", e2, e2 * (2 + 2 * q)),
+        ("W2 4o6 16x16 row+col", "k_tile_ts<bf16, MAE>", e2, e2 * (2 + 2 * q)),
         ("A dequantize", "k_dequant<bf16>", ea, ea * (q + 2)),
         ("W2 SR 1x16", "k_rows<bf16, plain, SR>", e2, e2 * (2 + q)),
     ]
