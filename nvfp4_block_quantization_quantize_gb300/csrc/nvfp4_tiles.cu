@@ -704,6 +704,126 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_ts(const QuantArgs a) {
     pdl_trigger();
 }
 
+// Plain 1x16 quantization with rowwise AND columnwise output, bf16 input,
+// nearest rounding (either scale association): one thread per 16x16 tile,
+// staged whole in shared memory as in k_tile_ts.  The tile's 16 rows are
+// its rowwise blocks and its 16 columns its columnwise blocks (rows of x^T),
+// each with its own scale; nothing is shared between them but the read of
+// x, so no barrier is needed until the columnwise output is staged.  A row
+// is read as its two 16-byte pieces; the columns are read as two half
+// tiles (8 columns x 16 rows: piece h of every row, 64 words held in
+// registers), each column's 16 values taken out of the words.  The
+// columnwise codes and scale bytes leave as in k_tile_ts: one 32-byte run
+// and four consecutive scale bytes per column of the CTA.
+template <int RND, bool GS>
+__global__ void __launch_bounds__(kTileThreads) k_tile_r1(const QuantArgs a) {
+    extern __shared__ __align__(16) unsigned char tile_s[];   // [row][thread][32 bytes]
+    __shared__ float rtab[GS ? 1 : 128];
+    __shared__ uint8_t scol[kBands][512];       // columnwise scale bytes, [band][column of the CTA]
+    if (!GS) fill_recip_table(rtab);
+    pdl_wait();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t M = a.M, K = a.K;
+    const int64_t band0 = static_cast<int64_t>(blockIdx.x) * kBands, band = band0 + warp;
+    const int64_t tile0 = static_cast<int64_t>(blockIdx.y) * 32, tile = tile0 + lane;
+    const int64_t nb = K / 16, nbands = M / 16;
+    const bool own = band < nbands && tile < nb;
+    const int64_t base = band * 16 * K + tile * 16;
+    const uint32_t swz = piece_swizzle<2>(tid);
+    auto slot = [&](int r) { return tile_s + (r * kTileThreads + tid) * 32; };
+    auto piece = [&](int r, uint32_t c) { return slot(r) + ((c ^ swz) << 4); };
+    if (own) {
+        const unsigned char* gx = static_cast<const unsigned char*>(a.x) + base * 2;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            cp_async16(piece(r, 0), gx + static_cast<int64_t>(r) * K * 2);
+            cp_async16(piece(r, 1), gx + static_cast<int64_t>(r) * K * 2 + 16);
+            if ((r & 3) == 3) cp_async_commit();
+        }
+    }
+    GScale g{0.0f, 1.0f, 1.0f};
+    if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
+        g.A = a.gamax[0];
+        global_scales(g.A, a.bound, g.Senc, g.Sdec);
+    }
+    // one 1x16 block: codes and scale byte
+    auto quant16 = [&](const float* y, uint32_t& w0, uint32_t& w1, uint32_t& sf) {
+        const float b = absmax16(y);
+        const float s6f = block_scale<GS>(b, g.Senc, RND == NVFP4_RTN_STD);
+        sf = e4m3_encode(min_nd(s6f, 448.0f));
+        const float d = e4m3_decode(sf);
+        const float D = GS ? mul_rn(d, g.Sdec) : d;
+        float q[16];
+        encode_plain16<RND>(y, D, b, 0, a.pk, w0, w1, GS ? nullptr : rtab, sf, q, false);
+    };
+    uint32_t cw[16][2];                         // columnwise code words of the tile's columns
+    if (own) {
+        const int64_t nbr = K / 16;
+        auto row_pass = [&](int r0) {           // rows r0 .. r0 + 3, rowwise blocks
+#pragma unroll 2
+            for (int r = r0; r < r0 + 4; ++r) {
+                float y[16];
+                lds16_swz<NVFP4_BF16>(slot(r), swz, y);
+                uint32_t w0, w1, sf;
+                quant16(y, w0, w1, sf);
+                const int64_t rowg = band * 16 + r;
+                reinterpret_cast<uint2*>(a.codes)[(rowg * K + tile * 16) / 16] = make_uint2(w0, w1);
+                a.scales[rowg * nbr + tile] = static_cast<uint8_t>(sf);
+            }
+        };
+        cp_async_wait<3>();
+        row_pass(0);
+        cp_async_wait<2>();
+        row_pass(4);
+        cp_async_wait<1>();
+        row_pass(8);
+        cp_async_wait<0>();
+        row_pass(12);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {           // columns 8h .. 8h + 7
+            uint32_t wv[16][4];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const uint4 u = *reinterpret_cast<const uint4*>(piece(r, h));
+                wv[r][0] = u.x;
+                wv[r][1] = u.y;
+                wv[r][2] = u.z;
+                wv[r][3] = u.w;
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float y[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r)
+                    y[r] = __uint_as_float((c & 1) ? (wv[r][c >> 1] & 0xFFFF0000u) : (wv[r][c >> 1] << 16));
+                uint32_t sf;
+                quant16(y, cw[8 * h + c][0], cw[8 * h + c][1], sf);
+                scol[warp][lane * 16 + 8 * h + c] = static_cast<uint8_t>(sf);
+            }
+        }
+    }
+    // columnwise output as in k_tile_ts, staged in the tile buffer once every
+    // thread is done with its slots
+    __syncthreads();
+    uint2* stg = reinterpret_cast<uint2*>(tile_s);
+    if (own) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) stg[stage_index(warp, lane * 16 + c)] = make_uint2(cw[c][0], cw[c][1]);
+    }
+    __syncthreads();
+    uint2* cc = reinterpret_cast<uint2*>(a.codes_col);
+#pragma unroll 4
+    for (int q = tid; q < 512 * kBands; q += kTileThreads) {
+        const int j = q / kBands, bb = q % kBands;          // column of the CTA, band of the CTA
+        const int64_t col = tile0 * 16 + j, bnd = band0 + bb;
+        if (col < K && bnd < nbands) {
+            cc[col * nbands + bnd] = stg[stage_index(bb, j)];
+            a.scales_col[col * nbands + bnd] = scol[bb][j];
+        }
+    }
+    pdl_trigger();
+}
+
 // Plain (map-to-6) 16x16 quantization with rowwise AND columnwise output:
 // the tile's one scale serves both outputs and x^T's codes are x's codes
 // transposed (stochastic rounding draws are keyed on x's index), so a thread
@@ -883,6 +1003,24 @@ int launch_tile_t(const QuantArgs& a, cudaStream_t s) {
     }
 }
 
+// k_tile_r1: 64 KB of dynamic shared memory (set once per device)
+template <int RND, bool GS>
+int launch_tile_r1(const QuantArgs& a, cudaStream_t s) {
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_dev != dev) {
+        cudaFuncSetAttribute(k_tile_r1<RND, GS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStagedTileBytes);
+        cudaFuncSetAttribute(k_tile_r1<RND, GS>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+        configured_dev = dev;
+    }
+    const dim3 grid(static_cast<unsigned>((a.M / 16 + kBands - 1) / kBands),
+                    static_cast<unsigned>((a.K / 16 + 31) / 32));
+    launch_pdl(k_tile_r1<RND, GS>, grid, kTileThreads, kStagedTileBytes, s, a);
+    return static_cast<int>(cudaGetLastError());
+}
+
 // rowwise + columnwise outputs (no residual)
 template <int DT, int BLK>
 int tiles_dispatch_blk(const QuantArgs& a, cudaStream_t s) {
@@ -905,6 +1043,11 @@ int tiles_dispatch_blk(const QuantArgs& a, cudaStream_t s) {
     if (a.rounding == NVFP4_SR)
         return gs ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, true>, a, s)
                   : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_SR, false>, a, s);
+    if constexpr (DT == NVFP4_BF16) {           // nearest rounding, bf16: a thread per staged tile
+        if (a.rounding == NVFP4_RTN_STD)
+            return gs ? launch_tile_r1<NVFP4_RTN_STD, true>(a, s) : launch_tile_r1<NVFP4_RTN_STD, false>(a, s);
+        return gs ? launch_tile_r1<NVFP4_RTN, true>(a, s) : launch_tile_r1<NVFP4_RTN, false>(a, s);
+    }
     if (a.rounding == NVFP4_RTN_STD)
         return gs ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN_STD, true>, a, s)
                   : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_NONE, NVFP4_RTN_STD, false>, a, s);

@@ -92,13 +92,14 @@ def test_standard_association_qdq():
     assert_same(to_np(res_g), res_o, "residual")
 
 
-SR_COL = list(itertools.product(["f32", "bf16"], ["1x16", "16x16"], ["none", "tensor", "tensor_given"]))
+PLAIN_COL = list(itertools.product(["rtn", "sr"], ["f32", "bf16"], ["1x16", "16x16"],
+                                   ["none", "tensor", "tensor_given"]))
 
 
-@pytest.mark.parametrize("dtype,block,gm", SR_COL)
-def test_sr_columnwise(dtype, block, gm):
-    x = W.matrix((304, 336), seed=_seed("sr", dtype, block, gm), dtype=dtype, dist="t")
-    kw = dict(block=block, rounding="sr", seed=13, step=6, row_offset=48, gamax_mode=gm, colwise=True)
+@pytest.mark.parametrize("rounding,dtype,block,gm", PLAIN_COL)
+def test_plain_columnwise(rounding, dtype, block, gm):
+    x = W.matrix((304, 336), seed=_seed(rounding, dtype, block, gm), dtype=dtype, dist="t")
+    kw = dict(block=block, rounding=rounding, seed=13, step=6, row_offset=48, gamax_mode=gm, colwise=True)
     if gm == "tensor_given":
         kw["gamax"] = np.array([9.25], np.float32)
     gpu, o = quantize_both(x, **kw)
@@ -113,7 +114,23 @@ def test_sr_columnwise(dtype, block, gm):
         assert np.array_equal(cols, rows.T)
 
 
-def test_sr_columnwise_specials():
+@pytest.mark.parametrize("rounding", ["rtn", "sr"])
+def test_plain_columnwise_specials(rounding):
     x = W.c4_specials(W.c4(256, 512), with_inf_nan=True)
-    gpu, o = quantize_both(x, block="1x16", rounding="sr", seed=2, step=3, colwise=True)
-    compare_quant(gpu, o)
+    for dt in (x, W.to_bf16_bits(x)):
+        gpu, o = quantize_both(dt, block="1x16", rounding=rounding, seed=2, step=3, colwise=True)
+        compare_quant(gpu, o)
+
+
+@pytest.mark.parametrize("rounding", ["rtn", "rtn_std"])
+@pytest.mark.parametrize("shape", [(16, 16), (48, 1552), (272, 528), (80, 48)])
+def test_rtn_columnwise_shapes(rounding, shape):
+    """1x16 rowwise + columnwise nearest rounding over CTA-sized and ragged
+    shapes: one tile; 97 tiles across (four CTA columns, the last ragged);
+    17 bands (five CTA rows, the last with one band); fewer tiles than a
+    warp's lanes."""
+    for dtype in ("bf16", "f32"):
+        x = W.matrix(shape, seed=_seed("rtncol", rounding, shape, dtype), dtype=dtype, dist="t")
+        for gm in ("none", "tensor"):
+            gpu, o = quantize_both(x, block="1x16", rounding=rounding, gamax_mode=gm, colwise=True)
+            compare_quant(gpu, o)
