@@ -108,6 +108,13 @@ __device__ __forceinline__ void fill_recip_table(float* rt) {
     __syncthreads();
 }
 
+// The nearest path's quotients outside the reciprocal sequence's range: IEEE
+// divisions, out of line (the blocks that need them are rare, and the fast
+// path is inlined many times in the tile kernels).
+static __device__ __noinline__ void plain_quotients16_ieee(const float* y, float D, float* v) {
+    for (int i = 0; i < 16; ++i) v[i] = plain_quotient<false>(y[i], D, 0.0f, false);
+}
+
 // codes of y / D (D = decoded scale * S_dec), nearest or stochastic; a zero
 // divisor zeroes the block.  b is the block amax (bounds |y|).  rt: the
 // reciprocal table when D is a bare E4M3 scale sf (no global scale), else
@@ -145,9 +152,13 @@ __device__ __forceinline__ void encode_plain16_impl(const float* y, float D, flo
                 v[i] = sign_of_first(q0a, qa);
                 v[i + 1] = sign_of_first(q0b, qb);
             }
-        } else {
+        } else {                                // copies, so that y and v stay in registers
+            float yl[16], vl[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = plain_quotient<false>(y[i], D, r, false);
+            for (int i = 0; i < 16; ++i) yl[i] = y[i];
+            plain_quotients16_ieee(yl, D, vl);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = vl[i];
         }
         w0 = e2m1_encode8(v);
         w1 = e2m1_encode8(v + 8);
