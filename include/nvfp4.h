@@ -33,7 +33,7 @@
  *   - M == 0 or K == 0 is a valid empty call (a per-tensor amax of an empty
  *     tensor is +0).  K must be a multiple of 16 [fp4-train, Requirements and
  *     limits]; 16x16 blocks and columnwise outputs also need M % 16 == 0.
- *     M and K are each below 2^35.
+ *     M and K are each below 2^35; a columnwise output needs K <= 16776960.
  *
  * Arithmetic: fp32, round-to-nearest-even, correctly rounded division, no
  * fused multiply-add and no flush-to-zero on the pinned steps [4o6 PR, Design].
@@ -134,7 +134,8 @@ enum nvfp4_status { NVFP4_OK = 0, NVFP4_EINVAL = 1, NVFP4_ECUDA = 2 };
  * with SR or RTN_STD, a residual, gamax NONE or a bound other than 256/448
  * (the recipe is nearest-rounding only [4o6 PR, What]); columnwise with a
  * residual (one residual cannot serve two quantizations); a bound outside
- * (0, 448]; only one of codes_col / scales_col given.
+ * (0, 448]; only one of codes_col / scales_col given; a columnwise output
+ * with K > 16776960.
  */
 int nvfp4_quantize(const void* x, int64_t M, int64_t K, int dtype, int block, int rounding,
                    float* residual, uint64_t seed, uint64_t step, int64_t row_offset,

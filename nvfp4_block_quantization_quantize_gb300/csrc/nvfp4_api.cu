@@ -47,6 +47,10 @@ int check_shape(int64_t M, int64_t K) {
 
 bool is_row_mode(int g) { return g == NVFP4_GAMAX_ROW || g == NVFP4_GAMAX_ROW_GIVEN; }
 
+// Largest K with a columnwise output: 65535 CTA columns of 256 (1x16 row-owner
+// kernel; the tile kernels cover 512 columns per CTA column).
+constexpr int64_t kMaxColwiseK = 65535LL * 256;
+
 // Checks shared by quantize and qdq.
 int check_quant(const void* x, int64_t M, int64_t K, int dtype, int block, int rounding,
                 const float* residual, int gamax_mode, const float* gamax, int err_mode,
@@ -73,6 +77,8 @@ int check_quant(const void* x, int64_t M, int64_t K, int dtype, int block, int r
         if (bound != 256.0f && bound != 448.0f) return fail(NVFP4_EINVAL, "four-over-six bound must be 256 or 448");
     }
     if (colwise && residual) return fail(NVFP4_EINVAL, "columnwise output takes no residual");
+    if (colwise && K > kMaxColwiseK)            // the columnwise kernels' grid spans K along y
+        return fail(NVFP4_EINVAL, "columnwise output needs K <= %lld", static_cast<long long>(kMaxColwiseK));
     const bool any = M > 0 && K > 0;
     if ((rc = check_ptr(x, "x", any))) return rc;
     if ((rc = check_ptr(residual, "residual", false))) return rc;

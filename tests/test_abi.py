@@ -90,6 +90,7 @@ BAD_QUANT = {
     "4o6 without global amax": dict(err=1, bound=256.0),
     "4o6 bound 300": dict(err=1, gm=1, gamax=A16, bound=300.0),
     "columnwise with residual": dict(residual=A16, ccol=A16, scol=A16),
+    "columnwise with K past the grid": dict(K=65535 * 256 + 16, ccol=A16, scol=A16),
     "x NULL": dict(x=None),
     "codes NULL": dict(codes=None),
     "scales NULL": dict(scales=None),
