@@ -22,13 +22,12 @@
 //               tiles (fully coalesced), and the columnwise output, staged in
 //               shared memory, leaves as one 32-byte run per column (4 bands
 //               x 8 bytes) instead of 8-byte pieces 32 to a warp store.
-// k_tile_t      the same for fp32 input, whose 1 KB tiles are too large to
-//               stage whole: each thread streams its 32 row reads through a
-//               3-slot ring of asynchronous copies, two reads ahead, and the
-//               code words wait in shared memory until the tile's choices
-//               are known (both candidates' code words, so x is read only
-//               twice).  The row loops stay rolled (a fully unrolled kernel
-//               overflowed the instruction cache).
+// k_tile_ts2    the same for fp32 input with two threads per tile (lanes 2t
+//               and 2t+1: columns 0-7 and 8-15), so that a thread's share,
+//               16 rows x 8 fp32, is staged whole too; the pair exchanges the
+//               tile amax and the column sums by shuffles, and on the exact
+//               path passes each row's partial sum from the left lane to the
+//               right.  A CTA is 4 bands x 16 tiles.
 //
 // Method: "Add NVFP4 four-over-six (row-wise) quantization to the training
 // prototype" (What: 16x16 blocks, rowwise / columnwise; CuTe DSL kernel
@@ -191,13 +190,6 @@ __global__ void __launch_bounds__(kThreads) k_tiles_rows(const QuantArgs a) {
 // ---------------------------------------------------------------------------------------------
 constexpr int kTileThreads = 128;
 
-// Ring of fp32 tile rows per thread of k_tile_t (3 slots of 64-byte rows).
-struct TileRing {
-    static constexpr int XB = 64;               // bytes of one tile row
-    static constexpr int SLOTS = 3;
-    static constexpr int BYTES = SLOTS * kTileThreads * XB;
-};
-
 // Ring of tile rows per thread of k_tile_p: 4 slots of bf16 rows, 3 of fp32
 // rows (the same bytes in flight).
 template <int DT>
@@ -225,256 +217,13 @@ __device__ __forceinline__ int stage_index(int b, int j) {
     return b * 512 + (j ^ ((j >> 4) & 15) ^ ((b & 1) << 3));
 }
 
-template <int DT, int ERR>
-__global__ void __launch_bounds__(kTileThreads) k_tile_t(const QuantArgs a) {
-    static_assert(DT == NVFP4_F32, "bf16 input takes k_tile_ts");
-    using Rg = TileRing;
-    __shared__ float tenc[128];                 // encode reciprocal of every scale byte
-    // per thread and candidate: the error value magnitude |dq| of each grid
-    // index k, [candidate][k][thread] so a warp's lookups are conflict-free
-    __shared__ float dqt[2][8][kTileThreads];
-    // exact path, per thread and candidate: row sums of rows 0-7, then the
-    // width-16 tree's first level (row i + row i + 8), [candidate][i][thread]
-    // so a warp's accesses are conflict-free
-    __shared__ float sR[2][8][kTileThreads];
-    // both candidates' code words of every row (map-to-6: [0..1], map-to-4: [2..3])
-    __shared__ uint32_t sW[4][16][kTileThreads];
-    // ring of tile rows: the thread streams its tile's rows twice (32 row
-    // reads) through Rg::SLOTS slots of asynchronous copies
-    __shared__ __align__(16) unsigned char ring[Rg::BYTES];
-    __shared__ uint8_t scol[kBands][32];        // columnwise scale byte of each tile
-    pdl_wait();
-    GScale g{0.0f, 1.0f, 1.0f};
-    if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
-        g.A = a.gamax[0];
-        global_scales(g.A, a.bound, g.Senc, g.Sdec);
-    }
-    const float C = mul_rn(6.0f, a.bound);
-    for (int i = threadIdx.x; i < 128; i += blockDim.x)
-        tenc[i] = min_nd(div_rn(1.0f, mul_rn(e4m3_decode(static_cast<uint32_t>(i)), g.Sdec)), FLT_MAX);
-    __syncthreads();
-
-    // warp w: band kBands * blockIdx.x + w; lane l: tile 32 * blockIdx.y + l
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t M = a.M, K = a.K;
-    const int64_t band0 = static_cast<int64_t>(blockIdx.x) * kBands, band = band0 + warp;
-    const int64_t tile0 = static_cast<int64_t>(blockIdx.y) * 32, tile = tile0 + lane;
-    const int64_t nb = K / 16, nbands = M / 16;
-    uint32_t lo[16], hi[16];                    // columnwise code words, transposed
-    uint32_t sf_c = 0;
-    if (band < nbands && tile < nb) {
-        const int64_t base = band * 16 * K + tile * 16;
-        const unsigned char* gx = static_cast<const unsigned char*>(a.x) + base * (Rg::XB / 16);
-        const int64_t row_bytes = K * (Rg::XB / 16);
-        unsigned char* slot0 = ring + tid * Rg::XB;
-
-        // row read j (0..31) is tile row j % 16, into slot j % Rg::SLOTS
-        auto issue = [&](int j) {
-            if (j < 32) {
-                const unsigned char* src = gx + static_cast<int64_t>(j & 15) * row_bytes;
-                unsigned char* dst = slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB);
-#pragma unroll
-                for (int c = 0; c < Rg::XB / 16; ++c) cp_async16(dst + 16 * c, src + 16 * c);
-            }
-            cp_async_commit();
-        };
-        auto next_row = [&](int j, float* y) {       // row read j, ready in y
-            issue(j + Rg::SLOTS - 1);
-            cp_async_wait<Rg::SLOTS - 1>();
-            lds16<DT>(slot0 + (j % Rg::SLOTS) * (kTileThreads * Rg::XB), y);
-        };
-#pragma unroll
-        for (int j = 0; j < Rg::SLOTS - 1; ++j) issue(j);
-
-        // pass 0: tile amax
-        float y[16];
-        float b = 0.0f;
-#pragma unroll 1
-        for (int r = 0; r < 16; ++r) {
-            next_row(r, y);
-            b = max_nd(b, absmax16(y));
-        }
-        const float s6f = block_s6f<true>(b, g.Senc);
-        const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
-        const uint32_t sf4 = e4m3_encode(min_nd(mul_rn(s6f, 1.5f), 448.0f));
-        const float enc6 = tenc[sf6], enc4 = tenc[sf4];
-        const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
-        // K: the error value of grid value 1, ((1 * d) * A) / (6 * bound)
-        const float K6 = div_rn(mul_rn(d6, g.A), C), K4 = div_rn(mul_rn(d4, g.A), C);
-
-        // pass 1: both candidates' codes, and approximate per-element errors in
-        // the scaled domain, |q - v| with v = y * enc (squared for MSE; q the
-        // code's signed grid value) from one mixed f16/f32 subtract, no table
-        // lookup; column sums in registers, accumulated in row order, their
-        // tree scaled back by K (K^2 for MSE) at the end
-        float F6[16], F4[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
-        const uint64_t ENC6 = pack2(enc6, enc6), ENC4 = pack2(enc4, enc4);
-        auto candidate = [&](const float* y, uint64_t enc2, uint32_t& w0, uint32_t& w1, float* e) {
-            float v[16];
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) unpack2(mul2(pack2(y[i], y[i + 1]), enc2), v[i], v[i + 1]);
-            uint32_t h[8];
-            w0 = e2m1_encode8_dec(v, h);
-            w1 = e2m1_encode8_dec(v + 8, h + 4);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                sub_f16x2_f32(h[j], v[2 * j], v[2 * j + 1], e[2 * j], e[2 * j + 1]);
-                if (ERR != NVFP4_ERR_MAE) {
-                    const uint64_t D = pack2(e[2 * j], e[2 * j + 1]);
-                    unpack2(mul2(D, D), e[2 * j], e[2 * j + 1]);
-                }
-            }
-            if (ERR == NVFP4_ERR_MAE) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) e[i] = fabsf(e[i]);
-            }
-        };
-        // column sums F[i] += e[i], two columns per instruction
-        auto col_sums = [&](float* F, const float* e) { add16(F, e); };
-        auto row_sums = [&](int r, float R6, float R4) {
-            const int i8 = r & 7;
-            if (r >= 8) {
-                R6 = add_rn(sR[0][i8][tid], R6);
-                R4 = add_rn(sR[1][i8][tid], R4);
-            }
-            sR[0][i8][tid] = R6;
-            sR[1][i8][tid] = R4;
-        };
-#pragma unroll 2
-        for (int r = 0; r < 16; ++r) {
-            next_row(16 + r, y);
-            float e[16];
-            uint32_t w0, w1;
-            candidate(y, ENC6, w0, w1, e);
-            sW[0][r][tid] = w0;
-            sW[1][r][tid] = w1;
-            col_sums(F6, e);
-            candidate(y, ENC4, w0, w1, e);
-            sW[2][r][tid] = w0;
-            sW[3][r][tid] = w1;
-            col_sums(F4, e);
-        }
-        cp_async_wait<0>();
-        float E6r, E4r, E6c, E4c;
-        auto tree_sums = [&]() {
-            float S[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) S[i] = sR[0][i][tid];
-            E6r = tree16_upper(S);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) S[i] = sR[1][i][tid];
-            E4r = tree16_upper(S);
-            E6c = tree16_regs(F6);
-            E4c = tree16_regs(F4);
-        };
-        {   // back from the scaled domain: E^ = RN(K * S'), or RN(RN(K * K) * S')
-            const float k6 = ERR == NVFP4_ERR_MAE ? K6 : mul_rn(K6, K6);
-            const float k4 = ERR == NVFP4_ERR_MAE ? K4 : mul_rn(K4, K4);
-            E6r = E6c = mul_rn(k6, tree16_regs(F6));
-            E4r = E4c = mul_rn(k4, tree16_regs(F4));
-        }
-        // one approximate sum per candidate serves both choices: the rowwise
-        // and the columnwise exact sums add the same 256 terms, each through
-        // at most 19 additions, so both lie within the tile bound of it
-        if (!tile_sums_decide<ERR>(E6c, E4c, K6, K4, b)) {
-            // the exact sums: error values |dq| = ((G[k] * d) * A) / (6 * bound)
-            // of each grid magnitude G[k] from a per-thread table (a code of
-            // index k stands for +-|dq| with the sign of its y, so |dq - y| =
-            // | |dq| - |y| | exactly, and likewise the square), the codes kept
-            // in sW, the rows read again
-            const float G[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                dqt[0][k][tid] = div_rn(mul_rn(mul_rn(G[k], d6), g.A), C);
-                dqt[1][k][tid] = div_rn(mul_rn(mul_rn(G[k], d4), g.A), C);
-            }
-            auto exact = [&](const float* y, uint32_t w0, uint32_t w1, int c, float* e) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const uint32_t k = ((i < 8 ? w0 : w1) >> (4 * (i & 7))) & 7u;
-                    const float diff = sub_rn(dqt[c][k][tid], fabsf(y[i]));
-                    e[i] = (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff);
-                }
-            };
-#pragma unroll
-            for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
-#pragma unroll 1
-            for (int r = 0; r < 16; ++r) {
-                load16<DT>(a.x, base + static_cast<int64_t>(r) * K, y);
-                float e[16];
-                exact(y, sW[0][r][tid], sW[1][r][tid], 0, e);
-                const float R6 = seq_sum16(e);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) F6[i] = add_rn(F6[i], e[i]);
-                exact(y, sW[2][r][tid], sW[3][r][tid], 1, e);
-                const float R4 = seq_sum16(e);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) F4[i] = add_rn(F4[i], e[i]);
-                row_sums(r, R6, R4);
-            }
-            tree_sums();
-        }
-        const bool row4 = E4r < E6r, col4 = E4c < E6c;       // ties and NaN keep map-to-6
-        const uint8_t sf_r = static_cast<uint8_t>(row4 ? sf4 : sf6);
-
-        // store the rowwise codes of the chosen candidate; gather the columnwise one's
-        const int64_t nbr = K / 16;
-        const int wr = row4 ? 2 : 0, wc = col4 ? 2 : 0;
-#pragma unroll 1
-        for (int r = 0; r < 16; ++r) {
-            const int64_t rowg = band * 16 + r;
-            reinterpret_cast<uint2*>(a.codes)[(rowg * K + tile * 16) / 16] =
-                make_uint2(sW[wr][r][tid], sW[wr + 1][r][tid]);
-            a.scales[rowg * nbr + tile] = sf_r;
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            lo[r] = sW[wc][r][tid];
-            hi[r] = sW[wc + 1][r][tid];
-        }
-        transpose8x8_nibbles(lo);          // rows 0-7,  cols 0-7
-        transpose8x8_nibbles(lo + 8);      // rows 8-15, cols 0-7
-        transpose8x8_nibbles(hi);          // rows 0-7,  cols 8-15
-        transpose8x8_nibbles(hi + 8);      // rows 8-15, cols 8-15
-        sf_c = col4 ? sf4 : sf6;
-    }
-    // columnwise output: x^T's row (tile0 * 16 + j) holds 8 code bytes of each
-    // band, so the CTA's kBands bands give each of its 512 columns 32
-    // consecutive bytes (one sector) and kBands consecutive scale bytes.  The
-    // transposed words are staged in the code-word buffer (free once every
-    // thread has read its own) and written column by column.
-    __syncthreads();
-    uint2* stg = reinterpret_cast<uint2*>(&sW[0][0][0]);
-    if (band < nbands && tile < nb) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            stg[stage_index(warp, lane * 16 + c)] = make_uint2(lo[c], lo[8 + c]);
-            stg[stage_index(warp, lane * 16 + 8 + c)] = make_uint2(hi[c], hi[8 + c]);
-        }
-    }
-    scol[warp][lane] = static_cast<uint8_t>(sf_c);
-    __syncthreads();
-    uint2* cc = reinterpret_cast<uint2*>(a.codes_col);
-#pragma unroll 4
-    for (int q = tid; q < 512 * kBands; q += kTileThreads) {
-        const int j = q / kBands, bb = q % kBands;          // column of the CTA, band of the CTA
-        const int64_t col = tile0 * 16 + j, bnd = band0 + bb;
-        if (col < K && bnd < nbands) {
-            cc[col * nbands + bnd] = stg[stage_index(bb, j)];
-            a.scales_col[col * nbands + bnd] = scol[bb][j >> 4];
-        }
-    }
-    pdl_trigger();
-}
-
 // Four-over-six 16x16 with rowwise and columnwise output, bf16 input, the
-// whole tile staged: the same per-tile work as k_tile_t (one thread per tile,
-// both candidates' row and column sums from one walk, the certified sums with
-// the exact fallback), but each thread copies its tile's 16 rows (512 bytes)
-// into shared memory with asynchronous copies as soon as it starts, so the
-// error pass reads shared memory instead of waiting on L2 one row ahead.  The
+// whole tile staged: one thread per tile computes both candidates' codes and
+// errors from one walk, certifies both choices with one approximate sum per
+// candidate and falls back to the exact sums where that fails.  Each thread
+// copies its tile's 16 rows (512 bytes) into shared memory with
+// asynchronous copies as soon as it starts, so the error pass reads shared
+// memory instead of waiting on L2 one row ahead.  The
 // 64 KB of a CTA's tiles leaves room for three CTAs per SM, so the other
 // CTAs' error passes cover a CTA's copies.  A thread's slot of row r (32
 // bytes, its 16-byte pieces swizzled by piece_swizzle<2>) is reused once row
@@ -552,8 +301,10 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_ts(const QuantArgs a) {
         // K: the error value of grid value 1, ((1 * d) * A) / (6 * bound)
         const float K6 = div_rn(mul_rn(d6, g.A), C), K4 = div_rn(mul_rn(d4, g.A), C);
 
-        // pass 1: as k_tile_t's (scaled-domain approximate errors, row sums
-        // and column sums in row order), reading the staged rows
+        // pass 1: both candidates' codes, and approximate per-element errors
+        // in the scaled domain, |q - v| with v = y * enc (squared for MSE; q
+        // the code's signed grid value) from one mixed f16/f32 subtract; the
+        // column sums in row order, from the staged rows
         float F6[16], F4[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) F6[i] = F4[i] = 0.0f;
@@ -622,9 +373,12 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_ts(const QuantArgs a) {
             E4r = E4c = mul_rn(k4, tree16_regs(F4));
         }
         if (!tile_sums_decide<ERR>(E6c, E4c, K6, K4, b)) {
-            // the exact sums as in k_tile_t: error values |dq| of each grid
-            // magnitude (row 8 + k's second piece: map-to-6, map-to-4), the
-            // codes kept in the first pieces, x read again
+            // the exact sums: error values |dq| = ((G[k] * d) * A) / (6 *
+            // bound) of each grid magnitude (a code of index k stands for
+            // +-|dq| with the sign of its y, so |dq - y| = | |dq| - |y| |
+            // exactly, and likewise the square) in row 8 + k's second piece
+            // (map-to-6, map-to-4), the codes kept in the first pieces, x
+            // read again; row sums in element order and x^T's column sums
             const float G[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
 #pragma unroll
             for (int k = 0; k < 8; ++k)
@@ -679,7 +433,11 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_ts(const QuantArgs a) {
         transpose8x8_nibbles(hi + 8);      // rows 8-15, cols 8-15
         sf_c = col4 ? sf4 : sf6;
     }
-    // columnwise output as in k_tile_t, staged in the tile buffer
+    // columnwise output: x^T's row (tile0 * 16 + j) holds 8 code bytes of
+    // each band, so the CTA's kBands bands give each of its 512 columns 32
+    // consecutive bytes (one sector) and kBands consecutive scale bytes.  The
+    // transposed words are staged in the tile buffer, once every thread is
+    // done with its slots, and written column by column.
     __syncthreads();
     uint2* stg = reinterpret_cast<uint2*>(tile_s);
     if (own) {
@@ -824,16 +582,296 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_r1(const QuantArgs a) {
     pdl_trigger();
 }
 
+// Four-over-six 16x16 with rowwise and columnwise output, fp32 input, two
+// threads per tile: lanes 2t and 2t+1 of a warp hold columns 0-7 and 8-15 of
+// tile t (16 tiles per warp, one band per warp, a CTA 4 bands x 16 tiles),
+// so a thread's share of a tile, 16 rows x 8 fp32 (512 bytes), is staged
+// whole in shared memory up front (64 KB per CTA, three CTAs per SM).  (The
+// same split for bf16, 32 KB per CTA, measured a little slower than
+// k_tile_ts.)  The pair exchanges the tile amax and the 8 column sums of each
+// candidate by shuffles; everything else is the thread's own.  The certified
+// approximate sum is the columns' tree as in k_tile_ts.  On the exact path
+// the left lane passes each row's partial sum (elements 0-7) to the right
+// lane, which continues it over elements 8-15: the method's element order.
+// A row's slot takes the row's code words of both candidates once read; the
+// exact path's first tree level and error values use the rest of the slots.
+struct Tile2 {
+    static constexpr int RB = 32;                // bytes of a thread's 8-element row piece
+    static constexpr int BYTES = 16 * kTileThreads * RB;     // the CTA's staged half tiles
+};
+
+template <int DT, int ERR>
+__global__ void __launch_bounds__(kTileThreads) k_tile_ts2(const QuantArgs a) {
+    static_assert(DT == NVFP4_F32, "bf16 input takes k_tile_ts");
+    using T2 = Tile2;
+    extern __shared__ __align__(16) unsigned char tile_s[];   // [row][thread][RB]
+    __shared__ float tenc[128];                 // encode reciprocal of every scale byte
+    __shared__ uint8_t scol[kBands][16];        // columnwise scale byte of each tile
+    pdl_wait();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, hh = lane & 1;
+    const unsigned pm = 3u << (lane & 30);      // the pair's lanes
+    const int64_t M = a.M, K = a.K;
+    const int64_t band0 = static_cast<int64_t>(blockIdx.x) * kBands, band = band0 + warp;
+    const int64_t tile0 = static_cast<int64_t>(blockIdx.y) * 16, tile = tile0 + (lane >> 1);
+    const int64_t nb = K / 16, nbands = M / 16;
+    const bool own = band < nbands && tile < nb;
+    const int64_t base = band * 16 * K + tile * 16 + 8 * hh;      // the thread's first element
+    constexpr int ES = 4;                       // element bytes
+    const uint32_t swz = piece_swizzle<2>(tid);
+    auto slot = [&](int r) { return tile_s + (r * kTileThreads + tid) * T2::RB; };
+    // 16-byte piece c of row r (two per row, swizzled)
+    auto piece = [&](int r, uint32_t c) { return slot(r) + ((c ^ swz) << 4); };
+    // once row r is consumed: its code words (both candidates) in the first
+    // piece, 8 bytes of scratch in the second
+    auto codes_at = [&](int r) { return reinterpret_cast<uint2*>(piece(r, 0)); };
+    auto scratch = [&](int r) { return reinterpret_cast<float2*>(piece(r, 1)); };
+    if (own) {
+        const unsigned char* gx = static_cast<const unsigned char*>(a.x) + base * ES;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const unsigned char* src = gx + static_cast<int64_t>(r) * K * ES;
+            cp_async16(piece(r, 0), src);
+            cp_async16(piece(r, 1), src + 16);
+            if ((r & 3) == 3) cp_async_commit();
+        }
+    }
+    GScale g{0.0f, 1.0f, 1.0f};
+    if (a.gamax_mode == NVFP4_GAMAX_TENSOR_GIVEN) {
+        g.A = a.gamax[0];
+        global_scales(g.A, a.bound, g.Senc, g.Sdec);
+    }
+    const float C = mul_rn(6.0f, a.bound);
+    for (int i = tid; i < 128; i += blockDim.x)
+        tenc[i] = min_nd(div_rn(1.0f, mul_rn(e4m3_decode(static_cast<uint32_t>(i)), g.Sdec)), FLT_MAX);
+    __syncthreads();
+
+    auto load8 = [&](int r, float* y) {         // the thread's 8 elements of row r
+        const float4 p = *reinterpret_cast<const float4*>(piece(r, 0));
+        const float4 q = *reinterpret_cast<const float4*>(piece(r, 1));
+        y[0] = p.x; y[1] = p.y; y[2] = p.z; y[3] = p.w;
+        y[4] = q.x; y[5] = q.y; y[6] = q.z; y[7] = q.w;
+    };
+    uint32_t cw[16];                            // columnwise code words (after the transpose)
+    uint32_t sf_c = 0;
+    if (own) {
+        // pass 0: tile amax, each copy group as it lands, then over the pair
+        float b = 0.0f;
+        auto amax4 = [&](int r0) {
+#pragma unroll
+            for (int r = r0; r < r0 + 4; ++r) {
+                float y[8];
+                load8(r, y);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) b = max_nd(b, fabsf(y[i]));
+            }
+        };
+        cp_async_wait<3>();
+        amax4(0);
+        cp_async_wait<2>();
+        amax4(4);
+        cp_async_wait<1>();
+        amax4(8);
+        cp_async_wait<0>();
+        amax4(12);
+        b = max_nd(b, __shfl_xor_sync(pm, b, 1));
+        const float s6f = block_s6f<true>(b, g.Senc);
+        const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
+        const uint32_t sf4 = e4m3_encode(min_nd(mul_rn(s6f, 1.5f), 448.0f));
+        const float enc6 = tenc[sf6], enc4 = tenc[sf4];
+        const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
+        const float K6 = div_rn(mul_rn(d6, g.A), C), K4 = div_rn(mul_rn(d4, g.A), C);
+
+        // pass 1: both candidates' codes and scaled-domain approximate errors
+        // (as k_tile_ts), the 8 column sums in row order
+        float F6[8], F4[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) F6[i] = F4[i] = 0.0f;
+        const uint64_t ENC6 = pack2(enc6, enc6), ENC4 = pack2(enc4, enc4);
+        auto candidate = [&](const float* y, uint64_t enc2, uint32_t& w, float* e) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) unpack2(mul2(pack2(y[i], y[i + 1]), enc2), v[i], v[i + 1]);
+            uint32_t h[4];
+            w = e2m1_encode8_dec(v, h);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                sub_f16x2_f32(h[j], v[2 * j], v[2 * j + 1], e[2 * j], e[2 * j + 1]);
+                if (ERR != NVFP4_ERR_MAE) {
+                    const uint64_t D = pack2(e[2 * j], e[2 * j + 1]);
+                    unpack2(mul2(D, D), e[2 * j], e[2 * j + 1]);
+                }
+            }
+            if (ERR == NVFP4_ERR_MAE) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) e[i] = fabsf(e[i]);
+            }
+        };
+        auto add8 = [&](float* F, const float* e) {
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) unpack2(add2(pack2(F[i], F[i + 1]), pack2(e[i], e[i + 1])), F[i], F[i + 1]);
+        };
+#pragma unroll 4
+        for (int r = 0; r < 16; ++r) {
+            float y[8], e[8];
+            load8(r, y);
+            uint32_t w6, w4;
+            candidate(y, ENC6, w6, e);
+            add8(F6, e);
+            candidate(y, ENC4, w4, e);
+            add8(F4, e);
+            *codes_at(r) = make_uint2(w6, w4);
+        }
+        // the tile's 16 column sums in column order (the partner's 8 by shuffle), then the tree
+        auto col_tree = [&](const float* F) {
+            float G[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float o = __shfl_xor_sync(pm, F[i], 1);
+                G[i] = hh ? o : F[i];
+                G[i + 8] = hh ? F[i] : o;
+            }
+            return tree16_regs(G);
+        };
+        float E6c = col_tree(F6), E4c = col_tree(F4);
+        {   // back from the scaled domain: E^ = RN(K * S'), or RN(RN(K * K) * S')
+            const float k6 = ERR == NVFP4_ERR_MAE ? K6 : mul_rn(K6, K6);
+            const float k4 = ERR == NVFP4_ERR_MAE ? K4 : mul_rn(K4, K4);
+            E6c = mul_rn(k6, E6c);
+            E4c = mul_rn(k4, E4c);
+        }
+        float E6r = E6c, E4r = E4c;
+        if (!tile_sums_decide<ERR>(E6c, E4c, K6, K4, b)) {     // both lanes of the pair alike
+            // the exact sums: error values |dq| of each grid magnitude (row
+            // 8 + k's scratch: map-to-6, map-to-4), x read again
+            const float G8[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                *scratch(8 + k) = make_float2(div_rn(mul_rn(mul_rn(G8[k], d6), g.A), C),
+                                              div_rn(mul_rn(mul_rn(G8[k], d4), g.A), C));
+            auto exact = [&](const float* y, uint32_t w, int c, float* e) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t k = (w >> (4 * i)) & 7u;
+                    const float2 t = *scratch(8 + static_cast<int>(k));
+                    const float diff = sub_rn(c ? t.y : t.x, fabsf(y[i]));
+                    e[i] = (ERR == NVFP4_ERR_MAE) ? fabsf(diff) : mul_rn(diff, diff);
+                }
+            };
+#pragma unroll
+            for (int i = 0; i < 8; ++i) F6[i] = F4[i] = 0.0f;
+#pragma unroll 1
+            for (int r = 0; r < 16; ++r) {
+                float y[8], e6[8], e4[8];
+                const unsigned char* src = static_cast<const unsigned char*>(a.x) +
+                                           (base + static_cast<int64_t>(r) * K) * ES;
+                {
+                    const float4 p = __ldg(reinterpret_cast<const float4*>(src));
+                    const float4 q = __ldg(reinterpret_cast<const float4*>(src) + 1);
+                    y[0] = p.x; y[1] = p.y; y[2] = p.z; y[3] = p.w;
+                    y[4] = q.x; y[5] = q.y; y[6] = q.z; y[7] = q.w;
+                }
+                const uint2 w = *codes_at(r);
+                exact(y, w.x, 0, e6);
+                exact(y, w.y, 1, e4);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    F6[i] = add_rn(F6[i], e6[i]);
+                    F4[i] = add_rn(F4[i], e4[i]);
+                }
+                // row r in element order: the left lane's 8 from zero, the
+                // right lane's 8 continuing from the left lane's partial
+                float p6 = 0.0f, p4 = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    p6 = add_rn(p6, e6[i]);
+                    p4 = add_rn(p4, e4[i]);
+                }
+                float s6 = __shfl_xor_sync(pm, p6, 1), s4 = __shfl_xor_sync(pm, p4, 1);
+                if (hh) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        s6 = add_rn(s6, e6[i]);
+                        s4 = add_rn(s4, e4[i]);
+                    }
+                    // the width-16 tree's first level: row i + row i + 8
+                    float2* p = scratch(r & 7);
+                    if (r >= 8) {
+                        const float2 t = *p;
+                        s6 = add_rn(t.x, s6);
+                        s4 = add_rn(t.y, s4);
+                    }
+                    *p = make_float2(s6, s4);
+                }
+            }
+            float R6 = 0.0f, R4 = 0.0f;
+            if (hh) {
+                float S6[8], S4[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 t = *scratch(i);
+                    S6[i] = t.x;
+                    S4[i] = t.y;
+                }
+                R6 = tree16_upper(S6);
+                R4 = tree16_upper(S4);
+            }
+            E6r = __shfl_sync(pm, R6, lane | 1);
+            E4r = __shfl_sync(pm, R4, lane | 1);
+            E6c = col_tree(F6);
+            E4c = col_tree(F4);
+        }
+        const bool row4 = E4r < E6r, col4 = E4c < E6c;       // ties and NaN keep map-to-6
+        const uint8_t sf_r = static_cast<uint8_t>(row4 ? sf4 : sf6);
+
+        // rowwise codes of the chosen candidate (the thread's 8 codes of each
+        // row), and the columnwise candidate's words, transposed
+        const int64_t nbr = K / 16;
+        uint32_t* codes32 = reinterpret_cast<uint32_t*>(a.codes);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const uint2 w = *codes_at(r);
+            const int64_t rowg = band * 16 + r;
+            codes32[(rowg * K + tile * 16) / 8 + hh] = row4 ? w.y : w.x;
+            if (!hh) a.scales[rowg * nbr + tile] = sf_r;
+            cw[r] = col4 ? w.y : w.x;
+        }
+        transpose8x8_nibbles(cw);          // rows 0-7
+        transpose8x8_nibbles(cw + 8);      // rows 8-15
+        sf_c = col4 ? sf4 : sf6;
+    }
+    // columnwise output as in k_tile_ts (the CTA's 256 columns), staged in the
+    // tile buffer once every thread is done with its slots
+    __syncthreads();
+    uint2* stg = reinterpret_cast<uint2*>(tile_s);
+    if (own) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) stg[stage_index(warp, (lane >> 1) * 16 + 8 * hh + c)] = make_uint2(cw[c], cw[8 + c]);
+        if (!hh) scol[warp][lane >> 1] = static_cast<uint8_t>(sf_c);
+    }
+    __syncthreads();
+    uint2* cc = reinterpret_cast<uint2*>(a.codes_col);
+#pragma unroll 4
+    for (int q = tid; q < 256 * kBands; q += kTileThreads) {
+        const int j = q / kBands, bb = q % kBands;          // column of the CTA, band of the CTA
+        const int64_t col = tile0 * 16 + j, bnd = band0 + bb;
+        if (col < K && bnd < nbands) {
+            cc[col * nbands + bnd] = stg[stage_index(bb, j)];
+            a.scales_col[col * nbands + bnd] = scol[bb][j >> 4];
+        }
+    }
+    pdl_trigger();
+}
+
 // Plain (map-to-6) 16x16 quantization with rowwise AND columnwise output:
 // the tile's one scale serves both outputs and x^T's codes are x's codes
 // transposed (stochastic rounding draws are keyed on x's index), so a thread
-// owns a tile as in k_tile_t, finds the tile amax in a first walk over its
+// owns a tile as in k_tile_ts, finds the tile amax in a first walk over its
 // rows and encodes each row in a second (from L2), storing the row's codes
 // and shifting its nibbles into the column words: rows come in pairs, whose
 // nibbles are interleaved into one byte per column (low nibble the even row)
 // and moved in at the top of that column's word, so after rows 0-7 (and
 // again 8-15) word c holds column c with row r in nibble r % 8.  The
-// columnwise output is staged and written as in k_tile_t.
+// columnwise output is staged and written as in k_tile_ts.
 template <int DT, int RND, bool GS>
 __global__ void __launch_bounds__(kTileThreads) k_tile_p(const QuantArgs a) {
     using Rg = TilePRing<DT>;
@@ -983,8 +1021,27 @@ int launch_tile(KernelT kernel, const QuantArgs& a, cudaStream_t s) {
 }
 
 template <int DT, int ERR>
-int launch_tile_t(const QuantArgs& a, cudaStream_t s) {
-    if constexpr (DT == NVFP4_BF16) {
+int launch_tile_ts2(const QuantArgs& a, cudaStream_t s) {
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_dev != dev) {
+        cudaFuncSetAttribute(k_tile_ts2<DT, ERR>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile2::BYTES);
+        cudaFuncSetAttribute(k_tile_ts2<DT, ERR>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+        configured_dev = dev;
+    }
+    const dim3 grid(static_cast<unsigned>((a.M / 16 + kBands - 1) / kBands),
+                    static_cast<unsigned>((a.K / 16 + 15) / 16));
+    launch_pdl(k_tile_ts2<DT, ERR>, grid, kTileThreads, Tile2::BYTES, s, a);
+    return static_cast<int>(cudaGetLastError());
+}
+
+template <int DT, int ERR>
+int launch_tile_4o6(const QuantArgs& a, cudaStream_t s) {
+    if constexpr (DT == NVFP4_F32) {
+        return launch_tile_ts2<DT, ERR>(a, s);
+    } else {
         static int configured_dev = -1;
         int dev = 0;
         cudaGetDevice(&dev);
@@ -998,8 +1055,6 @@ int launch_tile_t(const QuantArgs& a, cudaStream_t s) {
                         static_cast<unsigned>((a.K / 16 + 31) / 32));
         launch_pdl(k_tile_ts<ERR>, grid, kTileThreads, kStagedTileBytes, s, a);
         return static_cast<int>(cudaGetLastError());
-    } else {
-        return launch_tile(k_tile_t<DT, ERR>, a, s);
     }
 }
 
@@ -1026,8 +1081,8 @@ template <int DT, int BLK>
 int tiles_dispatch_blk(const QuantArgs& a, cudaStream_t s) {
     if (a.err_mode != NVFP4_ERR_NONE) {
         if (BLK == NVFP4_BLOCK_16X16)
-            return a.err_mode == NVFP4_ERR_MAE ? launch_tile_t<DT, NVFP4_ERR_MAE>(a, s)
-                                               : launch_tile_t<DT, NVFP4_ERR_MSE>(a, s);
+            return a.err_mode == NVFP4_ERR_MAE ? launch_tile_4o6<DT, NVFP4_ERR_MAE>(a, s)
+                                               : launch_tile_4o6<DT, NVFP4_ERR_MSE>(a, s);
         return a.err_mode == NVFP4_ERR_MAE ? launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_MAE, NVFP4_RTN, true>, a, s)
                                            : launch_rowowner(k_tiles_rows<DT, BLK, NVFP4_ERR_MSE, NVFP4_RTN, true>, a, s);
     }
