@@ -360,6 +360,32 @@ def test_host_pipelined_calls(dtype):
         assert_same(dn, e, f"dequantize {od}")
 
 
+ROWCOL_SHAPES = [(16, 16), (16, 1040), (48, 528), (80, 240), (272, 48), (64, 512), (208, 784)]
+
+
+@pytest.mark.parametrize("shape", ROWCOL_SHAPES)
+def test_row_col_kernels_shape_sweep(shape):
+    """The staged row+col kernels over shapes that start and end inside a
+    CTA along both axes (a CTA is 4 bands x 32 tiles for bf16 four-over-six
+    and 1x16 nearest rounding, 4 bands x 16 tiles for fp32 four-over-six):
+    one tile; one band of 65 tiles; 3 bands x 33 tiles; 5 bands x 15 tiles;
+    17 bands x 3 tiles; exactly one CTA; 13 bands x 49 tiles.  Every output
+    byte against the oracle, both error modes and both bounds for
+    four-over-six, and nearest rounding with either global-scale mode."""
+    M, K = shape
+    for dtype in ("bf16", "f32"):
+        x = mat(shape, seed=zlib.crc32(f"rc{shape}{dtype}".encode()) % 1000, dtype=dtype, dist="t",
+                outliers=0.02)
+        for err in ("mae", "mse"):
+            for bound in (256.0, 448.0):
+                gpu, o = quantize_both(x, block="16x16", gamax_mode="tensor", err_mode=err, scale_bound=bound,
+                                       colwise=True)
+                compare_quant(gpu, o)
+        for gm in ("none", "tensor"):
+            gpu, o = quantize_both(x, block="1x16", gamax_mode=gm, colwise=True)
+            compare_quant(gpu, o)
+
+
 def test_host_non_blocking_calls():
     """Non-blocking host calls (returning once enqueued, so successive calls
     overlap) give the oracle's bytes: row-chunked calls, whole calls
