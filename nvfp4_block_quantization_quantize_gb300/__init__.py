@@ -272,7 +272,7 @@ def _finish_host(res: dict, given: dict, stream=None) -> dict:
 # ~340 GB/s).  Chunks start on multiples of 16 rows (whole 16x16 tiles), and
 # each chunk's kernels get row_offset + its first row, so stochastic rounding
 # draws the same words and the bytes equal one call's.
-_PIPE_CHUNKS = 8
+_PIPE_CHUNKS = 4
 _PIPE_MIN_ROWS = 256
 _pipe_lock = threading.Lock()
 _pipe_streams = {}

@@ -316,7 +316,7 @@ def test_host_pipelined_calls(dtype):
     (copies in, kernels, copies out overlapping): every byte, the in-place
     residual and the stochastic draws (keyed on row_offset + the chunk's
     first row) must equal the oracle's for the whole tensor."""
-    M, K = 1040, 512                                   # chunks of 144 rows and a 32-row tail
+    M, K = 1040, 512                                   # chunks of 272 rows and a 224-row tail
     x = mat((M, K), seed=81, dtype=dtype, outliers=0.01)
     r0 = mat((M, K), seed=82) * np.float32(0.01)
     for blk in ("1x16", "16x16"):
