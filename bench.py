@@ -366,8 +366,8 @@ def run_mm_only(args, local_rank):
 def rowcol_measurement(nv, torch, W1, peaks, iters=10, variants=None):
     """Plain quantization with rowwise AND columnwise outputs from one read
     (timed beside the step, not part of it), on the step's W1 [4096,14336]
-    bf16: round-to-nearest 1x16 and 16x16, stochastic rounding 1x16 (draws
-    keyed on x's index, shared by both outputs)."""
+    bf16: round-to-nearest and stochastic rounding, 1x16 and 16x16 (the
+    stochastic draws keyed on x's index, shared by both outputs)."""
     M, K = W1.shape
     dev = W1.device
     outs = dict(codes=torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
@@ -378,7 +378,8 @@ def rowcol_measurement(nv, torch, W1, peaks, iters=10, variants=None):
     peak = peaks["hbm_gbs"] if peaks else 6800.0
     res = []
     for name, kw in (("RTN 1x16", dict(block="1x16")), ("RTN 16x16", dict(block="16x16")),
-                     ("SR 1x16", dict(block="1x16", rounding="sr", seed=0, step=7))):
+                     ("SR 1x16", dict(block="1x16", rounding="sr", seed=0, step=7)),
+                     ("SR 16x16", dict(block="16x16", rounding="sr", seed=0, step=7))):
         if variants and name not in variants:
             continue
         run = lambda: nv.nvfp4_quantize(W1, colwise=True, **kw, **outs)   # noqa: E731
