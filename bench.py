@@ -340,7 +340,7 @@ def c4_measurement(nv, torch, dev, peaks, iters=10, bounds=(256.0, 448.0)):
                     "frac_of_peak": round(nbytes / (ms * 1e-3) / GB / peak, 3)})
     del x, outs
     return {"workload": "c4: fp32 [8192,8192] Student-t(3) seed 3, four-over-six 16x16 MSE, "
-                        "per-tensor amax given, rowwise + columnwise", "kernel": "k_tile_ts2<f32, MSE>",
+                        "per-tensor amax given, rowwise + columnwise", "kernel": "k_tile_ts4<f32, MSE>",
             "algorithmic_bytes": int(nbytes), "runs": res}
 
 

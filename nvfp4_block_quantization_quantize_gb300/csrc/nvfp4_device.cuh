@@ -324,6 +324,21 @@ __device__ __forceinline__ uint32_t e2m1_encode8_dec(const float* v, uint32_t* h
     return r;
 }
 
+// Four values -> four 4-bit codes (the low 16 bits, element i in nibble i)
+// and the codes' grid values as two f16 pairs, as e2m1_encode8_dec.
+__device__ __forceinline__ uint32_t e2m1_encode4_dec(const float* v, uint32_t* h) {
+    uint16_t r;
+    asm("{\n\t.reg .b8 b0, b1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %6, %5;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b1;\n\t"
+        "mov.b16 %0, {b0, b1};\n\t}"
+        : "=h"(r), "=r"(h[0]), "=r"(h[1])
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]));
+    return r;
+}
+
 // Error values of 8 codes given as f16 pairs of grid values (q = 2^e * m):
 // dq = p * X_m with p = q without its 1.5 bit and X_m = X_1 + s * DX, s = 1
 // for m = 1.5 (exact: X_1 + DX = X_1.5).  s is built from the 1.5 bit by an

@@ -22,12 +22,12 @@
 //               tiles (fully coalesced), and the columnwise output, staged in
 //               shared memory, leaves as one 32-byte run per column (4 bands
 //               x 8 bytes) instead of 8-byte pieces 32 to a warp store.
-// k_tile_ts2    the same for fp32 input with two threads per tile (lanes 2t
-//               and 2t+1: columns 0-7 and 8-15), so that a thread's share,
-//               16 rows x 8 fp32, is staged whole too; the pair exchanges the
-//               tile amax and the column sums by shuffles, and on the exact
-//               path passes each row's partial sum from the left lane to the
-//               right.  A CTA is 4 bands x 16 tiles.
+// k_tile_ts4    the same for fp32 input with four threads per tile (lanes
+//               4t .. 4t+3: columns 0-3, 4-7, 8-11, 12-15), so that a
+//               thread's share, 16 rows x 4 fp32, is staged whole too; the
+//               quad exchanges the tile amax and the column sums by shuffles
+//               and on the exact path runs each row's sum along its lanes.
+//               A CTA is 4 bands x 8 tiles.
 //
 // Method: "Add NVFP4 four-over-six (row-wise) quantization to the training
 // prototype" (What: 16x16 blocks, rowwise / columnwise; CuTe DSL kernel
@@ -582,56 +582,45 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_r1(const QuantArgs a) {
     pdl_trigger();
 }
 
-// Four-over-six 16x16 with rowwise and columnwise output, fp32 input, two
-// threads per tile: lanes 2t and 2t+1 of a warp hold columns 0-7 and 8-15 of
-// tile t (16 tiles per warp, one band per warp, a CTA 4 bands x 16 tiles),
-// so a thread's share of a tile, 16 rows x 8 fp32 (512 bytes), is staged
-// whole in shared memory up front (64 KB per CTA, three CTAs per SM).  (The
-// same split for bf16, 32 KB per CTA, measured a little slower than
-// k_tile_ts.)  The pair exchanges the tile amax and the 8 column sums of each
-// candidate by shuffles; everything else is the thread's own.  The certified
-// approximate sum is the columns' tree as in k_tile_ts.  On the exact path
-// the left lane passes each row's partial sum (elements 0-7) to the right
-// lane, which continues it over elements 8-15: the method's element order.
-// A row's slot takes the row's code words of both candidates once read; the
-// exact path's first tree level and error values use the rest of the slots.
-struct Tile2 {
-    static constexpr int RB = 32;                // bytes of a thread's 8-element row piece
-    static constexpr int BYTES = 16 * kTileThreads * RB;     // the CTA's staged half tiles
-};
+// Four-over-six 16x16 with rowwise and columnwise output, fp32 input, four
+// threads per tile: lanes 4t .. 4t+3 of a warp hold columns 0-3, 4-7, 8-11
+// and 12-15 of tile t (8 tiles per warp, one band per warp, a CTA 4 bands x
+// 8 tiles), so a thread's share, 16 rows x 4 fp32 (256 bytes), is staged in
+// shared memory up front (32 KB per CTA, six CTAs per SM; with two threads
+// per tile, 64 KB and three CTAs per SM, c4 ran 15 % slower).  The quad exchanges the tile amax and the column sums by
+// shuffles: the width-16 tree's first level pairs lanes q and q^2 (columns j
+// and j+8), its second level lanes q and q^1 (j and j+4), and the last two
+// levels run in every lane alike.  On the exact path each row's element-
+// order sum runs along the quad, each lane continuing its left neighbour's
+// partial.  Row r's slot (16 bytes) takes, once read, the row's 4-code
+// words of both candidates and 8 bytes of scratch.
+constexpr int kTile4Bytes = 16 * kTileThreads * 16;
 
-template <int DT, int ERR>
-__global__ void __launch_bounds__(kTileThreads) k_tile_ts2(const QuantArgs a) {
-    static_assert(DT == NVFP4_F32, "bf16 input takes k_tile_ts");
-    using T2 = Tile2;
-    extern __shared__ __align__(16) unsigned char tile_s[];   // [row][thread][RB]
+template <int ERR>
+__global__ void __launch_bounds__(kTileThreads) k_tile_ts4(const QuantArgs a) {
+    extern __shared__ __align__(16) unsigned char tile_s[];   // [row][thread][16 bytes]
     __shared__ float tenc[128];                 // encode reciprocal of every scale byte
-    __shared__ uint8_t scol[kBands][16];        // columnwise scale byte of each tile
+    __shared__ uint8_t scol[kBands][8];         // columnwise scale byte of each tile
     pdl_wait();
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, hh = lane & 1;
-    const unsigned pm = 3u << (lane & 30);      // the pair's lanes
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q = lane & 3;
+    const int qbase = lane & 28;                // the quad's first lane
+    const unsigned pm = 15u << qbase;           // the quad's lanes
     const int64_t M = a.M, K = a.K;
-    const int64_t band0 = static_cast<int64_t>(blockIdx.x) * kBands, band = band0 + warp;
-    const int64_t tile0 = static_cast<int64_t>(blockIdx.y) * 16, tile = tile0 + (lane >> 1);
     const int64_t nb = K / 16, nbands = M / 16;
+    const int64_t ntg = (nb + 7) / 8;           // CTA columns of 8 tiles (a 1D grid: K/128 may pass 65535)
+    const int64_t cta = blockIdx.x;
+    const int64_t band0 = (cta / ntg) * kBands, band = band0 + warp;
+    const int64_t tile0 = (cta % ntg) * 8, tile = tile0 + (lane >> 2);
     const bool own = band < nbands && tile < nb;
-    const int64_t base = band * 16 * K + tile * 16 + 8 * hh;      // the thread's first element
-    constexpr int ES = 4;                       // element bytes
-    const uint32_t swz = piece_swizzle<2>(tid);
-    auto slot = [&](int r) { return tile_s + (r * kTileThreads + tid) * T2::RB; };
-    // 16-byte piece c of row r (two per row, swizzled)
-    auto piece = [&](int r, uint32_t c) { return slot(r) + ((c ^ swz) << 4); };
-    // once row r is consumed: its code words (both candidates) in the first
-    // piece, 8 bytes of scratch in the second
-    auto codes_at = [&](int r) { return reinterpret_cast<uint2*>(piece(r, 0)); };
-    auto scratch = [&](int r) { return reinterpret_cast<float2*>(piece(r, 1)); };
+    const int64_t base = band * 16 * K + tile * 16 + 4 * q;       // the thread's first element
+    auto slot = [&](int r) { return tile_s + (r * kTileThreads + tid) * 16; };
+    auto codes_at = [&](int r) { return reinterpret_cast<uint32_t*>(slot(r)); };   // 4-code words, both candidates
+    auto scratch = [&](int r) { return reinterpret_cast<float2*>(slot(r) + 8); };
     if (own) {
-        const unsigned char* gx = static_cast<const unsigned char*>(a.x) + base * ES;
+        const unsigned char* gx = static_cast<const unsigned char*>(a.x) + base * 4;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            const unsigned char* src = gx + static_cast<int64_t>(r) * K * ES;
-            cp_async16(piece(r, 0), src);
-            cp_async16(piece(r, 1), src + 16);
+            cp_async16(slot(r), gx + static_cast<int64_t>(r) * K * 4);
             if ((r & 3) == 3) cp_async_commit();
         }
     }
@@ -645,24 +634,37 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_ts2(const QuantArgs a) {
         tenc[i] = min_nd(div_rn(1.0f, mul_rn(e4m3_decode(static_cast<uint32_t>(i)), g.Sdec)), FLT_MAX);
     __syncthreads();
 
-    auto load8 = [&](int r, float* y) {         // the thread's 8 elements of row r
-        const float4 p = *reinterpret_cast<const float4*>(piece(r, 0));
-        const float4 q = *reinterpret_cast<const float4*>(piece(r, 1));
+    auto load4 = [&](int r, float* y) {         // the thread's 4 elements of row r
+        const float4 p = *reinterpret_cast<const float4*>(slot(r));
         y[0] = p.x; y[1] = p.y; y[2] = p.z; y[3] = p.w;
-        y[4] = q.x; y[5] = q.y; y[6] = q.z; y[7] = q.w;
     };
-    uint32_t cw[16];                            // columnwise code words (after the transpose)
+    // the width-16 tree over the tile's 16 column sums, 4 per lane
+    auto col_tree = [&](const float* F) {
+        float t[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {           // level 1: column j + column j + 8
+            const float o = __shfl_xor_sync(pm, F[i], 2);
+            t[i] = q < 2 ? add_rn(F[i], o) : add_rn(o, F[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {           // level 2: (j, j + 8) + (j + 4, j + 12)
+            const float o = __shfl_xor_sync(pm, t[i], 1);
+            t[i] = (q & 1) == 0 ? add_rn(t[i], o) : add_rn(o, t[i]);
+        }
+        return add_rn(add_rn(t[0], t[2]), add_rn(t[1], t[3]));
+    };
+    uint32_t lo[4], hi[4];                      // columnwise code words of the thread's 4 columns
     uint32_t sf_c = 0;
     if (own) {
-        // pass 0: tile amax, each copy group as it lands, then over the pair
+        // pass 0: tile amax, each copy group as it lands, then over the quad
         float b = 0.0f;
         auto amax4 = [&](int r0) {
 #pragma unroll
             for (int r = r0; r < r0 + 4; ++r) {
-                float y[8];
-                load8(r, y);
+                float y[4];
+                load4(r, y);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) b = max_nd(b, fabsf(y[i]));
+                for (int i = 0; i < 4; ++i) b = max_nd(b, fabsf(y[i]));
             }
         };
         cp_async_wait<3>();
@@ -674,6 +676,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_ts2(const QuantArgs a) {
         cp_async_wait<0>();
         amax4(12);
         b = max_nd(b, __shfl_xor_sync(pm, b, 1));
+        b = max_nd(b, __shfl_xor_sync(pm, b, 2));
         const float s6f = block_s6f<true>(b, g.Senc);
         const uint32_t sf6 = e4m3_encode(min_nd(s6f, 448.0f));
         const uint32_t sf4 = e4m3_encode(min_nd(mul_rn(s6f, 1.5f), 448.0f));
@@ -681,20 +684,20 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_ts2(const QuantArgs a) {
         const float d6 = e4m3_decode(sf6), d4 = e4m3_decode(sf4);
         const float K6 = div_rn(mul_rn(d6, g.A), C), K4 = div_rn(mul_rn(d4, g.A), C);
 
-        // pass 1: both candidates' codes and scaled-domain approximate errors
-        // (as k_tile_ts), the 8 column sums in row order
-        float F6[8], F4[8];
+        // pass 1: both candidates' codes and scaled-domain approximate errors,
+        // the 4 column sums in row order
+        float F6[4], F4[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) F6[i] = F4[i] = 0.0f;
+        for (int i = 0; i < 4; ++i) F6[i] = F4[i] = 0.0f;
         const uint64_t ENC6 = pack2(enc6, enc6), ENC4 = pack2(enc4, enc4);
         auto candidate = [&](const float* y, uint64_t enc2, uint32_t& w, float* e) {
-            float v[8];
+            float v[4];
 #pragma unroll
-            for (int i = 0; i < 8; i += 2) unpack2(mul2(pack2(y[i], y[i + 1]), enc2), v[i], v[i + 1]);
-            uint32_t h[4];
-            w = e2m1_encode8_dec(v, h);
+            for (int i = 0; i < 4; i += 2) unpack2(mul2(pack2(y[i], y[i + 1]), enc2), v[i], v[i + 1]);
+            uint32_t h[2];
+            w = e2m1_encode4_dec(v, h);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 sub_f16x2_f32(h[j], v[2 * j], v[2 * j + 1], e[2 * j], e[2 * j + 1]);
                 if (ERR != NVFP4_ERR_MAE) {
                     const uint64_t D = pack2(e[2 * j], e[2 * j + 1]);
@@ -703,35 +706,24 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_ts2(const QuantArgs a) {
             }
             if (ERR == NVFP4_ERR_MAE) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) e[i] = fabsf(e[i]);
+                for (int i = 0; i < 4; ++i) e[i] = fabsf(e[i]);
             }
         };
-        auto add8 = [&](float* F, const float* e) {
+        auto add4 = [&](float* F, const float* e) {
 #pragma unroll
-            for (int i = 0; i < 8; i += 2) unpack2(add2(pack2(F[i], F[i + 1]), pack2(e[i], e[i + 1])), F[i], F[i + 1]);
+            for (int i = 0; i < 4; i += 2) unpack2(add2(pack2(F[i], F[i + 1]), pack2(e[i], e[i + 1])), F[i], F[i + 1]);
         };
 #pragma unroll 4
         for (int r = 0; r < 16; ++r) {
-            float y[8], e[8];
-            load8(r, y);
+            float y[4], e[4];
+            load4(r, y);
             uint32_t w6, w4;
             candidate(y, ENC6, w6, e);
-            add8(F6, e);
+            add4(F6, e);
             candidate(y, ENC4, w4, e);
-            add8(F4, e);
-            *codes_at(r) = make_uint2(w6, w4);
+            add4(F4, e);
+            *codes_at(r) = w6 | (w4 << 16);
         }
-        // the tile's 16 column sums in column order (the partner's 8 by shuffle), then the tree
-        auto col_tree = [&](const float* F) {
-            float G[16];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float o = __shfl_xor_sync(pm, F[i], 1);
-                G[i] = hh ? o : F[i];
-                G[i + 8] = hh ? F[i] : o;
-            }
-            return tree16_regs(G);
-        };
         float E6c = col_tree(F6), E4c = col_tree(F4);
         {   // back from the scaled domain: E^ = RN(K * S'), or RN(RN(K * K) * S')
             const float k6 = ERR == NVFP4_ERR_MAE ? K6 : mul_rn(K6, K6);
@@ -740,7 +732,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_ts2(const QuantArgs a) {
             E4c = mul_rn(k4, E4c);
         }
         float E6r = E6c, E4r = E4c;
-        if (!tile_sums_decide<ERR>(E6c, E4c, K6, K4, b)) {     // both lanes of the pair alike
+        if (!tile_sums_decide<ERR>(E6c, E4c, K6, K4, b)) {     // all four lanes alike
             // the exact sums: error values |dq| of each grid magnitude (row
             // 8 + k's scratch: map-to-6, map-to-4), x read again
             const float G8[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
@@ -750,7 +742,7 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_ts2(const QuantArgs a) {
                                               div_rn(mul_rn(mul_rn(G8[k], d4), g.A), C));
             auto exact = [&](const float* y, uint32_t w, int c, float* e) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 4; ++i) {
                     const uint32_t k = (w >> (4 * i)) & 7u;
                     const float2 t = *scratch(8 + static_cast<int>(k));
                     const float diff = sub_rn(c ? t.y : t.x, fabsf(y[i]));
@@ -758,53 +750,53 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_ts2(const QuantArgs a) {
                 }
             };
 #pragma unroll
-            for (int i = 0; i < 8; ++i) F6[i] = F4[i] = 0.0f;
+            for (int i = 0; i < 4; ++i) F6[i] = F4[i] = 0.0f;
 #pragma unroll 1
             for (int r = 0; r < 16; ++r) {
-                float y[8], e6[8], e4[8];
-                const unsigned char* src = static_cast<const unsigned char*>(a.x) +
-                                           (base + static_cast<int64_t>(r) * K) * ES;
-                {
-                    const float4 p = __ldg(reinterpret_cast<const float4*>(src));
-                    const float4 q = __ldg(reinterpret_cast<const float4*>(src) + 1);
-                    y[0] = p.x; y[1] = p.y; y[2] = p.z; y[3] = p.w;
-                    y[4] = q.x; y[5] = q.y; y[6] = q.z; y[7] = q.w;
-                }
-                const uint2 w = *codes_at(r);
-                exact(y, w.x, 0, e6);
-                exact(y, w.y, 1, e4);
+                float y[4], e6[4], e4[4];
+                const float4 p = __ldg(reinterpret_cast<const float4*>(
+                    static_cast<const unsigned char*>(a.x) + (base + static_cast<int64_t>(r) * K) * 4));
+                y[0] = p.x; y[1] = p.y; y[2] = p.z; y[3] = p.w;
+                const uint32_t w = *codes_at(r);
+                exact(y, w & 0xFFFFu, 0, e6);
+                exact(y, w >> 16, 1, e4);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 4; ++i) {
                     F6[i] = add_rn(F6[i], e6[i]);
                     F4[i] = add_rn(F4[i], e4[i]);
                 }
-                // row r in element order: the left lane's 8 from zero, the
-                // right lane's 8 continuing from the left lane's partial
-                float p6 = 0.0f, p4 = 0.0f;
+                // row r in element order along the quad: lane 0 from zero,
+                // each next lane continuing its left neighbour's partial
+                float s6 = 0.0f, s4 = 0.0f;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    p6 = add_rn(p6, e6[i]);
-                    p4 = add_rn(p4, e4[i]);
-                }
-                float s6 = __shfl_xor_sync(pm, p6, 1), s4 = __shfl_xor_sync(pm, p4, 1);
-                if (hh) {
+                for (int k = 0; k < 4; ++k) {
+                    if (q == k) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        s6 = add_rn(s6, e6[i]);
-                        s4 = add_rn(s4, e4[i]);
+                        for (int i = 0; i < 4; ++i) {
+                            s6 = add_rn(s6, e6[i]);
+                            s4 = add_rn(s4, e4[i]);
+                        }
                     }
-                    // the width-16 tree's first level: row i + row i + 8
-                    float2* p = scratch(r & 7);
+                    if (k < 3) {
+                        const float t6 = __shfl_sync(pm, s6, qbase + k), t4 = __shfl_sync(pm, s4, qbase + k);
+                        if (q == k + 1) {
+                            s6 = t6;
+                            s4 = t4;
+                        }
+                    }
+                }
+                if (q == 3) {                   // the width-16 tree's first level: row i + row i + 8
+                    float2* p2 = scratch(r & 7);
                     if (r >= 8) {
-                        const float2 t = *p;
+                        const float2 t = *p2;
                         s6 = add_rn(t.x, s6);
                         s4 = add_rn(t.y, s4);
                     }
-                    *p = make_float2(s6, s4);
+                    *p2 = make_float2(s6, s4);
                 }
             }
             float R6 = 0.0f, R4 = 0.0f;
-            if (hh) {
+            if (q == 3) {
                 float S6[8], S4[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -815,44 +807,53 @@ __global__ void __launch_bounds__(kTileThreads) k_tile_ts2(const QuantArgs a) {
                 R6 = tree16_upper(S6);
                 R4 = tree16_upper(S4);
             }
-            E6r = __shfl_sync(pm, R6, lane | 1);
-            E4r = __shfl_sync(pm, R4, lane | 1);
+            E6r = __shfl_sync(pm, R6, qbase + 3);
+            E4r = __shfl_sync(pm, R4, qbase + 3);
             E6c = col_tree(F6);
             E4c = col_tree(F4);
         }
         const bool row4 = E4r < E6r, col4 = E4c < E6c;       // ties and NaN keep map-to-6
         const uint8_t sf_r = static_cast<uint8_t>(row4 ? sf4 : sf6);
 
-        // rowwise codes of the chosen candidate (the thread's 8 codes of each
-        // row), and the columnwise candidate's words, transposed
+        // rowwise codes of the chosen candidate (the thread's 4 codes of each
+        // row); the columnwise candidate's codes transposed (rows 0-7 and 8-15,
+        // the 16-bit words padded to 8x8 nibble blocks)
         const int64_t nbr = K / 16;
-        uint32_t* codes32 = reinterpret_cast<uint32_t*>(a.codes);
+        uint16_t* codes16 = reinterpret_cast<uint16_t*>(a.codes);
+        uint32_t cl[8], ch[8];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            const uint2 w = *codes_at(r);
+            const uint32_t w = *codes_at(r);
             const int64_t rowg = band * 16 + r;
-            codes32[(rowg * K + tile * 16) / 8 + hh] = row4 ? w.y : w.x;
-            if (!hh) a.scales[rowg * nbr + tile] = sf_r;
-            cw[r] = col4 ? w.y : w.x;
+            codes16[(rowg * K + tile * 16) / 4 + q] = static_cast<uint16_t>(row4 ? (w >> 16) : (w & 0xFFFFu));
+            if (q == 0) a.scales[rowg * nbr + tile] = sf_r;
+            const uint32_t c = col4 ? (w >> 16) : (w & 0xFFFFu);
+            if (r < 8) cl[r] = c;
+            else ch[r - 8] = c;
         }
-        transpose8x8_nibbles(cw);          // rows 0-7
-        transpose8x8_nibbles(cw + 8);      // rows 8-15
+        transpose8x8_nibbles(cl);          // rows 0-7: word c = column c
+        transpose8x8_nibbles(ch);          // rows 8-15
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            lo[c] = cl[c];
+            hi[c] = ch[c];
+        }
         sf_c = col4 ? sf4 : sf6;
     }
-    // columnwise output as in k_tile_ts (the CTA's 256 columns), staged in the
-    // tile buffer once every thread is done with its slots
+    // columnwise output (the CTA's 128 columns), staged in the tile buffer once
+    // every thread is done with its slots
     __syncthreads();
     uint2* stg = reinterpret_cast<uint2*>(tile_s);
     if (own) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) stg[stage_index(warp, (lane >> 1) * 16 + 8 * hh + c)] = make_uint2(cw[c], cw[8 + c]);
-        if (!hh) scol[warp][lane >> 1] = static_cast<uint8_t>(sf_c);
+        for (int c = 0; c < 4; ++c) stg[stage_index(warp, (lane >> 2) * 16 + 4 * q + c)] = make_uint2(lo[c], hi[c]);
+        if (q == 0) scol[warp][lane >> 2] = static_cast<uint8_t>(sf_c);
     }
     __syncthreads();
     uint2* cc = reinterpret_cast<uint2*>(a.codes_col);
 #pragma unroll 4
-    for (int q = tid; q < 256 * kBands; q += kTileThreads) {
-        const int j = q / kBands, bb = q % kBands;          // column of the CTA, band of the CTA
+    for (int qq = tid; qq < 128 * kBands; qq += kTileThreads) {
+        const int j = qq / kBands, bb = qq % kBands;        // column of the CTA, band of the CTA
         const int64_t col = tile0 * 16 + j, bnd = band0 + bb;
         if (col < K && bnd < nbands) {
             cc[col * nbands + bnd] = stg[stage_index(bb, j)];
@@ -1020,27 +1021,25 @@ int launch_tile(KernelT kernel, const QuantArgs& a, cudaStream_t s) {
     return static_cast<int>(cudaGetLastError());
 }
 
-template <int DT, int ERR>
-int launch_tile_ts2(const QuantArgs& a, cudaStream_t s) {
+template <int ERR>
+int launch_tile_ts4(const QuantArgs& a, cudaStream_t s) {
     static int configured_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
-        cudaFuncSetAttribute(k_tile_ts2<DT, ERR>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile2::BYTES);
-        cudaFuncSetAttribute(k_tile_ts2<DT, ERR>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        cudaFuncSetAttribute(k_tile_ts4<ERR>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
         configured_dev = dev;
     }
-    const dim3 grid(static_cast<unsigned>((a.M / 16 + kBands - 1) / kBands),
-                    static_cast<unsigned>((a.K / 16 + 15) / 16));
-    launch_pdl(k_tile_ts2<DT, ERR>, grid, kTileThreads, Tile2::BYTES, s, a);
+    const int64_t ctas = ((a.M / 16 + kBands - 1) / kBands) * ((a.K / 16 + 7) / 8);
+    launch_pdl(k_tile_ts4<ERR>, dim3(static_cast<unsigned>(ctas)), kTileThreads, kTile4Bytes, s, a);
     return static_cast<int>(cudaGetLastError());
 }
 
 template <int DT, int ERR>
 int launch_tile_4o6(const QuantArgs& a, cudaStream_t s) {
     if constexpr (DT == NVFP4_F32) {
-        return launch_tile_ts2<DT, ERR>(a, s);
+        return launch_tile_ts4<ERR>(a, s);
     } else {
         static int configured_dev = -1;
         int dev = 0;

@@ -367,7 +367,7 @@ ROWCOL_SHAPES = [(16, 16), (16, 1040), (48, 528), (80, 240), (272, 48), (64, 512
 def test_row_col_kernels_shape_sweep(shape):
     """The staged row+col kernels over shapes that start and end inside a
     CTA along both axes (a CTA is 4 bands x 32 tiles for bf16 four-over-six
-    and 1x16 nearest rounding, 4 bands x 16 tiles for fp32 four-over-six):
+    and 1x16 nearest rounding, 4 bands x 8 tiles for fp32 four-over-six):
     one tile; one band of 65 tiles; 3 bands x 33 tiles; 5 bands x 15 tiles;
     17 bands x 3 tiles; exactly one CTA; 13 bands x 49 tiles.  Every output
     byte against the oracle, both error modes and both bounds for
