@@ -8,7 +8,15 @@
 //               warp.  The band is then staged in shared memory and each
 //               thread owns one column (x^T's row) of it for the columnwise
 //               pass; the 4 bands' columnwise codes wait in shared memory and
-//               leave as one 32-byte run per column.
+//               leave as one 32-byte run per column.  It serves the 1x16
+//               row+col calls with stochastic rounding, with four-over-six
+//               and with fp32 input.
+// k_tile_r1     1x16 row+col, nearest rounding, bf16: one thread per 16x16
+//               tile staged in shared memory, its rows and columns encoded
+//               as independent blocks.
+// k_tile_p      plain 16x16 row+col (nearest or stochastic): one thread per
+//               tile, the tile's one scale serving both outputs, the
+//               columnwise codes the rowwise ones transposed.
 // k_tile_ts     four-over-six 16x16 with rowwise AND columnwise output, bf16
 //               input: one thread owns a whole 16x16 tile, copies its 16 rows
 //               into shared memory up front, and walks them twice (amax; both
