@@ -861,7 +861,9 @@ def run_gpu(args, rank, world, local_rank):
                    "launch": ("the K timed steps captured once as a CUDA graph and replayed (same kernels and "
                               "arguments, each step its own step index)" if args.graph else
                               "calls issued one by one from Python")},
-        "gpu_launches": nsteps * sum(1 for name, _, _, _ in plan if not args.only or args.only in name),
+        # a per-tensor amax call launches two kernels (the zero, then the amax)
+        "gpu_launches": nsteps * sum(2 if kern.startswith("k_amax_tensor") else 1
+                                     for name, kern, _, _ in plan if not args.only or args.only in name),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "calls": calls,
         "fp4_mm": mm, "c4_rowcol": c4, "rowcol_plain": rc, "variants": var,
     }

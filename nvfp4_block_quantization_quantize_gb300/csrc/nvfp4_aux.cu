@@ -89,6 +89,16 @@ constexpr int kAmaxUnroll = 4;
 
 // bf16 without a residual keeps its running maximum as a packed pair of bf16
 // magnitudes (absmax_bf16x2: exact, NaN-dropping) and widens it once at the end.
+// The per-tensor amax's zero, as a kernel so that the stream keeps
+// programmatic launch edges between kernels (a memset between two kernels
+// ends the overlap of one's tail with the next's launch).  It waits for the
+// previous kernel, which may still read the old amax.
+__global__ void k_amax_zero(float* out) {
+    pdl_wait();
+    out[0] = 0.0f;
+    pdl_trigger();
+}
+
 template <int DT, bool EF>
 __global__ void __launch_bounds__(kThreads) k_amax_tensor(const void* x, const float* res,
                                                           int64_t nvec, float* out) {
@@ -351,7 +361,7 @@ int launch_amax(const void* x, int64_t M, int64_t K, int dtype, const float* res
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool ef = residual != nullptr;
     if (mode == NVFP4_GAMAX_TENSOR) {
-        cudaMemsetAsync(out, 0, sizeof(float), s);
+        launch_pdl(k_amax_zero, 1, 1, 0, s, out);
         const int64_t nvec = M * (K / 8);
         if (nvec > 0) {
             const int g = grid_for((nvec + kAmaxUnroll - 1) / kAmaxUnroll);
