@@ -172,10 +172,17 @@ def _empty(shape, dtype, dev):
 # results ready unless they are non-blocking (below).  (Kernels reading and
 # writing mapped pinned memory in place
 # over the host link measured 2-2.5x slower than these bulk copies.)
-def _host_in(t, dev):
-    """An input (or the in-place residual) of a host call."""
-    if t is None or t.is_cuda:
+def _host_in(t, dev, name="input"):
+    """An input (or the in-place residual) of a host call: a host tensor is
+    staged on the call's device; a device tensor must already be there (the
+    kernels take its pointer) and is made contiguous (an in-place residual is
+    checked to be contiguous before, so it is passed itself)."""
+    if t is None:
         return t
+    if t.is_cuda:
+        if t.device != dev:
+            raise ValueError(f"nvfp4: {name} must be on {dev} (got {t.device})")
+        return t.contiguous()
     return _stage(t.contiguous(), dev)
 
 
@@ -227,8 +234,15 @@ def _dev_residual(residual, dev, M=None, K=None):
     return _check_dev(residual, "residual", torch.float32, M * K, dev)
 
 
-def _host_residual(residual, M, K):
-    if residual is not None and (residual.dtype != torch.float32 or residual.numel() != M * K):
+def _host_residual(residual, M, K, dev=None):
+    """The residual of a host call: a host float32 tensor of M*K elements
+    (staged and copied back), or a device one the kernels update in place,
+    which must then be float32 [M,K], contiguous and on the call's device."""
+    if residual is None:
+        return
+    if residual.is_cuda:
+        _check_dev(residual, "residual", torch.float32, M * K, dev)
+    elif residual.dtype != torch.float32 or residual.numel() != M * K:
         raise ValueError("nvfp4: the residual must be float32 with M*K elements")
 
 
@@ -486,7 +500,7 @@ def nvfp4_quantize(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=No
     bound = _default_bound(em, scale_bound)
     given = {"codes": codes, "scales": scales, "codes_col": codes_col, "scales_col": scales_col}
     if host:
-        _host_residual(residual, M, K)
+        _host_residual(residual, M, K, dev)
         _non_blocking_stream(non_blocking, stream)
         rows = not colwise and M >= _PIPE_MIN_ROWS and gm in (GAMAX_NONE, GAMAX_TENSOR_GIVEN, GAMAX_ROW_GIVEN)
         if stream is None and (rows or non_blocking):
@@ -673,7 +687,7 @@ def nvfp4_qdq(x: torch.Tensor, *, block="1x16", rounding="rtn", residual=None, s
     gm, em = _enum("gamax_mode", gamax_mode), _enum("err_mode", err_mode)
     bound = _default_bound(em, scale_bound)
     if host:
-        _host_residual(residual, M, K)
+        _host_residual(residual, M, K, dev)
         _non_blocking_stream(non_blocking, stream)
         rows = M >= _PIPE_MIN_ROWS and gm in (GAMAX_NONE, GAMAX_TENSOR_GIVEN, GAMAX_ROW_GIVEN)
         if stream is None and (rows or non_blocking):
@@ -726,6 +740,8 @@ def nvfp4_dequantize(codes: torch.Tensor, scales: torch.Tensor, M: int, K: int, 
     for t, name, n in ((codes, "codes", M * K // 2), (scales, "scales", M * K // 16)):
         if t.dtype != torch.uint8 or t.numel() != n:
             raise ValueError(f"nvfp4: {name} must be uint8 with {n} elements")
+    if not host and scales.device != dev:
+        raise ValueError(f"nvfp4: the scales of a call on device codes must be on {dev} (got {scales.device})")
     g = None
     if gm != GAMAX_NONE:
         if gamax is None:
@@ -744,8 +760,8 @@ def nvfp4_dequantize(codes: torch.Tensor, scales: torch.Tensor, M: int, K: int, 
             return r
     if host:
         _non_blocking_refused(non_blocking)
-    c = _host_in(codes, dev) if host else codes.contiguous()
-    s = _host_in(scales, dev) if host else scales.contiguous()
+    c = _host_in(codes, dev, "codes") if host else codes.contiguous()
+    s = _host_in(scales, dev, "scales") if host else scales.contiguous()
     o = _out_buf((M, K), torch.bfloat16 if od == BF16 else torch.float32, out, dev, host, "out")
     if host:
         _inputs_ready(stream)
@@ -763,7 +779,7 @@ def nvfp4_amax(x: torch.Tensor, *, residual=None, per_row: bool = False, out=Non
     dev = _device_of(x, residual)
     M, K = x.shape
     if host:
-        _host_residual(residual, M, K)
+        _host_residual(residual, M, K, dev)
     xd = _host_in(x, dev) if host else x.contiguous()
     rd = _host_in(residual, dev) if host else _dev_residual(residual, dev, M, K)
     need = max(M, 1) if per_row else 1
@@ -789,14 +805,24 @@ def nvfp4_scales_to_mma(scales: torch.Tensor, out=None, stream=None) -> torch.Te
     """Row-major scale bytes [rows, cols] -> the block-scaled matrix-multiply
     layout, [128*ceil(rows/128), 4*ceil(cols/4)] bytes (see nvfp4.h)."""
     lib = load_library()
+    if scales.dim() != 2 or scales.dtype != torch.uint8:
+        raise ValueError("nvfp4_scales_to_mma: scales must be a uint8 [rows, cols] tensor")
     host = not scales.is_cuda
-    dev = scales.device if scales.is_cuda else torch.device("cuda", torch.cuda.current_device())
-    s = _stage(scales.contiguous(), dev)
-    rows, cols = s.shape
+    rows, cols = scales.shape
     R, C = -(-rows // 128) * 128, -(-cols // 4) * 4
-    o = out if out is not None else _empty((R, C), torch.uint8, dev)
-    _check(lib, lib.nvfp4_scales_to_mma(_ptr(s), rows, cols, _ptr(o), _stream(stream)))
-    return o.cpu() if host else o
+    if out is not None and not out.is_cuda and not host:
+        raise ValueError("nvfp4_scales_to_mma: the output of a call on device scales must be a device tensor")
+    if out is not None and not out.is_cuda and (out.dtype != torch.uint8 or out.numel() != R * C):
+        raise ValueError(f"nvfp4_scales_to_mma: out must be uint8 with {R * C} elements")
+    dev = scales.device if scales.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    o = _check_dev(out, "out", torch.uint8, R * C, dev) if out is not None and out.is_cuda else \
+        _empty((R, C), torch.uint8, dev)
+    s = _stage(scales.contiguous(), dev)
+    with torch.cuda.device(dev):
+        _check(lib, lib.nvfp4_scales_to_mma(_ptr(s), rows, cols, _ptr(o), _stream(stream)))
+    if host or (out is not None and not out.is_cuda):
+        return _finish_host({"o": o}, {"o": out}, stream)["o"]
+    return o
 
 
 def nvfp4_mm(codes_a, scales_a, codes_b, scales_b, M: int, N: int, K: int, *, gamax_a=None, gamax_b=None,
@@ -805,12 +831,35 @@ def nvfp4_mm(codes_a, scales_a, codes_b, scales_b, M: int, N: int, K: int, *, ga
     scales in the nvfp4_scales_to_mma layout (see nvfp4.h).  Device tensors."""
     lib = load_library()
     odt = _enum("dtype", out_dtype)
-    dev = codes_a.device
+    dev = _check_mm_args(codes_a, scales_a, codes_b, scales_b, M, N, K, gamax_a, gamax_b, out, odt)
     o = out if out is not None else _empty((M, N), torch.float32 if odt == F32 else torch.bfloat16, dev)
-    rc = lib.nvfp4_mm(_ptr(codes_a), _ptr(scales_a), _ptr(codes_b), _ptr(scales_b), M, N, K, _ptr(gamax_a),
-                      _ptr(gamax_b), scale_bound, _ptr(o), odt, _stream(stream))
+    with torch.cuda.device(dev):
+        rc = lib.nvfp4_mm(_ptr(codes_a), _ptr(scales_a), _ptr(codes_b), _ptr(scales_b), M, N, K, _ptr(gamax_a),
+                          _ptr(gamax_b), scale_bound, _ptr(o), odt, _stream(stream))
     _check(lib, rc)
     return o
+
+
+def _check_mm_args(codes_a, scales_a, codes_b, scales_b, M, N, K, gamax_a, gamax_b, out, odt):
+    """nvfp4_mm's tensors, checked before their pointers reach the kernel:
+    all on codes_a's CUDA device, contiguous, of their dtype, and (for shapes
+    the library accepts: M, N multiples of 128, K of 64) holding at least
+    the bytes the product reads or writes.  Shapes the library refuses are
+    left to its own EINVAL.  Returns the device."""
+    if not torch.is_tensor(codes_a) or not codes_a.is_cuda:
+        raise ValueError("nvfp4_mm: the operands must be CUDA tensors")
+    dev = codes_a.device
+    ok = min(M, N, K) >= 0 and M % 128 == 0 and N % 128 == 0 and K % 64 == 0
+    for t, name, n in ((codes_a, "codes_a", M * K // 2), (scales_a, "scales_a", M * K // 16),
+                       (codes_b, "codes_b", N * K // 2), (scales_b, "scales_b", N * K // 16)):
+        _check_dev(t, name, torch.uint8, n if ok else 0, dev, at_least=True)
+    for g, name in ((gamax_a, "gamax_a"), (gamax_b, "gamax_b")):
+        if g is not None:
+            _check_dev(g, name, torch.float32, 1, dev, at_least=True)
+    if out is not None:
+        _check_dev(out, "out", torch.float32 if odt == F32 else torch.bfloat16, M * N if ok else 0, dev,
+                   at_least=True)
+    return dev
 
 
 def nvfp4_global_scales(gamax: torch.Tensor, scale_bound: float = 448.0, stream=None):
@@ -830,23 +879,41 @@ def nvfp4_global_scales(gamax: torch.Tensor, scale_bound: float = 448.0, stream=
 def nvfp4_probe_divide(a: torch.Tensor, b: torch.Tensor, stream=None) -> torch.Tensor:
     """Diagnostic: the plain path's device division a / b, elementwise (fp32)."""
     lib = load_library()
+    _check_probe_inputs((a, torch.float32, "a"), (b, torch.float32, "b"))
+    if a.numel() != b.numel():
+        raise ValueError("nvfp4_probe_divide: a and b must hold the same number of values")
     a = a.contiguous()
     b = b.contiguous()
     out = torch.empty_like(a)
-    _check(lib, lib.nvfp4_probe_divide(_ptr(a), _ptr(b), _ptr(out), a.numel(), _stream(stream)))
+    with torch.cuda.device(a.device):
+        _check(lib, lib.nvfp4_probe_divide(_ptr(a), _ptr(b), _ptr(out), a.numel(), _stream(stream)))
     return out
+
+
+def _check_probe_inputs(*specs):
+    """A diagnostic's inputs: (tensor, dtype, name) each a CUDA tensor of that
+    dtype, all on one device (their pointers go to the kernel as they are)."""
+    dev = None
+    for t, dtype, name in specs:
+        if not torch.is_tensor(t) or not t.is_cuda or t.dtype != dtype:
+            raise ValueError(f"nvfp4 probe: {name} must be a CUDA {dtype} tensor")
+        if dev is not None and t.device != dev:
+            raise ValueError(f"nvfp4 probe: {name} must be on {dev} (got {t.device})")
+        dev = t.device
 
 
 def nvfp4_probe_sub_f16(q: torch.Tensor, v: torch.Tensor, stream=None) -> torch.Tensor:
     """Diagnostic: f16 halves of the int32 words q minus the float32 pairs v,
     rounded once (float32 [2 * q.numel()])."""
     lib = load_library()
+    _check_probe_inputs((q, torch.int32, "q"), (v, torch.float32, "v"))
+    if v.numel() != 2 * q.numel():
+        raise ValueError("nvfp4: q must be int32 words and v float32 with two values per word")
     q = q.contiguous()
     v = v.contiguous()
-    if q.dtype != torch.int32 or v.dtype != torch.float32 or v.numel() != 2 * q.numel():
-        raise ValueError("nvfp4: q must be int32 words and v float32 with two values per word")
     out = torch.empty_like(v)
-    _check(lib, lib.nvfp4_probe_sub_f16(_ptr(q), _ptr(v), _ptr(out), q.numel(), _stream(stream)))
+    with torch.cuda.device(v.device):
+        _check(lib, lib.nvfp4_probe_sub_f16(_ptr(q), _ptr(v), _ptr(out), q.numel(), _stream(stream)))
     return out
 
 
@@ -854,9 +921,14 @@ def nvfp4_probe_e2m1(first: int, n: int, out=None, stream=None) -> torch.Tensor:
     """Diagnostic: the device e2m1 codes of the n fp32 bit patterns from
     ``first`` on, packed two per byte (uint8 [(n + 1) // 2])."""
     lib = load_library()
-    dev = torch.device("cuda", torch.cuda.current_device())
-    o = out if out is not None else _empty(((n + 1) // 2,), torch.uint8, dev)
-    _check(lib, lib.nvfp4_probe_e2m1(first, n, _ptr(o), _stream(stream)))
+    need = (max(n, 0) + 1) // 2
+    if out is not None:
+        _check_probe_inputs((out, torch.uint8, "out"))
+        o = _check_dev(out, "out", torch.uint8, need, out.device, at_least=True)
+    else:
+        o = _empty((need,), torch.uint8, torch.device("cuda", torch.cuda.current_device()))
+    with torch.cuda.device(o.device):
+        _check(lib, lib.nvfp4_probe_e2m1(first, n, _ptr(o), _stream(stream)))
     return o
 
 

@@ -127,3 +127,16 @@ def test_non_blocking_host_calls_refuse_a_stream():
     nv._non_blocking_stream(False, object())
     with pytest.raises(ValueError):
         nv._non_blocking_refused(True)
+
+
+def test_product_and_probe_operands_must_be_device_tensors():
+    """nvfp4_mm and the diagnostics hand their tensors' pointers to kernels
+    as they are: host tensors are refused before any CUDA call."""
+    z = torch.zeros(128 * 64, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        nv._check_mm_args(z, z, z, z, 128, 128, 128, None, None, None, nv.BF16)
+    with pytest.raises(ValueError):
+        nv._check_probe_inputs((torch.ones(4), torch.float32, "a"))
+    with pytest.raises(ValueError):                     # wrong dtype is refused before the device test
+        nv._check_probe_inputs((torch.ones(4, dtype=torch.int32), torch.float32, "v"))
+

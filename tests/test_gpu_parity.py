@@ -304,6 +304,45 @@ def test_host_pageable_outputs_and_device_call_refusal():
         nv.nvfp4_quantize(to_dev(x), rounding="sr", residual=torch.zeros((64, 128)))
 
 
+def test_mixed_device_tensors_are_checked_or_refused():
+    """Tensors whose pointers the kernels take as they are: a device residual
+    of a host call is updated in place when it is float32 [M,K] and
+    contiguous, and refused otherwise (a zero-stride view would have the
+    kernel write M*K floats into K); device codes with host scales, host or
+    short operands of the FP4 product, and host probe inputs are refused."""
+    x = mat((64, 128), seed=17)
+    r0 = mat((64, 128), seed=18) * np.float32(0.01)
+    rd = to_dev(r0.copy())
+    g = nv.nvfp4_quantize(torch.from_numpy(x), rounding="sr", seed=3, residual=rd)
+    ro = r0.copy()
+    o = oracle.quantize(x, rounding=oracle.SR, seed=3, residual=ro)
+    assert_same(g["codes"].numpy(), o["codes"], "codes")
+    assert_same(to_np(rd), ro, "device residual of a host call")
+    with pytest.raises(ValueError):
+        nv.nvfp4_quantize(torch.from_numpy(x), rounding="sr", residual=torch.zeros((1, 128), device="cuda").expand(64, 128))
+    with pytest.raises(ValueError):
+        nv.nvfp4_qdq(torch.from_numpy(x), rounding="sr", residual=to_dev(r0).t().contiguous().t())
+    with pytest.raises(ValueError):
+        nv.nvfp4_amax(torch.from_numpy(x), residual=to_dev(r0).to(torch.bfloat16))
+    q = nv.nvfp4_quantize(to_dev(x))
+    with pytest.raises(ValueError):
+        nv.nvfp4_dequantize(q["codes"], q["scales"].cpu(), 64, 128)
+    z = torch.zeros(128 * 64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ValueError):                      # a host operand
+        nv.nvfp4_mm(z, z.cpu(), z, z, 128, 128, 128)
+    with pytest.raises(ValueError):                      # codes_a holds 8 KB of the 16 KB it reads
+        nv.nvfp4_mm(z[:128 * 64], z, z, z, 128, 128, 256)
+    with pytest.raises(ValueError):
+        nv.nvfp4_mm(z, z, z, z, 128, 128, 128, out=torch.empty((128, 128), dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        nv.nvfp4_probe_divide(torch.ones(4), torch.ones(4, device="cuda"))
+    with pytest.raises(ValueError):
+        nv.nvfp4_scales_to_mma(q["scales"], out=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    host_out = torch.empty((128, 8), dtype=torch.uint8)
+    assert nv.nvfp4_scales_to_mma(q["scales"].cpu(), out=host_out) is host_out
+    assert_same(host_out.numpy(), to_np(nv.nvfp4_scales_to_mma(q["scales"])), "scales_to_mma into a host tensor")
+
+
 def _host(x: np.ndarray, pinned: bool = True) -> torch.Tensor:
     t = (torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16) if x.dtype == np.uint16
          else torch.from_numpy(x.copy()))
