@@ -20,12 +20,13 @@ from . import (nvfp4_dequantize, nvfp4_global_scales, nvfp4_mm, nvfp4_quantize,
 def to_fp4_operands(q: dict) -> dict:
     """{"codes", "scales"} of a rowwise quantize call (device tensors) ->
     {"fp4": codes as float4_e2m1fn_x2 [M, K/2], "scales": float8_e4m3fn in the
-    matrix-multiply layout, "scale_dec": the per-tensor decode scale or 1}."""
+    matrix-multiply layout, "gamax": the per-tensor amax the codes were made
+    with, or None without a global scale}; fp4_mm derives the decode scale
+    from it with the library's nvfp4_global_scales."""
     codes, scales = q["codes"], q["scales"]
     out = {"fp4": codes.view(torch.float4_e2m1fn_x2),
            "scales": nvfp4_scales_to_mma(scales).view(torch.float8_e4m3fn)}
-    g = q.get("gamax")
-    out["scale_dec"] = None if g is None else g
+    out["gamax"] = q.get("gamax")
     return out
 
 
@@ -40,7 +41,7 @@ def fp4_mm(a: dict, b: dict, *, out_dtype=torch.bfloat16, scale_bound: float = 4
     """a @ b^T for rowwise-quantized a [M, K] and b [N, K] (each the dict of
     to_fp4_operands): the block-scaled product times both decode scales."""
     y = torch._scaled_mm(a["fp4"], b["fp4"].t(), a["scales"], b["scales"], out_dtype=torch.float32)
-    s = _scale_dec(a.get("scale_dec"), scale_bound) * _scale_dec(b.get("scale_dec"), scale_bound)
+    s = _scale_dec(a.get("gamax"), scale_bound) * _scale_dec(b.get("gamax"), scale_bound)
     return (y * s).to(out_dtype)
 
 

@@ -168,3 +168,22 @@ def matrix(shape, seed: int, dtype: str = "f32", outlier_frac: float = 0.0,
     if outlier_frac:
         x = with_outlier_columns(x, outlier_frac, outlier_factor, rng)
     return to_bf16_bits(x) if dtype == "bf16" else x
+
+
+# ---- tensors past 2^32 elements ------------------------------------------------------------
+def tiled_row_map(M: int, P: int) -> tuple[np.ndarray, np.ndarray]:
+    """Row r of an [M, K] tensor built from P base rows is base row p[r]
+    scaled by 2^e[r], e in [-4, 4]: a fixed integer map, so the whole tensor
+    can be assembled on the device (a row gather and an exact power-of-two
+    multiply) while any band of it is rebuilt on the host with the same
+    values.  Returns (p, e) as int64 arrays of M entries."""
+    r = np.arange(M, dtype=np.int64)
+    p = (r * 97 + (r >> 8) * 13) % P
+    e = ((r >> 4) * 7 + r) % 9 - 4
+    return p, e
+
+
+def tiled_rows(base: np.ndarray, p: np.ndarray, e: np.ndarray, r0: int, r1: int) -> np.ndarray:
+    """Rows [r0, r1) of the tiled tensor as fp32 values (base: fp32 [P, K];
+    the scaling by a power of two is exact for values well inside the range)."""
+    return base[p[r0:r1]] * np.exp2(e[r0:r1]).astype(np.float32)[:, None]
