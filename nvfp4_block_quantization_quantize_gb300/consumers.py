@@ -45,6 +45,36 @@ def fp4_mm(a: dict, b: dict, *, out_dtype=torch.bfloat16, scale_bound: float = 4
     return (y * s).to(out_dtype)
 
 
+# ---- fp4_matmul: the portable product ---------------------------------------------------------
+def _dequantized_operand(t: torch.Tensor, stochastic: bool, seed: int, step: int) -> torch.Tensor:
+    q = nvfp4_quantize(t.contiguous(), rounding="sr" if stochastic else "rtn", seed=seed, step=step)
+    return nvfp4_dequantize(q["codes"], q["scales"], t.shape[0], t.shape[1], out_dtype="bf16")
+
+
+def fp4_matmul(a: torch.Tensor, b: torch.Tensor, stochastic: bool = False, seed: int = 0,
+               step: int = 0) -> torch.Tensor:
+    """a @ b^T with FP4 operands by the portable path ("fp4-train", API:
+    fp4_matmul, dequantize and a bf16 product).
+
+    Both operands are quantized rowwise in 1x16 blocks with the page's recipe
+    as fp4_linear does (no global scale; round-to-nearest, or stochastic
+    rounding keyed on (seed, step) for a and (seed + 1, step) for b) and
+    dequantized to bf16 by the library.  Those values are exact in bf16 (a
+    grid value of two significant bits times a scale of four), and the
+    product accumulates them in fp32 (a library GEMM on their fp32 widening,
+    at torch's default full fp32 matmul precision) before one rounding to bf16, so it equals the tensor-core
+    product (nvfp4_mm, bf16 out) wherever the fp32 sums are exact and
+    otherwise differs only in their order.  a [M, K], b [N, K]: CUDA float32
+    / bfloat16, K a multiple of 16; returns bf16 [M, N]."""
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError("fp4_matmul: a [M, K] and b [N, K]")
+    if a.shape[1] % 16:
+        raise ValueError("fp4_matmul: K must be a multiple of 16")
+    da = _dequantized_operand(a, stochastic, seed, step)
+    db = _dequantized_operand(b, stochastic, seed + 1, step)
+    return torch.matmul(da.float(), db.float().t()).to(torch.bfloat16)
+
+
 # ---- fp4_linear -------------------------------------------------------------------------------
 def _pad_rows(t: torch.Tensor, mult: int) -> torch.Tensor:
     pad = (-t.shape[0]) % mult

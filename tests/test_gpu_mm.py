@@ -144,3 +144,51 @@ def test_fp4_linear_rejects_bad_shapes():
     from nvfp4_block_quantization_quantize_gb300.consumers import fp4_linear
     with pytest.raises(ValueError):
         fp4_linear(torch.zeros(128, 48, device="cuda"), torch.zeros(128, 48, device="cuda"))
+
+
+def test_fp4_matmul_portable_path():
+    """fp4_matmul (dequantize, then the product): with operands on the e2m1
+    grid and a 6 in every 16-element block (every scale 1, so the oracle's
+    dequantized operands are the inputs) every fp32 partial sum is exact, and
+    the result is the exact product rounded once to bf16, bit for bit equal
+    to the tensor-core product (nvfp4_mm, bf16 out) on the same codes; with
+    stochastic rounding of normal operands it is the product of the oracle's
+    dequantized operands within one bf16 rounding and the fp32 accumulation
+    bound."""
+    from nvfp4_block_quantization_quantize_gb300.consumers import fp4_matmul
+    rng = np.random.default_rng(31)
+    M, N, K = 256, 384, 512
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float32)
+
+    def on_grid(rows):
+        v = grid[rng.integers(0, 8, (rows, K))] * rng.choice(np.array([-1, 1], np.float32), (rows, K))
+        v[:, ::16] = 6.0
+        return v
+
+    a, b = on_grid(M), on_grid(N)
+    y = fp4_matmul(to_dev(a), to_dev(b))
+    qa, qb = nv.nvfp4_quantize(to_dev(a)), nv.nvfp4_quantize(to_dev(b))
+    t = nv.nvfp4_mm(qa["codes"], nv.nvfp4_scales_to_mma(qa["scales"]), qb["codes"],
+                    nv.nvfp4_scales_to_mma(qb["scales"]), M, N, K, out_dtype="bf16")
+    torch.cuda.synchronize()
+    oa, ob = oracle.quantize(a), oracle.quantize(b)
+    da = oracle.dequantize(oa["codes"], oa["scales"], M, K, out_dtype=oracle.F32).astype(np.float64)
+    db = oracle.dequantize(ob["codes"], ob["scales"], N, K, out_dtype=oracle.F32).astype(np.float64)
+    exact = W.to_bf16_bits((da @ db.T).astype(np.float32))     # the float64 sums are exact, and so is the cast
+    assert np.array_equal(to_np(y), exact)
+    assert np.array_equal(to_np(t), exact)
+
+    x = W.matrix((M, K), seed=141)
+    w = W.matrix((N, K), seed=143, dist="t")
+    y = fp4_matmul(to_dev(x), to_dev(w), stochastic=True, seed=3, step=2)
+    torch.cuda.synchronize()
+    ox = oracle.quantize(x, rounding=oracle.SR, seed=3, step=2)
+    ow = oracle.quantize(w, rounding=oracle.SR, seed=4, step=2)
+    dx = oracle.dequantize(ox["codes"], ox["scales"], M, K, out_dtype=oracle.F32).astype(np.float64)
+    dw = oracle.dequantize(ow["codes"], ow["scales"], N, K, out_dtype=oracle.F32).astype(np.float64)
+    ref = dx @ dw.T
+    got = W.bf16_bits_to_f32(to_np(y)).astype(np.float64)
+    bound = (np.abs(dx) @ np.abs(dw).T) * K * 2.0 ** -23 + np.abs(ref) * 2.0 ** -8
+    assert (np.abs(got - ref) <= bound + 1e-30).all()
+    with pytest.raises(ValueError):
+        fp4_matmul(to_dev(x[:, :40]), to_dev(w[:, :40]))
