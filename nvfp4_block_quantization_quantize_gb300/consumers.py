@@ -17,12 +17,16 @@ from . import (nvfp4_dequantize, nvfp4_global_scales, nvfp4_mm, nvfp4_quantize,
                nvfp4_scales_to_mma)
 
 
-def to_fp4_operands(q: dict) -> dict:
-    """{"codes", "scales"} of a rowwise quantize call (device tensors) ->
+def to_fp4_operands(q, stochastic: bool = False, seed: int = 0, step: int = 0) -> dict:
+    """{"codes", "scales"} of a rowwise quantize call (device tensors), or a
+    CUDA tensor [M, K] to quantize first with the page's recipe (1x16 blocks,
+    no global scale; nearest, or stochastic rounding keyed on (seed, step)) ->
     {"fp4": codes as float4_e2m1fn_x2 [M, K/2], "scales": float8_e4m3fn in the
     matrix-multiply layout, "gamax": the per-tensor amax the codes were made
     with, or None without a global scale}; fp4_mm derives the decode scale
     from it with the library's nvfp4_global_scales."""
+    if torch.is_tensor(q):
+        q = nvfp4_quantize(q.contiguous(), rounding="sr" if stochastic else "rtn", seed=seed, step=step)
     codes, scales = q["codes"], q["scales"]
     out = {"fp4": codes.view(torch.float4_e2m1fn_x2),
            "scales": nvfp4_scales_to_mma(scales).view(torch.float8_e4m3fn)}
@@ -37,9 +41,16 @@ def _scale_dec(g, bound: float) -> torch.Tensor | float:
     return nvfp4_global_scales(g.float().reshape(-1)[:1].contiguous(), bound)[1]
 
 
-def fp4_mm(a: dict, b: dict, *, out_dtype=torch.bfloat16, scale_bound: float = 448.0) -> torch.Tensor:
-    """a @ b^T for rowwise-quantized a [M, K] and b [N, K] (each the dict of
-    to_fp4_operands): the block-scaled product times both decode scales."""
+def fp4_mm(a, b, stochastic: bool = False, seed: int = 0, step: int = 0, *, out_dtype=torch.bfloat16,
+           scale_bound: float = 448.0) -> torch.Tensor:
+    """a @ b^T for rowwise-quantized a [M, K] and b [N, K]: each the dict of
+    to_fp4_operands, or a CUDA tensor it quantizes first (stochastic rounding
+    keyed on (seed, step) for a and (seed + 1, step) for b, as fp4_matmul and
+    fp4_linear do); the block-scaled product times both decode scales."""
+    if torch.is_tensor(a):
+        a = to_fp4_operands(a, stochastic, seed, step)
+    if torch.is_tensor(b):
+        b = to_fp4_operands(b, stochastic, seed + 1, step)
     y = torch._scaled_mm(a["fp4"], b["fp4"].t(), a["scales"], b["scales"], out_dtype=torch.float32)
     s = _scale_dec(a.get("gamax"), scale_bound) * _scale_dec(b.get("gamax"), scale_bound)
     return (y * s).to(out_dtype)

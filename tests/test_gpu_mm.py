@@ -192,3 +192,23 @@ def test_fp4_matmul_portable_path():
     assert (np.abs(got - ref) <= bound + 1e-30).all()
     with pytest.raises(ValueError):
         fp4_matmul(to_dev(x[:, :40]), to_dev(w[:, :40]))
+
+
+def test_fp4_mm_and_operands_take_raw_tensors():
+    """fp4_mm(a, b, stochastic, seed, step) on raw tensors quantizes them as
+    to_fp4_operands does ((seed, step) for a, (seed + 1, step) for b) and
+    gives the same product as on those operands; the codes are the oracle's."""
+    from nvfp4_block_quantization_quantize_gb300.consumers import fp4_mm, to_fp4_operands
+    M, N, K = 128, 256, 512
+    a, b = W.matrix((M, K), seed=151, dtype="bf16"), W.matrix((N, K), seed=157, dtype="bf16")
+    oa = to_fp4_operands(to_dev(a), stochastic=True, seed=8, step=1)
+    assert np.array_equal(to_np(oa["fp4"].view(torch.uint8)),
+                          oracle.quantize(a, rounding=oracle.SR, seed=8, step=1)["codes"])
+    ob = to_fp4_operands(to_dev(b), stochastic=True, seed=9, step=1)
+    try:
+        y_ops = fp4_mm(oa, ob, out_dtype=torch.float32)
+        y_raw = fp4_mm(to_dev(a), to_dev(b), stochastic=True, seed=8, step=1, out_dtype=torch.float32)
+    except (RuntimeError, NotImplementedError, TypeError, AttributeError) as e:
+        pytest.skip(f"no library block-scaled FP4 GEMM: {e}")
+    torch.cuda.synchronize()
+    assert torch.equal(y_ops, y_raw)
