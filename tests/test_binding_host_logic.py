@@ -140,3 +140,21 @@ def test_product_and_probe_operands_must_be_device_tensors():
     with pytest.raises(ValueError):                     # wrong dtype is refused before the device test
         nv._check_probe_inputs((torch.ones(4, dtype=torch.int32), torch.float32, "v"))
 
+
+
+def test_error_feedback_keeps_one_residual_per_name():
+    from nvfp4_block_quantization_quantize_gb300.error_feedback import ErrorFeedback
+    ef = ErrorFeedback(stochastic=False)
+    w = torch.ones(4, 16)
+    r = ef.residual("a", w)
+    assert r.dtype == torch.float32 and r.shape == w.shape and not r.any()
+    r += 1.0
+    assert ef.residual("a", w) is r                      # carried, not re-created
+    with pytest.raises(ValueError):                     # another shape: refused, not reset
+        ef.residual("a", torch.ones(4, 32))
+    ef.residual("b", torch.ones(2, 16))
+    assert sorted(ef.names()) == ["a", "b"]
+    ef.reset("a")
+    assert not ef.residual("a", w).any()
+    ef.reset()
+    assert ef.names() == []

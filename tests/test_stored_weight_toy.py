@@ -173,3 +173,23 @@ def test_stored_weight_mlp_gpu():
     ref = _oracle_mlp_curves()
     for k in ("rtn", "sr", "ef"):
         assert np.array_equal(curves[k], ref[k]), k
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("stochastic", [False, True])
+def test_error_feedback_state_runs_the_usage_loop(stochastic):
+    """The page's stored-weight loop through ErrorFeedback (W = ef.qdq(name,
+    W - lr * grad, step)): its residual is carried across the steps, and the
+    loss curve equals the oracle's with the same residual, bit for bit."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import nvfp4_block_quantization_quantize_gb300 as nv
+    from nvfp4_block_quantization_quantize_gb300.error_feedback import ErrorFeedback
+    nv.build()
+    nv.load_library()
+    ef = ErrorFeedback(stochastic=stochastic, seed=7)
+    curve = _train(lambda W, t: ef.qdq("layer0.weight", torch.from_numpy(W).cuda(), step=t).float().cpu().numpy())
+    assert ef.names() == ["layer0.weight"]
+    ref = _train(_oracle_qdq(oracle.SR if stochastic else oracle.RTN, True))
+    assert np.array_equal(curve, ref)
