@@ -30,6 +30,12 @@ MUTATIONS = {
     "block amax propagates NaN": ("float max_nd(float a, float b) { return std::fmax(a, b); }",
                                   "float max_nd(float a, float b) { return (a > b || a != a) ? a : b; }"),
     "SR rounds up on u == p": ("(u < p ? k + 1 : k)", "(u <= p ? k + 1 : k)"),
+    "S_enc falls back to 1 only for a zero amax": ("if (!(A > 0.0f) || std::isinf(A)) enc = 1.0f;",
+                                                   "if (A == 0.0f) enc = 1.0f;"),
+    "S_enc not clamped to FLT_MAX": ("else enc = min_nd((6.0f * bound) / A, FLT_MAX);",
+                                     "else enc = (6.0f * bound) / A;"),
+    "S_dec computed from A instead of 1 / S_enc": (
+        "*S_dec = 1.0f / enc;", "*S_dec = (A > 0.0f && !std::isinf(A)) ? A / (6.0f * bound) : 1.0f;"),
     "Philox multipliers swapped": ("const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;",
                                    "const uint32_t M0 = 0xCD9E8D57u, M1 = 0xD2511F53u;"),
     "SR counter uses idx, not idx/4": ("const uint64_t blk = idx >> 2;", "const uint64_t blk = idx;"),
