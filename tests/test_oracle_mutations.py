@@ -30,6 +30,12 @@ MUTATIONS = {
     "block amax propagates NaN": ("float max_nd(float a, float b) { return std::fmax(a, b); }",
                                   "float max_nd(float a, float b) { return (a > b || a != a) ? a : b; }"),
     "SR rounds up on u == p": ("(u < p ? k + 1 : k)", "(u <= p ? k + 1 : k)"),
+    "four-over-six encode reciprocal not clamped to FLT_MAX": (
+        "const float enc = min_nd(1.0f / (dc[cand] * g.S_dec), FLT_MAX);",
+        "const float enc = 1.0f / (dc[cand] * g.S_dec);"),
+    "four-over-six encode divides instead of multiplying by the reciprocal": (
+        "cc[cand][i] = orc_e2m1_encode_rn(yv * enc);",
+        "cc[cand][i] = orc_e2m1_encode_rn(yv / (dc[cand] * g.S_dec));"),
     "S_enc falls back to 1 only for a zero amax": ("if (!(A > 0.0f) || std::isinf(A)) enc = 1.0f;",
                                                    "if (A == 0.0f) enc = 1.0f;"),
     "S_enc not clamped to FLT_MAX": ("else enc = min_nd((6.0f * bound) / A, FLT_MAX);",

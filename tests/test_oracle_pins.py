@@ -877,3 +877,52 @@ def test_scales_to_mma_is_the_blocked_permutation(rows, cols):
     idx = np.arange(R * C, dtype=np.int64).reshape(R, C)
     assert np.array_equal(np.sort(idx.reshape(R // 128, 4, 32, C // 4, 4).transpose(0, 3, 2, 1, 4).ravel()),
                           np.arange(R * C))
+
+
+def test_four_over_six_encode_is_the_clamped_reciprocal_multiply():
+    """[4o6 PR, What + Design]: a candidate encodes each element as y times
+    min(1/(d * S_dec), FLT_MAX), rounded to the nearest e2m1 value.  Two kinds
+    of blocks take the candidate decision out of the picture, so their codes
+    follow from that formula alone (brute-force e2m1 rounding):
+    - blocks whose amax is 2x a given global amax A: both candidates' scales
+      cap at 448, one scale byte 0x7E; the other elements sit at and next to
+      the e2m1 midpoints times the decode scale, where a multiply by the
+      rounded reciprocal and a true division round to different codes;
+    - blocks far below A: both scales encode to 0, and the FLT_MAX clamp
+      keeps zeros at code 0 (0 * inf would be NaN, code 7) while every other
+      value saturates."""
+    FLT_MAX = np.finfo(np.float32).max
+    differ = 0
+    for bound in (256.0, 448.0):
+        for A in (f32(0.37), f32(3.1), f32(1e-3)):
+            Senc, Sdec = oracle.global_scales(float(A), bound)
+            D = f32(f32(448.0) * f32(Sdec))
+            enc = np.minimum(f32(1.0) / D, FLT_MAX)
+            ys = []
+            for m in (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0):
+                y = f32(f32(m) * D)
+                for _ in range(4):
+                    y = np.nextafter(y, f32(0))
+                for _ in range(9):
+                    differ += int(brute_e2m1_rn(f32(y * enc))[0] != brute_e2m1_rn(f32(y / D))[0])
+                    ys += [y, -y]
+                    y = np.nextafter(y, f32(10))
+            ys += [f32(0.0)] * (-len(ys) % 15)
+            body = np.array(ys, np.float32).reshape(-1, 15)
+            big = np.concatenate([np.full((body.shape[0], 1), f32(2.0) * A, np.float32), body], axis=1)
+            tiny = np.zeros((2, 16), np.float32)
+            tiny[0, :4] = [1e-30, 0.0, -0.0, -3e-31]
+            tiny[1, 7] = np.float32(-0.0)
+            x = np.concatenate([big, tiny]).reshape(1, -1)      # the blocks along one row
+            for err in (oracle.ERR_MAE, oracle.ERR_MSE):
+                r = oracle.quantize(x, gamax_mode=oracle.GAMAX_TENSOR_GIVEN, gamax=np.array([A]),
+                                    err_mode=err, scale_bound=bound)
+                blocks = x.reshape(-1, 16)
+                sc = r["scales"].reshape(-1)
+                codes = np.stack([(r["codes"] & 0xF), (r["codes"] >> 4)], -1).reshape(-1, 16)
+                nb = big.shape[0]
+                assert np.all(sc[:nb] == 0x7E) and np.all(sc[nb:] == 0)
+                assert np.array_equal(codes[:nb], brute_e2m1_rn(f32(blocks[:nb] * enc)).reshape(-1, 16))
+                assert np.array_equal(codes[nb:], brute_e2m1_rn(f32(blocks[nb:] * FLT_MAX)).reshape(-1, 16))
+                assert codes[nb, 1] == 0 and codes[nb, 2] == 8       # +0 and -0 keep their codes
+    assert differ > 0       # the set holds cases a true division would round otherwise
