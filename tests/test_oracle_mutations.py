@@ -36,6 +36,14 @@ MUTATIONS = {
     "four-over-six encode divides instead of multiplying by the reciprocal": (
         "cc[cand][i] = orc_e2m1_encode_rn(yv * enc);",
         "cc[cand][i] = orc_e2m1_encode_rn(yv / (dc[cand] * g.S_dec));"),
+    "plain encode multiplies by the reciprocal": ("const float v = yv / D;", "const float v = yv * (1.0f / D);"),
+    "plain divisor d / S_enc instead of d * S_dec": ("const float D = d6 * g.S_dec;", "const float D = d6 / g.S_enc;"),
+    "tensor amax over x, not x + residual": (
+        "if (gamax_mode == ORC_GAMAX_TENSOR) orc_amax(y.data(), M, K, ORC_F32, nullptr, ORC_GAMAX_TENSOR, gamax);",
+        "if (gamax_mode == ORC_GAMAX_TENSOR) orc_amax(x, M, K, dtype, nullptr, ORC_GAMAX_TENSOR, gamax);"),
+    "row-given amax takes the first row's": (
+        "if (gamax_mode == ORC_GAMAX_ROW || gamax_mode == ORC_GAMAX_ROW_GIVEN) g.A = gamax[r];",
+        "if (gamax_mode == ORC_GAMAX_ROW) g.A = gamax[r]; if (gamax_mode == ORC_GAMAX_ROW_GIVEN) g.A = gamax[0];"),
     "S_enc falls back to 1 only for a zero amax": ("if (!(A > 0.0f) || std::isinf(A)) enc = 1.0f;",
                                                    "if (A == 0.0f) enc = 1.0f;"),
     "S_enc not clamped to FLT_MAX": ("else enc = min_nd((6.0f * bound) / A, FLT_MAX);",

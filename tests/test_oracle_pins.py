@@ -926,3 +926,92 @@ def test_four_over_six_encode_is_the_clamped_reciprocal_multiply():
                 assert np.array_equal(codes[nb:], brute_e2m1_rn(f32(blocks[nb:] * FLT_MAX)).reshape(-1, 16))
                 assert codes[nb, 1] == 0 and codes[nb, 2] == 8       # +0 and -0 keep their codes
     assert differ > 0       # the set holds cases a true division would round otherwise
+
+
+def _near_midpoints(D, reach=4):
+    """Values at and next to the e2m1 midpoints times D (both signs), and how
+    many of them a division by D and a multiply by RN(1/D) round to
+    different codes."""
+    ys, differ = [], 0
+    r = f32(1.0) / D
+    for m in (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0):
+        y = f32(f32(m) * D)
+        for _ in range(reach):
+            y = np.nextafter(y, f32(0))
+        for _ in range(2 * reach + 1):
+            differ += int(brute_e2m1_rn(f32(y / D))[0] != brute_e2m1_rn(f32(y * r))[0])
+            ys += [y, -y]
+            y = np.nextafter(y, f32(10))
+    return ys, differ
+
+
+def test_plain_encode_divides_by_the_decoded_scale():
+    """[fp4-train, Method]: every element is divided by the decoded scale and
+    rounded to the grid.  A block led by 6d (d an E4M3 value) has scale d
+    exactly; its other elements sit at and next to the e2m1 midpoints times d,
+    where the division and a multiply by the rounded reciprocal round to
+    different codes.  With a global scale the divisor is d * S_dec (d capped
+    at 448 by a block amax at the global amax)."""
+    tab = torch_e4m3_table()
+    differ = 0
+    blocks, expect_codes, expect_scales = [], [], []
+    for code in (0x39, 0x3B, 0x3D, 0x3F, 0x4B, 0x2D, 0x55, 0x1F):      # significands 9/8 .. 15/8
+        d = f32(tab[code])
+        ys, n = _near_midpoints(d)
+        differ += n
+        ys += [f32(0.0)] * (-len(ys) % 15)
+        for chunk in np.array(ys, np.float32).reshape(-1, 15):
+            blk = np.concatenate([[f32(6.0) * d], chunk]).astype(np.float32)
+            blocks.append(blk)
+            expect_codes.append(brute_e2m1_rn(f32(blk / d)))
+            expect_scales.append(code)
+    x = np.array(blocks, np.float32).reshape(1, -1)
+    r = oracle.quantize(x)
+    codes = np.stack([(r["codes"] & 0xF), (r["codes"] >> 4)], -1).reshape(-1)
+    assert np.array_equal(r["scales"].reshape(-1), np.array(expect_scales, np.uint8))
+    assert np.array_equal(codes, np.concatenate(expect_codes))
+    # with a given global amax A: the block amax A caps d at 448, the divisor is RN(448 * S_dec)
+    gdiffer = 0
+    for A in (f32(0.37), f32(3.1), f32(1e-3), f32(77.7), f32(0.0123)):
+        Senc, Sdec = oracle.global_scales(float(A), 448.0)
+        D = f32(f32(448.0) * f32(Sdec))
+        gdiffer += int(D != f32(f32(448.0) / f32(Senc)))
+        ys, n = _near_midpoints(D)
+        differ += n
+        ys += [f32(0.0)] * (-len(ys) % 15)
+        blk = np.concatenate([np.full((len(ys) // 15, 1), A, np.float32),
+                              np.array(ys, np.float32).reshape(-1, 15)], axis=1)
+        r = oracle.quantize(blk.reshape(1, -1), gamax_mode=oracle.GAMAX_TENSOR_GIVEN, gamax=np.array([A]))
+        codes = np.stack([(r["codes"] & 0xF), (r["codes"] >> 4)], -1).reshape(-1)
+        assert np.all(r["scales"] == 0x7E)
+        assert np.array_equal(codes, brute_e2m1_rn(f32(blk.reshape(-1) / D)))
+    assert differ > 0 and gdiffer > 0     # the sets hold cases the other forms would round otherwise
+
+
+def test_tensor_amax_under_error_feedback_is_over_x_plus_r():
+    """[fp4-train, Method] with the per-tensor scale of the four-over-six page:
+    under error feedback the quantized value is x + r, so its amax is
+    max |fp32(x + r)|, not max |x|."""
+    rng = np.random.default_rng(81)
+    x = rng.standard_normal((8, 64)).astype(np.float32)
+    res = np.zeros_like(x)
+    res[3, 5] = f32(np.abs(x).max() * 2.0)                  # x + r peaks where x does not
+    expect = f32(np.max(np.abs(f32(x + res))))
+    assert expect != f32(np.max(np.abs(x)))
+    for err, rnd in ((oracle.ERR_NONE, oracle.RTN), (oracle.ERR_NONE, oracle.SR)):
+        r = oracle.quantize(x, residual=res.copy(), rounding=rnd, gamax_mode=oracle.GAMAX_TENSOR, err_mode=err)
+        assert r["gamax"][0] == expect
+
+
+def test_row_given_amax_applies_row_by_row():
+    """Per-row given amaxes [4o6 PR, What: per-row or per-tensor global scale]:
+    row r of a row-given call equals that row quantized alone with its own
+    amax given per tensor (pinned above)."""
+    rng = np.random.default_rng(82)
+    x = rng.standard_normal((6, 64)).astype(np.float32)
+    g = (np.abs(x).max(1) * np.array([1.0, 2.0, 0.5, 3.0, 1.0, 7.0])).astype(np.float32)
+    for err in (oracle.ERR_NONE, oracle.ERR_MAE, oracle.ERR_MSE):
+        r = oracle.quantize(x, gamax_mode=oracle.GAMAX_ROW_GIVEN, gamax=g, err_mode=err)
+        for i in range(6):
+            o = oracle.quantize(x[i:i + 1], gamax_mode=oracle.GAMAX_TENSOR_GIVEN, gamax=g[i:i + 1], err_mode=err)
+            assert np.array_equal(r["codes"][i], o["codes"][0]) and np.array_equal(r["scales"][i], o["scales"][0])
