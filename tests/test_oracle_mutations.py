@@ -44,6 +44,9 @@ MUTATIONS = {
     "row-given amax takes the first row's": (
         "if (gamax_mode == ORC_GAMAX_ROW || gamax_mode == ORC_GAMAX_ROW_GIVEN) g.A = gamax[r];",
         "if (gamax_mode == ORC_GAMAX_ROW) g.A = gamax[r]; if (gamax_mode == ORC_GAMAX_ROW_GIVEN) g.A = gamax[0];"),
+    "row-given dequantize takes the first row's amax": (
+        "                orc_global_scales(gamax[r], scale_bound, &S_enc, &S_dec);\n            for (int64_t c = 0;",
+        "                orc_global_scales(gamax[0], scale_bound, &S_enc, &S_dec);\n            for (int64_t c = 0;"),
     "S_enc falls back to 1 only for a zero amax": ("if (!(A > 0.0f) || std::isinf(A)) enc = 1.0f;",
                                                    "if (A == 0.0f) enc = 1.0f;"),
     "S_enc not clamped to FLT_MAX": ("else enc = min_nd((6.0f * bound) / A, FLT_MAX);",

@@ -1005,8 +1005,8 @@ def test_tensor_amax_under_error_feedback_is_over_x_plus_r():
 
 def test_row_given_amax_applies_row_by_row():
     """Per-row given amaxes [4o6 PR, What: per-row or per-tensor global scale]:
-    row r of a row-given call equals that row quantized alone with its own
-    amax given per tensor (pinned above)."""
+    row r of a row-given call equals that row quantized (and dequantized)
+    alone with its own amax given per tensor (pinned above)."""
     rng = np.random.default_rng(82)
     x = rng.standard_normal((6, 64)).astype(np.float32)
     g = (np.abs(x).max(1) * np.array([1.0, 2.0, 0.5, 3.0, 1.0, 7.0])).astype(np.float32)
@@ -1015,3 +1015,11 @@ def test_row_given_amax_applies_row_by_row():
         for i in range(6):
             o = oracle.quantize(x[i:i + 1], gamax_mode=oracle.GAMAX_TENSOR_GIVEN, gamax=g[i:i + 1], err_mode=err)
             assert np.array_equal(r["codes"][i], o["codes"][0]) and np.array_equal(r["scales"][i], o["scales"][0])
+        bound = 448.0 if err == oracle.ERR_NONE else 256.0
+        dq = oracle.dequantize(r["codes"], r["scales"], 6, 64, gamax_mode=oracle.GAMAX_ROW_GIVEN, gamax=g,
+                               scale_bound=bound, out_dtype=oracle.F32)
+        for i in range(6):
+            di = oracle.dequantize(r["codes"][i:i + 1], r["scales"][i:i + 1], 1, 64,
+                                   gamax_mode=oracle.GAMAX_TENSOR_GIVEN, gamax=g[i:i + 1], scale_bound=bound,
+                                   out_dtype=oracle.F32)
+            assert np.array_equal(dq[i], di[0])
