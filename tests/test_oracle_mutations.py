@@ -47,6 +47,12 @@ MUTATIONS = {
     "row-given dequantize takes the first row's amax": (
         "                orc_global_scales(gamax[r], scale_bound, &S_enc, &S_dec);\n            for (int64_t c = 0;",
         "                orc_global_scales(gamax[0], scale_bound, &S_enc, &S_dec);\n            for (int64_t c = 0;"),
+    "qdq dequantizes without the global scale": (
+        "return orc_dequantize(codes, scales, M, K, gamax_mode, gamax, scale_bound, out_bf16, ORC_BF16);",
+        "return orc_dequantize(codes, scales, M, K, ORC_GAMAX_NONE, gamax, scale_bound, out_bf16, ORC_BF16);"),
+    "row amax over x, not x + residual": (
+        "if (gamax_mode == ORC_GAMAX_ROW) orc_amax(y.data(), M, K, ORC_F32, nullptr, ORC_GAMAX_ROW, gamax);",
+        "if (gamax_mode == ORC_GAMAX_ROW) orc_amax(x, M, K, dtype, nullptr, ORC_GAMAX_ROW, gamax);"),
     "S_enc falls back to 1 only for a zero amax": ("if (!(A > 0.0f) || std::isinf(A)) enc = 1.0f;",
                                                    "if (A == 0.0f) enc = 1.0f;"),
     "S_enc not clamped to FLT_MAX": ("else enc = min_nd((6.0f * bound) / A, FLT_MAX);",

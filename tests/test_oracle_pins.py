@@ -1001,6 +1001,37 @@ def test_tensor_amax_under_error_feedback_is_over_x_plus_r():
     for err, rnd in ((oracle.ERR_NONE, oracle.RTN), (oracle.ERR_NONE, oracle.SR)):
         r = oracle.quantize(x, residual=res.copy(), rounding=rnd, gamax_mode=oracle.GAMAX_TENSOR, err_mode=err)
         assert r["gamax"][0] == expect
+    # and per row: row 3's amax is the residual's peak
+    rows = np.max(np.abs(f32(x + res)), axis=1).astype(np.float32)
+    assert rows[3] != f32(np.max(np.abs(x[3])))
+    r = oracle.quantize(x, residual=res.copy(), gamax_mode=oracle.GAMAX_ROW)
+    assert np.array_equal(r["gamax"], rows)
+
+
+def test_qdq_is_quantize_then_dequantize():
+    """[fp4-train, API: qdq quantizes then dequantizes]: qdq's bf16 output is the
+    dequantize (to bf16) of the quantize's codes and scales, with the same
+    global amax, in every global-scale mode and with error feedback."""
+    rng = np.random.default_rng(83)
+    x = (rng.standard_t(3, (32, 64)) * 3.0).astype(np.float32)
+    for kw in (dict(), dict(gamax_mode=oracle.GAMAX_TENSOR, err_mode=oracle.ERR_MAE),
+               dict(gamax_mode=oracle.GAMAX_ROW, err_mode=oracle.ERR_MSE),
+               dict(gamax_mode=oracle.GAMAX_TENSOR, rounding=oracle.SR, seed=4, step=2),
+               dict(block=oracle.BLOCK_16X16, gamax_mode=oracle.GAMAX_TENSOR_GIVEN,
+                    gamax=np.array([f32(40.0)]), err_mode=oracle.ERR_MAE)):
+        q = oracle.quantize(x, **kw)
+        o = oracle.qdq(x, **kw)
+        bound = 256.0 if kw.get("err_mode", oracle.ERR_NONE) != oracle.ERR_NONE else 448.0
+        gm = kw.get("gamax_mode", oracle.GAMAX_NONE)
+        dq = oracle.dequantize(q["codes"], q["scales"], 32, 64, gamax_mode=gm,
+                               gamax=None if gm == oracle.GAMAX_NONE else q["gamax"], scale_bound=bound)
+        assert np.array_equal(o["codes"], q["codes"]) and np.array_equal(o["out"], dq)
+    r0 = (rng.standard_normal((32, 64)) * 0.1).astype(np.float32)
+    ra, rb = r0.copy(), r0.copy()
+    q = oracle.quantize(x, residual=ra, rounding=oracle.SR, seed=1)
+    o = oracle.qdq(x, residual=rb, rounding=oracle.SR, seed=1)
+    assert np.array_equal(ra, rb)
+    assert np.array_equal(o["out"], oracle.dequantize(q["codes"], q["scales"], 32, 64))
 
 
 def test_row_given_amax_applies_row_by_row():
