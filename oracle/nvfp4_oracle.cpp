@@ -9,6 +9,15 @@
  *
  * Build: g++ -O2 -ffp-contract=off -fno-fast-math (fp32 ops must round once,
  * exactly as written; orc_fp_env_ok() checks that subnormals survive).
+ *
+ * Parity unpinned: two steps rest on a reading that no value on the pages
+ * fixes, so only this restatement and the GPU's agreement check them: the
+ * association of the four-over-six error value ((q * d) * A) / (6 * bound)
+ * when S_enc != 1 (planted mistakes q * (d * A) and (q * d) * (A / C) pass
+ * every pin), and the S_enc = 1 fallback for a global amax that is 0, Inf,
+ * NaN or negative (pinned only against that reading).  Every other step is
+ * pinned by tests/test_oracle_pins.py, each pin checked by a planted mistake
+ * in tests/test_oracle_mutations.py.
  */
 #include "nvfp4_oracle.h"
 
