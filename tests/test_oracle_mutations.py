@@ -53,6 +53,11 @@ MUTATIONS = {
     "row amax over x, not x + residual": (
         "if (gamax_mode == ORC_GAMAX_ROW) orc_amax(y.data(), M, K, ORC_F32, nullptr, ORC_GAMAX_ROW, gamax);",
         "if (gamax_mode == ORC_GAMAX_ROW) orc_amax(x, M, K, dtype, nullptr, ORC_GAMAX_ROW, gamax);"),
+    "columnwise output without the global scale": (
+        "std::vector<GScale> gt(static_cast<size_t>(K > 0 ? K : 1), M > 0 ? gs[0] : GScale{0.0f, 1.0f, 1.0f});",
+        "std::vector<GScale> gt(static_cast<size_t>(K > 0 ? K : 1), GScale{0.0f, 1.0f, 1.0f});"),
+    "columnwise draws ignore row_offset": ("seed, step, row_offset, codes_col, scales_col, nullptr};",
+                                           "seed, step, 0, codes_col, scales_col, nullptr};"),
     "S_enc falls back to 1 only for a zero amax": ("if (!(A > 0.0f) || std::isinf(A)) enc = 1.0f;",
                                                    "if (A == 0.0f) enc = 1.0f;"),
     "S_enc not clamped to FLT_MAX": ("else enc = min_nd((6.0f * bound) / A, FLT_MAX);",
