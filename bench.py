@@ -84,6 +84,7 @@ def parse():
     return p.parse_args()
 
 
+METRIC = "NVFP4 quantize GB/s (Gelem/s alongside); % of HBM roofline"
 WORKLOAD = ("c5 LLM-shaped sweep, bf16: W1[4096,14336], W2[14336,4096] ~ 0.02*N(0,1), "
             "A[16384,4096] ~ Student-t(4) with 4 outlier channels x100 (seed 4); SR+EF 1x16 "
             "and 16x16 (seed 0, step t), four-over-six MAE bound 256 (1x16 rowwise on A, 16x16 "
@@ -253,7 +254,7 @@ def run_reference(args, rank, world):
         res = cpu_baseline(sample_rows=256, threads=(0,))
         times.append(res["seconds_per_sample_step"])
     val = res["value"]
-    line = {"impl": "reference", "metric": "NVFP4 quantize GB/s (Gelem/s alongside); % of HBM roofline",
+    line = {"impl": "reference", "metric": METRIC,
             "value": round(val, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.median(times), 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
@@ -858,7 +859,7 @@ def run_gpu(args, rank, world, local_rank):
                "kind": "oracle", "sample": cb["sample"],
                "single_thread_value": round(cb["single_thread_value"], 4)}
     line = {
-        "metric": "NVFP4 quantize GB/s (Gelem/s alongside); % of HBM roofline",
+        "metric": METRIC,
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": nsteps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
