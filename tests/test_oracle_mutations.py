@@ -58,6 +58,17 @@ MUTATIONS = {
         "std::vector<GScale> gt(static_cast<size_t>(K > 0 ? K : 1), GScale{0.0f, 1.0f, 1.0f});"),
     "columnwise draws ignore row_offset": ("seed, step, row_offset, codes_col, scales_col, nullptr};",
                                            "seed, step, 0, codes_col, scales_col, nullptr};"),
+    "standard association's 1/6 taken in double": (
+        "float block_s6f_std(float b, float S_enc) { return b * (S_enc * (1.0f / 6.0f)); }",
+        "float block_s6f_std(float b, float S_enc) { return b * static_cast<float>(S_enc / 6.0); }"),
+    "e4m3 subnormals one binade low": ("const double mag = (e == 0) ? std::ldexp(static_cast<double>(m), -9)",
+                                       "const double mag = (e == 0) ? std::ldexp(static_cast<double>(m), -10)"),
+    "fp32 dequantize rounded through bf16": (
+        "                else static_cast<float*>(out)[r * K + c] = v;",
+        "                else static_cast<float*>(out)[r * K + c] = orc_bf16_to_f32(orc_f32_to_bf16(v));"),
+    "empty tensor amax -inf": (
+        "        float A = 0.0f;\n        for (int64_t r = 0; r < M; ++r) A = max_nd(A, part[r]);",
+        "        float A = -INFINITY;\n        for (int64_t r = 0; r < M; ++r) A = max_nd(A, part[r]);"),
     "S_enc falls back to 1 only for a zero amax": ("if (!(A > 0.0f) || std::isinf(A)) enc = 1.0f;",
                                                    "if (A == 0.0f) enc = 1.0f;"),
     "S_enc not clamped to FLT_MAX": ("else enc = min_nd((6.0f * bound) / A, FLT_MAX);",

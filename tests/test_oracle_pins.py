@@ -1054,3 +1054,15 @@ def test_row_given_amax_applies_row_by_row():
                                    gamax_mode=oracle.GAMAX_TENSOR_GIVEN, gamax=g[i:i + 1], scale_bound=bound,
                                    out_dtype=oracle.F32)
             assert np.array_equal(dq[i], di[0])
+
+
+def test_amax_of_an_empty_tensor_is_plus_zero():
+    """An empty tensor (M = 0 or K = 0) is a valid no-op whose per-tensor amax
+    is +0: the identity of a maximum over non-negative magnitudes, which the
+    global scale then treats as A = 0 (S_enc falls back to 1)."""
+    for shape in ((0, 16), (4, 0), (0, 0)):
+        x = np.zeros(shape, np.float32)
+        a = oracle.amax(x)
+        assert a[0] == 0.0 and not np.signbit(a[0])
+        r = oracle.quantize(x, gamax_mode=oracle.GAMAX_TENSOR)
+        assert r["gamax"][0] == 0.0 and not np.signbit(r["gamax"][0])
