@@ -7,6 +7,7 @@ has to fail.  The committed oracle is never modified.
 import os
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -96,21 +97,45 @@ MUTATIONS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTATIONS))
-def test_pins_catch_planted_mistake(name, tmp_path):
+def _run_mutation(name: str, work: str):
+    """Build the oracle with one planted mistake under work/ and run the pin
+    suite against it.  Returns (anchor found, pin-suite exit code, output tail)."""
     old, new = MUTATIONS[name]
     src = open(SRC).read()
-    assert src.count(old) >= 1, f"mutation anchor not found: {name}"
-    mutated = src.replace(old, new, 1)
-    cpp = tmp_path / "nvfp4_oracle.cpp"
-    cpp.write_text(mutated)
-    hdr = os.path.join(ROOT, "oracle", "nvfp4_oracle.h")
-    (tmp_path / "nvfp4_oracle.h").write_text(open(hdr).read())
-    so = tmp_path / "liboracle_mut.so"
+    if src.count(old) < 1:
+        return False, None, ""
+    os.makedirs(work, exist_ok=True)
+    cpp = os.path.join(work, "nvfp4_oracle.cpp")
+    with open(cpp, "w") as f:
+        f.write(src.replace(old, new, 1))
+    with open(os.path.join(work, "nvfp4_oracle.h"), "w") as f:
+        f.write(open(os.path.join(ROOT, "oracle", "nvfp4_oracle.h")).read())
+    so = os.path.join(work, "liboracle_mut.so")
     subprocess.run(["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-w",
-                    "-pthread", "-shared", "-fPIC", str(cpp), "-o", str(so)], check=True)
-    env = dict(os.environ, NVFP4_ORACLE_LIB=str(so))
+                    "-pthread", "-shared", "-fPIC", cpp, "-o", so], check=True)
+    env = dict(os.environ, NVFP4_ORACLE_LIB=so)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
-                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode != 0, f"pins did not catch: {name}\n{r.stdout[-2000:]}"
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    return True, r.returncode, r.stdout[-2000:]
+
+
+@pytest.fixture(scope="module")
+def outcomes(tmp_path_factory):
+    """Every planted mistake, built and checked concurrently (each one is an
+    independent compile and pin-suite process)."""
+    base = str(tmp_path_factory.mktemp("mutations"))
+    names = sorted(MUTATIONS)
+    workers = max(1, min(8, os.cpu_count() or 1))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        runs = ex.map(lambda i: _run_mutation(names[i], os.path.join(base, f"m{i}")), range(len(names)))
+        return dict(zip(names, runs))
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, outcomes):
+    found, rc, tail = outcomes[name]
+    assert found, f"mutation anchor not found: {name}"
+    # exit code 1 is pytest's "tests failed": an interrupted, crashed or
+    # killed pin run (any other code) does not count as a catch
+    assert rc == 1, f"pins did not catch: {name} (exit code {rc})\n{tail}"
